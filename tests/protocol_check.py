@@ -1,0 +1,150 @@
+"""Happens-before checker for the three-stream event protocol (test helper).
+
+The hotdry.top page (section on the event-driven synchronisation protocol)
+states what each event is for: Weights-Ready lets compute use a buffer only
+after its weights arrived; Backward-Done lets the gradient stream export only
+after the gradients exist; Buffer-Free lets the weight stream refill a buffer
+only after its previous contents were consumed.  The same page and the
+dimensionstp review (3-2 (4)) add pinned staging (packed by the host, read by
+the copy) and the gradient slabs (written by the export, read by host Adam).
+
+This checker replays an op list with vector clocks over the streams W, C, G,
+the host thread H and the Adam dispatcher A, and asserts every data hazard
+those sentences forbid is ordered:
+  * H2D into buffer b after the previous compute on b and its export;
+  * compute on b after this visit's H2D into b;
+  * export from b after the compute that wrote its gradients;
+  * host pack into staging b after the previous H2D read staging b;
+  * D2H into slab k after the previous Adam on slab k, Adam after the D2H;
+  * next step's pack / H2D of block j after block j's Adam;
+  * checkpoint slots: write after the previous save, save after the write,
+    checkpoint H2D after the previous compute that read the slot.
+"""
+from __future__ import annotations
+
+STREAMS = ("W", "C", "G", "H", "A")
+
+
+class Clock:
+    def __init__(self, c=None):
+        self.c = dict(c or {s: 0 for s in STREAMS})
+
+    def merge(self, o: "Clock"):
+        for k in self.c:
+            self.c[k] = max(self.c[k], o.c[k])
+
+    def copy(self):
+        return Clock(self.c)
+
+
+def _hb(a, b) -> bool:
+    """True if op a (stream, clock) happens before op b."""
+    if a is None:
+        return True
+    sa, ca = a
+    _, cb = b
+    return ca.c[sa] <= cb.c[sa]
+
+
+def check(lines: list[str]) -> None:
+    clk = {s: Clock() for s in STREAMS}
+    ev: dict[str, Clock] = {}
+    last_buf_use: dict[int, list] = {0: [], 1: []}     # ops that read/wrote device buffer b
+    visit_h2d: dict[int, tuple] = {}                   # this visit's H2D into b
+    last_ckpt_read: dict[int, tuple] = {}              # compute that read xck[b]
+    stage_read: dict[int, tuple] = {}                  # H2D that read staging b
+    slab_adam: dict[int, tuple] = {}                   # Adam job that read slab k
+    slab_d2h: dict[int, tuple] = {}
+    adam_done: dict[int, tuple] = {}                   # block -> Adam job
+    xslot_write: dict[int, tuple] = {}
+    xslot_save: dict[int, tuple] = {}
+
+    def tick(s):
+        clk[s].c[s] += 1
+        return (s, clk[s].copy())
+
+    for ln, line in enumerate(lines):
+        step, s, op, a, b = line.split()
+        a, b = int(a), int(b)
+        where = f"line {ln}: {line}"
+        if s in ("W", "C", "G"):
+            clk[s].merge(clk["H"])  # enqueued by the host after its earlier actions
+        if op.startswith("WAIT_") and s in ("W", "C", "G"):
+            name = op[5:] + str(a)
+            if name in ev:
+                clk[s].merge(ev[name])
+            continue
+        if op.startswith("REC_"):
+            name = op[4:] + str(a)
+            me = tick(s)
+            ev[name] = me[1]
+            continue
+        if s == "H":
+            if op == "WAIT_ADAM":
+                assert a in adam_done, where
+                clk["H"].merge(adam_done[a][1])
+            elif op == "WAIT_STAGE":
+                clk["H"].merge(ev["WR" + str(a)])
+            elif op == "PACK":
+                me = tick("H")
+                assert _hb(stage_read.get(b), me), "pack overwrites staging still being copied: " + where
+                if a in adam_done:
+                    assert _hb(adam_done[a], me), "pack before Adam of the block: " + where
+            elif op == "ACQ_SLAB":
+                if a in slab_adam:
+                    clk["H"].merge(slab_adam[a][1])
+            elif op == "ADAM_ENQ":
+                clk["A"].merge(clk["H"])
+                clk["A"].merge(ev["SR" + str(b)])
+                me = tick("A")
+                assert _hb(slab_d2h[b], me), "Adam reads slab before its D2H: " + where
+                slab_adam[b] = me
+                adam_done[a] = me
+            continue
+        me = tick(s)
+        if op == "H2D":
+            for u in last_buf_use[b]:
+                assert _hb(u, me), "H2D overwrites buffer still in use: " + where
+            if a in adam_done:
+                assert _hb(adam_done[a], me), "H2D of a block before its Adam: " + where
+            visit_h2d[b] = me
+            stage_read[b] = me
+            last_buf_use[b] = [me]
+        elif op == "H2D_CKPT":
+            assert _hb(last_ckpt_read.get(b), me), "checkpoint H2D over a slot in use: " + where
+            for u in last_buf_use[b]:
+                assert _hb(u, me), "checkpoint H2D before buffer free: " + where
+            visit_h2d[b] = me
+        elif op in ("FWD", "HEAD", "BWD"):
+            assert _hb(visit_h2d.get(b), me), "compute before weights ready: " + where
+            for u in last_buf_use[b]:
+                assert _hb(u, me), "compute overlaps earlier use of buffer: " + where
+            last_buf_use[b] = [me]
+            if op == "BWD":
+                last_ckpt_read[b] = me
+            if op == "FWD" or op == "HEAD":
+                slot = a % 2
+                if op == "FWD":
+                    assert _hb(xslot_save.get(slot), me), "X slot overwritten before saved: " + where
+                    xslot_write[slot] = me
+        elif op == "D2H_CKPT":
+            assert _hb(xslot_write[b], me), "checkpoint saved before written: " + where
+            xslot_save[b] = me
+        elif op == "D2H":
+            buf = _buf_of(lines, ln)
+            assert _hb(last_buf_use[buf][-1], me), "export before gradients computed: " + where
+            if b in slab_adam:
+                assert _hb(slab_adam[b], me), "D2H into slab before its Adam finished: " + where
+            slab_d2h[b] = me
+            last_buf_use[buf].append(me)
+        else:
+            raise AssertionError("unknown op " + where)
+
+
+def _buf_of(lines, ln):
+    """Buffer of the export at line ln: the WAIT_BD just before it names it."""
+    for k in range(ln - 1, -1, -1):
+        p = lines[k].split()
+        if p[1] == "G" and p[2] == "WAIT_BD":
+            return int(p[3])
+    raise AssertionError("export without Backward-Done wait")
