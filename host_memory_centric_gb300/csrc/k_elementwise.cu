@@ -1,0 +1,453 @@
+// k_elementwise.cu -- HBM-bound kernels of the block math (sm_103a).
+//
+// RMSNorm forward / backward, rotate-half RoPE, SwiGLU forward / backward,
+// embedding gather / dense gradient, cross-entropy with in-place dlogits, and
+// small conversions.  Each kernel reads and writes its tensors once with
+// 16-byte vector accesses along contiguous rows (coalesced per warp), keeps
+// statistics in FP32 and reduces with warp shuffles.
+#include "mt_kernels.h"
+
+namespace mt {
+namespace {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ void unpack8(const uint4& q, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 t = __bfloat1622float2(h[k]);
+    f[2 * k] = t.x;
+    f[2 * k + 1] = t.y;
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint4 q;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);
+  return q;
+}
+
+constexpr int ROW_WARPS = 8;  // rows per 256-thread block in the row kernels
+
+// ------------------------------------------------------------------ RMSNorm
+__global__ void __launch_bounds__(256) rmsnorm_fwd_k(const bf16* __restrict__ x, const bf16* __restrict__ g,
+                                                     int64_t T, int H, float eps, bf16* __restrict__ y,
+                                                     float* __restrict__ rstd) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * ROW_WARPS + (threadIdx.x >> 5);
+  if (row >= T) return;
+  const bf16* xr = x + row * H;
+  float ss = 0.f;
+  for (int c = lane * 8; c < H; c += 256) {
+    float f[8];
+    unpack8(*reinterpret_cast<const uint4*>(xr + c), f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ss += f[k] * f[k];
+  }
+  ss = warp_sum(ss);
+  const float r = rsqrtf(ss / (float)H + eps);
+  bf16* yr = y + row * H;
+  for (int c = lane * 8; c < H; c += 256) {
+    float f[8], w[8];
+    unpack8(*reinterpret_cast<const uint4*>(xr + c), f);
+    unpack8(*reinterpret_cast<const uint4*>(g + c), w);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) f[k] = f[k] * r * w[k];
+    *reinterpret_cast<uint4*>(yr + c) = pack8(f);
+  }
+  if (lane == 0) rstd[row] = r;
+}
+
+// Each block owns a contiguous run of rows; dgamma partial sums for its rows
+// go to partial[blockIdx.x][H].
+__global__ void __launch_bounds__(256) rmsnorm_bwd_k(const bf16* __restrict__ dy, const bf16* __restrict__ x,
+                                                     const bf16* __restrict__ g, const float* __restrict__ rstd,
+                                                     const bf16* __restrict__ dres, int64_t T, int H,
+                                                     int64_t rows_per_block, bf16* __restrict__ dx,
+                                                     float* __restrict__ partial) {
+  extern __shared__ float part[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int c = threadIdx.x; c < H; c += blockDim.x) part[c] = 0.f;
+  __syncthreads();
+  const int64_t r0 = (int64_t)blockIdx.x * rows_per_block;
+  const int64_t r1 = min(T, r0 + rows_per_block);
+  for (int64_t row = r0 + warp; row < r1; row += ROW_WARPS) {
+    const bf16* dyr = dy + row * H;
+    const bf16* xr = x + row * H;
+    const float r = rstd[row];
+    float dot = 0.f;
+    for (int c = lane * 8; c < H; c += 256) {
+      float a[8], b[8], w[8];
+      unpack8(*reinterpret_cast<const uint4*>(dyr + c), a);
+      unpack8(*reinterpret_cast<const uint4*>(xr + c), b);
+      unpack8(*reinterpret_cast<const uint4*>(g + c), w);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) dot += a[k] * w[k] * b[k];
+    }
+    dot = warp_sum(dot);
+    const float c3 = r * r * r / (float)H * dot;
+    for (int c = lane * 8; c < H; c += 256) {
+      float a[8], b[8], w[8], o[8];
+      unpack8(*reinterpret_cast<const uint4*>(dyr + c), a);
+      unpack8(*reinterpret_cast<const uint4*>(xr + c), b);
+      unpack8(*reinterpret_cast<const uint4*>(g + c), w);
+      if (dres) {
+        unpack8(*reinterpret_cast<const uint4*>(dres + row * H + c), o);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[k] = 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        o[k] += r * w[k] * a[k] - c3 * b[k];
+        atomicAdd(&part[c + k], a[k] * b[k] * r);
+      }
+      *reinterpret_cast<uint4*>(dx + row * H + c) = pack8(o);
+    }
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < H; c += blockDim.x) partial[(int64_t)blockIdx.x * H + c] = part[c];
+}
+
+__global__ void rmsnorm_bwd_stage2_k(const float* __restrict__ partial, int nblk, int H, bf16* __restrict__ dg) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= H) return;
+  float s = 0.f;
+  for (int b = 0; b < nblk; ++b) s += partial[(int64_t)b * H + c];
+  dg[c] = __float2bfloat16_rn(s);
+}
+
+// ------------------------------------------------------------------ RoPE
+// One thread rotates 8 consecutive frequency pairs of one head of one row.
+__global__ void rope_k(bf16* __restrict__ x, int64_t T, int64_t ld, int n_heads, int hd, int S,
+                       const float* __restrict__ cs, int inverse) {
+  const int half = hd >> 1, per_head = half >> 3;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t per_row = (int64_t)n_heads * per_head;
+  if (idx >= T * per_row) return;
+  const int64_t row = idx / per_row;
+  const int rem = (int)(idx % per_row);
+  const int h = rem / per_head, i0 = (rem % per_head) * 8;
+  const int pos = (int)(row % S);
+  bf16* p = x + row * ld + (int64_t)h * hd;
+  float a[8], b[8];
+  unpack8(*reinterpret_cast<const uint4*>(p + i0), a);
+  unpack8(*reinterpret_cast<const uint4*>(p + half + i0), b);
+  const float4* c4 = reinterpret_cast<const float4*>(cs + ((int64_t)pos * half + i0) * 2);
+  float oa[8], ob[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4 v = c4[k];  // cos_i, sin_i, cos_{i+1}, sin_{i+1}
+    const float c0 = v.x, s0 = inverse ? -v.y : v.y, c1 = v.z, s1 = inverse ? -v.w : v.w;
+    oa[2 * k] = a[2 * k] * c0 - b[2 * k] * s0;
+    ob[2 * k] = b[2 * k] * c0 + a[2 * k] * s0;
+    oa[2 * k + 1] = a[2 * k + 1] * c1 - b[2 * k + 1] * s1;
+    ob[2 * k + 1] = b[2 * k + 1] * c1 + a[2 * k + 1] * s1;
+  }
+  *reinterpret_cast<uint4*>(p + i0) = pack8(oa);
+  *reinterpret_cast<uint4*>(p + half + i0) = pack8(ob);
+}
+
+// ------------------------------------------------------------------ SwiGLU
+__device__ __forceinline__ float sigm(float z) { return 1.f / (1.f + expf(-z)); }
+
+__global__ void swiglu_fwd_k(const bf16* __restrict__ gu, int64_t T, int F, bf16* __restrict__ h) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int per_row = F >> 3;
+  if (idx >= T * per_row) return;
+  const int64_t row = idx / per_row;
+  const int c = (int)(idx % per_row) * 8;
+  float g[8], u[8];
+  unpack8(*reinterpret_cast<const uint4*>(gu + row * 2 * F + c), g);
+  unpack8(*reinterpret_cast<const uint4*>(gu + row * 2 * F + F + c), u);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) g[k] = g[k] * sigm(g[k]) * u[k];
+  *reinterpret_cast<uint4*>(h + row * F + c) = pack8(g);
+}
+
+__global__ void swiglu_bwd_k(const bf16* __restrict__ gu, const bf16* __restrict__ dh, int64_t T, int F,
+                             bf16* __restrict__ dgu) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int per_row = F >> 3;
+  if (idx >= T * per_row) return;
+  const int64_t row = idx / per_row;
+  const int c = (int)(idx % per_row) * 8;
+  float g[8], u[8], d[8], dg[8], du[8];
+  unpack8(*reinterpret_cast<const uint4*>(gu + row * 2 * F + c), g);
+  unpack8(*reinterpret_cast<const uint4*>(gu + row * 2 * F + F + c), u);
+  unpack8(*reinterpret_cast<const uint4*>(dh + row * F + c), d);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float s = sigm(g[k]);
+    dg[k] = d[k] * u[k] * s * (1.f + g[k] * (1.f - s));
+    du[k] = d[k] * g[k] * s;
+  }
+  *reinterpret_cast<uint4*>(dgu + row * 2 * F + c) = pack8(dg);
+  *reinterpret_cast<uint4*>(dgu + row * 2 * F + F + c) = pack8(du);
+}
+
+// ------------------------------------------------------------------ embedding
+__global__ void embed_fwd_k(const int32_t* __restrict__ tok, const bf16* __restrict__ E, int64_t T, int H,
+                            bf16* __restrict__ X) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int per_row = H >> 3;
+  if (idx >= T * per_row) return;
+  const int64_t row = idx / per_row;
+  const int c = (int)(idx % per_row) * 8;
+  *reinterpret_cast<uint4*>(X + row * H + c) =
+      *reinterpret_cast<const uint4*>(E + (int64_t)tok[row] * H + c);
+}
+
+// One block per vocabulary row; rows no token selects are written as zeros.
+__global__ void __launch_bounds__(128) embed_bwd_k(const int32_t* __restrict__ row_start,
+                                                   const int32_t* __restrict__ rows, const bf16* __restrict__ dX,
+                                                   int H, bf16* __restrict__ dE) {
+  const int64_t v = blockIdx.x;
+  const int b = row_start[v], e = row_start[v + 1];
+  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int i = b; i < e; ++i) {
+      float f[8];
+      unpack8(*reinterpret_cast<const uint4*>(dX + (int64_t)rows[i] * H + c), f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] += f[k];
+    }
+    *reinterpret_cast<uint4*>(dE + v * H + c) = pack8(acc);
+  }
+}
+
+// ------------------------------------------------------------------ cross-entropy
+constexpr int CE_THREADS = 512;
+
+__global__ void __launch_bounds__(CE_THREADS) cross_entropy_k(bf16* __restrict__ logits,
+                                                              const int32_t* __restrict__ target, int V,
+                                                              float inv_norm, float* __restrict__ row_loss) {
+  __shared__ float sm[CE_THREADS / 32], ss[CE_THREADS / 32];
+  __shared__ float zt_s, lse_s;
+  const int64_t r = blockIdx.x;
+  bf16* z = logits + r * (int64_t)V;
+  const int tgt = target[r];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tgt < 0) {
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    if ((V & 7) == 0)
+      for (int c = tid * 8; c < V; c += CE_THREADS * 8) *reinterpret_cast<uint4*>(z + c) = zero;
+    else
+      for (int c = tid; c < V; c += CE_THREADS) z[c] = __float2bfloat16_rn(0.f);
+    if (tid == 0) row_loss[r] = 0.f;
+    return;
+  }
+  if (tid == 0) zt_s = __bfloat162float(z[tgt]);
+  // pass 1: per-thread running max and sum of exp, merged across the block
+  float m = -INFINITY, s = 0.f;
+  auto add = [&](float v) {
+    if (v > m) {
+      s = s * expf(m - v) + 1.f;
+      m = v;
+    } else {
+      s += expf(v - m);
+    }
+  };
+  if ((V & 7) == 0) {
+    for (int c = tid * 8; c < V; c += CE_THREADS * 8) {
+      float f[8];
+      unpack8(*reinterpret_cast<const uint4*>(z + c), f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) add(f[k]);
+    }
+  } else {
+    for (int c = tid; c < V; c += CE_THREADS) add(__bfloat162float(z[c]));
+  }
+  float wm = warp_max(m);
+  float wsum = (m == -INFINITY) ? 0.f : s * expf(m - wm);
+  wsum = warp_sum(wsum);
+  if (lane == 0) {
+    sm[warp] = wm;
+    ss[warp] = wsum;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float a = lane < CE_THREADS / 32 ? sm[lane] : -INFINITY;
+    float b = lane < CE_THREADS / 32 ? ss[lane] : 0.f;
+    const float M = warp_max(a);
+    b = (a == -INFINITY) ? 0.f : b * expf(a - M);
+    b = warp_sum(b);
+    if (lane == 0) {
+      lse_s = M + logf(b);
+      row_loss[r] = lse_s - zt_s;
+    }
+  }
+  __syncthreads();
+  const float lse = lse_s;
+  // pass 2: dlogits = (softmax - onehot) * inv_norm
+  if ((V & 7) == 0) {
+    for (int c = tid * 8; c < V; c += CE_THREADS * 8) {
+      float f[8];
+      unpack8(*reinterpret_cast<const uint4*>(z + c), f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) f[k] = (expf(f[k] - lse) - (c + k == tgt ? 1.f : 0.f)) * inv_norm;
+      *reinterpret_cast<uint4*>(z + c) = pack8(f);
+    }
+  } else {
+    for (int c = tid; c < V; c += CE_THREADS) {
+      const float v = __bfloat162float(z[c]);
+      z[c] = __float2bfloat16_rn((expf(v - lse) - (c == tgt ? 1.f : 0.f)) * inv_norm);
+    }
+  }
+}
+
+__global__ void reduce_sum_k(const float* __restrict__ x, int64_t n, float scale, float* out) {
+  __shared__ double sh[32];
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) s += (double)x[i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += sh[w];
+    out[0] = (float)(t * (double)scale);
+  }
+}
+
+__global__ void f32_to_bf16_k(const float* __restrict__ x, int64_t ldx, int64_t rows, int64_t cols,
+                              bf16* __restrict__ y, int64_t ldy, float scale) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * cols) return;
+  const int64_t r = idx / cols, c = idx % cols;
+  y[r * ldy + c] = __float2bfloat16_rn(x[r * ldx + c] * scale);
+}
+
+__global__ void add_bf16_k(const bf16* __restrict__ a, const bf16* __restrict__ b, int64_t n8, bf16* __restrict__ y) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  float fa[8], fb[8];
+  unpack8(reinterpret_cast<const uint4*>(a)[i], fa);
+  unpack8(reinterpret_cast<const uint4*>(b)[i], fb);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) fa[k] += fb[k];
+  reinterpret_cast<uint4*>(y)[i] = pack8(fa);
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+inline unsigned nblocks(int64_t n, int t) { return (unsigned)((n + t - 1) / t); }
+
+}  // namespace
+
+// ------------------------------------------------------------------ launchers
+cudaError_t rmsnorm_fwd(const bf16* x, const bf16* gamma, int64_t T, int H, float eps, bf16* y, float* rstd,
+                        cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (H % 8 || !al16(x) || !al16(gamma) || !al16(y)) return cudaErrorInvalidValue;
+  rmsnorm_fwd_k<<<nblocks(T, ROW_WARPS), 256, 0, s>>>(x, gamma, T, H, eps, y, rstd);
+  return cudaGetLastError();
+}
+
+int rmsnorm_bwd_blocks(int64_t T) {
+  const int64_t want = (T + ROW_WARPS * 4 - 1) / (ROW_WARPS * 4);  // >= 32 rows per block
+  return (int)(want < 304 ? (want < 1 ? 1 : want) : 304);
+}
+int64_t rmsnorm_bwd_partial_floats(int64_t T, int H) { return (int64_t)rmsnorm_bwd_blocks(T) * H; }
+
+cudaError_t rmsnorm_bwd_stage2(const float* partial, int nblk, int H, bf16* dgamma, cudaStream_t s) {
+  rmsnorm_bwd_stage2_k<<<nblocks(H, 256), 256, 0, s>>>(partial, nblk, H, dgamma);
+  return cudaGetLastError();
+}
+
+cudaError_t rmsnorm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const float* rstd, const bf16* dres,
+                        int64_t T, int H, bf16* dx, bf16* dgamma, float* partial, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (H % 8 || H > 12288 || !al16(dy) || !al16(x) || !al16(gamma) || !al16(dx) || (dres && !al16(dres)))
+    return cudaErrorInvalidValue;
+  const int nblk = rmsnorm_bwd_blocks(T);
+  const int64_t per = (T + nblk - 1) / nblk;
+  const size_t sm = (size_t)H * sizeof(float);
+  if (sm > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(rmsnorm_bwd_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+  }
+  rmsnorm_bwd_k<<<nblk, 256, sm, s>>>(dy, x, gamma, rstd, dres, T, H, per, dx, partial);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return rmsnorm_bwd_stage2(partial, nblk, H, dgamma, s);
+}
+
+cudaError_t rope(bf16* x, int64_t T, int64_t ld, int n_heads, int hd, int S, const float* cs, int inverse,
+                 cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (hd % 16 || ld % 8 || !al16(x) || !al16(cs)) return cudaErrorInvalidValue;
+  const int64_t n = T * n_heads * (hd / 16);
+  rope_k<<<nblocks(n, 256), 256, 0, s>>>(x, T, ld, n_heads, hd, S, cs, inverse);
+  return cudaGetLastError();
+}
+
+cudaError_t swiglu_fwd(const bf16* gu, int64_t T, int F, bf16* h, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (F % 8 || !al16(gu) || !al16(h)) return cudaErrorInvalidValue;
+  swiglu_fwd_k<<<nblocks(T * (F / 8), 256), 256, 0, s>>>(gu, T, F, h);
+  return cudaGetLastError();
+}
+
+cudaError_t swiglu_bwd(const bf16* gu, const bf16* dh, int64_t T, int F, bf16* dgu, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (F % 8 || !al16(gu) || !al16(dh) || !al16(dgu)) return cudaErrorInvalidValue;
+  swiglu_bwd_k<<<nblocks(T * (F / 8), 256), 256, 0, s>>>(gu, dh, T, F, dgu);
+  return cudaGetLastError();
+}
+
+cudaError_t embed_fwd(const int32_t* tok, const bf16* E, int64_t T, int H, int V, bf16* X, cudaStream_t s) {
+  (void)V;
+  if (T <= 0) return cudaSuccess;
+  if (H % 8 || !al16(E) || !al16(X)) return cudaErrorInvalidValue;
+  embed_fwd_k<<<nblocks(T * (H / 8), 256), 256, 0, s>>>(tok, E, T, H, X);
+  return cudaGetLastError();
+}
+
+cudaError_t embed_bwd(const int32_t* row_start, const int32_t* rows, const bf16* dX, int V, int H, bf16* dE,
+                      cudaStream_t s) {
+  if (V <= 0) return cudaSuccess;
+  if (H % 8 || !al16(dX) || !al16(dE)) return cudaErrorInvalidValue;
+  embed_bwd_k<<<V, 128, 0, s>>>(row_start, rows, dX, H, dE);
+  return cudaGetLastError();
+}
+
+cudaError_t cross_entropy(bf16* logits, const int32_t* target, int64_t rows, int V, float inv_norm,
+                          float* row_loss, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (((V & 7) == 0) && !al16(logits)) return cudaErrorInvalidValue;
+  if (rows > 0x7fffffff) return cudaErrorInvalidValue;
+  cross_entropy_k<<<(unsigned)rows, CE_THREADS, 0, s>>>(logits, target, V, inv_norm, row_loss);
+  return cudaGetLastError();
+}
+
+cudaError_t reduce_sum(const float* x, int64_t n, float scale, float* out, cudaStream_t s) {
+  reduce_sum_k<<<1, 1024, 0, s>>>(x, n, scale, out);
+  return cudaGetLastError();
+}
+
+cudaError_t f32_to_bf16_2d(const float* x, int64_t ldx, int64_t rows, int64_t cols, bf16* y, int64_t ldy,
+                           float scale, cudaStream_t s) {
+  if (rows * cols <= 0) return cudaSuccess;
+  f32_to_bf16_k<<<nblocks(rows * cols, 256), 256, 0, s>>>(x, ldx, rows, cols, y, ldy, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t add_bf16(const bf16* a, const bf16* b, int64_t n, bf16* y, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  if (n % 8 || !al16(a) || !al16(b) || !al16(y)) return cudaErrorInvalidValue;
+  add_bf16_k<<<nblocks(n / 8, 256), 256, 0, s>>>(a, b, n / 8, y);
+  return cudaGetLastError();
+}
+
+}  // namespace mt

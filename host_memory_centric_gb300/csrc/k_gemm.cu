@@ -1,0 +1,477 @@
+// k_gemm.cu -- BF16 GEMM on the 5th-generation tensor cores (sm_103a).
+//
+// Serves the projections of every block: Y = X W^T (forward and recompute),
+// dX = dY W (dgrad) and dW = dY^T X (wgrad, whose epilogue writes BF16 straight
+// into the gradient region of the streamed buffer, i.e. the flat layout the
+// gradient export copies out in one burst).
+//
+// Design (one CTA per SM, persistent over output tiles of 128 x 256):
+//   warp 0      TMA producer: 128B-swizzled tiles of A and B into a 4-stage
+//               shared-memory ring (mbarrier full/empty pairs);
+//   warp 1      allocates 512 TMEM columns (two 128x256 FP32 accumulators)
+//               and, from one thread, issues tcgen05.mma (M=128, N=256, K=16)
+//               and tcgen05.commit;
+//   warps 2..5  epilogue: tcgen05.ld 32x32b rows out of TMEM, optional FP32
+//               accumulate / residual add, BF16 round-to-nearest-even, store;
+//               the second accumulator lets the epilogue of tile i overlap the
+//               main loop of tile i+1.
+// Operands may be K-major or MN-major (the transpose bits of the instruction
+// descriptor), so dgrad and wgrad read activations and weights in place.
+// Every mbarrier wait is bounded; on expiry the kernel records an error code,
+// stops issuing, drains its own copies and frees its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "mt_kernels.h"
+
+namespace mt {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, UMMA_K = 16;
+constexpr int A_BYTES = BM * BK * 2;           // 16 KB
+constexpr int B_BYTES = BN * BK * 2;           // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int CHUNK_BYTES = 64 * BK * 2;       // one 64-wide MN chunk of an MN-major tile
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
+
+__device__ int g_kernel_error = 0;
+
+struct Epi {
+  bf16* D; int64_t ldd;
+  const bf16* R; int64_t ldr;
+  float* Dacc; int64_t ldacc; int acc_mode;
+  int M, N, K;
+  int tiles_m, tiles_n, group_m;
+};
+
+__device__ __forceinline__ uint32_t su32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity.  False on timeout or when
+// another role has aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_test(b, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_test(b, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+}
+__device__ __forceinline__ void tma_load(const CUtensorMap* map, uint64_t* bar, void* dst, int x,
+                                         int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(su32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum));
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading
+// and stride byte offsets (all >> 4), fixed version bit 46, 128B swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ULL << 46) | (2ULL << 61);
+}
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, transpose bits for
+// MN-major operands, N >> 3, M >> 4.
+__host__ __device__ constexpr uint32_t idesc(bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void tile_mn(int tile, const Epi& e, int& tm, int& tn) {
+  const int per_group = e.group_m * e.tiles_n;
+  const int first = (tile / per_group) * e.group_m;
+  const int gsize = min(e.tiles_m - first, e.group_m);
+  const int in = tile % per_group;
+  tm = first + in % gsize;
+  tn = in / gsize;
+}
+
+__device__ __forceinline__ void fail(volatile int* abort_flag, int code) {
+  *abort_flag = 1;
+  atomicCAS(&g_kernel_error, 0, code);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Epilogue of 32 consecutive columns of one output row.
+__device__ __forceinline__ void epi_store(const Epi& e, int row, int col, const uint32_t (&r)[32]) {
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  const int nv = min(32, e.N - col);
+  if (nv == 32) {
+    if (e.acc_mode) {
+      float4* p = reinterpret_cast<float4*>(e.Dacc + (int64_t)row * e.ldacc + col);
+      if (e.acc_mode == 2) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 o = p[i];
+          v[4 * i] += o.x; v[4 * i + 1] += o.y; v[4 * i + 2] += o.z; v[4 * i + 3] += o.w;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) p[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    }
+    if (e.R) {
+      const uint4* p = reinterpret_cast<const uint4*>(e.R + (int64_t)row * e.ldr + col);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint4 q = p[i];
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __bfloat1622float2(h[k]);
+          v[8 * i + 2 * k] += f.x;
+          v[8 * i + 2 * k + 1] += f.y;
+        }
+      }
+    }
+    if (e.D) {
+      uint4* p = reinterpret_cast<uint4*>(e.D + (int64_t)row * e.ldd + col);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        p[i] = make_uint4(pack_bf16(v[8 * i], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
+                          pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+    }
+  } else {
+    for (int i = 0; i < nv; ++i) {
+      float x = v[i];
+      if (e.acc_mode) {
+        float* p = e.Dacc + (int64_t)row * e.ldacc + col + i;
+        if (e.acc_mode == 2) x += *p;
+        *p = x;
+      }
+      if (e.R) x += __bfloat162float(e.R[(int64_t)row * e.ldr + col + i]);
+      if (e.D) e.D[(int64_t)row * e.ldd + col + i] = __float2bfloat16_rn(x);
+    }
+  }
+}
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const Epi e) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_tiles = e.tiles_m * e.tiles_n;
+  const int nk = (e.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // stages the producer has filled and may still be in flight (for the drain)
+  uint32_t inflight_mask = 0, inflight_parity = 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        int tm, tn;
+        tile_mn(tile, e, tm, tn);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&full[stage], STAGE_BYTES);
+          uint8_t* a = sA + stage * A_BYTES;
+          uint8_t* b = sB + stage * B_BYTES;
+          const int k0 = kb * BK;
+          if (!A_MN) {
+            tma_load(&tmA, &full[stage], a, k0, tm * BM);
+          } else {
+            tma_load(&tmA, &full[stage], a, tm * BM, k0);
+            tma_load(&tmA, &full[stage], a + CHUNK_BYTES, tm * BM + 64, k0);
+          }
+          if (!B_MN) {
+            tma_load(&tmB, &full[stage], b, k0, tn * BN);
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c) tma_load(&tmB, &full[stage], b + c * CHUNK_BYTES, tn * BN + 64 * c, k0);
+          }
+          inflight_mask |= 1u << stage;
+          inflight_parity = (inflight_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) fail(abort_flag, 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      constexpr uint32_t ID = idesc(A_MN, B_MN);
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = su32(sA + stage * A_BYTES), b0 = su32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            const uint64_t ad = A_MN ? sdesc(a0 + k * UMMA_K * 128, CHUNK_BYTES, 1024)
+                                     : sdesc(a0 + k * UMMA_K * 2, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc(b0 + k * UMMA_K * 128, CHUNK_BYTES, 1024)
+                                     : sdesc(b0 + k * UMMA_K * 2, 16, 1024);
+            tc_mma(d, ad, bd, ID, (kb | k) != 0);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+      }
+      if (!ok) fail(abort_flag, 2);
+    }
+  } else {
+    const int q = warp & 3;  // this warp may read TMEM lanes 32q .. 32q+31
+    const int row_in_tile = q * 32 + lane;
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      if (!mbar_wait(&tfull[acc], aph, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      int tm, tn;
+      tile_mn(tile, e, tm, tn);
+      const int row = tm * BM + row_in_tile;
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
+        const int col = tn * BN + c * 32;
+        if (row < e.M && col < e.N) epi_store(e, row, col, r);
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+    if (!ok && lane == 0) fail(abort_flag, 3);
+  }
+
+  // On an abort, let the producer's own copies land before the CTA exits.
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    for (int s = 0; s < STAGES; ++s)
+      if (inflight_mask & (1u << s)) {
+        const long long t0 = clock64();
+        while (!mbar_test(&full[s], (inflight_parity >> s) & 1) && clock64() - t0 < kWaitCycles) {
+        }
+      }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_once;
+int g_num_sms = 0;
+cudaError_t g_init_err = cudaSuccess;
+
+void init_once() {
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+    g_init_err = e != cudaSuccess ? e : cudaErrorNotSupported;
+    return;
+  }
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t a = cudaFuncSetAttribute(gemm_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t b = cudaFuncSetAttribute(gemm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t c = cudaFuncSetAttribute(gemm_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t d = cudaFuncSetAttribute(gemm_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (a != cudaSuccess) g_init_err = a;
+  else if (b != cudaSuccess) g_init_err = b;
+  else if (c != cudaSuccess) g_init_err = c;
+  else if (d != cudaSuccess) g_init_err = d;
+}
+
+// 2-D bf16 tensor map of a row-major [rows][cols] matrix with row stride ld,
+// box {64 columns, box_rows rows}, 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const bf16* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<bf16*>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+int gemm_num_sms() {
+  std::call_once(g_once, init_once);
+  return g_num_sms;
+}
+
+cudaError_t gemm(const GemmArgs& g, cudaStream_t s) {
+  std::call_once(g_once, init_once);
+  if (g_init_err != cudaSuccess) return g_init_err;
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0 || !g.A || !g.B) return cudaErrorInvalidValue;
+  if (!g.D && !g.acc_mode) return cudaErrorInvalidValue;
+  if ((g.lda | g.ldb) % 8 || (g.D && g.ldd % 8) || (g.R && g.ldr % 8) || (g.acc_mode && g.ldacc % 8))
+    return cudaErrorInvalidValue;
+  if (!al16(g.A) || !al16(g.B) || (g.D && !al16(g.D)) || (g.R && !al16(g.R)) || (g.acc_mode && !al16(g.Dacc)))
+    return cudaErrorInvalidValue;
+  if (g.acc_mode && !g.Dacc) return cudaErrorInvalidValue;
+  CUtensorMap ma, mb;
+  // A: K-major [M][K] (box 64 x 128) or MN-major [K][M] (box 64 x 64)
+  bool ok = g.a_mn ? make_map(&ma, g.A, g.K, g.M, g.lda, BK) : make_map(&ma, g.A, g.M, g.K, g.lda, BM);
+  ok = ok && (g.b_mn ? make_map(&mb, g.B, g.K, g.N, g.ldb, BK) : make_map(&mb, g.B, g.N, g.K, g.ldb, BN));
+  if (!ok) return cudaErrorInvalidValue;
+  Epi e;
+  e.D = g.D; e.ldd = g.ldd; e.R = g.R; e.ldr = g.ldr; e.Dacc = g.Dacc; e.ldacc = g.ldacc; e.acc_mode = g.acc_mode;
+  e.M = g.M; e.N = g.N; e.K = g.K;
+  e.tiles_m = (g.M + BM - 1) / BM;
+  e.tiles_n = (g.N + BN - 1) / BN;
+  e.group_m = 16;
+  const int tiles = e.tiles_m * e.tiles_n;
+  const int grid = tiles < g_num_sms ? tiles : g_num_sms;
+  if (!g.a_mn && !g.b_mn) gemm_kernel<false, false><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, e);
+  else if (!g.a_mn && g.b_mn) gemm_kernel<false, true><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, e);
+  else if (g.a_mn && !g.b_mn) gemm_kernel<true, false><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, e);
+  else gemm_kernel<true, true><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, e);
+  return cudaGetLastError();
+}
+
+cudaError_t kernel_error_read(int* code, int clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(code, g_kernel_error, sizeof(int));
+  if (e != cudaSuccess) return e;
+  if (clear) {
+    const int z = 0;
+    e = cudaMemcpyToSymbol(g_kernel_error, &z, sizeof(int));
+  }
+  return e;
+}
+
+}  // namespace mt

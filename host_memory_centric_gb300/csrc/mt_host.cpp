@@ -1,0 +1,256 @@
+// mt_host.cpp -- host-side pieces of libmt that need no GPU.
+#include "mt_host.h"
+
+#include <cmath>
+#include <cstring>
+
+namespace mth {
+
+// ---------------------------------------------------------------- layout
+bool config_valid(const mt_config* c, std::string* why) {
+  auto bad = [&](const char* s) {
+    if (why) *why = s;
+    return false;
+  };
+  if (!c) return bad("null config");
+  if (c->n_layers < 1 || c->hidden <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
+      c->ffn <= 0 || c->vocab <= 1 || c->batch <= 0 || c->seq <= 1 || c->micro_batches <= 0)
+    return bad("non-positive shape field");
+  if (c->n_heads % c->n_kv_heads) return bad("n_heads must be a multiple of n_kv_heads");
+  if (c->hidden % 8 || c->ffn % 8 || c->head_dim % 16) return bad("hidden, ffn must be multiples of 8; head_dim of 16");
+  if (c->ckpt_interval != 1) return bad("ckpt_interval must be 1");
+  if (c->n_grad_slabs < 1 || c->n_grad_slabs > 256) return bad("n_grad_slabs out of range");
+  if (c->timeout_ms == 0) return bad("timeout_ms must be positive");
+  if (!(c->rms_eps > 0) || !(c->rope_base > 1)) return bad("rms_eps / rope_base");
+  return true;
+}
+
+int64_t tokens_per_step(const mt_config* c) {
+  return (int64_t)c->micro_batches * c->batch * c->seq;
+}
+
+static int64_t up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+std::vector<BlockDesc> build_layout(const mt_config* c) {
+  const int64_t H = c->hidden, hd = c->head_dim, nh = c->n_heads, nkv = c->n_kv_heads, F = c->ffn;
+  const int64_t V = c->vocab, L = c->n_layers;
+  std::vector<BlockDesc> out((size_t)(L + 2));
+  int64_t store = 0;
+  for (int64_t j = 0; j <= L + 1; ++j) {
+    BlockDesc& b = out[(size_t)j];
+    int64_t shapes[MT_MAX_TENSORS][2];
+    int n = 0;
+    if (j == 0) {
+      shapes[n][0] = V; shapes[n++][1] = H;                      // E
+    } else if (j <= L) {
+      shapes[n][0] = (nh + 2 * nkv) * hd; shapes[n++][1] = H;    // W_qkv
+      shapes[n][0] = H; shapes[n++][1] = nh * hd;                // W_o
+      shapes[n][0] = 2 * F; shapes[n++][1] = H;                  // W_gu
+      shapes[n][0] = H; shapes[n++][1] = F;                      // W_down
+      shapes[n][0] = H; shapes[n++][1] = 1;                      // gamma1
+      shapes[n][0] = H; shapes[n++][1] = 1;                      // gamma2
+    } else {
+      shapes[n][0] = H; shapes[n++][1] = 1;                      // gamma_f
+      shapes[n][0] = V; shapes[n++][1] = H;                      // W_head
+    }
+    int64_t e = 0;
+    for (int t = 0; t < n; ++t) {
+      e = up(e, 128);
+      b.t[t] = {e, shapes[t][0], shapes[t][1]};
+      e += shapes[t][0] * shapes[t][1];
+      b.n_real += shapes[t][0] * shapes[t][1];
+    }
+    b.nt = n;
+    b.n_pad = up(e, 128);
+    b.wbytes = up(2 * b.n_pad, 4096);
+    b.fbytes = up(4 * b.n_pad, 4096);
+    b.region[0] = 0;
+    b.region[1] = b.wbytes;
+    b.region[2] = 2 * b.wbytes;
+    b.region[3] = 2 * b.wbytes + b.fbytes;
+    b.region[4] = 2 * b.wbytes + 2 * b.fbytes;
+    b.bytes = 2 * b.wbytes + 3 * b.fbytes;
+    b.store_off = store;
+    store += b.bytes;
+  }
+  return out;
+}
+
+// ---------------------------------------------------------------- numerics
+uint16_t bf16_rne(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof u);
+  const bool nan = ((u >> 23) & 0xFF) == 0xFF && (u & 0x7FFFFF) != 0;
+  if (nan) return (uint16_t)((u >> 16) | 0x0040);
+  u = u + 0x7FFF + ((u >> 16) & 1);
+  return (uint16_t)(u >> 16);
+}
+float bf16_val(uint16_t b) {
+  const uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+// SplitMix64 (Steele, Lea, Flood 2014) evaluated at a counter: the output
+// after i+1 increments of the golden gamma from `seed`.
+static inline uint64_t sm64(uint64_t seed, uint64_t i) {
+  uint64_t z = seed + (i + 1) * 0x9E3779B97F4A7C15ULL;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+  return z ^ (z >> 31);
+}
+
+void init_block(const mt_config* c, const BlockDesc& b, int j, float* master, int64_t e0, int64_t e1) {
+  // element e of the padded block; padding and gains handled per range
+  for (int t = 0; t < b.nt; ++t) {
+    const TensorDesc& d = b.t[t];
+    const int64_t n = d.rows * d.cols;
+    const int64_t lo = e0 > d.off ? e0 : d.off, hi = e1 < d.off + n ? e1 : d.off + n;
+    if (lo >= hi) continue;
+    if (d.cols == 1) {
+      for (int64_t e = lo; e < hi; ++e) master[e] = 1.0f;
+      continue;
+    }
+    const uint64_t key = sm64(c->seed, 1 + 64ULL * (uint64_t)j + (uint64_t)t);
+    for (int64_t e = lo; e < hi; ++e) {
+      const uint64_t i = (uint64_t)(e - d.off);
+      const uint64_t r1 = sm64(key, 2 * i), r2 = sm64(key, 2 * i + 1);
+      const double u1 = (double)((r1 >> 11) + 1) * (1.0 / 9007199254740992.0);
+      const double u2 = (double)(r2 >> 11) * (1.0 / 9007199254740992.0);
+      const double z = std::sqrt(-2.0 * std::log(u1)) * std::cos(6.283185307179586 * u2);
+      master[e] = (float)((double)c->init_std * z);
+    }
+  }
+}
+
+void adam(int64_t n, const uint16_t* __restrict g, float* __restrict th, float* __restrict m, float* __restrict v,
+          uint16_t* __restrict w, int32_t t, float lr, float b1, float b2, float eps, float wd) {
+  const float bc1 = (float)(1.0 - std::pow((double)b1, (double)t));
+  const float bc2 = (float)(1.0 - std::pow((double)b2, (double)t));
+  const float c1 = 1.0f - b1, c2 = 1.0f - b2;
+  for (int64_t i = 0; i < n; ++i) {
+    uint32_t gu = (uint32_t)g[i] << 16;
+    float gi;
+    std::memcpy(&gi, &gu, 4);
+    const float mi = b1 * m[i] + c1 * gi;
+    const float vi = b2 * v[i] + c2 * gi * gi;
+    m[i] = mi;
+    v[i] = vi;
+    float x = th[i];
+    if (wd != 0.0f) x -= lr * wd * x;
+    x -= lr * (mi / bc1) / (std::sqrt(vi / bc2) + eps);
+    th[i] = x;
+    uint32_t u;
+    std::memcpy(&u, &x, 4);
+    const bool nan = ((u >> 23) & 0xFF) == 0xFF && (u & 0x7FFFFF) != 0;
+    const uint32_t r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16;
+    w[i] = nan ? (uint16_t)((u >> 16) | 0x0040) : (uint16_t)r;
+  }
+}
+
+// ---------------------------------------------------------------- pool
+void Pool::start(int n) {
+  stop_ = false;
+  for (int i = 0; i < n; ++i)
+    threads_.emplace_back([this] {
+      for (;;) {
+        Task t;
+        {
+          std::unique_lock<std::mutex> lk(mu_);
+          cv_.wait(lk, [this] { return stop_ || !q_.empty(); });
+          if (q_.empty()) return;  // stopping
+          t = q_.front();
+          q_.pop_front();
+        }
+        run(t);
+      }
+    });
+}
+
+void Pool::stop() {
+  {
+    std::lock_guard<std::mutex> lk(mu_);
+    stop_ = true;
+  }
+  cv_.notify_all();
+  for (auto& t : threads_)
+    if (t.joinable()) t.join();
+  threads_.clear();
+}
+
+void Pool::run(Task& t) {
+  try {
+    (*t.fn)(t.i);
+  } catch (const std::exception& e) {
+    std::lock_guard<std::mutex> lk(t.latch->mu);
+    t.latch->bad = true;
+    t.latch->msg = e.what();
+  } catch (...) {
+    std::lock_guard<std::mutex> lk(t.latch->mu);
+    t.latch->bad = true;
+    t.latch->msg = "unknown exception in host worker";
+  }
+  if (t.latch->left.fetch_sub(1) == 1) {
+    std::lock_guard<std::mutex> lk(t.latch->mu);
+    t.latch->cv.notify_all();
+  }
+}
+
+bool Pool::run_one() {
+  Task t;
+  {
+    std::lock_guard<std::mutex> lk(mu_);
+    if (q_.empty()) return false;
+    t = q_.front();
+    q_.pop_front();
+  }
+  run(t);
+  return true;
+}
+
+bool Pool::parallel_for(int64_t n, const std::function<void(int64_t)>& fn, std::string* err) {
+  if (n <= 0) return true;
+  Latch latch;
+  latch.left = n;
+  {
+    std::lock_guard<std::mutex> lk(mu_);
+    for (int64_t i = 0; i < n; ++i) q_.push_back({&fn, i, &latch});
+  }
+  cv_.notify_all();
+  while (latch.left.load() > 0) {
+    if (run_one()) continue;
+    std::unique_lock<std::mutex> lk(latch.mu);
+    latch.cv.wait_for(lk, std::chrono::milliseconds(2), [&] { return latch.left.load() == 0; });
+  }
+  if (latch.bad) {
+    if (err) *err = latch.msg;
+    return false;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- schedule
+// Two device buffers: the stream-in of visit v+1 overlaps the compute of v and
+// may start once visit v-1's buffer is free, i.e. after its gradient export.
+// A slab is held from the start of its export until its Adam ends.
+int32_t schedule(int32_t n, const double* b, const double* d, const double* c, const double* a, double bw_h2d,
+                 double bw_d2h, double* stall) {
+  if (n <= 0 || !(bw_h2d > 0) || !(bw_d2h > 0)) return -1;
+  stall[0] = b[0] / bw_h2d;
+  for (int32_t v = 1; v < n; ++v) {
+    const double export_prev = v >= 2 ? d[v - 2] / bw_d2h : 0.0;
+    const double w = export_prev + b[v] / bw_h2d - c[v - 1];
+    stall[v] = w > 0.0 ? w : 0.0;
+  }
+  int32_t need = 1;
+  for (int32_t v = 0; v < n; ++v) {
+    if (!(d[v] > 0)) continue;
+    const double denom = c[v] > 0 ? c[v] : 1e-30;
+    const int32_t k = (int32_t)std::ceil((d[v] / bw_d2h + a[v]) / denom) + 1;
+    if (k > need) need = k;
+  }
+  return need;
+}
+
+}  // namespace mth

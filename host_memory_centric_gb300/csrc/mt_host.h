@@ -1,0 +1,89 @@
+// mt_host.h -- host-side pieces of libmt that need no GPU: flat layout,
+// seeded initialisation, BF16 rounding, Adam, the worker pool and the static
+// prefetch schedule.  Internal header.
+#pragma once
+#include <stdint.h>
+
+#include <atomic>
+#include <condition_variable>
+#include <deque>
+#include <functional>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "../../include/mt.h"
+
+namespace mth {
+
+// ---------------------------------------------------------------- layout
+// One block per layer ([Hotdry] layer-contiguous tiling; [Review] 3-2 (4)):
+// regions W (bf16) | G (bf16) | master | m | v (fp32), each at a 4096-byte
+// boundary of the block; the same tensors at the same element offsets in every
+// region, each tensor starting on a multiple of 128 elements.
+struct TensorDesc {
+  int64_t off, rows, cols;
+};
+struct BlockDesc {
+  TensorDesc t[MT_MAX_TENSORS];
+  int nt = 0;
+  int64_t n_real = 0, n_pad = 0;
+  int64_t region[5] = {0, 0, 0, 0, 0};  // byte offsets of W, G, master, m, v
+  int64_t wbytes = 0;                   // bytes of the W region (= G region)
+  int64_t fbytes = 0;                   // bytes of one fp32 region
+  int64_t bytes = 0, store_off = 0;
+};
+bool config_valid(const mt_config* c, std::string* why);
+std::vector<BlockDesc> build_layout(const mt_config* c);
+int64_t tokens_per_step(const mt_config* c);
+
+// ---------------------------------------------------------------- numerics
+uint16_t bf16_rne(float f);
+float bf16_val(uint16_t b);
+// Master values (n_pad floats) of block j: N(0, init_std) matrices from the
+// block/tensor stream of SplitMix64, RMSNorm gains 1, padding 0.
+void init_block(const mt_config* c, const BlockDesc& b, int j, float* master, int64_t e0, int64_t e1);
+// Adam over [0, n) (FP32 arithmetic).
+void adam(int64_t n, const uint16_t* g, float* th, float* m, float* v, uint16_t* w, int32_t t, float lr,
+          float b1, float b2, float eps, float wd);
+
+// ---------------------------------------------------------------- worker pool
+// Fixed threads running index ranges.  parallel_for may be called from several
+// threads at once; the caller works on queued ranges while it waits.
+class Pool {
+ public:
+  ~Pool() { stop(); }
+  void start(int n);
+  void stop();
+  int size() const { return (int)threads_.size(); }
+  // fn(i) for i in [0, n); returns false if any call threw (message in *err).
+  bool parallel_for(int64_t n, const std::function<void(int64_t)>& fn, std::string* err);
+
+ private:
+  struct Latch {
+    std::atomic<int64_t> left{0};
+    std::mutex mu;
+    std::condition_variable cv;
+    std::atomic<bool> bad{false};
+    std::string msg;
+  };
+  struct Task {
+    const std::function<void(int64_t)>* fn;
+    int64_t i;
+    Latch* latch;
+  };
+  bool run_one();
+  void run(Task& t);
+  std::vector<std::thread> threads_;
+  std::mutex mu_;
+  std::condition_variable cv_;
+  std::deque<Task> q_;
+  bool stop_ = false;
+};
+
+// ---------------------------------------------------------------- schedule
+int32_t schedule(int32_t n, const double* b, const double* d, const double* c, const double* a, double bw_h2d,
+                 double bw_d2h, double* stall);
+
+}  // namespace mth

@@ -1,0 +1,95 @@
+// mt_kernels.h -- internal launchers of the sm_103a kernels (not part of the C ABI).
+//
+// Every launcher enqueues on the given stream and returns a cudaError_t from
+// the launch; shape / alignment problems are reported as
+// cudaErrorInvalidValue before anything is launched.  All tensors are
+// row-major; "ld" is the row stride in elements.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mt {
+
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------- GEMM
+// D[m, n] = sum_k A(m, k) * B(n, k), FP32 accumulation in tensor memory.
+// A is K-major ([M][K], lda) unless a_mn ([K][M], lda); B is K-major
+// ([N][K], ldb) unless b_mn ([K][N], ldb).  Epilogue, in this order:
+//   acc_mode 2: acc += Dacc[m, n];  acc_mode >= 1: Dacc[m, n] = acc (fp32);
+//   R != null : acc += R[m, n];     D != null     : D[m, n] = bf16_rne(acc).
+// Requirements: lda, ldb, ldd, ldr, ldacc multiples of 8; pointers 16-byte
+// aligned; M, N, K >= 1.
+struct GemmArgs {
+  const bf16* A; int64_t lda; int a_mn;
+  const bf16* B; int64_t ldb; int b_mn;
+  int M, N, K;
+  bf16* D; int64_t ldd;
+  const bf16* R; int64_t ldr;
+  float* Dacc; int64_t ldacc; int acc_mode;
+};
+cudaError_t gemm(const GemmArgs& g, cudaStream_t s);
+int gemm_num_sms();
+
+// Device-side error word written by kernels whose bounded waits expired
+// (0 = none).  Read / cleared by the host.
+cudaError_t kernel_error_read(int* code, int clear);
+
+// ---------------------------------------------------------------- elementwise
+// RMSNorm forward: y = x * rstd * gamma, rstd = (mean(x^2) + eps)^-1/2.
+cudaError_t rmsnorm_fwd(const bf16* x, const bf16* gamma, int64_t T, int H, float eps, bf16* y,
+                        float* rstd, cudaStream_t s);
+// RMSNorm backward.  dx = r*gamma*dy - r^3/H * x * sum(dy*gamma*x) (+ dres
+// if not null).  dgamma (bf16, H) = sum over rows of dy * x * r; partial is
+// scratch of rmsnorm_bwd_partial_floats(T, H) floats.
+cudaError_t rmsnorm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const float* rstd,
+                        const bf16* dres, int64_t T, int H, bf16* dx, bf16* dgamma, float* partial,
+                        cudaStream_t s);
+int64_t rmsnorm_bwd_partial_floats(int64_t T, int H);
+int rmsnorm_bwd_blocks(int64_t T);
+// Reduces rmsnorm_bwd_blocks(T) rows of `partial` ([blocks][H] floats) into
+// dgamma (bf16).
+cudaError_t rmsnorm_bwd_stage2(const float* partial, int nblk, int H, bf16* dgamma, cudaStream_t s);
+
+// Rotate-half RoPE on the first n_heads heads (width hd) of every row of
+// x ([T][ld]); position = row % S; cs holds cos/sin [S][hd/2][2] in fp32.
+// inverse != 0 applies the transpose rotation.
+cudaError_t rope(bf16* x, int64_t T, int64_t ld, int n_heads, int hd, int S, const float* cs,
+                 int inverse, cudaStream_t s);
+// h = silu(g) * u with gu rows [g (F) | u (F)].
+cudaError_t swiglu_fwd(const bf16* gu, int64_t T, int F, bf16* h, cudaStream_t s);
+cudaError_t swiglu_bwd(const bf16* gu, const bf16* dh, int64_t T, int F, bf16* dgu, cudaStream_t s);
+// X[t] = E[tok[t]].
+cudaError_t embed_fwd(const int32_t* tok, const bf16* E, int64_t T, int H, int V, bf16* X,
+                      cudaStream_t s);
+// dE[v] = sum over t with tok[t] = v of dX[t], written densely as bf16 for all
+// V rows.  row_start[V+1] / rows[T] list, per vocabulary row, the token rows
+// that hold it (CSR, ascending).
+cudaError_t embed_bwd(const int32_t* row_start, const int32_t* rows, const bf16* dX, int V, int H,
+                      bf16* dE, cudaStream_t s);
+// Cross-entropy over `rows` rows of logits ([rows][V], bf16), overwritten with
+// dlogits = (softmax - onehot(target)) * inv_norm; rows with target < 0 get 0.
+// row_loss[r] = lse - logit[target] (0 without target).
+cudaError_t cross_entropy(bf16* logits, const int32_t* target, int64_t rows, int V, float inv_norm,
+                          float* row_loss, cudaStream_t s);
+// out[0] = sum(x[0..n)) * scale (single block, fixed order).
+cudaError_t reduce_sum(const float* x, int64_t n, float scale, float* out, cudaStream_t s);
+// y (bf16) = x (fp32) elementwise, n values; rows/ld variants for strided output.
+cudaError_t f32_to_bf16_2d(const float* x, int64_t ldx, int64_t rows, int64_t cols, bf16* y,
+                           int64_t ldy, float scale, cudaStream_t s);
+cudaError_t add_bf16(const bf16* a, const bf16* b, int64_t n, bf16* y, cudaStream_t s);
+
+// ---------------------------------------------------------------- attention
+// Causal grouped-query attention over n_seq sequences of S tokens.  qkv rows
+// ([T][(nh+2nkv)hd]) hold [q | k | v]; o is [T][nh*hd]; lse is [nh][T] fp32
+// (natural log).  hd in {64, 128}.
+cudaError_t attention_fwd(const bf16* qkv, int n_seq, int S, int nh, int nkv, int hd, bf16* o,
+                          float* lse, cudaStream_t s);
+// Backward: dqkv ([T][(nh+2nkv)hd]) receives dq, dk, dv.  delta ([nh][T]) and
+// dq_acc ([T][nh*hd] fp32) are scratch.
+cudaError_t attention_bwd(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout,
+                          int n_seq, int S, int nh, int nkv, int hd, bf16* dqkv, float* delta,
+                          float* dq_acc, cudaStream_t s);
+
+}  // namespace mt

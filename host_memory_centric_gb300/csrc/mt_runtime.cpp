@@ -1,0 +1,1326 @@
+// mt_runtime.cpp -- libmt: the layer-streamed training step behind the C ABI.
+//
+// Host RAM is the authoritative store of every parameter, gradient and Adam
+// moment; the GPU holds two ping-pong weight buffers and one layer's
+// activations ([Review] 3-2 (1)-(3); [Azure] "Layer-Wise Streaming",
+// "Stateless Execution").  A step visits the blocks forward (embedding,
+// decoder layers, head) and then backward in reverse, and each visit is:
+//   weight stream : wait Buffer-Free[b]; (pack W into pinned staging b);
+//                   H2D W (+ the block's checkpointed input); Weights-Ready[b]
+//   compute stream: wait Weights-Ready[b]; Bind; forward or recompute+backward;
+//                   Buffer-Free[b] (forward) or Backward-Done[b] (backward)
+//   gradient stream (backward visits): wait Backward-Done[b]; D2H G into a
+//                   free pinned slab; Buffer-Free[b]; slab event
+//   host          : an Adam worker waits for the slab event, unpacks the slab
+//                   into the G region and updates master / m / v / W
+// ([Hotdry] three CUDA streams and the event-driven synchronisation protocol;
+// [Review] 3-2 (3)-(6)).  No host barrier sits on the path: every host wait
+// is on a specific event or slab, with a deadline.
+#include <cuda_runtime.h>
+#include <sys/mman.h>
+
+#include <chrono>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <memory>
+
+#include "mt_host.h"
+#include "mt_kernels.h"
+
+using mt::bf16;
+using Clock = std::chrono::steady_clock;
+
+namespace {
+
+struct Job {
+  int32_t block, slab, t;
+};
+
+struct Dev {
+  uint8_t* buf[2] = {nullptr, nullptr};
+  bf16 *xslot[2] = {nullptr, nullptr}, *xck[2] = {nullptr, nullptr}, *dx[2] = {nullptr, nullptr};
+  bf16 *ckdev = nullptr, *xlast = nullptr;
+  bf16 *xn = nullptr, *x1 = nullptr, *yn = nullptr, *qkv = nullptr, *dqkv = nullptr, *attn = nullptr,
+       *dattn = nullptr;
+  bf16 *gu = nullptr, *dgu = nullptr, *h = nullptr, *dh = nullptr, *dyn = nullptr, *dx1 = nullptr,
+       *dxn = nullptr, *logits = nullptr;
+  float *rstd1 = nullptr, *rstd2 = nullptr, *lse = nullptr, *delta = nullptr, *dq_acc = nullptr,
+        *row_loss = nullptr, *loss = nullptr, *rms_part = nullptr, *dwacc = nullptr, *cs = nullptr;
+  int32_t *tok = nullptr, *tgt = nullptr, *csr_start = nullptr, *csr_rows = nullptr;
+};
+
+struct KStat {
+  int64_t launches = 0;
+  double ms = 0, flops = 0, bytes = 0;
+};
+struct Pending {
+  cudaEvent_t a, b;
+  int kind;
+  double flops, bytes;
+};
+
+}  // namespace
+
+struct mt_model {
+  mt_config c{};
+  int L = 0, H = 0, nh = 0, nkv = 0, hd = 0, F = 0, V = 0, B = 0, S = 0, M = 0, Nqkv = 0;
+  int64_t T = 0, chunk = 0;
+  std::vector<mth::BlockDesc> lay;
+  int64_t wb_max = 0;
+  bool live = false;  // false: scheduler dry run (log only)
+  // host memory
+  uint8_t* store = nullptr;
+  size_t store_bytes = 0;
+  bool registered = false;
+  uint8_t* staging[2] = {nullptr, nullptr};
+  uint8_t* slabs = nullptr;
+  uint8_t* ckpt = nullptr;
+  int32_t* htok = nullptr;  // pinned: tok[T] | tgt[T] | csr_start[V+1] | csr_rows[T]
+  float* hloss = nullptr;
+  size_t pinned_bytes = 0;
+  int K = 12;
+  // device
+  Dev d;
+  uint8_t* dev_base = nullptr;
+  size_t dev_bytes = 0, dev_used = 0;
+  cudaStream_t sc = nullptr, sw = nullptr, sg = nullptr;
+  cudaEvent_t WR[2] = {}, BD[2] = {}, BF[2] = {}, XR[2] = {}, XS[2] = {}, TOK = nullptr, LOSS = nullptr;
+  std::vector<cudaEvent_t> SR;
+  // host workers
+  mth::Pool pool;
+  std::thread adam_thr;
+  std::mutex amu;
+  std::condition_variable acv;
+  std::deque<Job> jobs;
+  bool stopping = false;
+  int inflight_jobs = 0;
+  std::vector<int64_t> adam_done;  // last Adam step applied per block
+  std::vector<char> slab_free;
+  // state
+  std::atomic<bool> failed{false};
+  mutable std::mutex emu;
+  std::string err;
+  int64_t steps_done = 0, exports = 0;
+  bool used[2] = {false, false};
+  int vis = 0, stage = 0;  // next visit of the current step, and its sub-stage
+  bool tokens_set = false;
+  std::vector<std::string> log;
+  // stats
+  std::atomic<int64_t> h2d{0}, d2h{0};
+  double last_step_ms = 0, pack_ms = 0;
+  std::atomic<int64_t> adam_us{0};
+  // kernel timing (events around launches on the compute stream)
+  bool timing = false;
+  std::vector<Pending> pend;
+  std::vector<cudaEvent_t> ev_pool;
+  KStat kstat[4];
+
+  ~mt_model();
+};
+
+namespace {
+
+// ---------------------------------------------------------------- errors
+mt_status set_err(mt_model* m, mt_status s, const std::string& msg, bool latch = true) {
+  if (m) {
+    std::lock_guard<std::mutex> lk(m->emu);
+    m->err = msg;
+    if (latch && s != MT_ERR_ARG) m->failed = true;
+  }
+  return s;
+}
+#define CU(m, call)                                                                              \
+  do {                                                                                           \
+    cudaError_t e_ = (call);                                                                     \
+    if (e_ != cudaSuccess)                                                                       \
+      return set_err(m, MT_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_));       \
+  } while (0)
+#define OK(x)                     \
+  do {                            \
+    mt_status s_ = (x);           \
+    if (s_ != MT_OK) return s_;   \
+  } while (0)
+
+double now_ms() {
+  return std::chrono::duration<double, std::milli>(Clock::now().time_since_epoch()).count();
+}
+
+// Bounded host wait on an event.
+mt_status wait_event(mt_model* m, cudaEvent_t ev, const char* what) {
+  const auto dl = Clock::now() + std::chrono::milliseconds(m->c.timeout_ms);
+  for (;;) {
+    const cudaError_t e = cudaEventQuery(ev);
+    if (e == cudaSuccess) return MT_OK;
+    if (e != cudaErrorNotReady)
+      return set_err(m, MT_ERR_CUDA, std::string("event ") + what + ": " + cudaGetErrorString(e));
+    if (Clock::now() > dl) return set_err(m, MT_ERR_TIMEOUT, std::string("timed out waiting for ") + what);
+    if (m->failed) return MT_ERR_STATE;
+    std::this_thread::sleep_for(std::chrono::microseconds(20));
+  }
+}
+
+void logop(mt_model* m, const char* s, const char* op, long a, long b) {
+  if (!m->c.log_protocol && m->live) return;
+  char line[96];
+  std::snprintf(line, sizeof line, "%lld %s %s %ld %ld", (long long)m->steps_done, s, op, a, b);
+  m->log.emplace_back(line);
+}
+
+int64_t up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+int64_t head_chunk(const mt_config* c, int64_t T) {
+  if (c->head_chunk > 0) return c->head_chunk < T ? c->head_chunk : T;
+  const int64_t cap = (int64_t)8 << 30;
+  const int64_t per = 2LL * c->vocab;
+  if (T * per <= cap) return T;
+  int64_t ch = cap / per / 128 * 128;
+  return ch < 128 ? 128 : ch;
+}
+
+// Carves the device region; with base == nullptr only sizes it.
+size_t carve(const mt_config* c, const std::vector<mth::BlockDesc>& lay, uint8_t* base, Dev* d) {
+  const int64_t T = mth::tokens_per_step(c), H = c->hidden, hd = c->head_dim, nh = c->n_heads,
+                nkv = c->n_kv_heads, F = c->ffn, V = c->vocab, L = c->n_layers, S = c->seq;
+  const int64_t Nqkv = (nh + 2 * nkv) * hd, chunk = head_chunk(c, T);
+  int64_t wb = 0;
+  for (auto& b : lay) wb = b.wbytes > wb ? b.wbytes : wb;
+  size_t off = 0;
+  auto take = [&](int64_t bytes) -> uint8_t* {
+    off = (size_t)up((int64_t)off, 256);
+    uint8_t* p = base ? base + off : nullptr;
+    off += (size_t)bytes;
+    return p;
+  };
+  const int64_t act = T * H * 2;
+  for (int b = 0; b < 2; ++b) d->buf[b] = take(2 * wb);
+  for (int b = 0; b < 2; ++b) d->dx[b] = (bf16*)take(act);
+  if (c->ckpt_on_host) {
+    for (int b = 0; b < 2; ++b) d->xslot[b] = (bf16*)take(act);
+    for (int b = 0; b < 2; ++b) d->xck[b] = (bf16*)take(act);
+  } else {
+    d->ckdev = (bf16*)take(act * L);
+    d->xlast = (bf16*)take(act);
+  }
+  d->xn = (bf16*)take(act);
+  d->x1 = (bf16*)take(act);
+  d->yn = (bf16*)take(act);
+  d->dyn = (bf16*)take(act);
+  d->dx1 = (bf16*)take(act);
+  d->dxn = (bf16*)take(act);
+  d->qkv = (bf16*)take(T * Nqkv * 2);
+  d->dqkv = (bf16*)take(T * Nqkv * 2);
+  d->attn = (bf16*)take(T * nh * hd * 2);
+  d->dattn = (bf16*)take(T * nh * hd * 2);
+  d->gu = (bf16*)take(T * 2 * F * 2);
+  d->dgu = (bf16*)take(T * 2 * F * 2);
+  d->h = (bf16*)take(T * F * 2);
+  d->dh = (bf16*)take(T * F * 2);
+  d->logits = (bf16*)take(chunk * V * 2);
+  d->rstd1 = (float*)take(T * 4);
+  d->rstd2 = (float*)take(T * 4);
+  d->lse = (float*)take(nh * T * 4);
+  d->delta = (float*)take(nh * T * 4);
+  d->dq_acc = (float*)take(T * nh * hd * 4);
+  d->row_loss = (float*)take(T * 4);
+  d->loss = (float*)take(256);
+  d->rms_part = (float*)take(mt::rmsnorm_bwd_partial_floats(T, (int)H) * 4);
+  d->dwacc = chunk < T ? (float*)take(V * H * 4) : nullptr;
+  d->cs = (float*)take(S * hd * 4);
+  d->tok = (int32_t*)take(T * 4);
+  d->tgt = (int32_t*)take(T * 4);
+  d->csr_start = (int32_t*)take((V + 1) * 4);
+  d->csr_rows = (int32_t*)take(T * 4);
+  return (size_t)up((int64_t)off, 256);
+}
+
+// ---------------------------------------------------------------- kernel timing
+cudaEvent_t take_event(mt_model* m) {
+  if (!m->ev_pool.empty()) {
+    cudaEvent_t e = m->ev_pool.back();
+    m->ev_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+struct Timed {
+  mt_model* m;
+  int kind;
+  double flops, bytes;
+  cudaEvent_t a = nullptr;
+  Timed(mt_model* mm, int k, double f, double b) : m(mm), kind(k), flops(f), bytes(b) {
+    if (m->timing) {
+      a = take_event(m);
+      cudaEventRecord(a, m->sc);
+    }
+  }
+  ~Timed() {
+    if (a) {
+      cudaEvent_t b = take_event(m);
+      cudaEventRecord(b, m->sc);
+      m->pend.push_back({a, b, kind, flops, bytes});
+    }
+  }
+};
+void collect_timing(mt_model* m) {
+  for (auto& p : m->pend) {
+    float ms = 0;
+    if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
+      KStat& k = m->kstat[p.kind];
+      k.launches++;
+      k.ms += ms;
+      k.flops += p.flops;
+      k.bytes += p.bytes;
+    }
+    m->ev_pool.push_back(p.a);
+    m->ev_pool.push_back(p.b);
+  }
+  m->pend.clear();
+}
+
+// ---------------------------------------------------------------- GEMM forms
+enum { K_GEMM = 0, K_ATTN_F = 1, K_ATTN_B = 2, K_OTHER = 3 };
+
+mt_status gemm_run(mt_model* m, const mt::GemmArgs& g) {
+  Timed t(m, K_GEMM, 2.0 * g.M * g.N * g.K, 0);
+  CU(m, mt::gemm(g, m->sc));
+  return MT_OK;
+}
+// Y[T,N] = X[T,K] W[N,K]^T (+ R)
+mt_status fprop(mt_model* m, const bf16* X, const bf16* W, int64_t T, int N, int K, bf16* Y, const bf16* R) {
+  mt::GemmArgs g{X, K, 0, W, K, 0, (int)T, N, K, Y, N, R, N, nullptr, 0, 0};
+  return gemm_run(m, g);
+}
+// dX[T,K] = dY[T,N] W[N,K]
+mt_status dgrad(mt_model* m, const bf16* dY, const bf16* W, int64_t T, int N, int K, bf16* dX) {
+  mt::GemmArgs g{dY, N, 0, W, K, 1, (int)T, K, N, dX, K, nullptr, 0, nullptr, 0, 0};
+  return gemm_run(m, g);
+}
+// dW[N,K] = dY[T,N]^T X[T,K]  (acc_mode / Dacc for chunked accumulation)
+mt_status wgrad(mt_model* m, const bf16* dY, const bf16* X, int64_t T, int N, int K, bf16* dW, float* acc,
+                int acc_mode) {
+  mt::GemmArgs g{dY, N, 1, X, K, 1, N, K, (int)T, dW, K, nullptr, 0, acc, K, acc_mode};
+  return gemm_run(m, g);
+}
+
+struct View {
+  const bf16* w[MT_MAX_TENSORS];
+  bf16* g[MT_MAX_TENSORS];
+};
+View make_view(mt_model* m, int j, int b) {
+  View v{};
+  const mth::BlockDesc& bd = m->lay[(size_t)j];
+  for (int t = 0; t < bd.nt; ++t) {
+    v.w[t] = reinterpret_cast<const bf16*>(m->d.buf[b] + bd.region[0]) + bd.t[t].off;
+    v.g[t] = reinterpret_cast<bf16*>(m->d.buf[b] + bd.region[1]) + bd.t[t].off;
+  }
+  return v;
+}
+
+const bf16* x_fwd_in(mt_model* m, int j) {  // X_{j-1}
+  const int i = j - 1;
+  if (m->c.ckpt_on_host) return m->d.xslot[i % 2];
+  return i < m->L ? m->d.ckdev + (int64_t)i * m->T * m->H : m->d.xlast;
+}
+bf16* x_out(mt_model* m, int j) {  // X_j
+  if (m->c.ckpt_on_host) return m->d.xslot[j % 2];
+  return j < m->L ? m->d.ckdev + (int64_t)j * m->T * m->H : m->d.xlast;
+}
+const bf16* x_bwd_in(mt_model* m, int j, int b) {  // checkpoint X_{j-1} for the recompute
+  if (m->c.ckpt_on_host) return m->d.xck[b];
+  return m->d.ckdev + (int64_t)(j - 1) * m->T * m->H;
+}
+
+// ---------------------------------------------------------------- block math
+// Decoder block forward (pre-RMSNorm, RoPE, GQA causal attention, SwiGLU).
+// With `recompute`, everything the backward reads is rebuilt and the final
+// projection is skipped.
+mt_status decoder_forward(mt_model* m, const View& v, const bf16* x, bf16* out, bool recompute) {
+  const int64_t T = m->T;
+  const int H = m->H, F = m->F, nhd = m->nh * m->hd;
+  cudaStream_t s = m->sc;
+  Dev& d = m->d;
+  {
+    Timed t(m, K_OTHER, 0, 4.0 * T * H + 4.0 * T);
+    CU(m, mt::rmsnorm_fwd(x, v.w[4], T, H, m->c.rms_eps, d.xn, d.rstd1, s));
+  }
+  OK(fprop(m, d.xn, v.w[0], T, m->Nqkv, H, d.qkv, nullptr));
+  {
+    Timed t(m, K_OTHER, 0, 4.0 * T * (m->nh + m->nkv) * m->hd);
+    CU(m, mt::rope(d.qkv, T, m->Nqkv, m->nh + m->nkv, m->hd, m->S, d.cs, 0, s));
+  }
+  {
+    const double fl = 4.0 * m->M * m->B * (double)m->nh * m->hd * (double)m->S * m->S / 2;
+    Timed t(m, K_ATTN_F, fl, 0);
+    CU(m, mt::attention_fwd(d.qkv, m->M * m->B, m->S, m->nh, m->nkv, m->hd, d.attn, d.lse, s));
+  }
+  OK(fprop(m, d.attn, v.w[1], T, H, nhd, d.x1, x));
+  {
+    Timed t(m, K_OTHER, 0, 4.0 * T * H + 4.0 * T);
+    CU(m, mt::rmsnorm_fwd(d.x1, v.w[5], T, H, m->c.rms_eps, d.yn, d.rstd2, s));
+  }
+  OK(fprop(m, d.yn, v.w[2], T, 2 * F, H, d.gu, nullptr));
+  {
+    Timed t(m, K_OTHER, 0, 6.0 * T * F);
+    CU(m, mt::swiglu_fwd(d.gu, T, F, d.h, s));
+  }
+  if (!recompute) OK(fprop(m, d.h, v.w[3], T, H, F, out, d.x1));
+  return MT_OK;
+}
+
+// Recompute + backward of a decoder block.  dout = dL/dX_j (read), din =
+// dL/dX_{j-1} (written); weight gradients land in v.g[*].
+mt_status decoder_backward(mt_model* m, const View& v, const bf16* x, const bf16* dout, bf16* din) {
+  OK(decoder_forward(m, v, x, nullptr, true));
+  const int64_t T = m->T;
+  const int H = m->H, F = m->F, nhd = m->nh * m->hd;
+  cudaStream_t s = m->sc;
+  Dev& d = m->d;
+  OK(wgrad(m, dout, d.h, T, H, F, v.g[3], nullptr, 0));
+  OK(dgrad(m, dout, v.w[3], T, H, F, d.dh));
+  {
+    Timed t(m, K_OTHER, 0, 10.0 * T * F);
+    CU(m, mt::swiglu_bwd(d.gu, d.dh, T, F, d.dgu, s));
+  }
+  OK(wgrad(m, d.dgu, d.yn, T, 2 * F, H, v.g[2], nullptr, 0));
+  OK(dgrad(m, d.dgu, v.w[2], T, 2 * F, H, d.dyn));
+  {
+    Timed t(m, K_OTHER, 0, 8.0 * T * H + 4.0 * T);
+    CU(m, mt::rmsnorm_bwd(d.dyn, d.x1, v.w[5], d.rstd2, dout, T, H, d.dx1, v.g[5], d.rms_part, s));
+  }
+  OK(wgrad(m, d.dx1, d.attn, T, H, nhd, v.g[1], nullptr, 0));
+  OK(dgrad(m, d.dx1, v.w[1], T, H, nhd, d.dattn));
+  {
+    const double fl = 10.0 * m->M * m->B * (double)m->nh * m->hd * (double)m->S * m->S / 2;
+    Timed t(m, K_ATTN_B, fl, 0);
+    CU(m, mt::attention_bwd(d.qkv, d.attn, d.lse, d.dattn, m->M * m->B, m->S, m->nh, m->nkv, m->hd, d.dqkv,
+                            d.delta, d.dq_acc, s));
+  }
+  {
+    Timed t(m, K_OTHER, 0, 4.0 * T * (m->nh + m->nkv) * m->hd);
+    CU(m, mt::rope(d.dqkv, T, m->Nqkv, m->nh + m->nkv, m->hd, m->S, d.cs, 1, s));
+  }
+  OK(wgrad(m, d.dqkv, d.xn, T, m->Nqkv, H, v.g[0], nullptr, 0));
+  OK(dgrad(m, d.dqkv, v.w[0], T, m->Nqkv, H, d.dxn));
+  {
+    Timed t(m, K_OTHER, 0, 8.0 * T * H + 4.0 * T);
+    CU(m, mt::rmsnorm_bwd(d.dxn, x, v.w[4], d.rstd1, d.dx1, T, H, din, v.g[4], d.rms_part, s));
+  }
+  return MT_OK;
+}
+
+// Head visit: final RMSNorm, LM head, cross-entropy and their backward,
+// token-chunked so the logits never exceed one chunk.
+mt_status head_forward_backward(mt_model* m, const View& v, const bf16* x, bf16* din) {
+  const int64_t T = m->T;
+  const int H = m->H, V = m->V;
+  cudaStream_t s = m->sc;
+  Dev& d = m->d;
+  bf16* hn = d.xn;
+  bf16* dhn = d.dxn;
+  float* rstd = d.rstd1;
+  {
+    Timed t(m, K_OTHER, 0, 4.0 * T * H);
+    CU(m, mt::rmsnorm_fwd(x, v.w[0], T, H, m->c.rms_eps, hn, rstd, s));
+  }
+  const float inv_norm = 1.0f / (float)((double)m->M * m->B * (m->S - 1));
+  for (int64_t c0 = 0; c0 < T; c0 += m->chunk) {
+    const int64_t rows = (T - c0) < m->chunk ? (T - c0) : m->chunk;
+    const bool first = c0 == 0, last = c0 + rows >= T;
+    OK(fprop(m, hn + c0 * H, v.w[1], rows, V, H, d.logits, nullptr));
+    {
+      Timed t(m, K_OTHER, 0, 6.0 * rows * V);
+      CU(m, mt::cross_entropy(d.logits, d.tgt + c0, rows, V, inv_norm, d.row_loss + c0, s));
+    }
+    OK(dgrad(m, d.logits, v.w[1], rows, V, H, dhn + c0 * H));
+    if (m->chunk >= T) {
+      OK(wgrad(m, d.logits, hn, rows, V, H, v.g[1], nullptr, 0));
+    } else {
+      OK(wgrad(m, d.logits, hn + c0 * H, rows, V, H, last ? v.g[1] : nullptr, d.dwacc, first ? 1 : 2));
+    }
+  }
+  CU(m, mt::reduce_sum(d.row_loss, T, inv_norm, d.loss, s));
+  CU(m, cudaMemcpyAsync(m->hloss, d.loss, sizeof(float), cudaMemcpyDeviceToHost, s));
+  CU(m, cudaEventRecord(m->LOSS, s));
+  {
+    Timed t(m, K_OTHER, 0, 8.0 * T * H);
+    CU(m, mt::rmsnorm_bwd(dhn, x, v.w[0], rstd, nullptr, T, H, din, v.g[0], d.rms_part, s));
+  }
+  return MT_OK;
+}
+
+// ---------------------------------------------------------------- Adam worker
+void adam_loop(mt_model* m) {
+  for (;;) {
+    Job job;
+    {
+      std::unique_lock<std::mutex> lk(m->amu);
+      m->acv.wait(lk, [m] { return m->stopping || !m->jobs.empty(); });
+      if (m->jobs.empty()) return;
+      job = m->jobs.front();
+      m->jobs.pop_front();
+    }
+    const auto t0 = Clock::now();
+    mt_status st = m->failed ? MT_ERR_STATE : wait_event(m, m->SR[(size_t)job.slab], "slab ready");
+    if (st == MT_OK) {
+      const mth::BlockDesc& b = m->lay[(size_t)job.block];
+      uint8_t* blk = m->store + b.store_off;
+      const uint16_t* slab = reinterpret_cast<const uint16_t*>(m->slabs + (size_t)job.slab * m->wb_max);
+      uint16_t* G = reinterpret_cast<uint16_t*>(blk + b.region[1]);
+      uint16_t* W = reinterpret_cast<uint16_t*>(blk + b.region[0]);
+      float* th = reinterpret_cast<float*>(blk + b.region[2]);
+      float* mm = reinterpret_cast<float*>(blk + b.region[3]);
+      float* vv = reinterpret_cast<float*>(blk + b.region[4]);
+      // work items: (tensor, chunk) ranges of at most 1 Mi elements
+      constexpr int64_t CH = 1 << 20;
+      std::vector<std::pair<int64_t, int64_t>> items;
+      for (int t = 0; t < b.nt; ++t) {
+        const int64_t o = b.t[t].off, n = b.t[t].rows * b.t[t].cols;
+        for (int64_t e = 0; e < n; e += CH) items.push_back({o + e, (n - e) < CH ? (n - e) : CH});
+      }
+      const mt_config& c = m->c;
+      std::function<void(int64_t)> fn = [&](int64_t i) {
+        const int64_t o = items[(size_t)i].first, n = items[(size_t)i].second;
+        std::memcpy(G + o, slab + o, (size_t)n * 2);
+        mth::adam(n, G + o, th + o, mm + o, vv + o, W + o, job.t, c.lr, c.beta1, c.beta2, c.adam_eps,
+                  c.weight_decay);
+      };
+      std::string werr;
+      if (!m->pool.parallel_for((int64_t)items.size(), fn, &werr))
+        st = set_err(m, MT_ERR_INTERNAL, "host Adam worker: " + werr);
+    }
+    m->adam_us += std::chrono::duration_cast<std::chrono::microseconds>(Clock::now() - t0).count();
+    {
+      std::lock_guard<std::mutex> lk(m->amu);
+      if (st == MT_OK) m->adam_done[(size_t)job.block] = job.t;
+      m->slab_free[(size_t)job.slab] = 1;
+      m->inflight_jobs--;
+    }
+    m->acv.notify_all();
+  }
+}
+
+// Host waits (bounded) until block j has had Adam step t applied.
+mt_status wait_adam(mt_model* m, int j, int64_t t) {
+  std::unique_lock<std::mutex> lk(m->amu);
+  const bool ok = m->acv.wait_for(lk, std::chrono::milliseconds(m->c.timeout_ms),
+                                  [&] { return m->failed || m->adam_done[(size_t)j] >= t; });
+  if (m->failed) return MT_ERR_STATE;
+  if (!ok) return set_err(m, MT_ERR_TIMEOUT, "timed out waiting for Adam of block " + std::to_string(j));
+  return MT_OK;
+}
+
+mt_status acquire_slab(mt_model* m, int k) {
+  std::unique_lock<std::mutex> lk(m->amu);
+  const bool ok = m->acv.wait_for(lk, std::chrono::milliseconds(m->c.timeout_ms),
+                                  [&] { return m->failed || m->slab_free[(size_t)k]; });
+  if (m->failed) return MT_ERR_STATE;
+  if (!ok) return set_err(m, MT_ERR_TIMEOUT, "timed out waiting for a free gradient slab");
+  m->slab_free[(size_t)k] = 0;
+  return MT_OK;
+}
+
+// ---------------------------------------------------------------- visit pieces
+int nvisits(const mt_model* m) { return 2 * m->L + 3; }
+int visit_block(const mt_model* m, int v) { return v <= m->L + 1 ? v : 2 * m->L + 2 - v; }
+bool visit_fwd(const mt_model* m, int v) { return v <= m->L + 1; }
+
+mt_status do_stream_in(mt_model* m, int j, int b) {
+  const bool fwd = visit_fwd(m, m->vis);
+  const bool copies = !(j == 0 && !fwd);
+  const mth::BlockDesc& bd = m->lay[(size_t)j];
+  if (fwd && m->steps_done > 0) {
+    logop(m, "H", "WAIT_ADAM", j, -1);
+    if (m->live) OK(wait_adam(m, j, m->steps_done));
+  }
+  const uint8_t* src = m->live ? m->store + bd.store_off + bd.region[0] : nullptr;
+  if (copies && !m->c.pin_store) {
+    if (m->used[b]) {
+      logop(m, "H", "WAIT_STAGE", b, -1);
+      if (m->live) OK(wait_event(m, m->WR[b], "staging free"));
+    }
+    logop(m, "H", "PACK", j, b);
+    if (m->live) {
+      const double t0 = now_ms();
+      uint8_t* dst = m->staging[b];
+      constexpr int64_t CH = 8 << 20;
+      const int64_t n = (bd.wbytes + CH - 1) / CH;
+      std::function<void(int64_t)> fn = [&](int64_t i) {
+        const int64_t o = i * CH, len = (bd.wbytes - o) < CH ? (bd.wbytes - o) : CH;
+        std::memcpy(dst + o, src + o, (size_t)len);
+      };
+      std::string werr;
+      if (!m->pool.parallel_for(n, fn, &werr)) return set_err(m, MT_ERR_INTERNAL, "pack: " + werr);
+      m->pack_ms += now_ms() - t0;
+      src = dst;
+    }
+  }
+  logop(m, "W", "WAIT_BF", b, -1);
+  if (m->live) CU(m, cudaStreamWaitEvent(m->sw, m->BF[b], 0));
+  if (copies) {
+    logop(m, "W", "H2D", j, b);
+    if (m->live) {
+      CU(m, cudaMemcpyAsync(m->d.buf[b], src, (size_t)bd.wbytes, cudaMemcpyHostToDevice, m->sw));
+      m->h2d += bd.wbytes;
+    }
+  }
+  if (!fwd && j >= 1 && j <= m->L && m->c.ckpt_on_host) {
+    logop(m, "W", "H2D_CKPT", j, b);
+    if (m->live) {
+      const size_t bytes = (size_t)m->T * m->H * 2;
+      CU(m, cudaMemcpyAsync(m->d.xck[b], m->ckpt + (size_t)(j - 1) * bytes, bytes, cudaMemcpyHostToDevice, m->sw));
+      m->h2d += (int64_t)bytes;
+    }
+  }
+  logop(m, "W", "REC_WR", b, -1);
+  if (m->live) CU(m, cudaEventRecord(m->WR[b], m->sw));
+  m->used[b] = true;
+  return MT_OK;
+}
+
+mt_status do_bind(mt_model* m, int j, int b, mt_layer_view* out) {
+  logop(m, "C", "WAIT_WR", b, -1);
+  if (m->live) CU(m, cudaStreamWaitEvent(m->sc, m->WR[b], 0));
+  if (out) {
+    std::memset(out, 0, sizeof *out);
+    out->block = j;
+    out->buf = b;
+    if (m->live) {
+      const View v = make_view(m, j, b);
+      out->n_tensors = m->lay[(size_t)j].nt;
+      for (int t = 0; t < out->n_tensors; ++t) {
+        out->w[t] = v.w[t];
+        out->g[t] = v.g[t];
+      }
+    }
+  }
+  return MT_OK;
+}
+
+mt_status do_forward(mt_model* m, int j, int b) {
+  const bool head = j == m->L + 1;
+  const bool writes_x = j <= m->L;
+  const bool ckh = m->c.ckpt_on_host != 0;
+  if (writes_x && ckh) {
+    logop(m, "C", "WAIT_XS", j % 2, -1);
+    if (m->live) CU(m, cudaStreamWaitEvent(m->sc, m->XS[j % 2], 0));
+  }
+  logop(m, "C", head ? "HEAD" : "FWD", j, b);
+  if (m->live) {
+    const View v = make_view(m, j, b);
+    if (j == 0) {
+      Timed t(m, K_OTHER, 0, 4.0 * m->T * m->H);
+      CU(m, mt::embed_fwd(m->d.tok, v.w[0], m->T, m->H, m->V, x_out(m, 0), m->sc));
+    } else if (!head) {
+      OK(decoder_forward(m, v, x_fwd_in(m, j), x_out(m, j), false));
+    } else {
+      OK(head_forward_backward(m, v, x_fwd_in(m, j), m->d.dx[m->L % 2]));
+    }
+  }
+  const bool saves = writes_x && j < m->L && ckh;
+  if (saves) {
+    logop(m, "C", "REC_XR", j % 2, -1);
+    if (m->live) CU(m, cudaEventRecord(m->XR[j % 2], m->sc));
+  }
+  if (!head) {
+    logop(m, "C", "REC_BF", b, -1);
+    if (m->live) CU(m, cudaEventRecord(m->BF[b], m->sc));
+  } else {
+    logop(m, "C", "REC_BD", b, -1);
+    if (m->live) CU(m, cudaEventRecord(m->BD[b], m->sc));
+  }
+  if (saves) {
+    const int s = j % 2;
+    logop(m, "G", "WAIT_XR", s, -1);
+    if (m->live) CU(m, cudaStreamWaitEvent(m->sg, m->XR[s], 0));
+    logop(m, "G", "D2H_CKPT", j, s);
+    if (m->live) {
+      const size_t bytes = (size_t)m->T * m->H * 2;
+      CU(m, cudaMemcpyAsync(m->ckpt + (size_t)j * bytes, m->d.xslot[s], bytes, cudaMemcpyDeviceToHost, m->sg));
+      m->d2h += (int64_t)bytes;
+    }
+    logop(m, "G", "REC_XS", s, -1);
+    if (m->live) CU(m, cudaEventRecord(m->XS[s], m->sg));
+  }
+  return MT_OK;
+}
+
+mt_status do_backward(mt_model* m, int j, int b) {
+  logop(m, "C", "BWD", j, b);
+  if (m->live) {
+    const View v = make_view(m, j, b);
+    if (j == 0) {
+      Timed t(m, K_OTHER, 0, 2.0 * m->T * m->H + 2.0 * m->V * m->H);
+      CU(m, mt::embed_bwd(m->d.csr_start, m->d.csr_rows, m->d.dx[0], m->V, m->H, v.g[0], m->sc));
+    } else {
+      OK(decoder_backward(m, v, x_bwd_in(m, j, b), m->d.dx[j % 2], m->d.dx[(j - 1) % 2]));
+    }
+  }
+  logop(m, "C", "REC_BD", b, -1);
+  if (m->live) CU(m, cudaEventRecord(m->BD[b], m->sc));
+  return MT_OK;
+}
+
+mt_status do_stream_out(mt_model* m, int j, int b, int* slab_out) {
+  const int k = (int)(m->exports % m->K);
+  m->exports++;
+  const mth::BlockDesc& bd = m->lay[(size_t)j];
+  logop(m, "G", "WAIT_BD", b, -1);
+  if (m->live) CU(m, cudaStreamWaitEvent(m->sg, m->BD[b], 0));
+  logop(m, "H", "ACQ_SLAB", k, -1);
+  if (m->live) OK(acquire_slab(m, k));
+  logop(m, "G", "D2H", j, k);
+  if (m->live) {
+    CU(m, cudaMemcpyAsync(m->slabs + (size_t)k * m->wb_max, m->d.buf[b] + bd.region[1], (size_t)bd.wbytes,
+                          cudaMemcpyDeviceToHost, m->sg));
+    m->d2h += bd.wbytes;
+  }
+  logop(m, "G", "REC_BF", b, -1);
+  if (m->live) CU(m, cudaEventRecord(m->BF[b], m->sg));
+  logop(m, "G", "REC_SR", k, -1);
+  if (m->live) CU(m, cudaEventRecord(m->SR[(size_t)k], m->sg));
+  if (slab_out) *slab_out = k;
+  return MT_OK;
+}
+
+mt_status do_adam_enqueue(mt_model* m, int j, int k, int32_t t) {
+  logop(m, "H", "ADAM_ENQ", j, k);
+  if (m->live) {
+    {
+      std::lock_guard<std::mutex> lk(m->amu);
+      m->jobs.push_back({j, k, t});
+      m->inflight_jobs++;
+    }
+    m->acv.notify_all();
+  }
+  return MT_OK;
+}
+
+// Sub-stages of a visit: 0 stream_in, 1 bind, 2 compute, 3 stream_out, 4 adam.
+bool exports_grad(const mt_model* m, int v) { return !visit_fwd(m, v) || visit_block(m, v) == m->L + 1; }
+
+void advance(mt_model* m) {
+  const bool exp = exports_grad(m, m->vis);
+  if ((!exp && m->stage == 2) || (exp && m->stage == 4)) {
+    m->stage = 0;
+    if (++m->vis == nvisits(m)) {
+      m->vis = 0;
+      m->steps_done++;
+    }
+  } else {
+    m->stage++;
+  }
+}
+
+mt_status expect(mt_model* m, int stage, int block) {
+  if (m->failed) return MT_ERR_STATE;
+  if (m->stage != stage || visit_block(m, m->vis) != block)
+    return set_err(m, MT_ERR_STATE, "call out of order: expected stage " + std::to_string(m->stage) +
+                                        " of block " + std::to_string(visit_block(m, m->vis)),
+                   false);
+  return MT_OK;
+}
+
+mt_status run_visit(mt_model* m) {
+  const int v = m->vis, j = visit_block(m, v), b = v % 2;
+  OK(do_stream_in(m, j, b));
+  advance(m);
+  OK(do_bind(m, j, b, nullptr));
+  advance(m);
+  if (visit_fwd(m, v)) OK(do_forward(m, j, b));
+  else OK(do_backward(m, j, b));
+  const bool exp = exports_grad(m, v);
+  const int64_t t = m->steps_done + 1;
+  advance(m);
+  if (exp) {
+    int k = 0;
+    OK(do_stream_out(m, j, b, &k));
+    advance(m);
+    OK(do_adam_enqueue(m, j, k, (int32_t)t));
+    advance(m);
+  }
+  return MT_OK;
+}
+
+void compute_tables(mt_model* m, std::vector<float>& cs) {
+  const int half = m->hd / 2;
+  cs.resize((size_t)m->S * m->hd);
+  for (int p = 0; p < m->S; ++p)
+    for (int i = 0; i < half; ++i) {
+      const double th = std::pow((double)m->c.rope_base, -2.0 * i / (double)m->hd);
+      const double a = (double)p * th;
+      cs[((size_t)p * half + i) * 2] = (float)std::cos(a);
+      cs[((size_t)p * half + i) * 2 + 1] = (float)std::sin(a);
+    }
+}
+
+void fill_shape(mt_model* m) {
+  const mt_config& c = m->c;
+  m->L = c.n_layers; m->H = c.hidden; m->nh = c.n_heads; m->nkv = c.n_kv_heads; m->hd = c.head_dim;
+  m->F = c.ffn; m->V = c.vocab; m->B = c.batch; m->S = c.seq; m->M = c.micro_batches;
+  m->Nqkv = (m->nh + 2 * m->nkv) * m->hd;
+  m->T = mth::tokens_per_step(&c);
+  m->chunk = head_chunk(&c, m->T);
+  m->lay = mth::build_layout(&c);
+  m->wb_max = 0;
+  for (auto& b : m->lay) m->wb_max = b.wbytes > m->wb_max ? b.wbytes : m->wb_max;
+  m->K = c.n_grad_slabs;
+}
+
+}  // namespace
+
+mt_model::~mt_model() {
+  {
+    std::lock_guard<std::mutex> lk(amu);
+    stopping = true;
+  }
+  acv.notify_all();
+  if (adam_thr.joinable()) adam_thr.join();
+  pool.stop();
+  if (live) {
+    if (sc) cudaStreamSynchronize(sc);
+    if (sw) cudaStreamSynchronize(sw);
+    if (sg) cudaStreamSynchronize(sg);
+    for (cudaEvent_t* e : {&WR[0], &WR[1], &BD[0], &BD[1], &BF[0], &BF[1], &XR[0], &XR[1], &XS[0], &XS[1], &TOK, &LOSS})
+      if (*e) cudaEventDestroy(*e);
+    for (auto e : SR)
+      if (e) cudaEventDestroy(e);
+    for (auto& p : pend) {
+      cudaEventDestroy(p.a);
+      cudaEventDestroy(p.b);
+    }
+    for (auto e : ev_pool) cudaEventDestroy(e);
+    if (registered) cudaHostUnregister(store);
+    for (int b = 0; b < 2; ++b)
+      if (staging[b]) cudaFreeHost(staging[b]);
+    if (slabs) cudaFreeHost(slabs);
+    if (ckpt) cudaFreeHost(ckpt);
+    if (htok) cudaFreeHost(htok);
+    if (hloss) cudaFreeHost(hloss);
+  }
+  if (store) munmap(store, store_bytes);
+}
+
+// ======================================================================== C ABI
+extern "C" {
+
+mt_status mt_default_config(mt_config* c) {
+  if (!c) return MT_ERR_ARG;
+  std::memset(c, 0, sizeof *c);
+  c->rope_base = 10000.0f;
+  c->rms_eps = 1e-6f;
+  c->init_std = 0.02f;
+  c->micro_batches = 1;
+  c->ckpt_interval = 1;
+  c->ckpt_on_host = 1;
+  c->n_grad_slabs = 12;
+  c->lr = 1e-3f;
+  c->beta1 = 0.9f;
+  c->beta2 = 0.999f;
+  c->adam_eps = 1e-8f;
+  c->seed = 1;
+  c->timeout_ms = 60000;
+  return MT_OK;
+}
+
+mt_status mt_query_device_bytes(const mt_config* c, size_t* bytes) {
+  if (!bytes || !mth::config_valid(c, nullptr)) return MT_ERR_ARG;
+  Dev d;
+  *bytes = carve(c, mth::build_layout(c), nullptr, &d);
+  return MT_OK;
+}
+
+mt_status mt_init_model(const mt_config* c, mt_dev_region dev, mt_streams s, mt_model** out) {
+  if (!out) return MT_ERR_ARG;
+  *out = nullptr;
+  std::string why;
+  if (!mth::config_valid(c, &why)) return MT_ERR_ARG;
+  if (!dev.base || !s.compute || !s.weight || !s.grad) return MT_ERR_ARG;
+  std::unique_ptr<mt_model> m(new mt_model());
+  m->c = *c;
+  m->live = true;
+  fill_shape(m.get());
+  m->dev_base = (uint8_t*)dev.base;
+  m->dev_bytes = dev.bytes;
+  m->dev_used = carve(c, m->lay, nullptr, &m->d);
+  if (m->dev_used > dev.bytes) return MT_ERR_DEVICE_OOM;
+  carve(c, m->lay, m->dev_base, &m->d);
+  m->sc = (cudaStream_t)s.compute;
+  m->sw = (cudaStream_t)s.weight;
+  m->sg = (cudaStream_t)s.grad;
+  mt_model* mm = m.get();
+
+  // host flat store: pageable anonymous memory, advised for huge pages
+  for (auto& b : m->lay) m->store_bytes += (size_t)b.bytes;
+  void* p = mmap(nullptr, m->store_bytes, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+  if (p == MAP_FAILED) return MT_ERR_HOST_OOM;
+  m->store = (uint8_t*)p;
+#ifdef MADV_HUGEPAGE
+  madvise(p, m->store_bytes, MADV_HUGEPAGE);
+#endif
+  int nth = c->n_host_threads > 0 ? c->n_host_threads : (int)std::thread::hardware_concurrency();
+  if (nth < 1) nth = 1;
+  m->pool.start(nth);
+
+  // initial values, in parallel over 4 Mi-element ranges (first touch included)
+  {
+    struct Item { int j; int64_t e0, e1; };
+    std::vector<Item> items;
+    for (int j = 0; j < (int)m->lay.size(); ++j)
+      for (int64_t e = 0; e < m->lay[(size_t)j].n_pad; e += (4 << 20))
+        items.push_back({j, e, std::min<int64_t>(m->lay[(size_t)j].n_pad, e + (4 << 20))});
+    std::function<void(int64_t)> fn = [&](int64_t i) {
+      const Item& it = items[(size_t)i];
+      const mth::BlockDesc& b = mm->lay[(size_t)it.j];
+      uint8_t* blk = mm->store + b.store_off;
+      float* th = (float*)(blk + b.region[2]);
+      mth::init_block(&mm->c, b, it.j, th, it.e0, it.e1);
+      uint16_t* W = (uint16_t*)(blk + b.region[0]);
+      uint16_t* G = (uint16_t*)(blk + b.region[1]);
+      float* m1 = (float*)(blk + b.region[3]);
+      float* v1 = (float*)(blk + b.region[4]);
+      for (int64_t e = it.e0; e < it.e1; ++e) {
+        W[e] = mth::bf16_rne(th[e]);
+        G[e] = 0;
+        m1[e] = 0.f;
+        v1[e] = 0.f;
+      }
+    };
+    std::string werr;
+    if (!m->pool.parallel_for((int64_t)items.size(), fn, &werr)) return MT_ERR_INTERNAL;
+  }
+  if (c->pin_store) {
+    if (cudaHostRegister(m->store, m->store_bytes, cudaHostRegisterDefault) != cudaSuccess) return MT_ERR_HOST_OOM;
+    m->registered = true;
+  } else {
+    for (int b = 0; b < 2; ++b) {
+      if (cudaHostAlloc((void**)&m->staging[b], (size_t)m->wb_max, cudaHostAllocDefault) != cudaSuccess)
+        return MT_ERR_HOST_OOM;
+      m->pinned_bytes += (size_t)m->wb_max;
+    }
+  }
+  if (cudaHostAlloc((void**)&m->slabs, (size_t)m->wb_max * m->K, cudaHostAllocDefault) != cudaSuccess)
+    return MT_ERR_HOST_OOM;
+  m->pinned_bytes += (size_t)m->wb_max * m->K;
+  if (c->ckpt_on_host) {
+    const size_t bytes = (size_t)m->L * m->T * m->H * 2;
+    if (cudaHostAlloc((void**)&m->ckpt, bytes, cudaHostAllocDefault) != cudaSuccess) return MT_ERR_HOST_OOM;
+    m->pinned_bytes += bytes;
+  }
+  const size_t tokb = (size_t)(3 * m->T + m->V + 1) * 4;
+  if (cudaHostAlloc((void**)&m->htok, tokb, cudaHostAllocDefault) != cudaSuccess) return MT_ERR_HOST_OOM;
+  if (cudaHostAlloc((void**)&m->hloss, 64, cudaHostAllocDefault) != cudaSuccess) return MT_ERR_HOST_OOM;
+  m->pinned_bytes += tokb + 64;
+
+  for (cudaEvent_t* e : {&m->WR[0], &m->WR[1], &m->BD[0], &m->BD[1], &m->BF[0], &m->BF[1], &m->XR[0], &m->XR[1],
+                         &m->XS[0], &m->XS[1], &m->TOK, &m->LOSS})
+    CU(mm, cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+  m->SR.assign((size_t)m->K, nullptr);
+  for (auto& e : m->SR) CU(mm, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+  m->slab_free.assign((size_t)m->K, 1);
+  m->adam_done.assign(m->lay.size(), 0);
+
+  std::vector<float> cs;
+  compute_tables(m.get(), cs);
+  CU(mm, cudaMemcpyAsync(m->d.cs, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice, m->sc));
+  CU(mm, cudaMemsetAsync(m->d.loss, 0, 256, m->sc));
+  for (int b = 0; b < 2; ++b) CU(mm, cudaMemsetAsync(m->d.buf[b], 0, (size_t)2 * m->wb_max, m->sc));
+  CU(mm, cudaStreamSynchronize(m->sc));
+  m->adam_thr = std::thread(adam_loop, mm);
+  *out = m.release();
+  return MT_OK;
+}
+
+mt_status mt_set_tokens(mt_model* m, const int32_t* tok) {
+  if (!m || !tok) return MT_ERR_ARG;
+  if (m->failed) return MT_ERR_STATE;
+  const int64_t T = m->T;
+  for (int64_t i = 0; i < T; ++i)
+    if (tok[i] < 0 || tok[i] >= m->V) return set_err(m, MT_ERR_ARG, "token id out of range", false);
+  if (m->tokens_set) OK(wait_event(m, m->TOK, "previous token upload"));
+  int32_t* h = m->htok;
+  int32_t* tg = h + T;
+  int32_t* cst = tg + T;
+  int32_t* rows = cst + m->V + 1;
+  std::memcpy(h, tok, (size_t)T * 4);
+  for (int64_t t = 0; t < T; ++t) tg[t] = (t % m->S) < m->S - 1 ? tok[t + 1] : -1;
+  mt_token_csr(tok, T, m->V, cst, rows);
+  CU(m, cudaMemcpyAsync(m->d.tok, h, (size_t)T * 4, cudaMemcpyHostToDevice, m->sc));
+  CU(m, cudaMemcpyAsync(m->d.tgt, tg, (size_t)T * 4, cudaMemcpyHostToDevice, m->sc));
+  CU(m, cudaMemcpyAsync(m->d.csr_start, cst, (size_t)(m->V + 1) * 4, cudaMemcpyHostToDevice, m->sc));
+  CU(m, cudaMemcpyAsync(m->d.csr_rows, rows, (size_t)T * 4, cudaMemcpyHostToDevice, m->sc));
+  CU(m, cudaEventRecord(m->TOK, m->sc));
+  m->h2d += (3 * T + m->V + 1) * 4;
+  m->tokens_set = true;
+  return MT_OK;
+}
+
+mt_status mt_stream_in(mt_model* m, int32_t block, int32_t buf) {
+  if (!m || buf < 0 || buf > 1) return MT_ERR_ARG;
+  OK(expect(m, 0, block));
+  OK(do_stream_in(m, block, buf));
+  advance(m);
+  return MT_OK;
+}
+
+mt_status mt_bind(mt_model* m, int32_t block, int32_t buf, mt_layer_view* view) {
+  if (!m || buf < 0 || buf > 1) return MT_ERR_ARG;
+  OK(expect(m, 1, block));
+  OK(do_bind(m, block, buf, view));
+  advance(m);
+  return MT_OK;
+}
+
+mt_status mt_step_forward(mt_model* m, const mt_layer_view* v) {
+  if (!m || !v) return MT_ERR_ARG;
+  if (!m->tokens_set) return set_err(m, MT_ERR_STATE, "no tokens set", false);
+  if (!visit_fwd(m, m->vis)) return set_err(m, MT_ERR_STATE, "forward called in the backward pass", false);
+  OK(expect(m, 2, v->block));
+  OK(do_forward(m, v->block, v->buf));
+  advance(m);
+  return MT_OK;
+}
+
+mt_status mt_step_backward(mt_model* m, const mt_layer_view* v) {
+  if (!m || !v) return MT_ERR_ARG;
+  if (visit_fwd(m, m->vis)) return set_err(m, MT_ERR_STATE, "backward called in the forward pass", false);
+  OK(expect(m, 2, v->block));
+  OK(do_backward(m, v->block, v->buf));
+  advance(m);
+  return MT_OK;
+}
+
+mt_status mt_stream_out(mt_model* m, int32_t block, int32_t buf, int32_t* slab) {
+  if (!m || buf < 0 || buf > 1) return MT_ERR_ARG;
+  OK(expect(m, 3, block));
+  int k = 0;
+  OK(do_stream_out(m, block, buf, &k));
+  if (slab) *slab = k;
+  advance(m);
+  return MT_OK;
+}
+
+mt_status mt_adam_host(mt_model* m, int32_t block, int32_t slab, int32_t adam_step) {
+  if (!m || slab < 0 || slab >= m->K || adam_step < 1) return MT_ERR_ARG;
+  OK(expect(m, 4, block));
+  OK(do_adam_enqueue(m, block, slab, adam_step));
+  advance(m);
+  return MT_OK;
+}
+
+mt_status mt_train_step(mt_model* m, int32_t step, float* loss) {
+  if (!m) return MT_ERR_ARG;
+  if (m->failed) return MT_ERR_STATE;
+  if (step != m->steps_done || m->vis != 0 || m->stage != 0)
+    return set_err(m, MT_ERR_STATE, "mt_train_step: step index or visit state mismatch", false);
+  if (!m->tokens_set) return set_err(m, MT_ERR_STATE, "no tokens set", false);
+  const double t0 = now_ms();
+  const int n = nvisits(m);
+  for (int v = 0; v < n; ++v) OK(run_visit(m));
+  if (loss) {
+    OK(wait_event(m, m->LOSS, "loss"));
+    *loss = *m->hloss;
+  }
+  m->last_step_ms = now_ms() - t0;
+  return MT_OK;
+}
+
+mt_status mt_sync(mt_model* m) {
+  if (!m) return MT_ERR_ARG;
+  if (m->failed) return MT_ERR_STATE;
+  for (cudaStream_t s : {m->sc, m->sw, m->sg}) {
+    cudaEvent_t e;
+    CU(m, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    CU(m, cudaEventRecord(e, s));
+    const mt_status st = wait_event(m, e, "stream drain");
+    cudaEventDestroy(e);
+    OK(st);
+  }
+  {
+    std::unique_lock<std::mutex> lk(m->amu);
+    const bool ok = m->acv.wait_for(lk, std::chrono::milliseconds(m->c.timeout_ms),
+                                    [&] { return m->failed || (m->jobs.empty() && m->inflight_jobs == 0); });
+    if (m->failed) return MT_ERR_STATE;
+    if (!ok) return set_err(m, MT_ERR_TIMEOUT, "timed out draining Adam jobs");
+  }
+  if (m->timing) collect_timing(m);
+  return MT_OK;
+}
+
+mt_status mt_read_host(mt_model* m, int32_t block, int32_t region, void* dst, size_t bytes) {
+  if (!m || !dst || block < 0 || block >= (int)m->lay.size() || region < 0 || region > 4) return MT_ERR_ARG;
+  const mth::BlockDesc& b = m->lay[(size_t)block];
+  const int64_t rb = region < 2 ? b.wbytes : b.fbytes;
+  if ((int64_t)bytes > rb) return MT_ERR_ARG;
+  std::memcpy(dst, m->store + b.store_off + b.region[region], bytes);
+  return MT_OK;
+}
+
+mt_status mt_write_host(mt_model* m, int32_t block, int32_t region, const void* src, size_t bytes) {
+  if (!m || !src || block < 0 || block >= (int)m->lay.size() || region < 0 || region > 4) return MT_ERR_ARG;
+  const mth::BlockDesc& b = m->lay[(size_t)block];
+  const int64_t rb = region < 2 ? b.wbytes : b.fbytes;
+  if ((int64_t)bytes > rb) return MT_ERR_ARG;
+  std::memcpy(m->store + b.store_off + b.region[region], src, bytes);
+  return MT_OK;
+}
+
+mt_status mt_get_stats(const mt_model* m, mt_stats* o) {
+  if (!m || !o) return MT_ERR_ARG;
+  std::memset(o, 0, sizeof *o);
+  o->steps_done = m->steps_done;
+  o->h2d_bytes = m->h2d.load();
+  o->d2h_bytes = m->d2h.load();
+  o->device_bytes_used = (int64_t)m->dev_used;
+  o->last_step_ms = m->last_step_ms;
+  o->adam_ms_total = m->adam_us.load() / 1000.0;
+  o->pack_ms_total = m->pack_ms;
+  o->host_store_bytes = (int64_t)m->store_bytes;
+  o->pinned_bytes = (int64_t)m->pinned_bytes;
+  return MT_OK;
+}
+
+int64_t mt_protocol_log(const mt_model* m, char* buf, int64_t cap) {
+  if (!m) return 0;
+  std::string s;
+  for (auto& l : m->log) {
+    s += l;
+    s += '\n';
+  }
+  const int64_t need = (int64_t)s.size() + 1;
+  if (!buf || cap < need) return -need;
+  std::memcpy(buf, s.c_str(), (size_t)need);
+  return need - 1;
+}
+
+const char* mt_last_error(const mt_model* m) {
+  if (!m) return "null model";
+  std::lock_guard<std::mutex> lk(m->emu);
+  static thread_local std::string copy;
+  copy = m->err;
+  return copy.c_str();
+}
+
+void mt_destroy(mt_model* m) { delete m; }
+
+// ------------------------------------------------------------------ host-only
+int64_t mt_layout_block(const mt_config* c, int32_t j, int64_t* out, int64_t cap) {
+  if (!mth::config_valid(c, nullptr) || !out || j < 0 || j > c->n_layers + 1) return -1;
+  const auto lay = mth::build_layout(c);
+  const mth::BlockDesc& b = lay[(size_t)j];
+  const int64_t need = 10 + 3 * b.nt;
+  if (cap < need) return -1;
+  out[0] = b.nt; out[1] = b.n_real; out[2] = b.n_pad;
+  for (int r = 0; r < 5; ++r) out[3 + r] = b.region[r];
+  out[8] = b.bytes; out[9] = b.store_off;
+  for (int t = 0; t < b.nt; ++t) {
+    out[10 + 3 * t] = b.t[t].off; out[11 + 3 * t] = b.t[t].rows; out[12 + 3 * t] = b.t[t].cols;
+  }
+  return need;
+}
+
+int64_t mt_param_count(const mt_config* c) {
+  if (!mth::config_valid(c, nullptr)) return -1;
+  int64_t p = 0;
+  for (auto& b : mth::build_layout(c)) p += b.n_real;
+  return p;
+}
+
+int64_t mt_store_bytes(const mt_config* c) {
+  if (!mth::config_valid(c, nullptr)) return -1;
+  int64_t s = 0;
+  for (auto& b : mth::build_layout(c)) s += b.bytes;
+  return s;
+}
+
+mt_status mt_host_init_block(const mt_config* c, int32_t j, float* master) {
+  if (!mth::config_valid(c, nullptr) || !master || j < 0 || j > c->n_layers + 1) return MT_ERR_ARG;
+  const auto lay = mth::build_layout(c);
+  const mth::BlockDesc& b = lay[(size_t)j];
+  std::memset(master, 0, (size_t)b.n_pad * 4);
+  mth::init_block(c, b, j, master, 0, b.n_pad);
+  return MT_OK;
+}
+
+mt_status mt_host_adam(int64_t n, const uint16_t* g, float* th, float* m, float* v, uint16_t* w, int32_t t,
+                       float lr, float b1, float b2, float eps, float wd, int32_t n_threads) {
+  if (n < 0 || !g || !th || !m || !v || !w || t < 1) return MT_ERR_ARG;
+  mth::Pool pool;
+  pool.start(n_threads > 0 ? n_threads : 1);
+  constexpr int64_t CH = 1 << 18;
+  std::function<void(int64_t)> fn = [&](int64_t i) {
+    const int64_t o = i * CH, len = (n - o) < CH ? (n - o) : CH;
+    mth::adam(len, g + o, th + o, m + o, v + o, w + o, t, lr, b1, b2, eps, wd);
+  };
+  std::string err;
+  const bool ok = pool.parallel_for((n + CH - 1) / CH, fn, &err);
+  pool.stop();
+  return ok ? MT_OK : MT_ERR_INTERNAL;
+}
+
+int64_t mt_plan_protocol(const mt_config* c, int32_t n_steps, char* buf, int64_t cap) {
+  if (!mth::config_valid(c, nullptr) || n_steps < 0) return 0;
+  mt_model m;
+  m.c = *c;
+  m.live = false;
+  fill_shape(&m);
+  m.tokens_set = true;
+  for (int s = 0; s < n_steps; ++s)
+    for (int v = 0; v < nvisits(&m); ++v)
+      if (run_visit(&m) != MT_OK) return 0;
+  return mt_protocol_log(&m, buf, cap);
+}
+
+int32_t mt_schedule(int32_t n, const double* b, const double* d, const double* c, const double* a, double bw_h2d,
+                    double bw_d2h, double* stall) {
+  if (!b || !d || !c || !a || !stall) return -1;
+  return mth::schedule(n, b, d, c, a, bw_h2d, bw_d2h, stall);
+}
+
+mt_status mt_token_csr(const int32_t* tok, int64_t T, int32_t V, int32_t* row_start, int32_t* rows) {
+  if (!tok || !row_start || !rows || V <= 0 || T < 0) return MT_ERR_ARG;
+  std::memset(row_start, 0, (size_t)(V + 1) * 4);
+  for (int64_t t = 0; t < T; ++t) {
+    if (tok[t] < 0 || tok[t] >= V) return MT_ERR_ARG;
+    row_start[tok[t] + 1]++;
+  }
+  for (int32_t v = 0; v < V; ++v) row_start[v + 1] += row_start[v];
+  std::vector<int32_t> fill(row_start, row_start + V);
+  for (int64_t t = 0; t < T; ++t) rows[fill[(size_t)tok[t]]++] = (int32_t)t;
+  return MT_OK;
+}
+
+mt_status mt_rope_table(int32_t S, int32_t hd, double base, float* out) {
+  if (S <= 0 || hd <= 0 || hd % 2 || !out) return MT_ERR_ARG;
+  const int half = hd / 2;
+  for (int p = 0; p < S; ++p)
+    for (int i = 0; i < half; ++i) {
+      const double a = (double)p * std::pow(base, -2.0 * i / (double)hd);
+      out[((size_t)p * half + i) * 2] = (float)std::cos(a);
+      out[((size_t)p * half + i) * 2 + 1] = (float)std::sin(a);
+    }
+  return MT_OK;
+}
+
+// ------------------------------------------------------------------ timing
+mt_status mt_timing(mt_model* m, int32_t enable) {
+  if (!m) return MT_ERR_ARG;
+  if (!enable) OK(mt_sync(m));
+  m->timing = enable != 0;
+  for (auto& k : m->kstat) k = KStat();
+  return MT_OK;
+}
+
+mt_status mt_timing_read(mt_model* m, int32_t kind, int64_t* launches, double* ms, double* flops, double* bytes) {
+  if (!m || kind < 0 || kind > 3) return MT_ERR_ARG;
+  collect_timing(m);
+  const KStat& k = m->kstat[kind];
+  if (launches) *launches = k.launches;
+  if (ms) *ms = k.ms;
+  if (flops) *flops = k.flops;
+  if (bytes) *bytes = k.bytes;
+  return MT_OK;
+}
+
+// ------------------------------------------------------------------ per-op
+static mt_status cu_status(cudaError_t e) {
+  if (e == cudaSuccess) return MT_OK;
+  if (e == cudaErrorInvalidValue) return MT_ERR_ARG;
+  return MT_ERR_CUDA;
+}
+
+mt_status mt_gemm(const void* A, int64_t lda, int32_t a_mn, const void* B, int64_t ldb, int32_t b_mn, int32_t M,
+                  int32_t N, int32_t K, void* D, int64_t ldd, const void* R, int64_t ldr, float* Dacc,
+                  int64_t ldacc, int32_t acc_mode, void* stream) {
+  if (acc_mode < 0 || acc_mode > 2) return MT_ERR_ARG;
+  mt::GemmArgs g{(const bf16*)A, lda, a_mn, (const bf16*)B, ldb, b_mn, M, N, K, (bf16*)D, ldd, (const bf16*)R,
+                 ldr, Dacc, ldacc, acc_mode};
+  return cu_status(mt::gemm(g, (cudaStream_t)stream));
+}
+
+mt_status mt_rmsnorm_fwd(const void* x, const void* gamma, int64_t T, int32_t H, float eps, void* y, float* rstd,
+                         void* stream) {
+  if (!x || !gamma || !y || !rstd) return MT_ERR_ARG;
+  return cu_status(mt::rmsnorm_fwd((const bf16*)x, (const bf16*)gamma, T, H, eps, (bf16*)y, rstd, (cudaStream_t)stream));
+}
+
+size_t mt_rmsnorm_bwd_scratch_bytes(int64_t T, int32_t H) {
+  return (size_t)mt::rmsnorm_bwd_partial_floats(T, H) * sizeof(float);
+}
+
+mt_status mt_rmsnorm_bwd(const void* dy, const void* x, const void* gamma, const float* rstd, const void* dres,
+                         int64_t T, int32_t H, void* dx, void* dgamma, void* scratch, size_t scratch_bytes,
+                         void* stream) {
+  if (!dy || !x || !gamma || !rstd || !dx || !dgamma || !scratch) return MT_ERR_ARG;
+  if (scratch_bytes < mt_rmsnorm_bwd_scratch_bytes(T, H)) return MT_ERR_ARG;
+  return cu_status(mt::rmsnorm_bwd((const bf16*)dy, (const bf16*)x, (const bf16*)gamma, rstd, (const bf16*)dres, T,
+                                   H, (bf16*)dx, (bf16*)dgamma, (float*)scratch, (cudaStream_t)stream));
+}
+
+mt_status mt_rope(void* x, int64_t T, int64_t ld, int32_t n_heads, int32_t hd, int32_t S, const float* cs,
+                  int32_t inverse, void* stream) {
+  if (!x || !cs || S <= 0) return MT_ERR_ARG;
+  return cu_status(mt::rope((bf16*)x, T, ld, n_heads, hd, S, cs, inverse, (cudaStream_t)stream));
+}
+
+mt_status mt_attention_fwd(const void* qkv, int32_t n_seq, int32_t S, int32_t nh, int32_t nkv, int32_t hd, void* o,
+                           float* lse, void* stream) {
+  if (!qkv || !o || !lse || nkv <= 0) return MT_ERR_ARG;
+  return cu_status(mt::attention_fwd((const bf16*)qkv, n_seq, S, nh, nkv, hd, (bf16*)o, lse, (cudaStream_t)stream));
+}
+
+size_t mt_attention_bwd_scratch_bytes(int32_t n_seq, int32_t S, int32_t nh, int32_t hd) {
+  const size_t T = (size_t)n_seq * S;
+  return (size_t)up((int64_t)(T * nh * 4), 256) + T * nh * hd * 4;
+}
+
+mt_status mt_attention_bwd(const void* qkv, const void* o, const float* lse, const void* dout, int32_t n_seq,
+                           int32_t S, int32_t nh, int32_t nkv, int32_t hd, void* dqkv, void* scratch,
+                           size_t scratch_bytes, void* stream) {
+  if (!qkv || !o || !lse || !dout || !dqkv || !scratch || nkv <= 0) return MT_ERR_ARG;
+  if (scratch_bytes < mt_attention_bwd_scratch_bytes(n_seq, S, nh, hd)) return MT_ERR_ARG;
+  const size_t T = (size_t)n_seq * S;
+  float* delta = (float*)scratch;
+  float* dq = (float*)((uint8_t*)scratch + up((int64_t)(T * nh * 4), 256));
+  return cu_status(mt::attention_bwd((const bf16*)qkv, (const bf16*)o, lse, (const bf16*)dout, n_seq, S, nh, nkv, hd,
+                                     (bf16*)dqkv, delta, dq, (cudaStream_t)stream));
+}
+
+mt_status mt_swiglu_fwd(const void* gu, int64_t T, int32_t F, void* h, void* stream) {
+  if (!gu || !h) return MT_ERR_ARG;
+  return cu_status(mt::swiglu_fwd((const bf16*)gu, T, F, (bf16*)h, (cudaStream_t)stream));
+}
+
+mt_status mt_swiglu_bwd(const void* gu, const void* dh, int64_t T, int32_t F, void* dgu, void* stream) {
+  if (!gu || !dh || !dgu) return MT_ERR_ARG;
+  return cu_status(mt::swiglu_bwd((const bf16*)gu, (const bf16*)dh, T, F, (bf16*)dgu, (cudaStream_t)stream));
+}
+
+mt_status mt_embed_fwd(const int32_t* tok, const void* E, int64_t T, int32_t H, int32_t V, void* X, void* stream) {
+  if (!tok || !E || !X) return MT_ERR_ARG;
+  return cu_status(mt::embed_fwd(tok, (const bf16*)E, T, H, V, (bf16*)X, (cudaStream_t)stream));
+}
+
+mt_status mt_embed_bwd(const int32_t* row_start, const int32_t* rows, const void* dX, int32_t V, int32_t H, void* dE,
+                       void* stream) {
+  if (!row_start || !rows || !dX || !dE) return MT_ERR_ARG;
+  return cu_status(mt::embed_bwd(row_start, rows, (const bf16*)dX, V, H, (bf16*)dE, (cudaStream_t)stream));
+}
+
+mt_status mt_cross_entropy(void* logits, const int32_t* target, int64_t rows, int32_t V, float inv_norm,
+                           float* row_loss, void* stream) {
+  if (!logits || !target || !row_loss) return MT_ERR_ARG;
+  return cu_status(mt::cross_entropy((bf16*)logits, target, rows, V, inv_norm, row_loss, (cudaStream_t)stream));
+}
+
+mt_status mt_kernel_error(int32_t* code, int32_t clear) {
+  if (!code) return MT_ERR_ARG;
+  int c = 0;
+  const mt_status s = cu_status(mt::kernel_error_read(&c, clear));
+  *code = c;
+  return s;
+}
+
+}  // extern "C"

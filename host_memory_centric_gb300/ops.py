@@ -1,0 +1,121 @@
+"""Per-op device entry points of libmt on torch tensors (marshalling only).
+
+Each function passes device pointers and the current torch stream to the
+matching ``mt_*`` call of ``include/mt.h``; all arithmetic runs in the
+library's sm_103a kernels.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+
+
+def _L():
+    from . import lib
+    return lib()
+
+
+def _chk(s):
+    from . import MtError
+    if s != 0:
+        raise MtError(s, "device op failed")
+
+
+def _stream():
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _p(t):
+    return None if t is None else t.data_ptr()
+
+
+def gemm(A, B, M, N, K, *, a_mn=False, b_mn=False, lda=None, ldb=None, D=None, ldd=None, R=None, ldr=None,
+         Dacc=None, ldacc=None, acc_mode=0):
+    lda = lda if lda is not None else (M if a_mn else K)
+    ldb = ldb if ldb is not None else (N if b_mn else K)
+    ldd = ldd if ldd is not None else N
+    ldr = ldr if ldr is not None else N
+    ldacc = ldacc if ldacc is not None else N
+    _chk(_L().mt_gemm(_p(A), lda, int(a_mn), _p(B), ldb, int(b_mn), M, N, K, _p(D), ldd, _p(R), ldr,
+                      _p(Dacc), ldacc, acc_mode, _stream()))
+
+
+def rmsnorm_fwd(x, gamma, eps, y, rstd):
+    T, H = x.shape
+    _chk(_L().mt_rmsnorm_fwd(_p(x), _p(gamma), T, H, eps, _p(y), _p(rstd), _stream()))
+
+
+def rmsnorm_bwd_scratch_bytes(T, H):
+    return int(_L().mt_rmsnorm_bwd_scratch_bytes(T, H))
+
+
+def rmsnorm_bwd(dy, x, gamma, rstd, dres, dx, dgamma, scratch):
+    T, H = x.shape
+    _chk(_L().mt_rmsnorm_bwd(_p(dy), _p(x), _p(gamma), _p(rstd), _p(dres), T, H, _p(dx), _p(dgamma),
+                             _p(scratch), scratch.numel() * scratch.element_size(), _stream()))
+
+
+def rope_table(S, hd, base) -> np.ndarray:
+    out = np.empty(S * hd, dtype=np.float32)
+    _chk(_L().mt_rope_table(S, hd, base, out.ctypes.data_as(C.POINTER(C.c_float))))
+    return out
+
+
+def rope(x, n_heads, hd, S, cs, inverse=False):
+    T, ld = x.shape
+    _chk(_L().mt_rope(_p(x), T, ld, n_heads, hd, S, _p(cs), int(inverse), _stream()))
+
+
+def attention_fwd(qkv, n_seq, S, nh, nkv, hd, o, lse):
+    _chk(_L().mt_attention_fwd(_p(qkv), n_seq, S, nh, nkv, hd, _p(o), _p(lse), _stream()))
+
+
+def attention_bwd_scratch_bytes(n_seq, S, nh, hd):
+    return int(_L().mt_attention_bwd_scratch_bytes(n_seq, S, nh, hd))
+
+
+def attention_bwd(qkv, o, lse, dout, n_seq, S, nh, nkv, hd, dqkv, scratch):
+    _chk(_L().mt_attention_bwd(_p(qkv), _p(o), _p(lse), _p(dout), n_seq, S, nh, nkv, hd, _p(dqkv), _p(scratch),
+                               scratch.numel() * scratch.element_size(), _stream()))
+
+
+def swiglu_fwd(gu, h):
+    T, F2 = gu.shape
+    _chk(_L().mt_swiglu_fwd(_p(gu), T, F2 // 2, _p(h), _stream()))
+
+
+def swiglu_bwd(gu, dh, dgu):
+    T, F2 = gu.shape
+    _chk(_L().mt_swiglu_bwd(_p(gu), _p(dh), T, F2 // 2, _p(dgu), _stream()))
+
+
+def embed_fwd(tok, E, X):
+    V, H = E.shape
+    _chk(_L().mt_embed_fwd(_p(tok), _p(E), tok.numel(), H, V, _p(X), _stream()))
+
+
+def token_csr(tok: np.ndarray, V: int):
+    tok = np.ascontiguousarray(tok, dtype=np.int32).ravel()
+    rs = np.empty(V + 1, dtype=np.int32)
+    rows = np.empty(tok.size, dtype=np.int32)
+    P = C.POINTER(C.c_int32)
+    _chk(_L().mt_token_csr(tok.ctypes.data_as(P), tok.size, V, rs.ctypes.data_as(P), rows.ctypes.data_as(P)))
+    return rs, rows
+
+
+def embed_bwd(row_start, rows, dX, V, dE):
+    H = dX.shape[1]
+    _chk(_L().mt_embed_bwd(_p(row_start), _p(rows), _p(dX), V, H, _p(dE), _stream()))
+
+
+def cross_entropy(logits, target, inv_norm, row_loss):
+    rows, V = logits.shape
+    _chk(_L().mt_cross_entropy(_p(logits), _p(target), rows, V, inv_norm, _p(row_loss), _stream()))
+
+
+def kernel_error(clear=True) -> int:
+    c = C.c_int32()
+    _chk(_L().mt_kernel_error(C.byref(c), int(clear)))
+    return int(c.value)

@@ -1,0 +1,265 @@
+/*
+ * mt.h -- C ABI of libmt: the layer-streamed, host-memory-centric training step
+ * of a decoder-only transformer on one GPU (GB300, sm_103a).
+ *
+ * The method (MegaTrain, as described on the pages cited below) keeps every
+ * parameter, gradient, FP32 master weight and Adam moment in host RAM as one
+ * contiguous block per layer, and treats the GPU as a transient compute
+ * engine: each block's BF16 weights stream host-to-device into one of two
+ * ping-pong device buffers, are bound to a weight-less layer template, run
+ * forward (and later recompute + backward), and the block's BF16 gradients
+ * stream device-to-host into one of K pinned slabs, where host threads apply
+ * mixed-precision Adam.  Three CUDA streams (compute, weight, gradient) are
+ * ordered only by three events: Weights-Ready, Backward-Done, Buffer-Free.
+ *
+ * Sources, cited by page and section:
+ *   [Review]  dimensionstp.github.io, "MegaTrain: Full Precision Training of
+ *             100B+ Parameter Large Language Models on a Single GPU Review",
+ *             3-2 Module breakdown (1)-(6)
+ *   [Hotdry]  blog.hotdry.top (2026-04-09), sections on the host memory layout
+ *             (flat tensors, pinned staging), the three CUDA streams and double
+ *             buffering, and the event-driven synchronisation protocol
+ *   [Lilting] lilting.ch, "MegaTrainはシングルGPUで120BパラメータLLMをフル精度
+ *             訓練する", sections on the memory breakdown, the pipelined double
+ *             buffering and the stateless layer templates
+ *   [Peter]   peter-blog.pages.dev, MegaTrain translation, 技術細節 (CUDA stream
+ *             management, static prefetch schedule)
+ *
+ * Conventions for every call:
+ *   - returns an mt_status; no exception crosses the ABI;
+ *   - a CUDA error maps to MT_ERR_CUDA with cudaGetErrorString text available
+ *     from mt_last_error(); any timeout or CUDA error latches the model into an
+ *     error state in which every call except mt_last_error / mt_destroy
+ *     returns MT_ERR_STATE;
+ *   - one driver thread per model; the library's host workers are internal;
+ *   - "device pointer" arguments are CUDA device addresses the caller owns;
+ *     "stream" arguments are cudaStream_t values passed as void*.
+ */
+#ifndef MT_H
+#define MT_H
+#include <stddef.h>
+#include <stdint.h>
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MT_OK = 0,
+  MT_ERR_ARG = -1,       /* bad argument (shape, alignment, index, null)      */
+  MT_ERR_STATE = -2,     /* call out of order, or model latched in error       */
+  MT_ERR_HOST_OOM = -3,  /* host (pageable or pinned) allocation failed        */
+  MT_ERR_CUDA = -4,      /* a CUDA runtime call or kernel launch failed        */
+  MT_ERR_TIMEOUT = -5,   /* a bounded host wait (event, slab, Adam) expired    */
+  MT_ERR_INTERNAL = -6,  /* a host worker failed                               */
+  MT_ERR_DEVICE_OOM = -7 /* the caller's device region is too small            */
+} mt_status;
+
+#define MT_MAX_TENSORS 8
+
+/* Opaque model handle, owned by the library (mt_destroy frees it). */
+typedef struct mt_model mt_model;
+
+/* Region of a flat block ([Hotdry] host memory layout: one contiguous block
+ * per layer holding BF16 weights, BF16 gradients and FP32 Adam state). */
+enum { MT_REGION_W = 0, MT_REGION_G = 1, MT_REGION_MASTER = 2, MT_REGION_M = 3, MT_REGION_V = 4 };
+
+/* Model, step and runtime configuration.  Plain data, copied by
+ * mt_init_model.  Tokens per step T = micro_batches * batch * seq. */
+typedef struct {
+  int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
+  float rope_base, rms_eps, init_std;          /* e.g. 1e4 or 1e6, 1e-6, 0.02 */
+  int32_t batch, seq, micro_batches;
+  int32_t ckpt_interval;   /* layers between kept activations; must be 1    */
+  int32_t ckpt_on_host;    /* 1: layer-boundary activations in pinned host RAM
+                              (device footprint independent of depth)      */
+  int32_t n_grad_slabs;    /* K pinned gradient slabs ([Hotdry]: default 12) */
+  int32_t n_host_threads;  /* host worker threads; 0 = online cores         */
+  float lr, beta1, beta2, adam_eps, weight_decay; /* 1e-3, .9, .999, 1e-8, 0 */
+  uint64_t seed;           /* weight initialisation seed                     */
+  uint32_t timeout_ms;     /* limit of every bounded host wait               */
+  int32_t pin_store;       /* 0: just-in-time pack of pageable W into two
+                              pinned staging buffers ([Review] 3-2 (4));
+                              1: register the whole store, copy directly    */
+  int32_t head_chunk;      /* tokens per LM-head chunk; 0 = automatic        */
+  int32_t log_protocol;    /* 1: keep the enqueue log (mt_protocol_log)      */
+} mt_config;
+
+typedef struct { void* base; size_t bytes; } mt_dev_region;          /* caller-owned device memory  */
+typedef struct { void* compute; void* weight; void* grad; } mt_streams; /* cudaStream_t, caller-owned */
+
+/* Bind result: a weight-less template's input slots filled with views into a
+ * streamed buffer ([Review] 3-2 (5); [Lilting] Stateless Layer Templates). */
+typedef struct {
+  const void* w[MT_MAX_TENSORS]; /* device address of each tensor's BF16 weights   */
+  void* g[MT_MAX_TENSORS];       /* device address of each tensor's BF16 gradient  */
+  int32_t n_tensors, block, buf;
+} mt_layer_view;
+
+typedef struct {
+  int64_t steps_done;
+  int64_t h2d_bytes, d2h_bytes;       /* cumulative copies issued by the library  */
+  int64_t device_bytes_used;          /* bytes of the caller's region carved      */
+  double last_step_ms;                /* host wall time of the last mt_train_step */
+  double adam_ms_total, pack_ms_total;/* host time in Adam workers / JIT packing  */
+  int64_t host_store_bytes, pinned_bytes;
+} mt_stats;
+
+/* ------------------------------------------------------------------ model */
+/* Defaults above for every runtime field; shape fields are zeroed. */
+mt_status mt_default_config(mt_config* cfg);
+/* Device bytes mt_init_model will carve from the caller's region. */
+mt_status mt_query_device_bytes(const mt_config* cfg, size_t* bytes_needed);
+/* Allocates the host flat store (library-owned), fills it from the seeded
+ * generator (FP32 master N(0, init_std) for matrices, 1 for RMSNorm gains,
+ * W = bf16_rne(master), m = v = 0), allocates pinned staging, slabs and the
+ * checkpoint store, creates the events and starts the host workers.  The
+ * device region and the streams must outlive the model. */
+mt_status mt_init_model(const mt_config* cfg, mt_dev_region dev, mt_streams s, mt_model** model_out);
+/* Copies the step's token ids (host, [micro][batch][seq] int32 in [0, V))
+ * and uploads them on the compute stream. */
+mt_status mt_set_tokens(mt_model* model, const int32_t* tok);
+
+/* The pages' primitives ([Hotdry] StreamIn / Bind / gradient export; [Review]
+ * 3-2 (2)-(6)).  Blocks: 0 = embedding, 1..L = decoder layers, L+1 = head
+ * (final RMSNorm + LM head).  A step visits blocks 0..L+1 forward (the head
+ * visit runs its forward, the loss and its backward) and then L..0 backward;
+ * the calls below must follow that order (MT_ERR_STATE otherwise). */
+/* Weight stream: waits Buffer-Free[buf], copies block's BF16 W (packed just in
+ * time through pinned staging unless pin_store) into device buffer buf and,
+ * for a decoder block's backward visit with host checkpoints, the block's
+ * input activation; records Weights-Ready[buf].  Asynchronous. */
+mt_status mt_stream_in(mt_model* model, int32_t block, int32_t buf);
+/* Compute stream waits Weights-Ready[buf]; fills *view. */
+mt_status mt_bind(mt_model* model, int32_t block, int32_t buf, mt_layer_view* view);
+/* Forward visit of view->block over all micro-batches of the step (they are
+ * concatenated along the token axis).  Records Buffer-Free (or, for the head,
+ * Backward-Done).  Asynchronous. */
+mt_status mt_step_forward(mt_model* model, const mt_layer_view* view);
+/* Backward visit: recompute the block forward from its checkpointed input,
+ * then the backward; weight gradients are written (BF16, round to nearest
+ * even) straight into the buffer's gradient region at the flat layout
+ * offsets; records Backward-Done.  Asynchronous. */
+mt_status mt_step_backward(mt_model* model, const mt_layer_view* view);
+/* Gradient stream: waits Backward-Done[buf], takes slab (export count mod K,
+ * waiting on the host, bounded, until its previous Adam finished), copies the
+ * gradient region into it, records Buffer-Free[buf] and the slab's event. */
+mt_status mt_stream_out(mt_model* model, int32_t block, int32_t buf, int32_t* slab);
+/* Queues block's host Adam: a worker waits (bounded) for the slab's event,
+ * copies the slab into the block's G region, runs Adam (t = adam_step >= 1)
+ * on master / m / v, rewrites W = bf16_rne(master) and releases the slab. */
+mt_status mt_adam_host(mt_model* model, int32_t block, int32_t slab, int32_t adam_step);
+/* One whole step (0-based index `step`, which must equal the number of steps
+ * done) following the static schedule; *loss (if not null) receives the step
+ * loss once its value has reached the host.  Returns after enqueuing the
+ * last backward visit; Adam of the last blocks may still run. */
+mt_status mt_train_step(mt_model* model, int32_t step, float* loss);
+/* Waits (bounded) for every queued copy, kernel and Adam job. */
+mt_status mt_sync(mt_model* model);
+/* Copies `bytes` of a block's region (MT_REGION_*) out of / into the host
+ * store (after mt_sync).  bytes must not exceed the region. */
+mt_status mt_read_host(mt_model* model, int32_t block, int32_t region, void* dst, size_t bytes);
+mt_status mt_write_host(mt_model* model, int32_t block, int32_t region, const void* src, size_t bytes);
+mt_status mt_get_stats(const mt_model* model, mt_stats* out);
+/* The enqueue log (lines "step stream op a b"); returns its length, or
+ * -(needed) when cap is too small. */
+int64_t mt_protocol_log(const mt_model* model, char* buf, int64_t cap);
+const char* mt_last_error(const mt_model* model);
+void mt_destroy(mt_model* model);
+
+/* ------------------------------------------------------------------ host-only */
+/* None of these touches a GPU. */
+/* Layout of block j, in the format: [0] n_tensors [1] n_real [2] n_pad,
+ * [3..7] byte offsets of the W, G, master, m, v regions, [8] block bytes,
+ * [9] offset in the store, then (element offset, rows, cols) per tensor.
+ * Returns the count written or -1. */
+int64_t mt_layout_block(const mt_config* cfg, int32_t j, int64_t* out, int64_t cap);
+int64_t mt_param_count(const mt_config* cfg);
+int64_t mt_store_bytes(const mt_config* cfg);
+/* The library's initialiser for block j (n_pad FP32 master values). */
+mt_status mt_host_init_block(const mt_config* cfg, int32_t j, float* master);
+/* The library's host Adam over n elements on n_threads threads. */
+mt_status mt_host_adam(int64_t n, const uint16_t* g_bf16, float* master, float* m, float* v,
+                       uint16_t* w_bf16, int32_t adam_step, float lr, float beta1, float beta2,
+                       float eps, float weight_decay, int32_t n_threads);
+/* Runs the step scheduler without any device or host work and returns the
+ * enqueue log of n_steps steps (as mt_protocol_log). */
+int64_t mt_plan_protocol(const mt_config* cfg, int32_t n_steps, char* buf, int64_t cap);
+/* Static prefetch schedule ([Peter] 記憶體預取策略: prefetch timing from each
+ * layer's bytes, the link bandwidth and its compute time).  Per visit v of a
+ * step: b[v] H2D bytes, d[v] exported gradient bytes, c[v] compute seconds,
+ * a[v] Adam seconds.  stall[v] = predicted wait before visit v computes;
+ * returns the slab count needed, or -1. */
+int32_t mt_schedule(int32_t n_visits, const double* b, const double* d, const double* c,
+                    const double* a, double bw_h2d, double bw_d2h, double* stall);
+/* Per-vocabulary-row lists of token rows (CSR) used by the embedding
+ * gradient: row_start[V+1], rows[T]. */
+mt_status mt_token_csr(const int32_t* tok, int64_t T, int32_t V, int32_t* row_start, int32_t* rows);
+/* RoPE cos/sin table [S][hd/2][2] in FP32 (angles in double). */
+mt_status mt_rope_table(int32_t S, int32_t hd, double base, float* out);
+
+/* ------------------------------------------------------------------ per-op (device) */
+/* The block math as individual device calls, for tests and other callers.
+ * All pointers are device addresses, row-major, 16-byte aligned; every "ld"
+ * is a row stride in elements and a multiple of 8. */
+
+/* D[m,n] = sum_k A(m,k) B(n,k) on tcgen05 tensor cores, FP32 accumulation.
+ * A is [M][K] (a_mn = 0) or [K][M] (a_mn = 1); B is [N][K] or [K][N].
+ * acc_mode 0: none; 1: Dacc = acc; 2: Dacc += acc (FP32, then used below);
+ * R (optional) is added; D (optional) receives bf16_rne.  BF16 operands. */
+mt_status mt_gemm(const void* A, int64_t lda, int32_t a_mn, const void* B, int64_t ldb,
+                  int32_t b_mn, int32_t M, int32_t N, int32_t K, void* D, int64_t ldd,
+                  const void* R, int64_t ldr, float* Dacc, int64_t ldacc, int32_t acc_mode,
+                  void* stream);
+/* RMSNorm forward: y = x * rstd * gamma, rstd = (mean(x^2)+eps)^-1/2 per row. */
+mt_status mt_rmsnorm_fwd(const void* x, const void* gamma, int64_t T, int32_t H, float eps,
+                         void* y, float* rstd, void* stream);
+/* RMSNorm backward: dx = d/dx + dres (dres optional), dgamma = sum over rows.
+ * scratch: device memory of mt_rmsnorm_bwd_scratch_bytes(T, H) bytes. */
+mt_status mt_rmsnorm_bwd(const void* dy, const void* x, const void* gamma, const float* rstd,
+                         const void* dres, int64_t T, int32_t H, void* dx, void* dgamma,
+                         void* scratch, size_t scratch_bytes, void* stream);
+size_t mt_rmsnorm_bwd_scratch_bytes(int64_t T, int32_t H);
+/* Rotate-half RoPE of the first n_heads heads of each row of x ([T][ld]),
+ * position = row mod S; cs from mt_rope_table (device copy). */
+mt_status mt_rope(void* x, int64_t T, int64_t ld, int32_t n_heads, int32_t hd, int32_t S,
+                  const float* cs, int32_t inverse, void* stream);
+/* Causal GQA attention; qkv rows [q (nh hd) | k (nkv hd) | v (nkv hd)];
+ * o [T][nh hd]; lse [nh][T] FP32 (natural log).  hd in {64, 128}. */
+mt_status mt_attention_fwd(const void* qkv, int32_t n_seq, int32_t S, int32_t nh, int32_t nkv,
+                           int32_t hd, void* o, float* lse, void* stream);
+/* Backward into dqkv (same layout as qkv); scratch of
+ * mt_attention_bwd_scratch_bytes bytes. */
+mt_status mt_attention_bwd(const void* qkv, const void* o, const float* lse, const void* dout,
+                           int32_t n_seq, int32_t S, int32_t nh, int32_t nkv, int32_t hd,
+                           void* dqkv, void* scratch, size_t scratch_bytes, void* stream);
+size_t mt_attention_bwd_scratch_bytes(int32_t n_seq, int32_t S, int32_t nh, int32_t hd);
+/* SwiGLU: gu rows [g (F) | u (F)], h = silu(g) * u; backward into dgu. */
+mt_status mt_swiglu_fwd(const void* gu, int64_t T, int32_t F, void* h, void* stream);
+mt_status mt_swiglu_bwd(const void* gu, const void* dh, int64_t T, int32_t F, void* dgu,
+                        void* stream);
+/* Embedding gather X[t] = E[tok[t]] and dense gradient dE (all V rows) from
+ * the token CSR of mt_token_csr. */
+mt_status mt_embed_fwd(const int32_t* tok, const void* E, int64_t T, int32_t H, int32_t V,
+                       void* X, void* stream);
+mt_status mt_embed_bwd(const int32_t* row_start, const int32_t* rows, const void* dX, int32_t V,
+                       int32_t H, void* dE, void* stream);
+/* Cross-entropy rows: logits [rows][V] BF16 are overwritten with
+ * (softmax - onehot(target)) * inv_norm; target < 0 marks a row with no
+ * target (zero gradient, zero loss); row_loss[r] = lse - logit[target]. */
+mt_status mt_cross_entropy(void* logits, const int32_t* target, int64_t rows, int32_t V,
+                           float inv_norm, float* row_loss, void* stream);
+/* Per-launch timing of the library's own kernels: CUDA events around each
+ * launch on the compute stream.  kind 0 = GEMMs, 1 = attention forward,
+ * 2 = attention backward, 3 = all other kernels.  mt_timing(model, 1) resets
+ * and starts, mt_timing(model, 0) stops (after draining); read after
+ * mt_sync.  flops / bytes are the algorithmic work of the timed launches. */
+mt_status mt_timing(mt_model* model, int32_t enable);
+mt_status mt_timing_read(mt_model* model, int32_t kind, int64_t* launches, double* ms,
+                         double* flops, double* bytes);
+/* Error word of the kernels' bounded waits (0 = none); clear != 0 resets it. */
+mt_status mt_kernel_error(int32_t* code, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

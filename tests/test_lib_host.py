@@ -1,0 +1,173 @@
+"""CPU tests of libmt's host side against the oracle (no GPU needed).
+
+The library and the oracle are independent implementations; here they must
+agree bit-exactly on the flat layout, the seeded initial weights, the event
+protocol and the schedule, and to FP32 rounding on host Adam.
+"""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import host_memory_centric_gb300 as mt
+from host_memory_centric_gb300 import configs
+from tests import protocol_check
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+F32_002 = float(np.float32(0.02))  # mt_config carries init_std as float
+
+
+def shape_for_oracle(c):
+    return dict(c, init_std=F32_002, rope_base=float(np.float32(c["rope_base"])))
+
+
+def test_library_exports_every_declared_symbol():
+    hdr = open(os.path.join(ROOT, "include", "mt.h")).read()
+    names = sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(mt_\w+)\s*\(", hdr, flags=re.M)))
+    assert len(names) > 40
+    L = mt.lib()
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+@pytest.mark.parametrize("name", list(configs.CONFIGS))
+def test_layout_bit_exact(orc, name):
+    c = configs.get(name)
+    assert mt.layout(mt.make_config(c)) == orc.layout(c)
+    cfg = mt.make_config(c)
+    assert mt.lib().mt_param_count(C.byref(cfg)) == orc.param_count(c)
+    assert mt.lib().mt_store_bytes(C.byref(cfg)) == orc.store_bytes(c)
+
+
+def _lib_init(c, j):
+    cfg = mt.make_config(c, seed=77)
+    n = mt.layout(cfg)[j]["n_pad"]
+    out = np.empty(n, dtype=np.float32)
+    assert mt.lib().mt_host_init_block(C.byref(cfg), j, out.ctypes.data_as(C.POINTER(C.c_float))) == 0
+    return out
+
+
+@pytest.mark.parametrize("j", [0, 1, 2, 3])
+def test_init_bit_exact_tiny(orc, j):
+    c = configs.get("tiny")
+    a = _lib_init(c, j)
+    b = orc.init_block(shape_for_oracle(c), 77, j)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_init_bit_exact_full_width_decoder_block(orc):
+    c = configs.get("1.2b", n_layers=1)
+    a = _lib_init(c, 1)
+    b = orc.init_block(shape_for_oracle(c), 77, 1)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_host_adam_matches_oracle(orc):
+    rng = np.random.default_rng(0)
+    n = 300_000
+    g = orc.bf16_rne_fast((rng.standard_normal(n) * 1e-3).astype(np.float32))
+    th = (0.02 * rng.standard_normal(n)).astype(np.float32)
+    m = (1e-4 * rng.standard_normal(n)).astype(np.float32)
+    v = (1e-7 * rng.random(n)).astype(np.float32)
+    a = [x.copy() for x in (th, m, v)]
+    b = [x.copy() for x in (th, m, v)]
+    wa = np.empty(n, np.uint16)
+    P = lambda x, t: x.ctypes.data_as(C.POINTER(t))
+    for t in (1, 2, 7):
+        assert mt.lib().mt_host_adam(n, P(g, C.c_uint16), P(a[0], C.c_float), P(a[1], C.c_float),
+                                     P(a[2], C.c_float), P(wa, C.c_uint16), t, 1e-3, 0.9, 0.999, 1e-8, 0.0,
+                                     4) == 0
+        wb = orc.adam(g, b[0], b[1], b[2], t)
+    for x, y in zip(a, b):
+        assert np.linalg.norm(x - y) <= 1e-6 * np.linalg.norm(y)
+    assert np.mean(wa == wb) > 0.999
+
+
+def _plan(c, steps, **rt):
+    cfg = mt.make_config(c, **rt)
+    need = -mt.lib().mt_plan_protocol(C.byref(cfg), steps, None, 0)
+    buf = C.create_string_buffer(int(need) + 1)
+    n = mt.lib().mt_plan_protocol(C.byref(cfg), steps, buf, need + 1)
+    assert n > 0
+    return buf.value.decode().splitlines()
+
+
+@pytest.mark.parametrize("ckpt", [0, 1])
+@pytest.mark.parametrize("pin", [0, 1])
+@pytest.mark.parametrize("slabs", [1, 3, 12])
+def test_protocol_plan_bit_exact(orc, ckpt, pin, slabs):
+    c = configs.get("tiny", n_layers=3)
+    lines = _plan(c, 3, ckpt_on_host=ckpt, pin_store=pin, n_grad_slabs=slabs)
+    assert lines == orc.protocol(c, 3, slabs, bool(ckpt), not pin)
+    protocol_check.check(lines)
+
+
+@pytest.mark.parametrize("name", ["1.2b", "7.6b", "14.7b"])
+def test_protocol_plan_full_depth(orc, name):
+    c = configs.get(name)
+    assert _plan(c, 2) == orc.protocol(c, 2, 12, True, True)
+
+
+def test_schedule_matches_oracle(orc):
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        n = int(rng.integers(3, 60))
+        b, d, cc, a = (rng.random(n) * s for s in (1e9, 1e9, 0.02, 0.05))
+        d[rng.random(n) < 0.5] = 0.0
+        st_o, k_o = orc.schedule(b, d, cc, a, 2e11, 1.9e11)
+        st_l = np.empty(n)
+        P = lambda x: np.ascontiguousarray(x, np.float64).ctypes.data_as(C.POINTER(C.c_double))
+        k_l = mt.lib().mt_schedule(n, P(b), P(d), P(cc), P(a), 2e11, 1.9e11, P(st_l))
+        assert k_l == k_o
+        assert np.allclose(st_l, st_o, rtol=1e-12, atol=1e-15)
+
+
+def test_token_csr():
+    rng = np.random.default_rng(4)
+    tok = rng.integers(0, 50, 1000).astype(np.int32)
+    rs, rows = mt.ops.token_csr(tok, 50)
+    assert rs[0] == 0 and rs[-1] == tok.size
+    for v in range(50):
+        assert list(rows[rs[v]:rs[v + 1]]) == list(np.nonzero(tok == v)[0])
+
+
+def test_rope_table():
+    t = mt.ops.rope_table(37, 16, 1e4).reshape(37, 8, 2)
+    p = np.arange(37)[:, None]
+    ang = p * 1e4 ** (-2 * np.arange(8) / 16.0)
+    assert np.allclose(t[..., 0], np.cos(ang), atol=1e-7) and np.allclose(t[..., 1], np.sin(ang), atol=1e-7)
+
+
+def test_bad_arguments_rejected_without_gpu():
+    L = mt.lib()
+    cfg = mt.make_config(configs.get("tiny"))
+    nbytes = C.c_size_t()
+    assert L.mt_query_device_bytes(C.byref(cfg), C.byref(nbytes)) == 0 and nbytes.value > 0
+    bad = mt.make_config(configs.get("tiny"), n_kv_heads=3)
+    assert L.mt_query_device_bytes(C.byref(bad), C.byref(nbytes)) == -1
+    bad = mt.make_config(configs.get("tiny"), ckpt_interval=2)
+    assert L.mt_query_device_bytes(C.byref(bad), C.byref(nbytes)) == -1
+    h = C.c_void_p()
+    assert L.mt_init_model(C.byref(cfg), mt.DevRegion(None, 0), mt.Streams(None, None, None), C.byref(h)) == -1
+    assert L.mt_train_step(None, 0, None) == -1
+
+
+def test_device_footprint_independent_of_depth():
+    """With host checkpoints the carved device region does not grow with depth."""
+    L = mt.lib()
+    sizes = []
+    for depth in (12, 24, 48):
+        cfg = mt.make_config(configs.get("14.7b", n_layers=depth))
+        n = C.c_size_t()
+        assert L.mt_query_device_bytes(C.byref(cfg), C.byref(n)) == 0
+        sizes.append(n.value)
+    assert sizes[0] == sizes[1] == sizes[2]
+    dev = []
+    for depth in (12, 24):
+        cfg = mt.make_config(configs.get("14.7b", n_layers=depth), ckpt_on_host=0)
+        n = C.c_size_t()
+        L.mt_query_device_bytes(C.byref(cfg), C.byref(n))
+        dev.append(n.value)
+    assert dev[1] > dev[0]
