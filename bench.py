@@ -1,0 +1,377 @@
+"""Benchmark of the layer-streamed training step on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  A step is one mt_train_step: every block
+streamed in, run forward, recomputed and run backward, its gradients streamed
+out and Adam applied on the host.  `value` is tokens/s with the step's tokens
+already resident on the device; `e2e` adds, every step, the upload of that
+step's tokens from pinned host memory and the read-back of the loss.  Host
+state (weights, gradients, master, moments) lives in host RAM by design, so
+every step streams it in both cases.
+
+Multi-GPU: one independent replica per GPU (the path has no exchange step),
+weak scaling; value = all ranks' tokens / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "training tokens/sec (1 GB300, host-resident state); % of step roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "fallback": True}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["fallback"] = False
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+def model_numbers(c):
+    """Parameter count P, tensor FLOPs the method executes per step (forward,
+    block recompute, backward; causal attention; head once), and the pages'
+    6NT + 12 L B S^2 H convention."""
+    L, H, nh, nkv, hd, F, V = (c[k] for k in ("n_layers", "hidden", "n_heads", "n_kv_heads", "head_dim", "ffn",
+                                              "vocab"))
+    B, S, M = c["batch"], c["seq"], c["micro"]
+    t = B * S
+    P_mm = H * (nh + 2 * nkv) * hd + nh * hd * H + 3 * H * F
+    P = L * (P_mm + 2 * H) + 2 * V * H + H
+    F_exec = M * (L * (8 * t * P_mm + 9 * B * nh * hd * S * S) + 6 * t * H * V)
+    F_pages = 6 * P * M * t + 12 * L * B * M * S * S * H
+    return P, F_exec, F_pages
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm = [float(r[1]) for r in self.rows if len(r) > 8 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) > 8 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in self.rows if len(r) > 8 for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def link_bandwidth(torch, nbytes=1 << 30, reps=10):
+    """Pinned cudaMemcpyAsync of 1 GiB per direction (best of reps) and both at once."""
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dev2 = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h2 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    out = {}
+    for name in ("h2d", "d2h", "both"):
+        best = 1e9
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            if name in ("h2d", "both"):
+                with torch.cuda.stream(s1):
+                    dev.copy_(h, non_blocking=True)
+            if name in ("d2h", "both"):
+                with torch.cuda.stream(s2):
+                    h2.copy_(dev2, non_blocking=True)
+            torch.cuda.current_stream().wait_stream(s1)
+            torch.cuda.current_stream().wait_stream(s2)
+            b.record()
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b) / 1e3)
+        out[name] = (2 if name == "both" else 1) * nbytes / best
+    del dev, dev2, h, h2
+    return out
+
+
+def cpu_sample(cfg_name, budget_s=20.0):
+    """Times the oracle (single-threaded) on a depth-1, full-width slice of
+    the workload with one short sequence and applies its FLOP rate to the
+    full workload's FLOPs (an extrapolation, labelled as such)."""
+    import oracle
+    from host_memory_centric_gb300 import configs, inputs
+    c = configs.get(cfg_name)
+    seq = 32 if c["vocab"] > 10000 else min(c["seq"], 128)
+    s = dict(c, n_layers=1, batch=1, micro=1, seq=seq, init_std=float(np.float32(0.02)))
+    oracle.build()
+    W = []
+    for j in range(3):
+        W.append(oracle.init_block(s, 1234, j))
+    tok = inputs.tokens(1234, 0, 1, 1, seq, c["vocab"])
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.step_fwd_bwd(s, W, tok, np.float32)
+        n += 1
+        if time.perf_counter() - t0 > budget_s / 2 or n >= 3:
+            break
+    dt = (time.perf_counter() - t0) / n
+    _, F_sample, _ = model_numbers(dict(s, micro=1))
+    _, F_full, _ = model_numbers(c)
+    T_full = c["micro"] * c["batch"] * c["seq"]
+    flops_rate = F_sample / dt
+    tok_s = flops_rate * T_full / F_full
+    return {"value": tok_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"oracle fwd+bwd of a 1-layer, full-width slice, 1 x {seq} tokens, {n} run(s) of "
+                      f"{dt:.2f} s; its FLOP rate ({flops_rate / 1e9:.2f} GFLOP/s) applied to the full "
+                      f"workload's {F_full / 1e15:.4f} PFLOP per step (extrapolated)",
+            "seconds": dt * n}
+
+
+def workload_desc(name, c):
+    return (f"{name}-shaped decoder: {c['n_layers']} layers, hidden {c['hidden']}, {c['n_heads']}x{c['head_dim']} "
+            f"heads ({c['n_kv_heads']} KV), FFN {c['ffn']}, vocab {c['vocab']}, batch {c['batch']} x seq "
+            f"{c['seq']} x {c['micro']} micro-batches; host-resident BF16/FP32 state, host Adam")
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from host_memory_centric_gb300 import configs
+    c = configs.get(args.config)
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state
+    vals = []
+    t0 = time.time()
+    per_step = max(5.0, 60.0 / max(1, args.steps))
+    for _ in range(args.steps):
+        r = cpu_sample(args.config, budget_s=per_step)
+        vals.append(r["value"])
+    v = statistics.median(vals)
+    T = c["micro"] * c["batch"] * c["seq"]
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * T / v, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": workload_desc(args.config, c), "model": args.config,
+                       "global_batch": c["batch"] * c["micro"], "seq_len": c["seq"], "parallelism": "none (CPU)"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": r["sample"]},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": time.time() - t0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="1.2b")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--pin-store", type=int, default=1)
+    ap.add_argument("--threads", type=int, default=0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import host_memory_centric_gb300 as mt
+    from host_memory_centric_gb300 import configs, inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    c = configs.get(args.config)
+    T = c["micro"] * c["batch"] * c["seq"]
+    P, F_exec, F_pages = model_numbers(c)
+    pk = peaks()
+    bw = link_bandwidth(torch)
+
+    t_init = time.time()
+    m = mt.Model(c, seed=1234, pin_store=args.pin_store, n_host_threads=args.threads)
+    init_s = time.time() - t_init
+    toks = [inputs.tokens_for(c, s) for s in range(args.warmup + 2 * args.steps + 1)]
+    step = 0
+    for w in range(args.warmup):
+        m.set_tokens(toks[step])
+        m.train_step(step)
+        step += 1
+    m.sync()
+
+    # ---------------- device-resident tokens: the kernel-side number
+    m.set_tokens(toks[step])
+    m.sync()
+    cs = m.streams[0]  # the compute stream the library launches on
+    barrier()
+    m.timing(True)
+    st0 = m.stats()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(cs)
+        w0 = time.perf_counter()
+        losses = []
+        for k in range(args.steps):
+            losses.append(m.train_step(step, want_loss=(k == args.steps - 1)))
+            step += 1
+        m.sync()
+        ev1.record(cs)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - w0
+    barrier()
+    dev_s = ev0.elapsed_time(ev1) / 1e3
+    kern = {name: m.timing_read(i) for i, name in enumerate(("gemm", "attn_fwd", "attn_bwd", "other"))}
+    m.timing(False)
+    st1 = m.stats()
+    t_step = max(dev_s, wall) / args.steps
+    if dist:
+        t = torch.tensor([t_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step = float(t.item())
+    value = world * T / t_step
+
+    # ---------------- end to end: tokens uploaded and loss read back every step
+    e2e = None
+    if not args.no_e2e:
+        barrier()
+        sh0 = m.stats()
+        w0 = time.perf_counter()
+        ev0.record(cs)
+        for k in range(args.steps):
+            m.set_tokens(toks[step])
+            m.train_step(step, want_loss=True)
+            step += 1
+        m.sync()
+        ev1.record(cs)
+        torch.cuda.synchronize()
+        e2e_s = max(time.perf_counter() - w0, ev0.elapsed_time(ev1) / 1e3) / args.steps
+        sh1 = m.stats()
+        if dist:
+            t = torch.tensor([e2e_s], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": world * T / e2e_s, "unit": "tokens/s",
+               "h2d_bytes_per_step": int((sh1["h2d_bytes"] - sh0["h2d_bytes"]) / args.steps),
+               "d2h_bytes_per_step": int((sh1["d2h_bytes"] - sh0["d2h_bytes"]) / args.steps)}
+
+    if rank != 0:
+        m.close()
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    g = kern["gemm"]
+    peak_t = pk.get("bf16_tflops_sustained", 1700.0)
+    achieved = g["flops"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else None
+    roof = {"bound": "tensor", "kernel": "gemm_kernel (tcgen05 BF16 GEMM, all projections)",
+            "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+            "frac": (achieved / peak_t) if achieved else None, "traffic": None,
+            "peak_source": "bf16_tflops_sustained of " + ("fallback" if pk.get("fallback") else "measured"),
+            "launches": g["launches"], "avg_launch_ms": g["ms"] / max(1, g["launches"]),
+            "flops_per_launch": g["flops"] / max(1, g["launches"])}
+    t_compute = F_exec / (peak_t * 1e12)
+    t_link = max(2 * P / bw["h2d"], 2 * P / bw["d2h"])
+    t_roof = max(t_compute, t_link)
+    kernels = {}
+    for name, k in kern.items():
+        if k["launches"]:
+            kernels[name] = {"launches": k["launches"], "ms_per_step": k["ms"] / args.steps,
+                             "TFLOP/s": (k["flops"] / (k["ms"] / 1e3) / 1e12) if k["flops"] else None,
+                             "GB/s": (k["bytes"] / (k["ms"] / 1e3) / 1e9) if k["bytes"] else None}
+    launches = sum(k["launches"] for k in kern.values())
+    cpu = None
+    if not args.no_cpu and world == 1:
+        try:
+            cpu = cpu_sample(args.config)
+        except Exception as e:  # the oracle is a reported baseline only
+            cpu = {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded uniform token ids, N(0,0.02) weights)",
+        "config": {"workload": workload_desc(args.config, c), "model": args.config,
+                   "global_batch": world * c["batch"] * c["micro"], "seq_len": c["seq"],
+                   "tokens_per_step": T, "parallelism": f"replicas x{world} (no exchange step)",
+                   "pin_store": args.pin_store, "l2": "inputs larger than L2 (every step streams "
+                   f"{2 * P / 1e9:.2f} GB of weights in and out)"},
+        "step_roofline": {"frac": t_roof / t_step, "t_roof_ms": t_roof * 1e3, "t_step_ms": t_step * 1e3,
+                          "bound": "tensor" if t_compute >= t_link else "host link",
+                          "F_exec_pflop": F_exec / 1e15, "peak_tflops": peak_t,
+                          "link_h2d_GBs": bw["h2d"] / 1e9, "link_d2h_GBs": bw["d2h"] / 1e9,
+                          "link_both_GBs": bw["both"] / 1e9, "params": P,
+                          "pages_tflops_convention": F_pages / t_step / 1e12,
+                          "model_tflops_executed": F_exec / t_step / 1e12},
+        "roofline": roof,
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "host": {"adam_ms_per_step": (st1["adam_ms_total"] - st0["adam_ms_total"]) / args.steps,
+                 "pack_ms_per_step": (st1["pack_ms_total"] - st0["pack_ms_total"]) / args.steps,
+                 "h2d_GB_per_step": (st1["h2d_bytes"] - st0["h2d_bytes"]) / args.steps / 1e9,
+                 "d2h_GB_per_step": (st1["d2h_bytes"] - st0["d2h_bytes"]) / args.steps / 1e9,
+                 "device_bytes": m.device_bytes, "host_store_GB": st1["host_store_bytes"] / 1e9,
+                 "pinned_GB": st1["pinned_bytes"] / 1e9, "init_s": init_s, "nproc": os.cpu_count(),
+                 "last_loss": losses[-1]},
+    }
+    print(json.dumps(line), flush=True)
+    m.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

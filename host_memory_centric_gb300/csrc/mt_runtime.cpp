@@ -51,12 +51,12 @@ struct Dev {
 };
 
 struct KStat {
-  int64_t launches = 0;
+  int64_t launches = 0;  // kernels launched
   double ms = 0, flops = 0, bytes = 0;
 };
 struct Pending {
   cudaEvent_t a, b;
-  int kind;
+  int kind, nk;
   double flops, bytes;
 };
 
@@ -247,10 +247,11 @@ cudaEvent_t take_event(mt_model* m) {
 }
 struct Timed {
   mt_model* m;
-  int kind;
+  int kind, nk;
   double flops, bytes;
   cudaEvent_t a = nullptr;
-  Timed(mt_model* mm, int k, double f, double b) : m(mm), kind(k), flops(f), bytes(b) {
+  // nk = kernels the timed call launches
+  Timed(mt_model* mm, int k, double f, double b, int n = 1) : m(mm), kind(k), nk(n), flops(f), bytes(b) {
     if (m->timing) {
       a = take_event(m);
       cudaEventRecord(a, m->sc);
@@ -260,7 +261,7 @@ struct Timed {
     if (a) {
       cudaEvent_t b = take_event(m);
       cudaEventRecord(b, m->sc);
-      m->pend.push_back({a, b, kind, flops, bytes});
+      m->pend.push_back({a, b, kind, nk, flops, bytes});
     }
   }
 };
@@ -269,7 +270,7 @@ void collect_timing(mt_model* m) {
     float ms = 0;
     if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
       KStat& k = m->kstat[p.kind];
-      k.launches++;
+      k.launches += p.nk;
       k.ms += ms;
       k.flops += p.flops;
       k.bytes += p.bytes;
@@ -387,14 +388,14 @@ mt_status decoder_backward(mt_model* m, const View& v, const bf16* x, const bf16
   OK(wgrad(m, d.dgu, d.yn, T, 2 * F, H, v.g[2], nullptr, 0));
   OK(dgrad(m, d.dgu, v.w[2], T, 2 * F, H, d.dyn));
   {
-    Timed t(m, K_OTHER, 0, 8.0 * T * H + 4.0 * T);
+    Timed t(m, K_OTHER, 0, 8.0 * T * H + 4.0 * T, 2);
     CU(m, mt::rmsnorm_bwd(d.dyn, d.x1, v.w[5], d.rstd2, dout, T, H, d.dx1, v.g[5], d.rms_part, s));
   }
   OK(wgrad(m, d.dx1, d.attn, T, H, nhd, v.g[1], nullptr, 0));
   OK(dgrad(m, d.dx1, v.w[1], T, H, nhd, d.dattn));
   {
     const double fl = 10.0 * m->M * m->B * (double)m->nh * m->hd * (double)m->S * m->S / 2;
-    Timed t(m, K_ATTN_B, fl, 0);
+    Timed t(m, K_ATTN_B, fl, 0, 3);
     CU(m, mt::attention_bwd(d.qkv, d.attn, d.lse, d.dattn, m->M * m->B, m->S, m->nh, m->nkv, m->hd, d.dqkv,
                             d.delta, d.dq_acc, s));
   }
@@ -405,7 +406,7 @@ mt_status decoder_backward(mt_model* m, const View& v, const bf16* x, const bf16
   OK(wgrad(m, d.dqkv, d.xn, T, m->Nqkv, H, v.g[0], nullptr, 0));
   OK(dgrad(m, d.dqkv, v.w[0], T, m->Nqkv, H, d.dxn));
   {
-    Timed t(m, K_OTHER, 0, 8.0 * T * H + 4.0 * T);
+    Timed t(m, K_OTHER, 0, 8.0 * T * H + 4.0 * T, 2);
     CU(m, mt::rmsnorm_bwd(d.dxn, x, v.w[4], d.rstd1, d.dx1, T, H, din, v.g[4], d.rms_part, s));
   }
   return MT_OK;
@@ -441,11 +442,14 @@ mt_status head_forward_backward(mt_model* m, const View& v, const bf16* x, bf16*
       OK(wgrad(m, d.logits, hn + c0 * H, rows, V, H, last ? v.g[1] : nullptr, d.dwacc, first ? 1 : 2));
     }
   }
-  CU(m, mt::reduce_sum(d.row_loss, T, inv_norm, d.loss, s));
+  {
+    Timed t(m, K_OTHER, 0, 4.0 * T);
+    CU(m, mt::reduce_sum(d.row_loss, T, inv_norm, d.loss, s));
+  }
   CU(m, cudaMemcpyAsync(m->hloss, d.loss, sizeof(float), cudaMemcpyDeviceToHost, s));
   CU(m, cudaEventRecord(m->LOSS, s));
   {
-    Timed t(m, K_OTHER, 0, 8.0 * T * H);
+    Timed t(m, K_OTHER, 0, 8.0 * T * H, 2);
     CU(m, mt::rmsnorm_bwd(dhn, x, v.w[0], rstd, nullptr, T, H, din, v.g[0], d.rms_part, s));
   }
   return MT_OK;

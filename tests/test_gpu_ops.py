@@ -6,7 +6,6 @@ the arithmetic: outputs are rounded to BF16 (relative step 2^-8), sums are
 FP32, so elementwise |gpu - ref| <= atol + 2^-6 |ref| and relative L2 error
 <= 1e-2 (5e-3 for single roundings).
 """
-import math
 
 import numpy as np
 import pytest
@@ -31,6 +30,8 @@ def rel_l2(a, b):
 
 
 def close(gpu, ref, rel=1e-2, elem_rtol=2 ** -6, atol=None):
+    """Relative L2 bound plus an elementwise bound |d| <= atol + elem_rtol |ref|;
+    atol may be an array (the magnitude of the terms an element sums)."""
     if atol is None:
         atol = 1e-3 * (np.abs(ref).max() + 1e-30)
     assert rel_l2(gpu, ref) <= rel, rel_l2(gpu, ref)
@@ -55,10 +56,21 @@ def rnd(shape, seed, scale=1.0):
 @pytest.mark.parametrize("M,N,K", [(300, 520, 200), (128, 256, 64), (1000, 264, 1032)])
 def test_gemm_majors(orc, a_mn, b_mn, M, N, K):
     A = rnd((M, K), 1); B = rnd((N, K), 2)
-    Ag = bf(A.T.copy() if a_mn else A)
-    Bg = bf(B.T.copy() if b_mn else B)
+    # MN-major operands are stored [K][MN] with the row stride padded to 8
+    # elements (16 bytes), as the tensor-memory-access unit requires
+    pad = lambda n: (n + 7) // 8 * 8
+    if a_mn:
+        At = np.zeros((K, pad(M)), np.float32); At[:, :M] = A.T
+        Ag, lda = bf(At), pad(M)
+    else:
+        Ag, lda = bf(A), K
+    if b_mn:
+        Bt = np.zeros((K, pad(N)), np.float32); Bt[:, :N] = B.T
+        Bg, ldb = bf(Bt), pad(N)
+    else:
+        Bg, ldb = bf(B), K
     D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    ops.gemm(Ag, Bg, M, N, K, a_mn=a_mn, b_mn=b_mn, D=D)
+    ops.gemm(Ag, Bg, M, N, K, a_mn=a_mn, b_mn=b_mn, lda=lda, ldb=ldb, D=D)
     ref = orc.linear_fwd(f64(bf(A)), f64(bf(B)))
     close(f64(D), ref, rel=5e-3)
 
@@ -137,7 +149,10 @@ def test_rope_fwd_inverse(orc, hd):
     ref = orc.rope(ref_in, n_seq, S, nh, hd, 1e6)
     close(f64(xg), ref, rel=5e-3)
     ops.rope(xg, nh, hd, S, cs, inverse=True)
-    close(f64(xg), ref_in, rel=1e-2)
+    # the round trip re-rounds rotated pairs: error scales with the pair norm
+    r = ref_in.reshape(n_seq * S, nh + 2, 2, hd // 2)
+    pair = np.broadcast_to(np.hypot(r[:, :, :1], r[:, :, 1:]), r.shape).reshape(ref_in.shape)
+    close(f64(xg), ref_in, rel=1e-2, elem_rtol=0.0, atol=2 ** -6 * pair + 1e-6)
 
 
 def test_swiglu(orc):
@@ -170,7 +185,11 @@ def test_attention_fwd_bwd(orc, hd, nh, nkv, S, n_seq):
     dg = bf(dout)
     ops.attention_bwd(qg, o, lse, dg, n_seq, S, nh, nkv, hd, dq, scratch)
     d_ref = orc.attention_bwd(f64(qg), o_ref, lse_ref, f64(dg), n_seq, S, nh, nkv, hd)
-    close(f64(dq), d_ref, rel=2e-2, elem_rtol=2 ** -5)
+    # P and dS enter the MMAs as BF16, so an element's error scales with the
+    # magnitude of its summands: bound it by the row RMS of each head slice
+    rr = d_ref.reshape(T, -1, hd)
+    row_rms = np.broadcast_to(np.sqrt((rr ** 2).mean(axis=2, keepdims=True)), rr.shape).reshape(d_ref.shape)
+    close(f64(dq), d_ref, rel=2e-2, elem_rtol=2 ** -6, atol=2 ** -4 * row_rms + 1e-4)
 
 
 # ------------------------------------------------------------------ embedding / CE
