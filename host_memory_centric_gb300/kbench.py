@@ -1,0 +1,104 @@
+"""Kernel micro-benchmark: one libmt device op at a chosen shape, timed with
+CUDA events on the launching stream after warm-up (inputs larger than L2
+unless the shape is small).
+
+python -m host_memory_centric_gb300.kbench gemm --M 8192 --N 11264 --K 2048 [--a-mn] [--b-mn]
+python -m host_memory_centric_gb300.kbench attn_fwd --S 2048 --nseq 4 --nh 16 --nkv 4 --hd 128
+python -m host_memory_centric_gb300.kbench attn_bwd --S 2048 --nseq 4 --nh 16 --nkv 4 --hd 128
+python -m host_memory_centric_gb300.kbench rmsnorm_bwd --T 8192 --H 2048
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import torch
+
+from . import ops
+
+
+def timeit(fn, iters, warmup):
+    for _ in range(warmup):
+        fn()
+    s = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(s)
+    for _ in range(iters):
+        fn()
+    b.record(s)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("op")
+    ap.add_argument("--M", type=int, default=8192)
+    ap.add_argument("--N", type=int, default=11264)
+    ap.add_argument("--K", type=int, default=2048)
+    ap.add_argument("--a-mn", action="store_true")
+    ap.add_argument("--b-mn", action="store_true")
+    ap.add_argument("--S", type=int, default=2048)
+    ap.add_argument("--nseq", type=int, default=4)
+    ap.add_argument("--nh", type=int, default=16)
+    ap.add_argument("--nkv", type=int, default=4)
+    ap.add_argument("--hd", type=int, default=128)
+    ap.add_argument("--T", type=int, default=8192)
+    ap.add_argument("--H", type=int, default=2048)
+    ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    a = ap.parse_args()
+    torch.manual_seed(0)
+    bf = torch.bfloat16
+    dev = "cuda"
+    res = {"op": a.op}
+    if a.op == "gemm":
+        A = (torch.randn(a.K, a.M) if a.a_mn else torch.randn(a.M, a.K)).to(bf).to(dev)
+        B = (torch.randn(a.K, a.N) if a.b_mn else torch.randn(a.N, a.K)).to(bf).to(dev)
+        D = torch.empty(a.M, a.N, dtype=bf, device=dev)
+        ms = timeit(lambda: ops.gemm(A, B, a.M, a.N, a.K, a_mn=a.a_mn, b_mn=a.b_mn, D=D), a.iters, a.warmup)
+        res.update(shape=[a.M, a.N, a.K], a_mn=a.a_mn, b_mn=a.b_mn, ms=ms, tflops=2 * a.M * a.N * a.K / ms / 1e9)
+        ref_ms = timeit(lambda: torch.matmul(A.T if a.a_mn else A, B if a.b_mn else B.T, out=D), a.iters, a.warmup)
+        res.update(torch_matmul_ms=ref_ms, torch_matmul_tflops=2 * a.M * a.N * a.K / ref_ms / 1e9)
+    elif a.op in ("attn_fwd", "attn_bwd"):
+        T = a.nseq * a.S
+        qkv = (torch.randn(T, (a.nh + 2 * a.nkv) * a.hd) * 0.5).to(bf).to(dev)
+        o = torch.empty(T, a.nh * a.hd, dtype=bf, device=dev)
+        lse = torch.empty(a.nh, T, dtype=torch.float32, device=dev)
+        fl = 4.0 * a.nseq * a.nh * a.hd * a.S * a.S / 2
+        ops.attention_fwd(qkv, a.nseq, a.S, a.nh, a.nkv, a.hd, o, lse)
+        if a.op == "attn_fwd":
+            ms = timeit(lambda: ops.attention_fwd(qkv, a.nseq, a.S, a.nh, a.nkv, a.hd, o, lse), a.iters, a.warmup)
+        else:
+            fl *= 2.5
+            do = torch.randn(T, a.nh * a.hd).to(bf).to(dev)
+            dq = torch.empty_like(qkv)
+            sc = torch.empty(ops.attention_bwd_scratch_bytes(a.nseq, a.S, a.nh, a.hd), dtype=torch.uint8,
+                             device=dev)
+            ms = timeit(lambda: ops.attention_bwd(qkv, o, lse, do, a.nseq, a.S, a.nh, a.nkv, a.hd, dq, sc),
+                        a.iters, a.warmup)
+        res.update(shape=dict(S=a.S, nseq=a.nseq, nh=a.nh, nkv=a.nkv, hd=a.hd), ms=ms, tflops=fl / ms / 1e9)
+    elif a.op in ("rmsnorm_fwd", "rmsnorm_bwd"):
+        x = torch.randn(a.T, a.H).to(bf).to(dev)
+        g = torch.ones(a.H, dtype=bf, device=dev)
+        y = torch.empty_like(x)
+        r = torch.empty(a.T, dtype=torch.float32, device=dev)
+        ops.rmsnorm_fwd(x, g, 1e-6, y, r)
+        if a.op == "rmsnorm_fwd":
+            ms = timeit(lambda: ops.rmsnorm_fwd(x, g, 1e-6, y, r), a.iters, a.warmup)
+            by = 4.0 * a.T * a.H
+        else:
+            dx = torch.empty_like(x)
+            dg = torch.empty(a.H, dtype=bf, device=dev)
+            sc = torch.empty(ops.rmsnorm_bwd_scratch_bytes(a.T, a.H), dtype=torch.uint8, device=dev)
+            ms = timeit(lambda: ops.rmsnorm_bwd(y, x, g, r, y, dx, dg, sc), a.iters, a.warmup)
+            by = 8.0 * a.T * a.H
+        res.update(shape=[a.T, a.H], ms=ms, gbs=by / ms / 1e6)
+    else:
+        raise SystemExit("unknown op " + a.op)
+    print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()
