@@ -256,6 +256,23 @@ mt_status mt_cross_entropy(void* logits, const int32_t* target, int64_t rows, in
 mt_status mt_timing(mt_model* model, int32_t enable);
 mt_status mt_timing_read(mt_model* model, int32_t kind, int64_t* launches, double* ms,
                          double* flops, double* bytes);
+/* RMSNorm backward that allocates nothing (same results as mt_rmsnorm_bwd).
+ * The pages have no counterpart: this is for callers that cannot allocate
+ * device memory -- code running during stream capture, code inside another
+ * framework whose allocator owns all device memory, or callers that cannot
+ * afford cudaMalloc's latency or implicit synchronisation.  The dgamma
+ * partial sums go to a fixed array inside the library (9.5 MiB,
+ * MT_NOALLOC_SCRATCH_FLOATS floats), which every GPU that loads the library
+ * holds until exit.  Returns MT_ERR_ARG when mt_rmsnorm_bwd_scratch_bytes(T, H)
+ * exceeds that array (or for the arguments mt_rmsnorm_bwd rejects).  All calls
+ * share the array: calls that overlap on the GPU race.  It keeps the last
+ * call's contents, and nothing in it needs to start at zero.  The first call
+ * on each device looks up the array's device address; make it before any
+ * stream capture. */
+#define MT_NOALLOC_SCRATCH_FLOATS (304u * 8192u)
+mt_status mt_rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* gamma,
+                                 const float* rstd, const void* dres, int64_t T, int32_t H,
+                                 void* dx, void* dgamma, void* stream);
 /* Error word of the kernels' bounded waits (0 = none); clear != 0 resets it. */
 mt_status mt_kernel_error(int32_t* code, int32_t clear);
 
