@@ -208,6 +208,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--pin-store", type=int, default=1)
     ap.add_argument("--threads", type=int, default=0)
+    ap.add_argument("--slabs", type=int, default=12)
+    ap.add_argument("--keep-host-grad", type=int, default=1)
+    ap.add_argument("--ckpt-on-host", type=int, default=1)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -241,7 +244,9 @@ def main():
     bw = link_bandwidth(torch)
 
     t_init = time.time()
-    m = mt.Model(c, seed=1234, pin_store=args.pin_store, n_host_threads=args.threads)
+    hbw = mt.host_bandwidth(1 << 30)
+    m = mt.Model(c, seed=1234, pin_store=args.pin_store, n_host_threads=args.threads, n_grad_slabs=args.slabs,
+                 keep_host_grad=args.keep_host_grad, ckpt_on_host=args.ckpt_on_host)
     init_s = time.time() - t_init
     toks = [inputs.tokens_for(c, s) for s in range(args.warmup + 2 * args.steps + 1)]
     step = 0
@@ -331,6 +336,12 @@ def main():
                              "TFLOP/s": (k["flops"] / (k["ms"] / 1e3) / 1e12) if k["flops"] else None,
                              "GB/s": (k["bytes"] / (k["ms"] / 1e3) / 1e9) if k["bytes"] else None}
     launches = sum(k["launches"] for k in kern.values())
+    # host memory traffic per step: Adam reads slab (2 B) + master, m, v (12 B), writes master, m, v
+    # (12 B) + W (2 B) [+ G (2 B) when unpacking], and every DMA reads or writes host memory once
+    n_pad = sum(b["n_pad"] for b in m.layout)
+    adam_b = n_pad * (28 + 2 * args.keep_host_grad)
+    dma_b = (st1["h2d_bytes"] - st0["h2d_bytes"] + st1["d2h_bytes"] - st0["d2h_bytes"]) / args.steps
+    t_host = (adam_b + dma_b) / (hbw["copy_gbs"] * 1e9)
     cpu = None
     if not args.no_cpu and world == 1:
         try:
@@ -344,7 +355,8 @@ def main():
         "config": {"workload": workload_desc(args.config, c), "model": args.config,
                    "global_batch": world * c["batch"] * c["micro"], "seq_len": c["seq"],
                    "tokens_per_step": T, "parallelism": f"replicas x{world} (no exchange step)",
-                   "pin_store": args.pin_store, "l2": "inputs larger than L2 (every step streams "
+                   "pin_store": args.pin_store, "n_grad_slabs": args.slabs, "keep_host_grad": args.keep_host_grad,
+                   "ckpt_on_host": args.ckpt_on_host, "l2": "inputs larger than L2 (every step streams "
                    f"{2 * P / 1e9:.2f} GB of weights in and out)"},
         "step_roofline": {"frac": t_roof / t_step, "t_roof_ms": t_roof * 1e3, "t_step_ms": t_step * 1e3,
                           "bound": "tensor" if t_compute >= t_link else "host link",
@@ -353,6 +365,11 @@ def main():
                           "link_both_GBs": bw["both"] / 1e9, "params": P,
                           "pages_tflops_convention": F_pages / t_step / 1e12,
                           "model_tflops_executed": F_exec / t_step / 1e12},
+        "host_dram_bound": {"host_copy_GBs": hbw["copy_gbs"], "host_adam_Gelem_s": hbw["adam_gelem_s"],
+                            "threads": hbw["threads"], "bytes_per_step_GB": (adam_b + dma_b) / 1e9,
+                            "t_host_ms": t_host * 1e3, "frac": t_host / t_step,
+                            "note": "host DRAM traffic of Adam + DMA over the measured 16-thread copy bandwidth; "
+                                    "not part of the step roofline"},
         "roofline": roof,
         "kernels": kernels,
         "cpu_baseline": cpu,

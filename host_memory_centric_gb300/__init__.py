@@ -43,7 +43,7 @@ class MtConfig(C.Structure):
                 ("n_host_threads", C.c_int32), ("lr", C.c_float), ("beta1", C.c_float),
                 ("beta2", C.c_float), ("adam_eps", C.c_float), ("weight_decay", C.c_float),
                 ("seed", C.c_uint64), ("timeout_ms", C.c_uint32), ("pin_store", C.c_int32),
-                ("head_chunk", C.c_int32), ("log_protocol", C.c_int32)]
+                ("head_chunk", C.c_int32), ("log_protocol", C.c_int32), ("keep_host_grad", C.c_int32)]
 
 
 class DevRegion(C.Structure):
@@ -108,6 +108,7 @@ def lib():
         "mt_plan_protocol": (i64, [pc, i32, C.c_char_p, i64]),
         "mt_schedule": (i32, [i32, _P(f64), _P(f64), _P(f64), _P(f64), f64, f64, _P(f64)]),
         "mt_token_csr": (i32, [_P(i32), i64, i32, _P(i32), _P(i32)]),
+        "mt_host_bandwidth": (i32, [sz, i32, _P(f64), _P(f64)]),
         "mt_rope_table": (i32, [i32, i32, f64, _P(f32)]),
         "mt_timing": (i32, [_v, i32]),
         "mt_timing_read": (i32, [_v, i32, _P(i64), _P(f64), _P(f64), _P(f64)]),
@@ -158,6 +159,15 @@ def make_config(shape: dict, **rt) -> MtConfig:
 def _ptr(a: np.ndarray, ct):
     assert a.flags["C_CONTIGUOUS"]
     return a.ctypes.data_as(_P(ct))
+
+
+def host_bandwidth(nbytes: int = 1 << 30, threads: int = 0) -> dict:
+    """Host memory copy bandwidth (GB/s, read + write) and Adam rate."""
+    if threads <= 0:
+        threads = os.cpu_count() or 1
+    a, b = C.c_double(), C.c_double()
+    check(lib().mt_host_bandwidth(nbytes, threads, C.byref(a), C.byref(b)))
+    return {"copy_gbs": a.value, "adam_gelem_s": b.value, "threads": threads}
 
 
 def layout(cfg: MtConfig) -> list[dict]:

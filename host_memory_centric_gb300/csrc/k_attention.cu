@@ -409,6 +409,13 @@ cudaError_t bwd_t(const bf16* qkv, const bf16* o, const float* lse, const bf16* 
 
 cudaError_t attention_fwd(const bf16* qkv, int n_seq, int S, int nh, int nkv, int hd, bf16* o, float* lse,
                           cudaStream_t s) {
+  return attention_fwd_tc(qkv, n_seq, S, nh, nkv, hd, o, lse, s);
+}
+
+// Warp-level (mma.sync) forward, kept as the reference the tensor-core
+// forward was validated against in the op tests.
+cudaError_t attention_fwd_warp(const bf16* qkv, int n_seq, int S, int nh, int nkv, int hd, bf16* o, float* lse,
+                               cudaStream_t s) {
   if (n_seq <= 0 || S <= 0) return cudaSuccess;
   if (nh % nkv || !al16(qkv) || !al16(o) || n_seq > 65535 || nh > 65535) return cudaErrorInvalidValue;
   if (hd == 64) return fwd_t<64>(qkv, n_seq, S, nh, nkv, o, lse, s);

@@ -1,0 +1,454 @@
+// k_attention_tc.cu -- causal GQA attention forward on the 5th-generation
+// tensor cores (sm_103a): tcgen05.mma with TMEM accumulators, TMA tiles.
+//
+// One CTA per (128 queries, query head, sequence), 192 threads:
+//   warp 0      TMA producer: the Q tile once, then K and V tiles of 128 keys
+//               into a 2-stage ring (128-byte swizzle);
+//   warp 1      allocates TMEM (S0 | S1 | O) and, from one thread, issues
+//               S_j = Q K_j^T (M=128, N=128) into S[j % 2] and, once the
+//               softmax has produced P_{j-1}, O += P_{j-1} V_{j-1} (M=128,
+//               N=hd, V as an MN-major operand);
+//   warps 2..5  softmax, one thread per query row: read S_j from TMEM, causal
+//               mask, online max / sum in the exp2 domain, rescale the row of O
+//               in TMEM when its max grows, write P_j as BF16 into the
+//               128B-swizzled K-major layout the next MMA reads; at the end
+//               O / l to global memory and LSE = (m + log2 l) ln 2.
+// The double-buffered S lets S_{j+1} run on the tensor core while the
+// softmax works on S_j.  Every mbarrier wait is bounded; an expired wait sets
+// the kernel error word and the CTA stops, drains its copies and frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "mt_kernels.h"
+
+namespace mt {
+namespace {
+
+constexpr int THREADS = 192;
+constexpr long long kWaitCycles = 4000000000LL;
+constexpr int CH = 16384;  // one 64-column chunk of a 128-row tile (128 rows x 128 B)
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_test(b, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_test(b, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+}
+__device__ __forceinline__ void tma_load(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(su32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum));
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])),
+      "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+      "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])),
+      "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])),
+      "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])),
+      "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ULL << 46) | (2ULL << 61);
+}
+__host__ __device__ constexpr uint32_t idesc(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ int g_attn_error = 0;
+
+template <int HD>
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_fwd_tc_k(const __grid_constant__ CUtensorMap tm, int S, int nh, int nkv, bf16* __restrict__ o,
+                  float* __restrict__ lse, float scale_log2) {
+  constexpr int NC = HD / 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = sm;
+  uint8_t* sK = sQ + NC * CH;       // 2 stages
+  uint8_t* sV = sK + 2 * NC * CH;   // 2 stages
+  uint8_t* sP = sV + 2 * NC * CH;   // 2 key chunks
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * CH);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = bars + 3;
+  uint64_t* s_full = bars + 5;
+  uint64_t* s_empty = bars + 7;
+  uint64_t* p_full = bars + 9;
+  uint64_t* o_done = bars + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first
+  const int h = blockIdx.y, n = blockIdx.z;
+  const int kh = h / (nh / nkv);
+  const int q0 = qb * 128;
+  const int ntiles = qb + 1;
+  const int row0 = n * S;  // first token row of this sequence
+  const int64_t T = (int64_t)gridDim.z * S;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(o_done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                 "r"(512));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS[2] = {tmem, tmem + 128};
+  const uint32_t tO = tmem + 256;
+  uint32_t kv_inflight = 0, kv_par = 0;  // producer drain bookkeeping
+  bool q_inflight = false;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      mbar_expect_tx(q_full, NC * CH);
+      for (int c = 0; c < NC; ++c) tma_load(&tm, q_full, sQ + c * CH, h * HD + 64 * c, row0 + q0);
+      q_inflight = true;
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int s = j & 1;
+        const uint32_t u = (uint32_t)(j >> 1);
+        if (!mbar_wait(&kv_empty[s], (u & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(&kv_full[s], 2 * NC * CH);
+        for (int c = 0; c < NC; ++c) {
+          tma_load(&tm, &kv_full[s], sK + (s * NC + c) * CH, (nh + kh) * HD + 64 * c, row0 + 128 * j);
+          tma_load(&tm, &kv_full[s], sV + (s * NC + c) * CH, (nh + nkv + kh) * HD + 64 * c, row0 + 128 * j);
+        }
+        kv_inflight |= 1u << s;
+        kv_par = (kv_par & ~(1u << s)) | ((u & 1) << s);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicCAS(&g_attn_error, 0, 11);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      constexpr uint32_t IS = idesc(128, 128, false, false);
+      constexpr uint32_t IO = idesc(128, HD, false, true);
+      auto issue_pv = [&](int i) -> bool {
+        if (!mbar_wait(p_full, (uint32_t)(i & 1), abort_flag)) return false;
+        tc_fence_after();
+        const int s = i & 1;
+        const uint32_t p0 = su32(sP), v0 = su32(sV + s * NC * CH);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sdesc(p0 + (kk >> 2) * CH + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc(v0 + kk * 16 * 128, CH, 1024);
+          tc_mma(tO, ad, bd, IO, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(o_done);
+        tc_commit(&kv_empty[s]);
+        return true;
+      };
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int s = j & 1, b = j & 1;
+        const uint32_t u = (uint32_t)(j >> 1);
+        if (!mbar_wait(&kv_full[s], u & 1, abort_flag) || !mbar_wait(&s_empty[b], (u & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t q0a = su32(sQ), k0a = su32(sK + s * NC * CH);
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc_mma(tS[b], sdesc(q0a + c * CH + k * 32, 16, 1024), sdesc(k0a + c * CH + k * 32, 16, 1024), IS,
+                   (c | k) != 0);
+        tc_commit(&s_full[b]);
+        if (j >= 1 && !issue_pv(j - 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (ok) ok = issue_pv(ntiles - 1);
+      if (!ok) {
+        *abort_flag = 1;
+        atomicCAS(&g_attn_error, 0, 12);
+      }
+    }
+  } else {
+    // softmax: this thread owns query row r of the tile; the warp may touch
+    // TMEM lanes 32*(warp%4) .. +31
+    const int qw = warp & 3;
+    const int r = qw * 32 + lane;
+    const int qpos = q0 + r;  // position inside the sequence
+    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+    float m_old = -INFINITY, l = 0.f;
+    bool ok = true;
+    uint8_t* prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
+    for (int j = 0; j < ntiles; ++j) {
+      const int b = j & 1;
+      const uint32_t u = (uint32_t)(j >> 1);
+      // warp-uniform outcome: the TMEM loads below are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], u & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float t[32];
+        tmem_ld32(tS[b] + lane_off + c * 32, t);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = t[i];
+      }
+      tc_fence_before();
+      mbar_arrive(&s_empty[b]);
+      const int kbase = 128 * j;
+      float mx = m_old;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        const int key = kbase + i;
+        float v = s[i] * scale_log2;
+        if (key > qpos || key >= S) v = -INFINITY;
+        s[i] = v;
+        mx = fmaxf(mx, v);
+      }
+      const float base = mx == -INFINITY ? 0.f : mx;
+      const float alpha = exp2f(m_old - base);  // 0 when m_old = -inf
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        s[i] = exp2f(s[i] - base);
+        sum += s[i];
+      }
+      l = l * alpha + sum;
+      // P_{j-1} consumed and O written by the previous PV before we touch them
+      if (j > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)((j - 1) & 1), abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, mx > m_old)) {
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            float t[32];
+            tmem_ld32(tO + lane_off + c * 32, t);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) t[i] *= alpha;
+            tmem_st32(tO + lane_off + c * 32, t);
+          }
+        }
+      }
+      m_old = mx;
+      // P row into the 128B-swizzled K-major tile: 16-byte unit u of key chunk kc
+      // of row r sits at unit (u ^ (r % 8)) of the row
+#pragma unroll
+      for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+        for (int uu = 0; uu < 8; ++uu) {
+          const float* p = s + kc * 64 + uu * 8;
+          const uint4 v = make_uint4(pack2(p[0], p[1]), pack2(p[2], p[3]), pack2(p[4], p[5]), pack2(p[6], p[7]));
+          *reinterpret_cast<uint4*>(prow + kc * CH + ((uu ^ (r & 7)) << 4)) = v;
+        }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)((ntiles - 1) & 1), abort_flag));
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const bool valid = qpos < S;
+      bf16* orow = o + ((int64_t)row0 + qpos) * ((int64_t)nh * HD) + (int64_t)h * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        float t[32];
+        tmem_ld32(tO + lane_off + c * 32, t);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            reinterpret_cast<uint4*>(orow + c * 32)[i] =
+                make_uint4(pack2(t[8 * i] * inv, t[8 * i + 1] * inv), pack2(t[8 * i + 2] * inv, t[8 * i + 3] * inv),
+                           pack2(t[8 * i + 4] * inv, t[8 * i + 5] * inv), pack2(t[8 * i + 6] * inv, t[8 * i + 7] * inv));
+        }
+      }
+      if (valid) lse[(int64_t)h * T + row0 + qpos] = (m_old + log2f(l)) * 0.6931471805599453f;
+    } else {
+      if (lane == 0) {
+        *abort_flag = 1;
+        atomicCAS(&g_attn_error, 0, 13);
+      }
+    }
+  }
+
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    const long long t0 = clock64();
+    if (q_inflight)
+      while (!mbar_test(q_full, 0) && clock64() - t0 < kWaitCycles) {
+      }
+    for (int s2 = 0; s2 < 2; ++s2)
+      if (kv_inflight & (1u << s2))
+        while (!mbar_test(&kv_full[s2], (kv_par >> s2) & 1) && clock64() - t0 < kWaitCycles) {
+        }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_once;
+cudaError_t g_init = cudaSuccess;
+
+void init_once() {
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+    g_init = e != cudaSuccess ? e : cudaErrorNotSupported;
+    return;
+  }
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+template <int HD>
+constexpr int smem_bytes() {
+  return (HD / 64) * 16384 * 5 + 2 * 16384 + 1024 + 256;
+}
+
+template <int HD>
+cudaError_t launch(const bf16* qkv, int n_seq, int S, int nh, int nkv, bf16* o, float* lse, cudaStream_t s) {
+  const int64_t ld = (int64_t)(nh + 2 * nkv) * HD;
+  const int64_t T = (int64_t)n_seq * S;
+  CUtensorMap m;
+  const cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)T};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  if (g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<bf16*>(qkv), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  constexpr int SM = smem_bytes<HD>();
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_k<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SM);
+  if (e != cudaSuccess) return e;
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
+  dim3 grid((S + 127) / 128, nh, n_seq);
+  attn_fwd_tc_k<HD><<<grid, THREADS, SM, s>>>(m, S, nh, nkv, o, lse, scale_log2);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Tensor-core attention forward (see the file comment).  Same contract as
+// attention_fwd; requires hd in {64, 128}, 16-byte aligned qkv and o.
+cudaError_t attention_fwd_tc(const bf16* qkv, int n_seq, int S, int nh, int nkv, int hd, bf16* o, float* lse,
+                             cudaStream_t s) {
+  std::call_once(g_once, init_once);
+  if (g_init != cudaSuccess) return g_init;
+  if (n_seq <= 0 || S <= 0) return cudaSuccess;
+  if (nh % nkv || n_seq > 65535 || nh > 65535 || (int64_t)n_seq * S > 0x7fffffff) return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(o)) & 15) return cudaErrorInvalidValue;
+  if (hd == 64) return launch<64>(qkv, n_seq, S, nh, nkv, o, lse, s);
+  if (hd == 128) return launch<128>(qkv, n_seq, S, nh, nkv, o, lse, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t attention_error_read(int* code, int clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(code, g_attn_error, sizeof(int));
+  if (e != cudaSuccess || !clear) return e;
+  const int z = 0;
+  return cudaMemcpyToSymbol(g_attn_error, &z, sizeof(int));
+}
+
+}  // namespace mt

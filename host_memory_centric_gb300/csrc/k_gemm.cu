@@ -347,7 +347,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      if (!mbar_wait(&tfull[acc], aph, abort_flag)) {
+      // warp-uniform outcome: the TMEM loads below are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, abort_flag))) {
         ok = false;
         break;
       }
@@ -470,7 +471,11 @@ cudaError_t kernel_error_read(int* code, int clear) {
   if (clear) {
     const int z = 0;
     e = cudaMemcpyToSymbol(g_kernel_error, &z, sizeof(int));
+    if (e != cudaSuccess) return e;
   }
+  int a = 0;
+  e = attention_error_read(&a, clear);
+  if (*code == 0) *code = a;
   return e;
 }
 

@@ -124,28 +124,51 @@ void init_block(const mt_config* c, const BlockDesc& b, int j, float* master, in
   }
 }
 
-void adam(int64_t n, const uint16_t* __restrict g, float* __restrict th, float* __restrict m, float* __restrict v,
-          uint16_t* __restrict w, int32_t t, float lr, float b1, float b2, float eps, float wd) {
-  const float bc1 = (float)(1.0 - std::pow((double)b1, (double)t));
-  const float bc2 = (float)(1.0 - std::pow((double)b2, (double)t));
-  const float c1 = 1.0f - b1, c2 = 1.0f - b2;
-  for (int64_t i = 0; i < n; ++i) {
-    uint32_t gu = (uint32_t)g[i] << 16;
-    float gi;
-    std::memcpy(&gi, &gu, 4);
-    const float mi = b1 * m[i] + c1 * gi;
-    const float vi = b2 * v[i] + c2 * gi * gi;
-    m[i] = mi;
-    v[i] = vi;
-    float x = th[i];
-    if (wd != 0.0f) x -= lr * wd * x;
-    x -= lr * (mi / bc1) / (std::sqrt(vi / bc2) + eps);
-    th[i] = x;
-    uint32_t u;
-    std::memcpy(&u, &x, 4);
-    const bool nan = ((u >> 23) & 0xFF) == 0xFF && (u & 0x7FFFFF) != 0;
-    const uint32_t r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16;
-    w[i] = nan ? (uint16_t)((u >> 16) | 0x0040) : (uint16_t)r;
+namespace {
+inline float bf16f(uint16_t b) {
+  const uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return f;
+}
+// One Adam element: gradient gi (FP32 of its BF16), moments and master in
+// FP32.  step = lr / (1 - b1^t) and isb2 = 1 / sqrt(1 - b2^t) fold the bias
+// corrections: m_hat / (sqrt(v_hat) + eps) = m / (1-b1^t) / (sqrt(v) isb2 + eps).
+inline uint16_t adam_elem(float gi, float& th, float& m, float& v, float b1, float c1, float b2, float c2,
+                          float step, float isb2, float eps, float lrwd) {
+  const float mi = b1 * m + c1 * gi;
+  const float vi = b2 * v + c2 * gi * gi;
+  m = mi;
+  v = vi;
+  float x = th;
+  x -= lrwd * x;
+  x -= step * mi / (std::sqrt(vi) * isb2 + eps);
+  th = x;
+  uint32_t u;
+  std::memcpy(&u, &x, 4);
+  const bool nan = ((u >> 23) & 0xFF) == 0xFF && (u & 0x7FFFFF) != 0;
+  const uint32_t r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16;
+  return nan ? (uint16_t)((u >> 16) | 0x0040) : (uint16_t)r;
+}
+}  // namespace
+
+void adam(int64_t n, const uint16_t* __restrict g, uint16_t* __restrict gcopy, float* __restrict th,
+          float* __restrict m, float* __restrict v, uint16_t* __restrict w, int32_t t, float lr, float b1, float b2,
+          float eps, float wd) {
+  const double bc1 = 1.0 - std::pow((double)b1, (double)t);
+  const double bc2 = 1.0 - std::pow((double)b2, (double)t);
+  const float step = (float)((double)lr / bc1);
+  const float isb2 = (float)(1.0 / std::sqrt(bc2));
+  const float c1 = 1.0f - b1, c2 = 1.0f - b2, lrwd = lr * wd;
+  if (gcopy) {
+    for (int64_t i = 0; i < n; ++i) {
+      const uint16_t gb = g[i];
+      gcopy[i] = gb;
+      w[i] = adam_elem(bf16f(gb), th[i], m[i], v[i], b1, c1, b2, c2, step, isb2, eps, lrwd);
+    }
+  } else {
+    for (int64_t i = 0; i < n; ++i)
+      w[i] = adam_elem(bf16f(g[i]), th[i], m[i], v[i], b1, c1, b2, c2, step, isb2, eps, lrwd);
   }
 }
 

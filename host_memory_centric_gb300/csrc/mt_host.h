@@ -44,9 +44,11 @@ float bf16_val(uint16_t b);
 // Master values (n_pad floats) of block j: N(0, init_std) matrices from the
 // block/tensor stream of SplitMix64, RMSNorm gains 1, padding 0.
 void init_block(const mt_config* c, const BlockDesc& b, int j, float* master, int64_t e0, int64_t e1);
-// Adam over [0, n) (FP32 arithmetic).
-void adam(int64_t n, const uint16_t* g, float* th, float* m, float* v, uint16_t* w, int32_t t, float lr,
-          float b1, float b2, float eps, float wd);
+// Adam over [0, n) (FP32 arithmetic) on gradient g (BF16); when gcopy is not
+// null the gradient is also written there (the slab unpack into the store's G
+// region, fused into the same pass).
+void adam(int64_t n, const uint16_t* g, uint16_t* gcopy, float* th, float* m, float* v, uint16_t* w, int32_t t,
+          float lr, float b1, float b2, float eps, float wd);
 
 // ---------------------------------------------------------------- worker pool
 // Fixed threads running index ranges.  parallel_for may be called from several

@@ -33,8 +33,10 @@ cudaError_t gemm(const GemmArgs& g, cudaStream_t s);
 int gemm_num_sms();
 
 // Device-side error word written by kernels whose bounded waits expired
-// (0 = none).  Read / cleared by the host.
+// (0 = none; the GEMM's and the tensor-core attention's).  Read / cleared by
+// the host.
 cudaError_t kernel_error_read(int* code, int clear);
+cudaError_t attention_error_read(int* code, int clear);
 
 // ---------------------------------------------------------------- elementwise
 // RMSNorm forward: y = x * rstd * gamma, rstd = (mean(x^2) + eps)^-1/2.
@@ -86,6 +88,10 @@ cudaError_t add_bf16(const bf16* a, const bf16* b, int64_t n, bf16* y, cudaStrea
 // (natural log).  hd in {64, 128}.
 cudaError_t attention_fwd(const bf16* qkv, int n_seq, int S, int nh, int nkv, int hd, bf16* o,
                           float* lse, cudaStream_t s);
+// The same forward on tcgen05 tensor cores with TMEM accumulators (used by
+// attention_fwd).
+cudaError_t attention_fwd_tc(const bf16* qkv, int n_seq, int S, int nh, int nkv, int hd, bf16* o, float* lse,
+                             cudaStream_t s);
 // Backward: dqkv ([T][(nh+2nkv)hd]) receives dq, dk, dv.  delta ([nh][T]) and
 // dq_acc ([T][nh*hd] fp32) are scratch.
 cudaError_t attention_bwd(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout,

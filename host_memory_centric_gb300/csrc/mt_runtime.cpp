@@ -22,6 +22,7 @@
 #include <chrono>
 #include <cmath>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <memory>
 
@@ -457,15 +458,51 @@ mt_status head_forward_backward(mt_model* m, const View& v, const bf16* x, bf16*
 
 // ---------------------------------------------------------------- Adam worker
 void adam_loop(mt_model* m) {
+  auto idle_since = Clock::now();
+  bool idle = false;
   for (;;) {
     Job job;
+    bool have = false;
     {
+      // Among queued jobs whose slab has landed, take the lowest block: the
+      // next step's forward consumes blocks in ascending order while the
+      // backward exports them in descending order.
       std::unique_lock<std::mutex> lk(m->amu);
       m->acv.wait(lk, [m] { return m->stopping || !m->jobs.empty(); });
       if (m->jobs.empty()) return;
-      job = m->jobs.front();
-      m->jobs.pop_front();
+      auto best = m->jobs.end();
+      for (auto it = m->jobs.begin(); it != m->jobs.end(); ++it) {
+        const cudaError_t q = cudaEventQuery(m->SR[(size_t)it->slab]);
+        if (q == cudaSuccess) {
+          if (best == m->jobs.end() || it->block < best->block) best = it;
+        } else if (q != cudaErrorNotReady) {
+          best = it;  // let the wait below report the error
+          break;
+        }
+      }
+      if (best != m->jobs.end()) {
+        job = *best;
+        m->jobs.erase(best);
+        have = true;
+      }
     }
+    if (!have) {
+      if (!idle) {
+        idle = true;
+        idle_since = Clock::now();
+      } else if (Clock::now() - idle_since > std::chrono::milliseconds(m->c.timeout_ms)) {
+        set_err(m, MT_ERR_TIMEOUT, "timed out waiting for any gradient slab to land");
+        std::lock_guard<std::mutex> lk(m->amu);
+        m->slab_free.assign(m->slab_free.size(), 1);
+        m->inflight_jobs = 0;
+        m->jobs.clear();
+        m->acv.notify_all();
+        continue;
+      }
+      std::this_thread::sleep_for(std::chrono::microseconds(20));
+      continue;
+    }
+    idle = false;
     const auto t0 = Clock::now();
     mt_status st = m->failed ? MT_ERR_STATE : wait_event(m, m->SR[(size_t)job.slab], "slab ready");
     if (st == MT_OK) {
@@ -487,9 +524,8 @@ void adam_loop(mt_model* m) {
       const mt_config& c = m->c;
       std::function<void(int64_t)> fn = [&](int64_t i) {
         const int64_t o = items[(size_t)i].first, n = items[(size_t)i].second;
-        std::memcpy(G + o, slab + o, (size_t)n * 2);
-        mth::adam(n, G + o, th + o, mm + o, vv + o, W + o, job.t, c.lr, c.beta1, c.beta2, c.adam_eps,
-                  c.weight_decay);
+        mth::adam(n, slab + o, c.keep_host_grad ? G + o : nullptr, th + o, mm + o, vv + o, W + o, job.t, c.lr,
+                  c.beta1, c.beta2, c.adam_eps, c.weight_decay);
       };
       std::string werr;
       if (!m->pool.parallel_for((int64_t)items.size(), fn, &werr))
@@ -516,14 +552,25 @@ mt_status wait_adam(mt_model* m, int j, int64_t t) {
   return MT_OK;
 }
 
-mt_status acquire_slab(mt_model* m, int k) {
+// Takes the lowest-numbered free slab, waiting (bounded) while all are held.
+mt_status acquire_slab(mt_model* m, int* k) {
   std::unique_lock<std::mutex> lk(m->amu);
+  auto any_free = [&] {
+    for (size_t i = 0; i < m->slab_free.size(); ++i)
+      if (m->slab_free[i]) return true;
+    return false;
+  };
   const bool ok = m->acv.wait_for(lk, std::chrono::milliseconds(m->c.timeout_ms),
-                                  [&] { return m->failed || m->slab_free[(size_t)k]; });
+                                  [&] { return m->failed || any_free(); });
   if (m->failed) return MT_ERR_STATE;
   if (!ok) return set_err(m, MT_ERR_TIMEOUT, "timed out waiting for a free gradient slab");
-  m->slab_free[(size_t)k] = 0;
-  return MT_OK;
+  for (size_t i = 0; i < m->slab_free.size(); ++i)
+    if (m->slab_free[i]) {
+      m->slab_free[i] = 0;
+      *k = (int)i;
+      return MT_OK;
+    }
+  return set_err(m, MT_ERR_INTERNAL, "slab bookkeeping");
 }
 
 // ---------------------------------------------------------------- visit pieces
@@ -668,13 +715,13 @@ mt_status do_backward(mt_model* m, int j, int b) {
 }
 
 mt_status do_stream_out(mt_model* m, int j, int b, int* slab_out) {
-  const int k = (int)(m->exports % m->K);
+  int k = 0;  // a dry run has no Adam: its slabs free at once and slab 0 is always taken
   m->exports++;
   const mth::BlockDesc& bd = m->lay[(size_t)j];
   logop(m, "G", "WAIT_BD", b, -1);
   if (m->live) CU(m, cudaStreamWaitEvent(m->sg, m->BD[b], 0));
+  if (m->live) OK(acquire_slab(m, &k));
   logop(m, "H", "ACQ_SLAB", k, -1);
-  if (m->live) OK(acquire_slab(m, k));
   logop(m, "G", "D2H", j, k);
   if (m->live) {
     CU(m, cudaMemcpyAsync(m->slabs + (size_t)k * m->wb_max, m->d.buf[b] + bd.region[1], (size_t)bd.wbytes,
@@ -826,6 +873,7 @@ mt_status mt_default_config(mt_config* c) {
   c->adam_eps = 1e-8f;
   c->seed = 1;
   c->timeout_ms = 60000;
+  c->keep_host_grad = 1;
   return MT_OK;
 }
 
@@ -1156,7 +1204,7 @@ mt_status mt_host_adam(int64_t n, const uint16_t* g, float* th, float* m, float*
   constexpr int64_t CH = 1 << 18;
   std::function<void(int64_t)> fn = [&](int64_t i) {
     const int64_t o = i * CH, len = (n - o) < CH ? (n - o) : CH;
-    mth::adam(len, g + o, th + o, m + o, v + o, w + o, t, lr, b1, b2, eps, wd);
+    mth::adam(len, g + o, nullptr, th + o, m + o, v + o, w + o, t, lr, b1, b2, eps, wd);
   };
   std::string err;
   const bool ok = pool.parallel_for((n + CH - 1) / CH, fn, &err);
@@ -1181,6 +1229,41 @@ int32_t mt_schedule(int32_t n, const double* b, const double* d, const double* c
                     double bw_d2h, double* stall) {
   if (!b || !d || !c || !a || !stall) return -1;
   return mth::schedule(n, b, d, c, a, bw_h2d, bw_d2h, stall);
+}
+
+mt_status mt_host_bandwidth(size_t bytes, int32_t n_threads, double* copy_gbs, double* adam_gelem_s) {
+  if (bytes < (1u << 20) || n_threads < 1) return MT_ERR_ARG;
+  const int64_t n = (int64_t)(bytes / 4);
+  std::vector<float> a((size_t)n, 1.0f), b((size_t)n, 0.0f);
+  std::vector<uint16_t> g((size_t)n, 0x3c00), w((size_t)n, 0);
+  std::vector<float> th((size_t)n, 0.01f), mv((size_t)n, 0.0f), vv((size_t)n, 0.0f);
+  mth::Pool pool;
+  pool.start(n_threads);
+  constexpr int64_t CH = 1 << 20;
+  const int64_t items = (n + CH - 1) / CH;
+  std::string err;
+  double best_copy = 1e30, best_adam = 1e30;
+  for (int rep = 0; rep < 3; ++rep) {
+    auto t0 = Clock::now();
+    std::function<void(int64_t)> cp = [&](int64_t i) {
+      const int64_t o = i * CH, len = (n - o) < CH ? (n - o) : CH;
+      std::memcpy(b.data() + o, a.data() + o, (size_t)len * 4);
+    };
+    pool.parallel_for(items, cp, &err);
+    best_copy = std::min(best_copy, std::chrono::duration<double>(Clock::now() - t0).count());
+    t0 = Clock::now();
+    std::function<void(int64_t)> ad = [&](int64_t i) {
+      const int64_t o = i * CH, len = (n - o) < CH ? (n - o) : CH;
+      mth::adam(len, g.data() + o, nullptr, th.data() + o, mv.data() + o, vv.data() + o, w.data() + o, rep + 1, 1e-3f,
+                0.9f, 0.999f, 1e-8f, 0.0f);
+    };
+    pool.parallel_for(items, ad, &err);
+    best_adam = std::min(best_adam, std::chrono::duration<double>(Clock::now() - t0).count());
+  }
+  pool.stop();
+  if (copy_gbs) *copy_gbs = 2.0 * (double)n * 4 / best_copy / 1e9;
+  if (adam_gelem_s) *adam_gelem_s = (double)n / best_adam / 1e9;
+  return MT_OK;
 }
 
 mt_status mt_token_csr(const int32_t* tok, int64_t T, int32_t V, int32_t* row_start, int32_t* rows) {

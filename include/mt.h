@@ -82,6 +82,8 @@ typedef struct {
                               1: register the whole store, copy directly    */
   int32_t head_chunk;      /* tokens per LM-head chunk; 0 = automatic        */
   int32_t log_protocol;    /* 1: keep the enqueue log (mt_protocol_log)      */
+  int32_t keep_host_grad;  /* 1: each slab is also unpacked into the store's
+                              BF16 G region; 0: Adam reads the slab only  */
 } mt_config;
 
 typedef struct { void* base; size_t bytes; } mt_dev_region;          /* caller-owned device memory  */
@@ -140,13 +142,16 @@ mt_status mt_step_forward(mt_model* model, const mt_layer_view* view);
  * even) straight into the buffer's gradient region at the flat layout
  * offsets; records Backward-Done.  Asynchronous. */
 mt_status mt_step_backward(mt_model* model, const mt_layer_view* view);
-/* Gradient stream: waits Backward-Done[buf], takes slab (export count mod K,
- * waiting on the host, bounded, until its previous Adam finished), copies the
- * gradient region into it, records Buffer-Free[buf] and the slab's event. */
+/* Gradient stream: waits Backward-Done[buf], takes a free slab (the
+ * lowest-numbered one; the host waits, bounded, while all K are held by
+ * pending Adam jobs), copies the gradient region into it, records
+ * Buffer-Free[buf] and the slab's event; *slab receives its index. */
 mt_status mt_stream_out(mt_model* model, int32_t block, int32_t buf, int32_t* slab);
 /* Queues block's host Adam: a worker waits (bounded) for the slab's event,
- * copies the slab into the block's G region, runs Adam (t = adam_step >= 1)
- * on master / m / v, rewrites W = bf16_rne(master) and releases the slab. */
+ * copies the slab into the block's G region (keep_host_grad), runs Adam
+ * (t = adam_step >= 1) on master / m / v, rewrites W = bf16_rne(master) and
+ * releases the slab.  Queued jobs run lowest block first: the next forward
+ * needs block 0 first although its gradient arrives last. */
 mt_status mt_adam_host(mt_model* model, int32_t block, int32_t slab, int32_t adam_step);
 /* One whole step (0-based index `step`, which must equal the number of steps
  * done) following the static schedule; *loss (if not null) receives the step
@@ -191,6 +196,10 @@ int64_t mt_plan_protocol(const mt_config* cfg, int32_t n_steps, char* buf, int64
  * returns the slab count needed, or -1. */
 int32_t mt_schedule(int32_t n_visits, const double* b, const double* d, const double* c,
                     const double* a, double bw_h2d, double bw_d2h, double* stall);
+/* Host memory bandwidth on this machine: a parallel copy of `bytes` (GB/s,
+ * read + write bytes) and the library's Adam (G elements/s) on n_threads
+ * threads; every pass runs 3 times and the best is reported. */
+mt_status mt_host_bandwidth(size_t bytes, int32_t n_threads, double* copy_gbs, double* adam_gelem_s);
 /* Per-vocabulary-row lists of token rows (CSR) used by the embedding
  * gradient: row_start[V+1], rows[T]. */
 mt_status mt_token_csr(const int32_t* tok, int64_t T, int32_t V, int32_t* row_start, int32_t* rows);

@@ -512,8 +512,10 @@ struct Model {
 //     index mod 2, restarting each step;
 //   * in a forward visit nothing is exported, so compute records Buffer-Free;
 //   * the embedding's backward reads no weights: its visit copies nothing;
-//   * slabs are taken round-robin (export count mod K) and the host waits for
-//     the chosen slab's previous Adam before reusing it;
+//   * an export takes a free slab and the host waits while none is free; which
+//     one is an allocation choice, so logs are compared modulo slab numbers and
+//     this simulator numbers them round-robin (export count mod K), one valid
+//     assignment;
 //   * the next step's stream-in of block j waits for block j's Adam;
 //   * with host-resident checkpoints, X_j (j < L) leaves on the idle gradient
 //     stream during the forward and returns on the weight stream, with the

@@ -148,3 +148,19 @@ def _buf_of(lines, ln):
         if p[1] == "G" and p[2] == "WAIT_BD":
             return int(p[3])
     raise AssertionError("export without Backward-Done wait")
+
+
+def mask_slabs(lines: list[str]) -> list[str]:
+    """The op list with slab numbers replaced by 'k'.  Which free slab an
+    export takes is an allocation choice (it depends on when host Adam jobs
+    finish); logs are compared modulo that choice and check() validates the
+    actual assignment."""
+    out = []
+    for l in lines:
+        step, s, op, a, b = l.split()
+        if op in ("ACQ_SLAB", "REC_SR"):
+            a = "k"
+        elif op in ("D2H", "ADAM_ENQ"):
+            b = "k"
+        out.append(" ".join((step, s, op, a, b)))
+    return out

@@ -87,7 +87,7 @@ def run_parity(orc, c, steps, **rt):
 def test_tiny_three_steps_parity(orc):
     c = configs.get("tiny")
     report, log = run_parity(orc, c, 3)
-    assert log == orc.protocol(oracle_shape(c), 3, 12, True, True)
+    assert protocol_check.mask_slabs(log) == protocol_check.mask_slabs(orc.protocol(oracle_shape(c), 3, 12, True, True))
     protocol_check.check(log)
     print("tiny parity", report)
 
@@ -95,7 +95,8 @@ def test_tiny_three_steps_parity(orc):
 def test_tiny_device_checkpoints_pinned_store_chunked_head(orc):
     c = configs.get("tiny")
     report, log = run_parity(orc, c, 2, ckpt_on_host=0, pin_store=1, head_chunk=128, n_grad_slabs=2)
-    assert log == orc.protocol(oracle_shape(c), 2, 2, False, False)
+    assert protocol_check.mask_slabs(log) == protocol_check.mask_slabs(orc.protocol(oracle_shape(c), 2, 2, False, False))
+    protocol_check.check(log)
 
 
 def test_gqa_shape_parity(orc):
