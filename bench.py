@@ -166,6 +166,23 @@ def cpu_sample(cfg_name, budget_s=20.0):
             "seconds": dt * n}
 
 
+def all_max(x: float, dist=None, device="cpu") -> float:
+    """Maximum of x over the ranks of the process group (x itself without one)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(t_step_local: float, tokens_per_step: int, world: int, dist=None, device="cpu"):
+    """Whole-job throughput of independent replicas: every rank trains its own
+    copy on its own tokens, so value = world x tokens / (slowest rank's step)."""
+    t = all_max(t_step_local, dist, device)
+    return world * tokens_per_step / t, t
+
+
 def workload_desc(name, c):
     return (f"{name}-shaped decoder: {c['n_layers']} layers, hidden {c['hidden']}, {c['n_heads']}x{c['head_dim']} "
             f"heads ({c['n_kv_heads']} KV), FFN {c['ffn']}, vocab {c['vocab']}, batch {c['batch']} x seq "
@@ -280,12 +297,7 @@ def main():
     kern = {name: m.timing_read(i) for i, name in enumerate(("gemm", "attn_fwd", "attn_bwd", "other"))}
     m.timing(False)
     st1 = m.stats()
-    t_step = max(dev_s, wall) / args.steps
-    if dist:
-        t = torch.tensor([t_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step = float(t.item())
-    value = world * T / t_step
+    value, t_step = aggregate(max(dev_s, wall) / args.steps, T, world, dist, "cuda")
 
     # ---------------- end to end: tokens uploaded and loss read back every step
     e2e = None
@@ -301,13 +313,10 @@ def main():
         m.sync()
         ev1.record(cs)
         torch.cuda.synchronize()
-        e2e_s = max(time.perf_counter() - w0, ev0.elapsed_time(ev1) / 1e3) / args.steps
+        e2e_v, e2e_s = aggregate(max(time.perf_counter() - w0, ev0.elapsed_time(ev1) / 1e3) / args.steps, T,
+                                 world, dist, "cuda")
         sh1 = m.stats()
-        if dist:
-            t = torch.tensor([e2e_s], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": world * T / e2e_s, "unit": "tokens/s",
+        e2e = {"value": e2e_v, "unit": "tokens/s",
                "h2d_bytes_per_step": int((sh1["h2d_bytes"] - sh0["h2d_bytes"]) / args.steps),
                "d2h_bytes_per_step": int((sh1["d2h_bytes"] - sh0["d2h_bytes"]) / args.steps)}
 

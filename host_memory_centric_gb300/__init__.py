@@ -126,6 +126,7 @@ def lib():
         "mt_embed_bwd": (i32, [_v, _v, _v, i32, i32, _v, _v]),
         "mt_cross_entropy": (i32, [_v, _v, i64, i32, f32, _v, _v]),
         "mt_kernel_error": (i32, [_P(i32), i32]),
+        "mt_fault_inject": (i32, [i32, i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)

@@ -405,6 +405,20 @@ cudaError_t bwd_t(const bf16* qkv, const bf16* o, const float* lse, const bf16* 
   return f32_to_bf16_2d(dq_acc, (int64_t)nh * HD, T, (int64_t)nh * HD, dqkv, (int64_t)(nh + 2 * nkv) * HD, 1.f, s);
 }
 
+template <int HD>
+cudaError_t bwd_tc(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, int n_seq, int S, int nh,
+                   int nkv, bf16* dqkv, float* delta, float* dq_acc, cudaStream_t s) {
+  const int64_t T = (int64_t)n_seq * S;
+  cudaError_t e = cudaMemsetAsync(dq_acc, 0, (size_t)T * nh * HD * sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  attn_delta_k<HD><<<(unsigned)((T * nh * 32 + 255) / 256), 256, 0, s>>>(o, dout, T, nh, delta);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = attention_bwd_tc_core(qkv, dout, lse, delta, n_seq, S, nh, nkv, HD, dqkv, dq_acc, s);
+  if (e != cudaSuccess) return e;
+  return f32_to_bf16_2d(dq_acc, (int64_t)nh * HD, T, (int64_t)nh * HD, dqkv, (int64_t)(nh + 2 * nkv) * HD, 1.f, s);
+}
+
 }  // namespace
 
 cudaError_t attention_fwd(const bf16* qkv, int n_seq, int S, int nh, int nkv, int hd, bf16* o, float* lse,
@@ -428,6 +442,16 @@ cudaError_t attention_bwd(const bf16* qkv, const bf16* o, const float* lse, cons
   if (n_seq <= 0 || S <= 0) return cudaSuccess;
   if (nh % nkv || !al16(qkv) || !al16(o) || !al16(dout) || !al16(dqkv) || n_seq > 65535 || nkv > 65535)
     return cudaErrorInvalidValue;
+  if (hd == 64) return bwd_tc<64>(qkv, o, lse, dout, n_seq, S, nh, nkv, dqkv, delta, dq_acc, s);
+  if (hd == 128) return bwd_tc<128>(qkv, o, lse, dout, n_seq, S, nh, nkv, dqkv, delta, dq_acc, s);
+  return cudaErrorInvalidValue;
+}
+
+// Warp-level (mma.sync) backward, the reference the tensor-core backward was
+// validated against.
+cudaError_t attention_bwd_warp(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, int n_seq, int S,
+                               int nh, int nkv, int hd, bf16* dqkv, float* delta, float* dq_acc, cudaStream_t s) {
+  if (n_seq <= 0 || S <= 0) return cudaSuccess;
   if (hd == 64) return bwd_t<64>(qkv, o, lse, dout, n_seq, S, nh, nkv, dqkv, delta, dq_acc, s);
   if (hd == 128) return bwd_t<128>(qkv, o, lse, dout, n_seq, S, nh, nkv, dqkv, delta, dq_acc, s);
   return cudaErrorInvalidValue;

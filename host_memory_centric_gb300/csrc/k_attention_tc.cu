@@ -386,6 +386,284 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Backward.  One CTA per (128 keys, kv head, sequence); it loops over the
+// query heads sharing the kv head and over the query tiles from the diagonal
+// down.  Per (head, query tile):
+//   MMA   S^T = K Q^T and dP^T = V dO^T into TMEM (M = 128 keys, N = 128 q);
+//   rows  (one thread per key) P^T = exp2(S^T scale - lse2) masked causally,
+//         dS^T = P^T (dP^T - delta); both written as BF16 into 128B-swizzled
+//         shared tiles laid out [key][q];
+//   MMA   dV += P^T dO and dK += dS^T Q (TMEM accumulators kept for the whole
+//         CTA), and dQ = dS K into the columns S^T used, reading the same
+//         [key][q] tile as an MN-major operand (dS = (dS^T)^T) and the K tile
+//         as an MN-major operand;
+//   rows  (one thread per query) dQ rows from TMEM added into the FP32 dQ
+//         accumulator in global memory.
+// TMEM: S^T | dP^T | dV | dK = 512 columns at hd = 128.
+template <int HD>
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_bwd_tc_k(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo, int S, int nh,
+                  int nkv, const float* __restrict__ lse, const float* __restrict__ delta, float scale,
+                  float scale_log2, bf16* __restrict__ dqkv, float* __restrict__ dq_acc) {
+  constexpr int NC = HD / 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = sm;
+  uint8_t* sV = sK + NC * CH;
+  uint8_t* sQ = sV + NC * CH;
+  uint8_t* sO = sQ + NC * CH;  // dO tile
+  uint8_t* sP = sO + NC * CH;  // P^T  [key][q], 2 chunks of 64 q
+  uint8_t* sD = sP + 2 * CH;   // dS^T [key][q]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sD + 2 * CH);
+  uint64_t* kv_full = bars;
+  uint64_t* qdo_full = bars + 1;
+  uint64_t* qdo_empty = bars + 2;
+  uint64_t* s_full = bars + 3;
+  uint64_t* p_full = bars + 4;
+  uint64_t* q_done = bars + 5;
+  uint64_t* st_free = bars + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kb = blockIdx.x, g = blockIdx.y, n = blockIdx.z;
+  const int grp = nh / nkv;
+  const int nqb = (S + 127) / 128;
+  const int per_head = nqb - kb;
+  const int iters = grp * per_head;
+  const int k0 = kb * 128;
+  const int row0 = n * S;
+  const int64_t T = (int64_t)gridDim.z * S;
+  const int64_t ld = (int64_t)(nh + 2 * nkv) * HD;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(qdo_full, 1);
+    mbar_init(qdo_empty, 1);
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(q_done, 1);
+    mbar_init(st_free, 128);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tq) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tdo) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                 "r"(512));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tSt = tmem, tdPt = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + HD;
+  bool kv_inflight = false, qdo_inflight = false;
+  uint32_t qdo_par = 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      mbar_expect_tx(kv_full, 2 * NC * CH);
+      for (int c = 0; c < NC; ++c) {
+        tma_load(&tq, kv_full, sK + c * CH, (nh + g) * HD + 64 * c, row0 + k0);
+        tma_load(&tq, kv_full, sV + c * CH, (nh + nkv + g) * HD + 64 * c, row0 + k0);
+      }
+      kv_inflight = true;
+      for (int i = 0; i < iters && ok; ++i) {
+        const int h = g * grp + i / per_head, q0 = (kb + i % per_head) * 128;
+        if (!mbar_wait(qdo_empty, (uint32_t)((i & 1) ^ 1), abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(qdo_full, 2 * NC * CH);
+        for (int c = 0; c < NC; ++c) {
+          tma_load(&tq, qdo_full, sQ + c * CH, h * HD + 64 * c, row0 + q0);
+          tma_load(&tdo, qdo_full, sO + c * CH, h * HD + 64 * c, row0 + q0);
+        }
+        qdo_inflight = true;
+        qdo_par = (uint32_t)(i & 1);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicCAS(&g_attn_error, 0, 21);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = mbar_wait(kv_full, 0, abort_flag);
+      constexpr uint32_t I_S = idesc(128, 128, false, false);
+      constexpr uint32_t I_KV = idesc(128, HD, false, true);  // dV, dK: B = dO / Q as MN-major
+      constexpr uint32_t I_Q = idesc(128, HD, true, true);    // dQ: A = dS (MN-major), B = K (MN-major)
+      const uint32_t aK = su32(sK), aV = su32(sV), aQ = su32(sQ), aO = su32(sO), aP = su32(sP), aD = su32(sD);
+      for (int i = 0; i < iters && ok; ++i) {
+        const uint32_t par = (uint32_t)(i & 1);
+        if (!mbar_wait(qdo_full, par, abort_flag) || !mbar_wait(st_free, par ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t off = c * CH + k * 32;
+            tc_mma(tSt, sdesc(aK + off, 16, 1024), sdesc(aQ + off, 16, 1024), I_S, (c | k) != 0);
+            tc_mma(tdPt, sdesc(aV + off, 16, 1024), sdesc(aO + off, 16, 1024), I_S, (c | k) != 0);
+          }
+        tc_commit(s_full);
+        if (!mbar_wait(p_full, par, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t pa = (kk >> 2) * CH + (kk & 3) * 32;  // K-major over q
+          const uint32_t rows = kk * 16 * 128;                 // 16 rows of an MN-major tile
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          tc_mma(tdV, sdesc(aP + pa, 16, 1024), sdesc(aO + rows, CH, 1024), I_KV, acc);
+          tc_mma(tdK, sdesc(aD + pa, 16, 1024), sdesc(aQ + rows, CH, 1024), I_KV, acc);
+          tc_mma(tSt, sdesc(aD + rows, CH, 1024), sdesc(aK + rows, CH, 1024), I_Q, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(q_done);
+        tc_commit(qdo_empty);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicCAS(&g_attn_error, 0, 22);
+      }
+    }
+  } else {
+    const int qw = warp & 3;
+    const int r = qw * 32 + lane;  // key row (S^T, dP^T, dV, dK) or query row (dQ)
+    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+    const int key = k0 + r;
+    uint8_t* prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
+    uint8_t* drow = sD + (r >> 3) * 1024 + (r & 7) * 128;
+    bool ok = true;
+    for (int i = 0; i < iters; ++i) {
+      const int h = g * grp + i / per_head, q0 = (kb + i % per_head) * 128;
+      const uint32_t par = (uint32_t)(i & 1);
+      // LSE and delta of this query tile: every row thread reads all 128 (the
+      // same addresses across the warp, served from L1); no block barrier, so
+      // an aborting warp can never leave the others waiting
+      const float* lse_h = lse + (int64_t)h * T + row0;
+      const float* dl_h = delta + (int64_t)h * T + row0;
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full, par, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float st[32], dp[32];
+        tmem_ld32(tSt + lane_off + c * 32, st);
+        tmem_ld32(tdPt + lane_off + c * 32, dp);
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int ql = c * 32 + e + t;
+            const int q = q0 + ql;
+            float p = 0.f, dq = 0.f;
+            if (q >= key && q < S) {
+              p = exp2f(st[e + t] * scale_log2 - lse_h[q] * 1.4426950408889634f);
+              dq = p * (dp[e + t] - dl_h[q]);
+            }
+            pv[t] = p;
+            dv[t] = dq;
+          }
+          pw[e / 2] = pack2(pv[0], pv[1]);
+          dw[e / 2] = pack2(dv[0], dv[1]);
+        }
+        // 32 queries = 4 sixteen-byte units of row r in q-chunk c/2
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+          const int unit = (c & 1) * 4 + u4;
+          const int off = (c >> 1) * CH + ((unit ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(prow + off) = make_uint4(pw[4 * u4], pw[4 * u4 + 1], pw[4 * u4 + 2], pw[4 * u4 + 3]);
+          *reinterpret_cast<uint4*>(drow + off) = make_uint4(dw[4 * u4], dw[4 * u4 + 1], dw[4 * u4 + 2], dw[4 * u4 + 3]);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(p_full);
+      if (!__all_sync(0xffffffffu, mbar_wait(q_done, par, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int q = q0 + r;
+      float* dst = dq_acc + ((int64_t)row0 + q) * ((int64_t)nh * HD) + (int64_t)h * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        float t[32];
+        tmem_ld32(tSt + lane_off + c * 32, t);
+        if (q < S) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + e),
+                      make_float4(t[e] * scale, t[e + 1] * scale, t[e + 2] * scale, t[e + 3] * scale));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(st_free);
+    }
+    if (ok) {
+      // dK, dV of this thread's key row (complete after the last q_done).  The
+      // TMEM loads are warp-collective: every lane loads, only valid rows store.
+      tc_fence_after();
+      const bool valid = key < S;
+      bf16* row = dqkv + ((int64_t)row0 + (valid ? key : 0)) * ld;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        float t[32];
+        tmem_ld32(tdK + lane_off + c * 32, t);
+        if (valid) {
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4)
+            reinterpret_cast<uint4*>(row + (int64_t)(nh + g) * HD + c * 32)[i4] = make_uint4(
+                pack2(t[8 * i4] * scale, t[8 * i4 + 1] * scale), pack2(t[8 * i4 + 2] * scale, t[8 * i4 + 3] * scale),
+                pack2(t[8 * i4 + 4] * scale, t[8 * i4 + 5] * scale), pack2(t[8 * i4 + 6] * scale, t[8 * i4 + 7] * scale));
+        }
+        tmem_ld32(tdV + lane_off + c * 32, t);
+        if (valid) {
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4)
+            reinterpret_cast<uint4*>(row + (int64_t)(nh + nkv + g) * HD + c * 32)[i4] =
+                make_uint4(pack2(t[8 * i4], t[8 * i4 + 1]), pack2(t[8 * i4 + 2], t[8 * i4 + 3]),
+                           pack2(t[8 * i4 + 4], t[8 * i4 + 5]), pack2(t[8 * i4 + 6], t[8 * i4 + 7]));
+        }
+      }
+    } else if (lane == 0) {
+      *abort_flag = 1;
+      atomicCAS(&g_attn_error, 0, 23);
+    }
+  }
+
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    const long long t0 = clock64();
+    if (kv_inflight)
+      while (!mbar_test(kv_full, 0) && clock64() - t0 < kWaitCycles) {
+      }
+    if (qdo_inflight)
+      while (!mbar_test(qdo_full, qdo_par) && clock64() - t0 < kWaitCycles) {
+      }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
 cudaError_t g_init = cudaSuccess;
@@ -428,7 +706,57 @@ cudaError_t launch(const bf16* qkv, int n_seq, int S, int nh, int nkv, bf16* o, 
   return cudaGetLastError();
 }
 
+template <int HD>
+constexpr int bwd_smem_bytes() {
+  return (HD / 64) * 16384 * 4 + 4 * 16384 + 1024 + 1024 + 256;
+}
+
+bool make_map128(CUtensorMap* m, const bf16* base, int64_t ld, int64_t rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<bf16*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int HD>
+cudaError_t launch_bwd(const bf16* qkv, const bf16* dout, const float* lse, const float* delta, int n_seq, int S,
+                       int nh, int nkv, bf16* dqkv, float* dq_acc, cudaStream_t s) {
+  const int64_t T = (int64_t)n_seq * S;
+  CUtensorMap mq, mo;
+  if (!make_map128(&mq, qkv, (int64_t)(nh + 2 * nkv) * HD, T) || !make_map128(&mo, dout, (int64_t)nh * HD, T))
+    return cudaErrorInvalidValue;
+  constexpr int SM = bwd_smem_bytes<HD>();
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_tc_k<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SM);
+  if (e != cudaSuccess) return e;
+  const float scale = 1.f / sqrtf((float)HD);
+  dim3 grid((S + 127) / 128, nkv, n_seq);
+  attn_bwd_tc_k<HD><<<grid, THREADS, SM, s>>>(mq, mo, S, nh, nkv, lse, delta, scale, scale * 1.4426950408889634f,
+                                              dqkv, dq_acc);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+// Tensor-core attention backward core: dK and dV into dqkv (BF16), dQ added
+// (already scaled) into the zeroed FP32 dq_acc ([T][nh*hd]).  delta[h][t] =
+// rowsum(dO o O) must be precomputed.
+cudaError_t attention_bwd_tc_core(const bf16* qkv, const bf16* dout, const float* lse, const float* delta,
+                                  int n_seq, int S, int nh, int nkv, int hd, bf16* dqkv, float* dq_acc,
+                                  cudaStream_t s) {
+  std::call_once(g_once, init_once);
+  if (g_init != cudaSuccess) return g_init;
+  if (n_seq <= 0 || S <= 0) return cudaSuccess;
+  if (nh % nkv || n_seq > 65535 || nkv > 65535 || (int64_t)n_seq * S > 0x7fffffff) return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dqkv) |
+       reinterpret_cast<uintptr_t>(dq_acc)) & 15)
+    return cudaErrorInvalidValue;
+  if (hd == 64) return launch_bwd<64>(qkv, dout, lse, delta, n_seq, S, nh, nkv, dqkv, dq_acc, s);
+  if (hd == 128) return launch_bwd<128>(qkv, dout, lse, delta, n_seq, S, nh, nkv, dqkv, dq_acc, s);
+  return cudaErrorInvalidValue;
+}
 
 // Tensor-core attention forward (see the file comment).  Same contract as
 // attention_fwd; requires hd in {64, 128}, 16-byte aligned qkv and o.

@@ -22,6 +22,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "mt_kernels.h"
@@ -48,6 +49,7 @@ struct Epi {
   float* Dacc; int64_t ldacc; int acc_mode;
   int M, N, K;
   int tiles_m, tiles_n, group_m;
+  int stall;  // test hook: the producer issues nothing, so the consumers' bounded waits run out
 };
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int tile = blockIdx.x; tile < num_tiles && ok && !e.stall; tile += gridDim.x) {
         int tm, tn;
         tile_mn(tile, e, tm, tn);
         for (int kb = 0; kb < nk; ++kb) {
@@ -430,6 +432,15 @@ inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) =
 
 }  // namespace
 
+std::atomic<int> g_stall_next{0};
+int gemm_stall_take() {
+  int v = g_stall_next.load();
+  while (v > 0 && !g_stall_next.compare_exchange_weak(v, v - 1)) {
+  }
+  return v > 0 ? 1 : 0;
+}
+void gemm_inject_stall(int launches) { g_stall_next = launches; }
+
 int gemm_num_sms() {
   std::call_once(g_once, init_once);
   return g_num_sms;
@@ -456,6 +467,7 @@ cudaError_t gemm(const GemmArgs& g, cudaStream_t s) {
   e.tiles_m = (g.M + BM - 1) / BM;
   e.tiles_n = (g.N + BN - 1) / BN;
   e.group_m = 16;
+  e.stall = gemm_stall_take();
   const int tiles = e.tiles_m * e.tiles_n;
   const int grid = tiles < g_num_sms ? tiles : g_num_sms;
   if (!g.a_mn && !g.b_mn) gemm_kernel<false, false><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, e);

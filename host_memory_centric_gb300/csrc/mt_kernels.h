@@ -31,6 +31,10 @@ struct GemmArgs {
 };
 cudaError_t gemm(const GemmArgs& g, cudaStream_t s);
 int gemm_num_sms();
+// Test hook: the next `launches` GEMM launches issue no loads, so their bounded
+// waits expire and they report through the kernel error word.
+void gemm_inject_stall(int launches);
+int gemm_stall_take();
 
 // Device-side error word written by kernels whose bounded waits expired
 // (0 = none; the GEMM's and the tensor-core attention's).  Read / cleared by
@@ -92,6 +96,12 @@ cudaError_t attention_fwd(const bf16* qkv, int n_seq, int S, int nh, int nkv, in
 // attention_fwd).
 cudaError_t attention_fwd_tc(const bf16* qkv, int n_seq, int S, int nh, int nkv, int hd, bf16* o, float* lse,
                              cudaStream_t s);
+// Tensor-core backward core (dK, dV into dqkv; scaled dQ added into the
+// zeroed FP32 dq_acc); delta = rowsum(dO o O) precomputed.  Used by
+// attention_bwd.
+cudaError_t attention_bwd_tc_core(const bf16* qkv, const bf16* dout, const float* lse, const float* delta,
+                                  int n_seq, int S, int nh, int nkv, int hd, bf16* dqkv, float* dq_acc,
+                                  cudaStream_t s);
 // Backward: dqkv ([T][(nh+2nkv)hd]) receives dq, dk, dv.  delta ([nh][T]) and
 // dq_acc ([T][nh*hd] fp32) are scratch.
 cudaError_t attention_bwd(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout,

@@ -25,6 +25,7 @@
 #include <algorithm>
 #include <cstring>
 #include <memory>
+#include <stdexcept>
 
 #include "mt_host.h"
 #include "mt_kernels.h"
@@ -33,6 +34,18 @@ using mt::bf16;
 using Clock = std::chrono::steady_clock;
 
 namespace {
+
+// test-only host fault injection (mt_fault_inject)
+std::atomic<int> g_inj_adam_delay_ms{0}, g_inj_adam_throw{0}, g_inj_pinned_fail{0};
+
+cudaError_t pinned_alloc(void** p, size_t bytes) {
+  if (g_inj_pinned_fail.load() > 0) {
+    g_inj_pinned_fail--;
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaHostAlloc(p, bytes, cudaHostAllocDefault);
+}
 
 struct Job {
   int32_t block, slab, t;
@@ -503,6 +516,7 @@ void adam_loop(mt_model* m) {
       continue;
     }
     idle = false;
+    if (const int d = g_inj_adam_delay_ms.load()) std::this_thread::sleep_for(std::chrono::milliseconds(d));
     const auto t0 = Clock::now();
     mt_status st = m->failed ? MT_ERR_STATE : wait_event(m, m->SR[(size_t)job.slab], "slab ready");
     if (st == MT_OK) {
@@ -522,7 +536,13 @@ void adam_loop(mt_model* m) {
         for (int64_t e = 0; e < n; e += CH) items.push_back({o + e, (n - e) < CH ? (n - e) : CH});
       }
       const mt_config& c = m->c;
+      bool inject_throw = false;
+      if (g_inj_adam_throw.load() > 0) {
+        g_inj_adam_throw--;
+        inject_throw = true;
+      }
       std::function<void(int64_t)> fn = [&](int64_t i) {
+        if (inject_throw && i == 0) throw std::runtime_error("injected host worker fault");
         const int64_t o = items[(size_t)i].first, n = items[(size_t)i].second;
         mth::adam(n, slab + o, c.keep_host_grad ? G + o : nullptr, th + o, mm + o, vv + o, W + o, job.t, c.lr,
                   c.beta1, c.beta2, c.adam_eps, c.weight_decay);
@@ -948,22 +968,22 @@ mt_status mt_init_model(const mt_config* c, mt_dev_region dev, mt_streams s, mt_
     m->registered = true;
   } else {
     for (int b = 0; b < 2; ++b) {
-      if (cudaHostAlloc((void**)&m->staging[b], (size_t)m->wb_max, cudaHostAllocDefault) != cudaSuccess)
+      if (pinned_alloc((void**)&m->staging[b], (size_t)m->wb_max) != cudaSuccess)
         return MT_ERR_HOST_OOM;
       m->pinned_bytes += (size_t)m->wb_max;
     }
   }
-  if (cudaHostAlloc((void**)&m->slabs, (size_t)m->wb_max * m->K, cudaHostAllocDefault) != cudaSuccess)
+  if (pinned_alloc((void**)&m->slabs, (size_t)m->wb_max * m->K) != cudaSuccess)
     return MT_ERR_HOST_OOM;
   m->pinned_bytes += (size_t)m->wb_max * m->K;
   if (c->ckpt_on_host) {
     const size_t bytes = (size_t)m->L * m->T * m->H * 2;
-    if (cudaHostAlloc((void**)&m->ckpt, bytes, cudaHostAllocDefault) != cudaSuccess) return MT_ERR_HOST_OOM;
+    if (pinned_alloc((void**)&m->ckpt, bytes) != cudaSuccess) return MT_ERR_HOST_OOM;
     m->pinned_bytes += bytes;
   }
   const size_t tokb = (size_t)(3 * m->T + m->V + 1) * 4;
-  if (cudaHostAlloc((void**)&m->htok, tokb, cudaHostAllocDefault) != cudaSuccess) return MT_ERR_HOST_OOM;
-  if (cudaHostAlloc((void**)&m->hloss, 64, cudaHostAllocDefault) != cudaSuccess) return MT_ERR_HOST_OOM;
+  if (pinned_alloc((void**)&m->htok, tokb) != cudaSuccess) return MT_ERR_HOST_OOM;
+  if (pinned_alloc((void**)&m->hloss, 64) != cudaSuccess) return MT_ERR_HOST_OOM;
   m->pinned_bytes += tokb + 64;
 
   for (cudaEvent_t* e : {&m->WR[0], &m->WR[1], &m->BD[0], &m->BD[1], &m->BF[0], &m->BF[1], &m->XR[0], &m->XR[1],
@@ -1400,6 +1420,17 @@ mt_status mt_cross_entropy(void* logits, const int32_t* target, int64_t rows, in
                            float* row_loss, void* stream) {
   if (!logits || !target || !row_loss) return MT_ERR_ARG;
   return cu_status(mt::cross_entropy((bf16*)logits, target, rows, V, inv_norm, row_loss, (cudaStream_t)stream));
+}
+
+mt_status mt_fault_inject(int32_t kind, int32_t value) {
+  if (value < 0) return MT_ERR_ARG;
+  switch (kind) {
+    case 1: g_inj_adam_delay_ms = value; return MT_OK;
+    case 2: g_inj_adam_throw = value; return MT_OK;
+    case 3: g_inj_pinned_fail = value; return MT_OK;
+    case 4: mt::gemm_inject_stall(value); return MT_OK;
+    default: return MT_ERR_ARG;
+  }
 }
 
 mt_status mt_kernel_error(int32_t* code, int32_t clear) {

@@ -282,6 +282,15 @@ mt_status mt_timing_read(mt_model* model, int32_t kind, int64_t* launches, doubl
 mt_status mt_rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* gamma,
                                  const float* rstd, const void* dres, int64_t T, int32_t H,
                                  void* dx, void* dgamma, void* stream);
+/* Host-side fault injection for failure-detection tests (process-wide):
+ * kind 1 = every Adam job sleeps `value` ms before it starts (a stalled
+ * worker); kind 2 = the next `value` Adam jobs throw inside a worker; kind 3 =
+ * the next `value` pinned host allocations fail; kind 4 = the next `value`
+ * GEMM launches issue no loads, so the kernel's bounded mbarrier waits run
+ * out (about 2 s), it records code 2 in the kernel error word and returns
+ * with the context intact.  value 0 clears the kind.  No kind faults, traps
+ * or hangs a GPU. */
+mt_status mt_fault_inject(int32_t kind, int32_t value);
 /* Error word of the kernels' bounded waits (0 = none); clear != 0 resets it. */
 mt_status mt_kernel_error(int32_t* code, int32_t clear);
 
