@@ -166,6 +166,28 @@ def cpu_sample(cfg_name, budget_s=20.0):
             "seconds": dt * n}
 
 
+def mem_available_bytes() -> int:
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def host_bytes_needed(c: dict, slabs: int, ckpt_on_host: int) -> int:
+    """Host RAM one replica allocates: the flat store, the pinned gradient
+    slabs (largest block's gradient region each) and the checkpoints."""
+    import ctypes
+    import host_memory_centric_gb300 as mt
+    cfg = mt.make_config(c)
+    store = mt.lib().mt_store_bytes(ctypes.byref(cfg))
+    wb = max(2 * b["n_pad"] for b in mt.layout(cfg))
+    ckpt = c["n_layers"] * c["micro"] * c["batch"] * c["seq"] * c["hidden"] * 2 if ckpt_on_host else 0
+    return int(store + slabs * wb + 2 * wb + ckpt)
+
+
 def all_max(x: float, dist=None, device="cpu") -> float:
     """Maximum of x over the ranks of the process group (x itself without one)."""
     if dist is None:
@@ -257,6 +279,17 @@ def main():
     c = configs.get(args.config)
     T = c["micro"] * c["batch"] * c["seq"]
     P, F_exec, F_pages = model_numbers(c)
+    # every replica on this host holds its own host state: refuse to start
+    # rather than exhaust host RAM
+    local_world = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    need = local_world * host_bytes_needed(c, args.slabs, args.ckpt_on_host)
+    avail = mem_available_bytes()
+    if avail and need > 0.85 * avail:
+        msg = (f"{local_world} replica(s) of the {args.config} workload need {need / 1e9:.1f} GB of host RAM; "
+               f"{avail / 1e9:.1f} GB available")
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "error": msg, "n_gpus": world}), flush=True)
+        sys.exit(2)
     pk = peaks()
     bw = link_bandwidth(torch)
 
