@@ -113,6 +113,8 @@ def lib():
         "mt_timing": (i32, [_v, i32]),
         "mt_timing_read": (i32, [_v, i32, _P(i64), _P(f64), _P(f64), _P(f64)]),
         "mt_gemm": (i32, [_v, i64, i32, _v, i64, i32, i32, i32, i32, _v, i64, _v, i64, _v, i64, i32, _v]),
+        "mt_gemm2": (i32, [_P(_v), _P(i64), _P(i32), _P(_v), _P(i64), _P(i32), _P(i32), _P(i32), _P(i32),
+                            _P(_v), _P(i64), _v]),
         "mt_rmsnorm_fwd": (i32, [_v, _v, i64, i32, f32, _v, _v, _v]),
         "mt_rmsnorm_bwd": (i32, [_v, _v, _v, _v, _v, i64, i32, _v, _v, _v, sz, _v]),
         "mt_rmsnorm_bwd_scratch_bytes": (sz, [i64, i32]),

@@ -290,23 +290,35 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(&s_empty[b]);
       const int kbase = 128 * j;
-      float mx = m_old;
+      // only the diagonal tile and a tile crossing the sequence end need masking
+      const bool need_mask = (kbase + 127 > q0) || (kbase + 128 > S);
+      if (need_mask) {
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        const int key = kbase + i;
-        float v = s[i] * scale_log2;
-        if (key > qpos || key >= S) v = -INFINITY;
-        s[i] = v;
-        mx = fmaxf(mx, v);
+        for (int i = 0; i < 128; ++i) {
+          const int key = kbase + i;
+          s[i] = (key > qpos || key >= S) ? -INFINITY : s[i] * scale_log2;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] *= scale_log2;
       }
+      // eight independent chains instead of one 128-long dependency chain
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = m_old;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], s[i]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float base = mx == -INFINITY ? 0.f : mx;
       const float alpha = exp2f(m_old - base);  // 0 when m_old = -inf
-      float sum = 0.f;
+      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < 128; ++i) {
         s[i] = exp2f(s[i] - base);
-        sum += s[i];
+        sum8[i & 7] += s[i];
       }
+      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       l = l * alpha + sum;
       // P_{j-1} consumed and O written by the previous PV before we touch them
       if (j > 0) {
@@ -416,7 +428,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sO = sQ + NC * CH;  // dO tile
   uint8_t* sP = sO + NC * CH;  // P^T  [key][q], 2 chunks of 64 q
   uint8_t* sD = sP + 2 * CH;   // dS^T [key][q]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sD + 2 * CH);
+  float* lse_s = reinterpret_cast<float*>(sD + 2 * CH);  // [128] log2-scaled LSE of the q tile
+  float* dl_s = lse_s + 128;                               // [128] delta of the q tile
+  uint64_t* bars = reinterpret_cast<uint64_t*>(dl_s + 128);
   uint64_t* kv_full = bars;
   uint64_t* qdo_full = bars + 1;
   uint64_t* qdo_empty = bars + 2;
@@ -424,7 +438,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* p_full = bars + 4;
   uint64_t* q_done = bars + 5;
   uint64_t* st_free = bars + 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
+  uint64_t* ld_ready = bars + 7;  // the row warps' LSE / delta stores of this tile are done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -446,6 +461,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(p_full, 128);
     mbar_init(q_done, 1);
     mbar_init(st_free, 128);
+    mbar_init(ld_ready, 128);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tq) : "memory");
@@ -548,11 +564,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < iters; ++i) {
       const int h = g * grp + i / per_head, q0 = (kb + i % per_head) * 128;
       const uint32_t par = (uint32_t)(i & 1);
-      // LSE and delta of this query tile: every row thread reads all 128 (the
-      // same addresses across the warp, served from L1); no block barrier, so
-      // an aborting warp can never leave the others waiting
-      const float* lse_h = lse + (int64_t)h * T + row0;
-      const float* dl_h = delta + (int64_t)h * T + row0;
+      // LSE and delta of this query tile into shared memory: thread t loads
+      // entry t, then all wait (bounded) until the 128 stores are done.  The
+      // previous tile's readers finished before its p_full, which this
+      // thread's q_done wait already ordered before these stores.
+      {
+        const int t = threadIdx.x - 64;
+        const int q = q0 + t;
+        lse_s[t] = q < S ? lse[(int64_t)h * T + row0 + q] * 1.4426950408889634f : 0.f;
+        dl_s[t] = q < S ? delta[(int64_t)h * T + row0 + q] : 0.f;
+        mbar_arrive(ld_ready);
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(ld_ready, par, abort_flag))) {
+        ok = false;
+        break;
+      }
+      const bool need_mask = (q0 < k0 + 127) || (q0 + 128 > S);
       if (!__all_sync(0xffffffffu, mbar_wait(s_full, par, abort_flag))) {
         ok = false;
         break;
@@ -570,14 +597,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             const int ql = c * 32 + e + t;
-            const int q = q0 + ql;
-            float p = 0.f, dq = 0.f;
-            if (q >= key && q < S) {
-              p = exp2f(st[e + t] * scale_log2 - lse_h[q] * 1.4426950408889634f);
-              dq = p * (dp[e + t] - dl_h[q]);
+            float p = exp2f(st[e + t] * scale_log2 - lse_s[ql]);
+            if (need_mask) {
+              const int q = q0 + ql;
+              if (q < key || q >= S) p = 0.f;
             }
             pv[t] = p;
-            dv[t] = dq;
+            dv[t] = p * (dp[e + t] - dl_s[ql]);
           }
           pw[e / 2] = pack2(pv[0], pv[1]);
           dw[e / 2] = pack2(dv[0], dv[1]);

@@ -23,6 +23,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cstring>
 #include <mutex>
 
 #include "mt_kernels.h"
@@ -49,7 +50,18 @@ struct Epi {
   float* Dacc; int64_t ldacc; int acc_mode;
   int M, N, K;
   int tiles_m, tiles_n, group_m;
-  int stall;  // test hook: the producer issues nothing, so the consumers' bounded waits run out
+  int a_mn, b_mn;
+};
+
+// Up to two independent GEMMs ("groups") share one persistent launch: their
+// output tiles form one list, so the tail of one fills SMs the other leaves
+// idle.
+struct Params {
+  CUtensorMap ta[2], tb[2];
+  Epi e[2];
+  int ngroups;
+  int tile_start[3];  // tiles of group g are [tile_start[g], tile_start[g+1])
+  int stall;          // test hook: the producer issues nothing, so the consumers' bounded waits run out
 };
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
@@ -141,6 +153,7 @@ __host__ __device__ constexpr uint32_t idesc(bool a_mn, bool b_mn) {
          ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
+
 __device__ __forceinline__ void tile_mn(int tile, const Epi& e, int& tm, int& tn) {
   const int per_group = e.group_m * e.tiles_n;
   const int first = (tile / per_group) * e.group_m;
@@ -214,10 +227,80 @@ __device__ __forceinline__ void epi_store(const Epi& e, int row, int col, const 
   }
 }
 
+// Producer side of one output tile: its K-blocks into the shared-memory ring.
 template <bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const Epi e) {
+__device__ __forceinline__ bool produce_tile(const CUtensorMap* tmA, const CUtensorMap* tmB, int tm, int tn, int nk,
+                                             uint8_t* sA, uint8_t* sB, uint64_t* full, uint64_t* empty, int& stage,
+                                             uint32_t& phase, volatile int* abort_flag, uint32_t& inflight_mask,
+                                             uint32_t& inflight_parity) {
+  for (int kb = 0; kb < nk; ++kb) {
+    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) return false;
+    mbar_expect_tx(&full[stage], STAGE_BYTES);
+    uint8_t* a = sA + stage * A_BYTES;
+    uint8_t* b = sB + stage * B_BYTES;
+    const int k0 = kb * BK;
+    if (!A_MN) {
+      tma_load(tmA, &full[stage], a, k0, tm * BM);
+    } else {
+      tma_load(tmA, &full[stage], a, tm * BM, k0);
+      tma_load(tmA, &full[stage], a + CHUNK_BYTES, tm * BM + 64, k0);
+    }
+    if (!B_MN) {
+      tma_load(tmB, &full[stage], b, k0, tn * BN);
+    } else {
+#pragma unroll
+      for (int c = 0; c < BN / 64; ++c) tma_load(tmB, &full[stage], b + c * CHUNK_BYTES, tn * BN + 64 * c, k0);
+    }
+    inflight_mask |= 1u << stage;
+    inflight_parity = (inflight_parity & ~(1u << stage)) | (phase << stage);
+    if (++stage == STAGES) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+  return true;
+}
+
+// MMA side of one output tile: nk K-blocks accumulated into TMEM column d.
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ bool mma_tile(uint32_t d, int nk, uint8_t* sA, uint8_t* sB, uint64_t* full,
+                                         uint64_t* empty, int& stage, uint32_t& phase, volatile int* abort_flag) {
+  constexpr uint32_t ID = idesc(A_MN, B_MN);
+  for (int kb = 0; kb < nk; ++kb) {
+    if (!mbar_wait(&full[stage], phase, abort_flag)) return false;
+    tc_fence_after();
+    const uint32_t a0 = su32(sA + stage * A_BYTES), b0 = su32(sB + stage * B_BYTES);
+#pragma unroll
+    for (int k = 0; k < BK / UMMA_K; ++k) {
+      const uint64_t ad = A_MN ? sdesc(a0 + k * UMMA_K * 128, CHUNK_BYTES, 1024) : sdesc(a0 + k * UMMA_K * 2, 16, 1024);
+      const uint64_t bd = B_MN ? sdesc(b0 + k * UMMA_K * 128, CHUNK_BYTES, 1024) : sdesc(b0 + k * UMMA_K * 2, 16, 1024);
+      tc_mma(d, ad, bd, ID, (kb | k) != 0);
+    }
+    tc_commit(&empty[stage]);
+    if (++stage == STAGES) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+  return true;
+}
+
+// Epilogue of one tile from accumulator column block acc (warp-collective loads).
+__device__ __forceinline__ void epilogue_tile(const Epi& e, int local, uint32_t taddr, int row_in_tile) {
+  int tm, tn;
+  tile_mn(local, e, tm, tn);
+  const int row = tm * BM + row_in_tile;
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(taddr + (uint32_t)(c * 32), r);
+    const int col = tn * BN + c * 32;
+    if (row < e.M && col < e.N) epi_store(e, row, col, r);
+  }
+}
+
+// NG groups (1 or 2) with compile-time majorness (A0, B0) and (A1, B1).
+template <int NG, bool A0, bool B0, bool A1, bool B1>
+__global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -230,8 +313,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_tiles = e.tiles_m * e.tiles_n;
-  const int nk = (e.K + BK - 1) / BK;
+  const int num_tiles = p.tile_start[NG];
+  const int split = NG > 1 ? p.tile_start[1] : num_tiles;  // first tile of group 1
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -244,8 +327,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&p.ta[0]) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&p.tb[0]) : "memory");
+    if (NG > 1) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&p.ta[1]) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&p.tb[1]) : "memory");
+    }
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
@@ -265,36 +352,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok && !e.stall; tile += gridDim.x) {
+      for (int tile = blockIdx.x; tile < num_tiles && ok && !p.stall; tile += gridDim.x) {
         int tm, tn;
-        tile_mn(tile, e, tm, tn);
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(&full[stage], STAGE_BYTES);
-          uint8_t* a = sA + stage * A_BYTES;
-          uint8_t* b = sB + stage * B_BYTES;
-          const int k0 = kb * BK;
-          if (!A_MN) {
-            tma_load(&tmA, &full[stage], a, k0, tm * BM);
-          } else {
-            tma_load(&tmA, &full[stage], a, tm * BM, k0);
-            tma_load(&tmA, &full[stage], a + CHUNK_BYTES, tm * BM + 64, k0);
-          }
-          if (!B_MN) {
-            tma_load(&tmB, &full[stage], b, k0, tn * BN);
-          } else {
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c) tma_load(&tmB, &full[stage], b + c * CHUNK_BYTES, tn * BN + 64 * c, k0);
-          }
-          inflight_mask |= 1u << stage;
-          inflight_parity = (inflight_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+        if (NG == 1 || tile < split) {
+          tile_mn(tile, p.e[0], tm, tn);
+          ok = produce_tile<A0, B0>(&p.ta[0], &p.tb[0], tm, tn, (p.e[0].K + BK - 1) / BK, sA, sB, full, empty, stage,
+                                    phase, abort_flag, inflight_mask, inflight_parity);
+        } else {
+          tile_mn(tile - split, p.e[1], tm, tn);
+          ok = produce_tile<A1, B1>(&p.ta[1], &p.tb[1], tm, tn, (p.e[1].K + BK - 1) / BK, sA, sB, full, empty, stage,
+                                    phase, abort_flag, inflight_mask, inflight_parity);
         }
       }
       if (!ok) fail(abort_flag, 1);
@@ -305,7 +372,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      constexpr uint32_t ID = idesc(A_MN, B_MN);
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
@@ -315,27 +381,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = su32(sA + stage * A_BYTES), b0 = su32(sB + stage * B_BYTES);
-#pragma unroll
-          for (int k = 0; k < BK / UMMA_K; ++k) {
-            const uint64_t ad = A_MN ? sdesc(a0 + k * UMMA_K * 128, CHUNK_BYTES, 1024)
-                                     : sdesc(a0 + k * UMMA_K * 2, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc(b0 + k * UMMA_K * 128, CHUNK_BYTES, 1024)
-                                     : sdesc(b0 + k * UMMA_K * 2, 16, 1024);
-            tc_mma(d, ad, bd, ID, (kb | k) != 0);
-          }
-          tc_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
+        if (NG == 1 || tile < split)
+          ok = mma_tile<A0, B0>(d, (p.e[0].K + BK - 1) / BK, sA, sB, full, empty, stage, phase, abort_flag);
+        else
+          ok = mma_tile<A1, B1>(d, (p.e[1].K + BK - 1) / BK, sA, sB, full, empty, stage, phase, abort_flag);
         if (!ok) break;
         tc_commit(&tfull[acc]);
       }
@@ -355,15 +404,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      int tm, tn;
-      tile_mn(tile, e, tm, tn);
-      const int row = tm * BM + row_in_tile;
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
-        const int col = tn * BN + c * 32;
-        if (row < e.M && col < e.N) epi_store(e, row, col, r);
-      }
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      if (NG == 1 || tile < split) epilogue_tile(p.e[0], tile, taddr, row_in_tile);
+      else epilogue_tile(p.e[1], tile - split, taddr, row_in_tile);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
@@ -405,14 +448,15 @@ void init_once() {
   int dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaError_t a = cudaFuncSetAttribute(gemm_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  cudaError_t b = cudaFuncSetAttribute(gemm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  cudaError_t c = cudaFuncSetAttribute(gemm_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  cudaError_t d = cudaFuncSetAttribute(gemm_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (a != cudaSuccess) g_init_err = a;
-  else if (b != cudaSuccess) g_init_err = b;
-  else if (c != cudaSuccess) g_init_err = c;
-  else if (d != cudaSuccess) g_init_err = d;
+  const void* kernels[] = {(const void*)gemm_kernel<1, false, false, false, false>,
+                           (const void*)gemm_kernel<1, false, true, false, false>,
+                           (const void*)gemm_kernel<1, true, false, false, false>,
+                           (const void*)gemm_kernel<1, true, true, false, false>,
+                           (const void*)gemm_kernel<2, true, true, false, true>};
+  for (const void* k : kernels) {
+    const cudaError_t a = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (a != cudaSuccess) g_init_err = a;
+  }
 }
 
 // 2-D bf16 tensor map of a row-major [rows][cols] matrix with row stride ld,
@@ -446,9 +490,8 @@ int gemm_num_sms() {
   return g_num_sms;
 }
 
-cudaError_t gemm(const GemmArgs& g, cudaStream_t s) {
-  std::call_once(g_once, init_once);
-  if (g_init_err != cudaSuccess) return g_init_err;
+namespace {
+cudaError_t fill_group(const GemmArgs& g, CUtensorMap* ma, CUtensorMap* mb, Epi* e) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0 || !g.A || !g.B) return cudaErrorInvalidValue;
   if (!g.D && !g.acc_mode) return cudaErrorInvalidValue;
   if ((g.lda | g.ldb) % 8 || (g.D && g.ldd % 8) || (g.R && g.ldr % 8) || (g.acc_mode && g.ldacc % 8))
@@ -456,25 +499,59 @@ cudaError_t gemm(const GemmArgs& g, cudaStream_t s) {
   if (!al16(g.A) || !al16(g.B) || (g.D && !al16(g.D)) || (g.R && !al16(g.R)) || (g.acc_mode && !al16(g.Dacc)))
     return cudaErrorInvalidValue;
   if (g.acc_mode && !g.Dacc) return cudaErrorInvalidValue;
-  CUtensorMap ma, mb;
   // A: K-major [M][K] (box 64 x 128) or MN-major [K][M] (box 64 x 64)
-  bool ok = g.a_mn ? make_map(&ma, g.A, g.K, g.M, g.lda, BK) : make_map(&ma, g.A, g.M, g.K, g.lda, BM);
-  ok = ok && (g.b_mn ? make_map(&mb, g.B, g.K, g.N, g.ldb, BK) : make_map(&mb, g.B, g.N, g.K, g.ldb, BN));
+  bool ok = g.a_mn ? make_map(ma, g.A, g.K, g.M, g.lda, BK) : make_map(ma, g.A, g.M, g.K, g.lda, BM);
+  ok = ok && (g.b_mn ? make_map(mb, g.B, g.K, g.N, g.ldb, BK) : make_map(mb, g.B, g.N, g.K, g.ldb, BN));
   if (!ok) return cudaErrorInvalidValue;
-  Epi e;
-  e.D = g.D; e.ldd = g.ldd; e.R = g.R; e.ldr = g.ldr; e.Dacc = g.Dacc; e.ldacc = g.ldacc; e.acc_mode = g.acc_mode;
-  e.M = g.M; e.N = g.N; e.K = g.K;
-  e.tiles_m = (g.M + BM - 1) / BM;
-  e.tiles_n = (g.N + BN - 1) / BN;
-  e.group_m = 16;
-  e.stall = gemm_stall_take();
-  const int tiles = e.tiles_m * e.tiles_n;
+  e->D = g.D; e->ldd = g.ldd; e->R = g.R; e->ldr = g.ldr; e->Dacc = g.Dacc; e->ldacc = g.ldacc;
+  e->acc_mode = g.acc_mode;
+  e->M = g.M; e->N = g.N; e->K = g.K;
+  e->tiles_m = (g.M + BM - 1) / BM;
+  e->tiles_n = (g.N + BN - 1) / BN;
+  e->group_m = 16;
+  e->a_mn = g.a_mn ? 1 : 0;
+  e->b_mn = g.b_mn ? 1 : 0;
+  return cudaSuccess;
+}
+
+cudaError_t launch(const GemmArgs* gs, int n, cudaStream_t s) {
+  std::call_once(g_once, init_once);
+  if (g_init_err != cudaSuccess) return g_init_err;
+  Params p;
+  std::memset(&p, 0, sizeof p);
+  p.ngroups = n;
+  p.tile_start[0] = 0;
+  for (int i = 0; i < n; ++i) {
+    cudaError_t e = fill_group(gs[i], &p.ta[i], &p.tb[i], &p.e[i]);
+    if (e != cudaSuccess) return e;
+    p.tile_start[i + 1] = p.tile_start[i] + p.e[i].tiles_m * p.e[i].tiles_n;
+  }
+  p.stall = gemm_stall_take();
+  const int tiles = p.tile_start[n];
   const int grid = tiles < g_num_sms ? tiles : g_num_sms;
-  if (!g.a_mn && !g.b_mn) gemm_kernel<false, false><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, e);
-  else if (!g.a_mn && g.b_mn) gemm_kernel<false, true><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, e);
-  else if (g.a_mn && !g.b_mn) gemm_kernel<true, false><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, e);
-  else gemm_kernel<true, true><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, e);
+  const Epi& e = p.e[0];
+  if (n == 1) {
+    if (!e.a_mn && !e.b_mn) gemm_kernel<1, false, false, false, false><<<grid, THREADS, SMEM_BYTES, s>>>(p);
+    else if (!e.a_mn && e.b_mn) gemm_kernel<1, false, true, false, false><<<grid, THREADS, SMEM_BYTES, s>>>(p);
+    else if (e.a_mn && !e.b_mn) gemm_kernel<1, true, false, false, false><<<grid, THREADS, SMEM_BYTES, s>>>(p);
+    else gemm_kernel<1, true, true, false, false><<<grid, THREADS, SMEM_BYTES, s>>>(p);
+  } else {
+    gemm_kernel<2, true, true, false, true><<<grid, THREADS, SMEM_BYTES, s>>>(p);
+  }
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t gemm(const GemmArgs& g, cudaStream_t s) { return launch(&g, 1, s); }
+
+cudaError_t gemm_pair(const GemmArgs& g0, const GemmArgs& g1, cudaStream_t s) {
+  // one launch for the (wgrad, dgrad) form: A and B MN-major, then B MN-major
+  if (g0.a_mn && g0.b_mn && !g1.a_mn && g1.b_mn) {
+    const GemmArgs gs[2] = {g0, g1};
+    return launch(gs, 2, s);
+  }
+  cudaError_t e = launch(&g0, 1, s);
+  return e != cudaSuccess ? e : launch(&g1, 1, s);
 }
 
 cudaError_t kernel_error_read(int* code, int clear) {

@@ -30,6 +30,9 @@ struct GemmArgs {
   float* Dacc; int64_t ldacc; int acc_mode;
 };
 cudaError_t gemm(const GemmArgs& g, cudaStream_t s);
+// Two independent GEMMs in one persistent launch (their tiles share the
+// schedule); same requirements as gemm() for each.
+cudaError_t gemm_pair(const GemmArgs& g0, const GemmArgs& g1, cudaStream_t s);
 int gemm_num_sms();
 // Test hook: the next `launches` GEMM launches issue no loads, so their bounded
 // waits expire and they report through the kernel error word.

@@ -303,21 +303,32 @@ mt_status gemm_run(mt_model* m, const mt::GemmArgs& g) {
   CU(m, mt::gemm(g, m->sc));
   return MT_OK;
 }
+// Two independent GEMMs in one persistent launch.
+mt_status gemm_run2(mt_model* m, const mt::GemmArgs& a, const mt::GemmArgs& b) {
+  Timed t(m, K_GEMM, 2.0 * a.M * a.N * a.K + 2.0 * b.M * b.N * b.K, 0);
+  CU(m, mt::gemm_pair(a, b, m->sc));
+  return MT_OK;
+}
 // Y[T,N] = X[T,K] W[N,K]^T (+ R)
-mt_status fprop(mt_model* m, const bf16* X, const bf16* W, int64_t T, int N, int K, bf16* Y, const bf16* R) {
-  mt::GemmArgs g{X, K, 0, W, K, 0, (int)T, N, K, Y, N, R, N, nullptr, 0, 0};
-  return gemm_run(m, g);
+mt::GemmArgs fprop_args(const bf16* X, const bf16* W, int64_t T, int N, int K, bf16* Y, const bf16* R) {
+  return mt::GemmArgs{X, K, 0, W, K, 0, (int)T, N, K, Y, N, R, N, nullptr, 0, 0};
 }
 // dX[T,K] = dY[T,N] W[N,K]
-mt_status dgrad(mt_model* m, const bf16* dY, const bf16* W, int64_t T, int N, int K, bf16* dX) {
-  mt::GemmArgs g{dY, N, 0, W, K, 1, (int)T, K, N, dX, K, nullptr, 0, nullptr, 0, 0};
-  return gemm_run(m, g);
+mt::GemmArgs dgrad_args(const bf16* dY, const bf16* W, int64_t T, int N, int K, bf16* dX) {
+  return mt::GemmArgs{dY, N, 0, W, K, 1, (int)T, K, N, dX, K, nullptr, 0, nullptr, 0, 0};
 }
 // dW[N,K] = dY[T,N]^T X[T,K]  (acc_mode / Dacc for chunked accumulation)
-mt_status wgrad(mt_model* m, const bf16* dY, const bf16* X, int64_t T, int N, int K, bf16* dW, float* acc,
-                int acc_mode) {
-  mt::GemmArgs g{dY, N, 1, X, K, 1, N, K, (int)T, dW, K, nullptr, 0, acc, K, acc_mode};
-  return gemm_run(m, g);
+mt::GemmArgs wgrad_args(const bf16* dY, const bf16* X, int64_t T, int N, int K, bf16* dW, float* acc, int acc_mode) {
+  return mt::GemmArgs{dY, N, 1, X, K, 1, N, K, (int)T, dW, K, nullptr, 0, acc, K, acc_mode};
+}
+mt_status fprop(mt_model* m, const bf16* X, const bf16* W, int64_t T, int N, int K, bf16* Y, const bf16* R) {
+  return gemm_run(m, fprop_args(X, W, T, N, K, Y, R));
+}
+// The weight gradient and the input gradient of one projection share dY and
+// are independent: one launch computes both.
+mt_status wgrad_dgrad(mt_model* m, const bf16* dY, const bf16* X, const bf16* W, int64_t T, int N, int K, bf16* dW,
+                      bf16* dX, float* acc = nullptr, int acc_mode = 0) {
+  return gemm_run2(m, wgrad_args(dY, X, T, N, K, dW, acc, acc_mode), dgrad_args(dY, W, T, N, K, dX));
 }
 
 struct View {
@@ -393,20 +404,17 @@ mt_status decoder_backward(mt_model* m, const View& v, const bf16* x, const bf16
   const int H = m->H, F = m->F, nhd = m->nh * m->hd;
   cudaStream_t s = m->sc;
   Dev& d = m->d;
-  OK(wgrad(m, dout, d.h, T, H, F, v.g[3], nullptr, 0));
-  OK(dgrad(m, dout, v.w[3], T, H, F, d.dh));
+  OK(wgrad_dgrad(m, dout, d.h, v.w[3], T, H, F, v.g[3], d.dh));
   {
     Timed t(m, K_OTHER, 0, 10.0 * T * F);
     CU(m, mt::swiglu_bwd(d.gu, d.dh, T, F, d.dgu, s));
   }
-  OK(wgrad(m, d.dgu, d.yn, T, 2 * F, H, v.g[2], nullptr, 0));
-  OK(dgrad(m, d.dgu, v.w[2], T, 2 * F, H, d.dyn));
+  OK(wgrad_dgrad(m, d.dgu, d.yn, v.w[2], T, 2 * F, H, v.g[2], d.dyn));
   {
     Timed t(m, K_OTHER, 0, 8.0 * T * H + 4.0 * T, 2);
     CU(m, mt::rmsnorm_bwd(d.dyn, d.x1, v.w[5], d.rstd2, dout, T, H, d.dx1, v.g[5], d.rms_part, s));
   }
-  OK(wgrad(m, d.dx1, d.attn, T, H, nhd, v.g[1], nullptr, 0));
-  OK(dgrad(m, d.dx1, v.w[1], T, H, nhd, d.dattn));
+  OK(wgrad_dgrad(m, d.dx1, d.attn, v.w[1], T, H, nhd, v.g[1], d.dattn));
   {
     const double fl = 10.0 * m->M * m->B * (double)m->nh * m->hd * (double)m->S * m->S / 2;
     Timed t(m, K_ATTN_B, fl, 0, 3);
@@ -417,8 +425,7 @@ mt_status decoder_backward(mt_model* m, const View& v, const bf16* x, const bf16
     Timed t(m, K_OTHER, 0, 4.0 * T * (m->nh + m->nkv) * m->hd);
     CU(m, mt::rope(d.dqkv, T, m->Nqkv, m->nh + m->nkv, m->hd, m->S, d.cs, 1, s));
   }
-  OK(wgrad(m, d.dqkv, d.xn, T, m->Nqkv, H, v.g[0], nullptr, 0));
-  OK(dgrad(m, d.dqkv, v.w[0], T, m->Nqkv, H, d.dxn));
+  OK(wgrad_dgrad(m, d.dqkv, d.xn, v.w[0], T, m->Nqkv, H, v.g[0], d.dxn));
   {
     Timed t(m, K_OTHER, 0, 8.0 * T * H + 4.0 * T, 2);
     CU(m, mt::rmsnorm_bwd(d.dxn, x, v.w[4], d.rstd1, d.dx1, T, H, din, v.g[4], d.rms_part, s));
@@ -449,11 +456,11 @@ mt_status head_forward_backward(mt_model* m, const View& v, const bf16* x, bf16*
       Timed t(m, K_OTHER, 0, 6.0 * rows * V);
       CU(m, mt::cross_entropy(d.logits, d.tgt + c0, rows, V, inv_norm, d.row_loss + c0, s));
     }
-    OK(dgrad(m, d.logits, v.w[1], rows, V, H, dhn + c0 * H));
     if (m->chunk >= T) {
-      OK(wgrad(m, d.logits, hn, rows, V, H, v.g[1], nullptr, 0));
+      OK(wgrad_dgrad(m, d.logits, hn, v.w[1], rows, V, H, v.g[1], dhn));
     } else {
-      OK(wgrad(m, d.logits, hn + c0 * H, rows, V, H, last ? v.g[1] : nullptr, d.dwacc, first ? 1 : 2));
+      OK(wgrad_dgrad(m, d.logits, hn + c0 * H, v.w[1], rows, V, H, last ? v.g[1] : nullptr, dhn + c0 * H, d.dwacc,
+                     first ? 1 : 2));
     }
   }
   {
@@ -1345,6 +1352,17 @@ mt_status mt_gemm(const void* A, int64_t lda, int32_t a_mn, const void* B, int64
   mt::GemmArgs g{(const bf16*)A, lda, a_mn, (const bf16*)B, ldb, b_mn, M, N, K, (bf16*)D, ldd, (const bf16*)R,
                  ldr, Dacc, ldacc, acc_mode};
   return cu_status(mt::gemm(g, (cudaStream_t)stream));
+}
+
+mt_status mt_gemm2(const void* const* A, const int64_t* lda, const int32_t* a_mn, const void* const* B,
+                   const int64_t* ldb, const int32_t* b_mn, const int32_t* M, const int32_t* N, const int32_t* K,
+                   void* const* D, const int64_t* ldd, void* stream) {
+  if (!A || !lda || !a_mn || !B || !ldb || !b_mn || !M || !N || !K || !D || !ldd) return MT_ERR_ARG;
+  mt::GemmArgs g[2];
+  for (int i = 0; i < 2; ++i)
+    g[i] = mt::GemmArgs{(const bf16*)A[i], lda[i], a_mn[i], (const bf16*)B[i], ldb[i], b_mn[i], M[i], N[i], K[i],
+                        (bf16*)D[i], ldd[i], nullptr, 0, nullptr, 0, 0};
+  return cu_status(mt::gemm_pair(g[0], g[1], (cudaStream_t)stream));
 }
 
 mt_status mt_rmsnorm_fwd(const void* x, const void* gamma, int64_t T, int32_t H, float eps, void* y, float* rstd,

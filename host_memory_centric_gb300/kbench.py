@@ -61,6 +61,22 @@ def main():
         res.update(shape=[a.M, a.N, a.K], a_mn=a.a_mn, b_mn=a.b_mn, ms=ms, tflops=2 * a.M * a.N * a.K / ms / 1e9)
         ref_ms = timeit(lambda: torch.matmul(A.T if a.a_mn else A, B if a.b_mn else B.T, out=D), a.iters, a.warmup)
         res.update(torch_matmul_ms=ref_ms, torch_matmul_tflops=2 * a.M * a.N * a.K / ref_ms / 1e9)
+    elif a.op == "gemm_pair":
+        # the 1.2B backward pair of the gate/up projection: dW = dY^T X (both MN-major) and dX = dY W
+        T, N, K = a.M, a.N, a.K
+        dY = torch.randn(T, N).to(bf).to(dev)
+        X = torch.randn(T, K).to(bf).to(dev)
+        W = torch.randn(N, K).to(bf).to(dev)
+        dW = torch.empty(N, K, dtype=bf, device=dev)
+        dX = torch.empty(T, K, dtype=bf, device=dev)
+        sw = dict(A=dY, B=X, M=N, N=K, K=T, a_mn=1, b_mn=1, lda=N, ldb=K, D=dW)
+        sd = dict(A=dY, B=W, M=T, N=K, K=N, b_mn=1, ldb=K, D=dX)
+        fl = 2 * 2 * T * N * K
+        ms_pair = timeit(lambda: ops.gemm2([sw, sd]), a.iters, a.warmup)
+        ms_w = timeit(lambda: ops.gemm(dY, X, N, K, T, a_mn=True, b_mn=True, lda=N, ldb=K, D=dW), a.iters, a.warmup)
+        ms_d = timeit(lambda: ops.gemm(dY, W, T, K, N, b_mn=True, ldb=K, D=dX), a.iters, a.warmup)
+        res.update(shape=[T, N, K], pair_ms=ms_pair, pair_tflops=fl / ms_pair / 1e9, wgrad_ms=ms_w, dgrad_ms=ms_d,
+                   separate_tflops=fl / (ms_w + ms_d) / 1e9)
     elif a.op in ("attn_fwd", "attn_bwd"):
         T = a.nseq * a.S
         qkv = (torch.randn(T, (a.nh + 2 * a.nkv) * a.hd) * 0.5).to(bf).to(dev)

@@ -42,6 +42,22 @@ def gemm(A, B, M, N, K, *, a_mn=False, b_mn=False, lda=None, ldb=None, D=None, l
                       _p(Dacc), ldacc, acc_mode, _stream()))
 
 
+def gemm2(specs):
+    """Two GEMMs in one launch; specs = two dicts with A, B, M, N, K, D and
+    optional a_mn, b_mn, lda, ldb, ldd (defaults as in gemm)."""
+    arr = lambda ct, vals: (ct * 2)(*vals)
+    A, B, D, lda, ldb, ldd, amn, bmn, M, N, K = ([] for _ in range(11))
+    for s in specs:
+        a_mn, b_mn = int(s.get("a_mn", 0)), int(s.get("b_mn", 0))
+        A.append(s["A"].data_ptr()); B.append(s["B"].data_ptr()); D.append(s["D"].data_ptr())
+        M.append(s["M"]); N.append(s["N"]); K.append(s["K"]); amn.append(a_mn); bmn.append(b_mn)
+        lda.append(s.get("lda", s["M"] if a_mn else s["K"])); ldb.append(s.get("ldb", s["N"] if b_mn else s["K"]))
+        ldd.append(s.get("ldd", s["N"]))
+    _chk(_L().mt_gemm2(arr(C.c_void_p, A), arr(C.c_int64, lda), arr(C.c_int32, amn), arr(C.c_void_p, B),
+                       arr(C.c_int64, ldb), arr(C.c_int32, bmn), arr(C.c_int32, M), arr(C.c_int32, N),
+                       arr(C.c_int32, K), arr(C.c_void_p, D), arr(C.c_int64, ldd), _stream()))
+
+
 def rmsnorm_fwd(x, gamma, eps, y, rstd):
     T, H = x.shape
     _chk(_L().mt_rmsnorm_fwd(_p(x), _p(gamma), T, H, eps, _p(y), _p(rstd), _stream()))

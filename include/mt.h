@@ -219,6 +219,11 @@ mt_status mt_gemm(const void* A, int64_t lda, int32_t a_mn, const void* B, int64
                   int32_t b_mn, int32_t M, int32_t N, int32_t K, void* D, int64_t ldd,
                   const void* R, int64_t ldr, float* Dacc, int64_t ldacc, int32_t acc_mode,
                   void* stream);
+/* Two independent GEMMs (each as mt_gemm, arguments given as arrays of two)
+ * in one persistent launch: their output tiles share one schedule. */
+mt_status mt_gemm2(const void* const* A, const int64_t* lda, const int32_t* a_mn, const void* const* B,
+                   const int64_t* ldb, const int32_t* b_mn, const int32_t* M, const int32_t* N,
+                   const int32_t* K, void* const* D, const int64_t* ldd, void* stream);
 /* RMSNorm forward: y = x * rstd * gamma, rstd = (mean(x^2)+eps)^-1/2 per row. */
 mt_status mt_rmsnorm_fwd(const void* x, const void* gamma, int64_t T, int32_t H, float eps,
                          void* y, float* rstd, void* stream);

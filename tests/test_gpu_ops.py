@@ -253,3 +253,16 @@ def test_cross_entropy(orc):
     loss_ref, dl_ref = orc.cross_entropy(zin, tok, n_seq, S, norm)
     assert float(rl.sum()) / norm == pytest.approx(loss_ref, rel=1e-4)
     close(f64(zg), dl_ref, rel=1e-2, atol=1e-3 * np.abs(dl_ref).max())
+
+
+def test_gemm_pair_in_one_launch(orc):
+    """wgrad (both operands MN-major) and dgrad of one projection in one launch."""
+    T, N, K = 320, 264, 200
+    dY = rnd((T, N), 30); X = rnd((T, K), 31); W = rnd((N, K), 32)
+    dYg, Xg, Wg = bf(dY), bf(X), bf(W)
+    dW = torch.empty(N, K, dtype=torch.bfloat16, device="cuda")
+    dX = torch.empty(T, K, dtype=torch.bfloat16, device="cuda")
+    ops.gemm2([dict(A=dYg, B=Xg, M=N, N=K, K=T, a_mn=1, b_mn=1, lda=N, ldb=K, D=dW),
+               dict(A=dYg, B=Wg, M=T, N=K, K=N, b_mn=1, ldb=K, D=dX)])
+    close(f64(dW), orc.linear_wgrad(f64(dYg), f64(Xg)), rel=5e-3)
+    close(f64(dX), orc.linear_dgrad(f64(dYg), f64(Wg)), rel=5e-3)
