@@ -1,4 +1,4 @@
-// k_attention.cu -- causal grouped-query attention, forward and backward.
+// k_attention.cu -- causal grouped-query attention entry points.
 //
 // Tiled exact attention with an online softmax (Milakov and Gimelshein 2018;
 // the FlashAttention-2 tiling of Dao 2023), so memory is O(S * hd) per head and
@@ -8,181 +8,15 @@
 // (s * log2(e) / sqrt(hd)); the forward keeps the natural-log LSE per row for
 // the backward, which recomputes P from it.
 //
-// Forward: one CTA per (64 queries, head, sequence); 4 warps x 16 query rows;
-// key tiles of 64 up to the diagonal (causal tiles above it are skipped).
-// Backward: one CTA per (64 keys, kv head, sequence); it loops over the query
-// heads that share the kv head and over query tiles from the diagonal down,
-// accumulates dK and dV in registers (computing S^T = K Q^T so P^T and dS^T
-// are already laid out as MMA A-operands), and adds dQ into an FP32 buffer
-// with atomics.  Warp-level BF16 MMA (m16n8k16) with ldmatrix operands.
+// The forward and the two backward kernels run on the tcgen05 tensor cores
+// (k_attention_tc.cu).  This file holds the backward's first pass,
+// delta = rowsum(dO o O), and the argument checks.
 #include "mt_kernels.h"
 
 namespace mt {
 namespace {
 
-__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ void ldsm4(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(a));
-}
-__device__ __forceinline__ void ldsm4t(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(a));
-}
-__device__ __forceinline__ void mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                    uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t pk(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// 64 rows x HD columns from global (row stride gld) into shared (row stride
-// LDS); rows at or beyond `valid` are zero.
-template <int HD, int LDS>
-__device__ __forceinline__ void load_tile(bf16* s, const bf16* g, int64_t gld, int valid) {
-  constexpr int CPR = HD / 8;
-  for (int c = threadIdx.x; c < 64 * CPR; c += 128) {
-    const int r = c / CPR, cc = (c % CPR) * 8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < valid) v = *reinterpret_cast<const uint4*>(g + (int64_t)r * gld + cc);
-    *reinterpret_cast<uint4*>(s + r * LDS + cc) = v;
-  }
-}
-
-template <int HD>
-__global__ void __launch_bounds__(128) attn_fwd_k(const bf16* __restrict__ qkv, int S, int nh, int nkv,
-                                                  bf16* __restrict__ o, float* __restrict__ lse,
-                                                  float scale_log2) {
-  constexpr int LDS = HD + 8;
-  extern __shared__ __align__(16) uint8_t smem[];
-  bf16* Qs = reinterpret_cast<bf16*>(smem);
-  bf16* Ks = Qs + 64 * LDS;
-  bf16* Vs = Ks + 64 * LDS;
-  const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first
-  const int h = blockIdx.y, n = blockIdx.z;
-  const int kh = h / (nh / nkv);
-  const int64_t ld = (int64_t)(nh + 2 * nkv) * HD;
-  const int64_t T = (int64_t)gridDim.z * S;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q0 = qb * 64;
-  const bf16* base = qkv + (int64_t)n * S * ld;
-
-  load_tile<HD, LDS>(Qs, base + (int64_t)q0 * ld + h * HD, ld, min(64, S - q0));
-  __syncthreads();
-  uint32_t qf[HD / 16][4];
-#pragma unroll
-  for (int kk = 0; kk < HD / 16; ++kk)
-    ldsm4(su32(Qs + (warp * 16 + (lane & 15)) * LDS + kk * 16 + (lane >> 4) * 8), qf[kk][0], qf[kk][1], qf[kk][2],
-          qf[kk][3]);
-
-  float oa[HD / 8][4];
-#pragma unroll
-  for (int i = 0; i < HD / 8; ++i) oa[i][0] = oa[i][1] = oa[i][2] = oa[i][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  const int qr0 = q0 + warp * 16 + (lane >> 2), qr1 = qr0 + 8;
-
-  for (int kb = 0; kb <= qb; ++kb) {
-    const int k0 = kb * 64;
-    __syncthreads();
-    load_tile<HD, LDS>(Ks, base + (int64_t)k0 * ld + (int64_t)(nh + kh) * HD, ld, min(64, S - k0));
-    load_tile<HD, LDS>(Vs, base + (int64_t)k0 * ld + (int64_t)(nh + nkv + kh) * HD, ld, min(64, S - k0));
-    __syncthreads();
-    float sa[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sa[i][0] = sa[i][1] = sa[i][2] = sa[i][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < HD / 16; ++kk)
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t b0, b1, b2, b3;
-        ldsm4(su32(Ks + (np * 16 + (lane & 7) + (lane >> 4) * 8) * LDS + kk * 16 + ((lane >> 3) & 1) * 8), b0, b1, b2,
-              b3);
-        mma(sa[2 * np], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
-        mma(sa[2 * np + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
-      }
-    float mx0 = m0, mx1 = m1;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = k0 + nt * 8 + (lane & 3) * 2 + (e & 1);
-        const int qr = e < 2 ? qr0 : qr1;
-        float v = sa[nt][e] * scale_log2;
-        if (key > qr || key >= S) v = -INFINITY;
-        sa[nt][e] = v;
-        if (e < 2) mx0 = fmaxf(mx0, v);
-        else mx1 = fmaxf(mx1, v);
-      }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float c0 = mx0 == -INFINITY ? 1.f : exp2f(m0 - mx0);
-    const float c1 = mx1 == -INFINITY ? 1.f : exp2f(m1 - mx1);
-    const float b0v = mx0 == -INFINITY ? 0.f : mx0, b1v = mx1 == -INFINITY ? 0.f : mx1;
-    m0 = mx0;
-    m1 = mx1;
-    float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      sa[nt][0] = exp2f(sa[nt][0] - b0v);
-      sa[nt][1] = exp2f(sa[nt][1] - b0v);
-      sa[nt][2] = exp2f(sa[nt][2] - b1v);
-      sa[nt][3] = exp2f(sa[nt][3] - b1v);
-      rs0 += sa[nt][0] + sa[nt][1];
-      rs1 += sa[nt][2] + sa[nt][3];
-    }
-    l0 = l0 * c0 + rs0;
-    l1 = l1 * c1 + rs1;
-#pragma unroll
-    for (int i = 0; i < HD / 8; ++i) {
-      oa[i][0] *= c0;
-      oa[i][1] *= c0;
-      oa[i][2] *= c1;
-      oa[i][3] *= c1;
-    }
-#pragma unroll
-    for (int kt = 0; kt < 4; ++kt) {
-      const uint32_t a0 = pk(sa[2 * kt][0], sa[2 * kt][1]), a1 = pk(sa[2 * kt][2], sa[2 * kt][3]);
-      const uint32_t a2 = pk(sa[2 * kt + 1][0], sa[2 * kt + 1][1]), a3 = pk(sa[2 * kt + 1][2], sa[2 * kt + 1][3]);
-#pragma unroll
-      for (int dp = 0; dp < HD / 16; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm4t(su32(Vs + (kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LDS + dp * 16 + (lane >> 4) * 8), b0, b1,
-               b2, b3);
-        mma(oa[2 * dp], a0, a1, a2, a3, b0, b1);
-        mma(oa[2 * dp + 1], a0, a1, a2, a3, b2, b3);
-      }
-    }
-  }
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const float i0 = 1.f / l0, i1 = 1.f / l1;
-  const int64_t ldo = (int64_t)nh * HD;
-#pragma unroll
-  for (int nd = 0; nd < HD / 8; ++nd) {
-    const int col = h * HD + nd * 8 + (lane & 3) * 2;
-    if (qr0 < S)
-      *reinterpret_cast<uint32_t*>(o + ((int64_t)n * S + qr0) * ldo + col) = pk(oa[nd][0] * i0, oa[nd][1] * i0);
-    if (qr1 < S)
-      *reinterpret_cast<uint32_t*>(o + ((int64_t)n * S + qr1) * ldo + col) = pk(oa[nd][2] * i1, oa[nd][3] * i1);
-  }
-  if ((lane & 3) == 0) {
-    const float LN2 = 0.6931471805599453f;
-    if (qr0 < S) lse[(int64_t)h * T + (int64_t)n * S + qr0] = (m0 + log2f(l0)) * LN2;
-    if (qr1 < S) lse[(int64_t)h * T + (int64_t)n * S + qr1] = (m1 + log2f(l1)) * LN2;
-  }
-}
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 // delta[h][t] = sum_d dO[t, h, d] * O[t, h, d]; one warp per (t, h).
 template <int HD>
@@ -207,216 +41,15 @@ __global__ void attn_delta_k(const bf16* __restrict__ o, const bf16* __restrict_
 }
 
 template <int HD>
-__global__ void __launch_bounds__(128) attn_bwd_k(const bf16* __restrict__ qkv, const bf16* __restrict__ dout,
-                                                  const float* __restrict__ lse, const float* __restrict__ delta,
-                                                  int S, int nh, int nkv, float scale, float scale_log2,
-                                                  bf16* __restrict__ dqkv, float* __restrict__ dq_acc) {
-  constexpr int LDS = HD + 8, LDP = 64 + 8;
-  extern __shared__ __align__(16) uint8_t smem[];
-  bf16* Ks = reinterpret_cast<bf16*>(smem);
-  bf16* Vs = Ks + 64 * LDS;
-  bf16* Qs = Vs + 64 * LDS;
-  bf16* Ds = Qs + 64 * LDS;  // dO tile
-  bf16* St = Ds + 64 * LDS;  // dS^T tile [key][q]
-  float* lse_s = reinterpret_cast<float*>(St + 64 * LDP);
-  float* dl_s = lse_s + 64;
-
-  const int kb = blockIdx.x, g = blockIdx.y, n = blockIdx.z;
-  const int grp = nh / nkv;
-  const int64_t ld = (int64_t)(nh + 2 * nkv) * HD;
-  const int64_t ldo = (int64_t)nh * HD;
-  const int64_t T = (int64_t)gridDim.z * S;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int k0 = kb * 64;
-  const bf16* base = qkv + (int64_t)n * S * ld;
-  const float LOG2E = 1.4426950408889634f;
-
-  load_tile<HD, LDS>(Ks, base + (int64_t)k0 * ld + (int64_t)(nh + g) * HD, ld, min(64, S - k0));
-  load_tile<HD, LDS>(Vs, base + (int64_t)k0 * ld + (int64_t)(nh + nkv + g) * HD, ld, min(64, S - k0));
-
-  float dk[HD / 8][4], dv[HD / 8][4];
-#pragma unroll
-  for (int i = 0; i < HD / 8; ++i) {
-    dk[i][0] = dk[i][1] = dk[i][2] = dk[i][3] = 0.f;
-    dv[i][0] = dv[i][1] = dv[i][2] = dv[i][3] = 0.f;
-  }
-  const int key0 = k0 + warp * 16 + (lane >> 2), key1 = key0 + 8;
-  const int nqb = (S + 63) / 64;
-
-  for (int hi = 0; hi < grp; ++hi) {
-    const int h = g * grp + hi;
-    for (int qb = kb; qb < nqb; ++qb) {
-      const int q0 = qb * 64;
-      __syncthreads();
-      load_tile<HD, LDS>(Qs, base + (int64_t)q0 * ld + (int64_t)h * HD, ld, min(64, S - q0));
-      load_tile<HD, LDS>(Ds, dout + ((int64_t)n * S + q0) * ldo + (int64_t)h * HD, ldo, min(64, S - q0));
-      if (threadIdx.x < 64) {
-        const int q = q0 + threadIdx.x;
-        lse_s[threadIdx.x] = q < S ? lse[(int64_t)h * T + (int64_t)n * S + q] * LOG2E : 0.f;
-        dl_s[threadIdx.x] = q < S ? delta[(int64_t)h * T + (int64_t)n * S + q] : 0.f;
-      }
-      __syncthreads();
-      float st[8][4], dp[8][4];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        st[i][0] = st[i][1] = st[i][2] = st[i][3] = 0.f;
-        dp[i][0] = dp[i][1] = dp[i][2] = dp[i][3] = 0.f;
-      }
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-        uint32_t ka0, ka1, ka2, ka3, va0, va1, va2, va3;
-        ldsm4(su32(Ks + (warp * 16 + (lane & 15)) * LDS + kk * 16 + (lane >> 4) * 8), ka0, ka1, ka2, ka3);
-        ldsm4(su32(Vs + (warp * 16 + (lane & 15)) * LDS + kk * 16 + (lane >> 4) * 8), va0, va1, va2, va3);
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-          const int r = np * 16 + (lane & 7) + (lane >> 4) * 8, c = kk * 16 + ((lane >> 3) & 1) * 8;
-          uint32_t b0, b1, b2, b3;
-          ldsm4(su32(Qs + r * LDS + c), b0, b1, b2, b3);
-          mma(st[2 * np], ka0, ka1, ka2, ka3, b0, b1);
-          mma(st[2 * np + 1], ka0, ka1, ka2, ka3, b2, b3);
-          ldsm4(su32(Ds + r * LDS + c), b0, b1, b2, b3);
-          mma(dp[2 * np], va0, va1, va2, va3, b0, b1);
-          mma(dp[2 * np + 1], va0, va1, va2, va3, b2, b3);
-        }
-      }
-      // P^T and dS^T (rows = keys, columns = queries)
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int ql = nt * 8 + (lane & 3) * 2 + (e & 1);
-          const int q = q0 + ql;
-          const int key = e < 2 ? key0 : key1;
-          float p = 0.f;
-          if (q < S && q >= key) p = exp2f(st[nt][e] * scale_log2 - lse_s[ql]);
-          st[nt][e] = p;
-          dp[nt][e] = p * (dp[nt][e] - dl_s[ql]);
-        }
-      // dV += P^T dO,  dK += dS^T Q
-#pragma unroll
-      for (int kt = 0; kt < 4; ++kt) {
-        const uint32_t pa0 = pk(st[2 * kt][0], st[2 * kt][1]), pa1 = pk(st[2 * kt][2], st[2 * kt][3]);
-        const uint32_t pa2 = pk(st[2 * kt + 1][0], st[2 * kt + 1][1]), pa3 = pk(st[2 * kt + 1][2], st[2 * kt + 1][3]);
-        const uint32_t sa0 = pk(dp[2 * kt][0], dp[2 * kt][1]), sa1 = pk(dp[2 * kt][2], dp[2 * kt][3]);
-        const uint32_t sa2 = pk(dp[2 * kt + 1][0], dp[2 * kt + 1][1]), sa3 = pk(dp[2 * kt + 1][2], dp[2 * kt + 1][3]);
-#pragma unroll
-        for (int dq2 = 0; dq2 < HD / 16; ++dq2) {
-          const int r = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, c = dq2 * 16 + (lane >> 4) * 8;
-          uint32_t b0, b1, b2, b3;
-          ldsm4t(su32(Ds + r * LDS + c), b0, b1, b2, b3);
-          mma(dv[2 * dq2], pa0, pa1, pa2, pa3, b0, b1);
-          mma(dv[2 * dq2 + 1], pa0, pa1, pa2, pa3, b2, b3);
-          ldsm4t(su32(Qs + r * LDS + c), b0, b1, b2, b3);
-          mma(dk[2 * dq2], sa0, sa1, sa2, sa3, b0, b1);
-          mma(dk[2 * dq2 + 1], sa0, sa1, sa2, sa3, b2, b3);
-        }
-      }
-      // dS^T to shared memory, then dQ = dS K for this warp's 16 queries
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int c = nt * 8 + (lane & 3) * 2;
-        *reinterpret_cast<uint32_t*>(St + (warp * 16 + (lane >> 2)) * LDP + c) = pk(dp[nt][0], dp[nt][1]);
-        *reinterpret_cast<uint32_t*>(St + (warp * 16 + 8 + (lane >> 2)) * LDP + c) = pk(dp[nt][2], dp[nt][3]);
-      }
-      __syncthreads();
-      float dq[HD / 8][4];
-#pragma unroll
-      for (int i = 0; i < HD / 8; ++i) dq[i][0] = dq[i][1] = dq[i][2] = dq[i][3] = 0.f;
-#pragma unroll
-      for (int kt = 0; kt < 4; ++kt) {
-        uint32_t a0, a1, a2, a3;
-        ldsm4t(su32(St + (kt * 16 + (lane & 7) + (lane >> 4) * 8) * LDP + warp * 16 + ((lane >> 3) & 1) * 8), a0, a1,
-               a2, a3);
-#pragma unroll
-        for (int dq2 = 0; dq2 < HD / 16; ++dq2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm4t(su32(Ks + (kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LDS + dq2 * 16 + (lane >> 4) * 8), b0, b1,
-                 b2, b3);
-          mma(dq[2 * dq2], a0, a1, a2, a3, b0, b1);
-          mma(dq[2 * dq2 + 1], a0, a1, a2, a3, b2, b3);
-        }
-      }
-      const int qa = q0 + warp * 16 + (lane >> 2), qb2 = qa + 8;
-#pragma unroll
-      for (int nd = 0; nd < HD / 8; ++nd) {
-        const int col = h * HD + nd * 8 + (lane & 3) * 2;
-        if (qa < S) {
-          float* p = dq_acc + ((int64_t)n * S + qa) * ldo + col;
-          atomicAdd(p, dq[nd][0] * scale);
-          atomicAdd(p + 1, dq[nd][1] * scale);
-        }
-        if (qb2 < S) {
-          float* p = dq_acc + ((int64_t)n * S + qb2) * ldo + col;
-          atomicAdd(p, dq[nd][2] * scale);
-          atomicAdd(p + 1, dq[nd][3] * scale);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int nd = 0; nd < HD / 8; ++nd) {
-    const int c = nd * 8 + (lane & 3) * 2;
-    if (key0 < S) {
-      bf16* row = dqkv + ((int64_t)n * S + key0) * ld;
-      *reinterpret_cast<uint32_t*>(row + (int64_t)(nh + g) * HD + c) = pk(dk[nd][0] * scale, dk[nd][1] * scale);
-      *reinterpret_cast<uint32_t*>(row + (int64_t)(nh + nkv + g) * HD + c) = pk(dv[nd][0], dv[nd][1]);
-    }
-    if (key1 < S) {
-      bf16* row = dqkv + ((int64_t)n * S + key1) * ld;
-      *reinterpret_cast<uint32_t*>(row + (int64_t)(nh + g) * HD + c) = pk(dk[nd][2] * scale, dk[nd][3] * scale);
-      *reinterpret_cast<uint32_t*>(row + (int64_t)(nh + nkv + g) * HD + c) = pk(dv[nd][2], dv[nd][3]);
-    }
-  }
-}
-
-inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-
-template <int HD>
-cudaError_t fwd_t(const bf16* qkv, int n_seq, int S, int nh, int nkv, bf16* o, float* lse, cudaStream_t s) {
-  const size_t sm = (size_t)3 * 64 * (HD + 8) * sizeof(bf16);
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_k<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  if (e != cudaSuccess) return e;
-  const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
-  dim3 grid((S + 63) / 64, nh, n_seq);
-  attn_fwd_k<HD><<<grid, 128, sm, s>>>(qkv, S, nh, nkv, o, lse, scale_log2);
-  return cudaGetLastError();
-}
-
-template <int HD>
-cudaError_t bwd_t(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, int n_seq, int S, int nh,
-                  int nkv, bf16* dqkv, float* delta, float* dq_acc, cudaStream_t s) {
-  const int64_t T = (int64_t)n_seq * S;
-  cudaError_t e = cudaMemsetAsync(dq_acc, 0, (size_t)T * nh * HD * sizeof(float), s);
-  if (e != cudaSuccess) return e;
-  const int64_t warps = T * nh;
-  attn_delta_k<HD><<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(o, dout, T, nh, delta);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const size_t sm = (size_t)4 * 64 * (HD + 8) * sizeof(bf16) + 64 * 72 * sizeof(bf16) + 128 * sizeof(float);
-  e = cudaFuncSetAttribute(attn_bwd_k<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  if (e != cudaSuccess) return e;
-  const float scale = 1.f / sqrtf((float)HD);
-  dim3 grid((S + 63) / 64, nkv, n_seq);
-  attn_bwd_k<HD><<<grid, 128, sm, s>>>(qkv, dout, lse, delta, S, nh, nkv, scale, scale * 1.4426950408889634f, dqkv,
-                                       dq_acc);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // dq (already scaled) into the q columns of dqkv
-  return f32_to_bf16_2d(dq_acc, (int64_t)nh * HD, T, (int64_t)nh * HD, dqkv, (int64_t)(nh + 2 * nkv) * HD, 1.f, s);
-}
-
-template <int HD>
 cudaError_t bwd_tc(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, int n_seq, int S, int nh,
-                   int nkv, bf16* dqkv, float* delta, float* dq_acc, cudaStream_t s) {
+                   int nkv, bf16* dqkv, float* delta, cudaStream_t s) {
   const int64_t T = (int64_t)n_seq * S;
-  cudaError_t e = cudaMemsetAsync(dq_acc, 0, (size_t)T * nh * HD * sizeof(float), s);
+  const int64_t blocks = (T * nh * 32 + 255) / 256;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  attn_delta_k<HD><<<(unsigned)blocks, 256, 0, s>>>(o, dout, T, nh, delta);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_delta_k<HD><<<(unsigned)((T * nh * 32 + 255) / 256), 256, 0, s>>>(o, dout, T, nh, delta);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  e = attention_bwd_tc_core(qkv, dout, lse, delta, n_seq, S, nh, nkv, HD, dqkv, dq_acc, s);
-  if (e != cudaSuccess) return e;
-  return f32_to_bf16_2d(dq_acc, (int64_t)nh * HD, T, (int64_t)nh * HD, dqkv, (int64_t)(nh + 2 * nkv) * HD, 1.f, s);
+  return attention_bwd_tc_core(qkv, dout, lse, delta, n_seq, S, nh, nkv, HD, dqkv, s);
 }
 
 }  // namespace
@@ -426,34 +59,12 @@ cudaError_t attention_fwd(const bf16* qkv, int n_seq, int S, int nh, int nkv, in
   return attention_fwd_tc(qkv, n_seq, S, nh, nkv, hd, o, lse, s);
 }
 
-// Warp-level (mma.sync) forward, kept as the reference the tensor-core
-// forward was validated against in the op tests.
-cudaError_t attention_fwd_warp(const bf16* qkv, int n_seq, int S, int nh, int nkv, int hd, bf16* o, float* lse,
-                               cudaStream_t s) {
-  if (n_seq <= 0 || S <= 0) return cudaSuccess;
-  if (nh % nkv || !al16(qkv) || !al16(o) || n_seq > 65535 || nh > 65535) return cudaErrorInvalidValue;
-  if (hd == 64) return fwd_t<64>(qkv, n_seq, S, nh, nkv, o, lse, s);
-  if (hd == 128) return fwd_t<128>(qkv, n_seq, S, nh, nkv, o, lse, s);
-  return cudaErrorInvalidValue;
-}
-
 cudaError_t attention_bwd(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, int n_seq, int S,
-                          int nh, int nkv, int hd, bf16* dqkv, float* delta, float* dq_acc, cudaStream_t s) {
+                          int nh, int nkv, int hd, bf16* dqkv, float* delta, cudaStream_t s) {
   if (n_seq <= 0 || S <= 0) return cudaSuccess;
-  if (nh % nkv || !al16(qkv) || !al16(o) || !al16(dout) || !al16(dqkv) || n_seq > 65535 || nkv > 65535)
-    return cudaErrorInvalidValue;
-  if (hd == 64) return bwd_tc<64>(qkv, o, lse, dout, n_seq, S, nh, nkv, dqkv, delta, dq_acc, s);
-  if (hd == 128) return bwd_tc<128>(qkv, o, lse, dout, n_seq, S, nh, nkv, dqkv, delta, dq_acc, s);
-  return cudaErrorInvalidValue;
-}
-
-// Warp-level (mma.sync) backward, the reference the tensor-core backward was
-// validated against.
-cudaError_t attention_bwd_warp(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, int n_seq, int S,
-                               int nh, int nkv, int hd, bf16* dqkv, float* delta, float* dq_acc, cudaStream_t s) {
-  if (n_seq <= 0 || S <= 0) return cudaSuccess;
-  if (hd == 64) return bwd_t<64>(qkv, o, lse, dout, n_seq, S, nh, nkv, dqkv, delta, dq_acc, s);
-  if (hd == 128) return bwd_t<128>(qkv, o, lse, dout, n_seq, S, nh, nkv, dqkv, delta, dq_acc, s);
+  if (nkv <= 0 || nh % nkv || !al16(qkv) || !al16(o) || !al16(dout) || !al16(dqkv)) return cudaErrorInvalidValue;
+  if (hd == 64) return bwd_tc<64>(qkv, o, lse, dout, n_seq, S, nh, nkv, dqkv, delta, s);
+  if (hd == 128) return bwd_tc<128>(qkv, o, lse, dout, n_seq, S, nh, nkv, dqkv, delta, s);
   return cudaErrorInvalidValue;
 }
 

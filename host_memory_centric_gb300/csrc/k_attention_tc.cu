@@ -1,7 +1,8 @@
-// k_attention_tc.cu -- causal GQA attention forward on the 5th-generation
-// tensor cores (sm_103a): tcgen05.mma with TMEM accumulators, TMA tiles.
+// k_attention_tc.cu -- causal GQA attention, forward and backward, on the
+// 5th-generation tensor cores (sm_103a): tcgen05.mma with TMEM accumulators,
+// TMA tiles, 192 threads per CTA (a TMA warp, an MMA warp, 4 row warps).
 //
-// One CTA per (128 queries, query head, sequence), 192 threads:
+// Forward: one CTA per (128 queries, query head, sequence):
 //   warp 0      TMA producer: the Q tile once, then K and V tiles of 128 keys
 //               into a 2-stage ring (128-byte swizzle);
 //   warp 1      allocates TMEM (S0 | S1 | O) and, from one thread, issues
@@ -400,68 +401,109 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 
 // ---------------------------------------------------------------------------
-// Backward.  One CTA per (128 keys, kv head, sequence); it loops over the
-// query heads sharing the kv head and over the query tiles from the diagonal
-// down.  Per (head, query tile):
-//   MMA   S^T = K Q^T and dP^T = V dO^T into TMEM (M = 128 keys, N = 128 q);
-//   rows  (one thread per key) P^T = exp2(S^T scale - lse2) masked causally,
-//         dS^T = P^T (dP^T - delta); both written as BF16 into 128B-swizzled
-//         shared tiles laid out [key][q];
-//   MMA   dV += P^T dO and dK += dS^T Q (TMEM accumulators kept for the whole
-//         CTA), and dQ = dS K into the columns S^T used, reading the same
-//         [key][q] tile as an MN-major operand (dS = (dS^T)^T) and the K tile
-//         as an MN-major operand;
-//   rows  (one thread per query) dQ rows from TMEM added into the FP32 dQ
-//         accumulator in global memory.
-// TMEM: S^T | dP^T | dV | dK = 512 columns at hd = 128.
+// Backward, as two kernels that share no accumulator (so no atomics and no
+// FP32 dQ buffer).  delta[h][t] = rowsum(dO o O) is computed before them.
+//
+// attn_bwd_kv_k: one CTA per (128 keys, kv head, sequence); it loops over the
+// query heads of its group and, per head, over 64-query sub-tiles from the
+// diagonal to the sequence end.  Per sub-tile i (TMEM and shared buffers
+// alternate with i, Q / dO sub-tiles sit in a 3-stage ring):
+//   MMA   S^T = K Q_i^T and dP^T = V dO_i^T (M = 128 keys, N = 64 queries);
+//   rows  (one thread per key) P^T = exp2(S^T scale log2e - lse log2e), masked
+//         causally where the sub-tile needs it, dS^T = P^T (dP^T - delta),
+//         both as BF16 into 128B-swizzled [key][q] tiles;
+//   MMA   dV += P^T dO_i and dK += dS^T Q_i (dO_i and Q_i as MN-major
+//         operands); the accumulators stay in TMEM for the whole CTA.
+// The MMA warp issues S of sub-tile i+1 before it waits for the rows' P of
+// sub-tile i, so the tensor core and the row warps work at the same time.
+// TMEM: (S^T | dP^T) x 2 = 256 columns, dV, dK.
+//
+// attn_bwd_q_k: one CTA per (128 queries, query head, sequence) looping over
+// 64-key sub-tiles up to the diagonal: S = Q K_j^T and dP = dO V_j^T, the rows
+// (one thread per query) form dS = P (dP - delta), and dQ += dS K_j (K_j as
+// an MN-major operand) accumulates in TMEM; dQ scale goes out as BF16.
+//
+// Both grids are ordered longest work first.  Every wait is bounded.
+constexpr int CH64 = 8192;  // one 64-column chunk of a 64-row tile (64 rows x 128 B)
+constexpr int NQS = 3;      // Q / dO sub-tile stages of the dK/dV kernel
+constexpr int NKS = 4;      // K / V sub-tile stages of the dQ kernel
+
+template <int HD>
+__host__ __device__ constexpr int kv_smem_bytes() {
+  return (HD / 64) * (2 * CH + 2 * NQS * CH64) + 4 * CH + 1024 + 256 + 1024;
+}
+template <int HD>
+__host__ __device__ constexpr int q_smem_bytes() {
+  return (HD / 64) * (2 * CH + 2 * NKS * CH64) + 2 * CH + 256 + 1024;
+}
+static_assert(kv_smem_bytes<128>() <= 232448, "dK/dV kernel shared memory");
+static_assert(q_smem_bytes<128>() <= 232448, "dQ kernel shared memory");
+
+// 32 (p, ds) pairs of one row into the 16-byte units 4c .. 4c+3 of that row
+// of a 128B-swizzled tile whose rows are 128 bytes (64 BF16 values).
+__device__ __forceinline__ void store_row_units(uint8_t* row, int r, int c, const uint32_t (&w)[16]) {
+#pragma unroll
+  for (int u4 = 0; u4 < 4; ++u4) {
+    const int unit = c * 4 + u4;
+    *reinterpret_cast<uint4*>(row + ((unit ^ (r & 7)) << 4)) =
+        make_uint4(w[4 * u4], w[4 * u4 + 1], w[4 * u4 + 2], w[4 * u4 + 3]);
+  }
+}
+
 template <int HD>
 __global__ void __launch_bounds__(THREADS, 1)
-    attn_bwd_tc_k(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo, int S, int nh,
-                  int nkv, const float* __restrict__ lse, const float* __restrict__ delta, float scale,
-                  float scale_log2, bf16* __restrict__ dqkv, float* __restrict__ dq_acc) {
+    attn_bwd_kv_k(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo, int S,
+                  int n_seq, int nh, int nkv, const float* __restrict__ lse, const float* __restrict__ delta,
+                  float scale, float scale_log2, bf16* __restrict__ dqkv) {
   constexpr int NC = HD / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = sm;
+  uint8_t* sK = sm;                    // [128 keys][HD]: NC chunks of 128 rows
   uint8_t* sV = sK + NC * CH;
-  uint8_t* sQ = sV + NC * CH;
-  uint8_t* sO = sQ + NC * CH;  // dO tile
-  uint8_t* sP = sO + NC * CH;  // P^T  [key][q], 2 chunks of 64 q
-  uint8_t* sD = sP + 2 * CH;   // dS^T [key][q]
-  float* lse_s = reinterpret_cast<float*>(sD + 2 * CH);  // [128] log2-scaled LSE of the q tile
-  float* dl_s = lse_s + 128;                               // [128] delta of the q tile
-  uint64_t* bars = reinterpret_cast<uint64_t*>(dl_s + 128);
+  uint8_t* sQ = sV + NC * CH;          // NQS stages of [64 q][HD]: NC chunks of 64 rows each
+  uint8_t* sO = sQ + NQS * NC * CH64;  // dO, the same
+  uint8_t* sP = sO + NQS * NC * CH64;  // 2 buffers of P^T  [128 keys][64 q]
+  uint8_t* sD = sP + 2 * CH;           // 2 buffers of dS^T [128 keys][64 q]
+  float* ls = reinterpret_cast<float*>(sD + 2 * CH);  // [2][64] lse log2e of the sub-tile
+  float* dls = ls + 128;                              // [2][64] delta of the sub-tile
+  uint64_t* bars = reinterpret_cast<uint64_t*>(dls + 128);
   uint64_t* kv_full = bars;
-  uint64_t* qdo_full = bars + 1;
-  uint64_t* qdo_empty = bars + 2;
-  uint64_t* s_full = bars + 3;
-  uint64_t* p_full = bars + 4;
-  uint64_t* q_done = bars + 5;
-  uint64_t* st_free = bars + 6;
-  uint64_t* ld_ready = bars + 7;  // the row warps' LSE / delta stores of this tile are done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  uint64_t* qf = bars + 1;           // [NQS] Q / dO stage loaded
+  uint64_t* qe = qf + NQS;           // [NQS] Q / dO stage consumed
+  uint64_t* s_full = qe + NQS;       // [2] S^T, dP^T in TMEM
+  uint64_t* p_full = s_full + 2;     // [2] P^T, dS^T in shared memory (TMEM buffer read)
+  uint64_t* pd_free = p_full + 2;    // [2] P^T, dS^T consumed by the MMAs
+  uint64_t* ld_ready = pd_free + 2;  // [2] lse / delta staged
+  uint64_t* acc_full = ld_ready + 2; // dK, dV complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kb = blockIdx.x, g = blockIdx.y, n = blockIdx.z;
+  const int per_kb = nkv * n_seq;
+  const int kb = (int)(blockIdx.x / per_kb);  // key tile 0 has the most query sub-tiles
+  const int g = (int)(blockIdx.x % per_kb) / n_seq, n = (int)(blockIdx.x % n_seq);
   const int grp = nh / nkv;
-  const int nqb = (S + 127) / 128;
-  const int per_head = nqb - kb;
+  const int nqs = (S + 63) / 64;
+  const int per_head = nqs - 2 * kb;
   const int iters = grp * per_head;
   const int k0 = kb * 128;
   const int row0 = n * S;
-  const int64_t T = (int64_t)gridDim.z * S;
+  const int64_t T = (int64_t)n_seq * S;
   const int64_t ld = (int64_t)(nh + 2 * nkv) * HD;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(qdo_full, 1);
-    mbar_init(qdo_empty, 1);
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
-    mbar_init(q_done, 1);
-    mbar_init(st_free, 128);
-    mbar_init(ld_ready, 128);
+    for (int i = 0; i < NQS; ++i) {
+      mbar_init(&qf[i], 1);
+      mbar_init(&qe[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&pd_free[i], 1);
+      mbar_init(&ld_ready[i], 128);
+    }
+    mbar_init(acc_full, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tq) : "memory");
@@ -476,32 +518,35 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tSt = tmem, tdPt = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + HD;
-  bool kv_inflight = false, qdo_inflight = false;
-  uint32_t qdo_par = 0;
+  const uint32_t tdV = tmem + 256, tdK = tmem + 256 + HD;
+  bool kv_inflight = false;
+  uint32_t q_inflight = 0, q_par = 0;
 
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
       mbar_expect_tx(kv_full, 2 * NC * CH);
-      for (int c = 0; c < NC; ++c) {
-        tma_load(&tq, kv_full, sK + c * CH, (nh + g) * HD + 64 * c, row0 + k0);
-        tma_load(&tq, kv_full, sV + c * CH, (nh + nkv + g) * HD + 64 * c, row0 + k0);
-      }
+      for (int c = 0; c < NC; ++c)
+        for (int hf = 0; hf < 2; ++hf) {
+          tma_load(&tq, kv_full, sK + c * CH + hf * CH64, (nh + g) * HD + 64 * c, row0 + k0 + 64 * hf);
+          tma_load(&tq, kv_full, sV + c * CH + hf * CH64, (nh + nkv + g) * HD + 64 * c, row0 + k0 + 64 * hf);
+        }
       kv_inflight = true;
       for (int i = 0; i < iters && ok; ++i) {
-        const int h = g * grp + i / per_head, q0 = (kb + i % per_head) * 128;
-        if (!mbar_wait(qdo_empty, (uint32_t)((i & 1) ^ 1), abort_flag)) {
+        const int st = i % NQS;
+        const uint32_t u = (uint32_t)(i / NQS);
+        const int h = g * grp + i / per_head, q0 = (2 * kb + i % per_head) * 64;
+        if (!mbar_wait(&qe[st], (u & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
-        mbar_expect_tx(qdo_full, 2 * NC * CH);
+        mbar_expect_tx(&qf[st], 2 * NC * CH64);
         for (int c = 0; c < NC; ++c) {
-          tma_load(&tq, qdo_full, sQ + c * CH, h * HD + 64 * c, row0 + q0);
-          tma_load(&tdo, qdo_full, sO + c * CH, h * HD + 64 * c, row0 + q0);
+          tma_load(&tq, &qf[st], sQ + (st * NC + c) * CH64, h * HD + 64 * c, row0 + q0);
+          tma_load(&tdo, &qf[st], sO + (st * NC + c) * CH64, h * HD + 64 * c, row0 + q0);
         }
-        qdo_inflight = true;
-        qdo_par = (uint32_t)(i & 1);
+        q_inflight |= 1u << st;
+        q_par = (q_par & ~(1u << st)) | ((u & 1) << st);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -511,43 +556,53 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       bool ok = mbar_wait(kv_full, 0, abort_flag);
-      constexpr uint32_t I_S = idesc(128, 128, false, false);
-      constexpr uint32_t I_KV = idesc(128, HD, false, true);  // dV, dK: B = dO / Q as MN-major
-      constexpr uint32_t I_Q = idesc(128, HD, true, true);    // dQ: A = dS (MN-major), B = K (MN-major)
+      constexpr uint32_t I_S = idesc(128, 64, false, false);  // S^T, dP^T: both operands K-major over hd
+      constexpr uint32_t I_G = idesc(128, HD, false, true);   // dV, dK: B = dO / Q as MN-major
       const uint32_t aK = su32(sK), aV = su32(sV), aQ = su32(sQ), aO = su32(sO), aP = su32(sP), aD = su32(sD);
-      for (int i = 0; i < iters && ok; ++i) {
-        const uint32_t par = (uint32_t)(i & 1);
-        if (!mbar_wait(qdo_full, par, abort_flag) || !mbar_wait(st_free, par ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
+      auto issue_s = [&](int i) -> bool {
+        const int st = i % NQS, b = i & 1;
+        if (!mbar_wait(&qf[st], (uint32_t)((i / NQS) & 1), abort_flag)) return false;
         tc_fence_after();
+        const uint32_t tS = tmem + 128 * b, tP = tS + 64;
 #pragma unroll
         for (int c = 0; c < NC; ++c)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint32_t off = c * CH + k * 32;
-            tc_mma(tSt, sdesc(aK + off, 16, 1024), sdesc(aQ + off, 16, 1024), I_S, (c | k) != 0);
-            tc_mma(tdPt, sdesc(aV + off, 16, 1024), sdesc(aO + off, 16, 1024), I_S, (c | k) != 0);
+            const uint32_t oa = c * CH + k * 32, ob = (st * NC + c) * CH64 + k * 32;
+            tc_mma(tS, sdesc(aK + oa, 16, 1024), sdesc(aQ + ob, 16, 1024), I_S, (c | k) != 0);
+            tc_mma(tP, sdesc(aV + oa, 16, 1024), sdesc(aO + ob, 16, 1024), I_S, (c | k) != 0);
           }
-        tc_commit(s_full);
-        if (!mbar_wait(p_full, par, abort_flag)) {
+        tc_commit(&s_full[b]);
+        return true;
+      };
+      auto issue_g = [&](int i) -> bool {
+        const int st = i % NQS, b = i & 1;
+        if (!mbar_wait(&p_full[b], (uint32_t)((i >> 1) & 1), abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t pa = b * CH + kk * 32;                // K-major over the 64 queries
+          const uint32_t rows = st * NC * CH64 + kk * 16 * 128;  // 16 query rows of the MN-major tile
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          tc_mma(tdV, sdesc(aP + pa, 16, 1024), sdesc(aO + rows, CH64, 1024), I_G, acc);
+          tc_mma(tdK, sdesc(aD + pa, 16, 1024), sdesc(aQ + rows, CH64, 1024), I_G, acc);
+        }
+        tc_commit(&pd_free[b]);
+        tc_commit(&qe[st]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int i = 0; i < iters && ok; ++i) {
+        if (i + 1 < iters && !issue_s(i + 1)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t pa = (kk >> 2) * CH + (kk & 3) * 32;  // K-major over q
-          const uint32_t rows = kk * 16 * 128;                 // 16 rows of an MN-major tile
-          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          tc_mma(tdV, sdesc(aP + pa, 16, 1024), sdesc(aO + rows, CH, 1024), I_KV, acc);
-          tc_mma(tdK, sdesc(aD + pa, 16, 1024), sdesc(aQ + rows, CH, 1024), I_KV, acc);
-          tc_mma(tSt, sdesc(aD + rows, CH, 1024), sdesc(aK + rows, CH, 1024), I_Q, kk > 0 ? 1u : 0u);
+        if (!issue_g(i)) {
+          ok = false;
+          break;
         }
-        tc_commit(q_done);
-        tc_commit(qdo_empty);
       }
+      if (ok) tc_commit(acc_full);
       if (!ok) {
         *abort_flag = 1;
         atomicCAS(&g_attn_error, 0, 22);
@@ -555,116 +610,98 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     const int qw = warp & 3;
-    const int r = qw * 32 + lane;  // key row (S^T, dP^T, dV, dK) or query row (dQ)
+    const int r = qw * 32 + lane;  // key row of S^T, dP^T, dV, dK
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
     const int key = k0 + r;
-    uint8_t* prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
-    uint8_t* drow = sD + (r >> 3) * 1024 + (r & 7) * 128;
+    const int t = threadIdx.x - 64;  // staging entry: lse (t < 64) or delta (t >= 64) of query t % 64
+    float* stage = t < 64 ? ls : dls;
+    auto fetch = [&](int i) -> float {
+      const int h = g * grp + i / per_head, q = (2 * kb + i % per_head) * 64 + (t & 63);
+      if (q >= S) return 0.f;
+      const int64_t idx = (int64_t)h * T + row0 + q;
+      return t < 64 ? lse[idx] * 1.4426950408889634f : delta[idx];
+    };
     bool ok = true;
+    float nxt = fetch(0);  // one sub-tile ahead, so the global load latency hides behind a sub-tile
     for (int i = 0; i < iters; ++i) {
-      const int h = g * grp + i / per_head, q0 = (kb + i % per_head) * 128;
-      const uint32_t par = (uint32_t)(i & 1);
-      // LSE and delta of this query tile into shared memory: thread t loads
-      // entry t, then all wait (bounded) until the 128 stores are done.  The
-      // previous tile's readers finished before its p_full, which this
-      // thread's q_done wait already ordered before these stores.
-      {
-        const int t = threadIdx.x - 64;
-        const int q = q0 + t;
-        lse_s[t] = q < S ? lse[(int64_t)h * T + row0 + q] * 1.4426950408889634f : 0.f;
-        dl_s[t] = q < S ? delta[(int64_t)h * T + row0 + q] : 0.f;
-        mbar_arrive(ld_ready);
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait(ld_ready, par, abort_flag))) {
-        ok = false;
-        break;
-      }
-      const bool need_mask = (q0 < k0 + 127) || (q0 + 128 > S);
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full, par, abort_flag))) {
+      const int b = i & 1;
+      const uint32_t u = (uint32_t)(i >> 1);
+      const int q0 = (2 * kb + i % per_head) * 64;
+      // Buffer b was last read in sub-tile i-2; every thread finished that
+      // before it arrived on ld_ready for sub-tile i-1, which this thread has
+      // waited for.
+      stage[b * 64 + (t & 63)] = nxt;
+      mbar_arrive(&ld_ready[b]);
+      if (i + 1 < iters) nxt = fetch(i + 1);
+      bool w = mbar_wait(&ld_ready[b], u & 1, abort_flag);
+      if (w && i >= 2) w = mbar_wait(&pd_free[b], (u - 1) & 1, abort_flag);
+      if (w) w = mbar_wait(&s_full[b], u & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) {  // warp-uniform: the TMEM loads below are warp-collective
         ok = false;
         break;
       }
       tc_fence_after();
+      const bool need_mask = (q0 < k0 + 127) || (q0 + 64 > S);
+      const float* lrow = ls + b * 64;
+      const float* drow_d = dls + b * 64;
+      uint8_t* prow = sP + b * CH + (r >> 3) * 1024 + (r & 7) * 128;
+      uint8_t* drow = sD + b * CH + (r >> 3) * 1024 + (r & 7) * 128;
+      const uint32_t tS = tmem + 128 * b, tP = tS + 64;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float st[32], dp[32];
-        tmem_ld32(tSt + lane_off + c * 32, st);
-        tmem_ld32(tdPt + lane_off + c * 32, dp);
+        tmem_ld32(tS + lane_off + c * 32, st);
+        tmem_ld32(tP + lane_off + c * 32, dp);
         uint32_t pw[16], dw[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float pv[2], dv[2];
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int ql = c * 32 + e + t;
-            float p = exp2f(st[e + t] * scale_log2 - lse_s[ql]);
+          for (int tt = 0; tt < 2; ++tt) {
+            const int ql = c * 32 + e + tt;
+            float p = exp2f(st[e + tt] * scale_log2 - lrow[ql]);
             if (need_mask) {
               const int q = q0 + ql;
               if (q < key || q >= S) p = 0.f;
             }
-            pv[t] = p;
-            dv[t] = p * (dp[e + t] - dl_s[ql]);
+            pv[tt] = p;
+            dv[tt] = p * (dp[e + tt] - drow_d[ql]);
           }
           pw[e / 2] = pack2(pv[0], pv[1]);
           dw[e / 2] = pack2(dv[0], dv[1]);
         }
-        // 32 queries = 4 sixteen-byte units of row r in q-chunk c/2
-#pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4) {
-          const int unit = (c & 1) * 4 + u4;
-          const int off = (c >> 1) * CH + ((unit ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(prow + off) = make_uint4(pw[4 * u4], pw[4 * u4 + 1], pw[4 * u4 + 2], pw[4 * u4 + 3]);
-          *reinterpret_cast<uint4*>(drow + off) = make_uint4(dw[4 * u4], dw[4 * u4 + 1], dw[4 * u4 + 2], dw[4 * u4 + 3]);
-        }
+        store_row_units(prow, r, c, pw);
+        store_row_units(drow, r, c, dw);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
-      mbar_arrive(p_full);
-      if (!__all_sync(0xffffffffu, mbar_wait(q_done, par, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int q = q0 + r;
-      float* dst = dq_acc + ((int64_t)row0 + q) * ((int64_t)nh * HD) + (int64_t)h * HD;
-#pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        float t[32];
-        tmem_ld32(tSt + lane_off + c * 32, t);
-        if (q < S) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + e),
-                      make_float4(t[e] * scale, t[e + 1] * scale, t[e + 2] * scale, t[e + 3] * scale));
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(st_free);
+      mbar_arrive(&p_full[b]);
     }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
     if (ok) {
-      // dK, dV of this thread's key row (complete after the last q_done).  The
-      // TMEM loads are warp-collective: every lane loads, only valid rows store.
+      // dK, dV of this thread's key row.  The TMEM loads are warp-collective:
+      // every lane loads, only rows inside the sequence store.
       tc_fence_after();
       const bool valid = key < S;
       bf16* row = dqkv + ((int64_t)row0 + (valid ? key : 0)) * ld;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
-        float t[32];
-        tmem_ld32(tdK + lane_off + c * 32, t);
+        float v[32];
+        tmem_ld32(tdK + lane_off + c * 32, v);
         if (valid) {
 #pragma unroll
           for (int i4 = 0; i4 < 4; ++i4)
             reinterpret_cast<uint4*>(row + (int64_t)(nh + g) * HD + c * 32)[i4] = make_uint4(
-                pack2(t[8 * i4] * scale, t[8 * i4 + 1] * scale), pack2(t[8 * i4 + 2] * scale, t[8 * i4 + 3] * scale),
-                pack2(t[8 * i4 + 4] * scale, t[8 * i4 + 5] * scale), pack2(t[8 * i4 + 6] * scale, t[8 * i4 + 7] * scale));
+                pack2(v[8 * i4] * scale, v[8 * i4 + 1] * scale), pack2(v[8 * i4 + 2] * scale, v[8 * i4 + 3] * scale),
+                pack2(v[8 * i4 + 4] * scale, v[8 * i4 + 5] * scale), pack2(v[8 * i4 + 6] * scale, v[8 * i4 + 7] * scale));
         }
-        tmem_ld32(tdV + lane_off + c * 32, t);
+        tmem_ld32(tdV + lane_off + c * 32, v);
         if (valid) {
 #pragma unroll
           for (int i4 = 0; i4 < 4; ++i4)
             reinterpret_cast<uint4*>(row + (int64_t)(nh + nkv + g) * HD + c * 32)[i4] =
-                make_uint4(pack2(t[8 * i4], t[8 * i4 + 1]), pack2(t[8 * i4 + 2], t[8 * i4 + 3]),
-                           pack2(t[8 * i4 + 4], t[8 * i4 + 5]), pack2(t[8 * i4 + 6], t[8 * i4 + 7]));
+                make_uint4(pack2(v[8 * i4], v[8 * i4 + 1]), pack2(v[8 * i4 + 2], v[8 * i4 + 3]),
+                           pack2(v[8 * i4 + 4], v[8 * i4 + 5]), pack2(v[8 * i4 + 6], v[8 * i4 + 7]));
         }
       }
     } else if (lane == 0) {
@@ -678,9 +715,248 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (kv_inflight)
       while (!mbar_test(kv_full, 0) && clock64() - t0 < kWaitCycles) {
       }
-    if (qdo_inflight)
-      while (!mbar_test(qdo_full, qdo_par) && clock64() - t0 < kWaitCycles) {
+    for (int s2 = 0; s2 < NQS; ++s2)
+      if (q_inflight & (1u << s2))
+        while (!mbar_test(&qf[s2], (q_par >> s2) & 1) && clock64() - t0 < kWaitCycles) {
+        }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_bwd_q_k(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo, int S, int n_seq,
+                 int nh, int nkv, const float* __restrict__ lse, const float* __restrict__ delta, float scale,
+                 float scale_log2, bf16* __restrict__ dqkv) {
+  constexpr int NC = HD / 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = sm;                    // [128 q][HD]: NC chunks of 128 rows
+  uint8_t* sO = sQ + NC * CH;          // dO, the same
+  uint8_t* sK = sO + NC * CH;          // NKS stages of [64 keys][HD]
+  uint8_t* sV = sK + NKS * NC * CH64;  // the same
+  uint8_t* sS = sV + NKS * NC * CH64;  // 2 buffers of dS [128 q][64 keys]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + 2 * CH);
+  uint64_t* q_full = bars;
+  uint64_t* kf = bars + 1;          // [NKS]
+  uint64_t* ke = kf + NKS;          // [NKS]
+  uint64_t* s_full = ke + NKS;      // [2]
+  uint64_t* p_full = s_full + 2;    // [2]
+  uint64_t* ds_free = p_full + 2;   // [2]
+  uint64_t* acc_full = ds_free + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nqb = (S + 127) / 128;
+  const int per_qb = nh * n_seq;
+  const int qb = nqb - 1 - (int)(blockIdx.x / per_qb);  // the last query tile has the most keys
+  const int h = (int)(blockIdx.x % per_qb) / n_seq, n = (int)(blockIdx.x % n_seq);
+  const int kh = h / (nh / nkv);
+  const int q0 = qb * 128;
+  const int nkt = min((S + 63) / 64, 2 * qb + 2);
+  const int row0 = n * S;
+  const int64_t T = (int64_t)n_seq * S;
+  const int64_t ld = (int64_t)(nh + 2 * nkv) * HD;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < NKS; ++i) {
+      mbar_init(&kf[i], 1);
+      mbar_init(&ke[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&ds_free[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tq) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tdo) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                 "r"(512));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tdQ = tmem + 256;
+  bool q_inflight = false;
+  uint32_t k_inflight = 0, k_par = 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      mbar_expect_tx(q_full, 2 * NC * CH);
+      for (int c = 0; c < NC; ++c)
+        for (int hf = 0; hf < 2; ++hf) {
+          tma_load(&tq, q_full, sQ + c * CH + hf * CH64, h * HD + 64 * c, row0 + q0 + 64 * hf);
+          tma_load(&tdo, q_full, sO + c * CH + hf * CH64, h * HD + 64 * c, row0 + q0 + 64 * hf);
+        }
+      q_inflight = true;
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int st = j % NKS;
+        const uint32_t u = (uint32_t)(j / NKS);
+        if (!mbar_wait(&ke[st], (u & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(&kf[st], 2 * NC * CH64);
+        for (int c = 0; c < NC; ++c) {
+          tma_load(&tq, &kf[st], sK + (st * NC + c) * CH64, (nh + kh) * HD + 64 * c, row0 + 64 * j);
+          tma_load(&tq, &kf[st], sV + (st * NC + c) * CH64, (nh + nkv + kh) * HD + 64 * c, row0 + 64 * j);
+        }
+        k_inflight |= 1u << st;
+        k_par = (k_par & ~(1u << st)) | ((u & 1) << st);
       }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicCAS(&g_attn_error, 0, 24);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      constexpr uint32_t I_S = idesc(128, 64, false, false);  // S, dP: K-major over hd
+      constexpr uint32_t I_G = idesc(128, HD, false, true);   // dQ: B = K_j as MN-major
+      const uint32_t aQ = su32(sQ), aO = su32(sO), aK = su32(sK), aV = su32(sV), aS = su32(sS);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % NKS, b = j & 1;
+        if (!mbar_wait(&kf[st], (uint32_t)((j / NKS) & 1), abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t tS = tmem + 128 * b, tP = tS + 64;
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t oa = c * CH + k * 32, ob = (st * NC + c) * CH64 + k * 32;
+            tc_mma(tS, sdesc(aQ + oa, 16, 1024), sdesc(aK + ob, 16, 1024), I_S, (c | k) != 0);
+            tc_mma(tP, sdesc(aO + oa, 16, 1024), sdesc(aV + ob, 16, 1024), I_S, (c | k) != 0);
+          }
+        tc_commit(&s_full[b]);
+        return true;
+      };
+      auto issue_g = [&](int j) -> bool {
+        const int st = j % NKS, b = j & 1;
+        if (!mbar_wait(&p_full[b], (uint32_t)((j >> 1) & 1), abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma(tdQ, sdesc(aS + b * CH + kk * 32, 16, 1024), sdesc(aK + st * NC * CH64 + kk * 16 * 128, CH64, 1024),
+                 I_G, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&ds_free[b]);
+        tc_commit(&ke[st]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < nkt && ok; ++j) {
+        if (j + 1 < nkt && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
+        if (!issue_g(j)) {
+          ok = false;
+          break;
+        }
+      }
+      if (ok) tc_commit(acc_full);
+      if (!ok) {
+        *abort_flag = 1;
+        atomicCAS(&g_attn_error, 0, 25);
+      }
+    }
+  } else {
+    const int qw = warp & 3;
+    const int r = qw * 32 + lane;  // query row of S, dP, dQ
+    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+    const int q = q0 + r;
+    const bool valid = q < S;
+    const int64_t li = (int64_t)h * T + row0 + (valid ? q : 0);
+    const float lse2 = valid ? lse[li] * 1.4426950408889634f : 0.f;
+    const float dl = valid ? delta[li] : 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkt; ++j) {
+      const int b = j & 1;
+      const uint32_t u = (uint32_t)(j >> 1);
+      bool w = true;
+      if (j >= 2) w = mbar_wait(&ds_free[b], (u - 1) & 1, abort_flag);
+      if (w) w = mbar_wait(&s_full[b], u & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int k0 = 64 * j;
+      const bool need_mask = (k0 + 63 > q0) || (k0 + 64 > S);
+      uint8_t* srow = sS + b * CH + (r >> 3) * 1024 + (r & 7) * 128;
+      const uint32_t tS = tmem + 128 * b, tP = tS + 64;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float sv[32], dp[32];
+        tmem_ld32(tS + lane_off + c * 32, sv);
+        tmem_ld32(tP + lane_off + c * 32, dp);
+        uint32_t dw[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float dv[2];
+#pragma unroll
+          for (int tt = 0; tt < 2; ++tt) {
+            float p = exp2f(sv[e + tt] * scale_log2 - lse2);
+            if (need_mask) {
+              const int key = k0 + c * 32 + e + tt;
+              if (key > q || key >= S) p = 0.f;
+            }
+            dv[tt] = p * (dp[e + tt] - dl);
+          }
+          dw[e / 2] = pack2(dv[0], dv[1]);
+        }
+        store_row_units(srow, r, c, dw);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(&p_full[b]);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
+    if (ok) {
+      tc_fence_after();
+      bf16* row = dqkv + ((int64_t)row0 + (valid ? q : 0)) * ld + (int64_t)h * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        float v[32];
+        tmem_ld32(tdQ + lane_off + c * 32, v);
+        if (valid) {
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4)
+            reinterpret_cast<uint4*>(row + c * 32)[i4] = make_uint4(
+                pack2(v[8 * i4] * scale, v[8 * i4 + 1] * scale), pack2(v[8 * i4 + 2] * scale, v[8 * i4 + 3] * scale),
+                pack2(v[8 * i4 + 4] * scale, v[8 * i4 + 5] * scale), pack2(v[8 * i4 + 6] * scale, v[8 * i4 + 7] * scale));
+        }
+      }
+    } else if (lane == 0) {
+      *abort_flag = 1;
+      atomicCAS(&g_attn_error, 0, 26);
+    }
+  }
+
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    const long long t0 = clock64();
+    if (q_inflight)
+      while (!mbar_test(q_full, 0) && clock64() - t0 < kWaitCycles) {
+      }
+    for (int s2 = 0; s2 < NKS; ++s2)
+      if (k_inflight & (1u << s2))
+        while (!mbar_test(&kf[s2], (k_par >> s2) & 1) && clock64() - t0 < kWaitCycles) {
+        }
   }
   tc_fence_before();
   __syncthreads();
@@ -732,15 +1008,10 @@ cudaError_t launch(const bf16* qkv, int n_seq, int S, int nh, int nkv, bf16* o, 
   return cudaGetLastError();
 }
 
-template <int HD>
-constexpr int bwd_smem_bytes() {
-  return (HD / 64) * 16384 * 4 + 4 * 16384 + 1024 + 1024 + 256;
-}
-
-bool make_map128(CUtensorMap* m, const bf16* base, int64_t ld, int64_t rows) {
+bool make_map(CUtensorMap* m, const bf16* base, int64_t ld, int64_t rows, int box_rows) {
   const cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<bf16*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -749,38 +1020,44 @@ bool make_map128(CUtensorMap* m, const bf16* base, int64_t ld, int64_t rows) {
 
 template <int HD>
 cudaError_t launch_bwd(const bf16* qkv, const bf16* dout, const float* lse, const float* delta, int n_seq, int S,
-                       int nh, int nkv, bf16* dqkv, float* dq_acc, cudaStream_t s) {
+                       int nh, int nkv, bf16* dqkv, cudaStream_t s) {
   const int64_t T = (int64_t)n_seq * S;
-  CUtensorMap mq, mo;
-  if (!make_map128(&mq, qkv, (int64_t)(nh + 2 * nkv) * HD, T) || !make_map128(&mo, dout, (int64_t)nh * HD, T))
+  CUtensorMap mq, mo;  // 64-row boxes: sub-tiles load as one box, 128-row tiles as two
+  if (!make_map(&mq, qkv, (int64_t)(nh + 2 * nkv) * HD, T, 64) || !make_map(&mo, dout, (int64_t)nh * HD, T, 64))
     return cudaErrorInvalidValue;
-  constexpr int SM = bwd_smem_bytes<HD>();
-  cudaError_t e = cudaFuncSetAttribute(attn_bwd_tc_k<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SM);
+  constexpr int SKV = kv_smem_bytes<HD>(), SQ = q_smem_bytes<HD>();
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_kv_k<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SKV);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attn_bwd_q_k<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SQ);
   if (e != cudaSuccess) return e;
   const float scale = 1.f / sqrtf((float)HD);
-  dim3 grid((S + 127) / 128, nkv, n_seq);
-  attn_bwd_tc_k<HD><<<grid, THREADS, SM, s>>>(mq, mo, S, nh, nkv, lse, delta, scale, scale * 1.4426950408889634f,
-                                              dqkv, dq_acc);
+  const int64_t nqb = (S + 127) / 128;
+  const int64_t gkv = nqb * nkv * n_seq, gq = nqb * nh * n_seq;
+  if (gkv > 0x7fffffff || gq > 0x7fffffff) return cudaErrorInvalidValue;
+  attn_bwd_kv_k<HD><<<(unsigned)gkv, THREADS, SKV, s>>>(mq, mo, S, n_seq, nh, nkv, lse, delta, scale,
+                                                         scale * 1.4426950408889634f, dqkv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_bwd_q_k<HD><<<(unsigned)gq, THREADS, SQ, s>>>(mq, mo, S, n_seq, nh, nkv, lse, delta, scale,
+                                                      scale * 1.4426950408889634f, dqkv);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-// Tensor-core attention backward core: dK and dV into dqkv (BF16), dQ added
-// (already scaled) into the zeroed FP32 dq_acc ([T][nh*hd]).  delta[h][t] =
-// rowsum(dO o O) must be precomputed.
+// Tensor-core attention backward core: dQ, dK and dV into dqkv (BF16, the
+// layout of qkv); delta[h][t] = rowsum(dO o O) must be precomputed.
 cudaError_t attention_bwd_tc_core(const bf16* qkv, const bf16* dout, const float* lse, const float* delta,
-                                  int n_seq, int S, int nh, int nkv, int hd, bf16* dqkv, float* dq_acc,
-                                  cudaStream_t s) {
+                                  int n_seq, int S, int nh, int nkv, int hd, bf16* dqkv, cudaStream_t s) {
   std::call_once(g_once, init_once);
   if (g_init != cudaSuccess) return g_init;
   if (n_seq <= 0 || S <= 0) return cudaSuccess;
-  if (nh % nkv || n_seq > 65535 || nkv > 65535 || (int64_t)n_seq * S > 0x7fffffff) return cudaErrorInvalidValue;
-  if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dqkv) |
-       reinterpret_cast<uintptr_t>(dq_acc)) & 15)
+  if (nh % nkv || (int64_t)n_seq * S > 0x7fffffff) return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dqkv)) &
+      15)
     return cudaErrorInvalidValue;
-  if (hd == 64) return launch_bwd<64>(qkv, dout, lse, delta, n_seq, S, nh, nkv, dqkv, dq_acc, s);
-  if (hd == 128) return launch_bwd<128>(qkv, dout, lse, delta, n_seq, S, nh, nkv, dqkv, dq_acc, s);
+  if (hd == 64) return launch_bwd<64>(qkv, dout, lse, delta, n_seq, S, nh, nkv, dqkv, s);
+  if (hd == 128) return launch_bwd<128>(qkv, dout, lse, delta, n_seq, S, nh, nkv, dqkv, s);
   return cudaErrorInvalidValue;
 }
 

@@ -99,16 +99,14 @@ cudaError_t attention_fwd(const bf16* qkv, int n_seq, int S, int nh, int nkv, in
 // attention_fwd).
 cudaError_t attention_fwd_tc(const bf16* qkv, int n_seq, int S, int nh, int nkv, int hd, bf16* o, float* lse,
                              cudaStream_t s);
-// Tensor-core backward core (dK, dV into dqkv; scaled dQ added into the
-// zeroed FP32 dq_acc); delta = rowsum(dO o O) precomputed.  Used by
-// attention_bwd.
+// Tensor-core backward core: dQ, dK, dV into dqkv (BF16); delta =
+// rowsum(dO o O) precomputed.  Used by attention_bwd.
 cudaError_t attention_bwd_tc_core(const bf16* qkv, const bf16* dout, const float* lse, const float* delta,
-                                  int n_seq, int S, int nh, int nkv, int hd, bf16* dqkv, float* dq_acc,
-                                  cudaStream_t s);
-// Backward: dqkv ([T][(nh+2nkv)hd]) receives dq, dk, dv.  delta ([nh][T]) and
-// dq_acc ([T][nh*hd] fp32) are scratch.
+                                  int n_seq, int S, int nh, int nkv, int hd, bf16* dqkv, cudaStream_t s);
+// Backward: dqkv ([T][(nh+2nkv)hd]) receives dq, dk, dv.  delta ([nh][T]
+// fp32) is scratch.
 cudaError_t attention_bwd(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout,
                           int n_seq, int S, int nh, int nkv, int hd, bf16* dqkv, float* delta,
-                          float* dq_acc, cudaStream_t s);
+                          cudaStream_t s);
 
 }  // namespace mt

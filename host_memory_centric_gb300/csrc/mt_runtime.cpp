@@ -59,7 +59,7 @@ struct Dev {
        *dattn = nullptr;
   bf16 *gu = nullptr, *dgu = nullptr, *h = nullptr, *dh = nullptr, *dyn = nullptr, *dx1 = nullptr,
        *dxn = nullptr, *logits = nullptr;
-  float *rstd1 = nullptr, *rstd2 = nullptr, *lse = nullptr, *delta = nullptr, *dq_acc = nullptr,
+  float *rstd1 = nullptr, *rstd2 = nullptr, *lse = nullptr, *delta = nullptr,
         *row_loss = nullptr, *loss = nullptr, *rms_part = nullptr, *dwacc = nullptr, *cs = nullptr;
   int32_t *tok = nullptr, *tgt = nullptr, *csr_start = nullptr, *csr_rows = nullptr;
 };
@@ -235,7 +235,6 @@ size_t carve(const mt_config* c, const std::vector<mth::BlockDesc>& lay, uint8_t
   d->rstd2 = (float*)take(T * 4);
   d->lse = (float*)take(nh * T * 4);
   d->delta = (float*)take(nh * T * 4);
-  d->dq_acc = (float*)take(T * nh * hd * 4);
   d->row_loss = (float*)take(T * 4);
   d->loss = (float*)take(256);
   d->rms_part = (float*)take(mt::rmsnorm_bwd_partial_floats(T, (int)H) * 4);
@@ -419,7 +418,7 @@ mt_status decoder_backward(mt_model* m, const View& v, const bf16* x, const bf16
     const double fl = 10.0 * m->M * m->B * (double)m->nh * m->hd * (double)m->S * m->S / 2;
     Timed t(m, K_ATTN_B, fl, 0, 3);
     CU(m, mt::attention_bwd(d.qkv, d.attn, d.lse, d.dattn, m->M * m->B, m->S, m->nh, m->nkv, m->hd, d.dqkv,
-                            d.delta, d.dq_acc, s));
+                            d.delta, s));
   }
   {
     Timed t(m, K_OTHER, 0, 4.0 * T * (m->nh + m->nkv) * m->hd);
@@ -1397,8 +1396,8 @@ mt_status mt_attention_fwd(const void* qkv, int32_t n_seq, int32_t S, int32_t nh
 }
 
 size_t mt_attention_bwd_scratch_bytes(int32_t n_seq, int32_t S, int32_t nh, int32_t hd) {
-  const size_t T = (size_t)n_seq * S;
-  return (size_t)up((int64_t)(T * nh * 4), 256) + T * nh * hd * 4;
+  (void)hd;
+  return (size_t)n_seq * (size_t)S * (size_t)nh * 4;  // delta [nh][T] FP32
 }
 
 mt_status mt_attention_bwd(const void* qkv, const void* o, const float* lse, const void* dout, int32_t n_seq,
@@ -1406,11 +1405,8 @@ mt_status mt_attention_bwd(const void* qkv, const void* o, const float* lse, con
                            size_t scratch_bytes, void* stream) {
   if (!qkv || !o || !lse || !dout || !dqkv || !scratch || nkv <= 0) return MT_ERR_ARG;
   if (scratch_bytes < mt_attention_bwd_scratch_bytes(n_seq, S, nh, hd)) return MT_ERR_ARG;
-  const size_t T = (size_t)n_seq * S;
-  float* delta = (float*)scratch;
-  float* dq = (float*)((uint8_t*)scratch + up((int64_t)(T * nh * 4), 256));
   return cu_status(mt::attention_bwd((const bf16*)qkv, (const bf16*)o, lse, (const bf16*)dout, n_seq, S, nh, nkv, hd,
-                                     (bf16*)dqkv, delta, dq, (cudaStream_t)stream));
+                                     (bf16*)dqkv, (float*)scratch, (cudaStream_t)stream));
 }
 
 mt_status mt_swiglu_fwd(const void* gu, int64_t T, int32_t F, void* h, void* stream) {

@@ -241,8 +241,9 @@ mt_status mt_rope(void* x, int64_t T, int64_t ld, int32_t n_heads, int32_t hd, i
  * o [T][nh hd]; lse [nh][T] FP32 (natural log).  hd in {64, 128}. */
 mt_status mt_attention_fwd(const void* qkv, int32_t n_seq, int32_t S, int32_t nh, int32_t nkv,
                            int32_t hd, void* o, float* lse, void* stream);
-/* Backward into dqkv (same layout as qkv); scratch of
- * mt_attention_bwd_scratch_bytes bytes. */
+/* Backward into dqkv (same layout as qkv; every element written); scratch of
+ * mt_attention_bwd_scratch_bytes bytes (n_seq * S * nh FP32 values: the row
+ * sums delta = rowsum(dO o O)), device memory owned by the caller. */
 mt_status mt_attention_bwd(const void* qkv, const void* o, const float* lse, const void* dout,
                            int32_t n_seq, int32_t S, int32_t nh, int32_t nkv, int32_t hd,
                            void* dqkv, void* scratch, size_t scratch_bytes, void* stream);

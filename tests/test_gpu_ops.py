@@ -168,7 +168,15 @@ def test_swiglu(orc):
 
 
 # ------------------------------------------------------------------ attention
-@pytest.mark.parametrize("hd,nh,nkv,S,n_seq", [(64, 4, 4, 150, 2), (128, 4, 2, 200, 1), (128, 8, 2, 64, 3)])
+@pytest.mark.parametrize("hd,nh,nkv,S,n_seq", [
+    (64, 4, 4, 150, 2),    # MHA, ragged 128-tile, two sequences
+    (128, 4, 2, 200, 1),   # ragged 64- and 128-sub-tiles
+    (128, 8, 2, 64, 3),    # one sub-tile per sequence
+    (128, 7, 1, 300, 1),   # seven query heads per kv head (the 7.6B grouping)
+    (128, 2, 2, 33, 2),    # shorter than one sub-tile
+    (64, 2, 1, 129, 1),    # one row past a tile
+    (128, 4, 4, 512, 1),   # several full tiles on and off the diagonal
+])
 def test_attention_fwd_bwd(orc, hd, nh, nkv, S, n_seq):
     T = n_seq * S
     qkv = rnd((T, (nh + 2 * nkv) * hd), 20)
@@ -180,7 +188,7 @@ def test_attention_fwd_bwd(orc, hd, nh, nkv, S, n_seq):
     o_ref, lse_ref = orc.attention_fwd(f64(qg), n_seq, S, nh, nkv, hd)
     close(f64(o), o_ref, rel=1e-2)
     assert np.allclose(lse.cpu().numpy().T, lse_ref, atol=2e-3)
-    dq = torch.empty_like(qg)
+    dq = torch.full_like(qg, float("nan"))  # every element must be written
     scratch = torch.empty(ops.attention_bwd_scratch_bytes(n_seq, S, nh, hd), dtype=torch.uint8, device="cuda")
     dg = bf(dout)
     ops.attention_bwd(qg, o, lse, dg, n_seq, S, nh, nkv, hd, dq, scratch)

@@ -39,17 +39,21 @@ def _no_kernel_errors():
     assert ops.kernel_error(clear=True) == 0
 
 
-def run_parity(orc, c, steps, **rt):
+def run_parity(orc, c, steps, check_init=True, **rt):
     oc = oracle_shape(c)
     m = mt.Model(c, log_protocol=1, n_host_threads=4, seed=1234, **rt)
     lay = orc.layout(oc)
     nb = len(lay)
     # the library's initial store equals the oracle's initialiser bit for bit
+    # (checked here, or for very large blocks by the host-side init tests)
     master_o, m_o, v_o = [], [], []
     for j in range(nb):
         got = m.read(j, mt.REGION_MASTER)
-        exp = orc.init_block(oc, 1234, j)
-        assert np.array_equal(got.view(np.uint32), exp.view(np.uint32)), j
+        if check_init:
+            exp = orc.init_block(oc, 1234, j)
+            assert np.array_equal(got.view(np.uint32), exp.view(np.uint32)), j
+        else:
+            exp = got
         assert np.array_equal(m.read(j, mt.REGION_W), orc.bf16_rne_fast(exp))
         master_o.append(exp.copy())
         m_o.append(np.zeros_like(exp))
