@@ -42,10 +42,11 @@ def peaks():
     return dict(FALLBACK_PEAKS)
 
 
-def model_numbers(c):
+def model_numbers(c, ckpt_interval=1):
     """Parameter count P, tensor FLOPs the method executes per step (forward,
-    block recompute, backward; causal attention; head once), and the pages'
-    6NT + 12 L B S^2 H convention."""
+    block recompute, backward; causal attention; head once; with a checkpoint
+    interval c > 1 also the segment forwards rebuilt in the backward, L - nseg
+    extra layer forwards), and the pages' 6NT + 12 L B S^2 H convention."""
     L, H, nh, nkv, hd, F, V = (c[k] for k in ("n_layers", "hidden", "n_heads", "n_kv_heads", "head_dim", "ffn",
                                               "vocab"))
     B, S, M = c["batch"], c["seq"], c["micro"]
@@ -53,6 +54,8 @@ def model_numbers(c):
     P_mm = H * (nh + 2 * nkv) * hd + nh * hd * H + 3 * H * F
     P = L * (P_mm + 2 * H) + 2 * V * H + H
     F_exec = M * (L * (8 * t * P_mm + 9 * B * nh * hd * S * S) + 6 * t * H * V)
+    n_recomp = L - -(-L // ckpt_interval)
+    F_exec += M * n_recomp * (2 * t * P_mm + 2 * B * nh * hd * S * S)
     F_pages = 6 * P * M * t + 12 * L * B * M * S * S * H
     return P, F_exec, F_pages
 
@@ -176,7 +179,7 @@ def mem_available_bytes() -> int:
     return 0
 
 
-def host_bytes_needed(c: dict, slabs: int, ckpt_on_host: int) -> int:
+def host_bytes_needed(c: dict, slabs: int, ckpt_on_host: int, ckpt_interval: int = 1) -> int:
     """Host RAM one replica allocates: the flat store, the pinned gradient
     slabs (largest block's gradient region each) and the checkpoints."""
     import ctypes
@@ -184,7 +187,8 @@ def host_bytes_needed(c: dict, slabs: int, ckpt_on_host: int) -> int:
     cfg = mt.make_config(c)
     store = mt.lib().mt_store_bytes(ctypes.byref(cfg))
     wb = max(2 * b["n_pad"] for b in mt.layout(cfg))
-    ckpt = c["n_layers"] * c["micro"] * c["batch"] * c["seq"] * c["hidden"] * 2 if ckpt_on_host else 0
+    nseg = -(-c["n_layers"] // ckpt_interval)
+    ckpt = nseg * c["micro"] * c["batch"] * c["seq"] * c["hidden"] * 2 if ckpt_on_host else 0
     return int(store + slabs * wb + 2 * wb + ckpt)
 
 
@@ -250,6 +254,8 @@ def main():
     ap.add_argument("--slabs", type=int, default=12)
     ap.add_argument("--keep-host-grad", type=int, default=1)
     ap.add_argument("--ckpt-on-host", type=int, default=1)
+    ap.add_argument("--ckpt-interval", type=int, default=1, help="layers per recompute segment")
+    ap.add_argument("--buffers", type=int, default=2, help="device weight buffers (1: single-buffer ablation)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -278,11 +284,11 @@ def main():
 
     c = configs.get(args.config)
     T = c["micro"] * c["batch"] * c["seq"]
-    P, F_exec, F_pages = model_numbers(c)
+    P, F_exec, F_pages = model_numbers(c, args.ckpt_interval)
     # every replica on this host holds its own host state: refuse to start
     # rather than exhaust host RAM
     local_world = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
-    need = local_world * host_bytes_needed(c, args.slabs, args.ckpt_on_host)
+    need = local_world * host_bytes_needed(c, args.slabs, args.ckpt_on_host, args.ckpt_interval)
     avail = mem_available_bytes()
     if avail and need > 0.85 * avail:
         msg = (f"{local_world} replica(s) of the {args.config} workload need {need / 1e9:.1f} GB of host RAM; "
@@ -296,7 +302,8 @@ def main():
     t_init = time.time()
     hbw = mt.host_bandwidth(1 << 30)
     m = mt.Model(c, seed=1234, pin_store=args.pin_store, n_host_threads=args.threads, n_grad_slabs=args.slabs,
-                 keep_host_grad=args.keep_host_grad, ckpt_on_host=args.ckpt_on_host)
+                 keep_host_grad=args.keep_host_grad, ckpt_on_host=args.ckpt_on_host,
+                 ckpt_interval=args.ckpt_interval, n_buffers=args.buffers)
     init_s = time.time() - t_init
     toks = [inputs.tokens_for(c, s) for s in range(args.warmup + 2 * args.steps + 1)]
     step = 0
@@ -398,7 +405,8 @@ def main():
                    "global_batch": world * c["batch"] * c["micro"], "seq_len": c["seq"],
                    "tokens_per_step": T, "parallelism": f"replicas x{world} (no exchange step)",
                    "pin_store": args.pin_store, "n_grad_slabs": args.slabs, "keep_host_grad": args.keep_host_grad,
-                   "ckpt_on_host": args.ckpt_on_host, "l2": "inputs larger than L2 (every step streams "
+                   "ckpt_on_host": args.ckpt_on_host, "ckpt_interval": args.ckpt_interval,
+                   "n_buffers": args.buffers, "l2": "inputs larger than L2 (every step streams "
                    f"{2 * P / 1e9:.2f} GB of weights in and out)"},
         "step_roofline": {"frac": t_roof / t_step, "t_roof_ms": t_roof * 1e3, "t_step_ms": t_step * 1e3,
                           "bound": "tensor" if t_compute >= t_link else "host link",

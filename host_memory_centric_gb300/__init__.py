@@ -43,7 +43,8 @@ class MtConfig(C.Structure):
                 ("n_host_threads", C.c_int32), ("lr", C.c_float), ("beta1", C.c_float),
                 ("beta2", C.c_float), ("adam_eps", C.c_float), ("weight_decay", C.c_float),
                 ("seed", C.c_uint64), ("timeout_ms", C.c_uint32), ("pin_store", C.c_int32),
-                ("head_chunk", C.c_int32), ("log_protocol", C.c_int32), ("keep_host_grad", C.c_int32)]
+                ("head_chunk", C.c_int32), ("log_protocol", C.c_int32), ("keep_host_grad", C.c_int32),
+                ("n_buffers", C.c_int32)]
 
 
 class DevRegion(C.Structure):
@@ -106,6 +107,7 @@ def lib():
         "mt_host_adam": (i32, [i64, _P(u16), _P(f32), _P(f32), _P(f32), _P(u16), i32, f32, f32, f32,
                                f32, f32, i32]),
         "mt_plan_protocol": (i64, [pc, i32, C.c_char_p, i64]),
+        "mt_visit_plan": (i32, [pc, _P(i32), _P(i32), i32]),
         "mt_schedule": (i32, [i32, _P(f64), _P(f64), _P(f64), _P(f64), f64, f64, _P(f64)]),
         "mt_token_csr": (i32, [_P(i32), i64, i32, _P(i32), _P(i32)]),
         "mt_host_bandwidth": (i32, [sz, i32, _P(f64), _P(f64)]),
@@ -162,6 +164,18 @@ def make_config(shape: dict, **rt) -> MtConfig:
 def _ptr(a: np.ndarray, ct):
     assert a.flags["C_CONTIGUOUS"]
     return a.ctypes.data_as(_P(ct))
+
+
+def visit_plan(cfg: MtConfig) -> list[tuple[int, int]]:
+    """(kind, block) of every visit of one step; kind 0 forward, 1 head,
+    2 recompute (driven with step_forward), 3 block backward."""
+    n = lib().mt_visit_plan(C.byref(cfg), None, None, 0)
+    if n < 0:
+        raise MtError(-1, "invalid config")
+    k = (C.c_int32 * n)()
+    b = (C.c_int32 * n)()
+    lib().mt_visit_plan(C.byref(cfg), k, b, n)
+    return list(zip(k, b))
 
 
 def host_bandwidth(nbytes: int = 1 << 30, threads: int = 0) -> dict:

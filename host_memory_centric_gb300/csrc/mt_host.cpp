@@ -18,7 +18,8 @@ bool config_valid(const mt_config* c, std::string* why) {
     return bad("non-positive shape field");
   if (c->n_heads % c->n_kv_heads) return bad("n_heads must be a multiple of n_kv_heads");
   if (c->hidden % 8 || c->ffn % 8 || c->head_dim % 16) return bad("hidden, ffn must be multiples of 8; head_dim of 16");
-  if (c->ckpt_interval != 1) return bad("ckpt_interval must be 1");
+  if (c->ckpt_interval < 1 || c->ckpt_interval > c->n_layers) return bad("ckpt_interval must be in [1, n_layers]");
+  if (c->n_buffers != 1 && c->n_buffers != 2) return bad("n_buffers must be 1 or 2");
   if (c->n_grad_slabs < 1 || c->n_grad_slabs > 256) return bad("n_grad_slabs out of range");
   if (c->timeout_ms == 0) return bad("timeout_ms must be positive");
   if (!(c->rms_eps > 0) || !(c->rope_base > 1)) return bad("rms_eps / rope_base");

@@ -54,7 +54,8 @@ struct Job {
 struct Dev {
   uint8_t* buf[2] = {nullptr, nullptr};
   bf16 *xslot[2] = {nullptr, nullptr}, *xck[2] = {nullptr, nullptr}, *dx[2] = {nullptr, nullptr};
-  bf16 *ckdev = nullptr, *xlast = nullptr;
+  bf16 *ckdev = nullptr, *fx[2] = {nullptr, nullptr};  // device checkpoints; non-kept forward outputs
+  std::vector<bf16*> seg;  // X_{s+1} .. X_{s+c-1} of the segment being recomputed
   bf16 *xn = nullptr, *x1 = nullptr, *yn = nullptr, *qkv = nullptr, *dqkv = nullptr, *attn = nullptr,
        *dattn = nullptr;
   bf16 *gu = nullptr, *dgu = nullptr, *h = nullptr, *dh = nullptr, *dyn = nullptr, *dx1 = nullptr,
@@ -63,6 +64,34 @@ struct Dev {
         *row_loss = nullptr, *loss = nullptr, *rms_part = nullptr, *dwacc = nullptr, *cs = nullptr;
   int32_t *tok = nullptr, *tgt = nullptr, *csr_start = nullptr, *csr_rows = nullptr;
 };
+
+// One visit of the step: 0 FWD, 1 HEAD (fused forward and backward), 2 RECOMP
+// (forward rebuilding a segment's activations), 3 BWD.  seg numbers the
+// backward's segments from the top; `first` marks the visit that loads the
+// segment's checkpoint.
+struct VisitDesc {
+  int kind, j, seg;
+  bool first;
+};
+enum { V_FWD = 0, V_HEAD = 1, V_RECOMP = 2, V_BWD = 3 };
+
+// Block-wise recomputation with checkpoint interval c: X_s is kept for
+// s = 0, c, 2c, ... < L; the decoder layers form segments [s+1, min(s+c, L)]
+// handled from the top, each recomputing X_{s+1} .. X_{e-1} from X_s and then
+// running the backward of layers e .. s+1.
+std::vector<VisitDesc> build_plan(int L, int c) {
+  std::vector<VisitDesc> p;
+  for (int j = 0; j <= L; ++j) p.push_back({V_FWD, j, -1, false});
+  p.push_back({V_HEAD, L + 1, -1, false});
+  const int nseg = (L + c - 1) / c;
+  for (int k = 0; k < nseg; ++k) {
+    const int s = (nseg - 1 - k) * c, e = s + c < L ? s + c : L;
+    for (int j = s + 1; j < e; ++j) p.push_back({V_RECOMP, j, k, j == s + 1});
+    for (int j = e; j > s; --j) p.push_back({V_BWD, j, k, j == s + 1 && e == s + 1});
+  }
+  p.push_back({V_BWD, 0, -1, false});
+  return p;
+}
 
 struct KStat {
   int64_t launches = 0;  // kernels launched
@@ -81,6 +110,8 @@ struct mt_model {
   int L = 0, H = 0, nh = 0, nkv = 0, hd = 0, F = 0, V = 0, B = 0, S = 0, M = 0, Nqkv = 0;
   int64_t T = 0, chunk = 0;
   std::vector<mth::BlockDesc> lay;
+  std::vector<VisitDesc> plan;
+  int nbuf = 2, ci = 1, nseg = 0;
   int64_t wb_max = 0;
   bool live = false;  // false: scheduler dry run (log only)
   // host memory
@@ -207,15 +238,18 @@ size_t carve(const mt_config* c, const std::vector<mth::BlockDesc>& lay, uint8_t
     return p;
   };
   const int64_t act = T * H * 2;
-  for (int b = 0; b < 2; ++b) d->buf[b] = take(2 * wb);
+  const int64_t ci = c->ckpt_interval, nseg = (L + ci - 1) / ci;
+  for (int b = 0; b < c->n_buffers; ++b) d->buf[b] = take(2 * wb);
   for (int b = 0; b < 2; ++b) d->dx[b] = (bf16*)take(act);
   if (c->ckpt_on_host) {
     for (int b = 0; b < 2; ++b) d->xslot[b] = (bf16*)take(act);
     for (int b = 0; b < 2; ++b) d->xck[b] = (bf16*)take(act);
   } else {
-    d->ckdev = (bf16*)take(act * L);
-    d->xlast = (bf16*)take(act);
+    d->ckdev = (bf16*)take(act * nseg);
+    for (int b = 0; b < 2; ++b) d->fx[b] = (bf16*)take(act);
   }
+  d->seg.assign((size_t)(ci - 1), nullptr);
+  for (int64_t i = 0; i + 1 < ci; ++i) d->seg[(size_t)i] = (bf16*)take(act);
   d->xn = (bf16*)take(act);
   d->x1 = (bf16*)take(act);
   d->yn = (bf16*)take(act);
@@ -344,18 +378,22 @@ View make_view(mt_model* m, int j, int b) {
   return v;
 }
 
-const bf16* x_fwd_in(mt_model* m, int j) {  // X_{j-1}
-  const int i = j - 1;
-  if (m->c.ckpt_on_host) return m->d.xslot[i % 2];
-  return i < m->L ? m->d.ckdev + (int64_t)i * m->T * m->H : m->d.xlast;
-}
-bf16* x_out(mt_model* m, int j) {  // X_j
+bf16* x_out(mt_model* m, int j) {  // where the forward writes X_j
   if (m->c.ckpt_on_host) return m->d.xslot[j % 2];
-  return j < m->L ? m->d.ckdev + (int64_t)j * m->T * m->H : m->d.xlast;
+  return (j % m->ci == 0 && j < m->L) ? m->d.ckdev + (int64_t)(j / m->ci) * m->T * m->H : m->d.fx[j % 2];
 }
-const bf16* x_bwd_in(mt_model* m, int j, int b) {  // checkpoint X_{j-1} for the recompute
-  if (m->c.ckpt_on_host) return m->d.xck[b];
-  return m->d.ckdev + (int64_t)(j - 1) * m->T * m->H;
+const bf16* x_fwd_in(mt_model* m, int j) { return x_out(m, j - 1); }  // X_{j-1}
+// X_{j-1} in the backward (recompute or block backward of layer j, segment
+// number seg): the segment's checkpoint X_s or a recomputed X_{s+i}.
+const bf16* x_seg_in(mt_model* m, int j, int seg) {
+  const int s = (j - 1) / m->ci * m->ci;
+  if (j - 1 == s)
+    return m->c.ckpt_on_host ? m->d.xck[seg % 2] : m->d.ckdev + (int64_t)(s / m->ci) * m->T * m->H;
+  return m->d.seg[(size_t)(j - s - 2)];
+}
+bf16* x_seg_out(mt_model* m, int j) {  // recomputed X_j, s < j < e
+  const int s = (j - 1) / m->ci * m->ci;
+  return m->d.seg[(size_t)(j - s - 1)];
 }
 
 // ---------------------------------------------------------------- block math
@@ -600,13 +638,15 @@ mt_status acquire_slab(mt_model* m, int* k) {
 }
 
 // ---------------------------------------------------------------- visit pieces
-int nvisits(const mt_model* m) { return 2 * m->L + 3; }
-int visit_block(const mt_model* m, int v) { return v <= m->L + 1 ? v : 2 * m->L + 2 - v; }
-bool visit_fwd(const mt_model* m, int v) { return v <= m->L + 1; }
+int nvisits(const mt_model* m) { return (int)m->plan.size(); }
+int visit_block(const mt_model* m, int v) { return m->plan[(size_t)v].j; }
+int visit_kind(const mt_model* m, int v) { return m->plan[(size_t)v].kind; }
+bool visit_fwd(const mt_model* m, int v) { return visit_kind(m, v) <= V_HEAD; }
 
 mt_status do_stream_in(mt_model* m, int j, int b) {
-  const bool fwd = visit_fwd(m, m->vis);
-  const bool copies = !(j == 0 && !fwd);
+  const VisitDesc& vd = m->plan[(size_t)m->vis];
+  const bool fwd = vd.kind <= V_HEAD;
+  const bool copies = !(j == 0 && vd.kind == V_BWD);
   const mth::BlockDesc& bd = m->lay[(size_t)j];
   if (fwd && m->steps_done > 0) {
     logop(m, "H", "WAIT_ADAM", j, -1);
@@ -643,11 +683,17 @@ mt_status do_stream_in(mt_model* m, int j, int b) {
       m->h2d += bd.wbytes;
     }
   }
-  if (!fwd && j >= 1 && j <= m->L && m->c.ckpt_on_host) {
-    logop(m, "W", "H2D_CKPT", j, b);
+  if (vd.first && m->c.ckpt_on_host) {
+    // The segment's checkpoint X_s (s = j - 1) into slot seg % 2, after the
+    // gradient stream finished saving it (XS of the ring slot it left from).
+    const int s = j - 1, q = vd.seg % 2;
+    logop(m, "W", "WAIT_XS", s % 2, -1);
+    if (m->live) CU(m, cudaStreamWaitEvent(m->sw, m->XS[s % 2], 0));
+    logop(m, "W", "H2D_CKPT", j, q);
     if (m->live) {
       const size_t bytes = (size_t)m->T * m->H * 2;
-      CU(m, cudaMemcpyAsync(m->d.xck[b], m->ckpt + (size_t)(j - 1) * bytes, bytes, cudaMemcpyHostToDevice, m->sw));
+      CU(m, cudaMemcpyAsync(m->d.xck[q], m->ckpt + (size_t)(s / m->ci) * bytes, bytes, cudaMemcpyHostToDevice,
+                            m->sw));
       m->h2d += (int64_t)bytes;
     }
   }
@@ -696,7 +742,7 @@ mt_status do_forward(mt_model* m, int j, int b) {
       OK(head_forward_backward(m, v, x_fwd_in(m, j), m->d.dx[m->L % 2]));
     }
   }
-  const bool saves = writes_x && j < m->L && ckh;
+  const bool saves = writes_x && j < m->L && j % m->ci == 0 && ckh;
   if (saves) {
     logop(m, "C", "REC_XR", j % 2, -1);
     if (m->live) CU(m, cudaEventRecord(m->XR[j % 2], m->sc));
@@ -715,12 +761,23 @@ mt_status do_forward(mt_model* m, int j, int b) {
     logop(m, "G", "D2H_CKPT", j, s);
     if (m->live) {
       const size_t bytes = (size_t)m->T * m->H * 2;
-      CU(m, cudaMemcpyAsync(m->ckpt + (size_t)j * bytes, m->d.xslot[s], bytes, cudaMemcpyDeviceToHost, m->sg));
+      CU(m, cudaMemcpyAsync(m->ckpt + (size_t)(j / m->ci) * bytes, m->d.xslot[s], bytes, cudaMemcpyDeviceToHost,
+                            m->sg));
       m->d2h += (int64_t)bytes;
     }
     logop(m, "G", "REC_XS", s, -1);
     if (m->live) CU(m, cudaEventRecord(m->XS[s], m->sg));
   }
+  return MT_OK;
+}
+
+// Forward of layer j inside the backward, rebuilding X_j of its segment.
+mt_status do_recompute(mt_model* m, int j, int b) {
+  const int seg = m->plan[(size_t)m->vis].seg;
+  logop(m, "C", "RECOMP", j, b);
+  if (m->live) OK(decoder_forward(m, make_view(m, j, b), x_seg_in(m, j, seg), x_seg_out(m, j), false));
+  logop(m, "C", "REC_BF", b, -1);
+  if (m->live) CU(m, cudaEventRecord(m->BF[b], m->sc));
   return MT_OK;
 }
 
@@ -732,7 +789,8 @@ mt_status do_backward(mt_model* m, int j, int b) {
       Timed t(m, K_OTHER, 0, 2.0 * m->T * m->H + 2.0 * m->V * m->H);
       CU(m, mt::embed_bwd(m->d.csr_start, m->d.csr_rows, m->d.dx[0], m->V, m->H, v.g[0], m->sc));
     } else {
-      OK(decoder_backward(m, v, x_bwd_in(m, j, b), m->d.dx[j % 2], m->d.dx[(j - 1) % 2]));
+      const int seg = m->plan[(size_t)m->vis].seg;
+      OK(decoder_backward(m, v, x_seg_in(m, j, seg), m->d.dx[j % 2], m->d.dx[(j - 1) % 2]));
     }
   }
   logop(m, "C", "REC_BD", b, -1);
@@ -776,7 +834,10 @@ mt_status do_adam_enqueue(mt_model* m, int j, int k, int32_t t) {
 }
 
 // Sub-stages of a visit: 0 stream_in, 1 bind, 2 compute, 3 stream_out, 4 adam.
-bool exports_grad(const mt_model* m, int v) { return !visit_fwd(m, v) || visit_block(m, v) == m->L + 1; }
+bool exports_grad(const mt_model* m, int v) {
+  const int k = visit_kind(m, v);
+  return k == V_BWD || k == V_HEAD;
+}
 
 void advance(mt_model* m) {
   const bool exp = exports_grad(m, m->vis);
@@ -801,12 +862,13 @@ mt_status expect(mt_model* m, int stage, int block) {
 }
 
 mt_status run_visit(mt_model* m) {
-  const int v = m->vis, j = visit_block(m, v), b = v % 2;
+  const int v = m->vis, j = visit_block(m, v), b = v % m->nbuf, kind = visit_kind(m, v);
   OK(do_stream_in(m, j, b));
   advance(m);
   OK(do_bind(m, j, b, nullptr));
   advance(m);
-  if (visit_fwd(m, v)) OK(do_forward(m, j, b));
+  if (kind <= V_HEAD) OK(do_forward(m, j, b));
+  else if (kind == V_RECOMP) OK(do_recompute(m, j, b));
   else OK(do_backward(m, j, b));
   const bool exp = exports_grad(m, v);
   const int64_t t = m->steps_done + 1;
@@ -844,6 +906,10 @@ void fill_shape(mt_model* m) {
   m->wb_max = 0;
   for (auto& b : m->lay) m->wb_max = b.wbytes > m->wb_max ? b.wbytes : m->wb_max;
   m->K = c.n_grad_slabs;
+  m->nbuf = c.n_buffers;
+  m->ci = c.ckpt_interval;
+  m->nseg = (m->L + m->ci - 1) / m->ci;
+  m->plan = build_plan(m->L, m->ci);
 }
 
 }  // namespace
@@ -892,6 +958,7 @@ mt_status mt_default_config(mt_config* c) {
   c->micro_batches = 1;
   c->ckpt_interval = 1;
   c->ckpt_on_host = 1;
+  c->n_buffers = 2;
   c->n_grad_slabs = 12;
   c->lr = 1e-3f;
   c->beta1 = 0.9f;
@@ -973,7 +1040,7 @@ mt_status mt_init_model(const mt_config* c, mt_dev_region dev, mt_streams s, mt_
     if (cudaHostRegister(m->store, m->store_bytes, cudaHostRegisterDefault) != cudaSuccess) return MT_ERR_HOST_OOM;
     m->registered = true;
   } else {
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < m->nbuf; ++b) {
       if (pinned_alloc((void**)&m->staging[b], (size_t)m->wb_max) != cudaSuccess)
         return MT_ERR_HOST_OOM;
       m->pinned_bytes += (size_t)m->wb_max;
@@ -983,7 +1050,7 @@ mt_status mt_init_model(const mt_config* c, mt_dev_region dev, mt_streams s, mt_
     return MT_ERR_HOST_OOM;
   m->pinned_bytes += (size_t)m->wb_max * m->K;
   if (c->ckpt_on_host) {
-    const size_t bytes = (size_t)m->L * m->T * m->H * 2;
+    const size_t bytes = (size_t)m->nseg * m->T * m->H * 2;  // X_0, X_c, X_2c, ...
     if (pinned_alloc((void**)&m->ckpt, bytes) != cudaSuccess) return MT_ERR_HOST_OOM;
     m->pinned_bytes += bytes;
   }
@@ -1004,7 +1071,7 @@ mt_status mt_init_model(const mt_config* c, mt_dev_region dev, mt_streams s, mt_
   compute_tables(m.get(), cs);
   CU(mm, cudaMemcpyAsync(m->d.cs, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice, m->sc));
   CU(mm, cudaMemsetAsync(m->d.loss, 0, 256, m->sc));
-  for (int b = 0; b < 2; ++b) CU(mm, cudaMemsetAsync(m->d.buf[b], 0, (size_t)2 * m->wb_max, m->sc));
+  for (int b = 0; b < m->nbuf; ++b) CU(mm, cudaMemsetAsync(m->d.buf[b], 0, (size_t)2 * m->wb_max, m->sc));
   CU(mm, cudaStreamSynchronize(m->sc));
   m->adam_thr = std::thread(adam_loop, mm);
   *out = m.release();
@@ -1036,7 +1103,7 @@ mt_status mt_set_tokens(mt_model* m, const int32_t* tok) {
 }
 
 mt_status mt_stream_in(mt_model* m, int32_t block, int32_t buf) {
-  if (!m || buf < 0 || buf > 1) return MT_ERR_ARG;
+  if (!m || buf < 0 || buf >= m->nbuf) return MT_ERR_ARG;
   OK(expect(m, 0, block));
   OK(do_stream_in(m, block, buf));
   advance(m);
@@ -1044,7 +1111,7 @@ mt_status mt_stream_in(mt_model* m, int32_t block, int32_t buf) {
 }
 
 mt_status mt_bind(mt_model* m, int32_t block, int32_t buf, mt_layer_view* view) {
-  if (!m || buf < 0 || buf > 1) return MT_ERR_ARG;
+  if (!m || buf < 0 || buf >= m->nbuf) return MT_ERR_ARG;
   OK(expect(m, 1, block));
   OK(do_bind(m, block, buf, view));
   advance(m);
@@ -1054,16 +1121,19 @@ mt_status mt_bind(mt_model* m, int32_t block, int32_t buf, mt_layer_view* view) 
 mt_status mt_step_forward(mt_model* m, const mt_layer_view* v) {
   if (!m || !v) return MT_ERR_ARG;
   if (!m->tokens_set) return set_err(m, MT_ERR_STATE, "no tokens set", false);
-  if (!visit_fwd(m, m->vis)) return set_err(m, MT_ERR_STATE, "forward called in the backward pass", false);
+  if (visit_kind(m, m->vis) == V_BWD)
+    return set_err(m, MT_ERR_STATE, "forward called on a block-backward visit", false);
   OK(expect(m, 2, v->block));
-  OK(do_forward(m, v->block, v->buf));
+  if (visit_kind(m, m->vis) == V_RECOMP) OK(do_recompute(m, v->block, v->buf));
+  else OK(do_forward(m, v->block, v->buf));
   advance(m);
   return MT_OK;
 }
 
 mt_status mt_step_backward(mt_model* m, const mt_layer_view* v) {
   if (!m || !v) return MT_ERR_ARG;
-  if (visit_fwd(m, m->vis)) return set_err(m, MT_ERR_STATE, "backward called in the forward pass", false);
+  if (visit_kind(m, m->vis) != V_BWD)
+    return set_err(m, MT_ERR_STATE, "backward called on a forward or recompute visit", false);
   OK(expect(m, 2, v->block));
   OK(do_backward(m, v->block, v->buf));
   advance(m);
@@ -1071,7 +1141,7 @@ mt_status mt_step_backward(mt_model* m, const mt_layer_view* v) {
 }
 
 mt_status mt_stream_out(mt_model* m, int32_t block, int32_t buf, int32_t* slab) {
-  if (!m || buf < 0 || buf > 1) return MT_ERR_ARG;
+  if (!m || buf < 0 || buf >= m->nbuf) return MT_ERR_ARG;
   OK(expect(m, 3, block));
   int k = 0;
   OK(do_stream_out(m, block, buf, &k));
@@ -1249,6 +1319,16 @@ int64_t mt_plan_protocol(const mt_config* c, int32_t n_steps, char* buf, int64_t
     for (int v = 0; v < nvisits(&m); ++v)
       if (run_visit(&m) != MT_OK) return 0;
   return mt_protocol_log(&m, buf, cap);
+}
+
+int32_t mt_visit_plan(const mt_config* c, int32_t* kind, int32_t* block, int32_t cap) {
+  if (!mth::config_valid(c, nullptr)) return -1;
+  const std::vector<VisitDesc> p = build_plan(c->n_layers, c->ckpt_interval);
+  for (size_t v = 0; v < p.size() && (int64_t)v < cap; ++v) {
+    if (kind) kind[v] = p[v].kind;
+    if (block) block[v] = p[v].j;
+  }
+  return (int32_t)p.size();
 }
 
 int32_t mt_schedule(int32_t n, const double* b, const double* d, const double* c, const double* a, double bw_h2d,

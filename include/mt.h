@@ -69,7 +69,10 @@ typedef struct {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
   float rope_base, rms_eps, init_std;          /* e.g. 1e4 or 1e6, 1e-6, 0.02 */
   int32_t batch, seq, micro_batches;
-  int32_t ckpt_interval;   /* layers between kept activations; must be 1    */
+  int32_t ckpt_interval;   /* c in [1, n_layers]: X_s kept for s = 0, c, 2c,
+                              ...; the backward recomputes each c-layer
+                              segment from it ([Review] 2, block-wise
+                              recomputation)                               */
   int32_t ckpt_on_host;    /* 1: layer-boundary activations in pinned host RAM
                               (device footprint independent of depth)      */
   int32_t n_grad_slabs;    /* K pinned gradient slabs ([Hotdry]: default 12) */
@@ -84,6 +87,8 @@ typedef struct {
   int32_t log_protocol;    /* 1: keep the enqueue log (mt_protocol_log)      */
   int32_t keep_host_grad;  /* 1: each slab is also unpacked into the store's
                               BF16 G region; 0: Adam reads the slab only  */
+  int32_t n_buffers;       /* device weight buffers: 2 (double-buffered, the
+                              pages' engine) or 1 (single-buffer ablation)  */
 } mt_config;
 
 typedef struct { void* base; size_t bytes; } mt_dev_region;          /* caller-owned device memory  */
@@ -189,6 +194,13 @@ mt_status mt_host_adam(int64_t n, const uint16_t* g_bf16, float* master, float* 
 /* Runs the step scheduler without any device or host work and returns the
  * enqueue log of n_steps steps (as mt_protocol_log). */
 int64_t mt_plan_protocol(const mt_config* cfg, int32_t n_steps, char* buf, int64_t cap);
+/* The visits of one step in order, for callers driving the per-visit calls:
+ * kind[v] (0 forward, 1 head: fused forward and backward, 2 recompute: a
+ * forward inside the backward that rebuilds a checkpoint segment, run with
+ * mt_step_forward, 3 block backward) and block[v]; the buffer of visit v is
+ * v % n_buffers.  Returns the number of visits (n_layers + 3 + the recompute
+ * visits), or -1 on a bad config; writes at most cap entries. */
+int32_t mt_visit_plan(const mt_config* cfg, int32_t* kind, int32_t* block, int32_t cap);
 /* Static prefetch schedule ([Peter] 記憶體預取策略: prefetch timing from each
  * layer's bytes, the link bandwidth and its compute time).  Per visit v of a
  * step: b[v] H2D bytes, d[v] exported gradient bytes, c[v] compute seconds,

@@ -85,7 +85,7 @@ def lib():
             "or_step_fwd_bwd_d": (d, [pc, _P(_P(d)), _P(i32), _P(_P(d))]),
             "or_forward_hidden_f": (d, [pc, _P(_P(f)), _P(i32), i32, _P(f)]),
             "or_adam": (None, [i64, _P(u16), _P(f), _P(f), _P(f), _P(u16), i32, f, f, f, f, f]),
-            "or_protocol": (i64, [pc, i32, i32, i32, i32, C.c_char_p, i64]),
+            "or_protocol": (i64, [pc, i32, i32, i32, i32, i32, i32, C.c_char_p, i64]),
             "or_schedule": (i32, [i32, _P(d), _P(d), _P(d), _P(d), d, d, _P(d)]),
         }
         for name, (res, args) in sig.items():
@@ -292,11 +292,14 @@ def adam(g_bf16, master, m, v, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, 
     return w
 
 
-def protocol(shape: dict, n_steps: int, n_slabs: int, ckpt_on_host: bool, jit_pack: bool) -> list[str]:
+def protocol(shape: dict, n_steps: int, n_slabs: int, ckpt_on_host: bool, jit_pack: bool,
+             ckpt_interval: int = 1, n_buffers: int = 2) -> list[str]:
     c = make_cfg(shape)
-    need = -lib().or_protocol(C.byref(c), n_steps, n_slabs, int(ckpt_on_host), int(jit_pack), None, 0)
+    args = (n_steps, n_slabs, int(ckpt_on_host), int(jit_pack), int(ckpt_interval), int(n_buffers))
+    need = -lib().or_protocol(C.byref(c), *args, None, 0)
+    assert need > 0, "invalid protocol arguments"
     buf = C.create_string_buffer(int(need) + 1)
-    n = lib().or_protocol(C.byref(c), n_steps, n_slabs, int(ckpt_on_host), int(jit_pack), buf, need + 1)
+    n = lib().or_protocol(C.byref(c), *args, buf, need + 1)
     assert n >= 0
     return buf.value.decode().splitlines()
 

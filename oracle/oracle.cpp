@@ -661,39 +661,98 @@ void or_adam(int64_t n, const uint16_t* g_bf16, float* master, float* m, float* 
   }
 }
 
+}  // extern "C"
+
+namespace {
+
+// Visits of one training step.  Forward j = 0..L, then the head (L+1; its
+// forward and backward are fused).  The backward runs block-wise
+// recomputation ([Review] 2) streaming forward and block-wise backward: with
+// checkpoint interval c only X_s, s in {0, c, 2c, ...} < L, is kept from the
+// forward; the decoder layers form segments [s+1, e], e = min(s+c, L), taken
+// from the top.  A segment first recomputes X_{s+1} .. X_{e-1} from X_s
+// (visits of kind RECOMP, layers s+1 .. e-1 streamed in again) and then runs
+// the backward of layers e .. s+1.  The embedding's backward comes last.
+// With c = 1 there is no RECOMP visit.  `seg` is the segment's number from the
+// top (the checkpoint-load slot is seg % 2); `first` marks the segment's first
+// visit, which loads X_s.
+struct Visit {
+  int kind;  // 0 FWD, 1 HEAD, 2 RECOMP, 3 BWD
+  long j;
+  long seg;
+  bool first;
+};
+std::vector<Visit> step_visits(long L, long c) {
+  std::vector<Visit> v;
+  for (long j = 0; j <= L; ++j) v.push_back({0, j, -1, false});
+  v.push_back({1, L + 1, -1, false});
+  const long nseg = (L + c - 1) / c;
+  for (long k = 0; k < nseg; ++k) {
+    const long s = (nseg - 1 - k) * c, e = std::min(s + c, L);
+    for (long j = s + 1; j <= e - 1; ++j) v.push_back({2, j, k, j == s + 1});
+    for (long j = e; j >= s + 1; --j) v.push_back({3, j, k, j == s + 1 && e == s + 1});
+  }
+  v.push_back({3, 0, -1, false});
+  return v;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Event protocol of the pages' three-stream engine ([Hotdry] event-driven
+// synchronisation): per visit, the weight stream (W) waits Buffer-Free of its
+// buffer, copies the block in and records Weights-Ready; compute (C) waits
+// Weights-Ready, runs, and records Buffer-Free (forward, recompute: nothing to
+// export) or Backward-Done; the gradient stream (G) waits Backward-Done,
+// copies the gradients into a free slab, records Buffer-Free and Slab-Ready;
+// the host (H) enqueues Adam on the slab.  Buffers alternate per visit
+// (n_buffers = 2) or one buffer serves every visit (n_buffers = 1, the pages'
+// single-buffer ablation).  Host-resident checkpoints: the forward saves X_s
+// from a two-slot ring (C records XR, G waits it, copies, records XS; the
+// next forward write into that slot waits XS), and a segment's first visit
+// loads X_s into checkpoint slot seg % 2 on W after waiting XS of the slot X_s
+// was saved from.  Slabs are numbered round-robin here, one valid assignment;
+// the library takes the lowest free slab and logs are compared modulo that.
 int64_t or_protocol(const or_cfg* c, int32_t n_steps, int32_t n_slabs, int32_t ckpt_on_host,
-                    int32_t jit_pack, char* buf, int64_t cap) {
-  if (!cfg_ok(c) || n_slabs < 1 || n_steps < 0) return 0;
-  const long L = c->n_layers;
+                    int32_t jit_pack, int32_t ckpt_interval, int32_t n_buffers, char* buf, int64_t cap) {
+  if (!cfg_ok(c) || n_slabs < 1 || n_steps < 0 || ckpt_interval < 1 || ckpt_interval > c->n_layers ||
+      n_buffers < 1 || n_buffers > 2)
+    return 0;
+  const long L = c->n_layers, ci = ckpt_interval;
+  const std::vector<Visit> vis = step_visits(L, ci);
   Log log;
   long exports = 0;
   bool used[2] = {false, false};
-  for (int s = 0; s < n_steps; ++s) {
-    log.step = s;
-    const long nvis = 2 * L + 3;
-    for (long v = 0; v < nvis; ++v) {
-      const bool fwd = v <= L + 1;
-      const long j = fwd ? v : 2 * L + 2 - v;
-      const long b = v % 2;
-      const bool head = (j == L + 1);
-      const bool copies = !(j == 0 && !fwd);
-      if (fwd && s > 0) log.op("H", "WAIT_ADAM", j, -1);
+  for (int st = 0; st < n_steps; ++st) {
+    log.step = st;
+    for (size_t vi = 0; vi < vis.size(); ++vi) {
+      const Visit& V = vis[vi];
+      const long j = V.j, b = (long)vi % n_buffers;
+      const bool fwd = V.kind <= 1, head = V.kind == 1;
+      const bool copies = !(j == 0 && V.kind == 3);
+      if (fwd && st > 0) log.op("H", "WAIT_ADAM", j, -1);
       if (copies && jit_pack) {
         if (used[b]) log.op("H", "WAIT_STAGE", b, -1);
         log.op("H", "PACK", j, b);
       }
       log.op("W", "WAIT_BF", b, -1);
       if (copies) log.op("W", "H2D", j, b);
-      if (!fwd && j >= 1 && ckpt_on_host) log.op("W", "H2D_CKPT", j, b);
+      if (V.first && ckpt_on_host) {
+        const long s = j - 1;  // the checkpoint X_s feeding this segment
+        log.op("W", "WAIT_XS", s % 2, -1);
+        log.op("W", "H2D_CKPT", j, V.seg % 2);
+      }
       log.op("W", "REC_WR", b, -1);
       used[b] = true;
       log.op("C", "WAIT_WR", b, -1);
-      const bool writes_x = fwd && j <= L;
+      const bool writes_x = V.kind == 0;
       if (writes_x && ckpt_on_host) log.op("C", "WAIT_XS", j % 2, -1);
-      log.op("C", fwd ? (head ? "HEAD" : "FWD") : "BWD", j, b);
-      const bool saves_x = writes_x && j < L && ckpt_on_host;
+      static const char* names[4] = {"FWD", "HEAD", "RECOMP", "BWD"};
+      log.op("C", names[V.kind], j, b);
+      const bool saves_x = writes_x && j < L && j % ci == 0 && ckpt_on_host;
       if (saves_x) log.op("C", "REC_XR", j % 2, -1);
-      if (fwd && !head) {
+      if (V.kind == 0 || V.kind == 2) {
         log.op("C", "REC_BF", b, -1);
       } else {
         log.op("C", "REC_BD", b, -1);
@@ -703,7 +762,7 @@ int64_t or_protocol(const or_cfg* c, int32_t n_steps, int32_t n_slabs, int32_t c
         log.op("G", "D2H_CKPT", j, j % 2);
         log.op("G", "REC_XS", j % 2, -1);
       }
-      if (!fwd || head) {
+      if (V.kind == 3 || head) {
         const long k = exports % n_slabs;
         ++exports;
         log.op("G", "WAIT_BD", b, -1);

@@ -94,9 +94,12 @@ void or_adam(int64_t n, const uint16_t* g_bf16, float* master, float* m, float* 
 
 /* ---- event protocol simulator ([Hotdry] event-driven synchronisation) ---- */
 /* Writes the ordered op list of `n_steps` training steps as text lines into
- * buf (NUL-terminated).  Returns the length, or -(needed) if cap is short. */
+ * buf (NUL-terminated).  Returns the length, or -(needed) if cap is short.
+ * ckpt_interval c in [1, n_layers]: X_s is kept for s = 0, c, 2c, ... and the
+ * backward recomputes each c-layer segment from it ([Review] 2, block-wise
+ * recomputation); n_buffers in {1, 2} device weight buffers. */
 int64_t or_protocol(const or_cfg* c, int32_t n_steps, int32_t n_slabs, int32_t ckpt_on_host,
-                    int32_t jit_pack, char* buf, int64_t cap);
+                    int32_t jit_pack, int32_t ckpt_interval, int32_t n_buffers, char* buf, int64_t cap);
 
 /* ---- static prefetch schedule ([Peter] 記憶體預取策略) ---- */
 /* Per visit v of one step (2L+3 visits): b[v] H2D bytes, d[v] gradient bytes

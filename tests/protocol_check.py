@@ -17,8 +17,10 @@ those sentences forbid is ordered:
   * host pack into staging b after the previous H2D read staging b;
   * D2H into slab k after the previous Adam on slab k, Adam after the D2H;
   * next step's pack / H2D of block j after block j's Adam;
-  * checkpoint slots: write after the previous save, save after the write,
-    checkpoint H2D after the previous compute that read the slot.
+  * checkpoint slots: write after the previous save, save after the write;
+    a host checkpoint is loaded only after it was saved and saved again only
+    after its last load; a device checkpoint slot is refilled only after the
+    last compute that read it, and read only after its load.
 """
 from __future__ import annotations
 
@@ -51,7 +53,11 @@ def check(lines: list[str]) -> None:
     ev: dict[str, Clock] = {}
     last_buf_use: dict[int, list] = {0: [], 1: []}     # ops that read/wrote device buffer b
     visit_h2d: dict[int, tuple] = {}                   # this visit's H2D into b
-    last_ckpt_read: dict[int, tuple] = {}              # compute that read xck[b]
+    slot_read: dict[int, tuple] = {}                   # compute that last read checkpoint slot q
+    slot_load: dict[int, tuple] = {}                   # H2D_CKPT that last filled slot q
+    slot_of_layer: dict[int, int] = {}                 # layer whose input X_{j-1} sits in slot q
+    ckpt_saved: dict[int, tuple] = {}                  # D2H_CKPT of X_j into host memory
+    ckpt_loaded: dict[int, tuple] = {}                 # H2D_CKPT that last read host X_j
     stage_read: dict[int, tuple] = {}                  # H2D that read staging b
     slab_adam: dict[int, tuple] = {}                   # Adam job that read slab k
     slab_d2h: dict[int, tuple] = {}
@@ -111,17 +117,21 @@ def check(lines: list[str]) -> None:
             stage_read[b] = me
             last_buf_use[b] = [me]
         elif op == "H2D_CKPT":
-            assert _hb(last_ckpt_read.get(b), me), "checkpoint H2D over a slot in use: " + where
-            for u in last_buf_use[b]:
-                assert _hb(u, me), "checkpoint H2D before buffer free: " + where
-            visit_h2d[b] = me
-        elif op in ("FWD", "HEAD", "BWD"):
+            assert (a - 1) in ckpt_saved, "checkpoint loaded that was never saved: " + where
+            assert _hb(ckpt_saved[a - 1], me), "checkpoint loaded before its save finished: " + where
+            assert _hb(slot_read.get(b), me), "checkpoint H2D over a slot in use: " + where
+            slot_load[b] = me
+            slot_of_layer[a] = b
+            ckpt_loaded[a - 1] = me
+        elif op in ("FWD", "HEAD", "RECOMP", "BWD"):
             assert _hb(visit_h2d.get(b), me), "compute before weights ready: " + where
             for u in last_buf_use[b]:
                 assert _hb(u, me), "compute overlaps earlier use of buffer: " + where
             last_buf_use[b] = [me]
-            if op == "BWD":
-                last_ckpt_read[b] = me
+            if op in ("RECOMP", "BWD") and a in slot_of_layer:
+                q = slot_of_layer[a]
+                assert _hb(slot_load[q], me), "compute reads a checkpoint slot before its load: " + where
+                slot_read[q] = me
             if op == "FWD" or op == "HEAD":
                 slot = a % 2
                 if op == "FWD":
@@ -129,7 +139,9 @@ def check(lines: list[str]) -> None:
                     xslot_write[slot] = me
         elif op == "D2H_CKPT":
             assert _hb(xslot_write[b], me), "checkpoint saved before written: " + where
+            assert _hb(ckpt_loaded.get(a), me), "host checkpoint overwritten before its load: " + where
             xslot_save[b] = me
+            ckpt_saved[a] = me
         elif op == "D2H":
             buf = _buf_of(lines, ln)
             assert _hb(last_buf_use[buf][-1], me), "export before gradients computed: " + where

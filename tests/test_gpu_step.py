@@ -109,33 +109,33 @@ def test_gqa_shape_parity(orc):
     report, _ = run_parity(orc, c, 2)
 
 
-def test_manual_primitives_match_train_step():
-    c = configs.get("tiny")
+@pytest.mark.parametrize("ci,nbuf", [(1, 2), (2, 1)])
+def test_manual_primitives_match_train_step(ci, nbuf):
+    c = configs.get("tiny", n_layers=3)
+    rt = dict(ckpt_interval=ci, n_buffers=nbuf)
     tok = inputs.tokens_for(c, 0)
-    a = mt.Model(c, seed=5)
+    a = mt.Model(c, seed=5, **rt)
     a.set_tokens(tok)
     la = a.train_step(0)
     a.sync()
-    b = mt.Model(c, seed=5)
+    b = mt.Model(c, seed=5, **rt)
     b.set_tokens(tok)
-    L = c["n_layers"]
-    v = 0
-    for j in list(range(L + 2)) + list(range(L, -1, -1)):
-        fwd = v <= L + 1
-        buf = v % 2
+    plan = mt.visit_plan(b.cfg)
+    assert len(plan) == 2 * c["n_layers"] + 3 + (c["n_layers"] - -(-c["n_layers"] // ci))
+    for v, (kind, j) in enumerate(plan):
+        buf = v % nbuf
         b.stream_in(j, buf)
         view = b.bind(j, buf)
         assert view.block == j and view.n_tensors == len(b.layout[j]["tensors"])
-        if fwd:
-            b.step_forward(view)
-        else:
+        if kind == 3:
             b.step_backward(view)
-        if (not fwd) or j == L + 1:
+        else:
+            b.step_forward(view)  # forward, head, or a segment's recompute
+        if kind in (1, 3):
             k = b.stream_out(j, buf)
             b.adam_host(j, k, 1)
-        v += 1
     b.sync()
-    for j in range(L + 2):
+    for j in range(c["n_layers"] + 2):
         ga = a.read(j, mt.REGION_G).view(np.int16).astype(np.float32)
         gb = b.read(j, mt.REGION_G).view(np.int16).astype(np.float32)
         ma, mb = a.read(j, mt.REGION_MASTER), b.read(j, mt.REGION_MASTER)
@@ -146,3 +146,35 @@ def test_manual_primitives_match_train_step():
     assert ei.value.status == -2
     a.close()
     b.close()
+
+
+@pytest.mark.parametrize("ci,host,nbuf", [(2, 1, 2), (3, 0, 2), (5, 1, 1), (1, 0, 1)])
+def test_checkpoint_interval_and_single_buffer_parity(orc, ci, host, nbuf):
+    """Block-wise recomputation with checkpoint interval c (segments rebuilt
+    from X_0, X_c, ...) and the single-buffer engine against the oracle, with
+    the enqueue log equal to the simulator's and race-free."""
+    c = configs.get("tiny", n_layers=5)
+    report, log = run_parity(orc, c, 2, ckpt_interval=ci, ckpt_on_host=host, n_buffers=nbuf)
+    ref = orc.protocol(oracle_shape(c), 2, 12, bool(host), True, ci, nbuf)
+    assert protocol_check.mask_slabs(log) == protocol_check.mask_slabs(ref)
+    protocol_check.check(log)
+
+
+def test_checkpoint_interval_reproduces_interval_one():
+    """The recompute visits run the same kernels on the same inputs as the
+    forward, so every interval gives the same step: the loss bit for bit and
+    the gradients up to the summation order of the RMSNorm-gain reduction."""
+    c = configs.get("tiny", n_layers=6)
+    tok = inputs.tokens_for(c, 0)
+    out = {}
+    for ci in (1, 2, 4, 6):
+        m = mt.Model(c, seed=9, ckpt_interval=ci)
+        m.set_tokens(tok)
+        loss = m.train_step(0)
+        m.sync()
+        out[ci] = (loss, [m.read(j, mt.REGION_G).view(np.int16).astype(np.float32) for j in range(len(m.layout))])
+        m.close()
+    for ci in (2, 4, 6):
+        assert out[ci][0] == out[1][0], ci
+        for j, (g, g1) in enumerate(zip(out[ci][1], out[1][1])):
+            assert np.mean(g == g1) > 0.999, (ci, j)

@@ -104,6 +104,42 @@ def test_protocol_plan_bit_exact(orc, ckpt, pin, slabs):
     protocol_check.check(lines)
 
 
+@pytest.mark.parametrize("ci,nbuf,ckpt", [(2, 2, 1), (3, 1, 0), (5, 2, 0), (1, 1, 1)])
+def test_protocol_plan_segments_bit_exact(orc, ci, nbuf, ckpt):
+    c = configs.get("tiny", n_layers=5)
+    lines = _plan(c, 2, ckpt_on_host=ckpt, pin_store=0, n_grad_slabs=3, ckpt_interval=ci, n_buffers=nbuf)
+    ref = orc.protocol(c, 2, 3, bool(ckpt), True, ci, nbuf)
+    assert protocol_check.mask_slabs(lines) == protocol_check.mask_slabs(ref)
+    protocol_check.check(lines)
+
+
+@pytest.mark.parametrize("L,ci", [(2, 1), (5, 2), (7, 3), (4, 4)])
+def test_visit_plan_matches_oracle(orc, L, ci):
+    c = configs.get("tiny", n_layers=L)
+    plan = mt.visit_plan(mt.make_config(c, ckpt_interval=ci))
+    names = {"FWD": 0, "HEAD": 1, "RECOMP": 2, "BWD": 3}
+    ref = [(names[l.split()[2]], int(l.split()[3])) for l in orc.protocol(c, 1, 12, True, False, ci, 2)
+           if l.split()[2] in names]
+    assert plan == ref
+
+
+def test_device_checkpoints_scale_with_segments():
+    """Device-resident checkpoints: one slot per segment plus c - 1 recompute
+    slots, so a larger interval needs less device memory."""
+    L = mt.lib()
+    c = configs.get("1.2b")
+    act = c["batch"] * c["seq"] * c["hidden"] * 2
+    size = {}
+    for ci in (1, 2, 5):
+        cfg = mt.make_config(c, ckpt_on_host=0, ckpt_interval=ci)
+        n = C.c_size_t()
+        assert L.mt_query_device_bytes(C.byref(cfg), C.byref(n)) == 0
+        size[ci] = n.value
+    nl = c["n_layers"]
+    assert size[1] - size[2] == pytest.approx((nl - (-(-nl // 2)) - 1) * act, abs=4096 * nl)
+    assert size[5] < size[2] < size[1]  # slots: 22, 12, 5 + 4
+
+
 @pytest.mark.parametrize("name", ["1.2b", "7.6b", "14.7b"])
 def test_protocol_plan_full_depth(orc, name):
     c = configs.get(name)
@@ -147,8 +183,11 @@ def test_bad_arguments_rejected_without_gpu():
     assert L.mt_query_device_bytes(C.byref(cfg), C.byref(nbytes)) == 0 and nbytes.value > 0
     bad = mt.make_config(configs.get("tiny"), n_kv_heads=3)
     assert L.mt_query_device_bytes(C.byref(bad), C.byref(nbytes)) == -1
-    bad = mt.make_config(configs.get("tiny"), ckpt_interval=2)
-    assert L.mt_query_device_bytes(C.byref(bad), C.byref(nbytes)) == -1
+    for kw in (dict(ckpt_interval=0), dict(ckpt_interval=3), dict(n_buffers=0), dict(n_buffers=3)):
+        bad = mt.make_config(configs.get("tiny"), **kw)  # tiny has 2 layers
+        assert L.mt_query_device_bytes(C.byref(bad), C.byref(nbytes)) == -1, kw
+    ok = mt.make_config(configs.get("tiny"), ckpt_interval=2, n_buffers=1)
+    assert L.mt_query_device_bytes(C.byref(ok), C.byref(nbytes)) == 0
     h = C.c_void_p()
     assert L.mt_init_model(C.byref(cfg), mt.DevRegion(None, 0), mt.Streams(None, None, None), C.byref(h)) == -1
     assert L.mt_train_step(None, 0, None) == -1

@@ -446,8 +446,41 @@ def test_protocol_is_race_free(orc, ckpt, jit, slabs):
     assert sum(1 for l in per_step if " ADAM_ENQ " in l) == L + 2
 
 
+@pytest.mark.parametrize("L,ci", [(3, 2), (3, 3), (5, 2), (7, 3)])
+@pytest.mark.parametrize("ckpt,nbuf", [(1, 2), (0, 2), (1, 1), (0, 1)])
+def test_protocol_segments_race_free(orc, L, ci, ckpt, nbuf):
+    shape = configs.get("tiny", n_layers=L)
+    lines = orc.protocol(shape, 3, 2, bool(ckpt), True, ci, nbuf)
+    protocol_check.check(lines)
+    per_step = [l for l in lines if l.startswith("1 ")]
+    nseg = -(-L // ci)
+    count = lambda op: sum(1 for l in per_step if f" {op} " in l)
+    assert count("RECOMP") == L - nseg  # every decoder layer but the top of each segment is rebuilt once
+    assert count("H2D") == (L + 2) + L + (L - nseg)
+    assert count("D2H_CKPT") == (nseg if ckpt else 0)
+    assert count("H2D_CKPT") == (nseg if ckpt else 0)
+    assert count("D2H") == L + 2 and count("ADAM_ENQ") == L + 2
+    bufs = {int(l.split()[4]) for l in per_step if " H2D " in l}
+    assert bufs == set(range(nbuf))
+
+
+def test_protocol_segment_order_hand_example(orc):
+    """L = 7, interval 3: X_0, X_3, X_6 kept; segments [7], [4..6], [1..3]
+    from the top, each rebuilding X_{s+1} .. X_{e-1} before its backward."""
+    shape = configs.get("tiny", n_layers=7)
+    lines = orc.protocol(shape, 1, 12, True, False, 3, 2)
+    comp = [" ".join(l.split()[2:4]) for l in lines if l.split()[2] in ("FWD", "HEAD", "RECOMP", "BWD")]
+    assert comp == ["FWD 0", "FWD 1", "FWD 2", "FWD 3", "FWD 4", "FWD 5", "FWD 6", "FWD 7", "HEAD 8",
+                    "BWD 7", "RECOMP 4", "RECOMP 5", "BWD 6", "BWD 5", "BWD 4",
+                    "RECOMP 1", "RECOMP 2", "BWD 3", "BWD 2", "BWD 1", "BWD 0"]
+    saves = [int(l.split()[3]) for l in lines if " D2H_CKPT " in l]
+    loads = [(int(l.split()[3]), int(l.split()[4])) for l in lines if " H2D_CKPT " in l]
+    assert saves == [0, 3, 6]
+    assert loads == [(7, 0), (4, 1), (1, 0)]  # (first layer of the segment, checkpoint slot)
+
+
 @pytest.mark.parametrize("drop", ["W WAIT_BF", "C WAIT_WR", "G WAIT_BD", "H WAIT_STAGE", "H WAIT_ADAM",
-                                  "C WAIT_XS", "H ACQ_SLAB"])
+                                  "C WAIT_XS", "W WAIT_XS", "H ACQ_SLAB"])
 def test_protocol_checker_catches_missing_wait(orc, drop):
     shape = configs.get("tiny", n_layers=3)
     lines = orc.protocol(shape, 3, 2, True, True)
