@@ -27,7 +27,8 @@
 namespace mt {
 namespace {
 
-constexpr int THREADS = 192;
+constexpr int THREADS = 192;      // forward, dK/dV: TMA warp, MMA warp, 4 row warps
+constexpr int BWD_THREADS = 320;  // dQ kernel: TMA warp, MMA warp, 8 row warps (two per TMEM lane quarter)
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr int CH = 16384;  // one 64-column chunk of a 128-row tile (128 rows x 128 B)
 
@@ -77,6 +78,15 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(accum));
 }
+// The same with the A operand in TMEM (K-major: lane = row of A, each 32-bit
+// column two consecutive K elements, a K-step of 16 = 8 columns).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(accum));
+}
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
                : "memory");
@@ -95,6 +105,51 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// tcgen05.ld without the wait, so several loads share one tcgen05.wait::ld.
+__device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+// Waits for this thread's outstanding tcgen05.ld and ties the destination
+// registers to the wait, so no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld2(uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(a[i]), "+r"(b[i]));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
@@ -118,6 +173,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
   return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ULL << 46) | (2ULL << 61);
 }
+// A descriptor advanced by `bytes`: the start-address field holds addr >> 4
+// and shared addresses stay below 256 KB, so the addition never carries out
+// of the field.  Building descriptors once and advancing them by constants
+// keeps the MMA-issuing thread's per-instruction work to one 64-bit add.
+__device__ __forceinline__ uint64_t dadv(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
 __host__ __device__ constexpr uint32_t idesc(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -219,17 +279,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = mbar_wait(q_full, 0, abort_flag);
       constexpr uint32_t IS = idesc(128, 128, false, false);
       constexpr uint32_t IO = idesc(128, HD, false, true);
+      const uint64_t dP = sdesc(su32(sP), 16, 1024), dV = sdesc(su32(sV), CH, 1024);
+      const uint64_t dQ = sdesc(su32(sQ), 16, 1024), dK = sdesc(su32(sK), 16, 1024);
       auto issue_pv = [&](int i) -> bool {
         if (!mbar_wait(p_full, (uint32_t)(i & 1), abort_flag)) return false;
         tc_fence_after();
         const int s = i & 1;
-        const uint32_t p0 = su32(sP), v0 = su32(sV + s * NC * CH);
+        const uint64_t v = dadv(dV, s * NC * CH);
+        const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = sdesc(p0 + (kk >> 2) * CH + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc(v0 + kk * 16 * 128, CH, 1024);
-          tc_mma(tO, ad, bd, IO, (i > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma(tO, dadv(dP, (kk >> 2) * CH + (kk & 3) * 32), dadv(v, kk * 16 * 128), IO, kk > 0 ? 1u : acc0);
         tc_commit(o_done);
         tc_commit(&kv_empty[s]);
         return true;
@@ -242,13 +302,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t q0a = su32(sQ), k0a = su32(sK + s * NC * CH);
+        const uint64_t kd = dadv(dK, s * NC * CH);
+        const uint32_t ts = tS[b];
 #pragma unroll
         for (int c = 0; c < NC; ++c)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            tc_mma(tS[b], sdesc(q0a + c * CH + k * 32, 16, 1024), sdesc(k0a + c * CH + k * 32, 16, 1024), IS,
-                   (c | k) != 0);
+            tc_mma(ts, dadv(dQ, c * CH + k * 32), dadv(kd, c * CH + k * 32), IS, (c | k) != 0);
         tc_commit(&s_full[b]);
         if (j >= 1 && !issue_pv(j - 1)) {
           ok = false;
@@ -419,14 +479,19 @@ __global__ void __launch_bounds__(THREADS, 1)
 // TMEM: (S^T | dP^T) x 2 = 256 columns, dV, dK.
 //
 // attn_bwd_q_k: one CTA per (128 queries, query head, sequence) looping over
-// 64-key sub-tiles up to the diagonal: S = Q K_j^T and dP = dO V_j^T, the rows
-// (one thread per query) form dS = P (dP - delta), and dQ += dS K_j (K_j as
-// an MN-major operand) accumulates in TMEM; dQ scale goes out as BF16.
+// 64-key sub-tiles up to the diagonal.  Q and dO are constant for the CTA and
+// sit in TMEM, where the tensor core reads them as A operands, so shared
+// memory only carries the K / V sub-tiles: S = Q K_j^T and dP = dO V_j^T go
+// to double-buffered TMEM, the rows form dS = P (dP - delta) and store it as
+// BF16 over the S columns they just read, and dQ += dS K_j takes dS from TMEM
+// and K_j (MN-major) from shared memory.  TMEM: Q, dO (hd/2 columns each),
+// 2 x (S | dP), dQ.
 //
 // Both grids are ordered longest work first.  Every wait is bounded.
 constexpr int CH64 = 8192;  // one 64-column chunk of a 64-row tile (64 rows x 128 B)
 constexpr int NQS = 3;      // Q / dO sub-tile stages of the dK/dV kernel
-constexpr int NKS = 4;      // K / V sub-tile stages of the dQ kernel
+constexpr int NKS = 4;      // K sub-tile stages of the dQ kernel (held until dQ += dS K)
+constexpr int NVS = 4;      // V sub-tile stages of the dQ kernel (held until dP = dO V^T)
 
 template <int HD>
 __host__ __device__ constexpr int kv_smem_bytes() {
@@ -434,7 +499,7 @@ __host__ __device__ constexpr int kv_smem_bytes() {
 }
 template <int HD>
 __host__ __device__ constexpr int q_smem_bytes() {
-  return (HD / 64) * (2 * CH + 2 * NKS * CH64) + 2 * CH + 256 + 1024;
+  return (HD / 64) * (NKS + NVS) * CH64 + 256 + 1024;
 }
 static_assert(kv_smem_bytes<128>() <= 232448, "dK/dV kernel shared memory");
 static_assert(q_smem_bytes<128>() <= 232448, "dQ kernel shared memory");
@@ -558,19 +623,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = mbar_wait(kv_full, 0, abort_flag);
       constexpr uint32_t I_S = idesc(128, 64, false, false);  // S^T, dP^T: both operands K-major over hd
       constexpr uint32_t I_G = idesc(128, HD, false, true);   // dV, dK: B = dO / Q as MN-major
-      const uint32_t aK = su32(sK), aV = su32(sV), aQ = su32(sQ), aO = su32(sO), aP = su32(sP), aD = su32(sD);
+      // K-major views (S^T, dP^T) and MN-major views (dV, dK) of the tiles
+      const uint64_t dK = sdesc(su32(sK), 16, 1024), dV = sdesc(su32(sV), 16, 1024);
+      const uint64_t dQ = sdesc(su32(sQ), 16, 1024), dO = sdesc(su32(sO), 16, 1024);
+      const uint64_t dQm = sdesc(su32(sQ), CH64, 1024), dOm = sdesc(su32(sO), CH64, 1024);
+      const uint64_t dP = sdesc(su32(sP), 16, 1024), dD = sdesc(su32(sD), 16, 1024);
       auto issue_s = [&](int i) -> bool {
         const int st = i % NQS, b = i & 1;
         if (!mbar_wait(&qf[st], (uint32_t)((i / NQS) & 1), abort_flag)) return false;
         tc_fence_after();
         const uint32_t tS = tmem + 128 * b, tP = tS + 64;
+        const uint64_t q = dadv(dQ, st * NC * CH64), o = dadv(dO, st * NC * CH64);
 #pragma unroll
         for (int c = 0; c < NC; ++c)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint32_t oa = c * CH + k * 32, ob = (st * NC + c) * CH64 + k * 32;
-            tc_mma(tS, sdesc(aK + oa, 16, 1024), sdesc(aQ + ob, 16, 1024), I_S, (c | k) != 0);
-            tc_mma(tP, sdesc(aV + oa, 16, 1024), sdesc(aO + ob, 16, 1024), I_S, (c | k) != 0);
+            const uint32_t oa = c * CH + k * 32, ob = c * CH64 + k * 32;
+            tc_mma(tS, dadv(dK, oa), dadv(q, ob), I_S, (c | k) != 0);
+            tc_mma(tP, dadv(dV, oa), dadv(o, ob), I_S, (c | k) != 0);
           }
         tc_commit(&s_full[b]);
         return true;
@@ -579,13 +649,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int st = i % NQS, b = i & 1;
         if (!mbar_wait(&p_full[b], (uint32_t)((i >> 1) & 1), abort_flag)) return false;
         tc_fence_after();
+        const uint64_t p = dadv(dP, b * CH), d = dadv(dD, b * CH);
+        const uint64_t om = dadv(dOm, st * NC * CH64), qm = dadv(dQm, st * NC * CH64);
+        const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t pa = b * CH + kk * 32;                // K-major over the 64 queries
-          const uint32_t rows = st * NC * CH64 + kk * 16 * 128;  // 16 query rows of the MN-major tile
-          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          tc_mma(tdV, sdesc(aP + pa, 16, 1024), sdesc(aO + rows, CH64, 1024), I_G, acc);
-          tc_mma(tdK, sdesc(aD + pa, 16, 1024), sdesc(aQ + rows, CH64, 1024), I_G, acc);
+          const uint32_t acc = kk > 0 ? 1u : acc0;
+          // A: K-major over the 64 queries; B: 16 query rows of the MN-major tile
+          tc_mma(tdV, dadv(p, kk * 32), dadv(om, kk * 16 * 128), I_G, acc);
+          tc_mma(tdK, dadv(d, kk * 32), dadv(qm, kk * 16 * 128), I_G, acc);
         }
         tc_commit(&pd_free[b]);
         tc_commit(&qe[st]);
@@ -729,26 +801,25 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 template <int HD>
-__global__ void __launch_bounds__(THREADS, 1)
-    attn_bwd_q_k(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo, int S, int n_seq,
-                 int nh, int nkv, const float* __restrict__ lse, const float* __restrict__ delta, float scale,
-                 float scale_log2, bf16* __restrict__ dqkv) {
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    attn_bwd_q_k(const __grid_constant__ CUtensorMap tq, const bf16* __restrict__ qkv, const bf16* __restrict__ dout,
+                 int S, int n_seq, int nh, int nkv, const float* __restrict__ lse, const float* __restrict__ delta,
+                 float scale, float scale_log2, bf16* __restrict__ dqkv) {
   constexpr int NC = HD / 64;
+  constexpr int QC = HD / 2;  // TMEM columns of one BF16 row of hd values
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = sm;                    // [128 q][HD]: NC chunks of 128 rows
-  uint8_t* sO = sQ + NC * CH;          // dO, the same
-  uint8_t* sK = sO + NC * CH;          // NKS stages of [64 keys][HD]
-  uint8_t* sV = sK + NKS * NC * CH64;  // the same
-  uint8_t* sS = sV + NKS * NC * CH64;  // 2 buffers of dS [128 q][64 keys]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + 2 * CH);
-  uint64_t* q_full = bars;
+  uint8_t* sK = sm;                    // NKS stages of [64 keys][HD]
+  uint8_t* sV = sK + NKS * NC * CH64;  // NVS stages of [64 keys][HD]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NVS * NC * CH64);
+  uint64_t* q_ready = bars;         // Q, dO written to TMEM by the rows
   uint64_t* kf = bars + 1;          // [NKS]
   uint64_t* ke = kf + NKS;          // [NKS]
-  uint64_t* s_full = ke + NKS;      // [2]
-  uint64_t* p_full = s_full + 2;    // [2]
-  uint64_t* ds_free = p_full + 2;   // [2]
-  uint64_t* acc_full = ds_free + 2;
+  uint64_t* vf = ke + NKS;          // [NVS]
+  uint64_t* ve = vf + NVS;          // [NVS]
+  uint64_t* s_full = ve + NVS;      // [2]
+  uint64_t* p_full = s_full + 2;    // [2] dS in TMEM
+  uint64_t* acc_full = p_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -765,21 +836,23 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int64_t ld = (int64_t)(nh + 2 * nkv) * HD;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(q_ready, 256);
     for (int i = 0; i < NKS; ++i) {
       mbar_init(&kf[i], 1);
       mbar_init(&ke[i], 1);
     }
+    for (int i = 0; i < NVS; ++i) {
+      mbar_init(&vf[i], 1);
+      mbar_init(&ve[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
-      mbar_init(&ds_free[i], 1);
+      mbar_init(&p_full[i], 256);
     }
     mbar_init(acc_full, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tq) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tdo) : "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
@@ -790,34 +863,33 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tdQ = tmem + 256;
-  bool q_inflight = false;
-  uint32_t k_inflight = 0, k_par = 0;
+  const uint32_t tQ = tmem, tdO = tmem + QC, tSP = tmem + 2 * QC, tdQ = tmem + 2 * QC + 256;
+  uint32_t k_inflight = 0, k_par = 0, v_inflight = 0, v_par = 0;
 
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      mbar_expect_tx(q_full, 2 * NC * CH);
-      for (int c = 0; c < NC; ++c)
-        for (int hf = 0; hf < 2; ++hf) {
-          tma_load(&tq, q_full, sQ + c * CH + hf * CH64, h * HD + 64 * c, row0 + q0 + 64 * hf);
-          tma_load(&tdo, q_full, sO + c * CH + hf * CH64, h * HD + 64 * c, row0 + q0 + 64 * hf);
-        }
-      q_inflight = true;
       for (int j = 0; j < nkt && ok; ++j) {
-        const int st = j % NKS;
-        const uint32_t u = (uint32_t)(j / NKS);
+        const int st = j % NKS, sv = j % NVS;
+        const uint32_t u = (uint32_t)(j / NKS), uv = (uint32_t)(j / NVS);
         if (!mbar_wait(&ke[st], (u & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
-        mbar_expect_tx(&kf[st], 2 * NC * CH64);
-        for (int c = 0; c < NC; ++c) {
+        mbar_expect_tx(&kf[st], NC * CH64);
+        for (int c = 0; c < NC; ++c)
           tma_load(&tq, &kf[st], sK + (st * NC + c) * CH64, (nh + kh) * HD + 64 * c, row0 + 64 * j);
-          tma_load(&tq, &kf[st], sV + (st * NC + c) * CH64, (nh + nkv + kh) * HD + 64 * c, row0 + 64 * j);
-        }
         k_inflight |= 1u << st;
         k_par = (k_par & ~(1u << st)) | ((u & 1) << st);
+        if (!mbar_wait(&ve[sv], (uv & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(&vf[sv], NC * CH64);
+        for (int c = 0; c < NC; ++c)
+          tma_load(&tq, &vf[sv], sV + (sv * NC + c) * CH64, (nh + nkv + kh) * HD + 64 * c, row0 + 64 * j);
+        v_inflight |= 1u << sv;
+        v_par = (v_par & ~(1u << sv)) | ((uv & 1) << sv);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -826,38 +898,46 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      bool ok = mbar_wait(q_full, 0, abort_flag);
-      constexpr uint32_t I_S = idesc(128, 64, false, false);  // S, dP: K-major over hd
-      constexpr uint32_t I_G = idesc(128, HD, false, true);   // dQ: B = K_j as MN-major
-      const uint32_t aQ = su32(sQ), aO = su32(sO), aK = su32(sK), aV = su32(sV), aS = su32(sS);
+      bool ok = mbar_wait(q_ready, 0, abort_flag);
+      constexpr uint32_t I_S = idesc(128, 64, false, false);  // S, dP: A (Q, dO) in TMEM, B K-major over hd
+      constexpr uint32_t I_G = idesc(128, HD, false, true);   // dQ: A (dS) in TMEM, B = K_j as MN-major
+      const uint64_t dK = sdesc(su32(sK), 16, 1024), dV = sdesc(su32(sV), 16, 1024);
+      const uint64_t dKm = sdesc(su32(sK), CH64, 1024);
       auto issue_s = [&](int j) -> bool {
-        const int st = j % NKS, b = j & 1;
-        if (!mbar_wait(&kf[st], (uint32_t)((j / NKS) & 1), abort_flag)) return false;
+        const int sk = j % NKS, sv = j % NVS, b = j & 1;
+        if (!mbar_wait(&kf[sk], (uint32_t)((j / NKS) & 1), abort_flag) ||
+            !mbar_wait(&vf[sv], (uint32_t)((j / NVS) & 1), abort_flag))
+          return false;
         tc_fence_after();
-        const uint32_t tS = tmem + 128 * b, tP = tS + 64;
+        const uint32_t tS = tSP + 128 * b, tP = tS + 64;
+        const uint64_t kd = dadv(dK, sk * NC * CH64), vd = dadv(dV, sv * NC * CH64);
 #pragma unroll
-        for (int c = 0; c < NC; ++c)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t oa = c * CH + k * 32, ob = (st * NC + c) * CH64 + k * 32;
-            tc_mma(tS, sdesc(aQ + oa, 16, 1024), sdesc(aK + ob, 16, 1024), I_S, (c | k) != 0);
-            tc_mma(tP, sdesc(aO + oa, 16, 1024), sdesc(aV + ob, 16, 1024), I_S, (c | k) != 0);
-          }
+        for (int ks = 0; ks < HD / 16; ++ks) {
+          const uint32_t ob = (ks >> 2) * CH64 + (ks & 3) * 32;
+          tc_mma_ts(tS, tQ + 8 * ks, dadv(kd, ob), I_S, ks != 0);
+          tc_mma_ts(tP, tdO + 8 * ks, dadv(vd, ob), I_S, ks != 0);
+        }
         tc_commit(&s_full[b]);
+        tc_commit(&ve[sv]);  // V_j is read by dP only
         return true;
       };
       auto issue_g = [&](int j) -> bool {
-        const int st = j % NKS, b = j & 1;
+        const int sk = j % NKS, b = j & 1;
         if (!mbar_wait(&p_full[b], (uint32_t)((j >> 1) & 1), abort_flag)) return false;
         tc_fence_after();
+        const uint32_t tS = tSP + 128 * b;
+        const uint64_t km = dadv(dKm, sk * NC * CH64);
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
+        // dS of keys 0..31 sits in S columns 0..15, keys 32..63 in columns 32..47
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma(tdQ, sdesc(aS + b * CH + kk * 32, 16, 1024), sdesc(aK + st * NC * CH64 + kk * 16 * 128, CH64, 1024),
-                 I_G, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&ds_free[b]);
-        tc_commit(&ke[st]);
+          tc_mma_ts(tdQ, tS + (kk >> 1) * 32 + (kk & 1) * 8, dadv(km, kk * 16 * 128), I_G, kk > 0 ? 1u : acc0);
+        tc_commit(&ke[sk]);
         return true;
       };
+      // S of sub-tile j + 1 goes to the TMEM buffer of sub-tile j - 1, whose
+      // S / dP the rows have read (p_full waited for in issue_g(j - 1)) and
+      // whose dS the dQ MMAs of j - 1, issued before, read first.
       if (ok) ok = issue_s(0);
       for (int j = 0; j < nkt && ok; ++j) {
         if (j + 1 < nkt && !issue_s(j + 1)) {
@@ -876,64 +956,87 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else {
-    const int qw = warp & 3;
-    const int r = qw * 32 + lane;  // query row of S, dP, dQ
+    // Row warps 2..9: query rows by TMEM lane quarter; warps 2..5 own key
+    // columns 0..31 of a sub-tile (and the first half of Q, dO, dQ's hd
+    // columns), warps 6..9 key columns 32..63 (and the second half).
+    const int qw = warp & 3, half = (warp - 2) >> 2;
+    const int r = qw * 32 + lane;  // query row
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
     const int q = q0 + r;
     const bool valid = q < S;
     const int64_t li = (int64_t)h * T + row0 + (valid ? q : 0);
     const float lse2 = valid ? lse[li] * 1.4426950408889634f : 0.f;
     const float dl = valid ? delta[li] : 0.f;
+    // this row's half of Q and of dO into TMEM (the A operands of S and dP)
+    {
+      const uint4* qs = reinterpret_cast<const uint4*>(qkv + ((int64_t)row0 + (valid ? q : 0)) * ld +
+                                                         (int64_t)h * HD + half * (HD / 2));
+      const uint4* os = reinterpret_cast<const uint4*>(dout + ((int64_t)row0 + (valid ? q : 0)) * ((int64_t)nh * HD) +
+                                                         (int64_t)h * HD + half * (HD / 2));
+      uint32_t qv[QC / 2], ov[QC / 2];
+#pragma unroll
+      for (int i = 0; i < QC / 8; ++i) {
+        const uint4 a = valid ? qs[i] : make_uint4(0, 0, 0, 0);
+        const uint4 c = valid ? os[i] : make_uint4(0, 0, 0, 0);
+        qv[4 * i] = a.x; qv[4 * i + 1] = a.y; qv[4 * i + 2] = a.z; qv[4 * i + 3] = a.w;
+        ov[4 * i] = c.x; ov[4 * i + 1] = c.y; ov[4 * i + 2] = c.z; ov[4 * i + 3] = c.w;
+      }
+      if constexpr (QC / 2 == 32) {
+        tmem_st32u(tQ + lane_off + half * (QC / 2), qv);
+        tmem_st32u(tdO + lane_off + half * (QC / 2), ov);
+      } else {
+        tmem_st16(tQ + lane_off + half * (QC / 2), qv);
+        tmem_st16(tdO + lane_off + half * (QC / 2), ov);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(q_ready);
+    }
     bool ok = true;
     for (int j = 0; j < nkt; ++j) {
       const int b = j & 1;
       const uint32_t u = (uint32_t)(j >> 1);
-      bool w = true;
-      if (j >= 2) w = mbar_wait(&ds_free[b], (u - 1) & 1, abort_flag);
-      if (w) w = mbar_wait(&s_full[b], u & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, w)) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], u & 1, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int k0 = 64 * j;
-      const bool need_mask = (k0 + 63 > q0) || (k0 + 64 > S);
-      uint8_t* srow = sS + b * CH + (r >> 3) * 1024 + (r & 7) * 128;
-      const uint32_t tS = tmem + 128 * b, tP = tS + 64;
+      const int k0 = 64 * j + 32 * half;  // first key of this thread's 32 columns
+      const bool need_mask = (k0 + 31 > q0) || (k0 + 32 > S);
+      const uint32_t tS = tSP + 128 * b + half * 32, tP = tS + 64;
+      uint32_t sv[32], dp[32];
+      tmem_ld32_nw(tS + lane_off, sv);
+      tmem_ld32_nw(tP + lane_off, dp);
+      tmem_wait_ld2(sv, dp);
+      uint32_t dw[16];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float sv[32], dp[32];
-        tmem_ld32(tS + lane_off + c * 32, sv);
-        tmem_ld32(tP + lane_off + c * 32, dp);
-        uint32_t dw[16];
+      for (int e = 0; e < 32; e += 2) {
+        float dv[2];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float dv[2];
-#pragma unroll
-          for (int tt = 0; tt < 2; ++tt) {
-            float p = exp2f(sv[e + tt] * scale_log2 - lse2);
-            if (need_mask) {
-              const int key = k0 + c * 32 + e + tt;
-              if (key > q || key >= S) p = 0.f;
-            }
-            dv[tt] = p * (dp[e + tt] - dl);
+        for (int tt = 0; tt < 2; ++tt) {
+          float p = ex2(__uint_as_float(sv[e + tt]) * scale_log2 - lse2);
+          if (need_mask) {
+            const int key = k0 + e + tt;
+            if (key > q || key >= S) p = 0.f;
           }
-          dw[e / 2] = pack2(dv[0], dv[1]);
+          dv[tt] = p * (__uint_as_float(dp[e + tt]) - dl);
         }
-        store_row_units(srow, r, c, dw);
+        dw[e / 2] = pack2(dv[0], dv[1]);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      // dS (BF16 pairs) over the first 16 of the S columns this thread just read
+      tmem_st16(tS + lane_off, dw);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full[b]);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
     if (ok) {
       tc_fence_after();
-      bf16* row = dqkv + ((int64_t)row0 + (valid ? q : 0)) * ld + (int64_t)h * HD;
+      bf16* row = dqkv + ((int64_t)row0 + (valid ? q : 0)) * ld + (int64_t)h * HD + half * (HD / 2);
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < HD / 64; ++c) {
         float v[32];
-        tmem_ld32(tdQ + lane_off + c * 32, v);
+        tmem_ld32(tdQ + lane_off + half * (HD / 2) + c * 32, v);
         if (valid) {
 #pragma unroll
           for (int i4 = 0; i4 < 4; ++i4)
@@ -950,12 +1053,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0 && lane == 0 && *abort_flag) {
     const long long t0 = clock64();
-    if (q_inflight)
-      while (!mbar_test(q_full, 0) && clock64() - t0 < kWaitCycles) {
-      }
     for (int s2 = 0; s2 < NKS; ++s2)
       if (k_inflight & (1u << s2))
         while (!mbar_test(&kf[s2], (k_par >> s2) & 1) && clock64() - t0 < kWaitCycles) {
+        }
+    for (int s2 = 0; s2 < NVS; ++s2)
+      if (v_inflight & (1u << s2))
+        while (!mbar_test(&vf[s2], (v_par >> s2) & 1) && clock64() - t0 < kWaitCycles) {
         }
   }
   tc_fence_before();
@@ -1038,8 +1142,8 @@ cudaError_t launch_bwd(const bf16* qkv, const bf16* dout, const float* lse, cons
                                                          scale * 1.4426950408889634f, dqkv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_bwd_q_k<HD><<<(unsigned)gq, THREADS, SQ, s>>>(mq, mo, S, n_seq, nh, nkv, lse, delta, scale,
-                                                      scale * 1.4426950408889634f, dqkv);
+  attn_bwd_q_k<HD><<<(unsigned)gq, BWD_THREADS, SQ, s>>>(mq, qkv, dout, S, n_seq, nh, nkv, lse, delta, scale,
+                                                          scale * 1.4426950408889634f, dqkv);
   return cudaGetLastError();
 }
 
