@@ -256,6 +256,7 @@ def main():
     ap.add_argument("--ckpt-on-host", type=int, default=1)
     ap.add_argument("--ckpt-interval", type=int, default=1, help="layers per recompute segment")
     ap.add_argument("--buffers", type=int, default=2, help="device weight buffers (1: single-buffer ablation)")
+    ap.add_argument("--layers", type=int, default=0, help="decoder depth override (depth sweeps; 0 = the config's)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -282,7 +283,7 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    c = configs.get(args.config)
+    c = configs.get(args.config, **({"n_layers": args.layers} if args.layers > 0 else {}))
     T = c["micro"] * c["batch"] * c["seq"]
     P, F_exec, F_pages = model_numbers(c, args.ckpt_interval)
     # every replica on this host holds its own host state: refuse to start

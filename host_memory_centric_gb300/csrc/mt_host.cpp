@@ -204,21 +204,23 @@ void Pool::stop() {
 }
 
 void Pool::run(Task& t) {
+  bool bad = false;
+  std::string msg;
   try {
     (*t.fn)(t.i);
   } catch (const std::exception& e) {
-    std::lock_guard<std::mutex> lk(t.latch->mu);
-    t.latch->bad = true;
-    t.latch->msg = e.what();
+    bad = true;
+    msg = e.what();
   } catch (...) {
-    std::lock_guard<std::mutex> lk(t.latch->mu);
+    bad = true;
+    msg = "unknown exception in host worker";
+  }
+  std::lock_guard<std::mutex> lk(t.latch->mu);
+  if (bad && !t.latch->bad) {
     t.latch->bad = true;
-    t.latch->msg = "unknown exception in host worker";
+    t.latch->msg = msg;
   }
-  if (t.latch->left.fetch_sub(1) == 1) {
-    std::lock_guard<std::mutex> lk(t.latch->mu);
-    t.latch->cv.notify_all();
-  }
+  if (--t.latch->left == 0) t.latch->cv.notify_all();
 }
 
 bool Pool::run_one() {
@@ -242,10 +244,10 @@ bool Pool::parallel_for(int64_t n, const std::function<void(int64_t)>& fn, std::
     for (int64_t i = 0; i < n; ++i) q_.push_back({&fn, i, &latch});
   }
   cv_.notify_all();
-  while (latch.left.load() > 0) {
-    if (run_one()) continue;
+  for (;;) {
+    if (run_one()) continue;  // help with queued tasks
     std::unique_lock<std::mutex> lk(latch.mu);
-    latch.cv.wait_for(lk, std::chrono::milliseconds(2), [&] { return latch.left.load() == 0; });
+    if (latch.cv.wait_for(lk, std::chrono::milliseconds(2), [&] { return latch.left == 0; })) break;
   }
   if (latch.bad) {
     if (err) *err = latch.msg;

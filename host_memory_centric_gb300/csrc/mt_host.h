@@ -63,11 +63,15 @@ class Pool {
   bool parallel_for(int64_t n, const std::function<void(int64_t)>& fn, std::string* err);
 
  private:
+  // Completion count of one parallel_for, on the caller's stack.  Every
+  // access after the tasks are queued happens under mu, so the caller, which
+  // sees left == 0 only under mu, returns (and destroys the latch) only after
+  // the last worker has released it.
   struct Latch {
-    std::atomic<int64_t> left{0};
+    int64_t left = 0;
     std::mutex mu;
     std::condition_variable cv;
-    std::atomic<bool> bad{false};
+    bool bad = false;
     std::string msg;
   };
   struct Task {

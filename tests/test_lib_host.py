@@ -210,3 +210,29 @@ def test_device_footprint_independent_of_depth():
         L.mt_query_device_bytes(C.byref(cfg), C.byref(n))
         dev.append(n.value)
     assert dev[1] > dev[0]
+
+
+def test_worker_pool_has_no_data_race(tmp_path):
+    """The host worker pool under ThreadSanitizer: concurrent parallel_for
+    calls from two threads must report no data race (a worker that touched a
+    caller's completion latch after the caller returned once crashed the
+    library intermittently)."""
+    import shutil
+    import subprocess
+    cxx = shutil.which("g++")
+    if cxx is None:
+        pytest.skip("no g++")
+    here = os.path.dirname(os.path.abspath(__file__))
+    src = os.path.join(os.path.dirname(here), "host_memory_centric_gb300", "csrc")
+    inc = os.path.join(os.path.dirname(here), "include")
+    exe = str(tmp_path / "pool_stress")
+    cmd = [cxx, "-std=c++17", "-O1", "-g", "-fsanitize=thread", "-I" + src, "-I" + inc,
+           "-I" + os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include"),
+           os.path.join(here, "pool_stress.cpp"), os.path.join(src, "mt_host.cpp"), "-o", exe, "-lpthread"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        pytest.skip("ThreadSanitizer build unavailable: " + r.stderr[-200:])
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=300,
+                       env=dict(os.environ, TSAN_OPTIONS="halt_on_error=1 exitcode=66"))
+    assert "ThreadSanitizer" not in r.stderr, r.stderr[-2000:]
+    assert r.returncode == 0 and r.stdout.startswith("ok"), (r.returncode, r.stdout, r.stderr[-500:])
