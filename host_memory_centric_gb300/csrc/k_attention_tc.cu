@@ -27,8 +27,8 @@
 namespace mt {
 namespace {
 
-constexpr int THREADS = 192;      // forward, dK/dV: TMA warp, MMA warp, 4 row warps
-constexpr int BWD_THREADS = 320;  // dQ kernel: TMA warp, MMA warp, 8 row warps (two per TMEM lane quarter)
+constexpr int THREADS = 192;      // forward: TMA warp, MMA warp, 4 softmax warps
+constexpr int BWD_THREADS = 320;  // backward: TMA warp, MMA warp, 8 row warps (two per TMEM lane quarter)
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr int CH = 16384;  // one 64-column chunk of a 128-row tile (128 rows x 128 B)
 
@@ -124,6 +124,13 @@ __device__ __forceinline__ void tmem_wait_ld2(uint32_t (&a)[32], uint32_t (&b)[3
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(a[i]), "+r"(b[i]));
+}
+// The same for four register arrays (all four loads behind one wait).
+__device__ __forceinline__ void tmem_wait_ld4(uint32_t (&a)[32], uint32_t (&b)[32], uint32_t (&c)[32],
+                                              uint32_t (&d)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(a[i]), "+r"(b[i]), "+r"(c[i]), "+r"(d[i]));
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
@@ -463,93 +470,84 @@ __global__ void __launch_bounds__(THREADS, 1)
 // ---------------------------------------------------------------------------
 // Backward, as two kernels that share no accumulator (so no atomics and no
 // FP32 dQ buffer).  delta[h][t] = rowsum(dO o O) is computed before them.
+// Both work on 128 x 128 tiles: inside these kernels a tcgen05.mma costs
+// about the same at N = 64 as at N = 128, so the wider tile halves the MMA
+// count per unit of work.  TMEM holds one tile's scores (single-buffered); the
+// row warps write P / dS back over the scores they have read, as BF16, and the
+// accumulating MMAs read them from there as their A operand.  The MMA warp
+// issues the accumulation of tile i before the scores of tile i + 1 into the
+// same columns; tcgen05.mma operations of one thread run in issue order.
 //
-// attn_bwd_kv_k: one CTA per (128 keys, kv head, sequence); it loops over the
-// query heads of its group and, per head, over 64-query sub-tiles from the
-// diagonal to the sequence end.  Per sub-tile i (TMEM and shared buffers
-// alternate with i, Q / dO sub-tiles sit in a 3-stage ring):
-//   MMA   S^T = K Q_i^T and dP^T = V dO_i^T (M = 128 keys, N = 64 queries);
-//   rows  (one thread per key) P^T = exp2(S^T scale log2e - lse log2e), masked
-//         causally where the sub-tile needs it, dS^T = P^T (dP^T - delta),
-//         both as BF16 into 128B-swizzled [key][q] tiles;
-//   MMA   dV += P^T dO_i and dK += dS^T Q_i (dO_i and Q_i as MN-major
-//         operands); the accumulators stay in TMEM for the whole CTA.
-// The MMA warp issues S of sub-tile i+1 before it waits for the rows' P of
-// sub-tile i, so the tensor core and the row warps work at the same time.
-// TMEM: (S^T | dP^T) x 2 = 256 columns, dV, dK.
+// attn_bwd_kv_k: one CTA per (128 keys, kv head, sequence), grid ordered
+// longest work first; it loops over the query heads of its group and, per
+// head, over 128-query tiles from the diagonal on.  Per tile:
+//   MMA   S^T = K Q^T and dP^T = V dO^T (K, V resident in shared memory; Q, dO
+//         tiles in a 2-stage TMA ring);
+//   rows  (8 warps: key rows by TMEM lane quarter, query halves) P^T =
+//         exp2(S^T scale log2e - lse log2e) with the causal mask where needed,
+//         dS^T = P^T (dP^T - delta), written as BF16 over S^T / dP^T;
+//   MMA   dV += P^T dO and dK += dS^T Q (dO, Q as MN-major operands).
+// TMEM: S^T | dP^T | dV | dK.
 //
-// attn_bwd_q_k: one CTA per (128 queries, query head, sequence) looping over
-// 64-key sub-tiles up to the diagonal.  Q and dO are constant for the CTA and
-// sit in TMEM, where the tensor core reads them as A operands, so shared
-// memory only carries the K / V sub-tiles: S = Q K_j^T and dP = dO V_j^T go
-// to double-buffered TMEM, the rows form dS = P (dP - delta) and store it as
-// BF16 over the S columns they just read, and dQ += dS K_j takes dS from TMEM
-// and K_j (MN-major) from shared memory.  TMEM: Q, dO (hd/2 columns each),
-// 2 x (S | dP), dQ.
-//
-// Both grids are ordered longest work first.  Every wait is bounded.
-constexpr int CH64 = 8192;  // one 64-column chunk of a 64-row tile (64 rows x 128 B)
-constexpr int NQS = 3;      // Q / dO sub-tile stages of the dK/dV kernel
-constexpr int NKS = 4;      // K sub-tile stages of the dQ kernel (held until dQ += dS K)
-constexpr int NVS = 4;      // V sub-tile stages of the dQ kernel (held until dP = dO V^T)
+// attn_bwd_q_k: one CTA per (128 queries, query head, sequence), longest work
+// first, looping over 128-key tiles up to the diagonal.  Q and dO are written
+// into TMEM once by the row warps and are the A operands of S = Q K^T and
+// dP = dO V^T; the rows write dS over S; dQ += dS K reads dS from TMEM and K
+// (MN-major) from shared memory; dQ scale leaves as BF16.  TMEM: Q | dO | S |
+// dP | dQ.  Every wait is bounded.
+constexpr int CH64 = 8192;  // one 64-column chunk of a 64-row box (64 rows x 128 B)
+constexpr int NQT = 2;      // Q / dO tile stages of the dK/dV kernel
+constexpr int NKT = 3;      // K / V tile stages of the dQ kernel
 
 template <int HD>
 __host__ __device__ constexpr int kv_smem_bytes() {
-  return (HD / 64) * (2 * CH + 2 * NQS * CH64) + 4 * CH + 1024 + 256 + 1024;
+  return (HD / 64) * CH * (2 + 2 * NQT) + 2048 + 256 + 1024;
 }
 template <int HD>
 __host__ __device__ constexpr int q_smem_bytes() {
-  return (HD / 64) * (NKS + NVS) * CH64 + 256 + 1024;
+  return (HD / 64) * CH * 2 * NKT + 256 + 1024;
 }
 static_assert(kv_smem_bytes<128>() <= 232448, "dK/dV kernel shared memory");
 static_assert(q_smem_bytes<128>() <= 232448, "dQ kernel shared memory");
 
-// 32 (p, ds) pairs of one row into the 16-byte units 4c .. 4c+3 of that row
-// of a 128B-swizzled tile whose rows are 128 bytes (64 BF16 values).
-__device__ __forceinline__ void store_row_units(uint8_t* row, int r, int c, const uint32_t (&w)[16]) {
-#pragma unroll
-  for (int u4 = 0; u4 < 4; ++u4) {
-    const int unit = c * 4 + u4;
-    *reinterpret_cast<uint4*>(row + ((unit ^ (r & 7)) << 4)) =
-        make_uint4(w[4 * u4], w[4 * u4 + 1], w[4 * u4 + 2], w[4 * u4 + 3]);
-  }
-}
+// P / dS columns of one 16-element K-step of a 128-wide tile written back by
+// the two row halves: half h's 64 values occupy columns 64 h .. 64 h + 31.
+__device__ __forceinline__ uint32_t pcol(int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); }
 
 template <int HD>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_kv_k(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo, int S,
                   int n_seq, int nh, int nkv, const float* __restrict__ lse, const float* __restrict__ delta,
                   float scale, float scale_log2, bf16* __restrict__ dqkv) {
   constexpr int NC = HD / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = sm;                    // [128 keys][HD]: NC chunks of 128 rows
+  uint8_t* sK = sm;                  // [128 keys][HD]: NC chunks of 128 rows
   uint8_t* sV = sK + NC * CH;
-  uint8_t* sQ = sV + NC * CH;          // NQS stages of [64 q][HD]: NC chunks of 64 rows each
-  uint8_t* sO = sQ + NQS * NC * CH64;  // dO, the same
-  uint8_t* sP = sO + NQS * NC * CH64;  // 2 buffers of P^T  [128 keys][64 q]
-  uint8_t* sD = sP + 2 * CH;           // 2 buffers of dS^T [128 keys][64 q]
-  float* ls = reinterpret_cast<float*>(sD + 2 * CH);  // [2][64] lse log2e of the sub-tile
-  float* dls = ls + 128;                              // [2][64] delta of the sub-tile
-  uint64_t* bars = reinterpret_cast<uint64_t*>(dls + 128);
+  uint8_t* sQ = sV + NC * CH;        // NQT stages of [128 q][HD]
+  uint8_t* sO = sQ + NQT * NC * CH;  // dO, the same
+  float* ls = reinterpret_cast<float*>(sO + NQT * NC * CH);  // [2][128] lse log2e of the tile
+  float* dls = ls + 256;                                      // [2][128] delta of the tile
+  uint64_t* bars = reinterpret_cast<uint64_t*>(dls + 256);
   uint64_t* kv_full = bars;
-  uint64_t* qf = bars + 1;           // [NQS] Q / dO stage loaded
-  uint64_t* qe = qf + NQS;           // [NQS] Q / dO stage consumed
-  uint64_t* s_full = qe + NQS;       // [2] S^T, dP^T in TMEM
-  uint64_t* p_full = s_full + 2;     // [2] P^T, dS^T in shared memory (TMEM buffer read)
-  uint64_t* pd_free = p_full + 2;    // [2] P^T, dS^T consumed by the MMAs
-  uint64_t* ld_ready = pd_free + 2;  // [2] lse / delta staged
+  uint64_t* qf = bars + 1;           // [NQT] Q / dO tile loaded
+  uint64_t* qe = qf + NQT;           // [NQT] Q / dO tile consumed
+  uint64_t* s1_full = qe + NQT;      // S^T in TMEM
+  uint64_t* s2_full = s1_full + 1;   // dP^T in TMEM
+  uint64_t* p1_full = s2_full + 1;   // P^T written back over S^T
+  uint64_t* p2_full = p1_full + 1;   // dS^T written back over dP^T
+  uint64_t* ld_ready = p2_full + 1;  // [2] lse / delta staged
   uint64_t* acc_full = ld_ready + 2; // dK, dV complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int per_kb = nkv * n_seq;
-  const int kb = (int)(blockIdx.x / per_kb);  // key tile 0 has the most query sub-tiles
+  const int kb = (int)(blockIdx.x / per_kb);  // key tile 0 has the most query tiles
   const int g = (int)(blockIdx.x % per_kb) / n_seq, n = (int)(blockIdx.x % n_seq);
   const int grp = nh / nkv;
-  const int nqs = (S + 63) / 64;
-  const int per_head = nqs - 2 * kb;
+  const int nqb = (S + 127) / 128;
+  const int per_head = nqb - kb;
   const int iters = grp * per_head;
   const int k0 = kb * 128;
   const int row0 = n * S;
@@ -558,16 +556,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int i = 0; i < NQS; ++i) {
+    for (int i = 0; i < NQT; ++i) {
       mbar_init(&qf[i], 1);
       mbar_init(&qe[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
-      mbar_init(&pd_free[i], 1);
-      mbar_init(&ld_ready[i], 128);
-    }
+    mbar_init(s1_full, 1);
+    mbar_init(s2_full, 1);
+    mbar_init(p1_full, 256);
+    mbar_init(p2_full, 256);
+    for (int i = 0; i < 2; ++i) mbar_init(&ld_ready[i], 256);
     mbar_init(acc_full, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -583,7 +580,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tdV = tmem + 256, tdK = tmem + 256 + HD;
+  const uint32_t tSt = tmem, tdPt = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + HD;
   bool kv_inflight = false;
   uint32_t q_inflight = 0, q_par = 0;
 
@@ -598,18 +595,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       kv_inflight = true;
       for (int i = 0; i < iters && ok; ++i) {
-        const int st = i % NQS;
-        const uint32_t u = (uint32_t)(i / NQS);
-        const int h = g * grp + i / per_head, q0 = (2 * kb + i % per_head) * 64;
+        const int st = i % NQT;
+        const uint32_t u = (uint32_t)(i / NQT);
+        const int h = g * grp + i / per_head, q0 = (kb + i % per_head) * 128;
         if (!mbar_wait(&qe[st], (u & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
-        mbar_expect_tx(&qf[st], 2 * NC * CH64);
-        for (int c = 0; c < NC; ++c) {
-          tma_load(&tq, &qf[st], sQ + (st * NC + c) * CH64, h * HD + 64 * c, row0 + q0);
-          tma_load(&tdo, &qf[st], sO + (st * NC + c) * CH64, h * HD + 64 * c, row0 + q0);
-        }
+        mbar_expect_tx(&qf[st], 2 * NC * CH);
+        for (int c = 0; c < NC; ++c)
+          for (int hf = 0; hf < 2; ++hf) {
+            tma_load(&tq, &qf[st], sQ + (st * NC + c) * CH + hf * CH64, h * HD + 64 * c, row0 + q0 + 64 * hf);
+            tma_load(&tdo, &qf[st], sO + (st * NC + c) * CH + hf * CH64, h * HD + 64 * c, row0 + q0 + 64 * hf);
+          }
         q_inflight |= 1u << st;
         q_par = (q_par & ~(1u << st)) | ((u & 1) << st);
       }
@@ -621,58 +619,66 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       bool ok = mbar_wait(kv_full, 0, abort_flag);
-      constexpr uint32_t I_S = idesc(128, 64, false, false);  // S^T, dP^T: both operands K-major over hd
-      constexpr uint32_t I_G = idesc(128, HD, false, true);   // dV, dK: B = dO / Q as MN-major
-      // K-major views (S^T, dP^T) and MN-major views (dV, dK) of the tiles
+      constexpr uint32_t I_S = idesc(128, 128, false, false);  // S^T, dP^T: both operands K-major over hd
+      constexpr uint32_t I_G = idesc(128, HD, false, true);    // dV, dK: A from TMEM, B = dO / Q MN-major
       const uint64_t dK = sdesc(su32(sK), 16, 1024), dV = sdesc(su32(sV), 16, 1024);
       const uint64_t dQ = sdesc(su32(sQ), 16, 1024), dO = sdesc(su32(sO), 16, 1024);
-      const uint64_t dQm = sdesc(su32(sQ), CH64, 1024), dOm = sdesc(su32(sO), CH64, 1024);
-      const uint64_t dP = sdesc(su32(sP), 16, 1024), dD = sdesc(su32(sD), 16, 1024);
-      auto issue_s = [&](int i) -> bool {
-        const int st = i % NQS, b = i & 1;
-        if (!mbar_wait(&qf[st], (uint32_t)((i / NQS) & 1), abort_flag)) return false;
+      const uint64_t dQm = sdesc(su32(sQ), CH, 1024), dOm = sdesc(su32(sO), CH, 1024);
+      // Per tile i the MMAs go out as dV(i), S^T(i+1), dK(i), dP^T(i+1): dV
+      // waits only for P^T, dK for dS^T, and the next tile's S^T is in flight
+      // while the rows form dS^T of tile i; S^T(i+1) overwrites the P^T(i)
+      // that dV(i) read before it, dP^T(i+1) the dS^T(i) dK(i) read.
+      auto issue_st = [&](int i) -> bool {  // S^T = K Q^T
+        const int st = i % NQT;
+        if (!mbar_wait(&qf[st], (uint32_t)((i / NQT) & 1), abort_flag)) return false;
         tc_fence_after();
-        const uint32_t tS = tmem + 128 * b, tP = tS + 64;
-        const uint64_t q = dadv(dQ, st * NC * CH64), o = dadv(dO, st * NC * CH64);
+        const uint64_t q = dadv(dQ, st * NC * CH);
 #pragma unroll
-        for (int c = 0; c < NC; ++c)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t oa = c * CH + k * 32, ob = c * CH64 + k * 32;
-            tc_mma(tS, dadv(dK, oa), dadv(q, ob), I_S, (c | k) != 0);
-            tc_mma(tP, dadv(dV, oa), dadv(o, ob), I_S, (c | k) != 0);
-          }
-        tc_commit(&s_full[b]);
+        for (int ks = 0; ks < HD / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * CH + (ks & 3) * 32;
+          tc_mma(tSt, dadv(dK, off), dadv(q, off), I_S, ks != 0);
+        }
+        tc_commit(s1_full);
         return true;
       };
-      auto issue_g = [&](int i) -> bool {
-        const int st = i % NQS, b = i & 1;
-        if (!mbar_wait(&p_full[b], (uint32_t)((i >> 1) & 1), abort_flag)) return false;
+      auto issue_dpt = [&](int i) {  // dP^T = V dO^T (its Q / dO stage was waited for by issue_st)
+        const uint64_t o = dadv(dO, (i % NQT) * NC * CH);
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * CH + (ks & 3) * 32;
+          tc_mma(tdPt, dadv(dV, off), dadv(o, off), I_S, ks != 0);
+        }
+        tc_commit(s2_full);
+      };
+      auto issue_dv = [&](int i) -> bool {  // dV += P^T dO
+        if (!mbar_wait(p1_full, (uint32_t)(i & 1), abort_flag)) return false;
         tc_fence_after();
-        const uint64_t p = dadv(dP, b * CH), d = dadv(dD, b * CH);
-        const uint64_t om = dadv(dOm, st * NC * CH64), qm = dadv(dQm, st * NC * CH64);
+        const uint64_t om = dadv(dOm, (i % NQT) * NC * CH);
         const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t acc = kk > 0 ? 1u : acc0;
-          // A: K-major over the 64 queries; B: 16 query rows of the MN-major tile
-          tc_mma(tdV, dadv(p, kk * 32), dadv(om, kk * 16 * 128), I_G, acc);
-          tc_mma(tdK, dadv(d, kk * 32), dadv(qm, kk * 16 * 128), I_G, acc);
-        }
-        tc_commit(&pd_free[b]);
+        for (int kk = 0; kk < 8; ++kk) tc_mma_ts(tdV, tSt + pcol(kk), dadv(om, kk * 2048), I_G, kk > 0 ? 1u : acc0);
+        return true;
+      };
+      auto issue_dk = [&](int i) -> bool {  // dK += dS^T Q; the Q / dO stage is then free
+        if (!mbar_wait(p2_full, (uint32_t)(i & 1), abort_flag)) return false;
+        tc_fence_after();
+        const int st = i % NQT;
+        const uint64_t qm = dadv(dQm, st * NC * CH);
+        const uint32_t acc0 = i > 0 ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) tc_mma_ts(tdK, tdPt + pcol(kk), dadv(qm, kk * 2048), I_G, kk > 0 ? 1u : acc0);
         tc_commit(&qe[st]);
         return true;
       };
-      if (ok) ok = issue_s(0);
+      if (ok) ok = issue_st(0);
+      if (ok) issue_dpt(0);
       for (int i = 0; i < iters && ok; ++i) {
-        if (i + 1 < iters && !issue_s(i + 1)) {
+        const bool more = i + 1 < iters;
+        if (!issue_dv(i) || (more && !issue_st(i + 1)) || !issue_dk(i)) {
           ok = false;
           break;
         }
-        if (!issue_g(i)) {
-          ok = false;
-          break;
-        }
+        if (more) issue_dpt(i + 1);
       }
       if (ok) tc_commit(acc_full);
       if (!ok) {
@@ -681,99 +687,123 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else {
-    const int qw = warp & 3;
+    // Row warps 2..9: warp w reads TMEM lanes 32 (w % 4) .. +31 (key rows);
+    // warps 2..5 take queries 0..63 of the tile, warps 6..9 queries 64..127
+    // (and at the end dK, dV respectively).
+    const int qw = warp & 3, half = (warp - 2) >> 2;
     const int r = qw * 32 + lane;  // key row of S^T, dP^T, dV, dK
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
     const int key = k0 + r;
-    const int t = threadIdx.x - 64;  // staging entry: lse (t < 64) or delta (t >= 64) of query t % 64
-    float* stage = t < 64 ? ls : dls;
+    const int t = threadIdx.x - 64;  // staging entry: lse (t < 128) or delta (t >= 128) of query t % 128
+    float* stage = t < 128 ? ls : dls;
     auto fetch = [&](int i) -> float {
-      const int h = g * grp + i / per_head, q = (2 * kb + i % per_head) * 64 + (t & 63);
+      const int h = g * grp + i / per_head, q = (kb + i % per_head) * 128 + (t & 127);
       if (q >= S) return 0.f;
       const int64_t idx = (int64_t)h * T + row0 + q;
-      return t < 64 ? lse[idx] * 1.4426950408889634f : delta[idx];
+      return t < 128 ? lse[idx] * 1.4426950408889634f : delta[idx];
     };
     bool ok = true;
-    float nxt = fetch(0);  // one sub-tile ahead, so the global load latency hides behind a sub-tile
+    float nxt = fetch(0);  // one tile ahead, so the global load latency hides behind a tile
     for (int i = 0; i < iters; ++i) {
       const int b = i & 1;
       const uint32_t u = (uint32_t)(i >> 1);
-      const int q0 = (2 * kb + i % per_head) * 64;
-      // Buffer b was last read in sub-tile i-2; every thread finished that
-      // before it arrived on ld_ready for sub-tile i-1, which this thread has
-      // waited for.
-      stage[b * 64 + (t & 63)] = nxt;
+      const int q0 = (kb + i % per_head) * 128;
+      // Buffer b was last read in tile i-2; every thread finished that before
+      // it arrived on ld_ready for tile i-1, which this thread has waited for.
+      stage[b * 128 + (t & 127)] = nxt;
       mbar_arrive(&ld_ready[b]);
       if (i + 1 < iters) nxt = fetch(i + 1);
       bool w = mbar_wait(&ld_ready[b], u & 1, abort_flag);
-      if (w && i >= 2) w = mbar_wait(&pd_free[b], (u - 1) & 1, abort_flag);
-      if (w) w = mbar_wait(&s_full[b], u & 1, abort_flag);
+      if (w) w = mbar_wait(s1_full, (uint32_t)(i & 1), abort_flag);
       if (!__all_sync(0xffffffffu, w)) {  // warp-uniform: the TMEM loads below are warp-collective
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool need_mask = (q0 < k0 + 127) || (q0 + 64 > S);
-      const float* lrow = ls + b * 64;
-      const float* drow_d = dls + b * 64;
-      uint8_t* prow = sP + b * CH + (r >> 3) * 1024 + (r & 7) * 128;
-      uint8_t* drow = sD + b * CH + (r >> 3) * 1024 + (r & 7) * 128;
-      const uint32_t tS = tmem + 128 * b, tP = tS + 64;
+      const bool need_mask = (q0 < k0 + 127) || (q0 + 128 > S);
+      const float4* lrow = reinterpret_cast<const float4*>(ls + b * 128 + half * 64);
+      const float4* drow = reinterpret_cast<const float4*>(dls + b * 128 + half * 64);
+      // phase 1: P^T from S^T, back over the first 32 S^T columns this thread read
+      float p[64];
+      {
+        uint32_t sv[2][32];
+        tmem_ld32_nw(tSt + lane_off + half * 64, sv[0]);
+        tmem_ld32_nw(tSt + lane_off + half * 64 + 32, sv[1]);
+        tmem_wait_ld2(sv[0], sv[1]);
+        uint32_t pw[32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float st[32], dp[32];
-        tmem_ld32(tS + lane_off + c * 32, st);
-        tmem_ld32(tP + lane_off + c * 32, dp);
-        uint32_t pw[16], dw[16];
+        for (int e4 = 0; e4 < 16; ++e4) {
+          const float4 l4 = lrow[e4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int tt = 0; tt < 2; ++tt) {
-            const int ql = c * 32 + e + tt;
-            float p = exp2f(st[e + tt] * scale_log2 - lrow[ql]);
+          for (int tt = 0; tt < 4; ++tt) {
+            const int e = e4 * 4 + tt;
+            float pe = ex2(__uint_as_float(sv[e >> 5][e & 31]) * scale_log2 - lv[tt]);
             if (need_mask) {
-              const int q = q0 + ql;
-              if (q < key || q >= S) p = 0.f;
+              const int q = q0 + half * 64 + e;
+              if (q < key || q >= S) pe = 0.f;
             }
-            pv[tt] = p;
-            dv[tt] = p * (dp[e + tt] - drow_d[ql]);
+            p[e] = pe;
           }
-          pw[e / 2] = pack2(pv[0], pv[1]);
-          dw[e / 2] = pack2(dv[0], dv[1]);
+          pw[2 * e4] = pack2(p[4 * e4], p[4 * e4 + 1]);
+          pw[2 * e4 + 1] = pack2(p[4 * e4 + 2], p[4 * e4 + 3]);
         }
-        store_row_units(prow, r, c, pw);
-        store_row_units(drow, r, c, dw);
+        tmem_st32u(tSt + lane_off + half * 64, pw);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p1_full);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tc_fence_before();
-      mbar_arrive(&p_full[b]);
+      // phase 2: dS^T = P^T (dP^T - delta), back over the first 32 dP^T columns
+      if (!__all_sync(0xffffffffu, mbar_wait(s2_full, (uint32_t)(i & 1), abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        uint32_t dp[2][32];
+        tmem_ld32_nw(tdPt + lane_off + half * 64, dp[0]);
+        tmem_ld32_nw(tdPt + lane_off + half * 64 + 32, dp[1]);
+        tmem_wait_ld2(dp[0], dp[1]);
+        uint32_t dw[32];
+#pragma unroll
+        for (int e4 = 0; e4 < 16; ++e4) {
+          const float4 d4 = drow[e4];
+          const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+          float dv[4];
+#pragma unroll
+          for (int tt = 0; tt < 4; ++tt) {
+            const int e = e4 * 4 + tt;
+            dv[tt] = p[e] * (__uint_as_float(dp[e >> 5][e & 31]) - dl[tt]);
+          }
+          dw[2 * e4] = pack2(dv[0], dv[1]);
+          dw[2 * e4 + 1] = pack2(dv[2], dv[3]);
+        }
+        tmem_st32u(tdPt + lane_off + half * 64, dw);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p2_full);
+      }
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
     if (ok) {
-      // dK, dV of this thread's key row.  The TMEM loads are warp-collective:
-      // every lane loads, only rows inside the sequence store.
+      // warps 2..5: dK (scaled) of their key rows; warps 6..9: dV.  The TMEM
+      // loads are warp-collective: every lane loads, only rows inside the
+      // sequence store.
       tc_fence_after();
       const bool valid = key < S;
-      bf16* row = dqkv + ((int64_t)row0 + (valid ? key : 0)) * ld;
+      const float f = half == 0 ? scale : 1.f;
+      const uint32_t tacc = half == 0 ? tdK : tdV;
+      bf16* row = dqkv + ((int64_t)row0 + (valid ? key : 0)) * ld + (int64_t)(nh + half * nkv + g) * HD;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         float v[32];
-        tmem_ld32(tdK + lane_off + c * 32, v);
+        tmem_ld32(tacc + lane_off + c * 32, v);
         if (valid) {
 #pragma unroll
           for (int i4 = 0; i4 < 4; ++i4)
-            reinterpret_cast<uint4*>(row + (int64_t)(nh + g) * HD + c * 32)[i4] = make_uint4(
-                pack2(v[8 * i4] * scale, v[8 * i4 + 1] * scale), pack2(v[8 * i4 + 2] * scale, v[8 * i4 + 3] * scale),
-                pack2(v[8 * i4 + 4] * scale, v[8 * i4 + 5] * scale), pack2(v[8 * i4 + 6] * scale, v[8 * i4 + 7] * scale));
-        }
-        tmem_ld32(tdV + lane_off + c * 32, v);
-        if (valid) {
-#pragma unroll
-          for (int i4 = 0; i4 < 4; ++i4)
-            reinterpret_cast<uint4*>(row + (int64_t)(nh + nkv + g) * HD + c * 32)[i4] =
-                make_uint4(pack2(v[8 * i4], v[8 * i4 + 1]), pack2(v[8 * i4 + 2], v[8 * i4 + 3]),
-                           pack2(v[8 * i4 + 4], v[8 * i4 + 5]), pack2(v[8 * i4 + 6], v[8 * i4 + 7]));
+            reinterpret_cast<uint4*>(row + c * 32)[i4] =
+                make_uint4(pack2(v[8 * i4] * f, v[8 * i4 + 1] * f), pack2(v[8 * i4 + 2] * f, v[8 * i4 + 3] * f),
+                           pack2(v[8 * i4 + 4] * f, v[8 * i4 + 5] * f), pack2(v[8 * i4 + 6] * f, v[8 * i4 + 7] * f));
         }
       }
     } else if (lane == 0) {
@@ -787,7 +817,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (kv_inflight)
       while (!mbar_test(kv_full, 0) && clock64() - t0 < kWaitCycles) {
       }
-    for (int s2 = 0; s2 < NQS; ++s2)
+    for (int s2 = 0; s2 < NQT; ++s2)
       if (q_inflight & (1u << s2))
         while (!mbar_test(&qf[s2], (q_par >> s2) & 1) && clock64() - t0 < kWaitCycles) {
         }
@@ -809,17 +839,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   constexpr int QC = HD / 2;  // TMEM columns of one BF16 row of hd values
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = sm;                    // NKS stages of [64 keys][HD]
-  uint8_t* sV = sK + NKS * NC * CH64;  // NVS stages of [64 keys][HD]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NVS * NC * CH64);
+  uint8_t* sK = sm;                  // NKT stages of [128 keys][HD]
+  uint8_t* sV = sK + NKT * NC * CH;  // NKT stages of [128 keys][HD]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NKT * NC * CH);
   uint64_t* q_ready = bars;         // Q, dO written to TMEM by the rows
-  uint64_t* kf = bars + 1;          // [NKS]
-  uint64_t* ke = kf + NKS;          // [NKS]
-  uint64_t* vf = ke + NKS;          // [NVS]
-  uint64_t* ve = vf + NVS;          // [NVS]
-  uint64_t* s_full = ve + NVS;      // [2]
-  uint64_t* p_full = s_full + 2;    // [2] dS in TMEM
-  uint64_t* acc_full = p_full + 2;
+  uint64_t* kvf = bars + 1;         // [NKT]
+  uint64_t* kve = kvf + NKT;        // [NKT]
+  uint64_t* s_full = kve + NKT;     // S, dP in TMEM
+  uint64_t* p_full = s_full + 1;    // dS written back
+  uint64_t* acc_full = p_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -830,25 +858,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const int h = (int)(blockIdx.x % per_qb) / n_seq, n = (int)(blockIdx.x % n_seq);
   const int kh = h / (nh / nkv);
   const int q0 = qb * 128;
-  const int nkt = min((S + 63) / 64, 2 * qb + 2);
+  const int nkt = qb + 1;  // key tiles 0 .. qb (the last one holds the diagonal)
   const int row0 = n * S;
   const int64_t T = (int64_t)n_seq * S;
   const int64_t ld = (int64_t)(nh + 2 * nkv) * HD;
 
   if (threadIdx.x == 0) {
     mbar_init(q_ready, 256);
-    for (int i = 0; i < NKS; ++i) {
-      mbar_init(&kf[i], 1);
-      mbar_init(&ke[i], 1);
+    for (int i = 0; i < NKT; ++i) {
+      mbar_init(&kvf[i], 1);
+      mbar_init(&kve[i], 1);
     }
-    for (int i = 0; i < NVS; ++i) {
-      mbar_init(&vf[i], 1);
-      mbar_init(&ve[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 256);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 256);
     mbar_init(acc_full, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -863,33 +885,29 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tQ = tmem, tdO = tmem + QC, tSP = tmem + 2 * QC, tdQ = tmem + 2 * QC + 256;
-  uint32_t k_inflight = 0, k_par = 0, v_inflight = 0, v_par = 0;
+  const uint32_t tQ = tmem, tdO = tmem + QC, tS = tmem + 2 * QC, tP = tS + 128, tdQ = tS + 256;
+  uint32_t kv_inflight = 0, kv_par = 0;
 
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
       for (int j = 0; j < nkt && ok; ++j) {
-        const int st = j % NKS, sv = j % NVS;
-        const uint32_t u = (uint32_t)(j / NKS), uv = (uint32_t)(j / NVS);
-        if (!mbar_wait(&ke[st], (u & 1) ^ 1, abort_flag)) {
+        const int st = j % NKT;
+        const uint32_t u = (uint32_t)(j / NKT);
+        if (!mbar_wait(&kve[st], (u & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
-        mbar_expect_tx(&kf[st], NC * CH64);
+        mbar_expect_tx(&kvf[st], 2 * NC * CH);
         for (int c = 0; c < NC; ++c)
-          tma_load(&tq, &kf[st], sK + (st * NC + c) * CH64, (nh + kh) * HD + 64 * c, row0 + 64 * j);
-        k_inflight |= 1u << st;
-        k_par = (k_par & ~(1u << st)) | ((u & 1) << st);
-        if (!mbar_wait(&ve[sv], (uv & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        mbar_expect_tx(&vf[sv], NC * CH64);
-        for (int c = 0; c < NC; ++c)
-          tma_load(&tq, &vf[sv], sV + (sv * NC + c) * CH64, (nh + nkv + kh) * HD + 64 * c, row0 + 64 * j);
-        v_inflight |= 1u << sv;
-        v_par = (v_par & ~(1u << sv)) | ((uv & 1) << sv);
+          for (int hf = 0; hf < 2; ++hf) {
+            tma_load(&tq, &kvf[st], sK + (st * NC + c) * CH + hf * CH64, (nh + kh) * HD + 64 * c,
+                     row0 + 128 * j + 64 * hf);
+            tma_load(&tq, &kvf[st], sV + (st * NC + c) * CH + hf * CH64, (nh + nkv + kh) * HD + 64 * c,
+                     row0 + 128 * j + 64 * hf);
+          }
+        kv_inflight |= 1u << st;
+        kv_par = (kv_par & ~(1u << st)) | ((u & 1) << st);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -899,52 +917,39 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       bool ok = mbar_wait(q_ready, 0, abort_flag);
-      constexpr uint32_t I_S = idesc(128, 64, false, false);  // S, dP: A (Q, dO) in TMEM, B K-major over hd
-      constexpr uint32_t I_G = idesc(128, HD, false, true);   // dQ: A (dS) in TMEM, B = K_j as MN-major
+      constexpr uint32_t I_S = idesc(128, 128, false, false);  // S, dP: A (Q, dO) in TMEM, B K-major over hd
+      constexpr uint32_t I_G = idesc(128, HD, false, true);    // dQ: A (dS) in TMEM, B = K as MN-major
       const uint64_t dK = sdesc(su32(sK), 16, 1024), dV = sdesc(su32(sV), 16, 1024);
-      const uint64_t dKm = sdesc(su32(sK), CH64, 1024);
+      const uint64_t dKm = sdesc(su32(sK), CH, 1024);
       auto issue_s = [&](int j) -> bool {
-        const int sk = j % NKS, sv = j % NVS, b = j & 1;
-        if (!mbar_wait(&kf[sk], (uint32_t)((j / NKS) & 1), abort_flag) ||
-            !mbar_wait(&vf[sv], (uint32_t)((j / NVS) & 1), abort_flag))
-          return false;
+        const int st = j % NKT;
+        if (!mbar_wait(&kvf[st], (uint32_t)((j / NKT) & 1), abort_flag)) return false;
         tc_fence_after();
-        const uint32_t tS = tSP + 128 * b, tP = tS + 64;
-        const uint64_t kd = dadv(dK, sk * NC * CH64), vd = dadv(dV, sv * NC * CH64);
+        const uint64_t kd = dadv(dK, st * NC * CH), vd = dadv(dV, st * NC * CH);
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
-          const uint32_t ob = (ks >> 2) * CH64 + (ks & 3) * 32;
+          const uint32_t ob = (ks >> 2) * CH + (ks & 3) * 32;
           tc_mma_ts(tS, tQ + 8 * ks, dadv(kd, ob), I_S, ks != 0);
           tc_mma_ts(tP, tdO + 8 * ks, dadv(vd, ob), I_S, ks != 0);
         }
-        tc_commit(&s_full[b]);
-        tc_commit(&ve[sv]);  // V_j is read by dP only
+        tc_commit(s_full);
         return true;
       };
       auto issue_g = [&](int j) -> bool {
-        const int sk = j % NKS, b = j & 1;
-        if (!mbar_wait(&p_full[b], (uint32_t)((j >> 1) & 1), abort_flag)) return false;
+        const int st = j % NKT;
+        if (!mbar_wait(p_full, (uint32_t)(j & 1), abort_flag)) return false;
         tc_fence_after();
-        const uint32_t tS = tSP + 128 * b;
-        const uint64_t km = dadv(dKm, sk * NC * CH64);
+        const uint64_t km = dadv(dKm, st * NC * CH);
         const uint32_t acc0 = j > 0 ? 1u : 0u;
-        // dS of keys 0..31 sits in S columns 0..15, keys 32..63 in columns 32..47
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc_mma_ts(tdQ, tS + (kk >> 1) * 32 + (kk & 1) * 8, dadv(km, kk * 16 * 128), I_G, kk > 0 ? 1u : acc0);
-        tc_commit(&ke[sk]);
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_ts(tdQ, tS + pcol(kk), dadv(km, kk * 2048), I_G, kk > 0 ? 1u : acc0);
+        tc_commit(&kve[st]);
         return true;
       };
-      // S of sub-tile j + 1 goes to the TMEM buffer of sub-tile j - 1, whose
-      // S / dP the rows have read (p_full waited for in issue_g(j - 1)) and
-      // whose dS the dQ MMAs of j - 1, issued before, read first.
       if (ok) ok = issue_s(0);
       for (int j = 0; j < nkt && ok; ++j) {
-        if (j + 1 < nkt && !issue_s(j + 1)) {
-          ok = false;
-          break;
-        }
-        if (!issue_g(j)) {
+        if (!issue_g(j) || (j + 1 < nkt && !issue_s(j + 1))) {
           ok = false;
           break;
         }
@@ -956,9 +961,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
     }
   } else {
-    // Row warps 2..9: query rows by TMEM lane quarter; warps 2..5 own key
-    // columns 0..31 of a sub-tile (and the first half of Q, dO, dQ's hd
-    // columns), warps 6..9 key columns 32..63 (and the second half).
+    // Row warps 2..9: query rows by TMEM lane quarter; warps 2..5 own keys
+    // 0..63 of a tile (and the first half of Q, dO, dQ's hd columns), warps
+    // 6..9 keys 64..127 (and the second half).
     const int qw = warp & 3, half = (warp - 2) >> 2;
     const int r = qw * 32 + lane;  // query row
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
@@ -994,40 +999,43 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
     bool ok = true;
     for (int j = 0; j < nkt; ++j) {
-      const int b = j & 1;
-      const uint32_t u = (uint32_t)(j >> 1);
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], u & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full, (uint32_t)(j & 1), abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int k0 = 64 * j + 32 * half;  // first key of this thread's 32 columns
-      const bool need_mask = (k0 + 31 > q0) || (k0 + 32 > S);
-      const uint32_t tS = tSP + 128 * b + half * 32, tP = tS + 64;
-      uint32_t sv[32], dp[32];
-      tmem_ld32_nw(tS + lane_off, sv);
-      tmem_ld32_nw(tP + lane_off, dp);
-      tmem_wait_ld2(sv, dp);
-      uint32_t dw[16];
+      const int k0 = 128 * j + 64 * half;  // first key of this thread's 64 columns
+      const bool need_mask = (k0 + 63 > q0) || (k0 + 64 > S);
+      uint32_t sv[2][32], dp[2][32];
+      tmem_ld32_nw(tS + lane_off + half * 64, sv[0]);
+      tmem_ld32_nw(tP + lane_off + half * 64, dp[0]);
+      tmem_ld32_nw(tS + lane_off + half * 64 + 32, sv[1]);
+      tmem_ld32_nw(tP + lane_off + half * 64 + 32, dp[1]);
+      tmem_wait_ld4(sv[0], dp[0], sv[1], dp[1]);
+      // dS (BF16 pairs) goes back over the first 32 of the S columns this
+      // thread read, 16 columns per half of its 64 keys
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        float dv[2];
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dw[16];
 #pragma unroll
-        for (int tt = 0; tt < 2; ++tt) {
-          float p = ex2(__uint_as_float(sv[e + tt]) * scale_log2 - lse2);
-          if (need_mask) {
-            const int key = k0 + e + tt;
-            if (key > q || key >= S) p = 0.f;
+        for (int e = 0; e < 32; e += 2) {
+          float dv[2];
+#pragma unroll
+          for (int tt = 0; tt < 2; ++tt) {
+            float p = ex2(__uint_as_float(sv[c][e + tt]) * scale_log2 - lse2);
+            if (need_mask) {
+              const int key = k0 + c * 32 + e + tt;
+              if (key > q || key >= S) p = 0.f;
+            }
+            dv[tt] = p * (__uint_as_float(dp[c][e + tt]) - dl);
           }
-          dv[tt] = p * (__uint_as_float(dp[e + tt]) - dl);
+          dw[e / 2] = pack2(dv[0], dv[1]);
         }
-        dw[e / 2] = pack2(dv[0], dv[1]);
+        tmem_st16(tS + lane_off + half * 64 + c * 16, dw);
       }
-      // dS (BF16 pairs) over the first 16 of the S columns this thread just read
-      tmem_st16(tS + lane_off, dw);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[b]);
+      mbar_arrive(p_full);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
     if (ok) {
@@ -1053,13 +1061,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 
   if (warp == 0 && lane == 0 && *abort_flag) {
     const long long t0 = clock64();
-    for (int s2 = 0; s2 < NKS; ++s2)
-      if (k_inflight & (1u << s2))
-        while (!mbar_test(&kf[s2], (k_par >> s2) & 1) && clock64() - t0 < kWaitCycles) {
-        }
-    for (int s2 = 0; s2 < NVS; ++s2)
-      if (v_inflight & (1u << s2))
-        while (!mbar_test(&vf[s2], (v_par >> s2) & 1) && clock64() - t0 < kWaitCycles) {
+    for (int s2 = 0; s2 < NKT; ++s2)
+      if (kv_inflight & (1u << s2))
+        while (!mbar_test(&kvf[s2], (kv_par >> s2) & 1) && clock64() - t0 < kWaitCycles) {
         }
   }
   tc_fence_before();
@@ -1138,7 +1142,7 @@ cudaError_t launch_bwd(const bf16* qkv, const bf16* dout, const float* lse, cons
   const int64_t nqb = (S + 127) / 128;
   const int64_t gkv = nqb * nkv * n_seq, gq = nqb * nh * n_seq;
   if (gkv > 0x7fffffff || gq > 0x7fffffff) return cudaErrorInvalidValue;
-  attn_bwd_kv_k<HD><<<(unsigned)gkv, THREADS, SKV, s>>>(mq, mo, S, n_seq, nh, nkv, lse, delta, scale,
+  attn_bwd_kv_k<HD><<<(unsigned)gkv, BWD_THREADS, SKV, s>>>(mq, mo, S, n_seq, nh, nkv, lse, delta, scale,
                                                          scale * 1.4426950408889634f, dqkv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
