@@ -492,9 +492,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 // attn_bwd_q_k: one CTA per (128 queries, query head, sequence), longest work
 // first, looping over 128-key tiles up to the diagonal.  Q and dO are written
 // into TMEM once by the row warps and are the A operands of S = Q K^T and
-// dP = dO V^T; the rows write dS over S; dQ += dS K reads dS from TMEM and K
-// (MN-major) from shared memory; dQ scale leaves as BF16.  TMEM: Q | dO | S |
-// dP | dQ.  Every wait is bounded.
+// dP = dO V^T; the rows form P as soon as S lands (S's columns then take the
+// next tile's S), then dS = P (dP - delta) written over dP; dQ += dS K reads
+// dS from TMEM and K (MN-major) from shared memory; dQ scale leaves as BF16.
+// TMEM: Q | dO | S | dP | dQ.  Every wait is bounded.
 constexpr int CH64 = 8192;  // one 64-column chunk of a 64-row box (64 rows x 128 B)
 constexpr int NQT = 2;      // Q / dO tile stages of the dK/dV kernel
 constexpr int NKT = 3;      // K / V tile stages of the dQ kernel
@@ -845,8 +846,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint64_t* q_ready = bars;         // Q, dO written to TMEM by the rows
   uint64_t* kvf = bars + 1;         // [NKT]
   uint64_t* kve = kvf + NKT;        // [NKT]
-  uint64_t* s_full = kve + NKT;     // S, dP in TMEM
-  uint64_t* p_full = s_full + 1;    // dS written back
+  uint64_t* s1_full = kve + NKT;    // S in TMEM
+  uint64_t* s2_full = s1_full + 1;  // dP in TMEM
+  uint64_t* ps_free = s2_full + 1;  // the rows have read S
+  uint64_t* p_full = ps_free + 1;   // dS written back over dP
   uint64_t* acc_full = p_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -869,7 +872,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_init(&kvf[i], 1);
       mbar_init(&kve[i], 1);
     }
-    mbar_init(s_full, 1);
+    mbar_init(s1_full, 1);
+    mbar_init(s2_full, 1);
+    mbar_init(ps_free, 256);
     mbar_init(p_full, 256);
     mbar_init(acc_full, 1);
     *abort_flag = 0;
@@ -921,21 +926,28 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       constexpr uint32_t I_G = idesc(128, HD, false, true);    // dQ: A (dS) in TMEM, B = K as MN-major
       const uint64_t dK = sdesc(su32(sK), 16, 1024), dV = sdesc(su32(sV), 16, 1024);
       const uint64_t dKm = sdesc(su32(sK), CH, 1024);
-      auto issue_s = [&](int j) -> bool {
+      // Per tile j: S(j+1) as soon as the rows have read S(j); then dQ(j),
+      // which reads dS(j) from the dP columns, then dP(j+1) over them.
+      auto issue_s = [&](int j) -> bool {  // S = Q K^T
         const int st = j % NKT;
         if (!mbar_wait(&kvf[st], (uint32_t)((j / NKT) & 1), abort_flag)) return false;
+        if (j > 0 && !mbar_wait(ps_free, (uint32_t)((j - 1) & 1), abort_flag)) return false;
         tc_fence_after();
-        const uint64_t kd = dadv(dK, st * NC * CH), vd = dadv(dV, st * NC * CH);
+        const uint64_t kd = dadv(dK, st * NC * CH);
 #pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
-          const uint32_t ob = (ks >> 2) * CH + (ks & 3) * 32;
-          tc_mma_ts(tS, tQ + 8 * ks, dadv(kd, ob), I_S, ks != 0);
-          tc_mma_ts(tP, tdO + 8 * ks, dadv(vd, ob), I_S, ks != 0);
-        }
-        tc_commit(s_full);
+        for (int ks = 0; ks < HD / 16; ++ks)
+          tc_mma_ts(tS, tQ + 8 * ks, dadv(kd, (ks >> 2) * CH + (ks & 3) * 32), I_S, ks != 0);
+        tc_commit(s1_full);
         return true;
       };
-      auto issue_g = [&](int j) -> bool {
+      auto issue_dp = [&](int j) {  // dP = dO V^T (its K / V stage was waited for by issue_s)
+        const uint64_t vd = dadv(dV, (j % NKT) * NC * CH);
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks)
+          tc_mma_ts(tP, tdO + 8 * ks, dadv(vd, (ks >> 2) * CH + (ks & 3) * 32), I_S, ks != 0);
+        tc_commit(s2_full);
+      };
+      auto issue_g = [&](int j) -> bool {  // dQ += dS K; the K / V stage is then free
         const int st = j % NKT;
         if (!mbar_wait(p_full, (uint32_t)(j & 1), abort_flag)) return false;
         tc_fence_after();
@@ -943,16 +955,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_ts(tdQ, tS + pcol(kk), dadv(km, kk * 2048), I_G, kk > 0 ? 1u : acc0);
+          tc_mma_ts(tdQ, tP + pcol(kk), dadv(km, kk * 2048), I_G, kk > 0 ? 1u : acc0);
         tc_commit(&kve[st]);
         return true;
       };
       if (ok) ok = issue_s(0);
+      if (ok) issue_dp(0);
       for (int j = 0; j < nkt && ok; ++j) {
-        if (!issue_g(j) || (j + 1 < nkt && !issue_s(j + 1))) {
+        const bool more = j + 1 < nkt;
+        if ((more && !issue_s(j + 1)) || !issue_g(j)) {
           ok = false;
           break;
         }
+        if (more) issue_dp(j + 1);
       }
       if (ok) tc_commit(acc_full);
       if (!ok) {
@@ -999,43 +1014,53 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
     bool ok = true;
     for (int j = 0; j < nkt; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full, (uint32_t)(j & 1), abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(s1_full, (uint32_t)(j & 1), abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
       const int k0 = 128 * j + 64 * half;  // first key of this thread's 64 columns
       const bool need_mask = (k0 + 63 > q0) || (k0 + 64 > S);
-      uint32_t sv[2][32], dp[2][32];
-      tmem_ld32_nw(tS + lane_off + half * 64, sv[0]);
-      tmem_ld32_nw(tP + lane_off + half * 64, dp[0]);
-      tmem_ld32_nw(tS + lane_off + half * 64 + 32, sv[1]);
-      tmem_ld32_nw(tP + lane_off + half * 64 + 32, dp[1]);
-      tmem_wait_ld4(sv[0], dp[0], sv[1], dp[1]);
-      // dS (BF16 pairs) goes back over the first 32 of the S columns this
-      // thread read, 16 columns per half of its 64 keys
+      // phase 1: P from S; then S's columns are free for the next tile
+      float p[64];
+      {
+        uint32_t sv[2][32];
+        tmem_ld32_nw(tS + lane_off + half * 64, sv[0]);
+        tmem_ld32_nw(tS + lane_off + half * 64 + 32, sv[1]);
+        tmem_wait_ld2(sv[0], sv[1]);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t dw[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float dv[2];
-#pragma unroll
-          for (int tt = 0; tt < 2; ++tt) {
-            float p = ex2(__uint_as_float(sv[c][e + tt]) * scale_log2 - lse2);
-            if (need_mask) {
-              const int key = k0 + c * 32 + e + tt;
-              if (key > q || key >= S) p = 0.f;
-            }
-            dv[tt] = p * (__uint_as_float(dp[c][e + tt]) - dl);
+        for (int e = 0; e < 64; ++e) {
+          float pe = ex2(__uint_as_float(sv[e >> 5][e & 31]) * scale_log2 - lse2);
+          if (need_mask) {
+            const int key = k0 + e;
+            if (key > q || key >= S) pe = 0.f;
           }
-          dw[e / 2] = pack2(dv[0], dv[1]);
+          p[e] = pe;
         }
-        tmem_st16(tS + lane_off + half * 64 + c * 16, dw);
+        tc_fence_before();
+        mbar_arrive(ps_free);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_full);
+      // phase 2: dS = P (dP - delta), back over the first 32 dP columns this thread read
+      if (!__all_sync(0xffffffffu, mbar_wait(s2_full, (uint32_t)(j & 1), abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        uint32_t dp[2][32];
+        tmem_ld32_nw(tP + lane_off + half * 64, dp[0]);
+        tmem_ld32_nw(tP + lane_off + half * 64 + 32, dp[1]);
+        tmem_wait_ld2(dp[0], dp[1]);
+        uint32_t dw[32];
+#pragma unroll
+        for (int e = 0; e < 64; e += 2)
+          dw[e / 2] = pack2(p[e] * (__uint_as_float(dp[e >> 5][e & 31]) - dl),
+                            p[e + 1] * (__uint_as_float(dp[(e + 1) >> 5][(e + 1) & 31]) - dl));
+        tmem_st32u(tP + lane_off + half * 64, dw);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full);
+      }
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
     if (ok) {
