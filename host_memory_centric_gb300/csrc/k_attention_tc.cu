@@ -1,22 +1,29 @@
 // k_attention_tc.cu -- causal GQA attention, forward and backward, on the
 // 5th-generation tensor cores (sm_103a): tcgen05.mma with TMEM accumulators,
-// TMA tiles, 192 threads per CTA (a TMA warp, an MMA warp, 4 row warps).
+// TMA tiles, 320 threads per CTA (a TMA warp, an MMA warp, 8 row warps, two
+// per TMEM lane quarter).
 //
 // Forward: one CTA per (128 queries, query head, sequence):
 //   warp 0      TMA producer: the Q tile once, then K and V tiles of 128 keys
 //               into a 2-stage ring (128-byte swizzle);
-//   warp 1      allocates TMEM (S0 | S1 | O) and, from one thread, issues
-//               S_j = Q K_j^T (M=128, N=128) into S[j % 2] and, once the
-//               softmax has produced P_{j-1}, O += P_{j-1} V_{j-1} (M=128,
-//               N=hd, V as an MN-major operand);
-//   warps 2..5  softmax, one thread per query row: read S_j from TMEM, causal
-//               mask, online max / sum in the exp2 domain, rescale the row of O
-//               in TMEM when its max grows, write P_j as BF16 into the
-//               128B-swizzled K-major layout the next MMA reads; at the end
-//               O / l to global memory and LSE = (m + log2 l) ln 2.
-// The double-buffered S lets S_{j+1} run on the tensor core while the
-// softmax works on S_j.  Every mbarrier wait is bounded; an expired wait sets
-// the kernel error word and the CTA stops, drains its copies and frees TMEM.
+//   warp 1      allocates TMEM (S0 | S1 | O_0 | O_1) and, from one thread,
+//               issues S_j = Q K_j^T (M=128, N=128) into S[j % 2] and, once the
+//               softmax has produced P_{j-1}, O_0 += P V over the tile's keys
+//               0..63 and O_1 += P V over keys 64..127 (V as an MN-major
+//               operand);
+//   warps 2..9  softmax: warp w owns the query rows of TMEM lane quarter w % 4
+//               and one half of every key tile (warps 2..5 keys 0..63, 6..9
+//               keys 64..127), with its own online max / sum in the exp2
+//               domain and its own accumulator O_half, rescaled in TMEM when
+//               its max grows; P goes to the 128B-swizzled K-major tile the
+//               next MMA reads.  At the end the two halves of a row merge
+//               (m = max, each side scaled by 2^(m_h - m)) and O / l and
+//               LSE = (m + log2 l) ln 2 go to global memory.
+// Splitting every row over two threads halves the per-thread softmax work per
+// tile without any per-tile exchange between them.  The double-buffered S
+// lets S_{j+1} run on the tensor core while the softmax works on S_j.  Every
+// mbarrier wait is bounded; an expired wait sets the kernel error word and the
+// CTA stops, drains its copies and frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -27,8 +34,10 @@
 namespace mt {
 namespace {
 
-constexpr int THREADS = 192;      // forward: TMA warp, MMA warp, 4 softmax warps
-constexpr int BWD_THREADS = 320;  // backward: TMA warp, MMA warp, 8 row warps (two per TMEM lane quarter)
+// TMA warp, MMA warp, 8 row warps (two per TMEM lane quarter)
+constexpr int ATTN_THREADS = 320;
+constexpr int NFK = 3;  // forward: K tile stages
+constexpr int NFV = 2;  // forward: V tile stages
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr int CH = 16384;  // one 64-column chunk of a 128-row tile (128 rows x 128 B)
 
@@ -197,25 +206,30 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 __device__ int g_attn_error = 0;
 
 template <int HD>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(ATTN_THREADS, 1)
     attn_fwd_tc_k(const __grid_constant__ CUtensorMap tm, int S, int nh, int nkv, bf16* __restrict__ o,
                   float* __restrict__ lse, float scale_log2) {
   constexpr int NC = HD / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = sm;
-  uint8_t* sK = sQ + NC * CH;       // 2 stages
-  uint8_t* sV = sK + 2 * NC * CH;   // 2 stages
-  uint8_t* sP = sV + 2 * NC * CH;   // 2 key chunks
+  uint8_t* sK = sQ + NC * CH;        // NFK stages: K is free once S has been computed
+  uint8_t* sV = sK + NFK * NC * CH;  // NFV stages: V is held until O += P V
+  uint8_t* sP = sV + NFV * NC * CH;  // 2 key chunks: half h of the rows' keys in chunk h
+  // after the last O += P V the P tile holds the merge values [2 halves][(m, l)][128 rows]
+  float* fin = reinterpret_cast<float*>(sP);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * CH);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = bars + 3;
-  uint64_t* s_full = bars + 5;
-  uint64_t* s_empty = bars + 7;
-  uint64_t* p_full = bars + 9;
-  uint64_t* o_done = bars + 10;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* k_full = bars + 1;          // [NFK]
+  uint64_t* k_empty = k_full + NFK;     // [NFK]
+  uint64_t* v_full = k_empty + NFK;     // [NFV]
+  uint64_t* v_empty = v_full + NFV;     // [NFV]
+  uint64_t* s_full = v_empty + NFV;     // [2]
+  uint64_t* s_empty = s_full + 2;       // [2]
+  uint64_t* p_full = s_empty + 2;
+  uint64_t* o_done = p_full + 1;
+  uint64_t* fin_ready = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin_ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -229,14 +243,21 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 128);
+    for (int i = 0; i < NFK; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
     }
-    mbar_init(p_full, 128);
+    for (int i = 0; i < NFV; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 256);
+    }
+    mbar_init(p_full, 256);
     mbar_init(o_done, 1);
+    mbar_init(fin_ready, 256);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm) : "memory");
@@ -251,30 +272,37 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO = tmem + 256;
-  uint32_t kv_inflight = 0, kv_par = 0;  // producer drain bookkeeping
+  const uint32_t tO[2] = {tmem + 256, tmem + 256 + HD};  // O of key halves 0 and 1
+  uint32_t x_inflight = 0, x_par = 0;  // producer drain bookkeeping (lane 0: K stages, lane 1: V stages)
   bool q_inflight = false;
 
   if (warp == 0) {
-    if (lane == 0) {
+    // lane 0 streams Q and the K ring, lane 1 the V ring, each on its own
+    // barriers, so a V stage still held by O += P V never delays K
+    if (lane < 2) {
+      const bool is_k = lane == 0;
+      const int ns = is_k ? NFK : NFV;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      uint8_t* base = is_k ? sK : sV;
+      const int col = (is_k ? nh + kh : nh + nkv + kh) * HD;
       bool ok = true;
-      mbar_expect_tx(q_full, NC * CH);
-      for (int c = 0; c < NC; ++c) tma_load(&tm, q_full, sQ + c * CH, h * HD + 64 * c, row0 + q0);
-      q_inflight = true;
+      if (is_k) {
+        mbar_expect_tx(q_full, NC * CH);
+        for (int c = 0; c < NC; ++c) tma_load(&tm, q_full, sQ + c * CH, h * HD + 64 * c, row0 + q0);
+        q_inflight = true;
+      }
       for (int j = 0; j < ntiles && ok; ++j) {
-        const int s = j & 1;
-        const uint32_t u = (uint32_t)(j >> 1);
-        if (!mbar_wait(&kv_empty[s], (u & 1) ^ 1, abort_flag)) {
+        const int s = j % ns;
+        const uint32_t u = (uint32_t)(j / ns);
+        if (!mbar_wait(&empty[s], (u & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
-        mbar_expect_tx(&kv_full[s], 2 * NC * CH);
-        for (int c = 0; c < NC; ++c) {
-          tma_load(&tm, &kv_full[s], sK + (s * NC + c) * CH, (nh + kh) * HD + 64 * c, row0 + 128 * j);
-          tma_load(&tm, &kv_full[s], sV + (s * NC + c) * CH, (nh + nkv + kh) * HD + 64 * c, row0 + 128 * j);
-        }
-        kv_inflight |= 1u << s;
-        kv_par = (kv_par & ~(1u << s)) | ((u & 1) << s);
+        mbar_expect_tx(&full[s], NC * CH);
+        for (int c = 0; c < NC; ++c) tma_load(&tm, &full[s], base + (s * NC + c) * CH, col + 64 * c, row0 + 128 * j);
+        x_inflight |= 1u << s;
+        x_par = (x_par & ~(1u << s)) | ((u & 1) << s);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -288,23 +316,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t IO = idesc(128, HD, false, true);
       const uint64_t dP = sdesc(su32(sP), 16, 1024), dV = sdesc(su32(sV), CH, 1024);
       const uint64_t dQ = sdesc(su32(sQ), 16, 1024), dK = sdesc(su32(sK), 16, 1024);
+      // O_0 += P[:, 0:64] V[0:64, :] and O_1 += P[:, 64:128] V[64:128, :]
       auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(p_full, (uint32_t)(i & 1), abort_flag)) return false;
+        if (!mbar_wait(p_full, (uint32_t)(i & 1), abort_flag) ||
+            !mbar_wait(&v_full[i % NFV], (uint32_t)((i / NFV) & 1), abort_flag))
+          return false;
         tc_fence_after();
-        const int s = i & 1;
-        const uint64_t v = dadv(dV, s * NC * CH);
+        const uint64_t v = dadv(dV, (i % NFV) * NC * CH);
         const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma(tO, dadv(dP, (kk >> 2) * CH + (kk & 3) * 32), dadv(v, kk * 16 * 128), IO, kk > 0 ? 1u : acc0);
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t acc = kk > 0 ? 1u : acc0;
+          tc_mma(tO[0], dadv(dP, kk * 32), dadv(v, kk * 16 * 128), IO, acc);
+          tc_mma(tO[1], dadv(dP, CH + kk * 32), dadv(v, (4 + kk) * 16 * 128), IO, acc);
+        }
         tc_commit(o_done);
-        tc_commit(&kv_empty[s]);
+        tc_commit(&v_empty[i % NFV]);
         return true;
       };
       for (int j = 0; j < ntiles && ok; ++j) {
-        const int s = j & 1, b = j & 1;
+        const int s = j % NFK, b = j & 1;
         const uint32_t u = (uint32_t)(j >> 1);
-        if (!mbar_wait(&kv_full[s], u & 1, abort_flag) || !mbar_wait(&s_empty[b], (u & 1) ^ 1, abort_flag)) {
+        if (!mbar_wait(&k_full[s], (uint32_t)((j / NFK) & 1), abort_flag) ||
+            !mbar_wait(&s_empty[b], (u & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -317,6 +351,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int k = 0; k < 4; ++k)
             tc_mma(ts, dadv(dQ, c * CH + k * 32), dadv(kd, c * CH + k * 32), IS, (c | k) != 0);
         tc_commit(&s_full[b]);
+        tc_commit(&k_empty[s]);  // K_j is read by S_j only
         if (j >= 1 && !issue_pv(j - 1)) {
           ok = false;
           break;
@@ -329,15 +364,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else {
-    // softmax: this thread owns query row r of the tile; the warp may touch
-    // TMEM lanes 32*(warp%4) .. +31
-    const int qw = warp & 3;
+    // Softmax warps 2..9: this thread owns query row r (TMEM lane quarter
+    // warp % 4) for keys 64 half .. 64 half + 63 of every key tile, with its
+    // own running max m, sum l and accumulator O_half; the two halves of a
+    // row merge once at the end.
+    const int qw = warp & 3, half = (warp - 2) >> 2;
     const int r = qw * 32 + lane;
     const int qpos = q0 + r;  // position inside the sequence
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
     float m_old = -INFINITY, l = 0.f;
     bool ok = true;
-    uint8_t* prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
+    uint8_t* prow = sP + half * CH + (r >> 3) * 1024 + (r & 7) * 128;
     for (int j = 0; j < ntiles; ++j) {
       const int b = j & 1;
       const uint32_t u = (uint32_t)(j >> 1);
@@ -347,44 +384,41 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float t[32];
-        tmem_ld32(tS[b] + lane_off + c * 32, t);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = t[i];
-      }
+      uint32_t sr[2][32];
+      tmem_ld32_nw(tS[b] + lane_off + half * 64, sr[0]);
+      tmem_ld32_nw(tS[b] + lane_off + half * 64 + 32, sr[1]);
+      tmem_wait_ld2(sr[0], sr[1]);
       tc_fence_before();
       mbar_arrive(&s_empty[b]);
-      const int kbase = 128 * j;
+      float sv[64];
+      const int kbase = 128 * j + 64 * half;
       // only the diagonal tile and a tile crossing the sequence end need masking
-      const bool need_mask = (kbase + 127 > q0) || (kbase + 128 > S);
+      const bool need_mask = (kbase + 63 > q0) || (kbase + 64 > S);
       if (need_mask) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
+        for (int i = 0; i < 64; ++i) {
           const int key = kbase + i;
-          s[i] = (key > qpos || key >= S) ? -INFINITY : s[i] * scale_log2;
+          sv[i] = (key > qpos || key >= S) ? -INFINITY : __uint_as_float(sr[i >> 5][i & 31]) * scale_log2;
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] *= scale_log2;
+        for (int i = 0; i < 64; ++i) sv[i] = __uint_as_float(sr[i >> 5][i & 31]) * scale_log2;
       }
-      // eight independent chains instead of one 128-long dependency chain
+      // eight independent chains instead of one 64-long dependency chain
       float mx8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = m_old;
 #pragma unroll
-      for (int i = 0; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], s[i]);
+      for (int i = 0; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float base = mx == -INFINITY ? 0.f : mx;
-      const float alpha = exp2f(m_old - base);  // 0 when m_old = -inf
+      const float alpha = ex2(m_old - base);  // 0 when m_old = -inf
       float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        s[i] = exp2f(s[i] - base);
-        sum8[i & 7] += s[i];
+      for (int i = 0; i < 64; ++i) {
+        sv[i] = ex2(sv[i] - base);
+        sum8[i & 7] += sv[i];
       }
       const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       l = l * alpha + sum;
@@ -399,63 +433,80 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int c = 0; c < HD / 32; ++c) {
             float t[32];
-            tmem_ld32(tO + lane_off + c * 32, t);
+            tmem_ld32(tO[half] + lane_off + c * 32, t);
 #pragma unroll
             for (int i = 0; i < 32; ++i) t[i] *= alpha;
-            tmem_st32(tO + lane_off + c * 32, t);
+            tmem_st32(tO[half] + lane_off + c * 32, t);
           }
         }
       }
       m_old = mx;
-      // P row into the 128B-swizzled K-major tile: 16-byte unit u of key chunk kc
-      // of row r sits at unit (u ^ (r % 8)) of the row
+      // P row half into the 128B-swizzled K-major tile: 16-byte unit u of
+      // row r sits at unit (u ^ (r % 8)) of the row
 #pragma unroll
-      for (int kc = 0; kc < 2; ++kc)
-#pragma unroll
-        for (int uu = 0; uu < 8; ++uu) {
-          const float* p = s + kc * 64 + uu * 8;
-          const uint4 v = make_uint4(pack2(p[0], p[1]), pack2(p[2], p[3]), pack2(p[4], p[5]), pack2(p[6], p[7]));
-          *reinterpret_cast<uint4*>(prow + kc * CH + ((uu ^ (r & 7)) << 4)) = v;
-        }
+      for (int uu = 0; uu < 8; ++uu) {
+        const float* p = sv + uu * 8;
+        const uint4 v = make_uint4(pack2(p[0], p[1]), pack2(p[2], p[3]), pack2(p[4], p[5]), pack2(p[6], p[7]));
+        *reinterpret_cast<uint4*>(prow + ((uu ^ (r & 7)) << 4)) = v;
+      }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       mbar_arrive(p_full);
     }
+    // merge the two halves of the row: m = max(m_0, m_1), c_h = 2^(m_h - m),
+    // l = l_0 c_0 + l_1 c_1, O = (O_0 c_0 + O_1 c_1) / l; each half writes
+    // half of the hd columns
+    // the last O += P V has read the P tile before it is reused for the merge
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)((ntiles - 1) & 1), abort_flag));
     if (ok) {
+      fin[(half * 2) * 128 + r] = m_old;
+      fin[(half * 2 + 1) * 128 + r] = l;
+      mbar_arrive(fin_ready);
+      ok = __all_sync(0xffffffffu, mbar_wait(fin_ready, 0, abort_flag));
+    }
+    if (ok) {
       tc_fence_after();
-      const float inv = 1.f / l;
+      const float m0 = fin[r], l0 = fin[128 + r], m1 = fin[256 + r], l1 = fin[384 + r];
+      float m = fmaxf(m0, m1);
+      if (m == -INFINITY) m = 0.f;  // a row past the sequence end: nothing is stored
+      const float c0 = ex2(m0 - m), c1 = ex2(m1 - m);
+      const float lt = l0 * c0 + l1 * c1;
+      const float inv = 1.f / lt;
+      const float f0 = c0 * inv, f1 = c1 * inv;
       const bool valid = qpos < S;
-      bf16* orow = o + ((int64_t)row0 + qpos) * ((int64_t)nh * HD) + (int64_t)h * HD;
+      bf16* orow = o + ((int64_t)row0 + qpos) * ((int64_t)nh * HD) + (int64_t)h * HD + half * (HD / 2);
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        float t[32];
-        tmem_ld32(tO + lane_off + c * 32, t);
+      for (int c = 0; c < HD / 64; ++c) {
+        float a0[32], a1[32];
+        tmem_ld32(tO[0] + lane_off + half * (HD / 2) + c * 32, a0);
+        tmem_ld32(tO[1] + lane_off + half * (HD / 2) + c * 32, a1);
         if (valid) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
+          for (int i = 0; i < 4; ++i) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = a0[8 * i + e] * f0 + a1[8 * i + e] * f1;
             reinterpret_cast<uint4*>(orow + c * 32)[i] =
-                make_uint4(pack2(t[8 * i] * inv, t[8 * i + 1] * inv), pack2(t[8 * i + 2] * inv, t[8 * i + 3] * inv),
-                           pack2(t[8 * i + 4] * inv, t[8 * i + 5] * inv), pack2(t[8 * i + 6] * inv, t[8 * i + 7] * inv));
+                make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+          }
         }
       }
-      if (valid) lse[(int64_t)h * T + row0 + qpos] = (m_old + log2f(l)) * 0.6931471805599453f;
-    } else {
-      if (lane == 0) {
-        *abort_flag = 1;
-        atomicCAS(&g_attn_error, 0, 13);
-      }
+      if (valid && half == 0) lse[(int64_t)h * T + row0 + qpos] = (m + log2f(lt)) * 0.6931471805599453f;
+    } else if (lane == 0) {
+      *abort_flag = 1;
+      atomicCAS(&g_attn_error, 0, 13);
     }
   }
 
-  if (warp == 0 && lane == 0 && *abort_flag) {
+  if (warp == 0 && lane < 2 && *abort_flag) {
     const long long t0 = clock64();
     if (q_inflight)
       while (!mbar_test(q_full, 0) && clock64() - t0 < kWaitCycles) {
       }
-    for (int s2 = 0; s2 < 2; ++s2)
-      if (kv_inflight & (1u << s2))
-        while (!mbar_test(&kv_full[s2], (kv_par >> s2) & 1) && clock64() - t0 < kWaitCycles) {
+    uint64_t* full = lane == 0 ? k_full : v_full;
+    for (int s2 = 0; s2 < (lane == 0 ? NFK : NFV); ++s2)
+      if (x_inflight & (1u << s2))
+        while (!mbar_test(&full[s2], (x_par >> s2) & 1) && clock64() - t0 < kWaitCycles) {
         }
   }
   tc_fence_before();
@@ -465,7 +516,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
   }
 }
-
 
 // ---------------------------------------------------------------------------
 // Backward, as two kernels that share no accumulator (so no atomics and no
@@ -516,7 +566,7 @@ static_assert(q_smem_bytes<128>() <= 232448, "dQ kernel shared memory");
 __device__ __forceinline__ uint32_t pcol(int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); }
 
 template <int HD>
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+__global__ void __launch_bounds__(ATTN_THREADS, 1)
     attn_bwd_kv_k(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo, int S,
                   int n_seq, int nh, int nkv, const float* __restrict__ lse, const float* __restrict__ delta,
                   float scale, float scale_log2, bf16* __restrict__ dqkv) {
@@ -832,7 +882,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 }
 
 template <int HD>
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+__global__ void __launch_bounds__(ATTN_THREADS, 1)
     attn_bwd_q_k(const __grid_constant__ CUtensorMap tq, const bf16* __restrict__ qkv, const bf16* __restrict__ dout,
                  int S, int n_seq, int nh, int nkv, const float* __restrict__ lse, const float* __restrict__ delta,
                  float scale, float scale_log2, bf16* __restrict__ dqkv) {
@@ -1116,7 +1166,7 @@ void init_once() {
 
 template <int HD>
 constexpr int smem_bytes() {
-  return (HD / 64) * 16384 * 5 + 2 * 16384 + 1024 + 256;
+  return (HD / 64) * 16384 * (1 + NFK + NFV) + 2 * 16384 + 1024 + 256;
 }
 
 template <int HD>
@@ -1137,7 +1187,7 @@ cudaError_t launch(const bf16* qkv, int n_seq, int S, int nh, int nkv, bf16* o, 
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   dim3 grid((S + 127) / 128, nh, n_seq);
-  attn_fwd_tc_k<HD><<<grid, THREADS, SM, s>>>(m, S, nh, nkv, o, lse, scale_log2);
+  attn_fwd_tc_k<HD><<<grid, ATTN_THREADS, SM, s>>>(m, S, nh, nkv, o, lse, scale_log2);
   return cudaGetLastError();
 }
 
@@ -1167,11 +1217,11 @@ cudaError_t launch_bwd(const bf16* qkv, const bf16* dout, const float* lse, cons
   const int64_t nqb = (S + 127) / 128;
   const int64_t gkv = nqb * nkv * n_seq, gq = nqb * nh * n_seq;
   if (gkv > 0x7fffffff || gq > 0x7fffffff) return cudaErrorInvalidValue;
-  attn_bwd_kv_k<HD><<<(unsigned)gkv, BWD_THREADS, SKV, s>>>(mq, mo, S, n_seq, nh, nkv, lse, delta, scale,
+  attn_bwd_kv_k<HD><<<(unsigned)gkv, ATTN_THREADS, SKV, s>>>(mq, mo, S, n_seq, nh, nkv, lse, delta, scale,
                                                          scale * 1.4426950408889634f, dqkv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_bwd_q_k<HD><<<(unsigned)gq, BWD_THREADS, SQ, s>>>(mq, qkv, dout, S, n_seq, nh, nkv, lse, delta, scale,
+  attn_bwd_q_k<HD><<<(unsigned)gq, ATTN_THREADS, SQ, s>>>(mq, qkv, dout, S, n_seq, nh, nkv, lse, delta, scale,
                                                           scale * 1.4426950408889634f, dqkv);
   return cudaGetLastError();
 }
