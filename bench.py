@@ -257,6 +257,11 @@ def main():
     ap.add_argument("--ckpt-interval", type=int, default=1, help="layers per recompute segment")
     ap.add_argument("--buffers", type=int, default=2, help="device weight buffers (1: single-buffer ablation)")
     ap.add_argument("--layers", type=int, default=0, help="decoder depth override (depth sweeps; 0 = the config's)")
+    ap.add_argument("--set", action="append", default=[], metavar="KEY=VALUE",
+                    help="override a shape field of the config (e.g. hidden=4096); repeatable")
+    ap.add_argument("--timeout", type=float, default=0,
+                    help="limit of every bounded host wait, seconds (0: four times the step's tensor work at "
+                         "400 TFLOP/s, at least 60 s)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -283,7 +288,11 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    c = configs.get(args.config, **({"n_layers": args.layers} if args.layers > 0 else {}))
+    over = {"n_layers": args.layers} if args.layers > 0 else {}
+    for kv in args.set:
+        key, _, val = kv.partition("=")
+        over[key] = float(val) if "." in val or "e" in val.lower() else int(val)
+    c = configs.get(args.config, **over)
     T = c["micro"] * c["batch"] * c["seq"]
     P, F_exec, F_pages = model_numbers(c, args.ckpt_interval)
     # every replica on this host holds its own host state: refuse to start
@@ -302,7 +311,10 @@ def main():
 
     t_init = time.time()
     hbw = mt.host_bandwidth(1 << 30)
+    # every host wait of the library is bounded; a long-context step is minutes of GPU work
+    timeout_s = args.timeout if args.timeout > 0 else max(60.0, 4.0 * F_exec / 4e14)
     m = mt.Model(c, seed=1234, pin_store=args.pin_store, n_host_threads=args.threads, n_grad_slabs=args.slabs,
+                 timeout_ms=int(min(timeout_s * 1e3, 4.0e9)),
                  keep_host_grad=args.keep_host_grad, ckpt_on_host=args.ckpt_on_host,
                  ckpt_interval=args.ckpt_interval, n_buffers=args.buffers)
     init_s = time.time() - t_init

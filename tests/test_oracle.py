@@ -494,3 +494,28 @@ def test_schedule_hand_example(orc):
     stall, k = orc.schedule([10, 20, 30], [0, 0, 5], [1.5, 1.0, 1.0], [0, 0, 2], 10.0, 5.0)
     assert np.allclose(stall, [1.0, 0.5, 2.0])
     assert k == 4
+
+
+def test_attention_rows_matches_full_oracle(orc):
+    """The O(S hd)-per-row attention used at long context equals the full
+    oracle's forward and backward on every row of a small case."""
+    from oracle.attention_rows import attention_rows
+    rng = np.random.default_rng(31)
+    S, nh, nkv, hd = 150, 4, 2, 16
+    qkv = rng.standard_normal((S, (nh + 2 * nkv) * hd))
+    dout = rng.standard_normal((S, nh * hd))
+    o_ref, lse_ref = orc.attention_fwd(qkv, 1, S, nh, nkv, hd)
+    d_ref = orc.attention_bwd(qkv, o_ref, lse_ref, dout, 1, S, nh, nkv, hd)
+    q, k, v = qkv[:, :nh * hd], qkv[:, nh * hd:(nh + nkv) * hd], qkv[:, (nh + nkv) * hd:]
+    rows = np.arange(S)
+    r = attention_rows(q, k, v, dout, nh, nkv, hd, rows, rows)
+    assert np.allclose(r["o"], o_ref, rtol=1e-10, atol=1e-12)
+    assert np.allclose(r["lse"], lse_ref, rtol=1e-10, atol=1e-12)
+    assert np.allclose(r["dq"], d_ref[:, :nh * hd], rtol=1e-9, atol=1e-11)
+    assert np.allclose(r["dk"], d_ref[:, nh * hd:(nh + nkv) * hd], rtol=1e-9, atol=1e-11)
+    assert np.allclose(r["dv"], d_ref[:, (nh + nkv) * hd:], rtol=1e-9, atol=1e-11)
+    # a subset of rows gives the same values as the full computation
+    sub = attention_rows(q, k, v, dout, nh, nkv, hd, [0, 77, 149], [140, 149])
+    assert np.allclose(sub["dq"], r["dq"][[0, 77, 149]], rtol=1e-12, atol=1e-13)
+    assert np.allclose(sub["dk"], r["dk"][[140, 149]], rtol=1e-12, atol=1e-13)
+    assert np.all(r["dq_mag"] >= np.abs(r["dq"]) - 1e-12) and np.all(r["dv_mag"] >= np.abs(r["dv"]) - 1e-12)
