@@ -179,7 +179,7 @@ def mem_available_bytes() -> int:
     return 0
 
 
-def host_bytes_needed(c: dict, slabs: int, ckpt_on_host: int, ckpt_interval: int = 1) -> int:
+def host_bytes_needed(c: dict, slabs: int, ckpt_on_host: int, ckpt_interval: int = 1, host_accum: int = 0) -> int:
     """Host RAM one replica allocates: the flat store, the pinned gradient
     slabs (largest block's gradient region each) and the checkpoints."""
     import ctypes
@@ -188,8 +188,10 @@ def host_bytes_needed(c: dict, slabs: int, ckpt_on_host: int, ckpt_interval: int
     store = mt.lib().mt_store_bytes(ctypes.byref(cfg))
     wb = max(2 * b["n_pad"] for b in mt.layout(cfg))
     nseg = -(-c["n_layers"] // ckpt_interval)
-    ckpt = nseg * c["micro"] * c["batch"] * c["seq"] * c["hidden"] * 2 if ckpt_on_host else 0
-    return int(store + slabs * wb + 2 * wb + ckpt)
+    micro_per_pass = 1 if host_accum else c["micro"]
+    ckpt = nseg * micro_per_pass * c["batch"] * c["seq"] * c["hidden"] * 2 if ckpt_on_host else 0
+    acc = 2 * sum(b["n_pad"] for b in mt.layout(cfg)) * 2 if host_accum else 0  # FP32 accumulator
+    return int(store + slabs * wb + 2 * wb + ckpt + acc)
 
 
 def all_max(x: float, dist=None, device="cpu") -> float:
@@ -257,6 +259,8 @@ def main():
     ap.add_argument("--ckpt-interval", type=int, default=1, help="layers per recompute segment")
     ap.add_argument("--buffers", type=int, default=2, help="device weight buffers (1: single-buffer ablation)")
     ap.add_argument("--layers", type=int, default=0, help="decoder depth override (depth sweeps; 0 = the config's)")
+    ap.add_argument("--host-accum", type=int, default=0,
+                    help="1: one pass per micro-batch, gradients summed in FP32 on the host")
     ap.add_argument("--set", action="append", default=[], metavar="KEY=VALUE",
                     help="override a shape field of the config (e.g. hidden=4096); repeatable")
     ap.add_argument("--timeout", type=float, default=0,
@@ -298,7 +302,7 @@ def main():
     # every replica on this host holds its own host state: refuse to start
     # rather than exhaust host RAM
     local_world = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
-    need = local_world * host_bytes_needed(c, args.slabs, args.ckpt_on_host, args.ckpt_interval)
+    need = local_world * host_bytes_needed(c, args.slabs, args.ckpt_on_host, args.ckpt_interval, args.host_accum)
     avail = mem_available_bytes()
     if avail and need > 0.85 * avail:
         msg = (f"{local_world} replica(s) of the {args.config} workload need {need / 1e9:.1f} GB of host RAM; "
@@ -316,7 +320,7 @@ def main():
     m = mt.Model(c, seed=1234, pin_store=args.pin_store, n_host_threads=args.threads, n_grad_slabs=args.slabs,
                  timeout_ms=int(min(timeout_s * 1e3, 4.0e9)),
                  keep_host_grad=args.keep_host_grad, ckpt_on_host=args.ckpt_on_host,
-                 ckpt_interval=args.ckpt_interval, n_buffers=args.buffers)
+                 ckpt_interval=args.ckpt_interval, n_buffers=args.buffers, host_grad_accum=args.host_accum)
     init_s = time.time() - t_init
     toks = [inputs.tokens_for(c, s) for s in range(args.warmup + 2 * args.steps + 1)]
     step = 0
@@ -419,7 +423,8 @@ def main():
                    "tokens_per_step": T, "parallelism": f"replicas x{world} (no exchange step)",
                    "pin_store": args.pin_store, "n_grad_slabs": args.slabs, "keep_host_grad": args.keep_host_grad,
                    "ckpt_on_host": args.ckpt_on_host, "ckpt_interval": args.ckpt_interval,
-                   "n_buffers": args.buffers, "l2": "inputs larger than L2 (every step streams "
+                   "n_buffers": args.buffers, "host_grad_accum": args.host_accum,
+                   "l2": "inputs larger than L2 (every step streams "
                    f"{2 * P / 1e9:.2f} GB of weights in and out)"},
         "step_roofline": {"frac": t_roof / t_step, "t_roof_ms": t_roof * 1e3, "t_step_ms": t_step * 1e3,
                           "bound": "tensor" if t_compute >= t_link else "host link",

@@ -21,7 +21,7 @@ from .build import build as _build
 __all__ = ["lib", "Model", "make_config", "MtConfig", "ops", "REGION_W", "REGION_G",
            "REGION_MASTER", "REGION_M", "REGION_V"]
 
-REGION_W, REGION_G, REGION_MASTER, REGION_M, REGION_V = range(5)
+REGION_W, REGION_G, REGION_MASTER, REGION_M, REGION_V, REGION_GACC = range(6)
 STATUS = {0: "MT_OK", -1: "MT_ERR_ARG", -2: "MT_ERR_STATE", -3: "MT_ERR_HOST_OOM", -4: "MT_ERR_CUDA",
           -5: "MT_ERR_TIMEOUT", -6: "MT_ERR_INTERNAL", -7: "MT_ERR_DEVICE_OOM"}
 MAX_TENSORS = 8
@@ -44,7 +44,7 @@ class MtConfig(C.Structure):
                 ("beta2", C.c_float), ("adam_eps", C.c_float), ("weight_decay", C.c_float),
                 ("seed", C.c_uint64), ("timeout_ms", C.c_uint32), ("pin_store", C.c_int32),
                 ("head_chunk", C.c_int32), ("log_protocol", C.c_int32), ("keep_host_grad", C.c_int32),
-                ("n_buffers", C.c_int32)]
+                ("n_buffers", C.c_int32), ("host_grad_accum", C.c_int32)]
 
 
 class DevRegion(C.Structure):

@@ -20,6 +20,7 @@ bool config_valid(const mt_config* c, std::string* why) {
   if (c->hidden % 8 || c->ffn % 8 || c->head_dim % 16) return bad("hidden, ffn must be multiples of 8; head_dim of 16");
   if (c->ckpt_interval < 1 || c->ckpt_interval > c->n_layers) return bad("ckpt_interval must be in [1, n_layers]");
   if (c->n_buffers != 1 && c->n_buffers != 2) return bad("n_buffers must be 1 or 2");
+  if (c->host_grad_accum != 0 && c->host_grad_accum != 1) return bad("host_grad_accum must be 0 or 1");
   if (c->n_grad_slabs < 1 || c->n_grad_slabs > 256) return bad("n_grad_slabs out of range");
   if (c->timeout_ms == 0) return bad("timeout_ms must be positive");
   if (!(c->rms_eps > 0) || !(c->rope_base > 1)) return bad("rms_eps / rope_base");
@@ -255,6 +256,35 @@ bool Pool::parallel_for(int64_t n, const std::function<void(int64_t)>& fn, std::
   }
   return true;
 }
+
+void accumulate(int64_t n, const uint16_t* __restrict g, float* __restrict acc, bool first) {
+  if (first) {
+    for (int64_t i = 0; i < n; ++i) acc[i] = bf16f(g[i]);
+  } else {
+    for (int64_t i = 0; i < n; ++i) acc[i] += bf16f(g[i]);
+  }
+}
+
+void adam_acc(int64_t n, const uint16_t* __restrict g, float* __restrict acc, uint16_t* __restrict gcopy,
+              float* __restrict th, float* __restrict m, float* __restrict v, uint16_t* __restrict w, int32_t t,
+              float lr, float b1, float b2, float eps, float wd) {
+  const double bc1 = 1.0 - std::pow((double)b1, (double)t);
+  const double bc2 = 1.0 - std::pow((double)b2, (double)t);
+  const float step = (float)((double)lr / bc1);
+  const float isb2 = (float)(1.0 / std::sqrt(bc2));
+  const float c1 = 1.0f - b1, c2 = 1.0f - b2, lrwd = lr * wd;
+  for (int64_t i = 0; i < n; ++i) {
+    const float gi = acc[i] + bf16f(g[i]);
+    acc[i] = gi;
+    if (gcopy) gcopy[i] = bf16_rne(gi);
+    w[i] = adam_elem(gi, th[i], m[i], v[i], b1, c1, b2, c2, step, isb2, eps, lrwd);
+  }
+}
+
+int64_t tokens_per_pass(const mt_config* c) {
+  return (int64_t)(c->host_grad_accum ? 1 : c->micro_batches) * c->batch * c->seq;
+}
+int passes_per_step(const mt_config* c) { return c->host_grad_accum ? c->micro_batches : 1; }
 
 // ---------------------------------------------------------------- schedule
 // Two device buffers: the stream-in of visit v+1 overlaps the compute of v and

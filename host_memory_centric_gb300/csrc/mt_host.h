@@ -49,6 +49,17 @@ void init_block(const mt_config* c, const BlockDesc& b, int j, float* master, in
 // region, fused into the same pass).
 void adam(int64_t n, const uint16_t* g, uint16_t* gcopy, float* th, float* m, float* v, uint16_t* w, int32_t t,
           float lr, float b1, float b2, float eps, float wd);
+// Host gradient accumulation over micro-batch passes: acc = float(g) on the
+// first pass, acc += float(g) on the later ones.
+void accumulate(int64_t n, const uint16_t* g, float* acc, bool first);
+// The last pass: the FP32 gradient acc + float(g) goes back into acc, as BF16
+// into gcopy when not null, and drives the same Adam update.
+void adam_acc(int64_t n, const uint16_t* g, float* acc, uint16_t* gcopy, float* th, float* m, float* v, uint16_t* w,
+              int32_t t, float lr, float b1, float b2, float eps, float wd);
+// Tokens one pass over the layers processes, and passes per step: with host
+// accumulation every micro-batch is its own pass.
+int64_t tokens_per_pass(const mt_config* c);
+int passes_per_step(const mt_config* c);
 
 // ---------------------------------------------------------------- worker pool
 // Fixed threads running index ranges.  parallel_for may be called from several

@@ -48,7 +48,7 @@ cudaError_t pinned_alloc(void** p, size_t bytes) {
 }
 
 struct Job {
-  int32_t block, slab, t;
+  int32_t block, slab, t, pass;  // pass < passes - 1: FP32 accumulation only
 };
 
 struct Dev {
@@ -122,7 +122,10 @@ struct mt_model {
   uint8_t* slabs = nullptr;
   uint8_t* ckpt = nullptr;
   int32_t* htok = nullptr;  // pinned: tok[T] | tgt[T] | csr_start[V+1] | csr_rows[T]
-  float* hloss = nullptr;
+  float* hloss = nullptr;    // pinned: the loss of every pass of a step
+  float* gacc = nullptr;     // host FP32 gradient accumulator (host_grad_accum)
+  size_t gacc_bytes = 0;
+  std::vector<int64_t> gacc_off;  // element offset of each block in gacc
   size_t pinned_bytes = 0;
   int K = 12;
   // device
@@ -148,7 +151,9 @@ struct mt_model {
   std::string err;
   int64_t steps_done = 0, exports = 0;
   bool used[2] = {false, false};
-  int vis = 0, stage = 0;  // next visit of the current step, and its sub-stage
+  int vis = 0, stage = 0;  // next visit of the current pass, and its sub-stage
+  int pass = 0, npass = 1;  // micro-batch pass of the step (host_grad_accum), passes per step
+  int Mp = 1;               // micro-batches one pass processes
   bool tokens_set = false;
   std::vector<std::string> log;
   // stats
@@ -225,7 +230,7 @@ int64_t head_chunk(const mt_config* c, int64_t T) {
 
 // Carves the device region; with base == nullptr only sizes it.
 size_t carve(const mt_config* c, const std::vector<mth::BlockDesc>& lay, uint8_t* base, Dev* d) {
-  const int64_t T = mth::tokens_per_step(c), H = c->hidden, hd = c->head_dim, nh = c->n_heads,
+  const int64_t T = mth::tokens_per_pass(c), H = c->hidden, hd = c->head_dim, nh = c->n_heads,
                 nkv = c->n_kv_heads, F = c->ffn, V = c->vocab, L = c->n_layers, S = c->seq;
   const int64_t Nqkv = (nh + 2 * nkv) * hd, chunk = head_chunk(c, T);
   int64_t wb = 0;
@@ -415,9 +420,9 @@ mt_status decoder_forward(mt_model* m, const View& v, const bf16* x, bf16* out, 
     CU(m, mt::rope(d.qkv, T, m->Nqkv, m->nh + m->nkv, m->hd, m->S, d.cs, 0, s));
   }
   {
-    const double fl = 4.0 * m->M * m->B * (double)m->nh * m->hd * (double)m->S * m->S / 2;
+    const double fl = 4.0 * m->Mp * m->B * (double)m->nh * m->hd * (double)m->S * m->S / 2;
     Timed t(m, K_ATTN_F, fl, 0);
-    CU(m, mt::attention_fwd(d.qkv, m->M * m->B, m->S, m->nh, m->nkv, m->hd, d.attn, d.lse, s));
+    CU(m, mt::attention_fwd(d.qkv, m->Mp * m->B, m->S, m->nh, m->nkv, m->hd, d.attn, d.lse, s));
   }
   OK(fprop(m, d.attn, v.w[1], T, H, nhd, d.x1, x));
   {
@@ -453,9 +458,9 @@ mt_status decoder_backward(mt_model* m, const View& v, const bf16* x, const bf16
   }
   OK(wgrad_dgrad(m, d.dx1, d.attn, v.w[1], T, H, nhd, v.g[1], d.dattn));
   {
-    const double fl = 10.0 * m->M * m->B * (double)m->nh * m->hd * (double)m->S * m->S / 2;
+    const double fl = 10.0 * m->Mp * m->B * (double)m->nh * m->hd * (double)m->S * m->S / 2;
     Timed t(m, K_ATTN_B, fl, 0, 3);
-    CU(m, mt::attention_bwd(d.qkv, d.attn, d.lse, d.dattn, m->M * m->B, m->S, m->nh, m->nkv, m->hd, d.dqkv,
+    CU(m, mt::attention_bwd(d.qkv, d.attn, d.lse, d.dattn, m->Mp * m->B, m->S, m->nh, m->nkv, m->hd, d.dqkv,
                             d.delta, s));
   }
   {
@@ -504,8 +509,8 @@ mt_status head_forward_backward(mt_model* m, const View& v, const bf16* x, bf16*
     Timed t(m, K_OTHER, 0, 4.0 * T);
     CU(m, mt::reduce_sum(d.row_loss, T, inv_norm, d.loss, s));
   }
-  CU(m, cudaMemcpyAsync(m->hloss, d.loss, sizeof(float), cudaMemcpyDeviceToHost, s));
-  CU(m, cudaEventRecord(m->LOSS, s));
+  CU(m, cudaMemcpyAsync(m->hloss + m->pass, d.loss, sizeof(float), cudaMemcpyDeviceToHost, s));
+  if (m->pass + 1 == m->npass) CU(m, cudaEventRecord(m->LOSS, s));
   {
     Timed t(m, K_OTHER, 0, 8.0 * T * H, 2);
     CU(m, mt::rmsnorm_bwd(dhn, x, v.w[0], rstd, nullptr, T, H, din, v.g[0], d.rms_part, s));
@@ -527,8 +532,13 @@ void adam_loop(mt_model* m) {
       std::unique_lock<std::mutex> lk(m->amu);
       m->acv.wait(lk, [m] { return m->stopping || !m->jobs.empty(); });
       if (m->jobs.empty()) return;
+      // Jobs of one block run in pass order (they share its FP32 accumulator):
+      // only the first queued job of each block is eligible.
       auto best = m->jobs.end();
+      std::vector<int32_t> seen;
       for (auto it = m->jobs.begin(); it != m->jobs.end(); ++it) {
+        if (std::find(seen.begin(), seen.end(), it->block) != seen.end()) continue;
+        seen.push_back(it->block);
         const cudaError_t q = cudaEventQuery(m->SR[(size_t)it->slab]);
         if (q == cudaSuccess) {
           if (best == m->jobs.end() || it->block < best->block) best = it;
@@ -585,11 +595,20 @@ void adam_loop(mt_model* m) {
         g_inj_adam_throw--;
         inject_throw = true;
       }
+      const bool last = job.pass + 1 == m->npass;
+      float* acc = m->gacc ? m->gacc + m->gacc_off[(size_t)job.block] : nullptr;
       std::function<void(int64_t)> fn = [&](int64_t i) {
         if (inject_throw && i == 0) throw std::runtime_error("injected host worker fault");
         const int64_t o = items[(size_t)i].first, n = items[(size_t)i].second;
-        mth::adam(n, slab + o, c.keep_host_grad ? G + o : nullptr, th + o, mm + o, vv + o, W + o, job.t, c.lr,
-                  c.beta1, c.beta2, c.adam_eps, c.weight_decay);
+        if (!acc) {
+          mth::adam(n, slab + o, c.keep_host_grad ? G + o : nullptr, th + o, mm + o, vv + o, W + o, job.t, c.lr,
+                    c.beta1, c.beta2, c.adam_eps, c.weight_decay);
+        } else if (!last) {
+          mth::accumulate(n, slab + o, acc + o, job.pass == 0);
+        } else {
+          mth::adam_acc(n, slab + o, acc + o, c.keep_host_grad ? G + o : nullptr, th + o, mm + o, vv + o, W + o,
+                        job.t, c.lr, c.beta1, c.beta2, c.adam_eps, c.weight_decay);
+        }
       };
       std::string werr;
       if (!m->pool.parallel_for((int64_t)items.size(), fn, &werr))
@@ -598,7 +617,7 @@ void adam_loop(mt_model* m) {
     m->adam_us += std::chrono::duration_cast<std::chrono::microseconds>(Clock::now() - t0).count();
     {
       std::lock_guard<std::mutex> lk(m->amu);
-      if (st == MT_OK) m->adam_done[(size_t)job.block] = job.t;
+      if (st == MT_OK && job.pass + 1 == m->npass) m->adam_done[(size_t)job.block] = job.t;
       m->slab_free[(size_t)job.slab] = 1;
       m->inflight_jobs--;
     }
@@ -643,12 +662,26 @@ int visit_block(const mt_model* m, int v) { return m->plan[(size_t)v].j; }
 int visit_kind(const mt_model* m, int v) { return m->plan[(size_t)v].kind; }
 bool visit_fwd(const mt_model* m, int v) { return visit_kind(m, v) <= V_HEAD; }
 
+// The token data of pass p (from mt_set_tokens' pinned copy) to the device,
+// on the compute stream ahead of the embedding forward that reads it.
+mt_status upload_tokens(mt_model* m, int p) {
+  const int64_t T = m->T;
+  const int32_t* h = m->htok + (int64_t)p * (3 * T + m->V + 1);
+  CU(m, cudaMemcpyAsync(m->d.tok, h, (size_t)T * 4, cudaMemcpyHostToDevice, m->sc));
+  CU(m, cudaMemcpyAsync(m->d.tgt, h + T, (size_t)T * 4, cudaMemcpyHostToDevice, m->sc));
+  CU(m, cudaMemcpyAsync(m->d.csr_start, h + 2 * T, (size_t)(m->V + 1) * 4, cudaMemcpyHostToDevice, m->sc));
+  CU(m, cudaMemcpyAsync(m->d.csr_rows, h + 2 * T + m->V + 1, (size_t)T * 4, cudaMemcpyHostToDevice, m->sc));
+  if (p + 1 == m->npass) CU(m, cudaEventRecord(m->TOK, m->sc));
+  m->h2d += (3 * T + m->V + 1) * 4;
+  return MT_OK;
+}
+
 mt_status do_stream_in(mt_model* m, int j, int b) {
   const VisitDesc& vd = m->plan[(size_t)m->vis];
   const bool fwd = vd.kind <= V_HEAD;
   const bool copies = !(j == 0 && vd.kind == V_BWD);
   const mth::BlockDesc& bd = m->lay[(size_t)j];
-  if (fwd && m->steps_done > 0) {
+  if (fwd && m->steps_done > 0 && m->pass == 0) {
     logop(m, "H", "WAIT_ADAM", j, -1);
     if (m->live) OK(wait_adam(m, j, m->steps_done));
   }
@@ -734,6 +767,7 @@ mt_status do_forward(mt_model* m, int j, int b) {
   if (m->live) {
     const View v = make_view(m, j, b);
     if (j == 0) {
+      OK(upload_tokens(m, m->pass));
       Timed t(m, K_OTHER, 0, 4.0 * m->T * m->H);
       CU(m, mt::embed_fwd(m->d.tok, v.w[0], m->T, m->H, m->V, x_out(m, 0), m->sc));
     } else if (!head) {
@@ -821,11 +855,11 @@ mt_status do_stream_out(mt_model* m, int j, int b, int* slab_out) {
 }
 
 mt_status do_adam_enqueue(mt_model* m, int j, int k, int32_t t) {
-  logop(m, "H", "ADAM_ENQ", j, k);
+  logop(m, "H", m->pass + 1 < m->npass ? "ACCUM_ENQ" : "ADAM_ENQ", j, k);
   if (m->live) {
     {
       std::lock_guard<std::mutex> lk(m->amu);
-      m->jobs.push_back({j, k, t});
+      m->jobs.push_back({j, k, t, m->pass});
       m->inflight_jobs++;
     }
     m->acv.notify_all();
@@ -845,7 +879,10 @@ void advance(mt_model* m) {
     m->stage = 0;
     if (++m->vis == nvisits(m)) {
       m->vis = 0;
-      m->steps_done++;
+      if (++m->pass == m->npass) {
+        m->pass = 0;
+        m->steps_done++;
+      }
     }
   } else {
     m->stage++;
@@ -900,7 +937,9 @@ void fill_shape(mt_model* m) {
   m->L = c.n_layers; m->H = c.hidden; m->nh = c.n_heads; m->nkv = c.n_kv_heads; m->hd = c.head_dim;
   m->F = c.ffn; m->V = c.vocab; m->B = c.batch; m->S = c.seq; m->M = c.micro_batches;
   m->Nqkv = (m->nh + 2 * m->nkv) * m->hd;
-  m->T = mth::tokens_per_step(&c);
+  m->T = mth::tokens_per_pass(&c);  // device tokens of one pass
+  m->npass = mth::passes_per_step(&c);
+  m->Mp = c.host_grad_accum ? 1 : c.micro_batches;
   m->chunk = head_chunk(&c, m->T);
   m->lay = mth::build_layout(&c);
   m->wb_max = 0;
@@ -944,6 +983,7 @@ mt_model::~mt_model() {
     if (hloss) cudaFreeHost(hloss);
   }
   if (store) munmap(store, store_bytes);
+  if (gacc) munmap(gacc, gacc_bytes);
 }
 
 // ======================================================================== C ABI
@@ -1054,9 +1094,20 @@ mt_status mt_init_model(const mt_config* c, mt_dev_region dev, mt_streams s, mt_
     if (pinned_alloc((void**)&m->ckpt, bytes) != cudaSuccess) return MT_ERR_HOST_OOM;
     m->pinned_bytes += bytes;
   }
-  const size_t tokb = (size_t)(3 * m->T + m->V + 1) * 4;
+  const size_t tokb = (size_t)m->npass * (3 * m->T + m->V + 1) * 4;  // per pass: tok | tgt | csr start | csr rows
   if (pinned_alloc((void**)&m->htok, tokb) != cudaSuccess) return MT_ERR_HOST_OOM;
-  if (pinned_alloc((void**)&m->hloss, 64) != cudaSuccess) return MT_ERR_HOST_OOM;
+  if (pinned_alloc((void**)&m->hloss, 64 + 4 * (size_t)m->npass) != cudaSuccess) return MT_ERR_HOST_OOM;
+  if (m->npass > 1) {  // host FP32 gradient accumulator, one n_pad range per block
+    int64_t n = 0;
+    for (auto& b : m->lay) {
+      m->gacc_off.push_back(n);
+      n += b.n_pad;
+    }
+    m->gacc_bytes = (size_t)n * 4;
+    void* p = mmap(nullptr, m->gacc_bytes, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    if (p == MAP_FAILED) return MT_ERR_HOST_OOM;
+    m->gacc = (float*)p;
+  }
   m->pinned_bytes += tokb + 64;
 
   for (cudaEvent_t* e : {&m->WR[0], &m->WR[1], &m->BD[0], &m->BD[1], &m->BF[0], &m->BF[1], &m->XR[0], &m->XR[1],
@@ -1081,23 +1132,24 @@ mt_status mt_init_model(const mt_config* c, mt_dev_region dev, mt_streams s, mt_
 mt_status mt_set_tokens(mt_model* m, const int32_t* tok) {
   if (!m || !tok) return MT_ERR_ARG;
   if (m->failed) return MT_ERR_STATE;
-  const int64_t T = m->T;
-  for (int64_t i = 0; i < T; ++i)
+  if (m->vis != 0 || m->stage != 0 || m->pass != 0)
+    return set_err(m, MT_ERR_STATE, "mt_set_tokens: a step is in progress", false);
+  const int64_t T = m->T, Tstep = T * m->npass;
+  for (int64_t i = 0; i < Tstep; ++i)
     if (tok[i] < 0 || tok[i] >= m->V) return set_err(m, MT_ERR_ARG, "token id out of range", false);
   if (m->tokens_set) OK(wait_event(m, m->TOK, "previous token upload"));
-  int32_t* h = m->htok;
-  int32_t* tg = h + T;
-  int32_t* cst = tg + T;
-  int32_t* rows = cst + m->V + 1;
-  std::memcpy(h, tok, (size_t)T * 4);
-  for (int64_t t = 0; t < T; ++t) tg[t] = (t % m->S) < m->S - 1 ? tok[t + 1] : -1;
-  mt_token_csr(tok, T, m->V, cst, rows);
-  CU(m, cudaMemcpyAsync(m->d.tok, h, (size_t)T * 4, cudaMemcpyHostToDevice, m->sc));
-  CU(m, cudaMemcpyAsync(m->d.tgt, tg, (size_t)T * 4, cudaMemcpyHostToDevice, m->sc));
-  CU(m, cudaMemcpyAsync(m->d.csr_start, cst, (size_t)(m->V + 1) * 4, cudaMemcpyHostToDevice, m->sc));
-  CU(m, cudaMemcpyAsync(m->d.csr_rows, rows, (size_t)T * 4, cudaMemcpyHostToDevice, m->sc));
-  CU(m, cudaEventRecord(m->TOK, m->sc));
-  m->h2d += (3 * T + m->V + 1) * 4;
+  // per pass: its tokens, next-token targets (-1 at a sequence's last
+  // position), and the token CSR of the embedding backward
+  for (int p = 0; p < m->npass; ++p) {
+    const int32_t* src = tok + (int64_t)p * T;
+    int32_t* h = m->htok + (int64_t)p * (3 * T + m->V + 1);
+    int32_t* tg = h + T;
+    int32_t* cst = tg + T;
+    int32_t* rows = cst + m->V + 1;
+    std::memcpy(h, src, (size_t)T * 4);
+    for (int64_t t = 0; t < T; ++t) tg[t] = (t % m->S) < m->S - 1 ? src[t + 1] : -1;
+    mt_token_csr(src, T, m->V, cst, rows);
+  }
   m->tokens_set = true;
   return MT_OK;
 }
@@ -1161,15 +1213,18 @@ mt_status mt_adam_host(mt_model* m, int32_t block, int32_t slab, int32_t adam_st
 mt_status mt_train_step(mt_model* m, int32_t step, float* loss) {
   if (!m) return MT_ERR_ARG;
   if (m->failed) return MT_ERR_STATE;
-  if (step != m->steps_done || m->vis != 0 || m->stage != 0)
+  if (step != m->steps_done || m->vis != 0 || m->stage != 0 || m->pass != 0)
     return set_err(m, MT_ERR_STATE, "mt_train_step: step index or visit state mismatch", false);
   if (!m->tokens_set) return set_err(m, MT_ERR_STATE, "no tokens set", false);
   const double t0 = now_ms();
   const int n = nvisits(m);
-  for (int v = 0; v < n; ++v) OK(run_visit(m));
+  for (int p = 0; p < m->npass; ++p)
+    for (int v = 0; v < n; ++v) OK(run_visit(m));
   if (loss) {
     OK(wait_event(m, m->LOSS, "loss"));
-    *loss = *m->hloss;
+    float sum = 0.f;  // the step loss is the sum of the passes' (each already divided by all micro-batches)
+    for (int p = 0; p < m->npass; ++p) sum += m->hloss[p];
+    *loss = sum;
   }
   m->last_step_ms = now_ms() - t0;
   return MT_OK;
@@ -1198,8 +1253,14 @@ mt_status mt_sync(mt_model* m) {
 }
 
 mt_status mt_read_host(mt_model* m, int32_t block, int32_t region, void* dst, size_t bytes) {
-  if (!m || !dst || block < 0 || block >= (int)m->lay.size() || region < 0 || region > 4) return MT_ERR_ARG;
+  if (!m || !dst || block < 0 || block >= (int)m->lay.size() || region < 0 || region > MT_REGION_GACC)
+    return MT_ERR_ARG;
   const mth::BlockDesc& b = m->lay[(size_t)block];
+  if (region == MT_REGION_GACC) {
+    if (!m->gacc || (int64_t)bytes > b.n_pad * 4) return MT_ERR_ARG;
+    std::memcpy(dst, m->gacc + m->gacc_off[(size_t)block], bytes);
+    return MT_OK;
+  }
   const int64_t rb = region < 2 ? b.wbytes : b.fbytes;
   if ((int64_t)bytes > rb) return MT_ERR_ARG;
   std::memcpy(dst, m->store + b.store_off + b.region[region], bytes);
@@ -1316,8 +1377,9 @@ int64_t mt_plan_protocol(const mt_config* c, int32_t n_steps, char* buf, int64_t
   fill_shape(&m);
   m.tokens_set = true;
   for (int s = 0; s < n_steps; ++s)
-    for (int v = 0; v < nvisits(&m); ++v)
-      if (run_visit(&m) != MT_OK) return 0;
+    for (int p = 0; p < m.npass; ++p)
+      for (int v = 0; v < nvisits(&m); ++v)
+        if (run_visit(&m) != MT_OK) return 0;
   return mt_protocol_log(&m, buf, cap);
 }
 

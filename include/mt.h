@@ -62,6 +62,9 @@ typedef struct mt_model mt_model;
 /* Region of a flat block ([Hotdry] host memory layout: one contiguous block
  * per layer holding BF16 weights, BF16 gradients and FP32 Adam state). */
 enum { MT_REGION_W = 0, MT_REGION_G = 1, MT_REGION_MASTER = 2, MT_REGION_M = 3, MT_REGION_V = 4 };
+/* mt_read_host only, with host_grad_accum: the FP32 gradient (n_pad floats)
+ * the last completed step's Adam used for the block. */
+enum { MT_REGION_GACC = 5 };
 
 /* Model, step and runtime configuration.  Plain data, copied by
  * mt_init_model.  Tokens per step T = micro_batches * batch * seq. */
@@ -89,6 +92,13 @@ typedef struct {
                               BF16 G region; 0: Adam reads the slab only  */
   int32_t n_buffers;       /* device weight buffers: 2 (double-buffered, the
                               pages' engine) or 1 (single-buffer ablation)  */
+  int32_t host_grad_accum; /* 0: the micro-batches of a step share each
+                              visit and the gradient sums on the device;
+                              1: one pass over all blocks per micro-batch,
+                              every pass exports its gradients, the host
+                              sums them in FP32 and Adam runs on the sum
+                              after the last pass ([Hotdry] gradient
+                              export: accumulated into the master store) */
 } mt_config;
 
 typedef struct { void* base; size_t bytes; } mt_dev_region;          /* caller-owned device memory  */

@@ -85,7 +85,8 @@ def lib():
             "or_step_fwd_bwd_d": (d, [pc, _P(_P(d)), _P(i32), _P(_P(d))]),
             "or_forward_hidden_f": (d, [pc, _P(_P(f)), _P(i32), i32, _P(f)]),
             "or_adam": (None, [i64, _P(u16), _P(f), _P(f), _P(f), _P(u16), i32, f, f, f, f, f]),
-            "or_protocol": (i64, [pc, i32, i32, i32, i32, i32, i32, C.c_char_p, i64]),
+            "or_protocol": (i64, [pc, i32, i32, i32, i32, i32, i32, i32, C.c_char_p, i64]),
+            "or_adam_f32": (None, [i64, _P(f), _P(u16), _P(f), _P(f), _P(f), _P(u16), i32, f, f, f, f, f]),
             "or_schedule": (i32, [i32, _P(d), _P(d), _P(d), _P(d), d, d, _P(d)]),
         }
         for name, (res, args) in sig.items():
@@ -292,10 +293,21 @@ def adam(g_bf16, master, m, v, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, 
     return w
 
 
+def adam_f32(g32, master, m, v, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0):
+    """In-place Adam on (master, m, v) with an FP32 gradient; returns the new BF16 weights."""
+    g = np.ascontiguousarray(g32, np.float32)
+    for a in (master, m, v):
+        assert a.dtype == np.float32 and a.flags["C_CONTIGUOUS"]
+    w = np.empty(g.size, dtype=np.uint16)
+    lib().or_adam_f32(g.size, _ptr(g, C.c_float), None, _ptr(master, C.c_float), _ptr(m, C.c_float),
+                      _ptr(v, C.c_float), _ptr(w, C.c_uint16), step, lr, beta1, beta2, eps, wd)
+    return w
+
+
 def protocol(shape: dict, n_steps: int, n_slabs: int, ckpt_on_host: bool, jit_pack: bool,
-             ckpt_interval: int = 1, n_buffers: int = 2) -> list[str]:
+             ckpt_interval: int = 1, n_buffers: int = 2, n_passes: int = 1) -> list[str]:
     c = make_cfg(shape)
-    args = (n_steps, n_slabs, int(ckpt_on_host), int(jit_pack), int(ckpt_interval), int(n_buffers))
+    args = (n_steps, n_slabs, int(ckpt_on_host), int(jit_pack), int(ckpt_interval), int(n_buffers), int(n_passes))
     need = -lib().or_protocol(C.byref(c), *args, None, 0)
     assert need > 0, "invalid protocol arguments"
     buf = C.create_string_buffer(int(need) + 1)

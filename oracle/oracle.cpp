@@ -643,12 +643,21 @@ double or_forward_hidden_f(const or_cfg* c, const float* const* W, const int32_t
 // re-derived from the master by round-to-nearest-even.  [Review] 3-2 (6) puts
 // the update on the CPU; [Lilting] (memory table) fixes BF16 W/G and FP32
 // master, m, v.  Decoupled weight decay (AdamW) when weight_decay != 0.
+void or_adam_f32(int64_t n, const float* g32, const uint16_t* g_bf16, float* master, float* m, float* v,
+                 uint16_t* w_bf16, int32_t step, float lr, float beta1, float beta2, float eps, float weight_decay);
 void or_adam(int64_t n, const uint16_t* g_bf16, float* master, float* m, float* v, uint16_t* w_bf16,
              int32_t step, float lr, float beta1, float beta2, float eps, float weight_decay) {
+  or_adam_f32(n, nullptr, g_bf16, master, m, v, w_bf16, step, lr, beta1, beta2, eps, weight_decay);
+}
+// The same update with the gradient given in FP32 (g32), as when micro-batch
+// gradients are summed in FP32 on the host before the optimizer step; with
+// g32 = nullptr the gradient is float(g_bf16).
+void or_adam_f32(int64_t n, const float* g32, const uint16_t* g_bf16, float* master, float* m, float* v,
+                 uint16_t* w_bf16, int32_t step, float lr, float beta1, float beta2, float eps, float weight_decay) {
   const float bc1 = (float)(1.0 - std::pow((double)beta1, (double)step));
   const float bc2 = (float)(1.0 - std::pow((double)beta2, (double)step));
   for (int64_t i = 0; i < n; ++i) {
-    const float g = bf16_f32(g_bf16[i]);
+    const float g = g32 ? g32[i] : bf16_f32(g_bf16[i]);
     m[i] = beta1 * m[i] + (1.0f - beta1) * g;
     v[i] = beta2 * v[i] + (1.0f - beta2) * g * g;
     const float mhat = m[i] / bc1;
@@ -706,7 +715,11 @@ extern "C" {
 // Weights-Ready, runs, and records Buffer-Free (forward, recompute: nothing to
 // export) or Backward-Done; the gradient stream (G) waits Backward-Done,
 // copies the gradients into a free slab, records Buffer-Free and Slab-Ready;
-// the host (H) enqueues Adam on the slab.  Buffers alternate per visit
+// the host (H) enqueues Adam on the slab.  With host gradient accumulation a
+// step is n_passes passes of the whole visit list, one per micro-batch: every
+// pass exports its gradients, the host adds them into an FP32 accumulator
+// (ACCUM) and only the last pass's export runs Adam; the next step's first
+// pass waits for Adam.  Buffers alternate per visit
 // (n_buffers = 2) or one buffer serves every visit (n_buffers = 1, the pages'
 // single-buffer ablation).  Host-resident checkpoints: the forward saves X_s
 // from a two-slot ring (C records XR, G waits it, copies, records XS; the
@@ -715,9 +728,10 @@ extern "C" {
 // was saved from.  Slabs are numbered round-robin here, one valid assignment;
 // the library takes the lowest free slab and logs are compared modulo that.
 int64_t or_protocol(const or_cfg* c, int32_t n_steps, int32_t n_slabs, int32_t ckpt_on_host,
-                    int32_t jit_pack, int32_t ckpt_interval, int32_t n_buffers, char* buf, int64_t cap) {
+                    int32_t jit_pack, int32_t ckpt_interval, int32_t n_buffers, int32_t n_passes, char* buf,
+                    int64_t cap) {
   if (!cfg_ok(c) || n_slabs < 1 || n_steps < 0 || ckpt_interval < 1 || ckpt_interval > c->n_layers ||
-      n_buffers < 1 || n_buffers > 2)
+      n_buffers < 1 || n_buffers > 2 || n_passes < 1)
     return 0;
   const long L = c->n_layers, ci = ckpt_interval;
   const std::vector<Visit> vis = step_visits(L, ci);
@@ -726,12 +740,13 @@ int64_t or_protocol(const or_cfg* c, int32_t n_steps, int32_t n_slabs, int32_t c
   bool used[2] = {false, false};
   for (int st = 0; st < n_steps; ++st) {
     log.step = st;
+    for (int pass = 0; pass < n_passes; ++pass)
     for (size_t vi = 0; vi < vis.size(); ++vi) {
       const Visit& V = vis[vi];
       const long j = V.j, b = (long)vi % n_buffers;
       const bool fwd = V.kind <= 1, head = V.kind == 1;
       const bool copies = !(j == 0 && V.kind == 3);
-      if (fwd && st > 0) log.op("H", "WAIT_ADAM", j, -1);
+      if (fwd && st > 0 && pass == 0) log.op("H", "WAIT_ADAM", j, -1);
       if (copies && jit_pack) {
         if (used[b]) log.op("H", "WAIT_STAGE", b, -1);
         log.op("H", "PACK", j, b);
@@ -770,7 +785,7 @@ int64_t or_protocol(const or_cfg* c, int32_t n_steps, int32_t n_slabs, int32_t c
         log.op("G", "D2H", j, k);
         log.op("G", "REC_BF", b, -1);
         log.op("G", "REC_SR", k, -1);
-        log.op("H", "ADAM_ENQ", j, k);
+        log.op("H", pass + 1 < n_passes ? "ACCUM_ENQ" : "ADAM_ENQ", j, k);
       }
     }
   }

@@ -88,6 +88,10 @@ double or_forward_hidden_f(const or_cfg* c, const float* const* W, const int32_t
                            float* out);
 
 /* ---- Adam ([Review] 3-2 (6); [Lilting] memory table) ---- */
+/* The same with an FP32 gradient g32 (g_bf16 unused when g32 is given). */
+void or_adam_f32(int64_t n, const float* g32, const uint16_t* g_bf16, float* master, float* m, float* v,
+                 uint16_t* w_bf16, int32_t step, float lr, float beta1, float beta2, float eps,
+                 float weight_decay);
 void or_adam(int64_t n, const uint16_t* g_bf16, float* master, float* m, float* v,
              uint16_t* w_bf16, int32_t step, float lr, float beta1, float beta2, float eps,
              float weight_decay);
@@ -97,9 +101,11 @@ void or_adam(int64_t n, const uint16_t* g_bf16, float* master, float* m, float* 
  * buf (NUL-terminated).  Returns the length, or -(needed) if cap is short.
  * ckpt_interval c in [1, n_layers]: X_s is kept for s = 0, c, 2c, ... and the
  * backward recomputes each c-layer segment from it ([Review] 2, block-wise
- * recomputation); n_buffers in {1, 2} device weight buffers. */
+ * recomputation); n_buffers in {1, 2} device weight buffers; n_passes passes
+ * per step (one per micro-batch with host FP32 gradient accumulation, else 1). */
 int64_t or_protocol(const or_cfg* c, int32_t n_steps, int32_t n_slabs, int32_t ckpt_on_host,
-                    int32_t jit_pack, int32_t ckpt_interval, int32_t n_buffers, char* buf, int64_t cap);
+                    int32_t jit_pack, int32_t ckpt_interval, int32_t n_buffers, int32_t n_passes, char* buf,
+                    int64_t cap);
 
 /* ---- static prefetch schedule ([Peter] 記憶體預取策略) ---- */
 /* Per visit v of one step (2L+3 visits): b[v] H2D bytes, d[v] gradient bytes

@@ -15,7 +15,8 @@ those sentences forbid is ordered:
   * compute on b after this visit's H2D into b;
   * export from b after the compute that wrote its gradients;
   * host pack into staging b after the previous H2D read staging b;
-  * D2H into slab k after the previous Adam on slab k, Adam after the D2H;
+  * D2H into slab k after the previous host job (Adam or FP32 accumulation)
+    on slab k, the job after the D2H;
   * next step's pack / H2D of block j after block j's Adam;
   * checkpoint slots: write after the previous save, save after the write;
     a host checkpoint is loaded only after it was saved and saved again only
@@ -99,13 +100,16 @@ def check(lines: list[str]) -> None:
             elif op == "ACQ_SLAB":
                 if a in slab_adam:
                     clk["H"].merge(slab_adam[a][1])
-            elif op == "ADAM_ENQ":
+            elif op in ("ADAM_ENQ", "ACCUM_ENQ"):
+                # a host job on slab b: Adam (the step's last export of block a) or
+                # the FP32 accumulation of an earlier micro-batch pass
                 clk["A"].merge(clk["H"])
                 clk["A"].merge(ev["SR" + str(b)])
                 me = tick("A")
-                assert _hb(slab_d2h[b], me), "Adam reads slab before its D2H: " + where
+                assert _hb(slab_d2h[b], me), "host job reads slab before its D2H: " + where
                 slab_adam[b] = me
-                adam_done[a] = me
+                if op == "ADAM_ENQ":
+                    adam_done[a] = me
             continue
         me = tick(s)
         if op == "H2D":
@@ -172,7 +176,7 @@ def mask_slabs(lines: list[str]) -> list[str]:
         step, s, op, a, b = l.split()
         if op in ("ACQ_SLAB", "REC_SR"):
             a = "k"
-        elif op in ("D2H", "ADAM_ENQ"):
+        elif op in ("D2H", "ADAM_ENQ", "ACCUM_ENQ"):
             b = "k"
         out.append(" ".join((step, s, op, a, b)))
     return out

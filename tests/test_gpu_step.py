@@ -75,9 +75,14 @@ def run_parity(orc, c, steps, check_init=True, **rt):
                 e = rel_l2(Gf[sl].astype(np.float64), G_ref[j][sl].astype(np.float64))
                 worst = max(worst, e)
                 assert e <= 2e-2, (step, j, t, e)
-            # teacher-forced oracle Adam on the library's gradient
-            orc.adam(G, master_o[j], m_o[j], v_o[j], step + 1, lr=c["lr"], beta1=c["beta1"],
-                     beta2=c["beta2"], eps=c["adam_eps"])
+            # teacher-forced oracle Adam on the library's gradient (with host
+            # accumulation: the FP32 sum of the passes that Adam used)
+            if rt.get("host_grad_accum"):
+                orc.adam_f32(m.read(j, mt.REGION_GACC), master_o[j], m_o[j], v_o[j], step + 1, lr=c["lr"],
+                             beta1=c["beta1"], beta2=c["beta2"], eps=c["adam_eps"])
+            else:
+                orc.adam(G, master_o[j], m_o[j], v_o[j], step + 1, lr=c["lr"], beta1=c["beta1"],
+                         beta2=c["beta2"], eps=c["adam_eps"])
         report.append((step, loss, loss_ref, worst))
     for j in range(nb):
         got = m.read(j, mt.REGION_MASTER)
@@ -178,3 +183,35 @@ def test_checkpoint_interval_reproduces_interval_one():
         assert out[ci][0] == out[1][0], ci
         for j, (g, g1) in enumerate(zip(out[ci][1], out[1][1])):
             assert np.mean(g == g1) > 0.999, (ci, j)
+
+
+@pytest.mark.parametrize("ckpt", [1, 0])
+def test_host_gradient_accumulation_parity(orc, ckpt):
+    """One pass per micro-batch with the gradients summed in FP32 on the host
+    (Adam on the sum after the last pass): oracle parity and the simulator's
+    enqueue log."""
+    c = configs.get("tiny", micro=3)
+    report, log = run_parity(orc, c, 3, host_grad_accum=1, ckpt_on_host=ckpt)
+    ref = orc.protocol(oracle_shape(c), 3, 12, bool(ckpt), True, 1, 2, 3)
+    assert protocol_check.mask_slabs(log) == protocol_check.mask_slabs(ref)
+    protocol_check.check(log)
+
+
+def test_host_and_device_accumulation_agree():
+    """Summing the micro-batches on the device (one visit per block) or on
+    the host in FP32 (one pass per micro-batch) gives the same step."""
+    c = configs.get("tiny", micro=2)
+    tok = inputs.tokens_for(c, 0)
+    out = {}
+    for acc in (0, 1):
+        m = mt.Model(c, seed=11, host_grad_accum=acc)
+        m.set_tokens(tok)
+        loss = m.train_step(0)
+        m.sync()
+        # BF16 gradients as FP32 values (the BF16 bits are the high half)
+        out[acc] = (loss, [(m.read(j, mt.REGION_G).astype(np.uint32) << 16).view(np.float32)
+                           for j in range(len(m.layout))])
+        m.close()
+    assert out[1][0] == pytest.approx(out[0][0], rel=1e-5)
+    for g1, g0 in zip(out[1][1], out[0][1]):
+        assert rel_l2(g1, g0) <= 1e-2

@@ -113,6 +113,29 @@ def test_protocol_plan_segments_bit_exact(orc, ci, nbuf, ckpt):
     protocol_check.check(lines)
 
 
+@pytest.mark.parametrize("micro,ckpt", [(2, 1), (3, 0)])
+def test_protocol_plan_host_accumulation_bit_exact(orc, micro, ckpt):
+    c = configs.get("tiny", n_layers=3, micro=micro)
+    lines = _plan(c, 2, ckpt_on_host=ckpt, pin_store=0, n_grad_slabs=3, host_grad_accum=1)
+    ref = orc.protocol(c, 2, 3, bool(ckpt), True, 1, 2, micro)
+    assert protocol_check.mask_slabs(lines) == protocol_check.mask_slabs(ref)
+    protocol_check.check(lines)
+
+
+def test_host_accumulation_shrinks_device_region():
+    """With one pass per micro-batch the device holds one micro-batch's
+    activations."""
+    L = mt.lib()
+    c = configs.get("1.2b", micro=4)
+    n = {}
+    for acc in (0, 1):
+        cfg = mt.make_config(c, host_grad_accum=acc)
+        b = C.c_size_t()
+        assert L.mt_query_device_bytes(C.byref(cfg), C.byref(b)) == 0
+        n[acc] = b.value
+    assert n[1] < 0.5 * n[0]
+
+
 @pytest.mark.parametrize("L,ci", [(2, 1), (5, 2), (7, 3), (4, 4)])
 def test_visit_plan_matches_oracle(orc, L, ci):
     c = configs.get("tiny", n_layers=L)
@@ -183,7 +206,8 @@ def test_bad_arguments_rejected_without_gpu():
     assert L.mt_query_device_bytes(C.byref(cfg), C.byref(nbytes)) == 0 and nbytes.value > 0
     bad = mt.make_config(configs.get("tiny"), n_kv_heads=3)
     assert L.mt_query_device_bytes(C.byref(bad), C.byref(nbytes)) == -1
-    for kw in (dict(ckpt_interval=0), dict(ckpt_interval=3), dict(n_buffers=0), dict(n_buffers=3)):
+    for kw in (dict(ckpt_interval=0), dict(ckpt_interval=3), dict(n_buffers=0), dict(n_buffers=3),
+               dict(host_grad_accum=2)):
         bad = mt.make_config(configs.get("tiny"), **kw)  # tiny has 2 layers
         assert L.mt_query_device_bytes(C.byref(bad), C.byref(nbytes)) == -1, kw
     ok = mt.make_config(configs.get("tiny"), ckpt_interval=2, n_buffers=1)

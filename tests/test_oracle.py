@@ -464,6 +464,23 @@ def test_protocol_segments_race_free(orc, L, ci, ckpt, nbuf):
     assert bufs == set(range(nbuf))
 
 
+@pytest.mark.parametrize("passes,ckpt", [(2, 1), (3, 0), (2, 0)])
+def test_protocol_host_accumulation_passes(orc, passes, ckpt):
+    """One pass of every block per micro-batch: each pass exports, only the
+    last pass's exports run Adam, and only the first pass waits for Adam."""
+    L = 3
+    shape = configs.get("tiny", n_layers=L)
+    lines = orc.protocol(shape, 3, 2, bool(ckpt), True, 1, 2, passes)
+    protocol_check.check(lines)
+    per_step = [l for l in lines if l.startswith("1 ")]
+    count = lambda op: sum(1 for l in per_step if f" {op} " in l)
+    assert count("ADAM_ENQ") == L + 2
+    assert count("ACCUM_ENQ") == (passes - 1) * (L + 2)
+    assert count("D2H") == passes * (L + 2)
+    assert count("WAIT_ADAM") == L + 2  # forward visits of the first pass only
+    assert count("H2D") == passes * ((L + 2) + L)
+
+
 def test_protocol_segment_order_hand_example(orc):
     """L = 7, interval 3: X_0, X_3, X_6 kept; segments [7], [4..6], [1..3]
     from the top, each rebuilding X_{s+1} .. X_{e-1} before its backward."""
