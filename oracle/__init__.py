@@ -39,14 +39,16 @@ class Cfg(C.Structure):
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn", C.c_int32),
                 ("vocab", C.c_int32), ("batch", C.c_int32), ("seq", C.c_int32),
                 ("micro", C.c_int32), ("rope_base", C.c_double), ("rms_eps", C.c_double),
-                ("init_std", C.c_double)]
+                ("init_std", C.c_double), ("n_experts", C.c_int32), ("top_k", C.c_int32),
+                ("expert_ffn", C.c_int32)]
 
 
 def make_cfg(shape: dict) -> Cfg:
     return Cfg(shape["n_layers"], shape["hidden"], shape["n_heads"], shape["n_kv_heads"],
                shape["head_dim"], shape["ffn"], shape["vocab"], shape["batch"], shape["seq"],
                shape["micro"], shape.get("rope_base", 10000.0), shape.get("rms_eps", 1e-6),
-               shape.get("init_std", 0.02))
+               shape.get("init_std", 0.02), shape.get("n_experts", 0), shape.get("top_k", 0),
+               shape.get("expert_ffn", 0))
 
 
 _lib = None
@@ -88,6 +90,9 @@ def lib():
             "or_protocol": (i64, [pc, i32, i32, i32, i32, i32, i32, i32, C.c_char_p, i64]),
             "or_adam_f32": (None, [i64, _P(f), _P(u16), _P(f), _P(f), _P(f), _P(u16), i32, f, f, f, f, f]),
             "or_schedule": (i32, [i32, _P(d), _P(d), _P(d), _P(d), d, d, _P(d)]),
+            "or_last_route_margin": (d, []),
+            "or_moe_layer_d": (d, [i64, i64, i64, i64, i64] + [_P(d)] * 9 + [_P(i32), _P(d)]),
+            "or_moe_layer_f": (d, [i64, i64, i64, i64, i64] + [_P(f)] * 9 + [_P(i32), _P(f)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -253,6 +258,28 @@ def cross_entropy(logits, tok, n_seq, S, norm):
     dl = np.empty_like(logits)
     loss = lib().or_cross_entropy_d(_d(logits), _ptr(tok, C.c_int32), n_seq, S, V, norm, _d(dl))
     return loss, dl
+
+
+def moe_layer(yn, x1, Wr, We, dout, k, Fe, dtype=np.float64):
+    """The MoE feed-forward of one layer and its backward (see or_moe_layer_d).
+    Returns out, dyn, dWr, dWe, idx [T, k], gate [T, k], smallest margin."""
+    ct = C.c_double if dtype == np.float64 else C.c_float
+    yn, x1, Wr, We, dout = (np.ascontiguousarray(a, dtype) for a in (yn, x1, Wr, We, dout))
+    T, H = yn.shape
+    E = Wr.shape[0]
+    out = np.empty((T, H), dtype); dyn = np.empty((T, H), dtype)
+    dWr = np.empty_like(Wr); dWe = np.empty_like(We)
+    idx = np.empty((T, k), np.int32); gate = np.empty((T, k), dtype)
+    fn = lib().or_moe_layer_d if dtype == np.float64 else lib().or_moe_layer_f
+    p = lambda a: _ptr(a, ct)
+    mg = fn(T, H, E, k, Fe, p(yn), p(x1), p(Wr), p(We), p(dout), p(out), p(dyn), p(dWr), p(dWe),
+            _ptr(idx, C.c_int32), p(gate))
+    return out, dyn, dWr, dWe, idx, gate, float(mg)
+
+
+def last_route_margin() -> float:
+    """Smallest routing margin of the last whole-step / forward call."""
+    return float(lib().or_last_route_margin())
 
 
 # ---------------------------------------------------------------- whole step

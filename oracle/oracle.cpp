@@ -84,6 +84,11 @@ float bf16_f32(uint16_t b) {
 //   block 1..L   : W_qkv [(nh+2nkv)hd, H], W_o [H, nh hd], W_gu [2F, H],
 //                  W_down [H, F], gamma1 [H], gamma2 [H]
 //   block L+1    : gamma_f [H], W_head [V, H]
+// With n_experts = E > 0 (routed mixture of experts, [Lilting] MoE section)
+// a decoder block holds W_qkv, W_o, W_router [E, H], W_experts [E, 3 Fe H],
+// gamma1, gamma2, where row e of W_experts is expert e's W_gu [2Fe, H]
+// followed by its W_down [H, Fe]: one expert is one contiguous range, so
+// streaming only the routed experts copies whole rows of this tensor.
 // ---------------------------------------------------------------------------
 struct Tensor { int64_t off, rows, cols; };
 struct Block {
@@ -96,7 +101,9 @@ inline int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 bool cfg_ok(const or_cfg* c) {
   return c && c->n_layers >= 0 && c->hidden > 0 && c->n_heads > 0 && c->n_kv_heads > 0 &&
          c->n_heads % c->n_kv_heads == 0 && c->head_dim > 0 && c->head_dim % 2 == 0 &&
-         c->ffn > 0 && c->vocab > 0 && c->batch > 0 && c->seq > 0 && c->micro > 0;
+         c->ffn > 0 && c->vocab > 0 && c->batch > 0 && c->seq > 0 && c->micro > 0 &&
+         c->n_experts >= 0 &&
+         (c->n_experts == 0 || (c->top_k >= 1 && c->top_k <= c->n_experts && c->expert_ffn > 0));
 }
 
 Block make_block(const or_cfg* c, int j) {
@@ -104,6 +111,9 @@ Block make_block(const or_cfg* c, int j) {
   const int64_t F = c->ffn, V = c->vocab, L = c->n_layers;
   std::vector<std::pair<int64_t, int64_t>> shapes;
   if (j == 0) shapes = {{V, H}};
+  else if (j <= L && c->n_experts > 0)
+    shapes = {{(nh + 2 * nkv) * hd, H}, {H, nh * hd}, {c->n_experts, H},
+              {c->n_experts, 3 * (int64_t)c->expert_ffn * H}, {H, 1}, {H, 1}};
   else if (j <= L) shapes = {{(nh + 2 * nkv) * hd, H}, {H, nh * hd}, {2 * F, H}, {H, F}, {H, 1}, {H, 1}};
   else shapes = {{H, 1}, {V, H}};
   Block b;
@@ -379,6 +389,150 @@ double cross_entropy(const S* logits, const int32_t* tok, int64_t n_seq, int64_t
 }
 
 // ---------------------------------------------------------------------------
+// Routed mixture-of-experts feed-forward ([Lilting] MoE section: per token the
+// router picks a few of the experts; GPT-OSS-style layer).  Readings where the
+// pages are silent: router logits = yn Wr^T with no bias; the selected experts
+// of token t are its top_k largest logits, equal logits ordered by lower
+// expert index; gates = softmax over the selected logits only; expert e is the
+// same SwiGLU MLP as the dense layer with its own weights; no auxiliary
+// (load-balancing) loss term:
+//   x2_t = x1_t + sum_i gate_ti FFN_{e_ti}(yn_t),
+//   FFN_e(y) = (silu(y Wg_e^T) * (y Wu_e^T)) Wd_e^T.
+// The rows routed to expert e are processed as one matrix, in ascending
+// (token, slot) order.  Backward: dgate_ti = dx2_t . FFN_e(yn_t); the
+// expert's output rows get dY = gate_ti dx2_t; softmax over the selected set
+// gives dlogit_{t,e_i} = gate_ti (dgate_ti - sum_l gate_tl dgate_tl) and zero
+// for the others; the selection itself has no gradient.  An expert no token
+// was routed to gets a zero gradient.
+// ---------------------------------------------------------------------------
+template <class S>
+struct MoeLayer {
+  int64_t T, H, E, k, Fe;
+  std::vector<int32_t> idx;                 // [T][k]
+  std::vector<S> gate;                      // [T][k]
+  std::vector<int64_t> pos;                 // row of assignment t*k+i inside its expert's rows
+  std::vector<std::vector<int64_t>> rows;   // per expert: its assignments t*k+i, ascending
+  std::vector<std::vector<S>> X, GU, Hh, Y; // per expert, one row per routed assignment
+  double min_margin = INFINITY;
+
+  const S* wgu(const S* We, int64_t e) const { return We + e * 3 * Fe * H; }
+  const S* wd(const S* We, int64_t e) const { return We + e * 3 * Fe * H + 2 * Fe * H; }
+
+  void forward(const S* yn, const S* x1, const S* Wr, const S* We, S* out) {
+    std::vector<S> lg((size_t)(T * E));
+    linear_fwd(yn, Wr, T, E, H, lg.data());
+    idx.assign((size_t)(T * k), 0);
+    gate.assign((size_t)(T * k), (S)0);
+    pos.assign((size_t)(T * k), 0);
+    rows.assign((size_t)E, {});
+    std::vector<int64_t> ord((size_t)E);
+    for (int64_t t = 0; t < T; ++t) {
+      const S* l = lg.data() + t * E;
+      for (int64_t e = 0; e < E; ++e) ord[(size_t)e] = e;
+      std::stable_sort(ord.begin(), ord.end(), [&](int64_t a, int64_t b) { return (double)l[a] > (double)l[b]; });
+      if (k < E) min_margin = std::min(min_margin, (double)l[ord[(size_t)k - 1]] - (double)l[ord[(size_t)k]]);
+      const double mx = (double)l[ord[0]];
+      double den = 0;
+      for (int64_t i = 0; i < k; ++i) den += std::exp((double)l[ord[(size_t)i]] - mx);
+      for (int64_t i = 0; i < k; ++i) {
+        const int64_t e = ord[(size_t)i];
+        idx[(size_t)(t * k + i)] = (int32_t)e;
+        gate[(size_t)(t * k + i)] = (S)(std::exp((double)l[e] - mx) / den);
+        pos[(size_t)(t * k + i)] = (int64_t)rows[(size_t)e].size();
+        rows[(size_t)e].push_back(t * k + i);
+      }
+    }
+    X.assign((size_t)E, {}); GU.assign((size_t)E, {}); Hh.assign((size_t)E, {}); Y.assign((size_t)E, {});
+    for (int64_t e = 0; e < E; ++e) {
+      const int64_t n = (int64_t)rows[(size_t)e].size();
+      if (!n) continue;
+      auto& Xe = X[(size_t)e];
+      Xe.resize((size_t)(n * H));
+      for (int64_t r = 0; r < n; ++r) {
+        const int64_t t = rows[(size_t)e][(size_t)r] / k;
+        std::copy(yn + t * H, yn + (t + 1) * H, Xe.begin() + r * H);
+      }
+      GU[(size_t)e].resize((size_t)(n * 2 * Fe));
+      Hh[(size_t)e].resize((size_t)(n * Fe));
+      Y[(size_t)e].resize((size_t)(n * H));
+      linear_fwd(Xe.data(), wgu(We, e), n, 2 * Fe, H, GU[(size_t)e].data());
+      swiglu_fwd(GU[(size_t)e].data(), n, Fe, Hh[(size_t)e].data());
+      linear_fwd(Hh[(size_t)e].data(), wd(We, e), n, H, Fe, Y[(size_t)e].data());
+    }
+    for (int64_t t = 0; t < T; ++t)
+      for (int64_t h = 0; h < H; ++h) {
+        double s = (double)x1[t * H + h];
+        for (int64_t i = 0; i < k; ++i) {
+          const int64_t a = t * k + i;
+          s += (double)gate[(size_t)a] * (double)Y[(size_t)idx[(size_t)a]][(size_t)(pos[(size_t)a] * H + h)];
+        }
+        out[t * H + h] = (S)s;
+      }
+  }
+
+  // dout = d loss / d x2; writes dyn (the part through this feed-forward),
+  // dWr and every expert's slice of dWe (zeros for experts with no rows).
+  void backward(const S* yn, const S* Wr, const S* We, const S* dout, S* dyn, S* dWr, S* dWe) const {
+    std::vector<double> acc((size_t)(T * H), 0.0);
+    std::vector<double> dgate((size_t)(T * k), 0.0);
+    for (int64_t a = 0; a < T * k; ++a) {
+      const int64_t t = a / k;
+      const S* y = Y[(size_t)idx[(size_t)a]].data() + pos[(size_t)a] * H;
+      double s = 0;
+      for (int64_t h = 0; h < H; ++h) s += (double)dout[t * H + h] * (double)y[h];
+      dgate[(size_t)a] = s;
+    }
+    std::fill(dWe, dWe + E * 3 * Fe * H, (S)0);
+    for (int64_t e = 0; e < E; ++e) {
+      const int64_t n = (int64_t)rows[(size_t)e].size();
+      if (!n) continue;
+      std::vector<S> dY((size_t)(n * H)), dH((size_t)(n * Fe)), dGU((size_t)(n * 2 * Fe)), dX((size_t)(n * H));
+      for (int64_t r = 0; r < n; ++r) {
+        const int64_t a = rows[(size_t)e][(size_t)r], t = a / k;
+        for (int64_t h = 0; h < H; ++h) dY[(size_t)(r * H + h)] = (S)((double)gate[(size_t)a] * (double)dout[t * H + h]);
+      }
+      S* gwgu = dWe + e * 3 * Fe * H;
+      S* gwd = gwgu + 2 * Fe * H;
+      linear_wgrad(dY.data(), Hh[(size_t)e].data(), n, H, Fe, gwd);
+      linear_dgrad(dY.data(), wd(We, e), n, H, Fe, dH.data());
+      swiglu_bwd(GU[(size_t)e].data(), dH.data(), n, Fe, dGU.data());
+      linear_wgrad(dGU.data(), X[(size_t)e].data(), n, 2 * Fe, H, gwgu);
+      linear_dgrad(dGU.data(), wgu(We, e), n, 2 * Fe, H, dX.data());
+      for (int64_t r = 0; r < n; ++r) {
+        const int64_t t = rows[(size_t)e][(size_t)r] / k;
+        for (int64_t h = 0; h < H; ++h) acc[(size_t)(t * H + h)] += (double)dX[(size_t)(r * H + h)];
+      }
+    }
+    std::vector<S> dl((size_t)(T * E), (S)0), tmp((size_t)(T * H));
+    for (int64_t t = 0; t < T; ++t) {
+      double s = 0;
+      for (int64_t i = 0; i < k; ++i) s += (double)gate[(size_t)(t * k + i)] * dgate[(size_t)(t * k + i)];
+      for (int64_t i = 0; i < k; ++i) {
+        const int64_t a = t * k + i;
+        dl[(size_t)(t * E + idx[(size_t)a])] = (S)((double)gate[(size_t)a] * (dgate[(size_t)a] - s));
+      }
+    }
+    linear_wgrad(dl.data(), yn, T, E, H, dWr);
+    linear_dgrad(dl.data(), Wr, T, E, H, tmp.data());
+    for (int64_t i = 0; i < T * H; ++i) dyn[i] = (S)(acc[(size_t)i] + (double)tmp[(size_t)i]);
+  }
+};
+
+double g_last_margin = INFINITY;
+
+template <class S>
+double moe_layer(int64_t T, int64_t H, int64_t E, int64_t k, int64_t Fe, const S* yn, const S* x1, const S* Wr,
+                 const S* We, const S* dout, S* out, S* dyn, S* dWr, S* dWe, int32_t* idx, S* gate) {
+  if (T < 0 || H <= 0 || E <= 0 || k < 1 || k > E || Fe <= 0) return NAN;
+  MoeLayer<S> m{T, H, E, k, Fe};
+  m.forward(yn, x1, Wr, We, out);
+  m.backward(yn, Wr, We, dout, dyn, dWr, dWe);
+  std::copy(m.idx.begin(), m.idx.end(), idx);
+  std::copy(m.gate.begin(), m.gate.end(), gate);
+  return m.min_margin;
+}
+
+// ---------------------------------------------------------------------------
 // One training step: embedding -> L decoder blocks -> final RMSNorm + LM head
 // -> loss, then the backward in reverse.  Decoder block (pre-RMSNorm):
 //   xn = RMSNorm(x, g1); [q|k|v] = xn Wqkv^T; RoPE(q, k); a = Attn(q, k, v)
@@ -403,13 +557,17 @@ struct Model {
 
   struct LayerActs {
     std::vector<S> x, xn, r1, qkv, a, lse, x1, yn, r2, gu, h;
+    MoeLayer<S> moe;
   };
+  bool moe() const { return c.n_experts > 0; }
+  double min_margin = INFINITY;
 
   void layer_fwd(const S* const* W, int j, const std::vector<S>& x, LayerActs& A, std::vector<S>& out) {
     A.x = x;
     A.xn.resize(T * H); A.r1.resize(T); A.qkv.resize(T * ldq); A.a.resize(T * nh * hd);
     A.lse.resize(T * nh); A.x1.resize(T * H); A.yn.resize(T * H); A.r2.resize(T);
-    A.gu.resize(T * 2 * F); A.h.resize(T * F); out.resize(T * H);
+    if (!moe()) { A.gu.resize(T * 2 * F); A.h.resize(T * F); }
+    out.resize(T * H);
     rmsnorm_fwd(x.data(), ten(W, j, 4), T, H, c.rms_eps, A.xn.data(), A.r1.data());
     linear_fwd(A.xn.data(), ten(W, j, 0), T, ldq, H, A.qkv.data());
     rope(A.qkv.data(), nseq, Sq, ldq, nh + nkv, hd, c.rope_base, 0);  // q heads then k heads
@@ -418,6 +576,12 @@ struct Model {
     linear_fwd(A.a.data(), ten(W, j, 1), T, H, nh * hd, tmp.data());
     for (int64_t i = 0; i < T * H; ++i) A.x1[i] = (S)((double)x[i] + (double)tmp[i]);
     rmsnorm_fwd(A.x1.data(), ten(W, j, 5), T, H, c.rms_eps, A.yn.data(), A.r2.data());
+    if (moe()) {
+      A.moe = MoeLayer<S>{T, H, (int64_t)c.n_experts, (int64_t)c.top_k, (int64_t)c.expert_ffn};
+      A.moe.forward(A.yn.data(), A.x1.data(), ten(W, j, 2), ten(W, j, 3), out.data());
+      min_margin = std::min(min_margin, A.moe.min_margin);
+      return;
+    }
     linear_fwd(A.yn.data(), ten(W, j, 2), T, 2 * F, H, A.gu.data());
     swiglu_fwd(A.gu.data(), T, F, A.h.data());
     linear_fwd(A.h.data(), ten(W, j, 3), T, H, F, tmp.data());
@@ -426,14 +590,19 @@ struct Model {
 
   // dx: in = dL/dx2, out = dL/dx (the layer input).
   void layer_bwd(const S* const* W, S* const* G, int j, const LayerActs& A, std::vector<S>& dx) {
-    std::vector<S> dh(T * F), dgu(T * 2 * F), dyn(T * H), dx1(T * H), tmp(T * H), da(T * nh * hd);
+    std::vector<S> dh(moe() ? 0 : T * F), dgu(moe() ? 0 : T * 2 * F), dyn(T * H), dx1(T * H), tmp(T * H), da(T * nh * hd);
     std::vector<S> dqkv(T * ldq), dxn(T * H);
-    // x2 = x1 + h Wd^T
-    linear_wgrad(dx.data(), A.h.data(), T, H, F, ten(G, j, 3));
-    linear_dgrad(dx.data(), ten(W, j, 3), T, H, F, dh.data());
-    swiglu_bwd(A.gu.data(), dh.data(), T, F, dgu.data());
-    linear_wgrad(dgu.data(), A.yn.data(), T, 2 * F, H, ten(G, j, 2));
-    linear_dgrad(dgu.data(), ten(W, j, 2), T, 2 * F, H, dyn.data());
+    if (moe()) {
+      // x2 = x1 + sum_i gate_i FFN_{e_i}(yn)
+      A.moe.backward(A.yn.data(), ten(W, j, 2), ten(W, j, 3), dx.data(), dyn.data(), ten(G, j, 2), ten(G, j, 3));
+    } else {
+      // x2 = x1 + h Wd^T
+      linear_wgrad(dx.data(), A.h.data(), T, H, F, ten(G, j, 3));
+      linear_dgrad(dx.data(), ten(W, j, 3), T, H, F, dh.data());
+      swiglu_bwd(A.gu.data(), dh.data(), T, F, dgu.data());
+      linear_wgrad(dgu.data(), A.yn.data(), T, 2 * F, H, ten(G, j, 2));
+      linear_dgrad(dgu.data(), ten(W, j, 2), T, 2 * F, H, dyn.data());
+    }
     rmsnorm_bwd(dyn.data(), A.x1.data(), ten(W, j, 5), A.r2.data(), T, H, tmp.data(), ten(G, j, 5));
     for (int64_t i = 0; i < T * H; ++i) dx1[i] = (S)((double)dx[i] + (double)tmp[i]);
     // x1 = x + a Wo^T
@@ -457,6 +626,7 @@ struct Model {
   double step(const S* const* W, const int32_t* tok, S* const* G) {
     for (int j = 0; j < L + 2; ++j) std::fill(G[j], G[j] + lay[j].n_pad, (S)0);
     std::vector<S> x;
+    min_margin = INFINITY;
     embed(W, tok, x);
     std::vector<LayerActs> acts(L);
     for (int j = 1; j <= L; ++j) {
@@ -481,11 +651,13 @@ struct Model {
     for (int64_t t = 0; t < T; ++t)
       for (int64_t i = 0; i < H; ++i) acc[(int64_t)tok[t] * H + i] += (double)dx[t * H + i];
     for (size_t i = 0; i < acc.size(); ++i) dE[i] = (S)acc[i];
+    g_last_margin = min_margin;
     return loss;
   }
 
   double forward_hidden(const S* const* W, const int32_t* tok, int jstop, S* out) {
     std::vector<S> x;
+    min_margin = INFINITY;
     embed(W, tok, x);
     for (int j = 1; j <= jstop && j <= L; ++j) {
       LayerActs A;
@@ -494,6 +666,7 @@ struct Model {
       x.swap(y);
     }
     std::copy(x.begin(), x.end(), out);
+    g_last_margin = min_margin;
     return 0.0;
   }
 };
@@ -638,6 +811,19 @@ double or_forward_hidden_f(const or_cfg* c, const float* const* W, const int32_t
   return m.forward_hidden(W, tok, j, out);
 }
 
+double or_last_route_margin(void) { return g_last_margin; }
+
+double or_moe_layer_d(int64_t T, int64_t H, int64_t E, int64_t k, int64_t Fe, const double* yn, const double* x1,
+                      const double* Wr, const double* We, const double* dout, double* out, double* dyn, double* dWr,
+                      double* dWe, int32_t* idx, double* gate) {
+  return moe_layer(T, H, E, k, Fe, yn, x1, Wr, We, dout, out, dyn, dWr, dWe, idx, gate);
+}
+double or_moe_layer_f(int64_t T, int64_t H, int64_t E, int64_t k, int64_t Fe, const float* yn, const float* x1,
+                      const float* Wr, const float* We, const float* dout, float* out, float* dyn, float* dWr,
+                      float* dWe, int32_t* idx, float* gate) {
+  return moe_layer(T, H, E, k, Fe, yn, x1, Wr, We, dout, out, dyn, dWr, dWe, idx, gate);
+}
+
 // Adam (Kingma and Ba 2015, Algorithm 1) on FP32 master weights with the
 // gradient taken from its BF16 copy; then the BF16 working weights are
 // re-derived from the master by round-to-nearest-even.  [Review] 3-2 (6) puts
@@ -765,6 +951,21 @@ int64_t or_protocol(const or_cfg* c, int32_t n_steps, int32_t n_slabs, int32_t c
       if (writes_x && ckpt_on_host) log.op("C", "WAIT_XS", j % 2, -1);
       static const char* names[4] = {"FWD", "HEAD", "RECOMP", "BWD"};
       log.op("C", names[V.kind], j, b);
+      if (V.kind == 0 && j >= 1 && c->n_experts > 0) {
+        // MoE forward: compute records Route-Ready after the router's per-expert
+        // token counts reached the host; the host reads them and queues the
+        // routed experts' copy into the same buffer on W, which records
+        // Experts-Ready; compute waits for it and runs the experts.  In the
+        // backward (and recompute) the forward's routing is known, so the
+        // experts come with the shared weights in the visit's H2D.
+        log.op("C", "REC_RT", j, -1);
+        log.op("H", "WAIT_RT", j, -1);
+        if (jit_pack) log.op("H", "PACK_EXP", j, b);
+        log.op("W", "H2D_EXP", j, b);
+        log.op("W", "REC_ER", b, -1);
+        log.op("C", "WAIT_ER", b, -1);
+        log.op("C", "FWD_EXP", j, b);
+      }
       const bool saves_x = writes_x && j < L && j % ci == 0 && ckpt_on_host;
       if (saves_x) log.op("C", "REC_XR", j % 2, -1);
       if (V.kind == 0 || V.kind == 2) {

@@ -34,6 +34,10 @@ typedef struct {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
   int32_t batch, seq, micro;       /* tokens per step = micro*batch*seq        */
   double rope_base, rms_eps, init_std;
+  /* Routed mixture of experts in place of every decoder MLP ([Lilting] MoE
+   * section, GPT-OSS-style): n_experts > 0 experts of hidden size expert_ffn,
+   * top_k of them per token; n_experts = 0 keeps the dense SwiGLU MLP. */
+  int32_t n_experts, top_k, expert_ffn;
 } or_cfg;
 
 /* ---- layout ([Hotdry] host memory layout; [Review] 3-2 (4)) ---- */
@@ -87,6 +91,24 @@ double or_step_fwd_bwd_d(const or_cfg* c, const double* const* W, const int32_t*
 double or_forward_hidden_f(const or_cfg* c, const float* const* W, const int32_t* tok, int32_t j,
                            float* out);
 
+/* Smallest routing margin of the last or_step_* / or_forward_hidden_f call:
+ * over every MoE layer and token, the k-th largest router logit minus the
+ * (k+1)-th (+inf when no layer selects, i.e. dense or top_k = n_experts). */
+double or_last_route_margin(void);
+/* The MoE feed-forward of one layer on its own ("d": fp64 throughout, "f":
+ * fp32 storage with double sums): given the normalised input yn [T, H], the
+ * residual x1 [T, H], router weights Wr [E, H], experts We [E][W_gu (2Fe x H)
+ * | W_d (H x Fe)] and the output gradient dout [T, H], writes
+ * out = x1 + sum_i gate_i FFN_{e_i}(yn), dyn = d loss / d yn, dWr, dWe (every
+ * expert; zero where no token was routed), the selected experts idx [T, k]
+ * and their gates [T, k]; returns the smallest routing margin. */
+double or_moe_layer_d(int64_t T, int64_t H, int64_t E, int64_t k, int64_t Fe, const double* yn,
+                      const double* x1, const double* Wr, const double* We, const double* dout, double* out,
+                      double* dyn, double* dWr, double* dWe, int32_t* idx, double* gate);
+double or_moe_layer_f(int64_t T, int64_t H, int64_t E, int64_t k, int64_t Fe, const float* yn,
+                      const float* x1, const float* Wr, const float* We, const float* dout, float* out,
+                      float* dyn, float* dWr, float* dWe, int32_t* idx, float* gate);
+
 /* ---- Adam ([Review] 3-2 (6); [Lilting] memory table) ---- */
 /* The same with an FP32 gradient g32 (g_bf16 unused when g32 is given). */
 void or_adam_f32(int64_t n, const float* g32, const uint16_t* g_bf16, float* master, float* m, float* v,
@@ -102,7 +124,10 @@ void or_adam(int64_t n, const uint16_t* g_bf16, float* master, float* m, float* 
  * ckpt_interval c in [1, n_layers]: X_s is kept for s = 0, c, 2c, ... and the
  * backward recomputes each c-layer segment from it ([Review] 2, block-wise
  * recomputation); n_buffers in {1, 2} device weight buffers; n_passes passes
- * per step (one per micro-batch with host FP32 gradient accumulation, else 1). */
+ * per step (one per micro-batch with host FP32 gradient accumulation, else 1).
+ * MoE layers ([Lilting] MoE section: only the experts the router selected are
+ * copied in) split each forward visit: the shared weights first, the routed
+ * experts after the host has read the router's choice. */
 int64_t or_protocol(const or_cfg* c, int32_t n_steps, int32_t n_slabs, int32_t ckpt_on_host,
                     int32_t jit_pack, int32_t ckpt_interval, int32_t n_buffers, int32_t n_passes, char* buf,
                     int64_t cap);

@@ -18,6 +18,10 @@ those sentences forbid is ordered:
   * D2H into slab k after the previous host job (Adam or FP32 accumulation)
     on slab k, the job after the D2H;
   * next step's pack / H2D of block j after block j's Adam;
+  * MoE forward (lilting.ch, MoE section: only the routed experts are copied):
+    the host reads the router's choice only after compute recorded it, the
+    experts' copy into b follows every earlier use of b, and compute runs the
+    experts only after that copy;
   * checkpoint slots: write after the previous save, save after the write;
     a host checkpoint is loaded only after it was saved and saved again only
     after its last load; a device checkpoint slot is refilled only after the
@@ -54,6 +58,8 @@ def check(lines: list[str]) -> None:
     ev: dict[str, Clock] = {}
     last_buf_use: dict[int, list] = {0: [], 1: []}     # ops that read/wrote device buffer b
     visit_h2d: dict[int, tuple] = {}                   # this visit's H2D into b
+    exp_h2d: dict[int, tuple] = {}                     # this visit's routed-expert H2D into b
+    route_rec: dict[int, tuple] = {}                   # compute's Route-Ready record of layer j
     slot_read: dict[int, tuple] = {}                   # compute that last read checkpoint slot q
     slot_load: dict[int, tuple] = {}                   # H2D_CKPT that last filled slot q
     slot_of_layer: dict[int, int] = {}                 # layer whose input X_{j-1} sits in slot q
@@ -85,6 +91,8 @@ def check(lines: list[str]) -> None:
             name = op[4:] + str(a)
             me = tick(s)
             ev[name] = me[1]
+            if op == "REC_RT":
+                route_rec[a] = me
             continue
         if s == "H":
             if op == "WAIT_ADAM":
@@ -92,6 +100,11 @@ def check(lines: list[str]) -> None:
                 clk["H"].merge(adam_done[a][1])
             elif op == "WAIT_STAGE":
                 clk["H"].merge(ev["WR" + str(a)])
+            elif op == "WAIT_RT":
+                clk["H"].merge(ev["RT" + str(a)])
+            elif op == "PACK_EXP":
+                me = tick("H")
+                assert _hb(route_rec.get(a), me) and a in route_rec, "experts packed before routing: " + where
             elif op == "PACK":
                 me = tick("H")
                 assert _hb(stage_read.get(b), me), "pack overwrites staging still being copied: " + where
@@ -120,6 +133,20 @@ def check(lines: list[str]) -> None:
             visit_h2d[b] = me
             stage_read[b] = me
             last_buf_use[b] = [me]
+        elif op == "H2D_EXP":
+            assert a in route_rec and _hb(route_rec[a], me), "experts copied before the routing was read: " + where
+            for u in last_buf_use[b]:
+                assert _hb(u, me), "expert H2D overwrites buffer still in use: " + where
+            if a in adam_done:
+                assert _hb(adam_done[a], me), "expert H2D of a block before its Adam: " + where
+            exp_h2d[b] = me
+            last_buf_use[b].append(me)
+        elif op == "FWD_EXP":
+            assert b in exp_h2d and _hb(exp_h2d[b], me), "experts computed before they arrived: " + where
+            for u in last_buf_use[b]:
+                assert _hb(u, me), "expert compute overlaps earlier use of buffer: " + where
+            last_buf_use[b] = [me]
+            del exp_h2d[b]
         elif op == "H2D_CKPT":
             assert (a - 1) in ckpt_saved, "checkpoint loaded that was never saved: " + where
             assert _hb(ckpt_saved[a - 1], me), "checkpoint loaded before its save finished: " + where
