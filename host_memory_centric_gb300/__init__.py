@@ -44,7 +44,8 @@ class MtConfig(C.Structure):
                 ("beta2", C.c_float), ("adam_eps", C.c_float), ("weight_decay", C.c_float),
                 ("seed", C.c_uint64), ("timeout_ms", C.c_uint32), ("pin_store", C.c_int32),
                 ("head_chunk", C.c_int32), ("log_protocol", C.c_int32), ("keep_host_grad", C.c_int32),
-                ("n_buffers", C.c_int32), ("host_grad_accum", C.c_int32)]
+                ("n_buffers", C.c_int32), ("host_grad_accum", C.c_int32), ("n_experts", C.c_int32),
+                ("top_k", C.c_int32), ("expert_ffn", C.c_int32)]
 
 
 class DevRegion(C.Structure):
@@ -131,6 +132,8 @@ def lib():
         "mt_cross_entropy": (i32, [_v, _v, i64, i32, f32, _v, _v]),
         "mt_kernel_error": (i32, [_P(i32), i32]),
         "mt_fault_inject": (i32, [i32, i32]),
+        "mt_moe_scratch_bytes": (sz, [i64, i32, i32, i32, i32]),
+        "mt_moe_ffn": (i32, [_v, _v, _v, _v, _v, i64, i32, i32, i32, i32, _v, _v, _v, _v, _v, _v, _v, sz, _v]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -153,6 +156,8 @@ def make_config(shape: dict, **rt) -> MtConfig:
     for k in ("n_layers", "hidden", "n_heads", "n_kv_heads", "head_dim", "ffn", "vocab", "batch", "seq"):
         setattr(c, k, int(shape[k]))
     c.micro_batches = int(shape.get("micro", shape.get("micro_batches", 1)))
+    for k in ("n_experts", "top_k", "expert_ffn"):
+        setattr(c, k, int(shape.get(k, 0)))
     for k in ("rope_base", "rms_eps", "init_std", "lr", "beta1", "beta2", "adam_eps", "weight_decay"):
         if k in shape:
             setattr(c, k, float(shape[k]))

@@ -20,7 +20,7 @@ CUDA = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA, "bin", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-CU_SRCS = ["k_gemm.cu", "k_attention.cu", "k_attention_tc.cu", "k_elementwise.cu", "k_noalloc.cu"]
+CU_SRCS = ["k_gemm.cu", "k_attention.cu", "k_attention_tc.cu", "k_elementwise.cu", "k_noalloc.cu", "k_moe.cu"]
 CPP_SRCS = ["mt_runtime.cpp", "mt_host.cpp"]
 HEADERS = ["mt_kernels.h", "mt_host.h"]
 

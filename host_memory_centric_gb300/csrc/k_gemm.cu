@@ -53,15 +53,29 @@ struct Epi {
   int a_mn, b_mn;
 };
 
+constexpr int MAX_EXPERT_GROUPS = 128;
+
 // Up to two independent GEMMs ("groups") share one persistent launch: their
 // output tiles form one list, so the tail of one fills SMs the other leaves
-// idle.
+// idle.  Two expert-grouped forms serve a routed mixture-of-experts layer
+// (rows of A sorted by expert, each expert's rows padded to whole 128-row
+// tiles):
+//   mode 1: B is a 3-D tensor [expert][N][K] (or [expert][K][N]) and M-tile
+//           tm multiplies expert tile_expert[tm] (< 0: no rows, skipped);
+//   mode 2: ngrp products D_g = A_g^T B_g over row ranges of A and B (both
+//           MN-major): group g covers rows [grp_k0[g], grp_k0[g] + 64 grp_nk[g])
+//           and writes D + grp_e[g] * d_estride (the weight gradient of expert
+//           grp_e[g]).
 struct Params {
   CUtensorMap ta[2], tb[2];
   Epi e[2];
   int ngroups;
   int tile_start[3];  // tiles of group g are [tile_start[g], tile_start[g+1])
   int stall;          // test hook: the producer issues nothing, so the consumers' bounded waits run out
+  const int* tile_expert;
+  int64_t d_estride;
+  int ngrp;
+  int grp_e[MAX_EXPERT_GROUPS], grp_k0[MAX_EXPERT_GROUPS], grp_nk[MAX_EXPERT_GROUPS];
 };
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
@@ -105,6 +119,14 @@ __device__ __forceinline__ void tma_load(const CUtensorMap* map, uint64_t* bar, 
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
       "l"((uint64_t)map), "r"(x), "r"(y), "r"(su32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load3(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y,
+                                          int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(su32(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(su32(bar))
       : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
@@ -228,17 +250,19 @@ __device__ __forceinline__ void epi_store(const Epi& e, int row, int col, const 
 }
 
 // Producer side of one output tile: its K-blocks into the shared-memory ring.
+// z >= 0: B is a 3-D map and z its expert coordinate; koff is added to every
+// K coordinate (the first row of a K-group).
 template <bool A_MN, bool B_MN>
 __device__ __forceinline__ bool produce_tile(const CUtensorMap* tmA, const CUtensorMap* tmB, int tm, int tn, int nk,
                                              uint8_t* sA, uint8_t* sB, uint64_t* full, uint64_t* empty, int& stage,
                                              uint32_t& phase, volatile int* abort_flag, uint32_t& inflight_mask,
-                                             uint32_t& inflight_parity) {
+                                             uint32_t& inflight_parity, int z = -1, int koff = 0) {
   for (int kb = 0; kb < nk; ++kb) {
     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) return false;
     mbar_expect_tx(&full[stage], STAGE_BYTES);
     uint8_t* a = sA + stage * A_BYTES;
     uint8_t* b = sB + stage * B_BYTES;
-    const int k0 = kb * BK;
+    const int k0 = koff + kb * BK;
     if (!A_MN) {
       tma_load(tmA, &full[stage], a, k0, tm * BM);
     } else {
@@ -246,10 +270,14 @@ __device__ __forceinline__ bool produce_tile(const CUtensorMap* tmA, const CUten
       tma_load(tmA, &full[stage], a + CHUNK_BYTES, tm * BM + 64, k0);
     }
     if (!B_MN) {
-      tma_load(tmB, &full[stage], b, k0, tn * BN);
+      if (z >= 0) tma_load3(tmB, &full[stage], b, k0, tn * BN, z);
+      else tma_load(tmB, &full[stage], b, k0, tn * BN);
     } else {
 #pragma unroll
-      for (int c = 0; c < BN / 64; ++c) tma_load(tmB, &full[stage], b + c * CHUNK_BYTES, tn * BN + 64 * c, k0);
+      for (int c = 0; c < BN / 64; ++c) {
+        if (z >= 0) tma_load3(tmB, &full[stage], b + c * CHUNK_BYTES, tn * BN + 64 * c, k0, z);
+        else tma_load(tmB, &full[stage], b + c * CHUNK_BYTES, tn * BN + 64 * c, k0);
+      }
     }
     inflight_mask |= 1u << stage;
     inflight_parity = (inflight_parity & ~(1u << stage)) | (phase << stage);
@@ -298,8 +326,35 @@ __device__ __forceinline__ void epilogue_tile(const Epi& e, int local, uint32_t 
   }
 }
 
-// NG groups (1 or 2) with compile-time majorness (A0, B0) and (A1, B1).
-template <int NG, bool A0, bool B0, bool A1, bool B1>
+// Where output tile `tile` of an expert-grouped launch (MODE 1 or 2) lives:
+// its local tile index and epilogue, the expert coordinate of B (mode 1), the
+// K offset and K-block count.  False: the tile has no rows (mode 1).
+template <int MODE>
+__device__ __forceinline__ bool grouped_tile(const Params& p, int tile, int& local, int& z, int& koff, int& nk,
+                                             Epi& e) {
+  e = p.e[0];
+  if (MODE == 1) {
+    int tm, tn;
+    tile_mn(tile, e, tm, tn);
+    z = p.tile_expert[tm];
+    local = tile;
+    koff = 0;
+    nk = (e.K + BK - 1) / BK;
+    return z >= 0;
+  }
+  const int per = e.tiles_m * e.tiles_n;
+  const int g = tile / per;
+  local = tile - g * per;
+  z = -1;
+  koff = p.grp_k0[g];
+  nk = p.grp_nk[g];
+  e.D += (int64_t)p.grp_e[g] * p.d_estride;
+  return true;
+}
+
+// NG groups (1 or 2) with compile-time majorness (A0, B0) and (A1, B1);
+// MODE 0 plain, 1 and 2 the expert-grouped forms (NG = 1).
+template <int NG, bool A0, bool B0, bool A1, bool B1, int MODE = 0>
 __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -354,7 +409,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok && !p.stall; tile += gridDim.x) {
         int tm, tn;
-        if (NG == 1 || tile < split) {
+        if (MODE != 0) {
+          int local, z, koff, nk;
+          Epi e;
+          if (!grouped_tile<MODE>(p, tile, local, z, koff, nk, e)) continue;
+          tile_mn(local, e, tm, tn);
+          ok = produce_tile<A0, B0>(&p.ta[0], &p.tb[0], tm, tn, nk, sA, sB, full, empty, stage, phase, abort_flag,
+                                    inflight_mask, inflight_parity, z, koff);
+        } else if (NG == 1 || tile < split) {
           tile_mn(tile, p.e[0], tm, tn);
           ok = produce_tile<A0, B0>(&p.ta[0], &p.tb[0], tm, tn, (p.e[0].K + BK - 1) / BK, sA, sB, full, empty, stage,
                                     phase, abort_flag, inflight_mask, inflight_parity);
@@ -372,16 +434,25 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        int gnk = 0;
+        if (MODE != 0) {
+          int local, z, koff;
+          Epi e;
+          if (!grouped_tile<MODE>(p, tile, local, z, koff, gnk, e)) continue;
+        }
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
+        ++it;
         if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
-        if (NG == 1 || tile < split)
+        if (MODE != 0)
+          ok = mma_tile<A0, B0>(d, gnk, sA, sB, full, empty, stage, phase, abort_flag);
+        else if (NG == 1 || tile < split)
           ok = mma_tile<A0, B0>(d, (p.e[0].K + BK - 1) / BK, sA, sB, full, empty, stage, phase, abort_flag);
         else
           ok = mma_tile<A1, B1>(d, (p.e[1].K + BK - 1) / BK, sA, sB, full, empty, stage, phase, abort_flag);
@@ -395,9 +466,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
     const int row_in_tile = q * 32 + lane;
     int it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      int local = tile;
+      Epi ge;
+      if (MODE != 0) {
+        int z, koff, nk;
+        if (!grouped_tile<MODE>(p, tile, local, z, koff, nk, ge)) continue;
+      }
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
+      ++it;
       // warp-uniform outcome: the TMEM loads below are warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, abort_flag))) {
         ok = false;
@@ -405,7 +483,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
       }
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      if (NG == 1 || tile < split) epilogue_tile(p.e[0], tile, taddr, row_in_tile);
+      if (MODE != 0) epilogue_tile(ge, local, taddr, row_in_tile);
+      else if (NG == 1 || tile < split) epilogue_tile(p.e[0], tile, taddr, row_in_tile);
       else epilogue_tile(p.e[1], tile - split, taddr, row_in_tile);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
@@ -452,7 +531,10 @@ void init_once() {
                            (const void*)gemm_kernel<1, false, true, false, false>,
                            (const void*)gemm_kernel<1, true, false, false, false>,
                            (const void*)gemm_kernel<1, true, true, false, false>,
-                           (const void*)gemm_kernel<2, true, true, false, true>};
+                           (const void*)gemm_kernel<2, true, true, false, true>,
+                           (const void*)gemm_kernel<1, false, false, false, false, 1>,
+                           (const void*)gemm_kernel<1, false, true, false, false, 1>,
+                           (const void*)gemm_kernel<1, true, true, false, false, 2>};
   for (const void* k : kernels) {
     const cudaError_t a = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (a != cudaSuccess) g_init_err = a;
@@ -467,6 +549,20 @@ bool make_map(CUtensorMap* m, const bf16* base, int64_t rows, int64_t cols, int6
   const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<bf16*>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D bf16 tensor map of n experts' row-major [rows][cols] matrices (row
+// stride ld, expert stride estride, in elements), box {64, box_rows, 1}.
+bool make_map3(CUtensorMap* m, const bf16* base, int64_t rows, int64_t cols, int64_t ld, int64_t n,
+               int64_t estride, int box_rows) {
+  const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)n};
+  const cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)estride * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<bf16*>(base), dims, strides, box,
                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -543,6 +639,78 @@ cudaError_t launch(const GemmArgs* gs, int n, cudaStream_t s) {
 }  // namespace
 
 cudaError_t gemm(const GemmArgs& g, cudaStream_t s) { return launch(&g, 1, s); }
+
+namespace {
+void fill_epi(Epi* e, int M, int N, int K, bf16* D, int64_t ldd) {
+  std::memset(e, 0, sizeof *e);
+  e->D = D; e->ldd = ldd;
+  e->M = M; e->N = N; e->K = K;
+  e->tiles_m = (M + BM - 1) / BM;
+  e->tiles_n = (N + BN - 1) / BN;
+  e->group_m = 16;
+}
+}  // namespace
+
+cudaError_t gemm_expert_rows(const GemmRowsArgs& g, cudaStream_t s) {
+  std::call_once(g_once, init_once);
+  if (g_init_err != cudaSuccess) return g_init_err;
+  if (g.M < 0 || g.M % BM || g.N <= 0 || g.K <= 0 || g.n_experts <= 0 || !g.A || !g.B || !g.D || !g.tile_expert)
+    return cudaErrorInvalidValue;
+  if (g.lda % 8 || g.ldb % 8 || g.ldd % 8 || g.b_estride % 8 || !al16(g.A) || !al16(g.B) || !al16(g.D))
+    return cudaErrorInvalidValue;
+  if (g.M == 0) return cudaSuccess;
+  Params p;
+  std::memset(&p, 0, sizeof p);
+  bool ok = make_map(&p.ta[0], g.A, g.M, g.K, g.lda, BM);
+  ok = ok && (g.b_mn ? make_map3(&p.tb[0], g.B, g.K, g.N, g.ldb, g.n_experts, g.b_estride, BK)
+                     : make_map3(&p.tb[0], g.B, g.N, g.K, g.ldb, g.n_experts, g.b_estride, BN));
+  if (!ok) return cudaErrorInvalidValue;
+  fill_epi(&p.e[0], g.M, g.N, g.K, g.D, g.ldd);
+  p.e[0].b_mn = g.b_mn ? 1 : 0;
+  p.ngroups = 1;
+  p.tile_start[1] = p.e[0].tiles_m * p.e[0].tiles_n;
+  p.tile_expert = g.tile_expert;
+  p.stall = gemm_stall_take();
+  const int tiles = p.tile_start[1];
+  const int grid = tiles < g_num_sms ? tiles : g_num_sms;
+  if (g.b_mn) gemm_kernel<1, false, true, false, false, 1><<<grid, THREADS, SMEM_BYTES, s>>>(p);
+  else gemm_kernel<1, false, false, false, false, 1><<<grid, THREADS, SMEM_BYTES, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t gemm_expert_kgroups(const GemmKGroupArgs& g, cudaStream_t s) {
+  std::call_once(g_once, init_once);
+  if (g_init_err != cudaSuccess) return g_init_err;
+  if (g.M <= 0 || g.N <= 0 || g.R <= 0 || g.ngrp < 0 || g.ngrp > MAX_EXPERT_GROUPS || !g.A || !g.B || !g.D)
+    return cudaErrorInvalidValue;
+  if (g.lda % 8 || g.ldb % 8 || g.ldd % 8 || g.d_estride % 8 || !al16(g.A) || !al16(g.B) || !al16(g.D))
+    return cudaErrorInvalidValue;
+  if (g.ngrp == 0) return cudaSuccess;
+  Params p;
+  std::memset(&p, 0, sizeof p);
+  for (int i = 0; i < g.ngrp; ++i) {
+    if (g.grp_klen[i] <= 0 || g.grp_klen[i] % BK || g.grp_k0[i] < 0 || g.grp_k0[i] % BK ||
+        g.grp_k0[i] + g.grp_klen[i] > g.R || g.grp_e[i] < 0)
+      return cudaErrorInvalidValue;
+    p.grp_e[i] = g.grp_e[i];
+    p.grp_k0[i] = g.grp_k0[i];
+    p.grp_nk[i] = g.grp_klen[i] / BK;
+  }
+  p.ngrp = g.ngrp;
+  p.d_estride = g.d_estride;
+  bool ok = make_map(&p.ta[0], g.A, g.R, g.M, g.lda, BK) && make_map(&p.tb[0], g.B, g.R, g.N, g.ldb, BK);
+  if (!ok) return cudaErrorInvalidValue;
+  fill_epi(&p.e[0], g.M, g.N, g.R, g.D, g.ldd);
+  p.e[0].a_mn = 1;
+  p.e[0].b_mn = 1;
+  p.ngroups = 1;
+  p.tile_start[1] = g.ngrp * p.e[0].tiles_m * p.e[0].tiles_n;
+  p.stall = gemm_stall_take();
+  const int tiles = p.tile_start[1];
+  const int grid = tiles < g_num_sms ? tiles : g_num_sms;
+  gemm_kernel<1, true, true, false, false, 2><<<grid, THREADS, SMEM_BYTES, s>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t gemm_pair(const GemmArgs& g0, const GemmArgs& g1, cudaStream_t s) {
   // one launch for the (wgrad, dgrad) form: A and B MN-major, then B MN-major

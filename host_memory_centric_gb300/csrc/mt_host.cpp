@@ -22,6 +22,14 @@ bool config_valid(const mt_config* c, std::string* why) {
   if (c->n_buffers != 1 && c->n_buffers != 2) return bad("n_buffers must be 1 or 2");
   if (c->host_grad_accum != 0 && c->host_grad_accum != 1) return bad("host_grad_accum must be 0 or 1");
   if (c->n_grad_slabs < 1 || c->n_grad_slabs > 256) return bad("n_grad_slabs out of range");
+  if (c->n_experts < 0) return bad("n_experts must be >= 0");
+  if (c->n_experts > 0) {
+    if (c->n_experts > 128 || c->n_experts % 8) return bad("n_experts must be a multiple of 8 and <= 128");
+    if (c->top_k < 1 || c->top_k > 8 || c->top_k > c->n_experts) return bad("top_k must be in [1, min(8, n_experts)]");
+    if (c->expert_ffn <= 0 || c->expert_ffn % 64 || c->hidden % 64)
+      return bad("expert_ffn and hidden must be positive multiples of 64 with experts");
+    if (c->host_grad_accum) return bad("host_grad_accum is not supported with experts");
+  }
   if (c->timeout_ms == 0) return bad("timeout_ms must be positive");
   if (!(c->rms_eps > 0) || !(c->rope_base > 1)) return bad("rms_eps / rope_base");
   return true;
@@ -44,6 +52,15 @@ std::vector<BlockDesc> build_layout(const mt_config* c) {
     int n = 0;
     if (j == 0) {
       shapes[n][0] = V; shapes[n++][1] = H;                      // E
+    } else if (j <= L && c->n_experts > 0) {
+      // routed MoE block; row e of W_experts = expert e's W_gu [2Fe, H] then
+      // W_down [H, Fe], so one expert is one contiguous range
+      shapes[n][0] = (nh + 2 * nkv) * hd; shapes[n++][1] = H;    // W_qkv
+      shapes[n][0] = H; shapes[n++][1] = nh * hd;                // W_o
+      shapes[n][0] = c->n_experts; shapes[n++][1] = H;           // W_router
+      shapes[n][0] = c->n_experts; shapes[n++][1] = 3 * (int64_t)c->expert_ffn * H;  // W_experts
+      shapes[n][0] = H; shapes[n++][1] = 1;                      // gamma1
+      shapes[n][0] = H; shapes[n++][1] = 1;                      // gamma2
     } else if (j <= L) {
       shapes[n][0] = (nh + 2 * nkv) * hd; shapes[n++][1] = H;    // W_qkv
       shapes[n][0] = H; shapes[n++][1] = nh * hd;                // W_o
@@ -162,7 +179,12 @@ void adam(int64_t n, const uint16_t* __restrict g, uint16_t* __restrict gcopy, f
   const float step = (float)((double)lr / bc1);
   const float isb2 = (float)(1.0 / std::sqrt(bc2));
   const float c1 = 1.0f - b1, c2 = 1.0f - b2, lrwd = lr * wd;
-  if (gcopy) {
+  if (!g) {  // zero gradient (an expert no token was routed to)
+    for (int64_t i = 0; i < n; ++i) {
+      if (gcopy) gcopy[i] = 0;
+      w[i] = adam_elem(0.0f, th[i], m[i], v[i], b1, c1, b2, c2, step, isb2, eps, lrwd);
+    }
+  } else if (gcopy) {
     for (int64_t i = 0; i < n; ++i) {
       const uint16_t gb = g[i];
       gcopy[i] = gb;

@@ -46,7 +46,8 @@ float bf16_val(uint16_t b);
 void init_block(const mt_config* c, const BlockDesc& b, int j, float* master, int64_t e0, int64_t e1);
 // Adam over [0, n) (FP32 arithmetic) on gradient g (BF16); when gcopy is not
 // null the gradient is also written there (the slab unpack into the store's G
-// region, fused into the same pass).
+// region, fused into the same pass).  g == nullptr: a zero gradient (the
+// experts of an MoE layer that no token was routed to).
 void adam(int64_t n, const uint16_t* g, uint16_t* gcopy, float* th, float* m, float* v, uint16_t* w, int32_t t,
           float lr, float b1, float b2, float eps, float wd);
 // Host gradient accumulation over micro-batch passes: acc = float(g) on the

@@ -34,6 +34,32 @@ cudaError_t gemm(const GemmArgs& g, cudaStream_t s);
 // schedule); same requirements as gemm() for each.
 cudaError_t gemm_pair(const GemmArgs& g0, const GemmArgs& g1, cudaStream_t s);
 int gemm_num_sms();
+// Expert-grouped GEMMs of a routed mixture-of-experts layer, whose rows are
+// sorted by expert with every expert's rows padded to whole 128-row tiles.
+// Rows form: D[r, n] = sum_k A[r, k] B_e(n, k), e = tile_expert[r / 128]
+// (device array; tiles with e < 0 are skipped and D's rows there untouched);
+// B_e = B + e * b_estride, [N][K] (ldb) or, with b_mn, [K][N].  M = rows of A
+// and D, a multiple of 128.
+struct GemmRowsArgs {
+  const bf16* A; int64_t lda;
+  const bf16* B; int64_t ldb; int b_mn; int64_t b_estride; int n_experts;
+  const int* tile_expert;
+  int M, N, K;
+  bf16* D; int64_t ldd;
+};
+cudaError_t gemm_expert_rows(const GemmRowsArgs& g, cudaStream_t s);
+// K-group form (the experts' weight gradients): for group i,
+// D + grp_e[i] * d_estride ([M][N], ldd) = A_i^T B_i, where A_i and B_i are
+// rows [grp_k0[i], grp_k0[i] + grp_klen[i]) of A ([R][M], lda) and B ([R][N],
+// ldb); k0 and klen multiples of 64; at most 128 groups (host arrays).
+struct GemmKGroupArgs {
+  const bf16* A; int64_t lda;
+  const bf16* B; int64_t ldb;
+  int M, N, R;
+  bf16* D; int64_t ldd; int64_t d_estride;
+  int ngrp; const int* grp_e; const int* grp_k0; const int* grp_klen;
+};
+cudaError_t gemm_expert_kgroups(const GemmKGroupArgs& g, cudaStream_t s);
 // Test hook: the next `launches` GEMM launches issue no loads, so their bounded
 // waits expire and they report through the kernel error word.
 void gemm_inject_stall(int launches);
@@ -88,6 +114,44 @@ cudaError_t reduce_sum(const float* x, int64_t n, float scale, float* out, cudaS
 cudaError_t f32_to_bf16_2d(const float* x, int64_t ldx, int64_t rows, int64_t cols, bf16* y,
                            int64_t ldy, float scale, cudaStream_t s);
 cudaError_t add_bf16(const bf16* a, const bf16* b, int64_t n, bf16* y, cudaStream_t s);
+
+// ---------------------------------------------------------------- routed MoE
+// Device arrays of one MoE layer's routing (k_moe.cu).  T tokens, E experts
+// (<= 128), k <= 8 of them per token.
+struct MoePlan {
+  int32_t* idx;          // [T][k] selected experts, descending logit
+  float* gate;           // [T][k] softmax over the selected logits
+  int32_t* slot_row;     // [T][k] row of assignment (t, i) in the expert-sorted layout
+  int32_t* cnt;          // [moe_chunks(T)][E] scratch
+  int32_t* base;         // [moe_chunks(T)][E] scratch
+  int32_t* counts;       // [E] tokens routed to each expert
+  int32_t* tile_expert;  // [moe_rows_max / 128] expert of each 128-row tile, -1 past the end
+  int32_t* perm_tok;     // [moe_rows_max] token of each sorted row, -1 on padding rows
+};
+// Rows of the expert-sorted layout in the worst case (every expert's segment
+// padded to a multiple of 128), and the counting sort's chunk count.
+int64_t moe_rows_max(int64_t T, int E, int k);
+int64_t moe_chunks(int64_t T);
+// From FP32 router logits [T][E]: top-k (ties: lower expert index), gates,
+// per-expert counts, segment layout (expert e's rows start at the sum of the
+// earlier experts' counts rounded up to 128; rows of one expert in ascending
+// (token, slot) order), perm_tok, slot_row and tile_expert.
+cudaError_t moe_plan(const float* logits, int64_t T, int E, int k, const MoePlan& p, cudaStream_t s);
+// xperm[r] = yn[perm_tok[r]] ([R][H]); padding rows zero.
+cudaError_t moe_gather(const bf16* yn, int H, const int32_t* perm_tok, int64_t R, bf16* xperm, cudaStream_t s);
+// out[t] = x1[t] + sum_i gate[t, i] Y[slot_row[t, i]].
+cudaError_t moe_combine(const bf16* x1, const bf16* Y, const int32_t* slot_row, const float* gate, int64_t T, int H,
+                        int k, bf16* out, cudaStream_t s);
+// dY[slot_row[t, i]] = gate[t, i] dout[t]; dlogits [T][E] (BF16) =
+// gradient of the router logits through the softmax over the selected ones.
+cudaError_t moe_combine_bwd(const bf16* dout, const bf16* Y, const int32_t* slot_row, const int32_t* idx,
+                            const float* gate, int64_t T, int H, int k, int E, bf16* dY, bf16* dlogits,
+                            cudaStream_t s);
+// Zero the padding rows (perm_tok < 0) of buf [R][cols].
+cudaError_t moe_zero_pad(bf16* buf, int cols, const int32_t* perm_tok, int64_t R, cudaStream_t s);
+// dyn[t] = sum_i dX[slot_row[t, i]].
+cudaError_t moe_scatter(const bf16* dX, const int32_t* slot_row, int64_t T, int H, int k, bf16* dyn,
+                        cudaStream_t s);
 
 // ---------------------------------------------------------------- attention
 // Causal grouped-query attention over n_seq sequences of S tokens.  qkv rows

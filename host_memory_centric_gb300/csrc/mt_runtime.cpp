@@ -49,7 +49,71 @@ cudaError_t pinned_alloc(void** p, size_t bytes) {
 
 struct Job {
   int32_t block, slab, t, pass;  // pass < passes - 1: FP32 accumulation only
+  std::vector<uint8_t> routed;   // MoE block: 1 for each expert some token was routed to
 };
+
+// Device workspace of a routed MoE layer (expert-sorted rows, R_max of them).
+struct MoeWs {
+  mt::MoePlan p{};
+  float* logits = nullptr;  // [T][E] router logits, FP32
+  bf16 *xperm = nullptr, *gu = nullptr, *h = nullptr, *y = nullptr, *dy = nullptr, *dh = nullptr,
+       *dgu = nullptr, *dlog = nullptr;
+};
+struct MoeShape {
+  int64_t T;
+  int H, E, k, Fe;
+};
+// Host view of one layer's routing: sorted rows in use and, per routed expert,
+// its segment (the K-groups of the expert weight gradients).
+struct MoeRoute {
+  int64_t R = 0, assigned = 0;
+  std::vector<int> e, k0, klen;
+};
+MoeRoute route_from_counts(const int32_t* counts, int E) {
+  MoeRoute r;
+  int64_t row = 0;
+  for (int e = 0; e < E; ++e) {
+    const int64_t n = counts[e], pad = (n + 127) / 128 * 128;
+    if (n > 0) {
+      r.e.push_back(e);
+      r.k0.push_back((int)row);
+      r.klen.push_back((int)pad);
+    }
+    row += pad;
+    r.assigned += n;
+  }
+  r.R = row;
+  return r;
+}
+// Carves an MoE workspace for T tokens from base (sizes only when null).
+size_t moe_carve(const MoeShape& q, uint8_t* base, MoeWs* w) {
+  size_t off = 0;
+  auto take = [&](int64_t bytes) -> uint8_t* {
+    off = (off + 255) / 256 * 256;
+    uint8_t* p = base ? base + off : nullptr;
+    off += (size_t)bytes;
+    return p;
+  };
+  const int64_t R = mt::moe_rows_max(q.T, q.E, q.k), nch = mt::moe_chunks(q.T), T = q.T;
+  w->logits = (float*)take(T * q.E * 4);
+  w->p.idx = (int32_t*)take(T * q.k * 4);
+  w->p.gate = (float*)take(T * q.k * 4);
+  w->p.slot_row = (int32_t*)take(T * q.k * 4);
+  w->p.cnt = (int32_t*)take(nch * q.E * 4);
+  w->p.base = (int32_t*)take(nch * q.E * 4);
+  w->p.counts = (int32_t*)take(q.E * 4);
+  w->p.tile_expert = (int32_t*)take(R / 128 * 4);
+  w->p.perm_tok = (int32_t*)take(R * 4);
+  w->xperm = (bf16*)take(R * q.H * 2);
+  w->y = (bf16*)take(R * q.H * 2);
+  w->dy = (bf16*)take(R * q.H * 2);
+  w->gu = (bf16*)take(R * 2 * q.Fe * 2);
+  w->dgu = (bf16*)take(R * 2 * q.Fe * 2);
+  w->h = (bf16*)take(R * q.Fe * 2);
+  w->dh = (bf16*)take(R * q.Fe * 2);
+  w->dlog = (bf16*)take(T * q.E * 2);
+  return (off + 255) / 256 * 256;
+}
 
 struct Dev {
   uint8_t* buf[2] = {nullptr, nullptr};
@@ -63,6 +127,7 @@ struct Dev {
   float *rstd1 = nullptr, *rstd2 = nullptr, *lse = nullptr, *delta = nullptr,
         *row_loss = nullptr, *loss = nullptr, *rms_part = nullptr, *dwacc = nullptr, *cs = nullptr;
   int32_t *tok = nullptr, *tgt = nullptr, *csr_start = nullptr, *csr_rows = nullptr;
+  MoeWs moe;  // routed MoE layers only
 };
 
 // One visit of the step: 0 FWD, 1 HEAD (fused forward and backward), 2 RECOMP
@@ -108,6 +173,9 @@ struct Pending {
 struct mt_model {
   mt_config c{};
   int L = 0, H = 0, nh = 0, nkv = 0, hd = 0, F = 0, V = 0, B = 0, S = 0, M = 0, Nqkv = 0;
+  bool moe = false;           // decoder blocks are routed mixtures of experts
+  int E = 0, topk = 0, Fe = 0;
+  int32_t* hcounts = nullptr; // pinned [L+2][E]: per-expert token counts of each MoE layer's forward
   int64_t T = 0, chunk = 0;
   std::vector<mth::BlockDesc> lay;
   std::vector<VisitDesc> plan;
@@ -134,6 +202,7 @@ struct mt_model {
   size_t dev_bytes = 0, dev_used = 0;
   cudaStream_t sc = nullptr, sw = nullptr, sg = nullptr;
   cudaEvent_t WR[2] = {}, BD[2] = {}, BF[2] = {}, XR[2] = {}, XS[2] = {}, TOK = nullptr, LOSS = nullptr;
+  cudaEvent_t RT = nullptr, ER[2] = {};  // MoE: Route-Ready (counts on the host), Experts-Ready[b]
   std::vector<cudaEvent_t> SR;
   // host workers
   mth::Pool pool;
@@ -265,10 +334,16 @@ size_t carve(const mt_config* c, const std::vector<mth::BlockDesc>& lay, uint8_t
   d->dqkv = (bf16*)take(T * Nqkv * 2);
   d->attn = (bf16*)take(T * nh * hd * 2);
   d->dattn = (bf16*)take(T * nh * hd * 2);
-  d->gu = (bf16*)take(T * 2 * F * 2);
-  d->dgu = (bf16*)take(T * 2 * F * 2);
-  d->h = (bf16*)take(T * F * 2);
-  d->dh = (bf16*)take(T * F * 2);
+  if (c->n_experts > 0) {
+    const MoeShape q{T, (int)H, c->n_experts, c->top_k, c->expert_ffn};
+    uint8_t* w = take((int64_t)moe_carve(q, nullptr, &d->moe));
+    moe_carve(q, w, &d->moe);
+  } else {
+    d->gu = (bf16*)take(T * 2 * F * 2);
+    d->dgu = (bf16*)take(T * 2 * F * 2);
+    d->h = (bf16*)take(T * F * 2);
+    d->dh = (bf16*)take(T * F * 2);
+  }
   d->logits = (bf16*)take(chunk * V * 2);
   d->rstd1 = (float*)take(T * 4);
   d->rstd2 = (float*)take(T * 4);
@@ -304,7 +379,7 @@ struct Timed {
   cudaEvent_t a = nullptr;
   // nk = kernels the timed call launches
   Timed(mt_model* mm, int k, double f, double b, int n = 1) : m(mm), kind(k), nk(n), flops(f), bytes(b) {
-    if (m->timing) {
+    if (m && m->timing) {
       a = take_event(m);
       cudaEventRecord(a, m->sc);
     }
@@ -369,6 +444,113 @@ mt_status wgrad_dgrad(mt_model* m, const bf16* dY, const bf16* X, const bf16* W,
   return gemm_run2(m, wgrad_args(dY, X, T, N, K, dW, acc, acc_mode), dgrad_args(dY, W, T, N, K, dX));
 }
 
+// ---------------------------------------------------------------- routed MoE block math
+// [Lilting] MoE section: the router picks each token's experts; the layer is
+// read as the GPT-OSS-style top-k mixture (softmax over the selected logits,
+// SwiGLU experts, no router bias).  Router logits in FP32, then the routing
+// plan (top-k, gates, expert-sorted rows).
+mt_status moe_route(mt_model* m, const MoeShape& q, const MoeWs& w, const bf16* yn, const bf16* Wr, cudaStream_t s) {
+  {
+    Timed t(m, K_GEMM, 2.0 * q.T * q.E * q.H, 0);
+    CU(m, mt::gemm(mt::GemmArgs{yn, q.H, 0, Wr, q.H, 0, (int)q.T, q.E, q.H, nullptr, 0, nullptr, 0, w.logits, q.E, 1},
+                   s));
+  }
+  Timed t(m, K_OTHER, 0, 4.0 * q.T * q.E + 16.0 * q.T * q.k, 4);
+  CU(m, mt::moe_plan(w.logits, q.T, q.E, q.k, w.p, s));
+  return MT_OK;
+}
+
+// The routed experts over the sorted rows: gather, W_gu, SwiGLU, W_down, and
+// out = x1 + gate-weighted sum (skipped when out is null: the backward's
+// recompute only rebuilds what the backward reads).
+mt_status moe_experts_fwd(mt_model* m, const MoeShape& q, const MoeWs& w, const MoeRoute& r, const bf16* yn,
+                          const bf16* x1, const bf16* We, bf16* out, cudaStream_t s) {
+  const int64_t est = 3LL * q.Fe * q.H;
+  const double rows = (double)r.assigned;
+  {
+    Timed t(m, K_OTHER, 0, 4.0 * r.R * q.H);
+    CU(m, mt::moe_gather(yn, q.H, w.p.perm_tok, r.R, w.xperm, s));
+  }
+  {
+    Timed t(m, K_GEMM, 4.0 * rows * q.Fe * q.H, 0);
+    CU(m, mt::gemm_expert_rows(mt::GemmRowsArgs{w.xperm, q.H, We, q.H, 0, est, q.E, w.p.tile_expert, (int)r.R,
+                                                2 * q.Fe, q.H, w.gu, 2 * q.Fe},
+                               s));
+  }
+  {
+    Timed t(m, K_OTHER, 0, 6.0 * r.R * q.Fe);
+    CU(m, mt::swiglu_fwd(w.gu, r.R, q.Fe, w.h, s));
+  }
+  {
+    Timed t(m, K_GEMM, 2.0 * rows * q.H * q.Fe, 0);
+    CU(m, mt::gemm_expert_rows(mt::GemmRowsArgs{w.h, q.Fe, We + 2LL * q.Fe * q.H, q.Fe, 0, est, q.E,
+                                                w.p.tile_expert, (int)r.R, q.H, q.Fe, w.y, q.H},
+                               s));
+  }
+  if (out) {
+    Timed t(m, K_OTHER, 0, 4.0 * q.T * q.H + 2.0 * rows * q.H);
+    CU(m, mt::moe_combine(x1, w.y, w.p.slot_row, w.p.gate, q.T, q.H, q.k, out, s));
+  }
+  return MT_OK;
+}
+
+// Backward of the MoE feed-forward from dout = dL/dx2: dyn = dL/dyn, the
+// router gradient dWr and the routed experts' gradients in dWe (experts with
+// no rows are not written).
+mt_status moe_backward(mt_model* m, const MoeShape& q, const MoeWs& w, const MoeRoute& r, const bf16* yn,
+                       const bf16* Wr, const bf16* We, const bf16* dout, bf16* dyn, bf16* dWr, bf16* dWe,
+                       cudaStream_t s) {
+  const int64_t est = 3LL * q.Fe * q.H;
+  const double rows = (double)r.assigned;
+  const int ng = (int)r.e.size();
+  {
+    Timed t(m, K_OTHER, 0, 4.0 * q.T * q.H + 4.0 * rows * q.H + 2.0 * q.T * q.E, 2);
+    CU(m, mt::moe_combine_bwd(dout, w.y, w.p.slot_row, w.p.idx, w.p.gate, q.T, q.H, q.k, q.E, w.dy, w.dlog, s));
+    CU(m, mt::moe_zero_pad(w.dy, q.H, w.p.perm_tok, r.R, s));
+  }
+  {  // dW_down_e = dY_e^T h_e
+    Timed t(m, K_GEMM, 2.0 * rows * q.H * q.Fe, 0);
+    CU(m, mt::gemm_expert_kgroups(mt::GemmKGroupArgs{w.dy, q.H, w.h, q.Fe, q.H, q.Fe, (int)r.R,
+                                                     dWe + 2LL * q.Fe * q.H, q.Fe, est, ng, r.e.data(), r.k0.data(),
+                                                     r.klen.data()},
+                                  s));
+  }
+  {  // dh = dY W_down_e
+    Timed t(m, K_GEMM, 2.0 * rows * q.H * q.Fe, 0);
+    CU(m, mt::gemm_expert_rows(mt::GemmRowsArgs{w.dy, q.H, We + 2LL * q.Fe * q.H, q.Fe, 1, est, q.E,
+                                                w.p.tile_expert, (int)r.R, q.Fe, q.H, w.dh, q.Fe},
+                               s));
+  }
+  {
+    Timed t(m, K_OTHER, 0, 10.0 * r.R * q.Fe);
+    CU(m, mt::swiglu_bwd(w.gu, w.dh, r.R, q.Fe, w.dgu, s));
+  }
+  {  // dW_gu_e = dGU_e^T xperm_e
+    Timed t(m, K_GEMM, 4.0 * rows * q.Fe * q.H, 0);
+    CU(m, mt::gemm_expert_kgroups(mt::GemmKGroupArgs{w.dgu, 2 * q.Fe, w.xperm, q.H, 2 * q.Fe, q.H, (int)r.R, dWe,
+                                                     q.H, est, ng, r.e.data(), r.k0.data(), r.klen.data()},
+                                  s));
+  }
+  {  // dX = dGU W_gu_e, into dy (free by now)
+    Timed t(m, K_GEMM, 4.0 * rows * q.Fe * q.H, 0);
+    CU(m, mt::gemm_expert_rows(mt::GemmRowsArgs{w.dgu, 2 * q.Fe, We, q.H, 1, est, q.E, w.p.tile_expert, (int)r.R,
+                                                q.H, 2 * q.Fe, w.dy, q.H},
+                               s));
+  }
+  {
+    Timed t(m, K_OTHER, 0, 2.0 * rows * q.H + 2.0 * q.T * q.H);
+    CU(m, mt::moe_scatter(w.dy, w.p.slot_row, q.T, q.H, q.k, dyn, s));
+  }
+  {  // router: dWr = dlogits^T yn; dyn += dlogits Wr
+    Timed t(m, K_GEMM, 4.0 * q.T * q.E * q.H, 0, 2);
+    CU(m, mt::gemm(mt::GemmArgs{w.dlog, q.E, 1, yn, q.H, 1, q.E, q.H, (int)q.T, dWr, q.H, nullptr, 0, nullptr, 0, 0},
+                   s));
+    CU(m, mt::gemm(mt::GemmArgs{w.dlog, q.E, 0, Wr, q.H, 1, (int)q.T, q.H, q.E, dyn, q.H, dyn, q.H, nullptr, 0, 0},
+                   s));
+  }
+  return MT_OK;
+}
+
 struct View {
   const bf16* w[MT_MAX_TENSORS];
   bf16* g[MT_MAX_TENSORS];
@@ -402,12 +584,14 @@ bf16* x_seg_out(mt_model* m, int j) {  // recomputed X_j, s < j < e
 }
 
 // ---------------------------------------------------------------- block math
-// Decoder block forward (pre-RMSNorm, RoPE, GQA causal attention, SwiGLU).
-// With `recompute`, everything the backward reads is rebuilt and the final
-// projection is skipped.
-mt_status decoder_forward(mt_model* m, const View& v, const bf16* x, bf16* out, bool recompute) {
+MoeShape moe_shape(const mt_model* m) { return MoeShape{m->T, m->H, m->E, m->topk, m->Fe}; }
+MoeRoute moe_route_of(const mt_model* m, int j) { return route_from_counts(m->hcounts + (size_t)j * m->E, m->E); }
+
+// Attention half of a decoder block: xn, qkv, attention, x1 = x + attn W_o^T
+// and yn = RMSNorm(x1) (the MLP's or the experts' input).
+mt_status attention_half(mt_model* m, const View& v, const bf16* x) {
   const int64_t T = m->T;
-  const int H = m->H, F = m->F, nhd = m->nh * m->hd;
+  const int H = m->H, nhd = m->nh * m->hd;
   cudaStream_t s = m->sc;
   Dev& d = m->d;
   {
@@ -429,6 +613,25 @@ mt_status decoder_forward(mt_model* m, const View& v, const bf16* x, bf16* out, 
     Timed t(m, K_OTHER, 0, 4.0 * T * H + 4.0 * T);
     CU(m, mt::rmsnorm_fwd(d.x1, v.w[5], T, H, m->c.rms_eps, d.yn, d.rstd2, s));
   }
+  return MT_OK;
+}
+
+// Decoder block forward (pre-RMSNorm, RoPE, GQA causal attention, SwiGLU MLP
+// or routed experts).  With `recompute`, everything the backward reads is
+// rebuilt and the final projection / combine is skipped.  An MoE block here
+// has its experts resident (recompute and backward visits, which know the
+// forward's routing); the forward visit itself goes through moe_forward_visit.
+mt_status decoder_forward(mt_model* m, const View& v, const bf16* x, bf16* out, bool recompute, int j) {
+  const int64_t T = m->T;
+  const int H = m->H, F = m->F;
+  cudaStream_t s = m->sc;
+  Dev& d = m->d;
+  OK(attention_half(m, v, x));
+  if (m->moe) {
+    const MoeShape q = moe_shape(m);
+    OK(moe_route(m, q, d.moe, d.yn, v.w[2], s));
+    return moe_experts_fwd(m, q, d.moe, moe_route_of(m, j), d.yn, d.x1, v.w[3], recompute ? nullptr : out, s);
+  }
   OK(fprop(m, d.yn, v.w[2], T, 2 * F, H, d.gu, nullptr));
   {
     Timed t(m, K_OTHER, 0, 6.0 * T * F);
@@ -440,18 +643,23 @@ mt_status decoder_forward(mt_model* m, const View& v, const bf16* x, bf16* out, 
 
 // Recompute + backward of a decoder block.  dout = dL/dX_j (read), din =
 // dL/dX_{j-1} (written); weight gradients land in v.g[*].
-mt_status decoder_backward(mt_model* m, const View& v, const bf16* x, const bf16* dout, bf16* din) {
-  OK(decoder_forward(m, v, x, nullptr, true));
+mt_status decoder_backward(mt_model* m, const View& v, const bf16* x, const bf16* dout, bf16* din, int j) {
+  OK(decoder_forward(m, v, x, nullptr, true, j));
   const int64_t T = m->T;
   const int H = m->H, F = m->F, nhd = m->nh * m->hd;
   cudaStream_t s = m->sc;
   Dev& d = m->d;
-  OK(wgrad_dgrad(m, dout, d.h, v.w[3], T, H, F, v.g[3], d.dh));
-  {
-    Timed t(m, K_OTHER, 0, 10.0 * T * F);
-    CU(m, mt::swiglu_bwd(d.gu, d.dh, T, F, d.dgu, s));
+  if (m->moe) {
+    OK(moe_backward(m, moe_shape(m), d.moe, moe_route_of(m, j), d.yn, v.w[2], v.w[3], dout, d.dyn, v.g[2], v.g[3],
+                    s));
+  } else {
+    OK(wgrad_dgrad(m, dout, d.h, v.w[3], T, H, F, v.g[3], d.dh));
+    {
+      Timed t(m, K_OTHER, 0, 10.0 * T * F);
+      CU(m, mt::swiglu_bwd(d.gu, d.dh, T, F, d.dgu, s));
+    }
+    OK(wgrad_dgrad(m, d.dgu, d.yn, v.w[2], T, 2 * F, H, v.g[2], d.dyn));
   }
-  OK(wgrad_dgrad(m, d.dgu, d.yn, v.w[2], T, 2 * F, H, v.g[2], d.dyn));
   {
     Timed t(m, K_OTHER, 0, 8.0 * T * H + 4.0 * T, 2);
     CU(m, mt::rmsnorm_bwd(d.dyn, d.x1, v.w[5], d.rstd2, dout, T, H, d.dx1, v.g[5], d.rms_part, s));
@@ -582,12 +790,25 @@ void adam_loop(mt_model* m) {
       float* th = reinterpret_cast<float*>(blk + b.region[2]);
       float* mm = reinterpret_cast<float*>(blk + b.region[3]);
       float* vv = reinterpret_cast<float*>(blk + b.region[4]);
-      // work items: (tensor, chunk) ranges of at most 1 Mi elements
+      // work items: (tensor, chunk) ranges of at most 1 Mi elements; in an MoE
+      // block each expert's row is its own range, and an expert no token was
+      // routed to takes a zero gradient (its slab range was not exported)
       constexpr int64_t CH = 1 << 20;
-      std::vector<std::pair<int64_t, int64_t>> items;
+      struct Item {
+        int64_t o, n;
+        bool zero;
+      };
+      std::vector<Item> items;
+      auto add_range = [&](int64_t o, int64_t n, bool zero) {
+        for (int64_t e = 0; e < n; e += CH) items.push_back({o + e, (n - e) < CH ? (n - e) : CH, zero});
+      };
       for (int t = 0; t < b.nt; ++t) {
         const int64_t o = b.t[t].off, n = b.t[t].rows * b.t[t].cols;
-        for (int64_t e = 0; e < n; e += CH) items.push_back({o + e, (n - e) < CH ? (n - e) : CH});
+        if (!job.routed.empty() && t == 3) {
+          for (int64_t e = 0; e < b.t[t].rows; ++e) add_range(o + e * b.t[t].cols, b.t[t].cols, !job.routed[(size_t)e]);
+        } else {
+          add_range(o, n, false);
+        }
       }
       const mt_config& c = m->c;
       bool inject_throw = false;
@@ -599,10 +820,10 @@ void adam_loop(mt_model* m) {
       float* acc = m->gacc ? m->gacc + m->gacc_off[(size_t)job.block] : nullptr;
       std::function<void(int64_t)> fn = [&](int64_t i) {
         if (inject_throw && i == 0) throw std::runtime_error("injected host worker fault");
-        const int64_t o = items[(size_t)i].first, n = items[(size_t)i].second;
+        const int64_t o = items[(size_t)i].o, n = items[(size_t)i].n;
         if (!acc) {
-          mth::adam(n, slab + o, c.keep_host_grad ? G + o : nullptr, th + o, mm + o, vv + o, W + o, job.t, c.lr,
-                    c.beta1, c.beta2, c.adam_eps, c.weight_decay);
+          mth::adam(n, items[(size_t)i].zero ? nullptr : slab + o, c.keep_host_grad ? G + o : nullptr, th + o, mm + o,
+                    vv + o, W + o, job.t, c.lr, c.beta1, c.beta2, c.adam_eps, c.weight_decay);
         } else if (!last) {
           mth::accumulate(n, slab + o, acc + o, job.pass == 0);
         } else {
@@ -676,6 +897,54 @@ mt_status upload_tokens(mt_model* m, int p) {
   return MT_OK;
 }
 
+bool moe_block(const mt_model* m, int j) { return m->moe && j >= 1 && j <= m->L; }
+
+// Byte ranges, inside a block's W (or G) region, that a copy moves: the whole
+// region, or for an MoE block the shared tensors (`trunk`: everything but
+// W_experts) and/or the rows of the experts its forward routed tokens to
+// (`experts`, from the counts in hcounts; adjacent rows merged).
+struct Range {
+  int64_t off, bytes;
+};
+std::vector<Range> block_ranges(const mt_model* m, int j, bool trunk, bool experts) {
+  const mth::BlockDesc& bd = m->lay[(size_t)j];
+  if (!moe_block(m, j)) return {{0, bd.wbytes}};
+  const mth::TensorDesc& ex = bd.t[3];
+  const int64_t e0 = ex.off * 2, row = ex.cols * 2, e1 = e0 + ex.rows * row;
+  std::vector<Range> r;
+  auto add = [&](int64_t off, int64_t bytes) {
+    if (bytes <= 0) return;
+    if (!r.empty() && r.back().off + r.back().bytes == off) r.back().bytes += bytes;
+    else r.push_back({off, bytes});
+  };
+  if (trunk) add(0, e0);
+  if (experts) {
+    const int32_t* cnt = m->hcounts + (size_t)j * m->E;
+    for (int e = 0; e < m->E; ++e)
+      if (cnt[e] > 0) add(e0 + e * row, row);
+  }
+  if (trunk) add(e1, bd.wbytes - e1);
+  return r;
+}
+
+// Host copy of the given ranges of src into dst (the just-in-time pack into
+// pinned staging), in 8 MiB pieces on the worker pool.
+mt_status pack_ranges(mt_model* m, uint8_t* dst, const uint8_t* src, const std::vector<Range>& rg) {
+  const double t0 = now_ms();
+  constexpr int64_t CH = 8 << 20;
+  std::vector<Range> pieces;
+  for (const Range& r : rg)
+    for (int64_t o = 0; o < r.bytes; o += CH) pieces.push_back({r.off + o, std::min(CH, r.bytes - o)});
+  std::function<void(int64_t)> fn = [&](int64_t i) {
+    const Range& q = pieces[(size_t)i];
+    std::memcpy(dst + q.off, src + q.off, (size_t)q.bytes);
+  };
+  std::string werr;
+  if (!m->pool.parallel_for((int64_t)pieces.size(), fn, &werr)) return set_err(m, MT_ERR_INTERNAL, "pack: " + werr);
+  m->pack_ms += now_ms() - t0;
+  return MT_OK;
+}
+
 mt_status do_stream_in(mt_model* m, int j, int b) {
   const VisitDesc& vd = m->plan[(size_t)m->vis];
   const bool fwd = vd.kind <= V_HEAD;
@@ -686,35 +955,31 @@ mt_status do_stream_in(mt_model* m, int j, int b) {
     if (m->live) OK(wait_adam(m, j, m->steps_done));
   }
   const uint8_t* src = m->live ? m->store + bd.store_off + bd.region[0] : nullptr;
+  // an MoE block's forward copies the shared tensors now and the routed
+  // experts once the router has chosen; recompute and backward visits know
+  // the forward's routing and copy both
+  const std::vector<Range> rg = m->live ? block_ranges(m, j, true, !fwd) : std::vector<Range>{};
   if (copies && !m->c.pin_store) {
     if (m->used[b]) {
       logop(m, "H", "WAIT_STAGE", b, -1);
       if (m->live) OK(wait_event(m, m->WR[b], "staging free"));
+      if (m->live && m->moe) OK(wait_event(m, m->ER[b], "staging free (experts)"));
     }
     logop(m, "H", "PACK", j, b);
     if (m->live) {
-      const double t0 = now_ms();
-      uint8_t* dst = m->staging[b];
-      constexpr int64_t CH = 8 << 20;
-      const int64_t n = (bd.wbytes + CH - 1) / CH;
-      std::function<void(int64_t)> fn = [&](int64_t i) {
-        const int64_t o = i * CH, len = (bd.wbytes - o) < CH ? (bd.wbytes - o) : CH;
-        std::memcpy(dst + o, src + o, (size_t)len);
-      };
-      std::string werr;
-      if (!m->pool.parallel_for(n, fn, &werr)) return set_err(m, MT_ERR_INTERNAL, "pack: " + werr);
-      m->pack_ms += now_ms() - t0;
-      src = dst;
+      OK(pack_ranges(m, m->staging[b], src, rg));
+      src = m->staging[b];
     }
   }
   logop(m, "W", "WAIT_BF", b, -1);
   if (m->live) CU(m, cudaStreamWaitEvent(m->sw, m->BF[b], 0));
   if (copies) {
     logop(m, "W", "H2D", j, b);
-    if (m->live) {
-      CU(m, cudaMemcpyAsync(m->d.buf[b], src, (size_t)bd.wbytes, cudaMemcpyHostToDevice, m->sw));
-      m->h2d += bd.wbytes;
-    }
+    if (m->live)
+      for (const Range& r : rg) {
+        CU(m, cudaMemcpyAsync(m->d.buf[b] + r.off, src + r.off, (size_t)r.bytes, cudaMemcpyHostToDevice, m->sw));
+        m->h2d += r.bytes;
+      }
   }
   if (vd.first && m->c.ckpt_on_host) {
     // The segment's checkpoint X_s (s = j - 1) into slot seg % 2, after the
@@ -755,6 +1020,52 @@ mt_status do_bind(mt_model* m, int j, int b, mt_layer_view* out) {
   return MT_OK;
 }
 
+// Forward visit of an MoE block ([Lilting] MoE section: after the router has
+// chosen, only the chosen experts' parameters go to the GPU):
+//   compute: attention half, router, routing plan; the per-expert counts to
+//            pinned host memory; Route-Ready;
+//   host   : waits Route-Ready, reads which experts have tokens;
+//   weight : copies those experts' rows into buffer b; Experts-Ready[b];
+//   compute: waits Experts-Ready[b]; the experts and the combine.
+mt_status moe_forward_visit(mt_model* m, int j, int b) {
+  const View v = m->live ? make_view(m, j, b) : View{};
+  const MoeShape q = moe_shape(m);
+  if (m->live) {
+    OK(attention_half(m, v, x_fwd_in(m, j)));
+    OK(moe_route(m, q, m->d.moe, m->d.yn, v.w[2], m->sc));
+    CU(m, cudaMemcpyAsync(m->hcounts + (size_t)j * m->E, m->d.moe.p.counts, (size_t)m->E * 4, cudaMemcpyDeviceToHost,
+                          m->sc));
+  }
+  logop(m, "C", "REC_RT", j, -1);
+  if (m->live) CU(m, cudaEventRecord(m->RT, m->sc));
+  logop(m, "H", "WAIT_RT", j, -1);
+  if (m->live) OK(wait_event(m, m->RT, "routing"));
+  const mth::BlockDesc& bd = m->lay[(size_t)j];
+  const std::vector<Range> rg = m->live ? block_ranges(m, j, false, true) : std::vector<Range>{};
+  const uint8_t* src = m->live ? m->store + bd.store_off + bd.region[0] : nullptr;
+  if (!m->c.pin_store) {
+    logop(m, "H", "PACK_EXP", j, b);
+    if (m->live) {
+      OK(pack_ranges(m, m->staging[b], src, rg));
+      src = m->staging[b];
+    }
+  }
+  logop(m, "W", "H2D_EXP", j, b);
+  if (m->live)
+    for (const Range& r : rg) {
+      CU(m, cudaMemcpyAsync(m->d.buf[b] + r.off, src + r.off, (size_t)r.bytes, cudaMemcpyHostToDevice, m->sw));
+      m->h2d += r.bytes;
+    }
+  logop(m, "W", "REC_ER", b, -1);
+  if (m->live) CU(m, cudaEventRecord(m->ER[b], m->sw));
+  logop(m, "C", "WAIT_ER", b, -1);
+  if (m->live) CU(m, cudaStreamWaitEvent(m->sc, m->ER[b], 0));
+  logop(m, "C", "FWD_EXP", j, b);
+  if (m->live)
+    OK(moe_experts_fwd(m, q, m->d.moe, moe_route_of(m, j), m->d.yn, m->d.x1, v.w[3], x_out(m, j), m->sc));
+  return MT_OK;
+}
+
 mt_status do_forward(mt_model* m, int j, int b) {
   const bool head = j == m->L + 1;
   const bool writes_x = j <= m->L;
@@ -764,14 +1075,16 @@ mt_status do_forward(mt_model* m, int j, int b) {
     if (m->live) CU(m, cudaStreamWaitEvent(m->sc, m->XS[j % 2], 0));
   }
   logop(m, "C", head ? "HEAD" : "FWD", j, b);
-  if (m->live) {
+  if (moe_block(m, j)) {
+    OK(moe_forward_visit(m, j, b));
+  } else if (m->live) {
     const View v = make_view(m, j, b);
     if (j == 0) {
       OK(upload_tokens(m, m->pass));
       Timed t(m, K_OTHER, 0, 4.0 * m->T * m->H);
       CU(m, mt::embed_fwd(m->d.tok, v.w[0], m->T, m->H, m->V, x_out(m, 0), m->sc));
     } else if (!head) {
-      OK(decoder_forward(m, v, x_fwd_in(m, j), x_out(m, j), false));
+      OK(decoder_forward(m, v, x_fwd_in(m, j), x_out(m, j), false, j));
     } else {
       OK(head_forward_backward(m, v, x_fwd_in(m, j), m->d.dx[m->L % 2]));
     }
@@ -809,7 +1122,7 @@ mt_status do_forward(mt_model* m, int j, int b) {
 mt_status do_recompute(mt_model* m, int j, int b) {
   const int seg = m->plan[(size_t)m->vis].seg;
   logop(m, "C", "RECOMP", j, b);
-  if (m->live) OK(decoder_forward(m, make_view(m, j, b), x_seg_in(m, j, seg), x_seg_out(m, j), false));
+  if (m->live) OK(decoder_forward(m, make_view(m, j, b), x_seg_in(m, j, seg), x_seg_out(m, j), false, j));
   logop(m, "C", "REC_BF", b, -1);
   if (m->live) CU(m, cudaEventRecord(m->BF[b], m->sc));
   return MT_OK;
@@ -824,7 +1137,7 @@ mt_status do_backward(mt_model* m, int j, int b) {
       CU(m, mt::embed_bwd(m->d.csr_start, m->d.csr_rows, m->d.dx[0], m->V, m->H, v.g[0], m->sc));
     } else {
       const int seg = m->plan[(size_t)m->vis].seg;
-      OK(decoder_backward(m, v, x_seg_in(m, j, seg), m->d.dx[j % 2], m->d.dx[(j - 1) % 2]));
+      OK(decoder_backward(m, v, x_seg_in(m, j, seg), m->d.dx[j % 2], m->d.dx[(j - 1) % 2], j));
     }
   }
   logop(m, "C", "REC_BD", b, -1);
@@ -841,11 +1154,12 @@ mt_status do_stream_out(mt_model* m, int j, int b, int* slab_out) {
   if (m->live) OK(acquire_slab(m, &k));
   logop(m, "H", "ACQ_SLAB", k, -1);
   logop(m, "G", "D2H", j, k);
-  if (m->live) {
-    CU(m, cudaMemcpyAsync(m->slabs + (size_t)k * m->wb_max, m->d.buf[b] + bd.region[1], (size_t)bd.wbytes,
-                          cudaMemcpyDeviceToHost, m->sg));
-    m->d2h += bd.wbytes;
-  }
+  if (m->live)  // an MoE block exports the shared tensors and the routed experts only
+    for (const Range& r : block_ranges(m, j, true, true)) {
+      CU(m, cudaMemcpyAsync(m->slabs + (size_t)k * m->wb_max + r.off, m->d.buf[b] + bd.region[1] + r.off,
+                            (size_t)r.bytes, cudaMemcpyDeviceToHost, m->sg));
+      m->d2h += r.bytes;
+    }
   logop(m, "G", "REC_BF", b, -1);
   if (m->live) CU(m, cudaEventRecord(m->BF[b], m->sg));
   logop(m, "G", "REC_SR", k, -1);
@@ -859,7 +1173,12 @@ mt_status do_adam_enqueue(mt_model* m, int j, int k, int32_t t) {
   if (m->live) {
     {
       std::lock_guard<std::mutex> lk(m->amu);
-      m->jobs.push_back({j, k, t, m->pass});
+      Job job{j, k, t, m->pass, {}};
+      if (moe_block(m, j)) {
+        job.routed.resize((size_t)m->E);
+        for (int e = 0; e < m->E; ++e) job.routed[(size_t)e] = m->hcounts[(size_t)j * m->E + e] > 0;
+      }
+      m->jobs.push_back(std::move(job));
       m->inflight_jobs++;
     }
     m->acv.notify_all();
@@ -937,6 +1256,8 @@ void fill_shape(mt_model* m) {
   m->L = c.n_layers; m->H = c.hidden; m->nh = c.n_heads; m->nkv = c.n_kv_heads; m->hd = c.head_dim;
   m->F = c.ffn; m->V = c.vocab; m->B = c.batch; m->S = c.seq; m->M = c.micro_batches;
   m->Nqkv = (m->nh + 2 * m->nkv) * m->hd;
+  m->moe = c.n_experts > 0;
+  m->E = c.n_experts; m->topk = c.top_k; m->Fe = c.expert_ffn;
   m->T = mth::tokens_per_pass(&c);  // device tokens of one pass
   m->npass = mth::passes_per_step(&c);
   m->Mp = c.host_grad_accum ? 1 : c.micro_batches;
@@ -965,7 +1286,8 @@ mt_model::~mt_model() {
     if (sc) cudaStreamSynchronize(sc);
     if (sw) cudaStreamSynchronize(sw);
     if (sg) cudaStreamSynchronize(sg);
-    for (cudaEvent_t* e : {&WR[0], &WR[1], &BD[0], &BD[1], &BF[0], &BF[1], &XR[0], &XR[1], &XS[0], &XS[1], &TOK, &LOSS})
+    for (cudaEvent_t* e : {&WR[0], &WR[1], &BD[0], &BD[1], &BF[0], &BF[1], &XR[0], &XR[1], &XS[0], &XS[1], &TOK, &LOSS,
+                           &RT, &ER[0], &ER[1]})
       if (*e) cudaEventDestroy(*e);
     for (auto e : SR)
       if (e) cudaEventDestroy(e);
@@ -981,6 +1303,7 @@ mt_model::~mt_model() {
     if (ckpt) cudaFreeHost(ckpt);
     if (htok) cudaFreeHost(htok);
     if (hloss) cudaFreeHost(hloss);
+    if (hcounts) cudaFreeHost(hcounts);
   }
   if (store) munmap(store, store_bytes);
   if (gacc) munmap(gacc, gacc_bytes);
@@ -1109,9 +1432,15 @@ mt_status mt_init_model(const mt_config* c, mt_dev_region dev, mt_streams s, mt_
     m->gacc = (float*)p;
   }
   m->pinned_bytes += tokb + 64;
+  if (m->moe) {
+    const size_t cb = (size_t)(m->L + 2) * m->E * 4;
+    if (pinned_alloc((void**)&m->hcounts, cb) != cudaSuccess) return MT_ERR_HOST_OOM;
+    std::memset(m->hcounts, 0, cb);
+    m->pinned_bytes += cb;
+  }
 
   for (cudaEvent_t* e : {&m->WR[0], &m->WR[1], &m->BD[0], &m->BD[1], &m->BF[0], &m->BF[1], &m->XR[0], &m->XR[1],
-                         &m->XS[0], &m->XS[1], &m->TOK, &m->LOSS})
+                         &m->XS[0], &m->XS[1], &m->TOK, &m->LOSS, &m->RT, &m->ER[0], &m->ER[1]})
     CU(mm, cudaEventCreateWithFlags(e, cudaEventDisableTiming));
   m->SR.assign((size_t)m->K, nullptr);
   for (auto& e : m->SR) CU(mm, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
@@ -1576,6 +1905,40 @@ mt_status mt_cross_entropy(void* logits, const int32_t* target, int64_t rows, in
                            float* row_loss, void* stream) {
   if (!logits || !target || !row_loss) return MT_ERR_ARG;
   return cu_status(mt::cross_entropy((bf16*)logits, target, rows, V, inv_norm, row_loss, (cudaStream_t)stream));
+}
+
+size_t mt_moe_scratch_bytes(int64_t T, int32_t H, int32_t E, int32_t k, int32_t Fe) {
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0 || Fe <= 0) return 0;
+  MoeWs w;
+  return moe_carve(MoeShape{T, H, E, k, Fe}, nullptr, &w);
+}
+
+mt_status mt_moe_ffn(const void* yn, const void* x1, const void* Wr, const void* We, const void* dout, int64_t T,
+                     int32_t H, int32_t E, int32_t k, int32_t Fe, void* out, void* dyn, void* dWr, void* dWe,
+                     int32_t* idx, float* gate, void* scratch, size_t scratch_bytes, void* stream) {
+  if (!yn || !x1 || !Wr || !We || !dout || !out || !dyn || !dWr || !dWe || !idx || !gate || !scratch)
+    return MT_ERR_ARG;
+  if (T < 1 || H <= 0 || H % 64 || Fe <= 0 || Fe % 64 || E < 8 || E > 128 || E % 8 || k < 1 || k > 8 || k > E)
+    return MT_ERR_ARG;
+  const MoeShape q{T, H, E, k, Fe};
+  MoeWs w;
+  if (scratch_bytes < moe_carve(q, nullptr, &w) || (reinterpret_cast<uintptr_t>(scratch) & 255)) return MT_ERR_ARG;
+  moe_carve(q, (uint8_t*)scratch, &w);
+  cudaStream_t s = (cudaStream_t)stream;
+  const bf16 *Y = (const bf16*)yn, *X1 = (const bf16*)x1, *R = (const bf16*)Wr, *Wex = (const bf16*)We;
+  OK(moe_route(nullptr, q, w, Y, R, s));
+  std::vector<int32_t> counts((size_t)E);
+  if (cudaMemcpyAsync(counts.data(), w.p.counts, (size_t)E * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MT_ERR_CUDA;
+  const MoeRoute r = route_from_counts(counts.data(), E);
+  OK(moe_experts_fwd(nullptr, q, w, r, Y, X1, Wex, (bf16*)out, s));
+  if (cudaMemsetAsync(dWe, 0, (size_t)E * 3 * Fe * H * 2, s) != cudaSuccess) return MT_ERR_CUDA;
+  OK(moe_backward(nullptr, q, w, r, Y, R, Wex, (const bf16*)dout, (bf16*)dyn, (bf16*)dWr, (bf16*)dWe, s));
+  if (cudaMemcpyAsync(idx, w.p.idx, (size_t)T * k * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(gate, w.p.gate, (size_t)T * k * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return MT_ERR_CUDA;
+  return MT_OK;
 }
 
 mt_status mt_fault_inject(int32_t kind, int32_t value) {

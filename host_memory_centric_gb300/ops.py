@@ -131,6 +131,19 @@ def cross_entropy(logits, target, inv_norm, row_loss):
     _chk(_L().mt_cross_entropy(_p(logits), _p(target), rows, V, inv_norm, _p(row_loss), _stream()))
 
 
+def moe_scratch_bytes(T, H, E, k, Fe):
+    return int(_L().mt_moe_scratch_bytes(T, H, E, k, Fe))
+
+
+def moe_ffn(yn, x1, Wr, We, dout, k, Fe, out, dyn, dWr, dWe, idx, gate, scratch):
+    """Routed MoE feed-forward forward + backward (mt_moe_ffn)."""
+    T, H = yn.shape
+    E = Wr.shape[0]
+    _chk(_L().mt_moe_ffn(_p(yn), _p(x1), _p(Wr), _p(We), _p(dout), T, H, E, k, Fe, _p(out), _p(dyn), _p(dWr),
+                         _p(dWe), _p(idx), _p(gate), _p(scratch), scratch.numel() * scratch.element_size(),
+                         _stream()))
+
+
 def kernel_error(clear=True) -> int:
     c = C.c_int32()
     _chk(_L().mt_kernel_error(C.byref(c), int(clear)))

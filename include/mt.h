@@ -99,6 +99,16 @@ typedef struct {
                               sums them in FP32 and Adam runs on the sum
                               after the last pass ([Hotdry] gradient
                               export: accumulated into the master store) */
+  int32_t n_experts;       /* 0: dense SwiGLU MLP in every decoder block;
+                              E > 0 (multiple of 8, <= 128): a routed mixture
+                              of E SwiGLU experts of hidden size expert_ffn,
+                              top_k (<= 8) per token ([Lilting] MoE section:
+                              the router picks the experts and only their
+                              weights are copied to the GPU); requires
+                              hidden and expert_ffn multiples of 64 and
+                              host_grad_accum = 0                           */
+  int32_t top_k;
+  int32_t expert_ffn;
 } mt_config;
 
 typedef struct { void* base; size_t bytes; } mt_dev_region;          /* caller-owned device memory  */
@@ -310,6 +320,22 @@ mt_status mt_timing_read(mt_model* model, int32_t kind, int64_t* launches, doubl
 mt_status mt_rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* gamma,
                                  const float* rstd, const void* dres, int64_t T, int32_t H,
                                  void* dx, void* dgamma, void* stream);
+/* Routed mixture-of-experts feed-forward of one layer, forward and backward
+ * in one call (the block math of an MoE decoder block after its second
+ * RMSNorm; [Lilting] MoE section).  yn, x1, dout: [T][H]; Wr: [E][H];
+ * We: [E][W_gu (2 Fe x H) | W_down (H x Fe)] (row e = expert e).  Writes
+ * out = x1 + sum_i gate_i FFN_{e_i}(yn) ([T][H]), dyn = d/d yn ([T][H]),
+ * dWr ([E][H]), dWe (same layout as We; rows of experts no token was routed
+ * to are zeroed), idx / gate ([T][k], int32 / FP32: the selected experts in
+ * descending logit order, ties to the lower index, and their softmax gates).
+ * Router logits are FP32 sums of BF16 products.  scratch: device memory of
+ * mt_moe_scratch_bytes bytes.  Synchronises `stream` once (the per-expert
+ * counts size the grouped products).  E multiple of 8 and <= 128, k <= 8,
+ * H and Fe multiples of 64. */
+size_t mt_moe_scratch_bytes(int64_t T, int32_t H, int32_t E, int32_t k, int32_t Fe);
+mt_status mt_moe_ffn(const void* yn, const void* x1, const void* Wr, const void* We, const void* dout, int64_t T,
+                     int32_t H, int32_t E, int32_t k, int32_t Fe, void* out, void* dyn, void* dWr, void* dWe,
+                     int32_t* idx, float* gate, void* scratch, size_t scratch_bytes, void* stream);
 /* Host-side fault injection for failure-detection tests (process-wide):
  * kind 1 = every Adam job sleeps `value` ms before it starts (a stalled
  * worker); kind 2 = the next `value` Adam jobs throw inside a worker; kind 3 =

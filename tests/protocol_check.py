@@ -99,7 +99,12 @@ def check(lines: list[str]) -> None:
                 assert a in adam_done, where
                 clk["H"].merge(adam_done[a][1])
             elif op == "WAIT_STAGE":
+                # the staging buffer is free once every copy that read it is done:
+                # the visit's H2D (Weights-Ready) and, for an MoE forward, the
+                # routed experts' H2D (Experts-Ready)
                 clk["H"].merge(ev["WR" + str(a)])
+                if "ER" + str(a) in ev:
+                    clk["H"].merge(ev["ER" + str(a)])
             elif op == "WAIT_RT":
                 clk["H"].merge(ev["RT" + str(a)])
             elif op == "PACK_EXP":
@@ -140,6 +145,7 @@ def check(lines: list[str]) -> None:
             if a in adam_done:
                 assert _hb(adam_done[a], me), "expert H2D of a block before its Adam: " + where
             exp_h2d[b] = me
+            stage_read[b] = me
             last_buf_use[b].append(me)
         elif op == "FWD_EXP":
             assert b in exp_h2d and _hb(exp_h2d[b], me), "experts computed before they arrived: " + where
@@ -147,6 +153,7 @@ def check(lines: list[str]) -> None:
                 assert _hb(u, me), "expert compute overlaps earlier use of buffer: " + where
             last_buf_use[b] = [me]
             del exp_h2d[b]
+            xslot_write[a % 2] = me  # the combine writes X_j
         elif op == "H2D_CKPT":
             assert (a - 1) in ckpt_saved, "checkpoint loaded that was never saved: " + where
             assert _hb(ckpt_saved[a - 1], me), "checkpoint loaded before its save finished: " + where

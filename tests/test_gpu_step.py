@@ -39,9 +39,14 @@ def _no_kernel_errors():
     assert ops.kernel_error(clear=True) == 0
 
 
-def run_parity(orc, c, steps, check_init=True, **rt):
+def run_parity(orc, c, steps, check_init=True, prepare=None, **rt):
+    """prepare(m), when given, rewrites the initial store before the first
+    step (check_init is then meaningless and skipped)."""
     oc = oracle_shape(c)
     m = mt.Model(c, log_protocol=1, n_host_threads=4, seed=1234, **rt)
+    if prepare is not None:
+        prepare(m)
+        check_init = False
     lay = orc.layout(oc)
     nb = len(lay)
     # the library's initial store equals the oracle's initialiser bit for bit
@@ -83,7 +88,7 @@ def run_parity(orc, c, steps, check_init=True, **rt):
             else:
                 orc.adam(G, master_o[j], m_o[j], v_o[j], step + 1, lr=c["lr"], beta1=c["beta1"],
                          beta2=c["beta2"], eps=c["adam_eps"])
-        report.append((step, loss, loss_ref, worst))
+        report.append((step, loss, loss_ref, worst) + ((orc.last_route_margin(),) if c.get("n_experts") else ()))
     for j in range(nb):
         got = m.read(j, mt.REGION_MASTER)
         for t, sl in enumerate(tensor_slices(lay[j])):

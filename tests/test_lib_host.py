@@ -260,3 +260,37 @@ def test_worker_pool_has_no_data_race(tmp_path):
                        env=dict(os.environ, TSAN_OPTIONS="halt_on_error=1 exitcode=66"))
     assert "ThreadSanitizer" not in r.stderr, r.stderr[-2000:]
     assert r.returncode == 0 and r.stdout.startswith("ok"), (r.returncode, r.stdout, r.stderr[-500:])
+
+
+# ------------------------------------------------------------------ routed MoE
+def test_init_bit_exact_moe_block(orc):
+    c = configs.get("tiny_moe")
+    for j in (1, 2):
+        a = _lib_init(c, j)
+        b = orc.init_block(shape_for_oracle(c), 77, j)
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("pin,ckpt,ci,nbuf", [(0, 1, 1, 2), (1, 1, 1, 2), (0, 0, 2, 2), (1, 0, 1, 1), (0, 1, 3, 1)])
+def test_protocol_plan_moe_bit_exact(orc, pin, ckpt, ci, nbuf):
+    """MoE forward visits: Route-Ready, the host's wait, the routed experts'
+    copy and Experts-Ready sit where the simulator puts them."""
+    c = configs.get("tiny_moe", n_layers=3)
+    lines = _plan(c, 3, ckpt_on_host=ckpt, pin_store=pin, n_grad_slabs=2, ckpt_interval=ci, n_buffers=nbuf)
+    ref = orc.protocol(c, 3, 2, bool(ckpt), not pin, ci, nbuf)
+    assert protocol_check.mask_slabs(lines) == protocol_check.mask_slabs(ref)
+    protocol_check.check(lines)
+    assert sum(" H2D_EXP " in l for l in lines) == 3 * 3
+
+
+def test_bad_moe_configs_rejected():
+    L = mt.lib()
+    n = C.c_size_t()
+    for kw in (dict(n_experts=12), dict(n_experts=136), dict(top_k=0), dict(top_k=9), dict(expert_ffn=100),
+               dict(hidden=320, n_heads=5), dict(host_grad_accum=1)):
+        bad = mt.make_config(configs.get("tiny_moe", **{k: v for k, v in kw.items() if k != "host_grad_accum"}),
+                             **({"host_grad_accum": 1} if "host_grad_accum" in kw else {}))
+        assert L.mt_query_device_bytes(C.byref(bad), C.byref(n)) == -1, kw
+    ok = mt.make_config(configs.get("tiny_moe"))
+    assert L.mt_query_device_bytes(C.byref(ok), C.byref(n)) == 0
+    assert L.mt_moe_scratch_bytes(256, 256, 8, 2, 256) > 0

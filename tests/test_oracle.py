@@ -83,13 +83,24 @@ def test_bf16_rne_matches_torch(orc):
 def closed_form_params(c):
     L, H, nh, nkv, hd, F, V = (c[k] for k in ("n_layers", "hidden", "n_heads", "n_kv_heads",
                                               "head_dim", "ffn", "vocab"))
-    return L * (H * (nh + 2 * nkv) * hd + nh * hd * H + 3 * H * F + 2 * H) + 2 * V * H + H
+    mlp = 3 * H * F
+    if c.get("n_experts", 0):  # router [E, H] and E experts of W_gu [2Fe, H] + W_down [H, Fe]
+        mlp = c["n_experts"] * H + c["n_experts"] * 3 * H * c["expert_ffn"]
+    return L * (H * (nh + 2 * nkv) * hd + nh * hd * H + mlp + 2 * H) + 2 * V * H + H
 
 
 @pytest.mark.parametrize("name", list(configs.CONFIGS))
 def test_param_count_closed_form(orc, name):
     c = configs.get(name)
     assert orc.param_count(c) == closed_form_params(c)
+
+
+def test_moe_shape_at_full_depth_is_gpt_oss_20b_sized(orc):
+    """The ``moe`` shape at GPT-OSS-20B's depth (24 layers) has about 21B
+    parameters, the published size of that model (no biases, sinks or
+    sliding windows here, so a little below)."""
+    p = orc.param_count(configs.get("moe", n_layers=24))
+    assert 20.5e9 < p < 21.5e9
 
 
 def test_param_counts_match_public_model_sizes(orc):
