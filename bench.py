@@ -51,12 +51,21 @@ def model_numbers(c, ckpt_interval=1):
                                               "vocab"))
     B, S, M = c["batch"], c["seq"], c["micro"]
     t = B * S
-    P_mm = H * (nh + 2 * nkv) * hd + nh * hd * H + 3 * H * F
-    P = L * (P_mm + 2 * H) + 2 * V * H + H
+    E = c.get("n_experts", 0)
+    attn = H * (nh + 2 * nkv) * hd + nh * hd * H
+    if E:  # routed experts: a token runs the router and top_k experts (P_mm = active matrix params)
+        k, Fe = c["top_k"], c["expert_ffn"]
+        P_mm = attn + E * H + k * 3 * H * Fe
+        P = L * (attn + E * H + E * 3 * H * Fe + 2 * H) + 2 * V * H + H
+    else:
+        P_mm = attn + 3 * H * F
+        P = L * (P_mm + 2 * H) + 2 * V * H + H
     F_exec = M * (L * (8 * t * P_mm + 9 * B * nh * hd * S * S) + 6 * t * H * V)
     n_recomp = L - -(-L // ckpt_interval)
     F_exec += M * n_recomp * (2 * t * P_mm + 2 * B * nh * hd * S * S)
-    F_pages = 6 * P * M * t + 12 * L * B * M * S * S * H
+    # 6 N T with N the parameters a token uses (all of them for a dense model)
+    N_active = L * (P_mm + 2 * H) + 2 * V * H + H
+    F_pages = 6 * N_active * M * t + 12 * L * B * M * S * S * H
     return P, F_exec, F_pages
 
 
@@ -212,8 +221,10 @@ def aggregate(t_step_local: float, tokens_per_step: int, world: int, dist=None, 
 
 
 def workload_desc(name, c):
+    mlp = (f"{c['n_experts']} routed SwiGLU experts of FFN {c['expert_ffn']}, top-{c['top_k']} (only routed "
+           f"experts streamed)" if c.get("n_experts") else f"FFN {c['ffn']}")
     return (f"{name}-shaped decoder: {c['n_layers']} layers, hidden {c['hidden']}, {c['n_heads']}x{c['head_dim']} "
-            f"heads ({c['n_kv_heads']} KV), FFN {c['ffn']}, vocab {c['vocab']}, batch {c['batch']} x seq "
+            f"heads ({c['n_kv_heads']} KV), {mlp}, vocab {c['vocab']}, batch {c['batch']} x seq "
             f"{c['seq']} x {c['micro']} micro-batches; host-resident BF16/FP32 state, host Adam")
 
 
@@ -475,6 +486,14 @@ def main():
                  "pinned_GB": st1["pinned_bytes"] / 1e9, "init_s": init_s, "nproc": os.cpu_count(),
                  "last_loss": losses[-1]},
     }
+    if c.get("n_experts"):
+        # routed experts of the last forward: how many experts each layer's
+        # stream-ins copied, and the load of the busiest expert over the mean
+        cnt = np.stack([m.expert_counts(j) for j in range(1, c["n_layers"] + 1)])
+        line["moe"] = {"n_experts": c["n_experts"], "top_k": c["top_k"],
+                       "routed_experts_per_layer": [int(x) for x in (cnt > 0).sum(axis=1)],
+                       "routed_frac": float((cnt > 0).mean()),
+                       "max_over_mean_load": float((cnt.max(axis=1) / cnt.mean(axis=1)).mean())}
     print(json.dumps(line), flush=True)
     m.close()
     if dist:

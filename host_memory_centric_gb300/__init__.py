@@ -133,6 +133,7 @@ def lib():
         "mt_kernel_error": (i32, [_P(i32), i32]),
         "mt_fault_inject": (i32, [i32, i32]),
         "mt_moe_scratch_bytes": (sz, [i64, i32, i32, i32, i32]),
+        "mt_expert_counts": (i32, [_v, i32, _P(i32), i32]),
         "mt_moe_ffn": (i32, [_v, _v, _v, _v, _v, i64, i32, i32, i32, i32, _v, _v, _v, _v, _v, _v, _v, sz, _v]),
     }
     for name, (res, args) in sig.items():
@@ -281,6 +282,13 @@ class Model:
         dt = np.uint16 if region < 2 else np.float32
         arr = np.ascontiguousarray(arr, dtype=dt)
         check(lib().mt_write_host(self.h, block, region, arr.ctypes.data, arr.nbytes), self.h)
+
+    def expert_counts(self, block: int) -> np.ndarray:
+        """Tokens routed to each expert in block's last forward (MoE models)."""
+        n = int(self.cfg.n_experts)
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        check(lib().mt_expert_counts(self.h, block, _ptr(out, C.c_int32), n), self.h)
+        return out
 
     def stats(self) -> dict:
         s = Stats()

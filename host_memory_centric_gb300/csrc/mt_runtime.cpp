@@ -1620,6 +1620,12 @@ mt_status mt_get_stats(const mt_model* m, mt_stats* o) {
   return MT_OK;
 }
 
+mt_status mt_expert_counts(const mt_model* m, int32_t block, int32_t* counts, int32_t n) {
+  if (!m || !counts || !m->moe || block < 1 || block > m->L || n < m->E) return MT_ERR_ARG;
+  std::memcpy(counts, m->hcounts + (size_t)block * m->E, (size_t)m->E * 4);
+  return MT_OK;
+}
+
 int64_t mt_protocol_log(const mt_model* m, char* buf, int64_t cap) {
   if (!m) return 0;
   std::string s;

@@ -190,6 +190,10 @@ mt_status mt_sync(mt_model* model);
 mt_status mt_read_host(mt_model* model, int32_t block, int32_t region, void* dst, size_t bytes);
 mt_status mt_write_host(mt_model* model, int32_t block, int32_t region, const void* src, size_t bytes);
 mt_status mt_get_stats(const mt_model* model, mt_stats* out);
+/* MoE models: the per-expert token counts (n_experts int32) of block j's
+ * last forward (1 <= j <= n_layers), i.e. which experts its stream-ins
+ * copied; read after mt_sync.  MT_ERR_ARG for a dense model or a bad j. */
+mt_status mt_expert_counts(const mt_model* model, int32_t block, int32_t* counts, int32_t n);
 /* The enqueue log (lines "step stream op a b"); returns its length, or
  * -(needed) when cap is too small. */
 int64_t mt_protocol_log(const mt_model* model, char* buf, int64_t cap);

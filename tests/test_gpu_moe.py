@@ -170,6 +170,9 @@ def test_moe_streams_only_routed_experts():
     m.train_step(0)
     m.sync()
     s1 = m.stats()
+    even = int((tok % 2 == 0).sum())
+    for j in range(1, L + 1):  # parity decides: even tokens -> experts 0, 1; odd -> 2, 3
+        assert m.expert_counts(j).tolist() == [even, even, tok.size - even, tok.size - even, 0, 0, 0, 0], j
     eo, E, row = lay[1]["tensors"][3]
     unused = 4 * row * 2  # bytes of experts 4..7 of one layer
     h2d = s1["h2d_bytes"] - s0["h2d_bytes"]
