@@ -1690,13 +1690,13 @@ mt_status mt_host_init_block(const mt_config* c, int32_t j, float* master) {
 
 mt_status mt_host_adam(int64_t n, const uint16_t* g, float* th, float* m, float* v, uint16_t* w, int32_t t,
                        float lr, float b1, float b2, float eps, float wd, int32_t n_threads) {
-  if (n < 0 || !g || !th || !m || !v || !w || t < 1) return MT_ERR_ARG;
+  if (n < 0 || !th || !m || !v || !w || t < 1) return MT_ERR_ARG;
   mth::Pool pool;
   pool.start(n_threads > 0 ? n_threads : 1);
   constexpr int64_t CH = 1 << 18;
   std::function<void(int64_t)> fn = [&](int64_t i) {
     const int64_t o = i * CH, len = (n - o) < CH ? (n - o) : CH;
-    mth::adam(len, g + o, nullptr, th + o, m + o, v + o, w + o, t, lr, b1, b2, eps, wd);
+    mth::adam(len, g ? g + o : nullptr, nullptr, th + o, m + o, v + o, w + o, t, lr, b1, b2, eps, wd);
   };
   std::string err;
   const bool ok = pool.parallel_for((n + CH - 1) / CH, fn, &err);

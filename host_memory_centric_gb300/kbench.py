@@ -6,6 +6,7 @@ python -m host_memory_centric_gb300.kbench gemm --M 8192 --N 11264 --K 2048 [--a
 python -m host_memory_centric_gb300.kbench attn_fwd --S 2048 --nseq 4 --nh 16 --nkv 4 --hd 128
 python -m host_memory_centric_gb300.kbench attn_bwd --S 2048 --nseq 4 --nh 16 --nkv 4 --hd 128
 python -m host_memory_centric_gb300.kbench rmsnorm_bwd --T 8192 --H 2048
+python -m host_memory_centric_gb300.kbench moe_ffn --T 16384 --H 2880 --E 32 --k 4 --Fe 2880
 """
 from __future__ import annotations
 
@@ -46,6 +47,9 @@ def main():
     ap.add_argument("--hd", type=int, default=128)
     ap.add_argument("--T", type=int, default=8192)
     ap.add_argument("--H", type=int, default=2048)
+    ap.add_argument("--E", type=int, default=32)
+    ap.add_argument("--k", type=int, default=4)
+    ap.add_argument("--Fe", type=int, default=2880)
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     a = ap.parse_args()
@@ -111,6 +115,24 @@ def main():
             ms = timeit(lambda: ops.rmsnorm_bwd(y, x, g, r, y, dx, dg, sc), a.iters, a.warmup)
             by = 8.0 * a.T * a.H
         res.update(shape=[a.T, a.H], ms=ms, gbs=by / ms / 1e6)
+    elif a.op == "moe_ffn":
+        # one MoE feed-forward, forward and backward (router, routing, grouped expert GEMMs, combine);
+        # includes one host synchronisation for the per-expert counts
+        T, H, E, k, Fe = a.T, a.H, a.E, a.k, a.Fe
+        yn = torch.randn(T, H).to(bf).to(dev)
+        x1 = torch.randn(T, H).to(bf).to(dev)
+        Wr = (torch.randn(E, H) / H ** 0.5).to(bf).to(dev)
+        We = torch.cat([torch.randn(E, 2 * Fe * H) / H ** 0.5, torch.randn(E, H * Fe) / Fe ** 0.5], 1).to(bf).to(dev)
+        dout = torch.randn(T, H).to(bf).to(dev)
+        out, dyn = torch.empty_like(yn), torch.empty_like(yn)
+        dWr, dWe = torch.empty_like(Wr), torch.empty_like(We)
+        idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+        gate = torch.empty(T, k, dtype=torch.float32, device=dev)
+        sc = torch.empty(ops.moe_scratch_bytes(T, H, E, k, Fe), dtype=torch.uint8, device=dev)
+        run = lambda: ops.moe_ffn(yn, x1, Wr, We, dout, k, Fe, out, dyn, dWr, dWe, idx, gate, sc)
+        ms = timeit(run, a.iters, a.warmup)
+        fl = 2.0 * T * k * 3 * H * Fe * 3 + 2.0 * T * E * H * 3  # experts fwd + dgrad + wgrad, router x3
+        res.update(shape=dict(T=T, H=H, E=E, k=k, Fe=Fe), ms=ms, tflops=fl / ms / 1e9)
     else:
         raise SystemExit("unknown op " + a.op)
     print(json.dumps(res))

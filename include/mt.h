@@ -211,7 +211,9 @@ int64_t mt_param_count(const mt_config* cfg);
 int64_t mt_store_bytes(const mt_config* cfg);
 /* The library's initialiser for block j (n_pad FP32 master values). */
 mt_status mt_host_init_block(const mt_config* cfg, int32_t j, float* master);
-/* The library's host Adam over n elements on n_threads threads. */
+/* The library's host Adam over n elements on n_threads threads; g_bf16 =
+ * NULL applies a zero gradient (what an MoE expert no token was routed to
+ * receives). */
 mt_status mt_host_adam(int64_t n, const uint16_t* g_bf16, float* master, float* m, float* v,
                        uint16_t* w_bf16, int32_t adam_step, float lr, float beta1, float beta2,
                        float eps, float weight_decay, int32_t n_threads);

@@ -119,9 +119,9 @@ def test_gqa_shape_parity(orc):
     report, _ = run_parity(orc, c, 2)
 
 
-@pytest.mark.parametrize("ci,nbuf", [(1, 2), (2, 1)])
-def test_manual_primitives_match_train_step(ci, nbuf):
-    c = configs.get("tiny", n_layers=3)
+@pytest.mark.parametrize("ci,nbuf,name", [(1, 2, "tiny"), (2, 1, "tiny"), (1, 2, "tiny_moe"), (2, 1, "tiny_moe")])
+def test_manual_primitives_match_train_step(ci, nbuf, name):
+    c = configs.get(name, n_layers=3)
     rt = dict(ckpt_interval=ci, n_buffers=nbuf)
     tok = inputs.tokens_for(c, 0)
     a = mt.Model(c, seed=5, **rt)

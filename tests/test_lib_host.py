@@ -85,6 +85,30 @@ def test_host_adam_matches_oracle(orc):
     assert np.mean(wa == wb) > 0.999
 
 
+def test_host_adam_zero_gradient_matches_oracle(orc):
+    """The unrouted-expert path (no gradient transferred, g = 0): after a step
+    with a gradient, further zero-gradient steps still move the master by
+    its momentum, exactly as the oracle's Adam fed zeros."""
+    rng = np.random.default_rng(1)
+    n = 100_000
+    g = orc.bf16_rne_fast((rng.standard_normal(n) * 1e-3).astype(np.float32))
+    zero = np.zeros(n, np.uint16)
+    th = (0.02 * rng.standard_normal(n)).astype(np.float32)
+    a = [th.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)]
+    b = [x.copy() for x in a]
+    w = np.empty(n, np.uint16)
+    P = lambda x, t: x.ctypes.data_as(C.POINTER(t))
+    for t, grad in ((1, g), (2, None), (3, None)):
+        gp = P(grad, C.c_uint16) if grad is not None else None
+        assert mt.lib().mt_host_adam(n, gp, P(a[0], C.c_float), P(a[1], C.c_float), P(a[2], C.c_float),
+                                     P(w, C.c_uint16), t, 1e-3, 0.9, 0.999, 1e-8, 0.0, 2) == 0
+        wb = orc.adam(grad if grad is not None else zero, b[0], b[1], b[2], t)
+    for x, y in zip(a, b):
+        assert np.linalg.norm(x - y) <= 1e-6 * np.linalg.norm(y)
+    assert np.mean(w == wb) > 0.999
+    assert np.linalg.norm(a[0] - th) > 0  # momentum kept moving the weights
+
+
 def _plan(c, steps, **rt):
     cfg = mt.make_config(c, **rt)
     need = -mt.lib().mt_plan_protocol(C.byref(cfg), steps, None, 0)
