@@ -178,6 +178,36 @@ def cpu_sample(cfg_name, budget_s=20.0):
             "seconds": dt * n}
 
 
+def static_schedule(m, vis_ms, bw, hbw, slabs):
+    """The static prefetch schedule (mt_schedule) evaluated on this run's
+    measurements: per visit the H2D bytes of its block, the exported gradient
+    bytes, the measured compute time of the visit and the host Adam time of
+    its block at the measured Adam rate; the measured link bandwidths.  It
+    predicts the compute stream's stalls and the slab pool the exports need
+    (the host Adam bound is outside its model)."""
+    import ctypes
+    import host_memory_centric_gb300 as mt
+    plan = mt.visit_plan(m.cfg)
+    lay = m.layout
+    n = len(plan)
+    if len(vis_ms) != n or not np.all(vis_ms > 0):
+        return None
+    D = ctypes.POINTER(ctypes.c_double)
+    b = np.array([0.0 if (k == 3 and j == 0) else 2.0 * lay[j]["n_pad"] for k, j in plan])
+    d = np.array([2.0 * lay[j]["n_pad"] if k in (1, 3) else 0.0 for k, j in plan])
+    a = np.array([lay[j]["n_pad"] / (hbw["adam_gelem_s"] * 1e9) if k in (1, 3) else 0.0 for k, j in plan])
+    cv = np.ascontiguousarray(vis_ms / 1e3)
+    stall = np.zeros(n)
+    p = lambda x: x.ctypes.data_as(D)
+    need = mt.lib().mt_schedule(n, p(b), p(d), p(cv), p(a), bw["h2d"], bw["d2h"], p(stall))
+    return {"visits": n, "compute_ms_per_step": float(cv.sum() * 1e3),
+            "predicted_stall_ms_per_step": float(stall.sum() * 1e3),
+            "predicted_gpu_timeline_ms": float((cv + stall).sum() * 1e3),
+            "worst_visit_stall_ms": float(stall.max() * 1e3), "slabs_needed": int(need), "slabs_used": slabs,
+            "note": "mt_schedule on measured per-visit compute, block bytes, link bandwidth and Adam rate; "
+                    "host Adam throughput is not in its model"}
+
+
 def mem_available_bytes() -> int:
     try:
         for line in open("/proc/meminfo"):
@@ -385,6 +415,7 @@ def main():
     barrier()
     dev_s = ev0.elapsed_time(ev1) / 1e3
     kern = {name: m.timing_read(i) for i, name in enumerate(("gemm", "attn_fwd", "attn_bwd", "other"))}
+    vis_ms = m.timing_visits()
     m.timing(False)
     st1 = m.stats()
     value, t_step = aggregate(max(dev_s, wall) / args.steps, T, world, dist, "cuda")
@@ -486,6 +517,7 @@ def main():
                  "pinned_GB": st1["pinned_bytes"] / 1e9, "init_s": init_s, "nproc": os.cpu_count(),
                  "last_loss": losses[-1]},
     }
+    line["schedule"] = static_schedule(m, vis_ms, bw, hbw, args.slabs)
     if c.get("n_experts"):
         # routed experts of the last forward: how many experts each layer's
         # stream-ins copied, and the load of the busiest expert over the mean

@@ -115,6 +115,7 @@ def lib():
         "mt_rope_table": (i32, [i32, i32, f64, _P(f32)]),
         "mt_timing": (i32, [_v, i32]),
         "mt_timing_read": (i32, [_v, i32, _P(i64), _P(f64), _P(f64), _P(f64)]),
+        "mt_timing_visits": (i32, [_v, _P(f64), i32, _P(i32)]),
         "mt_gemm": (i32, [_v, i64, i32, _v, i64, i32, i32, i32, i32, _v, i64, _v, i64, _v, i64, i32, _v]),
         "mt_gemm2": (i32, [_P(_v), _P(i64), _P(i32), _P(_v), _P(i64), _P(i32), _P(i32), _P(i32), _P(i32),
                             _P(_v), _P(i64), _v]),
@@ -308,6 +309,14 @@ class Model:
         n = C.c_int64(); ms = C.c_double(); fl = C.c_double(); by = C.c_double()
         check(lib().mt_timing_read(self.h, kind, C.byref(n), C.byref(ms), C.byref(fl), C.byref(by)), self.h)
         return dict(launches=n.value, ms=ms.value, flops=fl.value, bytes=by.value)
+
+    def timing_visits(self) -> np.ndarray:
+        """Mean compute time (ms) of each visit of the step over the timed steps."""
+        n = C.c_int32()
+        check(lib().mt_timing_visits(self.h, None, 0, C.byref(n)), self.h)
+        out = np.zeros(n.value, dtype=np.float64)
+        check(lib().mt_timing_visits(self.h, _ptr(out, C.c_double), n.value, C.byref(n)), self.h)
+        return out
 
     def last_error(self) -> str:
         return lib().mt_last_error(self.h).decode()

@@ -164,7 +164,7 @@ struct KStat {
 };
 struct Pending {
   cudaEvent_t a, b;
-  int kind, nk;
+  int kind, nk;  // kind < 0: the compute of visit nk (per-visit timing)
   double flops, bytes;
 };
 
@@ -234,6 +234,7 @@ struct mt_model {
   std::vector<Pending> pend;
   std::vector<cudaEvent_t> ev_pool;
   KStat kstat[4];
+  std::vector<KStat> vstat;  // per visit of the step: compute-stream time of its compute part
 
   ~mt_model();
 };
@@ -395,7 +396,12 @@ struct Timed {
 void collect_timing(mt_model* m) {
   for (auto& p : m->pend) {
     float ms = 0;
-    if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
+    if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess && p.kind < 0) {
+      if (p.nk >= 0 && p.nk < (int)m->vstat.size()) {
+        m->vstat[(size_t)p.nk].launches += 1;
+        m->vstat[(size_t)p.nk].ms += ms;
+      }
+    } else if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
       KStat& k = m->kstat[p.kind];
       k.launches += p.nk;
       k.ms += ms;
@@ -1223,9 +1229,19 @@ mt_status run_visit(mt_model* m) {
   advance(m);
   OK(do_bind(m, j, b, nullptr));
   advance(m);
+  cudaEvent_t ta = nullptr;
+  if (m->live && m->timing) {  // per-visit compute time, after the Weights-Ready wait
+    ta = take_event(m);
+    CU(m, cudaEventRecord(ta, m->sc));
+  }
   if (kind <= V_HEAD) OK(do_forward(m, j, b));
   else if (kind == V_RECOMP) OK(do_recompute(m, j, b));
   else OK(do_backward(m, j, b));
+  if (ta) {
+    cudaEvent_t tb = take_event(m);
+    CU(m, cudaEventRecord(tb, m->sc));
+    m->pend.push_back({ta, tb, -1, v, 0.0, 0.0});
+  }
   const bool exp = exports_grad(m, v);
   const int64_t t = m->steps_done + 1;
   advance(m);
@@ -1800,6 +1816,18 @@ mt_status mt_timing(mt_model* m, int32_t enable) {
   if (!enable) OK(mt_sync(m));
   m->timing = enable != 0;
   for (auto& k : m->kstat) k = KStat();
+  m->vstat.assign((size_t)nvisits(m), KStat());
+  return MT_OK;
+}
+
+mt_status mt_timing_visits(mt_model* m, double* ms, int32_t cap, int32_t* n_visits) {
+  if (!m || !n_visits) return MT_ERR_ARG;
+  collect_timing(m);
+  *n_visits = nvisits(m);
+  for (int v = 0; v < nvisits(m) && v < cap && ms; ++v) {
+    const KStat& k = v < (int)m->vstat.size() ? m->vstat[(size_t)v] : KStat();
+    ms[v] = k.launches ? k.ms / (double)k.launches : 0.0;
+  }
   return MT_OK;
 }
 

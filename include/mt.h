@@ -309,6 +309,13 @@ mt_status mt_cross_entropy(void* logits, const int32_t* target, int64_t rows, in
 mt_status mt_timing(mt_model* model, int32_t enable);
 mt_status mt_timing_read(mt_model* model, int32_t kind, int64_t* launches, double* ms,
                          double* flops, double* bytes);
+/* Per visit of the step (the order of mt_visit_plan), the mean compute-
+ * stream time of its compute part over the timed train steps (ms; from
+ * after its Weights-Ready wait to the end of its kernels, so an MoE forward
+ * includes its wait for the routed experts).  Writes min(cap, n) values and
+ * *n_visits = n.  These are the per-block compute times the static prefetch
+ * schedule (mt_schedule) takes. */
+mt_status mt_timing_visits(mt_model* model, double* ms, int32_t cap, int32_t* n_visits);
 /* RMSNorm backward that allocates nothing (same results as mt_rmsnorm_bwd).
  * The pages have no counterpart: this is for callers that cannot allocate
  * device memory -- code running during stream capture, code inside another

@@ -108,3 +108,38 @@ def test_bad_arguments_are_rejected_without_latching():
     assert np.isfinite(m.train_step(0))
     m.sync()
     m.close()
+
+
+def test_moe_route_wait_times_out_and_latches():
+    """An MoE forward visit waits on the host, bounded, for the router's
+    per-expert counts (Route-Ready).  A GEMM made to stall (its bounded waits
+    run out after about 2 s, with the context intact) delays that event past
+    a 1 s limit: train_step returns MT_ERR_TIMEOUT, the model latches, and a
+    fresh model trains normally afterwards."""
+    c = configs.get("tiny_moe")
+    m = mt.Model(c, timeout_ms=1000)
+    # one normal step first: the first launch of a kernel not yet loaded
+    # (CUDA's lazy module loading) waits for the device, which would hold the
+    # host behind the stalled GEMM before it reaches the bounded wait
+    m.set_tokens(inputs.tokens_for(c, 0))
+    m.train_step(0)
+    m.sync()
+    m.set_tokens(inputs.tokens_for(c, 1))
+    ops.kernel_error(clear=True)
+    assert mt.lib().mt_fault_inject(4, 1) == 0  # layer 1's first GEMM (QKV) issues no loads
+    with pytest.raises(mt.MtError) as ei:
+        m.train_step(1)
+    assert ei.value.status == -5
+    assert "routing" in m.last_error()
+    with pytest.raises(mt.MtError) as ei:
+        m.train_step(1)
+    assert ei.value.status == -2  # latched
+    m.close()
+    torch.cuda.synchronize()
+    assert ops.kernel_error(clear=True) != 0
+    m2 = mt.Model(c)
+    m2.set_tokens(inputs.tokens_for(c, 0))
+    assert np.isfinite(m2.train_step(0))
+    m2.sync()
+    assert ops.kernel_error(clear=True) == 0
+    m2.close()
