@@ -219,3 +219,34 @@ def test_moe_full_width_zero_head_properties():
     for j in range(L + 1):
         assert not np.any(m.read(j, mt.REGION_G)), j
     m.close()
+
+
+def test_moe_full_width_one_layer_parity(orc):
+    """The `moe` shape at full width (hidden 2880, 64 x 64 heads / 8 KV, 32
+    experts of FFN 2880, top-4, vocabulary 201088), one decoder layer and one
+    64-token sequence, against the oracle with the same unambiguous routing
+    (a +-16 embedding sign channel and router column 1)."""
+    c = configs.get("moe", n_layers=1, batch=1, seq=64, micro=1, lr=1e-4)
+    E = c["n_experts"]
+
+    def prep(m):
+        import oracle
+        lay = m.layout
+        V = c["vocab"]
+        th = m.read(0, mt.REGION_MASTER)
+        eo, r, cc = lay[0]["tensors"][0]
+        # +-16: at this width the attention output at init (about N(0, 1.4) per element for the
+        # first positions) must not flip the sign channel
+        th[eo:eo + r * cc].reshape(r, cc)[:, 1] = np.where(np.arange(V) % 2 == 0, 16.0, -16.0)
+        m.write(0, mt.REGION_MASTER, th)
+        m.write(0, mt.REGION_W, oracle.bf16_rne_fast(th))
+        b = np.zeros(E, np.float32)
+        b[:4], b[4:8] = [1.0, 0.9, 0.8, 0.7], [-1.0, -0.9, -0.8, -0.7]  # even -> 0..3, odd -> 4..7
+        th = m.read(1, mt.REGION_MASTER)
+        ro, EE, H = lay[1]["tensors"][2]
+        th[ro:ro + EE * H].reshape(EE, H)[:, 1] = b
+        m.write(1, mt.REGION_MASTER, th)
+        m.write(1, mt.REGION_W, oracle.bf16_rne_fast(th))
+
+    report, _ = run_parity(orc, c, 1, prepare=prep)
+    assert report[0][4] > 1.0, report
