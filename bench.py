@@ -208,6 +208,24 @@ def static_schedule(m, vis_ms, bw, hbw, slabs):
                     "host Adam throughput is not in its model"}
 
 
+def cpu_model() -> str:
+    """CPU model of this host (lscpu's model name, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def mem_available_bytes() -> int:
     try:
         for line in open("/proc/meminfo"):
@@ -515,6 +533,7 @@ def main():
                  "d2h_GB_per_step": (st1["d2h_bytes"] - st0["d2h_bytes"]) / args.steps / 1e9,
                  "device_bytes": m.device_bytes, "host_store_GB": st1["host_store_bytes"] / 1e9,
                  "pinned_GB": st1["pinned_bytes"] / 1e9, "init_s": init_s, "nproc": os.cpu_count(),
+                 "cpu_model": cpu_model(),
                  "last_loss": losses[-1]},
     }
     line["schedule"] = static_schedule(m, vis_ms, bw, hbw, args.slabs)
