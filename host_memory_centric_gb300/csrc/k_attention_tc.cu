@@ -8,22 +8,28 @@
 //               into a 2-stage ring (128-byte swizzle);
 //   warp 1      allocates TMEM (S0 | S1 | O_0 | O_1) and, from one thread,
 //               issues S_j = Q K_j^T (M=128, N=128) into S[j % 2] and, once the
-//               softmax has produced P_{j-1}, O_0 += P V over the tile's keys
-//               0..63 and O_1 += P V over keys 64..127 (V as an MN-major
-//               operand);
+//               softmax has written P_{j-1} over S_{j-1} (BF16, in TMEM),
+//               O_0 += P V over the tile's keys 0..63 and O_1 += P V over keys
+//               64..127 with P as the A operand from TMEM and V an MN-major
+//               operand from shared memory;
 //   warps 2..9  softmax: warp w owns the query rows of TMEM lane quarter w % 4
 //               and one half of every key tile (warps 2..5 keys 0..63, 6..9
-//               keys 64..127), with its own online max / sum in the exp2
-//               domain and its own accumulator O_half, rescaled in TMEM when
-//               its max grows; P goes to the 128B-swizzled K-major tile the
-//               next MMA reads.  At the end the two halves of a row merge
-//               (m = max, each side scaled by 2^(m_h - m)) and O / l and
-//               LSE = (m + log2 l) ln 2 go to global memory.
+//               keys 64..127), with its own exponent base, sum and accumulator
+//               O_half.  The base follows the running max lazily: it moves (and
+//               O_half and the sum are rescaled) only when a tile's max exceeds
+//               it by more than 8 in the exp2 domain, so P stays below 2^8 and
+//               most tiles touch neither O nor the previous P V.  At the end the
+//               two halves of a row merge (m = max, each side scaled by
+//               2^(m_h - m)) and O / l and LSE = (m + log2 l) ln 2 go to global
+//               memory.
 // Splitting every row over two threads halves the per-thread softmax work per
 // tile without any per-tile exchange between them.  The double-buffered S
-// lets S_{j+1} run on the tensor core while the softmax works on S_j.  Every
-// mbarrier wait is bounded; an expired wait sets the kernel error word and the
-// CTA stops, drains its copies and frees TMEM.
+// lets S_{j+1} run on the tensor core while the softmax works on S_j; P in
+// TMEM needs no shared-memory tile, so the softmax of tile j waits for the
+// previous P V only when it rescales.  tcgen05.mma operations of one thread
+// run in issue order, so S_{j+2} overwrites P_j only after O += P_j V read it.
+// Every mbarrier wait is bounded; an expired wait sets the kernel error word
+// and the CTA stops, drains its copies and frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -215,19 +221,20 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   uint8_t* sQ = sm;
   uint8_t* sK = sQ + NC * CH;        // NFK stages: K is free once S has been computed
   uint8_t* sV = sK + NFK * NC * CH;  // NFV stages: V is held until O += P V
-  uint8_t* sP = sV + NFV * NC * CH;  // 2 key chunks: half h of the rows' keys in chunk h
-  // after the last O += P V the P tile holds the merge values [2 halves][(m, l)][128 rows]
-  float* fin = reinterpret_cast<float*>(sP);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * CH);
+  // the merge values of the two halves of each row [2 halves][(m, l)][128 rows]
+  float* fin = reinterpret_cast<float*>(sV + NFV * NC * CH);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(fin + 512);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;          // [NFK]
   uint64_t* k_empty = k_full + NFK;     // [NFK]
   uint64_t* v_full = k_empty + NFK;     // [NFV]
   uint64_t* v_empty = v_full + NFV;     // [NFV]
   uint64_t* s_full = v_empty + NFV;     // [2]
-  uint64_t* s_empty = s_full + 2;       // [2]
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* o_done = p_full + 1;
+  // [2]: P_j over S buffer j % 2.  One barrier per buffer: tile j + 2's P
+  // needs S_{j+2}, issued only after O += P_j V, so neither barrier can
+  // complete a second phase before the MMA thread has seen the first
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 2;
   uint64_t* fin_ready = o_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin_ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -253,9 +260,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 256);
+      mbar_init(&p_full[i], 256);
     }
-    mbar_init(p_full, 256);
     mbar_init(o_done, 1);
     mbar_init(fin_ready, 256);
     *abort_flag = 0;
@@ -313,32 +319,34 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     if (lane == 0) {
       bool ok = mbar_wait(q_full, 0, abort_flag);
       constexpr uint32_t IS = idesc(128, 128, false, false);
-      constexpr uint32_t IO = idesc(128, HD, false, true);
-      const uint64_t dP = sdesc(su32(sP), 16, 1024), dV = sdesc(su32(sV), CH, 1024);
+      constexpr uint32_t IO = idesc(128, HD, false, true);  // A = P from TMEM, B = V MN-major
+      const uint64_t dV = sdesc(su32(sV), CH, 1024);
       const uint64_t dQ = sdesc(su32(sQ), 16, 1024), dK = sdesc(su32(sK), 16, 1024);
-      // O_0 += P[:, 0:64] V[0:64, :] and O_1 += P[:, 64:128] V[64:128, :]
+      // O_0 += P[:, 0:64] V[0:64, :] and O_1 += P[:, 64:128] V[64:128, :]; P_i
+      // sits over S_i: the 64 keys of half h packed in columns 64 h .. 64 h + 31
       auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(p_full, (uint32_t)(i & 1), abort_flag) ||
+        if (!mbar_wait(&p_full[i & 1], (uint32_t)((i >> 1) & 1), abort_flag) ||
             !mbar_wait(&v_full[i % NFV], (uint32_t)((i / NFV) & 1), abort_flag))
           return false;
         tc_fence_after();
         const uint64_t v = dadv(dV, (i % NFV) * NC * CH);
+        const uint32_t tp = tS[i & 1];
         const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint32_t acc = kk > 0 ? 1u : acc0;
-          tc_mma(tO[0], dadv(dP, kk * 32), dadv(v, kk * 16 * 128), IO, acc);
-          tc_mma(tO[1], dadv(dP, CH + kk * 32), dadv(v, (4 + kk) * 16 * 128), IO, acc);
+          tc_mma_ts(tO[0], tp + (uint32_t)(kk * 8), dadv(v, kk * 16 * 128), IO, acc);
+          tc_mma_ts(tO[1], tp + (uint32_t)(64 + kk * 8), dadv(v, (4 + kk) * 16 * 128), IO, acc);
         }
         tc_commit(o_done);
         tc_commit(&v_empty[i % NFV]);
         return true;
       };
+      // S_j goes into the columns of S_{j-2} / P_{j-2}, whose O += P V was
+      // issued before it (one thread's MMAs run in order)
       for (int j = 0; j < ntiles && ok; ++j) {
         const int s = j % NFK, b = j & 1;
-        const uint32_t u = (uint32_t)(j >> 1);
-        if (!mbar_wait(&k_full[s], (uint32_t)((j / NFK) & 1), abort_flag) ||
-            !mbar_wait(&s_empty[b], (u & 1) ^ 1, abort_flag)) {
+        if (!mbar_wait(&k_full[s], (uint32_t)((j / NFK) & 1), abort_flag)) {
           ok = false;
           break;
         }
@@ -372,9 +380,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     const int r = qw * 32 + lane;
     const int qpos = q0 + r;  // position inside the sequence
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-    float m_old = -INFINITY, l = 0.f;
+    float m_used = -INFINITY, l = 0.f;  // exponent base of this half and the sum relative to it
     bool ok = true;
-    uint8_t* prow = sP + half * CH + (r >> 3) * 1024 + (r & 7) * 128;
     for (int j = 0; j < ntiles; ++j) {
       const int b = j & 1;
       const uint32_t u = (uint32_t)(j >> 1);
@@ -388,8 +395,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       tmem_ld32_nw(tS[b] + lane_off + half * 64, sr[0]);
       tmem_ld32_nw(tS[b] + lane_off + half * 64 + 32, sr[1]);
       tmem_wait_ld2(sr[0], sr[1]);
-      tc_fence_before();
-      mbar_arrive(&s_empty[b]);
       float sv[64];
       const int kbase = 128 * j + 64 * half;
       // only the diagonal tile and a tile crossing the sequence end need masking
@@ -407,56 +412,58 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       // eight independent chains instead of one 64-long dependency chain
       float mx8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = m_old;
+      for (int k = 0; k < 8; ++k) mx8[k] = sv[k];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
+      for (int i = 8; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float base = mx == -INFINITY ? 0.f : mx;
-      const float alpha = ex2(m_old - base);  // 0 when m_old = -inf
-      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        sv[i] = ex2(sv[i] - base);
-        sum8[i & 7] += sv[i];
+      // lazy base: move it only when this tile's max exceeds it by more than
+      // 2^8 (always on the first tile with a key); P = 2^(s - base) <= 2^8
+      const bool move = mx > m_used + 8.f;
+      const float alpha = move ? ex2(m_used - mx) : 1.f;  // 0 when m_used = -inf
+      if (move) {
+        m_used = mx;
+        l *= alpha;
       }
-      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-      l = l * alpha + sum;
-      // P_{j-1} consumed and O written by the previous PV before we touch them
-      if (j > 0) {
+      // O_half of rows whose base moved is rescaled once the previous P V has
+      // landed in it (warp-collective TMEM traffic: the whole warp joins)
+      if (j > 0 && __any_sync(0xffffffffu, move)) {
         if (!__all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)((j - 1) & 1), abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, mx > m_old)) {
 #pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            float t[32];
-            tmem_ld32(tO[half] + lane_off + c * 32, t);
+        for (int c = 0; c < HD / 32; ++c) {
+          float t[32];
+          tmem_ld32(tO[half] + lane_off + c * 32, t);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) t[i] *= alpha;
-            tmem_st32(tO[half] + lane_off + c * 32, t);
-          }
+          for (int i = 0; i < 32; ++i) t[i] *= alpha;
+          tmem_st32(tO[half] + lane_off + c * 32, t);
         }
       }
-      m_old = mx;
-      // P row half into the 128B-swizzled K-major tile: 16-byte unit u of
-      // row r sits at unit (u ^ (r % 8)) of the row
+      const float base = m_used == -INFINITY ? 0.f : m_used;
+      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      uint32_t pw[32];
 #pragma unroll
-      for (int uu = 0; uu < 8; ++uu) {
-        const float* p = sv + uu * 8;
-        const uint4 v = make_uint4(pack2(p[0], p[1]), pack2(p[2], p[3]), pack2(p[4], p[5]), pack2(p[6], p[7]));
-        *reinterpret_cast<uint4*>(prow + ((uu ^ (r & 7)) << 4)) = v;
+      for (int i = 0; i < 64; i += 2) {
+        const float p0 = ex2(sv[i] - base), p1 = ex2(sv[i + 1] - base);
+        sum8[i & 7] += p0;
+        sum8[(i + 1) & 7] += p1;
+        pw[i >> 1] = pack2(p0, p1);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      // P_j (BF16 pairs) over this half's first 32 columns of S_j, which this
+      // thread has already read: the A operand of the next O += P V
+      tmem_st32u(tS[b] + lane_off + half * 64, pw);
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[b]);
     }
+    const float m_old = m_used;
     // merge the two halves of the row: m = max(m_0, m_1), c_h = 2^(m_h - m),
     // l = l_0 c_0 + l_1 c_1, O = (O_0 c_0 + O_1 c_1) / l; each half writes
-    // half of the hd columns
-    // the last O += P V has read the P tile before it is reused for the merge
+    // half of the hd columns, once the last O += P V has landed
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)((ntiles - 1) & 1), abort_flag));
     if (ok) {
       fin[(half * 2) * 128 + r] = m_old;
@@ -1166,7 +1173,7 @@ void init_once() {
 
 template <int HD>
 constexpr int smem_bytes() {
-  return (HD / 64) * 16384 * (1 + NFK + NFV) + 2 * 16384 + 1024 + 256;
+  return (HD / 64) * 16384 * (1 + NFK + NFV) + 2048 + 1024 + 256;
 }
 
 template <int HD>
