@@ -395,6 +395,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       tmem_ld32_nw(tS[b] + lane_off + half * 64, sr[0]);
       tmem_ld32_nw(tS[b] + lane_off + half * 64 + 32, sr[1]);
       tmem_wait_ld2(sr[0], sr[1]);
+      // raw scores (masked ones -inf); the exp2-domain scale enters once, in
+      // the max and in one FMA per score before ex2 (scale_log2 > 0)
       float sv[64];
       const int kbase = 128 * j + 64 * half;
       // only the diagonal tile and a tile crossing the sequence end need masking
@@ -403,11 +405,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           const int key = kbase + i;
-          sv[i] = (key > qpos || key >= S) ? -INFINITY : __uint_as_float(sr[i >> 5][i & 31]) * scale_log2;
+          sv[i] = (key > qpos || key >= S) ? -INFINITY : __uint_as_float(sr[i >> 5][i & 31]);
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) sv[i] = __uint_as_float(sr[i >> 5][i & 31]) * scale_log2;
+        for (int i = 0; i < 64; ++i) sv[i] = __uint_as_float(sr[i >> 5][i & 31]);
       }
       // eight independent chains instead of one 64-long dependency chain
       float mx8[8];
@@ -416,7 +418,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
 #pragma unroll
       for (int i = 8; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * scale_log2;
       // lazy base: move it only when this tile's max exceeds it by more than
       // 2^8 (always on the first tile with a key); P = 2^(s - base) <= 2^8
       const bool move = mx > m_used + 8.f;
@@ -447,7 +449,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       uint32_t pw[32];
 #pragma unroll
       for (int i = 0; i < 64; i += 2) {
-        const float p0 = ex2(sv[i] - base), p1 = ex2(sv[i + 1] - base);
+        const float p0 = ex2(fmaf(sv[i], scale_log2, -base)), p1 = ex2(fmaf(sv[i + 1], scale_log2, -base));
         sum8[i & 7] += p0;
         sum8[(i + 1) & 7] += p1;
         pw[i >> 1] = pack2(p0, p1);
