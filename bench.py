@@ -208,6 +208,54 @@ def static_schedule(m, vis_ms, bw, hbw, slabs):
                     "host Adam throughput is not in its model"}
 
 
+def _union(iv):
+    """Total length of the union of intervals [(t0, t1), ...]."""
+    tot, end = 0.0, None
+    for a, b in sorted(iv):
+        if end is None or a > end:
+            tot += b - a
+            end = b
+        elif b > end:
+            tot += b - end
+            end = b
+    return tot
+
+
+def _overlap(x, y):
+    """Length of union(x) intersected with union(y)."""
+    return _union(x) + _union(y) - _union(x + y)
+
+
+def timeline(m, tok, step, path=""):
+    """One extra step (outside the timed region) with the stream timeline
+    on: busy fractions of the weight, compute and gradient streams and of
+    host Adam over the step's span (first copy to last Adam job), and how
+    much of the weight stream's copying overlaps compute (the pages' overlap
+    ratio)."""
+    m.set_tokens(tok)
+    m.trace(True)
+    m.train_step(step, want_loss=False)
+    m.sync()
+    ev = m.trace_events()
+    m.trace(False)
+    if path:
+        with open(path, "w") as f:
+            json.dump({"traceEvents": ev}, f)
+    by = {}
+    for e in ev:
+        by.setdefault(e["tid"], []).append((e["ts"] / 1e3, (e["ts"] + e["dur"]) / 1e3))
+    allv = [iv for v in by.values() for iv in v]
+    if not allv:
+        return None
+    t0, t1 = min(a for a, _ in allv), max(b for _, b in allv)  # first copy .. last Adam
+    span = t1 - t0
+    busy = {k: _union(v) / span for k, v in by.items()}
+    w, c = by.get("weight stream", []), by.get("compute stream", [])
+    return {"span_ms": span, "busy_frac": busy,
+            "weight_copy_overlapped_by_compute": _overlap(w, c) / max(_union(w), 1e-9),
+            "events": len(ev), "file": path or None}
+
+
 def cpu_model() -> str:
     """CPU model of this host (lscpu's model name, else /proc/cpuinfo)."""
     try:
@@ -340,6 +388,7 @@ def main():
     ap.add_argument("--ckpt-interval", type=int, default=1, help="layers per recompute segment")
     ap.add_argument("--buffers", type=int, default=2, help="device weight buffers (1: single-buffer ablation)")
     ap.add_argument("--layers", type=int, default=0, help="decoder depth override (depth sweeps; 0 = the config's)")
+    ap.add_argument("--trace", default="", help="write the stream timeline of one extra step (Chrome trace JSON)")
     ap.add_argument("--host-accum", type=int, default=0,
                     help="1: one pass per micro-batch, gradients summed in FP32 on the host")
     ap.add_argument("--set", action="append", default=[], metavar="KEY=VALUE",
@@ -537,6 +586,7 @@ def main():
                  "last_loss": losses[-1]},
     }
     line["schedule"] = static_schedule(m, vis_ms, bw, hbw, args.slabs)
+    line["timeline"] = timeline(m, toks[step % len(toks)], step, args.trace)
     if c.get("n_experts"):
         # routed experts of the last forward: how many experts each layer's
         # stream-ins copied, and the load of the busiest expert over the mean

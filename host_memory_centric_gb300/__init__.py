@@ -116,6 +116,10 @@ def lib():
         "mt_timing": (i32, [_v, i32]),
         "mt_timing_read": (i32, [_v, i32, _P(i64), _P(f64), _P(f64), _P(f64)]),
         "mt_timing_visits": (i32, [_v, _P(f64), i32, _P(i32)]),
+        "mt_trace": (i32, [_v, i32]),
+        "mt_save": (i32, [_v, C.c_char_p]),
+        "mt_load": (i32, [_v, C.c_char_p]),
+        "mt_trace_json": (i64, [_v, C.c_char_p, i64]),
         "mt_gemm": (i32, [_v, i64, i32, _v, i64, i32, i32, i32, i32, _v, i64, _v, i64, _v, i64, i32, _v]),
         "mt_gemm2": (i32, [_P(_v), _P(i64), _P(i32), _P(_v), _P(i64), _P(i32), _P(i32), _P(i32), _P(i32),
                             _P(_v), _P(i64), _v]),
@@ -309,6 +313,28 @@ class Model:
         n = C.c_int64(); ms = C.c_double(); fl = C.c_double(); by = C.c_double()
         check(lib().mt_timing_read(self.h, kind, C.byref(n), C.byref(ms), C.byref(fl), C.byref(by)), self.h)
         return dict(launches=n.value, ms=ms.value, flops=fl.value, bytes=by.value)
+
+    def save(self, path: str):
+        """Write the host store and the step count (mt_save)."""
+        check(lib().mt_save(self.h, os.fsencode(path)), self.h)
+
+    def load(self, path: str):
+        """Resume from a file written by save() for a model of this shape."""
+        check(lib().mt_load(self.h, os.fsencode(path)), self.h)
+
+    def trace(self, on: bool):
+        """Start (clearing it) or stop the stream timeline (mt_trace)."""
+        check(lib().mt_trace(self.h, int(on)), self.h)
+
+    def trace_events(self) -> list[dict]:
+        """The recorded timeline as Chrome trace events (ts / dur in us)."""
+        import json
+        need = -lib().mt_trace_json(self.h, None, 0)
+        if need <= 0:
+            return []
+        buf = C.create_string_buffer(int(need) + 1)
+        n = lib().mt_trace_json(self.h, buf, need + 1)
+        return json.loads(buf.value.decode())["traceEvents"] if n > 0 else []
 
     def timing_visits(self) -> np.ndarray:
         """Mean compute time (ms) of each visit of the step over the timed steps."""

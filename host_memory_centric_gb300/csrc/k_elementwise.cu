@@ -70,15 +70,17 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_k(const bf16* __restrict__ x,
 
 // Each block owns a contiguous run of rows; dgamma partial sums for its rows
 // go to partial[blockIdx.x][H].
+// dx per row (one warp per row; the row's dot product needs the whole row),
+// then this block's dgamma partial column by column: thread t owns 8
+// consecutive columns and sums its block's rows in row order, so the result
+// does not depend on warp scheduling (the rows were just read: the second read
+// hits L2).
 __global__ void __launch_bounds__(256) rmsnorm_bwd_k(const bf16* __restrict__ dy, const bf16* __restrict__ x,
                                                      const bf16* __restrict__ g, const float* __restrict__ rstd,
                                                      const bf16* __restrict__ dres, int64_t T, int H,
                                                      int64_t rows_per_block, bf16* __restrict__ dx,
                                                      float* __restrict__ partial) {
-  extern __shared__ float part[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) part[c] = 0.f;
-  __syncthreads();
   const int64_t r0 = (int64_t)blockIdx.x * rows_per_block;
   const int64_t r1 = min(T, r0 + rows_per_block);
   for (int64_t row = r0 + warp; row < r1; row += ROW_WARPS) {
@@ -108,15 +110,24 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_k(const bf16* __restrict__ dy
         for (int k = 0; k < 8; ++k) o[k] = 0.f;
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        o[k] += r * w[k] * a[k] - c3 * b[k];
-        atomicAdd(&part[c + k], a[k] * b[k] * r);
-      }
+      for (int k = 0; k < 8; ++k) o[k] += r * w[k] * a[k] - c3 * b[k];
       *reinterpret_cast<uint4*>(dx + row * H + c) = pack8(o);
     }
   }
-  __syncthreads();
-  for (int c = threadIdx.x; c < H; c += blockDim.x) partial[(int64_t)blockIdx.x * H + c] = part[c];
+  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int64_t row = r0; row < r1; ++row) {
+      float a[8], b[8];
+      unpack8(*reinterpret_cast<const uint4*>(dy + row * H + c), a);
+      unpack8(*reinterpret_cast<const uint4*>(x + row * H + c), b);
+      const float r = rstd[row];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] += a[k] * b[k] * r;
+    }
+    float4* p = reinterpret_cast<float4*>(partial + (int64_t)blockIdx.x * H + c);
+    p[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    p[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
 }
 
 __global__ void rmsnorm_bwd_stage2_k(const float* __restrict__ partial, int nblk, int H, bf16* __restrict__ dg) {
@@ -372,12 +383,8 @@ cudaError_t rmsnorm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const 
     return cudaErrorInvalidValue;
   const int nblk = rmsnorm_bwd_blocks(T);
   const int64_t per = (T + nblk - 1) / nblk;
-  const size_t sm = (size_t)H * sizeof(float);
-  if (sm > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(rmsnorm_bwd_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (e != cudaSuccess) return e;
-  }
-  rmsnorm_bwd_k<<<nblk, 256, sm, s>>>(dy, x, gamma, rstd, dres, T, H, per, dx, partial);
+  if (reinterpret_cast<uintptr_t>(partial) & 15) return cudaErrorInvalidValue;
+  rmsnorm_bwd_k<<<nblk, 256, 0, s>>>(dy, x, gamma, rstd, dres, T, H, per, dx, partial);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return rmsnorm_bwd_stage2(partial, nblk, H, dgamma, s);

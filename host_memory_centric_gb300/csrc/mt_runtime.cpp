@@ -17,6 +17,7 @@
 // [Review] 3-2 (3)-(6)).  No host barrier sits on the path: every host wait
 // is on a specific event or slab, with a deadline.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <sys/mman.h>
 
 #include <chrono>
@@ -235,6 +236,25 @@ struct mt_model {
   std::vector<cudaEvent_t> ev_pool;
   KStat kstat[4];
   std::vector<KStat> vstat;  // per visit of the step: compute-stream time of its compute part
+  // stream timeline (mt_trace): device intervals as event pairs on the stream
+  // that ran them, host Adam jobs as wall-clock intervals
+  struct TraceDev {
+    cudaEvent_t a, b;
+    char stream;
+    int op, block;
+    int64_t step;
+  };
+  struct TraceHost {
+    double t0, t1;
+    int block, pass;
+    int64_t step;
+  };
+  std::atomic<bool> tracing{false};
+  cudaEvent_t trace_base = nullptr;
+  double trace_host_base = 0;
+  std::vector<TraceDev> tdev;
+  std::mutex tmu;  // thost is appended by the Adam dispatcher
+  std::vector<TraceHost> thost;
 
   ~mt_model();
 };
@@ -413,6 +433,43 @@ void collect_timing(mt_model* m) {
   }
   m->pend.clear();
 }
+
+// Timeline ops: weights (and checkpoint) in, routed experts in, a visit's
+// compute (10 + visit kind), gradients out, checkpoint out.
+enum { TR_H2D = 0, TR_H2D_EXP = 1, TR_D2H = 3, TR_D2H_CKPT = 4, TR_COMPUTE = 10 };
+// An NVTX range over a scope (visible to profilers attached to the process;
+// inert otherwise).
+struct Nvtx {
+  explicit Nvtx(const char* fmt, int a, int b = -1) {
+    char name[48];
+    std::snprintf(name, sizeof name, fmt, a, b);
+    nvtxRangePushA(name);
+  }
+  ~Nvtx() { nvtxRangePop(); }
+};
+
+// An event pair around the work enqueued on stream s inside its scope, kept
+// when the timeline is on.
+struct TraceSpan {
+  mt_model* m;
+  cudaStream_t s;
+  char stream;
+  int op, block;
+  cudaEvent_t a = nullptr;
+  TraceSpan(mt_model* mm, cudaStream_t ss, char st, int o, int j) : m(mm), s(ss), stream(st), op(o), block(j) {
+    if (m->live && m->tracing) {
+      a = take_event(m);
+      cudaEventRecord(a, s);
+    }
+  }
+  ~TraceSpan() {
+    if (a) {
+      cudaEvent_t b = take_event(m);
+      cudaEventRecord(b, s);
+      m->tdev.push_back({a, b, stream, op, block, m->steps_done});
+    }
+  }
+};
 
 // ---------------------------------------------------------------- GEMM forms
 enum { K_GEMM = 0, K_ATTN_F = 1, K_ATTN_B = 2, K_OTHER = 3 };
@@ -786,6 +843,7 @@ void adam_loop(mt_model* m) {
     idle = false;
     if (const int d = g_inj_adam_delay_ms.load()) std::this_thread::sleep_for(std::chrono::milliseconds(d));
     const auto t0 = Clock::now();
+    Nvtx range("ADAM block %d (slab %d)", job.block, job.slab);
     mt_status st = m->failed ? MT_ERR_STATE : wait_event(m, m->SR[(size_t)job.slab], "slab ready");
     if (st == MT_OK) {
       const mth::BlockDesc& b = m->lay[(size_t)job.block];
@@ -842,6 +900,12 @@ void adam_loop(mt_model* m) {
         st = set_err(m, MT_ERR_INTERNAL, "host Adam worker: " + werr);
     }
     m->adam_us += std::chrono::duration_cast<std::chrono::microseconds>(Clock::now() - t0).count();
+    if (m->tracing) {
+      const double a = std::chrono::duration<double, std::milli>(t0.time_since_epoch()).count();
+      const double e = now_ms();
+      std::lock_guard<std::mutex> lk(m->tmu);
+      m->thost.push_back({a - m->trace_host_base, e - m->trace_host_base, job.block, job.pass, (int64_t)job.t - 1});
+    }
     {
       std::lock_guard<std::mutex> lk(m->amu);
       if (st == MT_OK && job.pass + 1 == m->npass) m->adam_done[(size_t)job.block] = job.t;
@@ -979,6 +1043,7 @@ mt_status do_stream_in(mt_model* m, int j, int b) {
   }
   logop(m, "W", "WAIT_BF", b, -1);
   if (m->live) CU(m, cudaStreamWaitEvent(m->sw, m->BF[b], 0));
+  std::unique_ptr<TraceSpan> trace_in(new TraceSpan(m, m->sw, 'W', TR_H2D, j));
   if (copies) {
     logop(m, "W", "H2D", j, b);
     if (m->live)
@@ -1001,6 +1066,7 @@ mt_status do_stream_in(mt_model* m, int j, int b) {
       m->h2d += (int64_t)bytes;
     }
   }
+  trace_in.reset();  // the span ends before Weights-Ready releases the compute stream
   logop(m, "W", "REC_WR", b, -1);
   if (m->live) CU(m, cudaEventRecord(m->WR[b], m->sw));
   m->used[b] = true;
@@ -1057,11 +1123,13 @@ mt_status moe_forward_visit(mt_model* m, int j, int b) {
     }
   }
   logop(m, "W", "H2D_EXP", j, b);
-  if (m->live)
+  if (m->live) {
+    TraceSpan trace_exp(m, m->sw, 'W', TR_H2D_EXP, j);
     for (const Range& r : rg) {
       CU(m, cudaMemcpyAsync(m->d.buf[b] + r.off, src + r.off, (size_t)r.bytes, cudaMemcpyHostToDevice, m->sw));
       m->h2d += r.bytes;
     }
+  }
   logop(m, "W", "REC_ER", b, -1);
   if (m->live) CU(m, cudaEventRecord(m->ER[b], m->sw));
   logop(m, "C", "WAIT_ER", b, -1);
@@ -1081,6 +1149,7 @@ mt_status do_forward(mt_model* m, int j, int b) {
     if (m->live) CU(m, cudaStreamWaitEvent(m->sc, m->XS[j % 2], 0));
   }
   logop(m, "C", head ? "HEAD" : "FWD", j, b);
+  std::unique_ptr<TraceSpan> trace_c(new TraceSpan(m, m->sc, 'C', TR_COMPUTE + (head ? V_HEAD : V_FWD), j));
   if (moe_block(m, j)) {
     OK(moe_forward_visit(m, j, b));
   } else if (m->live) {
@@ -1095,6 +1164,7 @@ mt_status do_forward(mt_model* m, int j, int b) {
       OK(head_forward_backward(m, v, x_fwd_in(m, j), m->d.dx[m->L % 2]));
     }
   }
+  trace_c.reset();  // the span ends before the events that release other streams
   const bool saves = writes_x && j < m->L && j % m->ci == 0 && ckh;
   if (saves) {
     logop(m, "C", "REC_XR", j % 2, -1);
@@ -1113,6 +1183,7 @@ mt_status do_forward(mt_model* m, int j, int b) {
     if (m->live) CU(m, cudaStreamWaitEvent(m->sg, m->XR[s], 0));
     logop(m, "G", "D2H_CKPT", j, s);
     if (m->live) {
+      TraceSpan trace_ck(m, m->sg, 'G', TR_D2H_CKPT, j);
       const size_t bytes = (size_t)m->T * m->H * 2;
       CU(m, cudaMemcpyAsync(m->ckpt + (size_t)(j / m->ci) * bytes, m->d.xslot[s], bytes, cudaMemcpyDeviceToHost,
                             m->sg));
@@ -1128,7 +1199,10 @@ mt_status do_forward(mt_model* m, int j, int b) {
 mt_status do_recompute(mt_model* m, int j, int b) {
   const int seg = m->plan[(size_t)m->vis].seg;
   logop(m, "C", "RECOMP", j, b);
-  if (m->live) OK(decoder_forward(m, make_view(m, j, b), x_seg_in(m, j, seg), x_seg_out(m, j), false, j));
+  if (m->live) {
+    TraceSpan trace_c(m, m->sc, 'C', TR_COMPUTE + V_RECOMP, j);
+    OK(decoder_forward(m, make_view(m, j, b), x_seg_in(m, j, seg), x_seg_out(m, j), false, j));
+  }
   logop(m, "C", "REC_BF", b, -1);
   if (m->live) CU(m, cudaEventRecord(m->BF[b], m->sc));
   return MT_OK;
@@ -1137,6 +1211,7 @@ mt_status do_recompute(mt_model* m, int j, int b) {
 mt_status do_backward(mt_model* m, int j, int b) {
   logop(m, "C", "BWD", j, b);
   if (m->live) {
+    TraceSpan trace_c(m, m->sc, 'C', TR_COMPUTE + V_BWD, j);
     const View v = make_view(m, j, b);
     if (j == 0) {
       Timed t(m, K_OTHER, 0, 2.0 * m->T * m->H + 2.0 * m->V * m->H);
@@ -1160,12 +1235,14 @@ mt_status do_stream_out(mt_model* m, int j, int b, int* slab_out) {
   if (m->live) OK(acquire_slab(m, &k));
   logop(m, "H", "ACQ_SLAB", k, -1);
   logop(m, "G", "D2H", j, k);
-  if (m->live)  // an MoE block exports the shared tensors and the routed experts only
+  if (m->live) {  // an MoE block exports the shared tensors and the routed experts only
+    TraceSpan trace_out(m, m->sg, 'G', TR_D2H, j);
     for (const Range& r : block_ranges(m, j, true, true)) {
       CU(m, cudaMemcpyAsync(m->slabs + (size_t)k * m->wb_max + r.off, m->d.buf[b] + bd.region[1] + r.off,
                             (size_t)r.bytes, cudaMemcpyDeviceToHost, m->sg));
       m->d2h += r.bytes;
     }
+  }
   logop(m, "G", "REC_BF", b, -1);
   if (m->live) CU(m, cudaEventRecord(m->BF[b], m->sg));
   logop(m, "G", "REC_SR", k, -1);
@@ -1225,6 +1302,9 @@ mt_status expect(mt_model* m, int stage, int block) {
 
 mt_status run_visit(mt_model* m) {
   const int v = m->vis, j = visit_block(m, v), b = v % m->nbuf, kind = visit_kind(m, v);
+  static const char* kname[] = {"FWD %d (buffer %d)", "HEAD %d (buffer %d)", "RECOMP %d (buffer %d)",
+                                "BWD %d (buffer %d)"};
+  Nvtx range(kname[kind], j, b);
   OK(do_stream_in(m, j, b));
   advance(m);
   OK(do_bind(m, j, b, nullptr));
@@ -1312,6 +1392,11 @@ mt_model::~mt_model() {
       cudaEventDestroy(p.b);
     }
     for (auto e : ev_pool) cudaEventDestroy(e);
+    for (auto& t : tdev) {
+      cudaEventDestroy(t.a);
+      cudaEventDestroy(t.b);
+    }
+    if (trace_base) cudaEventDestroy(trace_base);
     if (registered) cudaHostUnregister(store);
     for (int b = 0; b < 2; ++b)
       if (staging[b]) cudaFreeHost(staging[b]);
@@ -1636,6 +1721,78 @@ mt_status mt_get_stats(const mt_model* m, mt_stats* o) {
   return MT_OK;
 }
 
+// ---------------------------------------------------------------- save / load
+// Between steps the GPU holds no model state: the host store (W, G, master,
+// m, v of every block) and the step count are the whole training state.
+namespace {
+constexpr char kMagic[8] = {'M', 'T', 'S', 'T', 'O', 'R', 'E', '1'};
+struct FileHeader {
+  char magic[8];
+  int32_t shape[10];  // n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab, n_experts, top_k, expert_ffn
+  int64_t steps_done, store_bytes;
+};
+void fill_header(const mt_model* m, FileHeader* h) {
+  std::memset(h, 0, sizeof *h);
+  std::memcpy(h->magic, kMagic, 8);
+  const mt_config& c = m->c;
+  const int32_t v[10] = {c.n_layers, c.hidden, c.n_heads, c.n_kv_heads, c.head_dim, c.ffn, c.vocab,
+                         c.n_experts, c.top_k, c.expert_ffn};
+  std::memcpy(h->shape, v, sizeof v);
+  h->steps_done = m->steps_done;
+  h->store_bytes = (int64_t)m->store_bytes;
+}
+mt_status between_steps(mt_model* m) {
+  if (m->failed) return MT_ERR_STATE;
+  if (m->vis != 0 || m->stage != 0 || m->pass != 0)
+    return set_err(m, MT_ERR_STATE, "save / load only between steps", false);
+  return mt_sync(m);
+}
+}  // namespace
+
+mt_status mt_save(mt_model* m, const char* path) {
+  if (!m || !path) return MT_ERR_ARG;
+  OK(between_steps(m));
+  FileHeader h;
+  fill_header(m, &h);
+  FILE* f = std::fopen(path, "wb");
+  if (!f) return set_err(m, MT_ERR_ARG, std::string("cannot open ") + path, false);
+  bool ok = std::fwrite(&h, sizeof h, 1, f) == 1;
+  constexpr size_t CH = (size_t)64 << 20;
+  for (size_t o = 0; ok && o < m->store_bytes; o += CH)
+    ok = std::fwrite(m->store + o, 1, std::min(CH, m->store_bytes - o), f) == std::min(CH, m->store_bytes - o);
+  ok = (std::fclose(f) == 0) && ok;
+  if (!ok) return set_err(m, MT_ERR_INTERNAL, std::string("write failed: ") + path, false);
+  return MT_OK;
+}
+
+mt_status mt_load(mt_model* m, const char* path) {
+  if (!m || !path) return MT_ERR_ARG;
+  OK(between_steps(m));
+  FileHeader want, got;
+  fill_header(m, &want);
+  FILE* f = std::fopen(path, "rb");
+  if (!f) return set_err(m, MT_ERR_ARG, std::string("cannot open ") + path, false);
+  if (std::fread(&got, sizeof got, 1, f) != 1 || std::memcmp(got.magic, kMagic, 8) ||
+      std::memcmp(got.shape, want.shape, sizeof want.shape) || got.store_bytes != want.store_bytes || got.steps_done < 0) {
+    std::fclose(f);
+    return set_err(m, MT_ERR_ARG, std::string("not a saved store of this model's shape: ") + path, false);
+  }
+  bool ok = true;
+  constexpr size_t CH = (size_t)64 << 20;
+  for (size_t o = 0; ok && o < m->store_bytes; o += CH)
+    ok = std::fread(m->store + o, 1, std::min(CH, m->store_bytes - o), f) == std::min(CH, m->store_bytes - o);
+  std::fclose(f);
+  // a short read leaves a partly overwritten store: the model cannot continue
+  if (!ok) return set_err(m, MT_ERR_INTERNAL, std::string("read failed: ") + path);
+  m->steps_done = got.steps_done;
+  {
+    std::lock_guard<std::mutex> lk(m->amu);
+    for (auto& d : m->adam_done) d = got.steps_done;  // Adam of every block is in the store
+  }
+  m->tokens_set = false;
+  return MT_OK;
+}
+
 mt_status mt_expert_counts(const mt_model* m, int32_t block, int32_t* counts, int32_t n) {
   if (!m || !counts || !m->moe || block < 1 || block > m->L || n < m->E) return MT_ERR_ARG;
   std::memcpy(counts, m->hcounts + (size_t)block * m->E, (size_t)m->E * 4);
@@ -1818,6 +1975,66 @@ mt_status mt_timing(mt_model* m, int32_t enable) {
   for (auto& k : m->kstat) k = KStat();
   m->vstat.assign((size_t)nvisits(m), KStat());
   return MT_OK;
+}
+
+mt_status mt_trace(mt_model* m, int32_t enable) {
+  if (!m) return MT_ERR_ARG;
+  OK(mt_sync(m));
+  if (!enable) {
+    m->tracing = false;
+    return MT_OK;
+  }
+  for (auto& t : m->tdev) {
+    m->ev_pool.push_back(t.a);
+    m->ev_pool.push_back(t.b);
+  }
+  m->tdev.clear();
+  {
+    std::lock_guard<std::mutex> lk(m->tmu);
+    m->thost.clear();
+  }
+  // all three streams are idle here: device time 0 and host time 0 coincide
+  if (!m->trace_base) CU(m, cudaEventCreate(&m->trace_base));
+  CU(m, cudaEventRecord(m->trace_base, m->sc));
+  CU(m, cudaEventSynchronize(m->trace_base));
+  m->trace_host_base = now_ms();
+  m->tracing = true;
+  return MT_OK;
+}
+
+int64_t mt_trace_json(mt_model* m, char* buf, int64_t cap) {
+  if (!m || m->failed) return 0;
+  static const char* names[] = {"H2D", "H2D_EXP", "", "D2H", "D2H_CKPT"};
+  static const char* kinds[] = {"FWD", "HEAD", "RECOMP", "BWD"};
+  std::string js = "{\"traceEvents\":[";
+  bool first = true;
+  char line[256];
+  auto add = [&](const char* name, const char* tid, double t0, double t1, int block, int64_t step) {
+    std::snprintf(line, sizeof line,
+                  "%s{\"name\":\"%s %d\",\"cat\":\"%s\",\"ph\":\"X\",\"ts\":%.3f,\"dur\":%.3f,\"pid\":0,"
+                  "\"tid\":\"%s\",\"args\":{\"block\":%d,\"step\":%lld}}",
+                  first ? "" : ",", name, block, tid, t0 * 1e3, (t1 - t0) * 1e3, tid, block, (long long)step);
+    js += line;
+    first = false;
+  };
+  for (const auto& t : m->tdev) {
+    float a = 0, b = 0;
+    if (cudaEventElapsedTime(&a, m->trace_base, t.a) != cudaSuccess ||
+        cudaEventElapsedTime(&b, m->trace_base, t.b) != cudaSuccess)
+      continue;  // not yet complete
+    const char* name = t.op >= TR_COMPUTE ? kinds[t.op - TR_COMPUTE] : names[t.op];
+    const char* tid = t.stream == 'W' ? "weight stream" : t.stream == 'C' ? "compute stream" : "gradient stream";
+    add(name, tid, a, b, t.block, t.step);
+  }
+  {
+    std::lock_guard<std::mutex> lk(m->tmu);
+    for (const auto& h : m->thost) add(h.pass + 1 < m->npass ? "ACCUM" : "ADAM", "host Adam", h.t0, h.t1, h.block, h.step);
+  }
+  js += "]}";
+  const int64_t need = (int64_t)js.size() + 1;
+  if (!buf || cap < need) return -need;
+  std::memcpy(buf, js.c_str(), (size_t)need);
+  return need - 1;
 }
 
 mt_status mt_timing_visits(mt_model* m, double* ms, int32_t cap, int32_t* n_visits) {

@@ -190,6 +190,18 @@ mt_status mt_sync(mt_model* model);
 mt_status mt_read_host(mt_model* model, int32_t block, int32_t region, void* dst, size_t bytes);
 mt_status mt_write_host(mt_model* model, int32_t block, int32_t region, const void* src, size_t bytes);
 mt_status mt_get_stats(const mt_model* model, mt_stats* out);
+/* Save / resume.  Between steps the GPU holds no model state, so the host
+ * store (every block's W, G, master, m, v) and the number of steps done are
+ * the whole training state.  mt_save drains all work and writes them to a
+ * file (a 64-byte header: magic, the model shape, steps done, store size;
+ * then the store); mt_load reads such a file into a model of the same shape
+ * and continues from its step count (the next mt_train_step takes that
+ * index; tokens must be set again).  Both only between steps (MT_ERR_STATE
+ * otherwise); a file of another shape or a missing file is MT_ERR_ARG; an
+ * I/O failure while writing is MT_ERR_INTERNAL, while reading it latches
+ * the model (its store is partly overwritten). */
+mt_status mt_save(mt_model* model, const char* path);
+mt_status mt_load(mt_model* model, const char* path);
 /* MoE models: the per-expert token counts (n_experts int32) of block j's
  * last forward (1 <= j <= n_layers), i.e. which experts its stream-ins
  * copied; read after mt_sync.  MT_ERR_ARG for a dense model or a bad j. */
@@ -316,6 +328,18 @@ mt_status mt_timing_read(mt_model* model, int32_t kind, int64_t* launches, doubl
  * *n_visits = n.  These are the per-block compute times the static prefetch
  * schedule (mt_schedule) takes. */
 mt_status mt_timing_visits(mt_model* model, double* ms, int32_t cap, int32_t* n_visits);
+/* Stream timeline.  mt_trace(model, 1) drains all work, clears the timeline
+ * and starts recording: CUDA events around every weight / expert / checkpoint
+ * copy on the weight stream, every visit's compute on the compute stream and
+ * every gradient / checkpoint export on the gradient stream, and the wall
+ * time of every host Adam job, all relative to one instant (the streams are
+ * idle when recording starts).  mt_trace(model, 0) drains and stops.
+ * mt_trace_json writes the timeline (after mt_sync) as Chrome trace-event
+ * JSON ({"traceEvents": [...]}, times in microseconds; threads "weight
+ * stream", "compute stream", "gradient stream", "host Adam"); returns its
+ * length, or -(needed) when cap is too small. */
+mt_status mt_trace(mt_model* model, int32_t enable);
+int64_t mt_trace_json(mt_model* model, char* buf, int64_t cap);
 /* RMSNorm backward that allocates nothing (same results as mt_rmsnorm_bwd).
  * The pages have no counterpart: this is for callers that cannot allocate
  * device memory -- code running during stream capture, code inside another
