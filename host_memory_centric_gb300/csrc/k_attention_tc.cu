@@ -445,16 +445,21 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         }
       }
       const float base = m_used == -INFINITY ? 0.f : m_used;
-      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // paired FP32 arithmetic (two lanes per instruction, each rounded as
+      // the scalar form) for the exponent arguments and the sums
+      const float2 sc2 = make_float2(scale_log2, scale_log2), nb2 = make_float2(-base, -base);
+      float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       uint32_t pw[32];
 #pragma unroll
       for (int i = 0; i < 64; i += 2) {
-        const float p0 = ex2(fmaf(sv[i], scale_log2, -base)), p1 = ex2(fmaf(sv[i + 1], scale_log2, -base));
-        sum8[i & 7] += p0;
-        sum8[(i + 1) & 7] += p1;
-        pw[i >> 1] = pack2(p0, p1);
+        const float2 e = __ffma2_rn(make_float2(sv[i], sv[i + 1]), sc2, nb2);
+        const float2 p = make_float2(ex2(e.x), ex2(e.y));
+        sum2[(i >> 1) & 3] = __fadd2_rn(sum2[(i >> 1) & 3], p);
+        pw[i >> 1] = pack2(p.x, p.y);
       }
-      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
+      const float2 st = __fadd2_rn(s01, s23);
+      l += st.x + st.y;
       // P_j (BF16 pairs) over this half's first 32 columns of S_j, which this
       // thread has already read: the A operand of the next O += P V
       tmem_st32u(tS[b] + lane_off + half * 64, pw);
@@ -791,19 +796,24 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         tmem_ld32_nw(tSt + lane_off + half * 64 + 32, sv[1]);
         tmem_wait_ld2(sv[0], sv[1]);
         uint32_t pw[32];
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
         for (int e4 = 0; e4 < 16; ++e4) {
           const float4 l4 = lrow[e4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-          for (int tt = 0; tt < 4; ++tt) {
-            const int e = e4 * 4 + tt;
-            float pe = ex2(__uint_as_float(sv[e >> 5][e & 31]) * scale_log2 - lv[tt]);
+          for (int hh = 0; hh < 2; ++hh) {  // two paired FMAs: exponent arguments of 4 columns
+            const int e = e4 * 4 + 2 * hh;
+            const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[e >> 5][e & 31]),
+                                                      __uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31])),
+                                          sc2, hh ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y));
+            float pa = ex2(arg.x), pb = ex2(arg.y);
             if (need_mask) {
               const int q = q0 + half * 64 + e;
-              if (q < key || q >= S) pe = 0.f;
+              if (q < key || q >= S) pa = 0.f;
+              if (q + 1 < key || q + 1 >= S) pb = 0.f;
             }
-            p[e] = pe;
+            p[e] = pa;
+            p[e + 1] = pb;
           }
           pw[2 * e4] = pack2(p[4 * e4], p[4 * e4 + 1]);
           pw[2 * e4 + 1] = pack2(p[4 * e4 + 2], p[4 * e4 + 3]);
@@ -828,15 +838,15 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
 #pragma unroll
         for (int e4 = 0; e4 < 16; ++e4) {
           const float4 d4 = drow[e4];
-          const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
-          float dv[4];
 #pragma unroll
-          for (int tt = 0; tt < 4; ++tt) {
-            const int e = e4 * 4 + tt;
-            dv[tt] = p[e] * (__uint_as_float(dp[e >> 5][e & 31]) - dl[tt]);
+          for (int hh = 0; hh < 2; ++hh) {  // dS = P (dP - delta), two columns per paired op
+            const int e = e4 * 4 + 2 * hh;
+            const float2 dd = __fadd2_rn(make_float2(__uint_as_float(dp[e >> 5][e & 31]),
+                                                     __uint_as_float(dp[(e + 1) >> 5][(e + 1) & 31])),
+                                         hh ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y));
+            const float2 v = __fmul2_rn(make_float2(p[e], p[e + 1]), dd);
+            dw[2 * e4 + hh] = pack2(v.x, v.y);
           }
-          dw[2 * e4] = pack2(dv[0], dv[1]);
-          dw[2 * e4 + 1] = pack2(dv[2], dv[3]);
         }
         tmem_st32u(tdPt + lane_off + half * 64, dw);
         tmem_wait_st();
@@ -1087,14 +1097,20 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         tmem_ld32_nw(tS + lane_off + half * 64, sv[0]);
         tmem_ld32_nw(tS + lane_off + half * 64 + 32, sv[1]);
         tmem_wait_ld2(sv[0], sv[1]);
+        const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(-lse2, -lse2);
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          float pe = ex2(__uint_as_float(sv[e >> 5][e & 31]) * scale_log2 - lse2);
+        for (int e = 0; e < 64; e += 2) {
+          const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[e >> 5][e & 31]),
+                                                    __uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31])),
+                                        sc2, nl2);
+          float pa = ex2(arg.x), pb = ex2(arg.y);
           if (need_mask) {
             const int key = k0 + e;
-            if (key > q || key >= S) pe = 0.f;
+            if (key > q || key >= S) pa = 0.f;
+            if (key + 1 > q || key + 1 >= S) pb = 0.f;
           }
-          p[e] = pe;
+          p[e] = pa;
+          p[e + 1] = pb;
         }
         tc_fence_before();
         mbar_arrive(ps_free);
@@ -1111,10 +1127,15 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         tmem_ld32_nw(tP + lane_off + half * 64 + 32, dp[1]);
         tmem_wait_ld2(dp[0], dp[1]);
         uint32_t dw[32];
+        const float2 nd2 = make_float2(-dl, -dl);
 #pragma unroll
-        for (int e = 0; e < 64; e += 2)
-          dw[e / 2] = pack2(p[e] * (__uint_as_float(dp[e >> 5][e & 31]) - dl),
-                            p[e + 1] * (__uint_as_float(dp[(e + 1) >> 5][(e + 1) & 31]) - dl));
+        for (int e = 0; e < 64; e += 2) {
+          const float2 dd = __fadd2_rn(make_float2(__uint_as_float(dp[e >> 5][e & 31]),
+                                                   __uint_as_float(dp[(e + 1) >> 5][(e + 1) & 31])),
+                                       nd2);
+          const float2 v = __fmul2_rn(make_float2(p[e], p[e + 1]), dd);
+          dw[e / 2] = pack2(v.x, v.y);
+        }
         tmem_st32u(tP + lane_off + half * 64, dw);
         tmem_wait_st();
         tc_fence_before();
