@@ -45,7 +45,7 @@ class MtConfig(C.Structure):
                 ("seed", C.c_uint64), ("timeout_ms", C.c_uint32), ("pin_store", C.c_int32),
                 ("head_chunk", C.c_int32), ("log_protocol", C.c_int32), ("keep_host_grad", C.c_int32),
                 ("n_buffers", C.c_int32), ("host_grad_accum", C.c_int32), ("n_experts", C.c_int32),
-                ("top_k", C.c_int32), ("expert_ffn", C.c_int32)]
+                ("top_k", C.c_int32), ("expert_ffn", C.c_int32), ("debug_guards", C.c_int32)]
 
 
 class DevRegion(C.Structure):
@@ -139,6 +139,7 @@ def lib():
         "mt_fault_inject": (i32, [i32, i32]),
         "mt_moe_scratch_bytes": (sz, [i64, i32, i32, i32, i32]),
         "mt_expert_counts": (i32, [_v, i32, _P(i32), i32]),
+        "mt_debug_poke_guard": (i32, [_v, i32, _P(i32)]),
         "mt_moe_ffn": (i32, [_v, _v, _v, _v, _v, i64, i32, i32, i32, i32, _v, _v, _v, _v, _v, _v, _v, sz, _v]),
     }
     for name, (res, args) in sig.items():

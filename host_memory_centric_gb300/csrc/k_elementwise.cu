@@ -138,6 +138,17 @@ __global__ void rmsnorm_bwd_stage2_k(const float* __restrict__ partial, int nblk
   dg[c] = __float2bfloat16_rn(s);
 }
 
+// ------------------------------------------------------------------ debug guards
+// One block per guard; 256 threads compare the 4096 bytes as 16-byte words.
+__global__ void guard_check_k(const uint8_t* __restrict__ base, const int64_t* __restrict__ offs, int n,
+                              int* __restrict__ bad) {
+  const int g = blockIdx.x;
+  if (g >= n) return;
+  const uint4 w = reinterpret_cast<const uint4*>(base + offs[g])[threadIdx.x];
+  const uint32_t k = 0xA5A5A5A5u;
+  if (w.x != k || w.y != k || w.z != k || w.w != k) atomicMin(bad, g);
+}
+
 // ------------------------------------------------------------------ RoPE
 // One thread rotates 8 consecutive frequency pairs of one head of one row.
 __global__ void rope_k(bf16* __restrict__ x, int64_t T, int64_t ld, int n_heads, int hd, int S,
@@ -388,6 +399,12 @@ cudaError_t rmsnorm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return rmsnorm_bwd_stage2(partial, nblk, H, dgamma, s);
+}
+
+cudaError_t guard_check(const uint8_t* base, const int64_t* offs, int n, int* bad, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  guard_check_k<<<n, 256, 0, s>>>(base, offs, n, bad);
+  return cudaGetLastError();
 }
 
 cudaError_t rope(bf16* x, int64_t T, int64_t ld, int n_heads, int hd, int S, const float* cs, int inverse,

@@ -115,6 +115,11 @@ cudaError_t f32_to_bf16_2d(const float* x, int64_t ldx, int64_t rows, int64_t co
                            int64_t ldy, float scale, cudaStream_t s);
 cudaError_t add_bf16(const bf16* a, const bf16* b, int64_t n, bf16* y, cudaStream_t s);
 
+// ---------------------------------------------------------------- debug guards
+// bad[0] = the lowest index g < n whose 4096 bytes at base + offs[g] are not
+// all 0xA5 (left unchanged when every guard is intact).
+cudaError_t guard_check(const uint8_t* base, const int64_t* offs, int n, int* bad, cudaStream_t s);
+
 // ---------------------------------------------------------------- routed MoE
 // Device arrays of one MoE layer's routing (k_moe.cu).  T tokens, E experts
 // (<= 128), k <= 8 of them per token.

@@ -129,7 +129,13 @@ struct Dev {
         *row_loss = nullptr, *loss = nullptr, *rms_part = nullptr, *dwacc = nullptr, *cs = nullptr;
   int32_t *tok = nullptr, *tgt = nullptr, *csr_start = nullptr, *csr_rows = nullptr;
   MoeWs moe;  // routed MoE layers only
+  // debug guards: offset (from the region base) of the 4 KiB canary after
+  // each carved piece, their device copy and the first-bad-guard word
+  std::vector<int64_t> guards;
+  int64_t* guard_offs = nullptr;
+  int* guard_bad = nullptr;
 };
+constexpr int64_t kGuardBytes = 4096;
 
 // One visit of the step: 0 FWD, 1 HEAD (fused forward and backward), 2 RECOMP
 // (forward rebuilding a segment's activations), 3 BWD.  seg numbers the
@@ -249,6 +255,7 @@ struct mt_model {
     int block, pass;
     int64_t step;
   };
+  std::vector<std::pair<uint8_t*, std::string>> hguards;  // pinned host canaries (debug_guards)
   std::atomic<bool> tracing{false};
   cudaEvent_t trace_base = nullptr;
   double trace_host_base = 0;
@@ -326,10 +333,16 @@ size_t carve(const mt_config* c, const std::vector<mth::BlockDesc>& lay, uint8_t
   int64_t wb = 0;
   for (auto& b : lay) wb = b.wbytes > wb ? b.wbytes : wb;
   size_t off = 0;
+  d->guards.clear();
   auto take = [&](int64_t bytes) -> uint8_t* {
     off = (size_t)up((int64_t)off, 256);
     uint8_t* p = base ? base + off : nullptr;
     off += (size_t)bytes;
+    if (c->debug_guards) {  // canary after the piece
+      off = (size_t)up((int64_t)off, 256);
+      d->guards.push_back((int64_t)off);
+      off += (size_t)kGuardBytes;
+    }
     return p;
   };
   const int64_t act = T * H * 2;
@@ -379,6 +392,14 @@ size_t carve(const mt_config* c, const std::vector<mth::BlockDesc>& lay, uint8_t
   d->tgt = (int32_t*)take(T * 4);
   d->csr_start = (int32_t*)take((V + 1) * 4);
   d->csr_rows = (int32_t*)take(T * 4);
+  if (c->debug_guards) {  // the guard table and the first-bad word, themselves unguarded
+    off = (size_t)up((int64_t)off, 256);
+    d->guard_offs = base ? (int64_t*)(base + off) : nullptr;
+    off += d->guards.size() * sizeof(int64_t);
+    off = (size_t)up((int64_t)off, 256);
+    d->guard_bad = base ? (int*)(base + off) : nullptr;
+    off += 256;
+  }
   return (size_t)up((int64_t)off, 256);
 }
 
@@ -1500,26 +1521,36 @@ mt_status mt_init_model(const mt_config* c, mt_dev_region dev, mt_streams s, mt_
     std::string werr;
     if (!m->pool.parallel_for((int64_t)items.size(), fn, &werr)) return MT_ERR_INTERNAL;
   }
+  const size_t gb = c->debug_guards ? (size_t)kGuardBytes : 0;  // canary after each pinned region
+  auto guard = [&](uint8_t* p, size_t bytes, const char* name) {
+    if (!gb) return;
+    std::memset(p + bytes, 0xA5, gb);
+    m->hguards.push_back({p + bytes, name});
+  };
   if (c->pin_store) {
     if (cudaHostRegister(m->store, m->store_bytes, cudaHostRegisterDefault) != cudaSuccess) return MT_ERR_HOST_OOM;
     m->registered = true;
   } else {
     for (int b = 0; b < m->nbuf; ++b) {
-      if (pinned_alloc((void**)&m->staging[b], (size_t)m->wb_max) != cudaSuccess)
+      if (pinned_alloc((void**)&m->staging[b], (size_t)m->wb_max + gb) != cudaSuccess)
         return MT_ERR_HOST_OOM;
       m->pinned_bytes += (size_t)m->wb_max;
+      guard(m->staging[b], (size_t)m->wb_max, b ? "pinned staging 1" : "pinned staging 0");
     }
   }
-  if (pinned_alloc((void**)&m->slabs, (size_t)m->wb_max * m->K) != cudaSuccess)
+  if (pinned_alloc((void**)&m->slabs, (size_t)m->wb_max * m->K + gb) != cudaSuccess)
     return MT_ERR_HOST_OOM;
   m->pinned_bytes += (size_t)m->wb_max * m->K;
+  guard(m->slabs, (size_t)m->wb_max * m->K, "gradient slabs");
   if (c->ckpt_on_host) {
     const size_t bytes = (size_t)m->nseg * m->T * m->H * 2;  // X_0, X_c, X_2c, ...
-    if (pinned_alloc((void**)&m->ckpt, bytes) != cudaSuccess) return MT_ERR_HOST_OOM;
+    if (pinned_alloc((void**)&m->ckpt, bytes + gb) != cudaSuccess) return MT_ERR_HOST_OOM;
     m->pinned_bytes += bytes;
+    guard(m->ckpt, bytes, "host checkpoints");
   }
   const size_t tokb = (size_t)m->npass * (3 * m->T + m->V + 1) * 4;  // per pass: tok | tgt | csr start | csr rows
-  if (pinned_alloc((void**)&m->htok, tokb) != cudaSuccess) return MT_ERR_HOST_OOM;
+  if (pinned_alloc((void**)&m->htok, tokb + gb) != cudaSuccess) return MT_ERR_HOST_OOM;
+  guard((uint8_t*)m->htok, tokb, "pinned tokens");
   if (pinned_alloc((void**)&m->hloss, 64 + 4 * (size_t)m->npass) != cudaSuccess) return MT_ERR_HOST_OOM;
   if (m->npass > 1) {  // host FP32 gradient accumulator, one n_pad range per block
     int64_t n = 0;
@@ -1553,6 +1584,12 @@ mt_status mt_init_model(const mt_config* c, mt_dev_region dev, mt_streams s, mt_
   CU(mm, cudaMemcpyAsync(m->d.cs, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice, m->sc));
   CU(mm, cudaMemsetAsync(m->d.loss, 0, 256, m->sc));
   for (int b = 0; b < m->nbuf; ++b) CU(mm, cudaMemsetAsync(m->d.buf[b], 0, (size_t)2 * m->wb_max, m->sc));
+  if (c->debug_guards) {
+    for (int64_t g : m->d.guards) CU(mm, cudaMemsetAsync(m->dev_base + g, 0xA5, (size_t)kGuardBytes, m->sc));
+    CU(mm, cudaMemcpyAsync(m->d.guard_offs, m->d.guards.data(), m->d.guards.size() * sizeof(int64_t),
+                           cudaMemcpyHostToDevice, m->sc));
+    CU(mm, cudaMemsetAsync(m->d.guard_bad, 0x7F, sizeof(int), m->sc));  // 0x7F7F7F7F: no bad guard
+  }
   CU(mm, cudaStreamSynchronize(m->sc));
   m->adam_thr = std::thread(adam_loop, mm);
   *out = m.release();
@@ -1660,6 +1697,37 @@ mt_status mt_train_step(mt_model* m, int32_t step, float* loss) {
   return MT_OK;
 }
 
+// debug_guards: every canary still 0xA5 (all work drained)?
+static mt_status check_guards(mt_model* m) {
+  const int n = (int)m->d.guards.size();
+  CU(m, mt::guard_check(m->dev_base, m->d.guard_offs, n, m->d.guard_bad, m->sc));
+  int bad = 0;
+  CU(m, cudaMemcpyAsync(&bad, m->d.guard_bad, sizeof bad, cudaMemcpyDeviceToHost, m->sc));
+  CU(m, cudaStreamSynchronize(m->sc));
+  if (bad >= 0 && bad < n)
+    return set_err(m, MT_ERR_INTERNAL, "device guard " + std::to_string(bad) + " (after carved piece " +
+                                           std::to_string(bad) + ", region offset " +
+                                           std::to_string(m->d.guards[(size_t)bad]) + ") overwritten");
+  for (const auto& g : m->hguards)
+    for (int64_t i = 0; i < kGuardBytes; ++i)
+      if (g.first[i] != 0xA5) return set_err(m, MT_ERR_INTERNAL, "host guard after " + g.second + " overwritten");
+  return MT_OK;
+}
+
+mt_status mt_debug_poke_guard(mt_model* m, int32_t which, int32_t* n_guards) {
+  if (!m || !m->c.debug_guards) return MT_ERR_ARG;
+  const int nd = (int)m->d.guards.size(), nh = (int)m->hguards.size();
+  if (n_guards) *n_guards = nd + nh;
+  if (which < 0 || which >= nd + nh) return MT_ERR_ARG;
+  if (which < nd) {
+    CU(m, cudaMemsetAsync(m->dev_base + m->d.guards[(size_t)which], 0, 1, m->sc));
+    CU(m, cudaStreamSynchronize(m->sc));
+  } else {
+    m->hguards[(size_t)(which - nd)].first[0] = 0;
+  }
+  return MT_OK;
+}
+
 mt_status mt_sync(mt_model* m) {
   if (!m) return MT_ERR_ARG;
   if (m->failed) return MT_ERR_STATE;
@@ -1679,6 +1747,7 @@ mt_status mt_sync(mt_model* m) {
     if (!ok) return set_err(m, MT_ERR_TIMEOUT, "timed out draining Adam jobs");
   }
   if (m->timing) collect_timing(m);
+  if (m->c.debug_guards) OK(check_guards(m));
   return MT_OK;
 }
 

@@ -109,6 +109,10 @@ typedef struct {
                               host_grad_accum = 0                           */
   int32_t top_k;
   int32_t expert_ffn;
+  int32_t debug_guards;    /* 1: a 4 KiB canary (0xA5) after every carved device
+                              piece and every pinned host region, checked by
+                              mt_sync: an overwrite latches MT_ERR_INTERNAL
+                              naming the region (overflow / race detector) */
 } mt_config;
 
 typedef struct { void* base; size_t bytes; } mt_dev_region;          /* caller-owned device memory  */
@@ -373,6 +377,11 @@ size_t mt_moe_scratch_bytes(int64_t T, int32_t H, int32_t E, int32_t k, int32_t 
 mt_status mt_moe_ffn(const void* yn, const void* x1, const void* Wr, const void* We, const void* dout, int64_t T,
                      int32_t H, int32_t E, int32_t k, int32_t Fe, void* out, void* dyn, void* dWr, void* dWe,
                      int32_t* idx, float* gate, void* scratch, size_t scratch_bytes, void* stream);
+/* Test hook for debug_guards: overwrites one byte of guard `which` (device
+ * guards first, then the pinned host ones), so that the next mt_sync must
+ * report it.  MT_ERR_ARG without debug_guards or for a bad index; returns the
+ * number of guards through *n_guards when not null. */
+mt_status mt_debug_poke_guard(mt_model* model, int32_t which, int32_t* n_guards);
 /* Host-side fault injection for failure-detection tests (process-wide):
  * kind 1 = every Adam job sleeps `value` ms before it starts (a stalled
  * worker); kind 2 = the next `value` Adam jobs throw inside a worker; kind 3 =

@@ -143,3 +143,37 @@ def test_moe_route_wait_times_out_and_latches():
     m2.sync()
     assert ops.kernel_error(clear=True) == 0
     m2.close()
+
+
+@pytest.mark.parametrize("name,rt", [("tiny", dict(ckpt_interval=2, pin_store=0)), ("tiny_moe", {})])
+def test_debug_guards_hold_over_steps(name, rt):
+    """With debug_guards every carved device piece and every pinned region has
+    a canary after it; training steps leave all of them intact."""
+    c = configs.get(name)
+    m = mt.Model(c, debug_guards=1, **rt)
+    for s in range(2):
+        m.set_tokens(inputs.tokens_for(c, s))
+        assert np.isfinite(m.train_step(s))
+        m.sync()  # checks every guard
+    m.close()
+
+
+@pytest.mark.parametrize("where", ["device", "host"])
+def test_debug_guards_catch_an_overwrite(where):
+    """A byte written into a guard (test hook, ordinary memory writes) is
+    reported by the next mt_sync, which latches the model."""
+    import ctypes as C
+    c = configs.get("tiny")
+    m = mt.Model(c, debug_guards=1)
+    m.set_tokens(inputs.tokens_for(c, 0))
+    m.train_step(0)
+    m.sync()
+    n = C.c_int32()
+    assert mt.lib().mt_debug_poke_guard(m.h, 1 << 30, C.byref(n)) == -1 and n.value > 10
+    which = 5 if where == "device" else n.value - 1
+    assert mt.lib().mt_debug_poke_guard(m.h, which, None) == 0
+    with pytest.raises(mt.MtError) as ei:
+        m.sync()
+    assert ei.value.status == -6 and "guard" in m.last_error()
+    assert (where == "device") == ("device guard" in m.last_error())
+    m.close()
