@@ -18,33 +18,43 @@ namespace {
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// delta[h][t] = sum_d dO[t, h, d] * O[t, h, d]; one warp per (t, h).
+// delta[h][t] = sum_d dO[t, h, d] * O[t, h, d].  HD / 8 lanes per (t, h),
+// one 16-byte vector of each operand per lane, so a warp covers 32 * 8 / HD
+// consecutive (t, h) rows with all its loads in flight at once.
 template <int HD>
-__global__ void attn_delta_k(const bf16* __restrict__ o, const bf16* __restrict__ dout, int64_t T, int nh,
-                             float* __restrict__ delta) {
-  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (w >= T * nh) return;
-  const int64_t t = w / nh;
-  const int h = (int)(w % nh);
-  const bf16* a = o + t * nh * HD + h * HD;
-  const bf16* b = dout + t * nh * HD + h * HD;
+__global__ void __launch_bounds__(256) attn_delta_k(const bf16* __restrict__ o, const bf16* __restrict__ dout,
+                                                    int64_t T, int nh, float* __restrict__ delta) {
+  constexpr int LPR = HD / 8;
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t w = gid / LPR;  // (t, h) row, t-major as the tensors are laid out
+  const int sub = (int)(gid % LPR);
   float s = 0.f;
-  for (int d = lane * 2; d < HD; d += 64) {
-    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(a + d));
-    const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(b + d));
-    s += x.x * y.x + x.y * y.y;
+  if (w < T * nh) {
+    const uint4 a = reinterpret_cast<const uint4*>(o + w * HD)[sub];
+    const uint4 b = reinterpret_cast<const uint4*>(dout + w * HD)[sub];
+    const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 u = __bfloat1622float2(x[k]);
+      const float2 v = __bfloat1622float2(y[k]);
+      s += u.x * v.x + u.y * v.y;
+    }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) delta[(int64_t)h * T + t] = s;
+  for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (sub == 0 && w < T * nh) {
+    const int64_t t = w / nh;
+    const int h = (int)(w % nh);
+    delta[(int64_t)h * T + t] = s;
+  }
 }
 
 template <int HD>
 cudaError_t bwd_tc(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, int n_seq, int S, int nh,
                    int nkv, bf16* dqkv, float* delta, cudaStream_t s) {
   const int64_t T = (int64_t)n_seq * S;
-  const int64_t blocks = (T * nh * 32 + 255) / 256;
+  const int64_t blocks = (T * nh * (HD / 8) + 255) / 256;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
   attn_delta_k<HD><<<(unsigned)blocks, 256, 0, s>>>(o, dout, T, nh, delta);
   cudaError_t e = cudaGetLastError();

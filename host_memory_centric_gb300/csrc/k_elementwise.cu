@@ -7,6 +7,8 @@
 // statistics in FP32 and reduces with warp shuffles.
 #include "mt_kernels.h"
 
+#include <type_traits>
+
 namespace mt {
 namespace {
 
@@ -40,102 +42,249 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 constexpr int ROW_WARPS = 8;  // rows per 256-thread block in the row kernels
 
 // ------------------------------------------------------------------ RMSNorm
-__global__ void __launch_bounds__(256) rmsnorm_fwd_k(const bf16* __restrict__ x, const bf16* __restrict__ g,
+// Row kernels: one warp per row, lane l owning the 16-byte vectors l, l + 32,
+// ... of the row.  NV (vectors per lane, H <= 256 NV) is a template argument
+// so that every load of a row is issued before the first use and the row stays
+// in registers between the statistic and the output pass; NV = 0 is the
+// generic form for wider rows (loads unrolled by four, the row re-read).
+// gamma is staged once per block in shared memory.
+template <int NV>
+__global__ void __launch_bounds__(256, 2) rmsnorm_fwd_k(const bf16* __restrict__ x, const bf16* __restrict__ g,
                                                      int64_t T, int H, float eps, bf16* __restrict__ y,
                                                      float* __restrict__ rstd) {
+  extern __shared__ uint4 sg[];  // gamma, H / 8 vectors
+  for (int i = threadIdx.x; i < H / 8; i += blockDim.x) sg[i] = reinterpret_cast<const uint4*>(g)[i];
+  __syncthreads();
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * ROW_WARPS + (threadIdx.x >> 5);
   if (row >= T) return;
-  const bf16* xr = x + row * H;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * H);
+  uint4* yr = reinterpret_cast<uint4*>(y + row * H);
+  const int nv = H / 8;
   float ss = 0.f;
-  for (int c = lane * 8; c < H; c += 256) {
-    float f[8];
-    unpack8(*reinterpret_cast<const uint4*>(xr + c), f);
+  if constexpr (NV > 0) {
+    uint4 xv[NV];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) ss += f[k] * f[k];
-  }
-  ss = warp_sum(ss);
-  const float r = rsqrtf(ss / (float)H + eps);
-  bf16* yr = y + row * H;
-  for (int c = lane * 8; c < H; c += 256) {
-    float f[8], w[8];
-    unpack8(*reinterpret_cast<const uint4*>(xr + c), f);
-    unpack8(*reinterpret_cast<const uint4*>(g + c), w);
+    for (int j = 0; j < NV; ++j) xv[j] = j * 32 + lane < nv ? xr[j * 32 + lane] : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) f[k] = f[k] * r * w[k];
-    *reinterpret_cast<uint4*>(yr + c) = pack8(f);
+    for (int j = 0; j < NV; ++j) {
+      float f[8];
+      unpack8(xv[j], f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ss += f[k] * f[k];
+    }
+    ss = warp_sum(ss);
+    const float r = rsqrtf(ss / (float)H + eps);
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int v = j * 32 + lane;
+      if (v < nv) {
+        float f[8], w[8];
+        unpack8(xv[j], f);
+        unpack8(sg[v], w);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] = f[k] * r * w[k];
+        yr[v] = pack8(f);
+      }
+    }
+    if (lane == 0) rstd[row] = r;
+  } else {
+#pragma unroll 4
+    for (int v = lane; v < nv; v += 32) {
+      float f[8];
+      unpack8(xr[v], f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ss += f[k] * f[k];
+    }
+    ss = warp_sum(ss);
+    const float r = rsqrtf(ss / (float)H + eps);
+#pragma unroll 4
+    for (int v = lane; v < nv; v += 32) {
+      float f[8], w[8];
+      unpack8(xr[v], f);
+      unpack8(sg[v], w);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) f[k] = f[k] * r * w[k];
+      yr[v] = pack8(f);
+    }
+    if (lane == 0) rstd[row] = r;
   }
-  if (lane == 0) rstd[row] = r;
 }
 
-// Each block owns a contiguous run of rows; dgamma partial sums for its rows
-// go to partial[blockIdx.x][H].
-// dx per row (one warp per row; the row's dot product needs the whole row),
-// then this block's dgamma partial column by column: thread t owns 8
-// consecutive columns and sums its block's rows in row order, so the result
-// does not depend on warp scheduling (the rows were just read: the second read
-// hits L2).
-__global__ void __launch_bounds__(256) rmsnorm_bwd_k(const bf16* __restrict__ dy, const bf16* __restrict__ x,
-                                                     const bf16* __restrict__ g, const float* __restrict__ rstd,
-                                                     const bf16* __restrict__ dres, int64_t T, int H,
-                                                     int64_t rows_per_block, bf16* __restrict__ dx,
-                                                     float* __restrict__ partial) {
+// Each block owns a contiguous run of rows and writes the dgamma partial sum
+// of its rows to partial[blockIdx.x][H].  The rows go in chunks of eight:
+// first dx, one warp per row (the row's dot product needs the whole row; dy
+// and x stay in registers between the dot product and the output), then the
+// chunk's dgamma contribution column by column: thread t owns the 16-byte
+// column vectors t, t + 256, ... and adds the chunk's rows in row order into
+// its own FP32 accumulators in shared memory (the rows were just read by the
+// block, so they come from L1).  Every column is summed in row order whatever
+// the warp scheduling, so the result is reproducible.
+template <int NV>
+__global__ void __launch_bounds__(256, 2) rmsnorm_bwd_k(const bf16* __restrict__ dy, const bf16* __restrict__ x,
+                                                        const bf16* __restrict__ g, const float* __restrict__ rstd,
+                                                        const bf16* __restrict__ dres, int64_t T, int H,
+                                                        int64_t rows_per_block, bf16* __restrict__ dx,
+                                                        float* __restrict__ partial) {
+  extern __shared__ uint4 sg[];  // gamma (H / 8 vectors), then the FP32 accumulators (H floats)
+  float* acc = reinterpret_cast<float*>(sg + H / 8);
+  const int nv = H / 8;
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+    sg[i] = reinterpret_cast<const uint4*>(g)[i];
+    reinterpret_cast<float4*>(acc)[2 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    reinterpret_cast<float4*>(acc)[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t r0 = (int64_t)blockIdx.x * rows_per_block;
   const int64_t r1 = min(T, r0 + rows_per_block);
-  for (int64_t row = r0 + warp; row < r1; row += ROW_WARPS) {
-    const bf16* dyr = dy + row * H;
-    const bf16* xr = x + row * H;
-    const float r = rstd[row];
-    float dot = 0.f;
-    for (int c = lane * 8; c < H; c += 256) {
-      float a[8], b[8], w[8];
-      unpack8(*reinterpret_cast<const uint4*>(dyr + c), a);
-      unpack8(*reinterpret_cast<const uint4*>(xr + c), b);
-      unpack8(*reinterpret_cast<const uint4*>(g + c), w);
+  for (int64_t c0 = r0; c0 < r1; c0 += ROW_WARPS) {  // block-uniform trip count
+    const int64_t row = c0 + warp;
+    if (row < r1) {
+      const uint4* dyr = reinterpret_cast<const uint4*>(dy + row * H);
+      const uint4* xr = reinterpret_cast<const uint4*>(x + row * H);
+      const uint4* dr = dres ? reinterpret_cast<const uint4*>(dres + row * H) : nullptr;
+      uint4* dxr = reinterpret_cast<uint4*>(dx + row * H);
+      const float r = rstd[row];
+      float dot = 0.f;
+      if constexpr (NV > 0) {
+        uint4 av[NV], bv[NV];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) dot += a[k] * w[k] * b[k];
-    }
-    dot = warp_sum(dot);
-    const float c3 = r * r * r / (float)H * dot;
-    for (int c = lane * 8; c < H; c += 256) {
-      float a[8], b[8], w[8], o[8];
-      unpack8(*reinterpret_cast<const uint4*>(dyr + c), a);
-      unpack8(*reinterpret_cast<const uint4*>(xr + c), b);
-      unpack8(*reinterpret_cast<const uint4*>(g + c), w);
-      if (dres) {
-        unpack8(*reinterpret_cast<const uint4*>(dres + row * H + c), o);
+        for (int j = 0; j < NV; ++j) {
+          const int v = j * 32 + lane;
+          av[j] = v < nv ? dyr[v] : make_uint4(0, 0, 0, 0);
+          bv[j] = v < nv ? xr[v] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          const int v = j * 32 + lane;
+          if (v < nv) {
+            float a[8], b[8], w[8];
+            unpack8(av[j], a);
+            unpack8(bv[j], b);
+            unpack8(sg[v], w);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) dot += a[k] * w[k] * b[k];
+          }
+        }
+        dot = warp_sum(dot);
+        const float c3 = r * r * r / (float)H * dot;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          const int v = j * 32 + lane;
+          if (v < nv) {
+            float a[8], b[8], w[8], o[8];
+            unpack8(av[j], a);
+            unpack8(bv[j], b);
+            unpack8(sg[v], w);
+            if (dr) {
+              unpack8(dr[v], o);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) o[k] = 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] += r * w[k] * a[k] - c3 * b[k];
+            dxr[v] = pack8(o);
+          }
+        }
       } else {
+#pragma unroll 4
+        for (int v = lane; v < nv; v += 32) {
+          float a[8], b[8], w[8];
+          unpack8(dyr[v], a);
+          unpack8(xr[v], b);
+          unpack8(sg[v], w);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) o[k] = 0.f;
+          for (int k = 0; k < 8; ++k) dot += a[k] * w[k] * b[k];
+        }
+        dot = warp_sum(dot);
+        const float c3 = r * r * r / (float)H * dot;
+#pragma unroll 4
+        for (int v = lane; v < nv; v += 32) {
+          float a[8], b[8], w[8], o[8];
+          unpack8(dyr[v], a);
+          unpack8(xr[v], b);
+          unpack8(sg[v], w);
+          if (dr) {
+            unpack8(dr[v], o);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] = 0.f;
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) o[k] += r * w[k] * a[k] - c3 * b[k];
+          dxr[v] = pack8(o);
+        }
       }
+    }
+    __syncthreads();  // the chunk's rows are in L1 before the column pass reads them
+    const int n = (int)min((int64_t)ROW_WARPS, r1 - c0);
+    float rr[ROW_WARPS];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) o[k] += r * w[k] * a[k] - c3 * b[k];
-      *reinterpret_cast<uint4*>(dx + row * H + c) = pack8(o);
+    for (int u = 0; u < ROW_WARPS; ++u) rr[u] = u < n ? rstd[c0 + u] : 0.f;
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+      uint4 av[ROW_WARPS], bv[ROW_WARPS];
+#pragma unroll
+      for (int u = 0; u < ROW_WARPS; ++u) {
+        av[u] = u < n ? reinterpret_cast<const uint4*>(dy + (c0 + u) * H)[v] : make_uint4(0, 0, 0, 0);
+        bv[u] = u < n ? reinterpret_cast<const uint4*>(x + (c0 + u) * H)[v] : make_uint4(0, 0, 0, 0);
+      }
+      float4* ap = reinterpret_cast<float4*>(acc + v * 8);
+      const float4 p0 = ap[0], p1 = ap[1];
+      float s8[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+      for (int u = 0; u < ROW_WARPS; ++u) {
+        if (u < n) {
+          float a[8], b[8];
+          unpack8(av[u], a);
+          unpack8(bv[u], b);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) s8[k] += a[k] * b[k] * rr[u];
+        }
+      }
+      ap[0] = make_float4(s8[0], s8[1], s8[2], s8[3]);
+      ap[1] = make_float4(s8[4], s8[5], s8[6], s8[7]);
     }
   }
-  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int64_t row = r0; row < r1; ++row) {
-      float a[8], b[8];
-      unpack8(*reinterpret_cast<const uint4*>(dy + row * H + c), a);
-      unpack8(*reinterpret_cast<const uint4*>(x + row * H + c), b);
-      const float r = rstd[row];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) acc[k] += a[k] * b[k] * r;
-    }
-    float4* p = reinterpret_cast<float4*>(partial + (int64_t)blockIdx.x * H + c);
-    p[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    p[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  // each thread reads back only the accumulators it wrote
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    const float4* ap = reinterpret_cast<const float4*>(acc + v * 8);
+    float4* p = reinterpret_cast<float4*>(partial + (int64_t)blockIdx.x * H + v * 8);
+    p[0] = ap[0];
+    p[1] = ap[1];
   }
 }
 
-__global__ void rmsnorm_bwd_stage2_k(const float* __restrict__ partial, int nblk, int H, bf16* __restrict__ dg) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= H) return;
+// dgamma[c] = sum over b of partial[b][c], b ascending in eight interleaved
+// slices (warp w sums b = w, w + 8, ...; four loads in flight), the slices
+// then added in order: a fixed order, so the result is reproducible.  One
+// block per 32 columns; lane = column.
+__global__ void __launch_bounds__(256) rmsnorm_bwd_stage2_k(const float* __restrict__ partial, int nblk, int H,
+                                                            bf16* __restrict__ dg) {
+  __shared__ float red[ROW_WARPS][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + lane;
   float s = 0.f;
-  for (int b = 0; b < nblk; ++b) s += partial[(int64_t)b * H + c];
-  dg[c] = __float2bfloat16_rn(s);
+  if (c < H) {
+    int b = warp;
+    for (; b + 3 * ROW_WARPS < nblk; b += 4 * ROW_WARPS) {
+      float t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) t[u] = partial[(int64_t)(b + u * ROW_WARPS) * H + c];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) s += t[u];
+    }
+    for (; b < nblk; b += ROW_WARPS) s += partial[(int64_t)b * H + c];
+  }
+  red[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && c < H) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < ROW_WARPS; ++w) tot += red[w][lane];
+    dg[c] = __float2bfloat16_rn(tot);
+  }
 }
 
 // ------------------------------------------------------------------ debug guards
@@ -368,12 +517,32 @@ inline unsigned nblocks(int64_t n, int t) { return (unsigned)((n + t - 1) / t); 
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
+// Vectors per lane the row kernels keep in registers for a row of H
+// elements, at most MaxNV (so that two 256-thread blocks fit on an SM); 0
+// selects the generic (re-reading) form.
+template <int MaxNV, typename F>
+cudaError_t with_nv(int H, F&& f) {
+  const int per_lane = (H / 8 + 31) / 32;
+  if (per_lane <= 1) return f(std::integral_constant<int, 1>());
+  if (per_lane <= 2) return f(std::integral_constant<int, 2>());
+  if (per_lane <= 4) return f(std::integral_constant<int, 4>());
+  if constexpr (MaxNV >= 8)
+    if (per_lane <= 8) return f(std::integral_constant<int, 8>());
+  if constexpr (MaxNV >= 12)
+    if (per_lane <= 12) return f(std::integral_constant<int, 12>());
+  if constexpr (MaxNV >= 16)
+    if (per_lane <= 16) return f(std::integral_constant<int, 16>());
+  return f(std::integral_constant<int, 0>());
+}
+
 cudaError_t rmsnorm_fwd(const bf16* x, const bf16* gamma, int64_t T, int H, float eps, bf16* y, float* rstd,
                         cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  if (H % 8 || !al16(x) || !al16(gamma) || !al16(y)) return cudaErrorInvalidValue;
-  rmsnorm_fwd_k<<<nblocks(T, ROW_WARPS), 256, 0, s>>>(x, gamma, T, H, eps, y, rstd);
-  return cudaGetLastError();
+  if (H % 8 || H > 24576 || !al16(x) || !al16(gamma) || !al16(y)) return cudaErrorInvalidValue;
+  return with_nv<16>(H, [&](auto nv) {
+    rmsnorm_fwd_k<decltype(nv)::value><<<nblocks(T, ROW_WARPS), 256, (size_t)H * 2, s>>>(x, gamma, T, H, eps, y, rstd);
+    return cudaGetLastError();
+  });
 }
 
 int rmsnorm_bwd_blocks(int64_t T) {
@@ -383,7 +552,7 @@ int rmsnorm_bwd_blocks(int64_t T) {
 int64_t rmsnorm_bwd_partial_floats(int64_t T, int H) { return (int64_t)rmsnorm_bwd_blocks(T) * H; }
 
 cudaError_t rmsnorm_bwd_stage2(const float* partial, int nblk, int H, bf16* dgamma, cudaStream_t s) {
-  rmsnorm_bwd_stage2_k<<<nblocks(H, 256), 256, 0, s>>>(partial, nblk, H, dgamma);
+  rmsnorm_bwd_stage2_k<<<nblocks(H, 32), 256, 0, s>>>(partial, nblk, H, dgamma);
   return cudaGetLastError();
 }
 
@@ -395,8 +564,16 @@ cudaError_t rmsnorm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const 
   const int nblk = rmsnorm_bwd_blocks(T);
   const int64_t per = (T + nblk - 1) / nblk;
   if (reinterpret_cast<uintptr_t>(partial) & 15) return cudaErrorInvalidValue;
-  rmsnorm_bwd_k<<<nblk, 256, 0, s>>>(dy, x, gamma, rstd, dres, T, H, per, dx, partial);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = with_nv<8>(H, [&](auto nv) {
+    constexpr int K = decltype(nv)::value;
+    const size_t smem = (size_t)H * 6;  // gamma + FP32 accumulators
+    if (smem > 48 * 1024) {
+      const cudaError_t a = cudaFuncSetAttribute(rmsnorm_bwd_k<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (a != cudaSuccess) return a;
+    }
+    rmsnorm_bwd_k<K><<<nblk, 256, smem, s>>>(dy, x, gamma, rstd, dres, T, H, per, dx, partial);
+    return cudaGetLastError();
+  });
   if (e != cudaSuccess) return e;
   return rmsnorm_bwd_stage2(partial, nblk, H, dgamma, s);
 }

@@ -278,10 +278,14 @@ mt_status mt_gemm(const void* A, int64_t lda, int32_t a_mn, const void* B, int64
 mt_status mt_gemm2(const void* const* A, const int64_t* lda, const int32_t* a_mn, const void* const* B,
                    const int64_t* ldb, const int32_t* b_mn, const int32_t* M, const int32_t* N,
                    const int32_t* K, void* const* D, const int64_t* ldd, void* stream);
-/* RMSNorm forward: y = x * rstd * gamma, rstd = (mean(x^2)+eps)^-1/2 per row. */
+/* RMSNorm forward: y = x * rstd * gamma, rstd = (mean(x^2)+eps)^-1/2 per row.
+ * x, y: [T][H] BF16, gamma: [H] BF16, rstd: [T] FP32; H a multiple of 8 and at
+ * most 24576, x, gamma and y 16-byte aligned, else MT_ERR_ARG. */
 mt_status mt_rmsnorm_fwd(const void* x, const void* gamma, int64_t T, int32_t H, float eps,
                          void* y, float* rstd, void* stream);
-/* RMSNorm backward: dx = d/dx + dres (dres optional), dgamma = sum over rows.
+/* RMSNorm backward: dx = d/dx + dres (dres optional), dgamma = sum over rows,
+ * summed in a fixed order (the same inputs give the same bits).  H a multiple
+ * of 8 and at most 12288, BF16 tensors 16-byte aligned, else MT_ERR_ARG.
  * scratch: device memory of mt_rmsnorm_bwd_scratch_bytes(T, H) bytes. */
 mt_status mt_rmsnorm_bwd(const void* dy, const void* x, const void* gamma, const float* rstd,
                          const void* dres, int64_t T, int32_t H, void* dx, void* dgamma,
