@@ -972,7 +972,6 @@ mt_status acquire_slab(mt_model* m, int* k) {
 int nvisits(const mt_model* m) { return (int)m->plan.size(); }
 int visit_block(const mt_model* m, int v) { return m->plan[(size_t)v].j; }
 int visit_kind(const mt_model* m, int v) { return m->plan[(size_t)v].kind; }
-bool visit_fwd(const mt_model* m, int v) { return visit_kind(m, v) <= V_HEAD; }
 
 // The token data of pass p (from mt_set_tokens' pinned copy) to the device,
 // on the compute stream ahead of the embedding forward that reads it.
