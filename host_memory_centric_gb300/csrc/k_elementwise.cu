@@ -111,16 +111,124 @@ __global__ void __launch_bounds__(256, 2) rmsnorm_fwd_k(const bf16* __restrict__
   }
 }
 
-// Each block owns a contiguous run of rows and writes the dgamma partial sum
-// of its rows to partial[blockIdx.x][H].  The rows go in chunks of eight:
-// first dx, one warp per row (the row's dot product needs the whole row; dy
-// and x stay in registers between the dot product and the output), then the
-// chunk's dgamma contribution column by column: thread t owns the 16-byte
-// column vectors t, t + 256, ... and adds the chunk's rows in row order into
-// its own FP32 accumulators in shared memory (the rows were just read by the
-// block, so they come from L1).  Every column is summed in row order whatever
-// the warp scheduling, so the result is reproducible.
+// RMSNorm backward.  Each block owns a contiguous run of rows and writes the
+// dgamma partial sum of its rows to partial[blockIdx.x][H]; a second kernel
+// adds the blocks' partials in a fixed order.  dx is computed one warp per row
+// (the row's dot product needs the whole row).  No atomics: every sum runs in
+// an order fixed by the row and block indices, so results are reproducible.
+//
+// Rows of up to 2048 (NV = H / 256 vectors per lane, a template argument):
+// dy and x stay in registers between the dot product and the output, and each
+// warp adds its own rows' dgamma contribution straight from those registers
+// into its own FP32 accumulator row in shared memory ([8 warps][H]); the
+// block then adds the eight warp rows in warp order.  Nothing is read twice
+// and the warps never wait for one another inside the row loop.
 template <int NV>
+__global__ void __launch_bounds__(256, 2) rmsnorm_bwd_warp_k(const bf16* __restrict__ dy,
+                                                             const bf16* __restrict__ x,
+                                                             const bf16* __restrict__ g,
+                                                             const float* __restrict__ rstd,
+                                                             const bf16* __restrict__ dres, int64_t T, int H,
+                                                             int64_t rows_per_block, bf16* __restrict__ dx,
+                                                             float* __restrict__ partial) {
+  extern __shared__ uint4 sg[];  // gamma (H / 8 vectors), then [ROW_WARPS][H] FP32 accumulators
+  float* acc = reinterpret_cast<float*>(sg + H / 8);
+  const int nv = H / 8;
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) sg[i] = reinterpret_cast<const uint4*>(g)[i];
+  for (int i = threadIdx.x; i < ROW_WARPS * nv * 2; i += blockDim.x)
+    reinterpret_cast<float4*>(acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* wacc = acc + (int64_t)warp * H;
+  const int64_t r0 = (int64_t)blockIdx.x * rows_per_block;
+  const int64_t r1 = min(T, r0 + rows_per_block);
+  for (int64_t row = r0 + warp; row < r1; row += ROW_WARPS) {
+    const uint4* dyr = reinterpret_cast<const uint4*>(dy + row * H);
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * H);
+    const uint4* dr = dres ? reinterpret_cast<const uint4*>(dres + row * H) : nullptr;
+    uint4* dxr = reinterpret_cast<uint4*>(dx + row * H);
+    const float r = rstd[row];
+    uint4 av[NV], bv[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int v = j * 32 + lane;
+      av[j] = v < nv ? dyr[v] : make_uint4(0, 0, 0, 0);
+      bv[j] = v < nv ? xr[v] : make_uint4(0, 0, 0, 0);
+    }
+    float dot = 0.f;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int v = j * 32 + lane;
+      if (v < nv) {
+        float a[8], b[8], w[8];
+        unpack8(av[j], a);
+        unpack8(bv[j], b);
+        unpack8(sg[v], w);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dot += a[k] * w[k] * b[k];
+      }
+    }
+    dot = warp_sum(dot);
+    const float c3 = r * r * r / (float)H * dot;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int v = j * 32 + lane;
+      if (v < nv) {
+        float a[8], b[8], w[8], o[8];
+        unpack8(av[j], a);
+        unpack8(bv[j], b);
+        unpack8(sg[v], w);
+        if (dr) {
+          unpack8(dr[v], o);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) o[k] = 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[k] += r * w[k] * a[k] - c3 * b[k];
+        dxr[v] = pack8(o);
+        float4* ap = reinterpret_cast<float4*>(wacc + v * 8);
+        float4 p0 = ap[0], p1 = ap[1];
+        p0.x += a[0] * b[0] * r;
+        p0.y += a[1] * b[1] * r;
+        p0.z += a[2] * b[2] * r;
+        p0.w += a[3] * b[3] * r;
+        p1.x += a[4] * b[4] * r;
+        p1.y += a[5] * b[5] * r;
+        p1.z += a[6] * b[6] * r;
+        p1.w += a[7] * b[7] * r;
+        ap[0] = p0;
+        ap[1] = p1;
+      }
+    }
+  }
+  __syncthreads();
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+#pragma unroll
+    for (int w = 0; w < ROW_WARPS; ++w) {
+      const float4* ap = reinterpret_cast<const float4*>(acc + (int64_t)w * H + v * 8);
+      const float4 p0 = ap[0], p1 = ap[1];
+      s0.x += p0.x;
+      s0.y += p0.y;
+      s0.z += p0.z;
+      s0.w += p0.w;
+      s1.x += p1.x;
+      s1.y += p1.y;
+      s1.z += p1.z;
+      s1.w += p1.w;
+    }
+    float4* p = reinterpret_cast<float4*>(partial + (int64_t)blockIdx.x * H + v * 8);
+    p[0] = s0;
+    p[1] = s1;
+  }
+}
+
+// Wider rows: the rows go in chunks of eight.  dx one warp per row (the row
+// read twice, loads unrolled by four), then the chunk's dgamma contribution
+// column by column: thread t owns the 16-byte column vectors t, t + 256, ...
+// and adds the chunk's rows in row order into its own FP32 accumulators in
+// shared memory (the rows were just read by the block, so they come from L1).
 __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_k(const bf16* __restrict__ dy, const bf16* __restrict__ x,
                                                         const bf16* __restrict__ g, const float* __restrict__ rstd,
                                                         const bf16* __restrict__ dres, int64_t T, int H,
@@ -147,75 +255,32 @@ __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_k(const bf16* __restrict__
       uint4* dxr = reinterpret_cast<uint4*>(dx + row * H);
       const float r = rstd[row];
       float dot = 0.f;
-      if constexpr (NV > 0) {
-        uint4 av[NV], bv[NV];
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-          const int v = j * 32 + lane;
-          av[j] = v < nv ? dyr[v] : make_uint4(0, 0, 0, 0);
-          bv[j] = v < nv ? xr[v] : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-          const int v = j * 32 + lane;
-          if (v < nv) {
-            float a[8], b[8], w[8];
-            unpack8(av[j], a);
-            unpack8(bv[j], b);
-            unpack8(sg[v], w);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) dot += a[k] * w[k] * b[k];
-          }
-        }
-        dot = warp_sum(dot);
-        const float c3 = r * r * r / (float)H * dot;
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-          const int v = j * 32 + lane;
-          if (v < nv) {
-            float a[8], b[8], w[8], o[8];
-            unpack8(av[j], a);
-            unpack8(bv[j], b);
-            unpack8(sg[v], w);
-            if (dr) {
-              unpack8(dr[v], o);
-            } else {
-#pragma unroll
-              for (int k = 0; k < 8; ++k) o[k] = 0.f;
-            }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) o[k] += r * w[k] * a[k] - c3 * b[k];
-            dxr[v] = pack8(o);
-          }
-        }
-      } else {
 #pragma unroll 4
-        for (int v = lane; v < nv; v += 32) {
-          float a[8], b[8], w[8];
-          unpack8(dyr[v], a);
-          unpack8(xr[v], b);
-          unpack8(sg[v], w);
+      for (int v = lane; v < nv; v += 32) {
+        float a[8], b[8], w[8];
+        unpack8(dyr[v], a);
+        unpack8(xr[v], b);
+        unpack8(sg[v], w);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) dot += a[k] * w[k] * b[k];
-        }
-        dot = warp_sum(dot);
-        const float c3 = r * r * r / (float)H * dot;
+        for (int k = 0; k < 8; ++k) dot += a[k] * w[k] * b[k];
+      }
+      dot = warp_sum(dot);
+      const float c3 = r * r * r / (float)H * dot;
 #pragma unroll 4
-        for (int v = lane; v < nv; v += 32) {
-          float a[8], b[8], w[8], o[8];
-          unpack8(dyr[v], a);
-          unpack8(xr[v], b);
-          unpack8(sg[v], w);
-          if (dr) {
-            unpack8(dr[v], o);
-          } else {
+      for (int v = lane; v < nv; v += 32) {
+        float a[8], b[8], w[8], o[8];
+        unpack8(dyr[v], a);
+        unpack8(xr[v], b);
+        unpack8(sg[v], w);
+        if (dr) {
+          unpack8(dr[v], o);
+        } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) o[k] = 0.f;
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) o[k] += r * w[k] * a[k] - c3 * b[k];
-          dxr[v] = pack8(o);
+          for (int k = 0; k < 8; ++k) o[k] = 0.f;
         }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[k] += r * w[k] * a[k] - c3 * b[k];
+        dxr[v] = pack8(o);
       }
     }
     __syncthreads();  // the chunk's rows are in L1 before the column pass reads them
@@ -419,7 +484,8 @@ __global__ void __launch_bounds__(CE_THREADS) cross_entropy_k(bf16* __restrict__
     return;
   }
   if (tid == 0) zt_s = __bfloat162float(z[tgt]);
-  // pass 1: per-thread running max and sum of exp, merged across the block
+  // pass 1: per-thread running max and sum of exp, merged across the block;
+  // four 16-byte loads in flight per thread
   float m = -INFINITY, s = 0.f;
   auto add = [&](float v) {
     if (v > m) {
@@ -430,6 +496,7 @@ __global__ void __launch_bounds__(CE_THREADS) cross_entropy_k(bf16* __restrict__
     }
   };
   if ((V & 7) == 0) {
+#pragma unroll 4
     for (int c = tid * 8; c < V; c += CE_THREADS * 8) {
       float f[8];
       unpack8(*reinterpret_cast<const uint4*>(z + c), f);
@@ -460,8 +527,9 @@ __global__ void __launch_bounds__(CE_THREADS) cross_entropy_k(bf16* __restrict__
   }
   __syncthreads();
   const float lse = lse_s;
-  // pass 2: dlogits = (softmax - onehot) * inv_norm
+  // pass 2: dlogits = (softmax - onehot) * inv_norm (the row comes from L2)
   if ((V & 7) == 0) {
+#pragma unroll 4
     for (int c = tid * 8; c < V; c += CE_THREADS * 8) {
       float f[8];
       unpack8(*reinterpret_cast<const uint4*>(z + c), f);
@@ -564,16 +632,32 @@ cudaError_t rmsnorm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const 
   const int nblk = rmsnorm_bwd_blocks(T);
   const int64_t per = (T + nblk - 1) / nblk;
   if (reinterpret_cast<uintptr_t>(partial) & 15) return cudaErrorInvalidValue;
-  cudaError_t e = with_nv<8>(H, [&](auto nv) {
-    constexpr int K = decltype(nv)::value;
-    const size_t smem = (size_t)H * 6;  // gamma + FP32 accumulators
+  cudaError_t e;
+  if (H <= 2048) {
+    // gamma + eight FP32 accumulator rows: at most 69,632 bytes
+    const size_t smem = (size_t)H * 2 + (size_t)ROW_WARPS * H * 4;
+    e = with_nv<8>(H, [&](auto nv) {
+      constexpr int K = decltype(nv)::value;
+      if constexpr (K == 0) {
+        return cudaErrorInvalidValue;  // not reached: H <= 2048 has at most 8 vectors per lane
+      } else {
+        // the opt-in is per device, so it is set on every call (a host-side attribute write)
+        const cudaError_t attr = cudaFuncSetAttribute(rmsnorm_bwd_warp_k<K>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (attr != cudaSuccess) return attr;
+        rmsnorm_bwd_warp_k<K><<<nblk, 256, smem, s>>>(dy, x, gamma, rstd, dres, T, H, per, dx, partial);
+        return cudaGetLastError();
+      }
+    });
+  } else {
+    const size_t smem = (size_t)H * 6;  // gamma + one FP32 accumulator row
     if (smem > 48 * 1024) {
-      const cudaError_t a = cudaFuncSetAttribute(rmsnorm_bwd_k<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (a != cudaSuccess) return a;
+      e = cudaFuncSetAttribute(rmsnorm_bwd_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
     }
-    rmsnorm_bwd_k<K><<<nblk, 256, smem, s>>>(dy, x, gamma, rstd, dres, T, H, per, dx, partial);
-    return cudaGetLastError();
-  });
+    rmsnorm_bwd_k<<<nblk, 256, smem, s>>>(dy, x, gamma, rstd, dres, T, H, per, dx, partial);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
   return rmsnorm_bwd_stage2(partial, nblk, H, dgamma, s);
 }

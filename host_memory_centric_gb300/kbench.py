@@ -6,6 +6,7 @@ python -m host_memory_centric_gb300.kbench gemm --M 8192 --N 11264 --K 2048 [--a
 python -m host_memory_centric_gb300.kbench attn_fwd --S 2048 --nseq 4 --nh 16 --nkv 4 --hd 128
 python -m host_memory_centric_gb300.kbench attn_bwd --S 2048 --nseq 4 --nh 16 --nkv 4 --hd 128
 python -m host_memory_centric_gb300.kbench rmsnorm_bwd --T 8192 --H 2048
+python -m host_memory_centric_gb300.kbench cross_entropy --T 8192 --V 32000
 python -m host_memory_centric_gb300.kbench moe_ffn --T 16384 --H 2880 --E 32 --k 4 --Fe 2880
 """
 from __future__ import annotations
@@ -47,6 +48,7 @@ def main():
     ap.add_argument("--hd", type=int, default=128)
     ap.add_argument("--T", type=int, default=8192)
     ap.add_argument("--H", type=int, default=2048)
+    ap.add_argument("--V", type=int, default=32000)
     ap.add_argument("--E", type=int, default=32)
     ap.add_argument("--k", type=int, default=4)
     ap.add_argument("--Fe", type=int, default=2880)
@@ -115,6 +117,16 @@ def main():
             ms = timeit(lambda: ops.rmsnorm_bwd(y, x, g, r, y, dx, dg, sc), a.iters, a.warmup)
             by = 8.0 * a.T * a.H
         res.update(shape=[a.T, a.H], ms=ms, gbs=by / ms / 1e6)
+    elif a.op == "cross_entropy":
+        # --T rows of --V logits, every row with a target; the kernel rewrites the logits in place
+        # with dlogits, so each timed launch runs on the previous launch's output (same work)
+        V = a.V
+        z = torch.randn(a.T, V).to(bf).to(dev)
+        tgt = torch.randint(0, V, (a.T,), dtype=torch.int32, device=dev)
+        rl = torch.empty(a.T, dtype=torch.float32, device=dev)
+        ms = timeit(lambda: ops.cross_entropy(z, tgt, 1.0 / a.T, rl), a.iters, a.warmup)
+        by = 4.0 * a.T * V
+        res.update(shape=[a.T, V], ms=ms, gbs=by / ms / 1e6)
     elif a.op == "moe_ffn":
         # one MoE feed-forward, forward and backward (router, routing, grouped expert GEMMs, combine);
         # includes one host synchronisation for the per-expert counts

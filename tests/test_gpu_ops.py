@@ -121,10 +121,11 @@ def test_gemm_rejects_misaligned():
 
 
 # ------------------------------------------------------------------ RMSNorm / RoPE / SwiGLU
-# H picks the row kernels' register forms (vectors per lane 1, 4, 8, 12, 16
-# and the generic re-reading form); T spans ragged row blocks and, at 4099,
-# more partial blocks than the dgamma reduction's eight slices.
-@pytest.mark.parametrize("T,H,with_res", [(333, 520, True), (1, 8, True), (4099, 2048, True),
+# H picks the row kernels' forms (forward: vectors per lane 1, 4, 8, 12, 16
+# and the generic re-reading form; backward: per-warp dgamma rows up to
+# H = 2048, chunked column passes above); T spans ragged row blocks and, at
+# 4099, more partial blocks than the dgamma reduction's eight slices.
+@pytest.mark.parametrize("T,H,with_res", [(333, 520, True), (1, 8, True), (4099, 2048, True), (64, 2048, False),
                                           (257, 2880, False), (130, 3584, True), (70, 5120, True)])
 def test_rmsnorm_fwd_bwd(orc, T, H, with_res):
     x = rnd((T, H), 13); g = 1 + 0.1 * rnd(H, 14); dy = rnd((T, H), 15); dres = rnd((T, H), 16)
@@ -255,10 +256,16 @@ def test_embedding_fwd_bwd():
     close(f64(dE), ref, rel=5e-3)
 
 
-def test_cross_entropy(orc):
-    n_seq, S, V = 3, 50, 1000
+# V = 1000: one 8-logit group per thread at most; 32000: several groups per
+# thread and a ragged last round; 1001: the scalar path.  ramp: logits rising
+# along the row, so the running max moves at almost every group.
+@pytest.mark.parametrize("n_seq,S,V,ramp", [(3, 50, 1000, False), (2, 20, 32000, False), (2, 20, 32000, True),
+                                            (2, 30, 1001, False)])
+def test_cross_entropy(orc, n_seq, S, V, ramp):
     T = n_seq * S
     z = rnd((T, V), 25, 2.0)
+    if ramp:
+        z = z + np.linspace(-12.0, 12.0, V, dtype=np.float32)
     tok = np.random.default_rng(26).integers(0, V, T).astype(np.int32)
     tgt = np.array([tok[t + 1] if (t % S) < S - 1 else -1 for t in range(T)], dtype=np.int32)
     zg = bf(z)
