@@ -524,6 +524,35 @@ def test_schedule_hand_example(orc):
     assert k == 4
 
 
+def _golden_rows(name):
+    rows = []
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", name)):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append(line.split())
+    return rows
+
+
+def test_schedule_transfer_times_match_pages(orc):
+    """The schedule's transfer model against the per-layer transfer times the
+    pages print (tests/golden/layer_transfer_times.txt): the first block has
+    nothing to hide behind, so its predicted stall is its transfer time; a
+    layer whose predecessor computes at least that long is fully hidden (the
+    pages' condition for the pipeline), and one that computes less leaves the
+    difference as stall."""
+    rows = _golden_rows("layer_transfer_times.txt")
+    assert len(rows) == 5
+    for _src, _link, bw, mb, ms, dec in rows:
+        bw, b, ms, dec = float(bw) * 1e9, float(mb) * 1e6, float(ms), int(dec)
+        t = b / bw  # seconds
+        stall, _ = orc.schedule([b, b], [0, 0], [t, 0], [0, 0], bw, bw)
+        # the printed value is the transfer time rounded to `dec` decimals (in ms)
+        assert abs(stall[0] * 1e3 - ms) <= 0.5 * 10.0 ** -dec + 1e-9, (_link, stall[0])
+        assert stall[1] == pytest.approx(0.0, abs=1e-12)
+        stall, _ = orc.schedule([b, b], [0, 0], [0.5 * t, 0], [0, 0], bw, bw)
+        assert stall[1] == pytest.approx(0.5 * t, rel=1e-12)
+
+
 def test_attention_rows_matches_full_oracle(orc):
     """The O(S hd)-per-row attention used at long context equals the full
     oracle's forward and backward on every row of a small case."""
