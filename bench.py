@@ -226,6 +226,30 @@ def _overlap(x, y):
     return _union(x) + _union(y) - _union(x + y)
 
 
+def switch_gaps(ev):
+    """Buffer-switch latency on the compute stream: for each pair of
+    consecutive visits whose second visit's weights were already resident
+    (its block's latest H2D copy ended before the first visit's compute
+    ended), the idle time between the two compute spans -- the cost of
+    switching buffers and binding the next layer (one page sets a target
+    under 100 us).  Such a gap can also hold a wait for a checkpoint slot or
+    a gradient slab; those show up in the tail.  Times in us."""
+    comp = sorted((e for e in ev if e.get("tid") == "compute stream"), key=lambda e: e["ts"])
+    h2d = sorted((e for e in ev if e.get("tid") == "weight stream" and e["name"].split()[0] == "H2D"),
+                 key=lambda e: e["ts"])
+    gaps = []
+    for a, b in zip(comp, comp[1:]):
+        blk = b.get("args", {}).get("block")
+        ready = [h for h in h2d if h.get("args", {}).get("block") == blk and h["ts"] < b["ts"]]
+        if ready and ready[-1]["ts"] + ready[-1]["dur"] <= a["ts"] + a["dur"]:
+            gaps.append(max(0.0, b["ts"] - (a["ts"] + a["dur"])))
+    if not gaps:
+        return None
+    g = np.sort(np.array(gaps))
+    return {"pairs": int(len(g)), "median_us": float(np.median(g)), "p90_us": float(np.percentile(g, 90)),
+            "max_us": float(g[-1]), "over_100us": int((g > 100.0).sum())}
+
+
 def timeline(m, tok, step, path=""):
     """One extra step (outside the timed region) with the stream timeline
     on: busy fractions of the weight, compute and gradient streams and of
@@ -251,9 +275,13 @@ def timeline(m, tok, step, path=""):
     span = t1 - t0
     busy = {k: _union(v) / span for k, v in by.items()}
     w, c = by.get("weight stream", []), by.get("compute stream", [])
+    try:
+        sw = switch_gaps(ev)
+    except Exception as e:  # a statistic of the trace must not cost the benchmark line
+        sw = {"error": repr(e)}
     return {"span_ms": span, "busy_frac": busy,
             "weight_copy_overlapped_by_compute": _overlap(w, c) / max(_union(w), 1e-9),
-            "events": len(ev), "file": path or None}
+            "buffer_switch": sw, "events": len(ev), "file": path or None}
 
 
 def cpu_model() -> str:
