@@ -82,3 +82,12 @@ def test_model_numbers_checkpoint_interval_adds_segment_forwards():
         c["n_heads"] * c["head_dim"] * c["hidden"] + 3 * c["hidden"] * c["ffn"]
     rebuilt = L - 7  # 28 layers in segments of 4: 7 stored boundaries, 21 layers rebuilt
     assert f4 - f1 == rebuilt * (2 * t * P_mm + 2 * c["batch"] * c["n_heads"] * c["head_dim"] * S * S)
+
+
+@pytest.mark.parametrize("name", ["tiny_moe", "moe"])
+def test_moe_parameter_count_matches_layout(name):
+    import host_memory_centric_gb300 as mt
+    c = configs.get(name)
+    P, _, _ = bench.model_numbers(c)
+    lay = mt.layout(mt.make_config(c))
+    assert P == sum(r * cc for b in lay for (_o, r, cc) in b["tensors"])
