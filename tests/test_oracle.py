@@ -384,6 +384,72 @@ def test_random_init_loss_near_ln_vocab(orc):
     assert abs(loss - math.log(1024)) < 0.05
 
 
+def test_forward_hidden_embedding_identity_layers_and_causality(orc):
+    """Hidden states after block j: block 0 is the embedding gather; a decoder
+    layer with W_o = 0 and W_down = 0 adds nothing to its residual stream;
+    and causal attention makes position p depend only on tokens 0..p of its
+    own sequence."""
+    shape = configs.get("tiny")
+    L, H = shape["n_layers"], shape["hidden"]
+    W = [orc.init_block(shape, 3, j) for j in range(L + 2)]
+    tok = inputs.tokens_for(shape, 0)
+    flat = tok.reshape(-1)
+    E = W[0][:shape["vocab"] * H].reshape(shape["vocab"], H)
+    h0 = orc.forward_hidden(shape, W, tok, 0)
+    assert np.array_equal(h0, E[flat])
+    lay = orc.layout(shape)
+    Wz = [w.copy() for w in W]
+    for j in range(1, L + 1):
+        for t in (1, 3):  # W_o, W_down
+            o, r, cc = lay[j]["tensors"][t]
+            Wz[j][o:o + r * cc] = 0.0
+    assert np.array_equal(orc.forward_hidden(shape, Wz, tok, L), h0)
+    # causality: change the token at position p of sequence 0
+    hL = orc.forward_hidden(shape, W, tok, L)
+    S, p = shape["seq"], 77
+    tok2 = tok.copy().reshape(-1, S)
+    tok2[0, p] = (tok2[0, p] + 1) % shape["vocab"]
+    hL2 = orc.forward_hidden(shape, W, tok2.reshape(tok.shape), L)
+    assert np.array_equal(hL2[:p], hL[:p])            # earlier positions of that sequence
+    assert not np.array_equal(hL2[p:S], hL[p:S])      # the changed position and later ones move
+    assert np.array_equal(hL2[S:], hL[S:])            # the other sequence is untouched
+
+
+def test_adam_f32_closed_form_and_torch(orc):
+    """Adam on an FP32 gradient (the host-accumulation path): constant g gives
+    a step of -lr g / (|g| + eps) every step; on BF16-representable gradients
+    it equals the BF16-gradient Adam bit for bit; random FP32 gradients match
+    torch.optim.Adam."""
+    g = np.array([0.1234567, -3.3e-5, 7.77, 0.0], np.float32)
+    master = np.array([0.1, 0.2, -0.3, 0.4], np.float32)
+    m = np.zeros(4, np.float32); v = np.zeros(4, np.float32)
+    for step in (1, 2, 3):
+        before = master.copy()
+        w = orc.adam_f32(g, master, m, v, step)
+        assert np.allclose(master - before, -1e-3 * g / (np.abs(g) + 1e-8), rtol=2e-5, atol=1e-10)
+        assert np.array_equal(w, orc.bf16_rne(master))
+    rng = np.random.default_rng(12)
+    gb = orc.bf16_rne((rng.standard_normal(256) * 1e-2).astype(np.float32))
+    m1, v1, m2, v2 = (np.zeros(256, np.float32) for _ in range(4))
+    p1 = (0.02 * rng.standard_normal(256)).astype(np.float32); p2 = p1.copy()
+    for step in (1, 2):
+        w1 = orc.adam(gb, p1, m1, v1, step)
+        w2 = orc.adam_f32(orc.bf16_to_f32(gb), p2, m2, v2, step)
+        assert np.array_equal(p1, p2) and np.array_equal(w1, w2)
+    torch = pytest.importorskip("torch")
+    n = 1000
+    p0 = (0.02 * rng.standard_normal(n)).astype(np.float32)
+    master = p0.copy(); m = np.zeros(n, np.float32); v = np.zeros(n, np.float32)
+    tp = torch.nn.Parameter(torch.from_numpy(p0.copy()))
+    opt = torch.optim.Adam([tp], lr=1e-3, betas=(0.9, 0.999), eps=1e-8, foreach=False)
+    for step in (1, 2, 3):
+        g32 = (rng.standard_normal(n) * 1e-2).astype(np.float32)
+        orc.adam_f32(g32, master, m, v, step)
+        tp.grad = torch.from_numpy(g32.copy())
+        opt.step()
+    assert np.allclose(master, tp.detach().numpy(), rtol=1e-5, atol=1e-8)
+
+
 def test_micro_batch_copies_give_single_batch_gradient(orc):
     s1 = dict(FD_SHAPE, micro=1)
     s2 = dict(FD_SHAPE, micro=3)
