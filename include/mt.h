@@ -193,6 +193,9 @@ mt_status mt_sync(mt_model* model);
  * store (after mt_sync).  bytes must not exceed the region. */
 mt_status mt_read_host(mt_model* model, int32_t block, int32_t region, void* dst, size_t bytes);
 mt_status mt_write_host(mt_model* model, int32_t block, int32_t region, const void* src, size_t bytes);
+/* Counters since mt_init_model (bytes copied per direction, host Adam and
+ * packing time, store and pinned sizes); read after mt_sync.  MT_ERR_ARG
+ * for a null argument. */
 mt_status mt_get_stats(const mt_model* model, mt_stats* out);
 /* Save / resume.  Between steps the GPU holds no model state, so the host
  * store (every block's W, G, master, m, v) and the number of steps done are
@@ -213,7 +216,13 @@ mt_status mt_expert_counts(const mt_model* model, int32_t block, int32_t* counts
 /* The enqueue log (lines "step stream op a b"); returns its length, or
  * -(needed) when cap is too small. */
 int64_t mt_protocol_log(const mt_model* model, char* buf, int64_t cap);
+/* Text of the last error ("" if none, "null model" for NULL), copied into
+ * storage of the calling thread: valid until that thread calls again. */
 const char* mt_last_error(const mt_model* model);
+/* Stops the host workers, waits for the work queued on the model's three
+ * streams, then frees everything the library owns (host store, pinned
+ * memory, events).  The caller's device region and streams are left alone.
+ * Accepts NULL. */
 void mt_destroy(mt_model* model);
 
 /* ------------------------------------------------------------------ host-only */
@@ -223,6 +232,9 @@ void mt_destroy(mt_model* model);
  * [9] offset in the store, then (element offset, rows, cols) per tensor.
  * Returns the count written or -1. */
 int64_t mt_layout_block(const mt_config* cfg, int32_t j, int64_t* out, int64_t cap);
+/* Parameters of the model (every block's tensors, no padding), and the
+ * bytes of its host flat store (16 per padded parameter, regions 4096-byte
+ * aligned); -1 for an invalid config. */
 int64_t mt_param_count(const mt_config* cfg);
 int64_t mt_store_bytes(const mt_config* cfg);
 /* The library's initialiser for block j (n_pad FP32 master values). */
@@ -290,6 +302,8 @@ mt_status mt_rmsnorm_fwd(const void* x, const void* gamma, int64_t T, int32_t H,
 mt_status mt_rmsnorm_bwd(const void* dy, const void* x, const void* gamma, const float* rstd,
                          const void* dres, int64_t T, int32_t H, void* dx, void* dgamma,
                          void* scratch, size_t scratch_bytes, void* stream);
+/* Scratch bytes mt_rmsnorm_bwd needs for T rows of H: the dgamma partial
+ * sums, min(304, ceil(T / 32)) rows of H FP32 values. */
 size_t mt_rmsnorm_bwd_scratch_bytes(int64_t T, int32_t H);
 /* Rotate-half RoPE of the first n_heads heads of each row of x ([T][ld]),
  * position = row mod S; cs from mt_rope_table (device copy). */
@@ -305,13 +319,19 @@ mt_status mt_attention_fwd(const void* qkv, int32_t n_seq, int32_t S, int32_t nh
 mt_status mt_attention_bwd(const void* qkv, const void* o, const float* lse, const void* dout,
                            int32_t n_seq, int32_t S, int32_t nh, int32_t nkv, int32_t hd,
                            void* dqkv, void* scratch, size_t scratch_bytes, void* stream);
+/* Scratch bytes mt_attention_bwd needs (n_seq * S * nh FP32). */
 size_t mt_attention_bwd_scratch_bytes(int32_t n_seq, int32_t S, int32_t nh, int32_t hd);
-/* SwiGLU: gu rows [g (F) | u (F)], h = silu(g) * u; backward into dgu. */
+/* SwiGLU: gu rows [g (F) | u (F)] BF16, h = silu(g) * u [T][F]; the
+ * backward writes dgu (same layout as gu) from dh.  F a multiple of 8 and
+ * 16-byte aligned tensors, else MT_ERR_ARG. */
 mt_status mt_swiglu_fwd(const void* gu, int64_t T, int32_t F, void* h, void* stream);
 mt_status mt_swiglu_bwd(const void* gu, const void* dh, int64_t T, int32_t F, void* dgu,
                         void* stream);
-/* Embedding gather X[t] = E[tok[t]] and dense gradient dE (all V rows) from
- * the token CSR of mt_token_csr. */
+/* Embedding gather X[t] = E[tok[t]] ([T][H] from E [V][H]) and the dense
+ * gradient dE (all V rows written; rows of unseen ids are zero) from the
+ * token CSR of mt_token_csr (device copies of row_start[V+1], rows[T]); each
+ * row sums its tokens in row order, no atomics.  H a multiple of 8 and
+ * 16-byte aligned tensors, else MT_ERR_ARG. */
 mt_status mt_embed_fwd(const int32_t* tok, const void* E, int64_t T, int32_t H, int32_t V,
                        void* X, void* stream);
 mt_status mt_embed_bwd(const int32_t* row_start, const int32_t* rows, const void* dX, int32_t V,
