@@ -275,7 +275,11 @@ mt_status mt_rope_table(int32_t S, int32_t hd, double base, float* out);
 /* ------------------------------------------------------------------ per-op (device) */
 /* The block math as individual device calls, for tests and other callers.
  * All pointers are device addresses, row-major, 16-byte aligned; every "ld"
- * is a row stride in elements and a multiple of 8. */
+ * is a row stride in elements and a multiple of 8.  A call with no rows
+ * (T, rows, V or n_seq * S = 0) launches nothing, writes nothing (dgamma
+ * included) and returns MT_OK; pointers must still be non-null.  mt_gemm
+ * needs M, N, K >= 1 (MT_ERR_ARG otherwise).  Kernels are enqueued on
+ * `stream` (a cudaStream_t; NULL = the legacy default stream). */
 
 /* D[m,n] = sum_k A(m,k) B(n,k) on tcgen05 tensor cores, FP32 accumulation.
  * A is [M][K] (a_mn = 0) or [K][M] (a_mn = 1); B is [N][K] or [K][N].

@@ -241,6 +241,29 @@ def test_bad_arguments_rejected_without_gpu():
     assert L.mt_train_step(None, 0, None) == -1
 
 
+def test_empty_inputs_launch_nothing_and_succeed():
+    """Zero rows (T = 0, rows = 0, V = 0) are no-ops: the device calls return
+    MT_OK before any CUDA call, so they succeed here without a GPU (pointers
+    must still be non-null)."""
+    L = mt.lib()
+    buf = np.zeros(4096, np.float32)
+    p = buf.ctypes.data_as(C.c_void_p)
+    H = 256
+    sc = L.mt_rmsnorm_bwd_scratch_bytes(0, H)
+    assert sc >= H * 4  # one partial row even for no rows
+    assert L.mt_rmsnorm_fwd(p, p, 0, H, 1e-6, p, p, None) == 0
+    assert L.mt_rmsnorm_bwd(p, p, p, p, None, 0, H, p, p, p, sc, None) == 0
+    assert L.mt_rope(p, 0, 512, 4, 64, 16, p, 0, None) == 0
+    assert L.mt_swiglu_fwd(p, 0, 64, p, None) == 0
+    assert L.mt_swiglu_bwd(p, p, 0, 64, p, None) == 0
+    assert L.mt_embed_fwd(p, p, 0, H, 100, p, None) == 0
+    assert L.mt_embed_bwd(p, p, p, 0, H, p, None) == 0
+    assert L.mt_cross_entropy(p, p, 0, 1000, 1.0, p, None) == 0
+    # null pointers are still rejected, empty or not
+    assert L.mt_rmsnorm_fwd(None, p, 0, H, 1e-6, p, p, None) == -1
+    assert L.mt_cross_entropy(p, None, 0, 1000, 1.0, p, None) == -1
+
+
 def test_device_footprint_independent_of_depth():
     """With host checkpoints the carved device region does not grow with depth."""
     L = mt.lib()
