@@ -45,7 +45,8 @@ class MtConfig(C.Structure):
                 ("seed", C.c_uint64), ("timeout_ms", C.c_uint32), ("pin_store", C.c_int32),
                 ("head_chunk", C.c_int32), ("log_protocol", C.c_int32), ("keep_host_grad", C.c_int32),
                 ("n_buffers", C.c_int32), ("host_grad_accum", C.c_int32), ("n_experts", C.c_int32),
-                ("top_k", C.c_int32), ("expert_ffn", C.c_int32), ("debug_guards", C.c_int32)]
+                ("top_k", C.c_int32), ("expert_ffn", C.c_int32), ("debug_guards", C.c_int32),
+                ("n_pack_threads", C.c_int32)]
 
 
 class DevRegion(C.Structure):
@@ -59,6 +60,22 @@ class Streams(C.Structure):
 class LayerView(C.Structure):
     _fields_ = [("w", C.c_void_p * MAX_TENSORS), ("g", C.c_void_p * MAX_TENSORS),
                 ("n_tensors", C.c_int32), ("block", C.c_int32), ("buf", C.c_int32)]
+
+
+class SchedIn(C.Structure):
+    _fields_ = [("n_visits", C.c_int32), ("kind", C.POINTER(C.c_int32)), ("block", C.POINTER(C.c_int32)),
+                ("b", C.POINTER(C.c_double)), ("p", C.POINTER(C.c_double)), ("d", C.POINTER(C.c_double)),
+                ("c", C.POINTER(C.c_double)), ("a", C.POINTER(C.c_double)), ("n_buffers", C.c_int32),
+                ("bw_h2d", C.c_double), ("bw_d2h", C.c_double), ("pack_rate1", C.c_double),
+                ("adam_rate1", C.c_double), ("adam_rate_max", C.c_double), ("threads", C.c_int32)]
+
+
+class SchedPlan(C.Structure):
+    _fields_ = [("K", C.c_int32), ("n_pack", C.c_int32), ("measured", C.c_int32), ("period_ms", C.c_double),
+                ("stall_ms", C.c_double), ("adam_busy_ms", C.c_double), ("slab_wait_ms", C.c_double),
+                ("pack_ms", C.c_double), ("bw_h2d_gbs", C.c_double), ("bw_d2h_gbs", C.c_double),
+                ("pack_gbs_thread", C.c_double), ("adam_gelem_s_thread", C.c_double),
+                ("adam_gelem_s_max", C.c_double)]
 
 
 class Stats(C.Structure):
@@ -110,6 +127,9 @@ def lib():
         "mt_plan_protocol": (i64, [pc, i32, C.c_char_p, i64]),
         "mt_visit_plan": (i32, [pc, _P(i32), _P(i32), i32]),
         "mt_schedule": (i32, [i32, _P(f64), _P(f64), _P(f64), _P(f64), f64, f64, _P(f64)]),
+        "mt_schedule_simulate": (i32, [_P(SchedIn), i32, i32, _P(SchedPlan), _P(f64)]),
+        "mt_schedule_plan": (i32, [_P(SchedIn), i32, _P(SchedPlan)]),
+        "mt_get_schedule": (i32, [_v, i32, _P(SchedPlan)]),
         "mt_token_csr": (i32, [_P(i32), i64, i32, _P(i32), _P(i32)]),
         "mt_host_bandwidth": (i32, [sz, i32, _P(f64), _P(f64)]),
         "mt_rope_table": (i32, [i32, i32, f64, _P(f32)]),
@@ -188,6 +208,32 @@ def visit_plan(cfg: MtConfig) -> list[tuple[int, int]]:
     b = (C.c_int32 * n)()
     lib().mt_visit_plan(C.byref(cfg), k, b, n)
     return list(zip(k, b))
+
+
+def sched_in(kind, block, b, p, d, c, a, n_buffers=2, bw_h2d=2e11, bw_d2h=2e11, pack_rate1=2e10,
+             adam_rate1=2e9, adam_rate_max=8e9, threads=16):
+    """An mt_sched_in over numpy arrays (kept alive on the returned object)."""
+    arrs = [np.ascontiguousarray(kind, np.int32), np.ascontiguousarray(block, np.int32)]
+    arrs += [np.ascontiguousarray(x, np.float64) for x in (b, p, d, c, a)]
+    s = SchedIn(len(arrs[0]), *(_ptr(x, C.c_int32) for x in arrs[:2]), *(_ptr(x, C.c_double) for x in arrs[2:]),
+                n_buffers, bw_h2d, bw_d2h, pack_rate1, adam_rate1, adam_rate_max, threads)
+    s._keep = arrs
+    return s
+
+
+def schedule_simulate(si: SchedIn, K: int, n_pack: int) -> tuple[dict, np.ndarray]:
+    """mt_schedule_simulate: the predicted steady-state step and per-visit stalls."""
+    p = SchedPlan()
+    stall = np.zeros(si.n_visits)
+    check(lib().mt_schedule_simulate(C.byref(si), K, n_pack, C.byref(p), _ptr(stall, C.c_double)))
+    return {k: getattr(p, k) for k, _ in SchedPlan._fields_}, stall
+
+
+def schedule_plan(si: SchedIn, k_max: int) -> dict:
+    """mt_schedule_plan: K and packing threads chosen by the simulation."""
+    p = SchedPlan()
+    check(lib().mt_schedule_plan(C.byref(si), k_max, C.byref(p)))
+    return {k: getattr(p, k) for k, _ in SchedPlan._fields_}
 
 
 def host_bandwidth(nbytes: int = 1 << 30, threads: int = 0) -> dict:
@@ -344,6 +390,17 @@ class Model:
         out = np.zeros(n.value, dtype=np.float64)
         check(lib().mt_timing_visits(self.h, _ptr(out, C.c_double), n.value, C.byref(n)), self.h)
         return out
+
+    def schedule(self, which: int = 0) -> dict | None:
+        """The static schedule the model runs with (mt_get_schedule): 0 the
+        plan made at init, 1 the plan on the first step's measured compute
+        times (None until that step has completed)."""
+        p = SchedPlan()
+        st = lib().mt_get_schedule(self.h, which, C.byref(p))
+        if st == -2:
+            return None
+        check(st, self.h)
+        return {k: getattr(p, k) for k, _ in SchedPlan._fields_}
 
     def last_error(self) -> str:
         return lib().mt_last_error(self.h).decode()

@@ -104,4 +104,48 @@ class Pool {
 int32_t schedule(int32_t n, const double* b, const double* d, const double* c, const double* a, double bw_h2d,
                  double bw_d2h, double* stall);
 
+// Steady-state model of the whole pipeline ([Peter] 記憶體預取策略: prefetch
+// timed from each layer's bytes, the link bandwidth and its compute time),
+// extended with the host side: the just-in-time pack, the K gradient slabs
+// and host Adam.  One entry per visit of a step (the visit plan's order).
+struct SimIn {
+  int32_t n = 0;                   // visits per step
+  const int32_t* kind = nullptr;   // 0 forward, 1 head, 2 recompute, 3 backward
+  const int32_t* block = nullptr;  // block of the visit
+  const double* b = nullptr;       // bytes copied host-to-device before the visit computes
+  const double* p = nullptr;       // bytes packed on the host first (0 with a pinned store)
+  const double* d = nullptr;       // gradient bytes exported after it (0: no export)
+  const double* c = nullptr;       // compute seconds
+  const double* a = nullptr;       // Adam elements of the exported block
+  int32_t nbuf = 2;                // device buffers (= pinned staging buffers)
+  double bw_h2d = 0, bw_d2h = 0;   // bytes/s
+  double pack_rate1 = 0;           // bytes/s one packing thread copies
+  double adam_rate1 = 0;           // Adam elements/s of one thread and the asymptote of
+  double adam_rate_max = 0;        // r(n) = r_max (1 - exp(-n r1 / r_max)) (host memory bound)
+  int32_t threads = 1;             // host threads shared by packing and Adam
+};
+struct SimOut {
+  double period = 0;      // seconds between the starts of two steps' first computes
+  double stall = 0;       // compute-stream idle seconds within that period
+  double adam_busy = 0;   // seconds host Adam works within it
+  double slab_wait = 0;   // seconds the driver waits for a free slab within it
+  double pack = 0;        // seconds of packing on the driver's path within it
+};
+// Simulates `steps` consecutive steps with K slabs and n_pack packing threads
+// (the rest run Adam) and reports the last step; stall_v (n entries, may be
+// null) receives the compute stream's wait before each visit of that step.
+SimOut simulate(const SimIn& in, int32_t K, int32_t n_pack, int32_t steps, double* stall_v);
+// Adam elements/s of n threads under the saturating model, and the asymptote
+// r_max for which the model gives rn at n threads when one thread gives r1.
+double adam_rate(const SimIn& in, int n);
+double adam_asymptote(double r1, double rn, int n);
+// Chooses K in [k_min, k_max] and the packing threads in [np_min, np_max]
+// (0 without packing): the shortest simulated period, then the fewest slabs
+// and packing threads within 0.5 % of it.
+struct Plan {
+  int32_t K = 1, n_pack = 0;
+  SimOut out;
+};
+Plan plan(const SimIn& in, int32_t k_min, int32_t k_max, int32_t np_min, int32_t np_max);
+
 }  // namespace mth

@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 #include <sys/mman.h>
+#include <unistd.h>
 
 #include <chrono>
 #include <cmath>
@@ -211,8 +212,19 @@ struct mt_model {
   cudaEvent_t WR[2] = {}, BD[2] = {}, BF[2] = {}, XR[2] = {}, XS[2] = {}, TOK = nullptr, LOSS = nullptr;
   cudaEvent_t RT = nullptr, ER[2] = {};  // MoE: Route-Ready (counts on the host), Experts-Ready[b]
   std::vector<cudaEvent_t> SR;
-  // host workers
-  mth::Pool pool;
+  // host workers: Adam (and initialisation) on `pool`; the just-in-time pack
+  // on `pack_pool`, whose work the driver thread shares, so that a pack never
+  // queues behind Adam's chunks
+  mth::Pool pool, pack_pool;
+  int n_pack = 0, n_pack_active = 0;
+  // static schedule: per-visit inputs of one pass, the plans made at init
+  // (compute estimated) and after the first step (compute measured)
+  std::vector<int32_t> sk_kind, sk_block;
+  std::vector<double> sk_b, sk_p, sk_d, sk_c, sk_a;
+  mth::SimIn sim;
+  mt_sched_plan plan0{}, plan1{};
+  bool have_plan1 = false;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> first_ev;  // compute of each visit of the first step
   std::thread adam_thr;
   std::mutex amu;
   std::condition_variable acv;
@@ -258,6 +270,7 @@ struct mt_model {
   std::vector<std::pair<uint8_t*, std::string>> hguards;  // pinned host canaries (debug_guards)
   std::atomic<bool> tracing{false};
   cudaEvent_t trace_base = nullptr;
+  cudaStream_t trace_stream = nullptr;  // idle stream that timestamps the timeline's origin
   double trace_host_base = 0;
   std::vector<TraceDev> tdev;
   std::mutex tmu;  // thost is appended by the Adam dispatcher
@@ -1018,19 +1031,24 @@ std::vector<Range> block_ranges(const mt_model* m, int j, bool trunk, bool exper
 }
 
 // Host copy of the given ranges of src into dst (the just-in-time pack into
-// pinned staging), in 8 MiB pieces on the worker pool.
+// pinned staging): 8 MiB pieces split into n_pack_active contiguous shares,
+// copied by the packing threads and the driver thread.
 mt_status pack_ranges(mt_model* m, uint8_t* dst, const uint8_t* src, const std::vector<Range>& rg) {
   const double t0 = now_ms();
   constexpr int64_t CH = 8 << 20;
   std::vector<Range> pieces;
   for (const Range& r : rg)
     for (int64_t o = 0; o < r.bytes; o += CH) pieces.push_back({r.off + o, std::min(CH, r.bytes - o)});
-  std::function<void(int64_t)> fn = [&](int64_t i) {
-    const Range& q = pieces[(size_t)i];
-    std::memcpy(dst + q.off, src + q.off, (size_t)q.bytes);
+  const int64_t np = (int64_t)pieces.size();
+  const int64_t nt = std::max<int64_t>(1, std::min<int64_t>(m->n_pack_active, np));
+  std::function<void(int64_t)> fn = [&](int64_t t) {
+    for (int64_t i = t * np / nt; i < (t + 1) * np / nt; ++i) {
+      const Range& q = pieces[(size_t)i];
+      std::memcpy(dst + q.off, src + q.off, (size_t)q.bytes);
+    }
   };
   std::string werr;
-  if (!m->pool.parallel_for((int64_t)pieces.size(), fn, &werr)) return set_err(m, MT_ERR_INTERNAL, "pack: " + werr);
+  if (!m->pack_pool.parallel_for(nt, fn, &werr)) return set_err(m, MT_ERR_INTERNAL, "pack: " + werr);
   m->pack_ms += now_ms() - t0;
   return MT_OK;
 }
@@ -1334,9 +1352,13 @@ mt_status run_visit(mt_model* m) {
     ta = take_event(m);
     CU(m, cudaEventRecord(ta, m->sc));
   }
+  // the first step's per-visit compute times feed the schedule's second plan
+  const bool first = m->live && m->steps_done == 0 && m->pass == 0 && (size_t)v < m->first_ev.size();
+  if (first) CU(m, cudaEventRecord(m->first_ev[(size_t)v].first, m->sc));
   if (kind <= V_HEAD) OK(do_forward(m, j, b));
   else if (kind == V_RECOMP) OK(do_recompute(m, j, b));
   else OK(do_backward(m, j, b));
+  if (first) CU(m, cudaEventRecord(m->first_ev[(size_t)v].second, m->sc));
   if (ta) {
     cudaEvent_t tb = take_event(m);
     CU(m, cudaEventRecord(tb, m->sc));
@@ -1381,11 +1403,191 @@ void fill_shape(mt_model* m) {
   m->lay = mth::build_layout(&c);
   m->wb_max = 0;
   for (auto& b : m->lay) m->wb_max = b.wbytes > m->wb_max ? b.wbytes : m->wb_max;
-  m->K = c.n_grad_slabs;
+  m->K = c.n_grad_slabs > 0 ? c.n_grad_slabs : 12;  // mt_init_model plans it when 0
   m->nbuf = c.n_buffers;
   m->ci = c.ckpt_interval;
   m->nseg = (m->L + m->ci - 1) / m->ci;
   m->plan = build_plan(m->L, m->ci);
+}
+
+// ---------------------------------------------------------------- static schedule
+// Tensor FLOPs of a visit's compute (forward: 2 t P_mm + causal attention
+// 2 B nh hd S^2; backward: recompute without the last projection, 4 t P_mm
+// and 7 B nh hd S^2 of attention; head: 6 t H V).
+double visit_flops(const mt_model* m, int kind, int j) {
+  const double T = (double)m->T, H = m->H, nh = m->nh, nkv = m->nkv, hd = m->hd;
+  const double att = (double)m->Mp * m->B * nh * hd * (double)m->S * m->S;
+  const double mlp = m->moe ? (double)m->topk * 3.0 * H * m->Fe + (double)m->E * H : 3.0 * H * m->F;
+  const double last = m->moe ? (double)m->topk * H * m->Fe : H * m->F;  // down projection
+  const double pmm = H * (nh + 2 * nkv) * hd + nh * hd * H + mlp;
+  if (j == 0) return 0.0;
+  if (j == m->L + 1) return 6.0 * T * H * m->V;
+  if (kind == V_BWD) return 2.0 * T * (pmm - last) + 4.0 * T * pmm + 7.0 * att;
+  return 2.0 * T * pmm + 2.0 * att;
+}
+
+// Per-visit schedule inputs of one pass; c[] estimated from FLOPs at the
+// assumed rate until measured (plus a fixed 0.2 ms of launches and
+// memory-bound kernels per visit).
+constexpr double kAssumedFlops = 1.2e15;
+void sched_inputs(mt_model* m) {
+  const int n = nvisits(m);
+  m->sk_kind.assign((size_t)n, 0);
+  m->sk_block.assign((size_t)n, 0);
+  m->sk_b.assign((size_t)n, 0.0);
+  m->sk_p.assign((size_t)n, 0.0);
+  m->sk_d.assign((size_t)n, 0.0);
+  m->sk_c.assign((size_t)n, 0.0);
+  m->sk_a.assign((size_t)n, 0.0);
+  for (int v = 0; v < n; ++v) {
+    const VisitDesc& vd = m->plan[(size_t)v];
+    const mth::BlockDesc& bd = m->lay[(size_t)vd.j];
+    const bool copies = !(vd.j == 0 && vd.kind == V_BWD);
+    double b = copies ? (double)bd.wbytes : 0.0;
+    if (vd.first && m->c.ckpt_on_host) b += (double)m->T * m->H * 2;
+    m->sk_kind[(size_t)v] = vd.kind;
+    m->sk_block[(size_t)v] = vd.j;
+    m->sk_b[(size_t)v] = b;
+    m->sk_p[(size_t)v] = (!m->c.pin_store && copies) ? (double)bd.wbytes : 0.0;
+    const bool exp = vd.kind == V_HEAD || vd.kind == V_BWD;
+    m->sk_d[(size_t)v] = exp ? (double)bd.wbytes : 0.0;
+    m->sk_a[(size_t)v] = exp ? (double)bd.n_pad : 0.0;
+    m->sk_c[(size_t)v] = visit_flops(m, vd.kind, vd.j) / kAssumedFlops + 2e-4;
+  }
+  mth::SimIn& in = m->sim;
+  in.n = n;
+  in.kind = m->sk_kind.data();
+  in.block = m->sk_block.data();
+  in.b = m->sk_b.data();
+  in.p = m->sk_p.data();
+  in.d = m->sk_d.data();
+  in.c = m->sk_c.data();
+  in.a = m->sk_a.data();
+  in.nbuf = m->nbuf;
+}
+
+void fill_plan_out(const mth::Plan& pl, const mth::SimIn& in, int measured, mt_sched_plan* o) {
+  o->K = pl.K;
+  o->n_pack = pl.n_pack;
+  o->measured = measured;
+  o->period_ms = pl.out.period * 1e3;
+  o->stall_ms = pl.out.stall * 1e3;
+  o->adam_busy_ms = pl.out.adam_busy * 1e3;
+  o->slab_wait_ms = pl.out.slab_wait * 1e3;
+  o->pack_ms = pl.out.pack * 1e3;
+  o->bw_h2d_gbs = in.bw_h2d / 1e9;
+  o->bw_d2h_gbs = in.bw_d2h / 1e9;
+  o->pack_gbs_thread = in.pack_rate1 / 1e9;
+  o->adam_gelem_s_thread = in.adam_rate1 / 1e9;
+  o->adam_gelem_s_max = in.adam_rate_max / 1e9;
+}
+
+// Init-time measurements for the schedule: pinned copies over the link in
+// each direction (best of three), a one-thread copy from the pageable store
+// into pinned memory (the pack), and host Adam on scratch arrays with one
+// thread and with the whole pool.  A failed probe leaves its rate at 0 (the
+// model then treats that stage as free).
+void run_probes(mt_model* m, int nth) {
+  mth::SimIn& in = m->sim;
+  const size_t bytes = (size_t)std::min<int64_t>((int64_t)64 << 20, m->wb_max);
+  void* hp = nullptr;
+  if (cudaHostAlloc(&hp, bytes, cudaHostAllocDefault) == cudaSuccess) {
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) == cudaSuccess && cudaEventCreate(&e1) == cudaSuccess) {
+      for (int dir = 0; dir < 2; ++dir) {
+        cudaStream_t st = dir == 0 ? m->sw : m->sg;
+        float best = 1e30f;
+        for (int r = 0; r < 3; ++r) {
+          cudaEventRecord(e0, st);
+          if (dir == 0) cudaMemcpyAsync(m->d.buf[0], hp, bytes, cudaMemcpyHostToDevice, st);
+          else cudaMemcpyAsync(hp, m->d.buf[0], bytes, cudaMemcpyDeviceToHost, st);
+          cudaEventRecord(e1, st);
+          float ms = 0;
+          if (cudaEventSynchronize(e1) == cudaSuccess && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess && ms > 0)
+            best = std::min(best, ms);
+        }
+        if (best < 1e30f) (dir == 0 ? in.bw_h2d : in.bw_d2h) = (double)bytes / (best * 1e-3);
+      }
+    }
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    const mth::BlockDesc* big = &m->lay[0];
+    for (auto& b : m->lay)
+      if (b.wbytes > big->wbytes) big = &b;
+    const size_t pb = std::min<size_t>(bytes, (size_t)big->wbytes);
+    double best = 1e30;
+    for (int r = 0; r < 2; ++r) {
+      const double t0 = now_ms();
+      std::memcpy(hp, m->store + big->store_off, pb);
+      best = std::min(best, now_ms() - t0);
+    }
+    if (best > 0) in.pack_rate1 = (double)pb / (best * 1e-3);
+    cudaFreeHost(hp);
+  }
+  // Adam: 2 Mi elements on one thread, 8 Mi elements over the pool
+  const int64_t n1 = (int64_t)2 << 20, nn = (int64_t)8 << 20;
+  std::vector<float> th((size_t)nn, 0.01f), mm((size_t)nn, 0.0f), vv((size_t)nn, 0.0f);
+  std::vector<uint16_t> g((size_t)nn, 0x3c00), w((size_t)nn, 0), gc(m->c.keep_host_grad ? (size_t)nn : 0, 0);
+  uint16_t* gcp = m->c.keep_host_grad ? gc.data() : nullptr;
+  double best1 = 1e30, bestn = 1e30;
+  for (int r = 0; r < 2; ++r) {
+    double t0 = now_ms();
+    mth::adam(n1, g.data(), gcp, th.data(), mm.data(), vv.data(), w.data(), r + 1, 1e-3f, 0.9f, 0.999f, 1e-8f, 0.f);
+    best1 = std::min(best1, now_ms() - t0);
+    constexpr int64_t CH = 1 << 18;
+    std::function<void(int64_t)> fn = [&](int64_t i) {
+      const int64_t o = i * CH, len = std::min(CH, nn - o);
+      mth::adam(len, g.data() + o, gcp ? gcp + o : nullptr, th.data() + o, mm.data() + o, vv.data() + o,
+                w.data() + o, r + 1, 1e-3f, 0.9f, 0.999f, 1e-8f, 0.f);
+    };
+    std::string err;
+    t0 = now_ms();
+    if (m->pool.parallel_for((nn + CH - 1) / CH, fn, &err)) bestn = std::min(bestn, now_ms() - t0);
+  }
+  if (best1 > 0 && best1 < 1e30) in.adam_rate1 = (double)n1 / (best1 * 1e-3);
+  const double rn = bestn > 0 && bestn < 1e30 ? (double)nn / (bestn * 1e-3) : 0.0;
+  in.adam_rate_max = mth::adam_asymptote(in.adam_rate1, rn, nth);
+  in.threads = nth;
+}
+
+// The plan with the knobs the config leaves open (K when n_grad_slabs = 0,
+// packing threads when n_pack_threads = 0 and the store is not pinned).
+mth::Plan make_plan(const mt_model* m, int k_max_budget, int np_fixed) {
+  const mt_config& c = m->c;
+  const int kmin = c.n_grad_slabs > 0 ? c.n_grad_slabs : 1;
+  const int kmax = c.n_grad_slabs > 0 ? c.n_grad_slabs : k_max_budget;
+  int npmin = 1, npmax = std::max(1, m->sim.threads / 3);
+  if (np_fixed > 0) npmin = npmax = np_fixed;
+  return mth::plan(m->sim, kmin, kmax, npmin, npmax);
+}
+
+// Once the first step's per-visit compute events have completed: the second
+// plan, on measured compute times, which sets how many packing threads work.
+void replan_measured(mt_model* m) {
+  if (m->have_plan1 || m->first_ev.empty() || m->npass != 1) return;
+  std::vector<double> c(m->first_ev.size());
+  for (size_t v = 0; v < m->first_ev.size(); ++v) {
+    if (cudaEventQuery(m->first_ev[v].second) != cudaSuccess) return;
+    float ms = 0;
+    if (cudaEventElapsedTime(&ms, m->first_ev[v].first, m->first_ev[v].second) != cudaSuccess) return;
+    c[v] = ms * 1e-3;
+  }
+  m->sk_c = c;
+  m->sim.c = m->sk_c.data();
+  // K is allocated already; the packing threads can only shrink
+  mth::SimIn in = m->sim;
+  mth::Plan pl;
+  const int kfix = m->K;
+  if (m->c.pin_store || m->c.n_pack_threads > 0) {
+    pl.K = kfix;
+    pl.n_pack = m->n_pack;
+    pl.out = mth::simulate(in, kfix, m->n_pack, 4, nullptr);
+  } else {
+    pl = mth::plan(in, kfix, kfix, 1, std::max(1, m->n_pack));
+    m->n_pack_active = pl.n_pack;
+  }
+  fill_plan_out(pl, m->sim, 1, &m->plan1);
+  m->have_plan1 = true;
 }
 
 }  // namespace
@@ -1398,6 +1600,7 @@ mt_model::~mt_model() {
   acv.notify_all();
   if (adam_thr.joinable()) adam_thr.join();
   pool.stop();
+  pack_pool.stop();
   if (live) {
     if (sc) cudaStreamSynchronize(sc);
     if (sw) cudaStreamSynchronize(sw);
@@ -1407,6 +1610,10 @@ mt_model::~mt_model() {
       if (*e) cudaEventDestroy(*e);
     for (auto e : SR)
       if (e) cudaEventDestroy(e);
+    for (auto& e : first_ev) {
+      if (e.first) cudaEventDestroy(e.first);
+      if (e.second) cudaEventDestroy(e.second);
+    }
     for (auto& p : pend) {
       cudaEventDestroy(p.a);
       cudaEventDestroy(p.b);
@@ -1417,6 +1624,7 @@ mt_model::~mt_model() {
       cudaEventDestroy(t.b);
     }
     if (trace_base) cudaEventDestroy(trace_base);
+    if (trace_stream) cudaStreamDestroy(trace_stream);
     if (registered) cudaHostUnregister(store);
     for (int b = 0; b < 2; ++b)
       if (staging[b]) cudaFreeHost(staging[b]);
@@ -1443,7 +1651,7 @@ mt_status mt_default_config(mt_config* c) {
   c->ckpt_interval = 1;
   c->ckpt_on_host = 1;
   c->n_buffers = 2;
-  c->n_grad_slabs = 12;
+  c->n_grad_slabs = 0;  // sized by the static schedule
   c->lr = 1e-3f;
   c->beta1 = 0.9f;
   c->beta2 = 0.999f;
@@ -1519,6 +1727,34 @@ mt_status mt_init_model(const mt_config* c, mt_dev_region dev, mt_streams s, mt_
     };
     std::string werr;
     if (!m->pool.parallel_for((int64_t)items.size(), fn, &werr)) return MT_ERR_INTERNAL;
+  }
+  // The static schedule ([Peter] 記憶體預取策略): per-visit bytes from the
+  // layout, link / pack / Adam rates measured here, compute estimated from
+  // FLOPs; it sizes the slab pool (n_grad_slabs = 0) within a tenth of the
+  // host's memory and splits the host threads between packing and Adam.
+  sched_inputs(m.get());
+  run_probes(m.get(), nth);
+  {
+    const long pages = sysconf(_SC_PHYS_PAGES), psz = sysconf(_SC_PAGESIZE);
+    const double phys = pages > 0 && psz > 0 ? (double)pages * (double)psz : 64e9;
+    const int kbud = (int)std::max(2.0, std::min(32.0, std::floor(0.1 * phys / (double)m->wb_max)));
+    const mth::Plan pl = make_plan(m.get(), kbud, c->n_pack_threads);
+    m->K = c->n_grad_slabs > 0 ? c->n_grad_slabs : pl.K;
+    m->n_pack = c->pin_store ? 0 : (c->n_pack_threads > 0 ? c->n_pack_threads : std::max(1, pl.n_pack));
+    m->n_pack_active = m->n_pack;
+    fill_plan_out(pl, m->sim, 0, &m->plan0);
+    if (m->n_pack > 0) {  // the packing threads (the driver is one of them) leave the Adam pool
+      m->pool.stop();
+      m->pool.start(std::max(1, nth - m->n_pack));
+      m->pack_pool.start(m->n_pack - 1);
+    }
+  }
+  if (m->npass == 1) {
+    m->first_ev.assign((size_t)nvisits(m.get()), {nullptr, nullptr});
+    for (auto& e : m->first_ev) {
+      CU(mm, cudaEventCreate(&e.first));
+      CU(mm, cudaEventCreate(&e.second));
+    }
   }
   const size_t gb = c->debug_guards ? (size_t)kGuardBytes : 0;  // canary after each pinned region
   auto guard = [&](uint8_t* p, size_t bytes, const char* name) {
@@ -1682,6 +1918,7 @@ mt_status mt_train_step(mt_model* m, int32_t step, float* loss) {
   if (step != m->steps_done || m->vis != 0 || m->stage != 0 || m->pass != 0)
     return set_err(m, MT_ERR_STATE, "mt_train_step: step index or visit state mismatch", false);
   if (!m->tokens_set) return set_err(m, MT_ERR_STATE, "no tokens set", false);
+  if (step >= 1) replan_measured(m);
   const double t0 = now_ms();
   const int n = nvisits(m);
   for (int p = 0; p < m->npass; ++p)
@@ -1746,6 +1983,7 @@ mt_status mt_sync(mt_model* m) {
     if (!ok) return set_err(m, MT_ERR_TIMEOUT, "timed out draining Adam jobs");
   }
   if (m->timing) collect_timing(m);
+  replan_measured(m);
   if (m->c.debug_guards) OK(check_guards(m));
   return MT_OK;
 }
@@ -1975,6 +2213,58 @@ int32_t mt_schedule(int32_t n, const double* b, const double* d, const double* c
   return mth::schedule(n, b, d, c, a, bw_h2d, bw_d2h, stall);
 }
 
+static bool sim_in(const mt_sched_in* s, mth::SimIn* o) {
+  if (!s || s->n_visits < 1 || !s->kind || !s->block || !s->b || !s->p || !s->d || !s->c || !s->a) return false;
+  if (!(s->bw_h2d > 0) || !(s->bw_d2h > 0) || s->n_buffers < 1 || s->threads < 1) return false;
+  for (int v = 0; v < s->n_visits; ++v)
+    if (s->block[v] < 0 || s->kind[v] < 0 || s->kind[v] > 3) return false;
+  o->n = s->n_visits;
+  o->kind = s->kind;
+  o->block = s->block;
+  o->b = s->b;
+  o->p = s->p;
+  o->d = s->d;
+  o->c = s->c;
+  o->a = s->a;
+  o->nbuf = s->n_buffers;
+  o->bw_h2d = s->bw_h2d;
+  o->bw_d2h = s->bw_d2h;
+  o->pack_rate1 = s->pack_rate1;
+  o->adam_rate1 = s->adam_rate1;
+  o->adam_rate_max = s->adam_rate_max;
+  o->threads = s->threads;
+  return true;
+}
+
+mt_status mt_schedule_simulate(const mt_sched_in* in, int32_t K, int32_t n_pack, mt_sched_plan* out,
+                               double* stall_v) {
+  mth::SimIn si;
+  if (!out || K < 1 || n_pack < 0 || !sim_in(in, &si)) return MT_ERR_ARG;
+  mth::Plan pl;
+  pl.K = K;
+  pl.n_pack = n_pack;
+  pl.out = mth::simulate(si, K, n_pack, 4, stall_v);
+  std::memset(out, 0, sizeof *out);
+  fill_plan_out(pl, si, 0, out);
+  return MT_OK;
+}
+
+mt_status mt_schedule_plan(const mt_sched_in* in, int32_t k_max, mt_sched_plan* out) {
+  mth::SimIn si;
+  if (!out || k_max < 1 || !sim_in(in, &si)) return MT_ERR_ARG;
+  const mth::Plan pl = mth::plan(si, 1, k_max, 1, std::max(1, si.threads / 3));
+  std::memset(out, 0, sizeof *out);
+  fill_plan_out(pl, si, 0, out);
+  return MT_OK;
+}
+
+mt_status mt_get_schedule(const mt_model* m, int32_t which, mt_sched_plan* out) {
+  if (!m || !out || which < 0 || which > 1) return MT_ERR_ARG;
+  if (which == 1 && !m->have_plan1) return MT_ERR_STATE;
+  *out = which == 0 ? m->plan0 : m->plan1;
+  return MT_OK;
+}
+
 mt_status mt_host_bandwidth(size_t bytes, int32_t n_threads, double* copy_gbs, double* adam_gelem_s) {
   if (bytes < (1u << 20) || n_threads < 1) return MT_ERR_ARG;
   const int64_t n = (int64_t)(bytes / 4);
@@ -2047,7 +2337,7 @@ mt_status mt_timing(mt_model* m, int32_t enable) {
 
 mt_status mt_trace(mt_model* m, int32_t enable) {
   if (!m) return MT_ERR_ARG;
-  OK(mt_sync(m));
+  if (!enable || m->tracing) OK(mt_sync(m));  // the previous timeline's events complete before reuse
   if (!enable) {
     m->tracing = false;
     return MT_OK;
@@ -2061,9 +2351,12 @@ mt_status mt_trace(mt_model* m, int32_t enable) {
     std::lock_guard<std::mutex> lk(m->tmu);
     m->thost.clear();
   }
-  // all three streams are idle here: device time 0 and host time 0 coincide
+  // Device time 0: an event on a private stream with nothing queued, so it
+  // completes at once; host time 0 is taken right after it has.  The model's
+  // streams keep running: a timeline can start in the middle of training.
+  if (!m->trace_stream) CU(m, cudaStreamCreateWithFlags(&m->trace_stream, cudaStreamNonBlocking));
   if (!m->trace_base) CU(m, cudaEventCreate(&m->trace_base));
-  CU(m, cudaEventRecord(m->trace_base, m->sc));
+  CU(m, cudaEventRecord(m->trace_base, m->trace_stream));
   CU(m, cudaEventSynchronize(m->trace_base));
   m->trace_host_base = now_ms();
   m->tracing = true;

@@ -78,7 +78,9 @@ typedef struct {
                               recomputation)                               */
   int32_t ckpt_on_host;    /* 1: layer-boundary activations in pinned host RAM
                               (device footprint independent of depth)      */
-  int32_t n_grad_slabs;    /* K pinned gradient slabs ([Hotdry]: default 12) */
+  int32_t n_grad_slabs;    /* K pinned gradient slabs ([Hotdry]: 12 in the
+                              pages' system); 0 (the default): K chosen at
+                              init by the static schedule (mt_get_schedule) */
   int32_t n_host_threads;  /* host worker threads; 0 = online cores         */
   float lr, beta1, beta2, adam_eps, weight_decay; /* 1e-3, .9, .999, 1e-8, 0 */
   uint64_t seed;           /* weight initialisation seed                     */
@@ -113,6 +115,10 @@ typedef struct {
                               piece and every pinned host region, checked by
                               mt_sync: an overwrite latches MT_ERR_INTERNAL
                               naming the region (overflow / race detector) */
+  int32_t n_pack_threads;  /* pin_store = 0: host threads that pack weights
+                              into pinned staging (the driver thread is one
+                              of them); the others run Adam.  0 (the
+                              default): chosen by the static schedule */
 } mt_config;
 
 typedef struct { void* base; size_t bytes; } mt_dev_region;          /* caller-owned device memory  */
@@ -138,16 +144,35 @@ typedef struct {
 /* ------------------------------------------------------------------ model */
 /* Defaults above for every runtime field; shape fields are zeroed. */
 mt_status mt_default_config(mt_config* cfg);
-/* Device bytes mt_init_model will carve from the caller's region. */
+/* Device bytes mt_init_model will carve from the caller's region: the two
+ * ping-pong buffers (each the largest block's W and G regions), one layer's
+ * activations for the step's tokens and fixed scratch.  It depends on the
+ * widest block and the tokens per step, not on the depth ([Lilting] design
+ * section: only the two buffers stay on the GPU, a fixed allocation from 7.6B
+ * to 43B; [Review] 3-2 (1): device memory is bound by the layer being
+ * computed and its buffers).  MT_ERR_ARG for an invalid config. */
 mt_status mt_query_device_bytes(const mt_config* cfg, size_t* bytes_needed);
 /* Allocates the host flat store (library-owned), fills it from the seeded
  * generator (FP32 master N(0, init_std) for matrices, 1 for RMSNorm gains,
  * W = bf16_rne(master), m = v = 0), allocates pinned staging, slabs and the
  * checkpoint store, creates the events and starts the host workers.  The
- * device region and the streams must outlive the model. */
+ * device region and the streams must outlive the model.
+ * Sources: [Review] 3-2 (1) (host memory is the authoritative store of
+ * parameters, gradients and optimizer state; the GPU starts empty) and 3-2
+ * (4) (one contiguous block per layer, a few pinned staging buffers);
+ * [Hotdry] host memory layout (pageable master store, two pinned staging
+ * buffers sized to the largest layer, K = 12 gradient slabs); [Peter]
+ * 記憶體預取策略 (the static prefetch schedule, planned here from the
+ * blocks' bytes and the link bandwidth measured at init).
+ * Errors: MT_ERR_ARG (invalid config, null region or stream),
+ * MT_ERR_DEVICE_OOM (region smaller than mt_query_device_bytes),
+ * MT_ERR_HOST_OOM (store or pinned memory), MT_ERR_CUDA. */
 mt_status mt_init_model(const mt_config* cfg, mt_dev_region dev, mt_streams s, mt_model** model_out);
 /* Copies the step's token ids (host, [micro][batch][seq] int32 in [0, V))
- * and uploads them on the compute stream. */
+ * into pinned memory; the embedding's forward visit uploads them on the
+ * compute stream.  The pages do not describe how a batch reaches the GPU;
+ * the tokens are the input of the streaming forward of [Review] 3-2 (2).
+ * MT_ERR_ARG for a token outside [0, V) or a null pointer. */
 mt_status mt_set_tokens(mt_model* model, const int32_t* tok);
 
 /* The pages' primitives ([Hotdry] StreamIn / Bind / gradient export; [Review]
@@ -185,12 +210,20 @@ mt_status mt_adam_host(mt_model* model, int32_t block, int32_t slab, int32_t ada
 /* One whole step (0-based index `step`, which must equal the number of steps
  * done) following the static schedule; *loss (if not null) receives the step
  * loss once its value has reached the host.  Returns after enqueuing the
- * last backward visit; Adam of the last blocks may still run. */
+ * last backward visit; Adam of the last blocks may still run.
+ * Sources: [Review] 3-2 (2)-(3) (streaming forward, block-wise recomputing
+ * backward, three streams overlapping the next transfer, the current compute
+ * and the previous gradient export); [Hotdry] event protocol; [Peter]
+ * 記憶體預取策略 (prefetch timed from each layer's bytes, the link bandwidth
+ * and the layer's compute time). */
 mt_status mt_train_step(mt_model* model, int32_t step, float* loss);
 /* Waits (bounded) for every queued copy, kernel and Adam job. */
 mt_status mt_sync(mt_model* model);
 /* Copies `bytes` of a block's region (MT_REGION_*) out of / into the host
- * store (after mt_sync).  bytes must not exceed the region. */
+ * store (after mt_sync).  bytes must not exceed the region (MT_ERR_ARG).
+ * The store is the model's authoritative state ([Review] 3-2 (1); [Hotdry]
+ * host memory layout: W, G and FP32 state of one layer in one block), so
+ * these calls read and write the model itself. */
 mt_status mt_read_host(mt_model* model, int32_t block, int32_t region, void* dst, size_t bytes);
 mt_status mt_write_host(mt_model* model, int32_t block, int32_t region, const void* src, size_t bytes);
 /* Counters since mt_init_model (bytes copied per direction, host Adam and
@@ -217,12 +250,16 @@ mt_status mt_expert_counts(const mt_model* model, int32_t block, int32_t* counts
  * -(needed) when cap is too small. */
 int64_t mt_protocol_log(const mt_model* model, char* buf, int64_t cap);
 /* Text of the last error ("" if none, "null model" for NULL), copied into
- * storage of the calling thread: valid until that thread calls again. */
+ * storage of the calling thread: valid until that thread calls again.
+ * Error reporting has no counterpart on the pages; it belongs to this C ABI,
+ * where no exception may cross the boundary. */
 const char* mt_last_error(const mt_model* model);
 /* Stops the host workers, waits for the work queued on the model's three
  * streams, then frees everything the library owns (host store, pinned
  * memory, events).  The caller's device region and streams are left alone.
- * Accepts NULL. */
+ * Accepts NULL.  Teardown has no counterpart on the pages; the ownership it
+ * releases is the one of [Hotdry] host memory layout (store and pinned
+ * buffers on the host side). */
 void mt_destroy(mt_model* model);
 
 /* ------------------------------------------------------------------ host-only */
@@ -262,6 +299,56 @@ int32_t mt_visit_plan(const mt_config* cfg, int32_t* kind, int32_t* block, int32
  * returns the slab count needed, or -1. */
 int32_t mt_schedule(int32_t n_visits, const double* b, const double* d, const double* c,
                     const double* a, double bw_h2d, double bw_d2h, double* stall);
+/* The static schedule as a steady-state model of the whole pipeline: the
+ * pack of each visit's weights into pinned staging (n_pack threads), the
+ * host-to-device copy, the compute, the gradient export into one of K slabs
+ * and host Adam (the remaining threads, lowest block first among landed
+ * slabs), with every dependency of the event protocol (Buffer-Free,
+ * Weights-Ready, Backward-Done, a free slab, and the next step's forward of a
+ * block after its Adam).  Per visit v of a step (mt_visit_plan order):
+ * kind[v], block[v], b[v] host-to-device bytes, p[v] bytes packed first (0
+ * with a pinned store), d[v] exported gradient bytes, c[v] compute seconds,
+ * a[v] Adam elements of the exported block.  Rates: link bytes/s per
+ * direction, pack bytes/s of one thread, Adam elements/s of one thread (r1)
+ * and the asymptote r_max of n threads, r(n) = r_max (1 - exp(-n r1 /
+ * r_max)) (host memory saturates).  Sources: [Peter]
+ * 記憶體預取策略 (prefetch from layer bytes, link bandwidth and compute time);
+ * [Hotdry] slab pool and event protocol; [Review] 3-2 (4), (6). */
+typedef struct {
+  int32_t n_visits;
+  const int32_t *kind, *block;
+  const double *b, *p, *d, *c, *a;
+  int32_t n_buffers;
+  double bw_h2d, bw_d2h, pack_rate1, adam_rate1, adam_rate_max;
+  int32_t threads;   /* host threads shared by packing and Adam */
+} mt_sched_in;
+typedef struct {
+  int32_t K, n_pack; /* slabs, packing threads */
+  int32_t measured;  /* mt_get_schedule: 1 if c[] was measured in the first step */
+  double period_ms;  /* predicted steady-state step time */
+  double stall_ms;   /* predicted compute-stream idle time per step */
+  double adam_busy_ms, slab_wait_ms, pack_ms;
+  /* mt_get_schedule: the init-time measurements the plan used */
+  double bw_h2d_gbs, bw_d2h_gbs, pack_gbs_thread, adam_gelem_s_thread, adam_gelem_s_max;
+} mt_sched_plan;
+/* Simulates the pipeline with K slabs and n_pack packing threads (stall_v:
+ * n_visits entries, may be null: the predicted wait before each visit
+ * computes).  MT_ERR_ARG for missing arrays, n_visits < 1, K < 1 or a
+ * non-positive link bandwidth. */
+mt_status mt_schedule_simulate(const mt_sched_in* in, int32_t K, int32_t n_pack, mt_sched_plan* out,
+                               double* stall_v);
+/* Chooses K in [1, k_max] and n_pack (0 when nothing is packed, else in
+ * [1, threads / 3]): the shortest predicted step, then the fewest slabs and
+ * packing threads within 0.5 % of it. */
+mt_status mt_schedule_plan(const mt_sched_in* in, int32_t k_max, mt_sched_plan* out);
+/* The plan a model runs with: which = 0, made in mt_init_model from the
+ * blocks' bytes, the link, pack and Adam rates measured there and compute
+ * times estimated from each visit's tensor FLOPs at 1.2 PFLOP/s (it set K
+ * when n_grad_slabs was 0, and the packing threads when n_pack_threads was
+ * 0); which = 1, made again once the first step's per-visit compute times
+ * (CUDA events) are known, which then sets how many of the packing threads
+ * work (MT_ERR_STATE until then). */
+mt_status mt_get_schedule(const mt_model* model, int32_t which, mt_sched_plan* out);
 /* Host memory bandwidth on this machine: a parallel copy of `bytes` (GB/s,
  * read + write bytes) and the library's Adam (G elements/s) on n_threads
  * threads; every pass runs 3 times and the best is reported. */
@@ -360,12 +447,15 @@ mt_status mt_timing_read(mt_model* model, int32_t kind, int64_t* launches, doubl
  * *n_visits = n.  These are the per-block compute times the static prefetch
  * schedule (mt_schedule) takes. */
 mt_status mt_timing_visits(mt_model* model, double* ms, int32_t cap, int32_t* n_visits);
-/* Stream timeline.  mt_trace(model, 1) drains all work, clears the timeline
- * and starts recording: CUDA events around every weight / expert / checkpoint
- * copy on the weight stream, every visit's compute on the compute stream and
- * every gradient / checkpoint export on the gradient stream, and the wall
- * time of every host Adam job, all relative to one instant (the streams are
- * idle when recording starts).  mt_trace(model, 0) drains and stops.
+/* Stream timeline.  mt_trace(model, 1) clears the timeline and starts
+ * recording, without draining the work already queued (so a timeline can be
+ * taken in the steady state of training): CUDA events around every weight /
+ * expert / checkpoint copy on the weight stream, every visit's compute on the
+ * compute stream and every gradient / checkpoint export on the gradient
+ * stream enqueued from then on, and the wall time of every host Adam job that
+ * ends from then on, all relative to one instant (an event on an idle private
+ * stream, and the host clock right after it completed).  Calling it while
+ * recording drains first.  mt_trace(model, 0) drains and stops.
  * mt_trace_json writes the timeline (after mt_sync) as Chrome trace-event
  * JSON ({"traceEvents": [...]}, times in microseconds; threads "weight
  * stream", "compute stream", "gradient stream", "host Adam"); returns its

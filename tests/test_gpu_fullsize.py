@@ -2,11 +2,15 @@
 
 Two kinds of checks:
 * full-width, depth-truncated steps (the real hidden, FFN, head and
-  vocabulary sizes of the 1.2B- and 7.6B-shaped decoders with one or two
-  layers and one short sequence) against the oracle element by element, with
-  the whole-step tolerances;
-* properties that hold at any size, run in exactly the configuration the
-  benchmark times (the 1.2B shape: 22 layers, 4 x 2048 tokens): with a zero
+  vocabulary sizes of the 1.2B-, 7.6B- and 14.7B-shaped decoders with one or
+  two layers and one short sequence) against the oracle element by element,
+  with the whole-step tolerances;
+* properties that hold at any size, run in the configuration the benchmark
+  times (the 7.6B shape: 28 layers, 4 micro-batches of 4096 tokens, weights
+  packed just in time into pinned staging, slabs and packing threads chosen
+  by the static schedule; the one difference is that each gradient slab is
+  also unpacked into the store's G region, so that the tests can read the
+  gradients): with a zero
   LM head the loss is ln V and every upstream gradient is exactly zero, the
   head-gradient rows of vocabulary entries no target names are identical,
   embedding rows of tokens seen only at a sequence's last position (or not at
@@ -44,10 +48,21 @@ def test_full_width_7p6b_one_layer(orc):
     run_parity(orc, c, 1, check_init=False)
 
 
+def test_full_width_14p7b_one_layer(orc):
+    """The Qwen2.5-14B width: hidden 5120, 40 query heads sharing 8 KV heads
+    (groups of 5), FFN 13824, vocabulary 152064."""
+    c = configs.get("14.7b", n_layers=1, batch=1, seq=64, micro=1)
+    assert c["n_heads"] // c["n_kv_heads"] == 5
+    run_parity(orc, c, 1, check_init=False)
+
+
+BENCH = dict(pin_store=0, keep_host_grad=1)  # the benchmark's launch configuration, G kept for reading
+
+
 def test_bench_size_zero_head_properties():
-    c = configs.get("1.2b")  # the benchmark's workload
+    c = configs.get("7.6b")  # the benchmark's workload
     V, H = c["vocab"], c["hidden"]
-    m = mt.Model(c, seed=1234, n_grad_slabs=12)
+    m = mt.Model(c, seed=1234, **BENCH)
     L = c["n_layers"]
     head = m.layout[L + 1]
     eo, r, cc = head["tensors"][1]
@@ -75,9 +90,9 @@ def test_bench_size_zero_head_properties():
 
 
 def test_bench_size_embedding_rows_and_sampled_adam(orc):
-    c = configs.get("1.2b")
+    c = configs.get("7.6b")
     V, H = c["vocab"], c["hidden"]
-    m = mt.Model(c, seed=1234)
+    m = mt.Model(c, seed=1234, **BENCH)
     L = c["n_layers"]
     master0 = [m.read(j, mt.REGION_MASTER) for j in (0, 1, L, L + 1)]
     tok = inputs.tokens_for(c, 0)

@@ -146,10 +146,12 @@ def test_manual_primitives_match_train_step(ci, nbuf, name):
             b.adam_host(j, k, 1)
     b.sync()
     for j in range(c["n_layers"] + 2):
-        ga = a.read(j, mt.REGION_G).view(np.int16).astype(np.float32)
-        gb = b.read(j, mt.REGION_G).view(np.int16).astype(np.float32)
+        # the same kernels run in the same order on the same inputs: the
+        # exported BF16 gradients agree bit for bit
+        ga, gb = a.read(j, mt.REGION_G), b.read(j, mt.REGION_G)
+        assert np.array_equal(ga, gb), j
         ma, mb = a.read(j, mt.REGION_MASTER), b.read(j, mt.REGION_MASTER)
-        assert rel_l2(mb, ma) <= 1e-5
+        assert np.array_equal(ma.view(np.uint32), mb.view(np.uint32)), j
     # out-of-order calls are refused without latching the model
     with pytest.raises(mt.MtError) as ei:
         b.stream_in(3, 0)

@@ -18,8 +18,10 @@ from host_memory_centric_gb300 import configs, inputs  # noqa: E402
 EPS = 2e-3  # ms: event timestamp resolution
 
 
-@pytest.mark.parametrize("name", ["tiny", "tiny_moe"])
-def test_timeline_records_the_protocol_order(name):
+@pytest.mark.parametrize("name,steady", [("tiny", False), ("tiny_moe", False), ("tiny", True)])
+def test_timeline_records_the_protocol_order(name, steady):
+    """steady: recording starts while the previous step is still in flight
+    (no drain), as for a timeline of training in its steady state."""
     c = configs.get(name, n_layers=3)
     L = c["n_layers"]
     m = mt.Model(c, seed=3)
@@ -27,12 +29,17 @@ def test_timeline_records_the_protocol_order(name):
     m.train_step(0)  # first step: lazy loading and caches out of the way
     m.sync()
     m.set_tokens(inputs.tokens_for(c, 1))
+    if steady:
+        m.train_step(1)
+        m.set_tokens(inputs.tokens_for(c, 2))
     m.trace(True)
-    m.train_step(1)
+    m.train_step(2 if steady else 1)
     m.sync()
     ev = m.trace_events()
     m.trace(False)
     m.close()
+    # host Adam jobs of the previous step that ended after recording started are recorded too
+    ev = [e for e in ev if e["tid"] != "host Adam" or e["args"]["step"] == (2 if steady else 1)]
     by = {}
     for e in ev:
         by.setdefault((e["tid"], e["name"].split()[0]), []).append(e)

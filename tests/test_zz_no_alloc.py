@@ -68,11 +68,29 @@ def test_noalloc_matches_allocating_entry_point_twice(T, H):
         assert torch.equal(dx_b, dx_a) and torch.equal(dg_b, dg_a), (_rel_l2(dx_b, dx_a), _rel_l2(dg_b, dg_a))
 
 
-def test_noalloc_rejects_sizes_beyond_its_array():
-    T, H = 65536, 12288  # 304 partial rows of 12288 floats > the 304 x 8192 array
+def test_noalloc_at_its_limit_and_beyond():
+    """At exactly the array's size the call runs and matches the allocating
+    entry point; one size past it is refused before anything is launched.
+    Both calls get real buffers of the full [T, H] size, so that a broken size
+    check shows up as a wrong status or wrong values, never as an access past
+    the end of a buffer."""
+    T = 9728  # the smallest T that gives the maximum of 304 blocks (32 rows each)
+    assert ops.rmsnorm_bwd_scratch_bytes(T, 8192) == 4 * 304 * 8192
+    dy, x, g, r, dres = _case(T, 8192, 3)
+    dx_a, dg_a = torch.empty_like(x), torch.empty(8192, dtype=torch.bfloat16, device="cuda")
+    scratch = torch.empty(ops.rmsnorm_bwd_scratch_bytes(T, 8192), dtype=torch.uint8, device="cuda")
+    ops.rmsnorm_bwd(dy, x, g, r, dres, dx_a, dg_a, scratch)
+    dx_b, dg_b = torch.empty_like(x), torch.empty(8192, dtype=torch.bfloat16, device="cuda")
+    assert _call_noalloc(dy, x, g, r, dres, dx_b, dg_b) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(dx_b, dx_a) and torch.equal(dg_b, dg_a)
+    del dy, x, g, r, dres, dx_a, dg_a, dx_b, dg_b, scratch
+
+    H = 8200  # 304 partial rows of 8200 floats: one column more than the array holds
     assert ops.rmsnorm_bwd_scratch_bytes(T, H) > 4 * 304 * 8192
-    t = torch.empty(8, dtype=torch.bfloat16, device="cuda")
-    r = torch.empty(8, dtype=torch.float32, device="cuda")
-    st = _noalloc()(t.data_ptr(), t.data_ptr(), t.data_ptr(), r.data_ptr(), None, T, H, t.data_ptr(),
-                    t.data_ptr(), torch.cuda.current_stream().cuda_stream)
-    assert st == -1  # MT_ERR_ARG, nothing launched
+    dy, x, g, r, dres = _case(T, H, 4)
+    dx = torch.full_like(x, 7.0)
+    dg = torch.full((H,), 7.0, dtype=torch.bfloat16, device="cuda")
+    assert _call_noalloc(dy, x, g, r, dres, dx, dg) == -1  # MT_ERR_ARG
+    torch.cuda.synchronize()
+    assert bool((dx == 7.0).all()) and bool((dg == 7.0).all())  # nothing was launched
