@@ -250,15 +250,14 @@ def schedule_report(m, vis_ms, t_step):
     beside the stall measured here: the timed step minus the compute of its
     visits (per-visit CUDA events of the timed steps)."""
     p0, p1 = m.schedule(0), m.schedule(1)
-    keep = ("K", "n_pack", "measured", "period_ms", "stall_ms", "adam_busy_ms", "slab_wait_ms", "pack_ms")
+    keep = ("K", "measured", "period_ms", "stall_ms", "adam_busy_ms", "slab_wait_ms", "pack_ms", "adam_gelem_s")
     out = {"init": {k: p0[k] for k in keep}, "after_first_step": ({k: p1[k] for k in keep} if p1 else None),
-           "probes": {k: p0[k] for k in ("bw_h2d_gbs", "bw_d2h_gbs", "pack_gbs_thread", "adam_gelem_s_thread",
-                                         "adam_gelem_s_max")}}
+           "probes": {k: p0[k] for k in ("bw_h2d_gbs", "bw_d2h_gbs", "pack_gbs", "adam_gelem_s_idle", "host_gbs")}}
     if len(vis_ms) and np.all(vis_ms > 0):
         out["measured"] = {"step_ms": t_step * 1e3, "compute_ms": float(vis_ms.sum()),
                            "stall_ms": float(t_step * 1e3 - vis_ms.sum())}
-    out["note"] = ("slabs and packing threads set by the plan at init; predicted = the pipeline model "
-                   "(link, pack, compute, export, slabs, host Adam; no host-memory contention between DMA and Adam)")
+    out["note"] = ("K set by the plan at init; predicted = the pipeline model (link, chunked pack, compute, "
+                   "export into K slabs, host Adam sharing the measured host-memory bandwidth with DMA and the pack)")
     return out
 
 
@@ -552,7 +551,6 @@ def main():
                     help="0: just-in-time pack into pinned staging (the method); 1: register the whole store")
     ap.add_argument("--threads", type=int, default=0)
     ap.add_argument("--slabs", type=int, default=0, help="gradient slabs K (0: chosen by the static schedule)")
-    ap.add_argument("--pack-threads", type=int, default=0, help="packing threads (0: chosen by the static schedule)")
     ap.add_argument("--keep-host-grad", type=int, default=0)
     ap.add_argument("--ckpt-on-host", type=int, default=1)
     ap.add_argument("--ckpt-interval", type=int, default=1, help="layers per recompute segment")
@@ -620,7 +618,7 @@ def main():
     timeout_s = args.timeout if args.timeout > 0 else max(60.0, 4.0 * F_exec / 4e14)
     dev_base = device_used(torch)
     m = mt.Model(c, seed=1234, pin_store=args.pin_store, n_host_threads=args.threads, n_grad_slabs=args.slabs,
-                 n_pack_threads=args.pack_threads, timeout_ms=int(min(timeout_s * 1e3, 4.0e9)),
+                 timeout_ms=int(min(timeout_s * 1e3, 4.0e9)),
                  keep_host_grad=args.keep_host_grad, ckpt_on_host=args.ckpt_on_host,
                  ckpt_interval=args.ckpt_interval, n_buffers=args.buffers, host_grad_accum=args.host_accum)
     init_s = time.time() - t_init

@@ -45,8 +45,7 @@ class MtConfig(C.Structure):
                 ("seed", C.c_uint64), ("timeout_ms", C.c_uint32), ("pin_store", C.c_int32),
                 ("head_chunk", C.c_int32), ("log_protocol", C.c_int32), ("keep_host_grad", C.c_int32),
                 ("n_buffers", C.c_int32), ("host_grad_accum", C.c_int32), ("n_experts", C.c_int32),
-                ("top_k", C.c_int32), ("expert_ffn", C.c_int32), ("debug_guards", C.c_int32),
-                ("n_pack_threads", C.c_int32)]
+                ("top_k", C.c_int32), ("expert_ffn", C.c_int32), ("debug_guards", C.c_int32)]
 
 
 class DevRegion(C.Structure):
@@ -66,16 +65,15 @@ class SchedIn(C.Structure):
     _fields_ = [("n_visits", C.c_int32), ("kind", C.POINTER(C.c_int32)), ("block", C.POINTER(C.c_int32)),
                 ("b", C.POINTER(C.c_double)), ("p", C.POINTER(C.c_double)), ("d", C.POINTER(C.c_double)),
                 ("c", C.POINTER(C.c_double)), ("a", C.POINTER(C.c_double)), ("n_buffers", C.c_int32),
-                ("bw_h2d", C.c_double), ("bw_d2h", C.c_double), ("pack_rate1", C.c_double),
-                ("adam_rate1", C.c_double), ("adam_rate_max", C.c_double), ("threads", C.c_int32)]
+                ("bw_h2d", C.c_double), ("bw_d2h", C.c_double), ("pack_rate", C.c_double),
+                ("adam_rate", C.c_double), ("adam_bytes", C.c_double), ("host_bw", C.c_double)]
 
 
 class SchedPlan(C.Structure):
-    _fields_ = [("K", C.c_int32), ("n_pack", C.c_int32), ("measured", C.c_int32), ("period_ms", C.c_double),
-                ("stall_ms", C.c_double), ("adam_busy_ms", C.c_double), ("slab_wait_ms", C.c_double),
-                ("pack_ms", C.c_double), ("bw_h2d_gbs", C.c_double), ("bw_d2h_gbs", C.c_double),
-                ("pack_gbs_thread", C.c_double), ("adam_gelem_s_thread", C.c_double),
-                ("adam_gelem_s_max", C.c_double)]
+    _fields_ = [("K", C.c_int32), ("measured", C.c_int32), ("period_ms", C.c_double), ("stall_ms", C.c_double),
+                ("adam_busy_ms", C.c_double), ("slab_wait_ms", C.c_double), ("pack_ms", C.c_double),
+                ("adam_gelem_s", C.c_double), ("bw_h2d_gbs", C.c_double), ("bw_d2h_gbs", C.c_double),
+                ("pack_gbs", C.c_double), ("adam_gelem_s_idle", C.c_double), ("host_gbs", C.c_double)]
 
 
 class Stats(C.Structure):
@@ -127,7 +125,7 @@ def lib():
         "mt_plan_protocol": (i64, [pc, i32, C.c_char_p, i64]),
         "mt_visit_plan": (i32, [pc, _P(i32), _P(i32), i32]),
         "mt_schedule": (i32, [i32, _P(f64), _P(f64), _P(f64), _P(f64), f64, f64, _P(f64)]),
-        "mt_schedule_simulate": (i32, [_P(SchedIn), i32, i32, _P(SchedPlan), _P(f64)]),
+        "mt_schedule_simulate": (i32, [_P(SchedIn), i32, _P(SchedPlan), _P(f64)]),
         "mt_schedule_plan": (i32, [_P(SchedIn), i32, _P(SchedPlan)]),
         "mt_get_schedule": (i32, [_v, i32, _P(SchedPlan)]),
         "mt_token_csr": (i32, [_P(i32), i64, i32, _P(i32), _P(i32)]),
@@ -210,27 +208,27 @@ def visit_plan(cfg: MtConfig) -> list[tuple[int, int]]:
     return list(zip(k, b))
 
 
-def sched_in(kind, block, b, p, d, c, a, n_buffers=2, bw_h2d=2e11, bw_d2h=2e11, pack_rate1=2e10,
-             adam_rate1=2e9, adam_rate_max=8e9, threads=16):
+def sched_in(kind, block, b, p, d, c, a, n_buffers=2, bw_h2d=2e11, bw_d2h=2e11, pack_rate=1.2e11,
+             adam_rate=8.5e9, adam_bytes=28.0, host_bw=0.0):
     """An mt_sched_in over numpy arrays (kept alive on the returned object)."""
     arrs = [np.ascontiguousarray(kind, np.int32), np.ascontiguousarray(block, np.int32)]
     arrs += [np.ascontiguousarray(x, np.float64) for x in (b, p, d, c, a)]
     s = SchedIn(len(arrs[0]), *(_ptr(x, C.c_int32) for x in arrs[:2]), *(_ptr(x, C.c_double) for x in arrs[2:]),
-                n_buffers, bw_h2d, bw_d2h, pack_rate1, adam_rate1, adam_rate_max, threads)
+                n_buffers, bw_h2d, bw_d2h, pack_rate, adam_rate, adam_bytes, host_bw)
     s._keep = arrs
     return s
 
 
-def schedule_simulate(si: SchedIn, K: int, n_pack: int) -> tuple[dict, np.ndarray]:
+def schedule_simulate(si: SchedIn, K: int) -> tuple[dict, np.ndarray]:
     """mt_schedule_simulate: the predicted steady-state step and per-visit stalls."""
     p = SchedPlan()
     stall = np.zeros(si.n_visits)
-    check(lib().mt_schedule_simulate(C.byref(si), K, n_pack, C.byref(p), _ptr(stall, C.c_double)))
+    check(lib().mt_schedule_simulate(C.byref(si), K, C.byref(p), _ptr(stall, C.c_double)))
     return {k: getattr(p, k) for k, _ in SchedPlan._fields_}, stall
 
 
 def schedule_plan(si: SchedIn, k_max: int) -> dict:
-    """mt_schedule_plan: K and packing threads chosen by the simulation."""
+    """mt_schedule_plan: the slab count chosen by the simulation."""
     p = SchedPlan()
     check(lib().mt_schedule_plan(C.byref(si), k_max, C.byref(p)))
     return {k: getattr(p, k) for k, _ in SchedPlan._fields_}

@@ -1,6 +1,7 @@
 // mt_host.cpp -- host-side pieces of libmt that need no GPU.
 #include "mt_host.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 
@@ -22,7 +23,6 @@ bool config_valid(const mt_config* c, std::string* why) {
   if (c->n_buffers != 1 && c->n_buffers != 2) return bad("n_buffers must be 1 or 2");
   if (c->host_grad_accum != 0 && c->host_grad_accum != 1) return bad("host_grad_accum must be 0 or 1");
   if (c->n_grad_slabs < 0 || c->n_grad_slabs > 256) return bad("n_grad_slabs out of range");
-  if (c->n_pack_threads < 0 || c->n_pack_threads > 256) return bad("n_pack_threads out of range");
   if (c->n_experts < 0) return bad("n_experts must be >= 0");
   if (c->n_experts > 0) {
     if (c->n_experts > 128 || c->n_experts % 8) return bad("n_experts must be a multiple of 8 and <= 128");
@@ -247,29 +247,33 @@ void Pool::run(Task& t) {
   if (--t.latch->left == 0) t.latch->cv.notify_all();
 }
 
-bool Pool::run_one() {
+bool Pool::run_own(const Latch* latch) {
   Task t;
   {
     std::lock_guard<std::mutex> lk(mu_);
-    if (q_.empty()) return false;
-    t = q_.front();
-    q_.pop_front();
+    auto it = std::find_if(q_.begin(), q_.end(), [&](const Task& x) { return x.latch == latch; });
+    if (it == q_.end()) return false;
+    t = *it;
+    q_.erase(it);
   }
   run(t);
   return true;
 }
 
-bool Pool::parallel_for(int64_t n, const std::function<void(int64_t)>& fn, std::string* err) {
+bool Pool::parallel_for(int64_t n, const std::function<void(int64_t)>& fn, std::string* err, bool urgent) {
   if (n <= 0) return true;
   Latch latch;
   latch.left = n;
   {
     std::lock_guard<std::mutex> lk(mu_);
-    for (int64_t i = 0; i < n; ++i) q_.push_back({&fn, i, &latch});
+    if (urgent)
+      for (int64_t i = n - 1; i >= 0; --i) q_.push_front({&fn, i, &latch});
+    else
+      for (int64_t i = 0; i < n; ++i) q_.push_back({&fn, i, &latch});
   }
   cv_.notify_all();
   for (;;) {
-    if (run_one()) continue;  // help with queued tasks
+    if (run_own(&latch)) continue;  // help with this call's own queued tasks only
     std::unique_lock<std::mutex> lk(latch.mu);
     if (latch.cv.wait_for(lk, std::chrono::milliseconds(2), [&] { return latch.left == 0; })) break;
   }
@@ -367,105 +371,92 @@ struct AdamSim {
     return true;
   }
 };
-}  // namespace
 
-double adam_rate(const SimIn& in, int n) {
-  if (!(in.adam_rate1 > 0)) return 1e30;
-  if (!(in.adam_rate_max > 0)) return n * in.adam_rate1;
-  return in.adam_rate_max * (1.0 - std::exp(-(double)n * in.adam_rate1 / in.adam_rate_max));
-}
-
-double adam_asymptote(double r1, double rn, int n) {
-  if (!(r1 > 0) || !(rn > 0) || n < 1) return rn;
-  if (rn >= n * r1) return n * r1 * 1e3;  // no saturation seen: practically linear
-  double a = rn;
-  for (int i = 0; i < 100; ++i) a = rn / (1.0 - std::exp(-(double)n * r1 / a));
-  return a;
-}
-
-SimOut simulate(const SimIn& in, int32_t K, int32_t n_pack, int32_t steps, double* stall_v) {
+SimOut simulate_at(const SimIn& in, int32_t K, int32_t steps, double* stall_v, double adam_rate) {
   SimOut out;
   const int n = in.n, nb = in.nbuf < 1 ? 1 : in.nbuf;
-  if (n <= 0 || K < 1 || steps < 2 || !(in.bw_h2d > 0) || !(in.bw_d2h > 0)) return out;
-  bool packs = false;
-  for (int v = 0; v < n; ++v) packs = packs || in.p[v] > 0;
-  const int np = packs ? (n_pack < 1 ? 1 : n_pack) : 0;
-  const int na = in.threads - np > 1 ? in.threads - np : 1;
   AdamSim ad;
-  ad.rate = adam_rate(in, na);
-  if (!(ad.rate > 0)) ad.rate = 1e30;
-  const double prate = np * in.pack_rate1 > 0 ? np * in.pack_rate1 : 1e30;
-  std::vector<double> h2d_end(nb, 0.0), bf(nb, 0.0), slab_release;  // release time of each slab holder
-  std::vector<int> holder;  // job index holding each slab, -1 when released at slab_release
-  holder.assign((size_t)K, -1);
-  slab_release.assign((size_t)K, 0.0);
-  std::vector<double> adam_done;  // [step][block]
+  ad.rate = adam_rate > 0 ? adam_rate : 1e30;
+  const double prate = in.pack_rate > 0 ? in.pack_rate : 1e30;
+  std::vector<double> h2d_end((size_t)nb, 0.0), bf((size_t)nb, 0.0), slab_release((size_t)K, 0.0);
+  std::vector<int> holder((size_t)K, -1);  // job holding each slab (-1: released at slab_release)
   int nblocks = 0;
   for (int v = 0; v < n; ++v) nblocks = in.block[v] + 1 > nblocks ? in.block[v] + 1 : nblocks;
-  adam_done.assign((size_t)steps * nblocks, -1.0);
+  std::vector<double> adam_done((size_t)steps * nblocks, -1.0);  // [step][block]
   double drv = 0, w_free = 0, c_free = 0, g_free = 0;
-  double first_c[2] = {0, 0}, stall_sum[1] = {0}, slab_sum[2] = {0, 0}, pack_sum[2] = {0, 0};
-  auto release_of = [&](int k) { return holder[(size_t)k] < 0 ? slab_release[(size_t)k] : ad.jobs[(size_t)holder[(size_t)k]].end; };
+  double first_c[2] = {0, 0}, stall_sum = 0, slab_sum = 0, pack_sum = 0;
+  auto release_of = [&](int k) {
+    return holder[(size_t)k] < 0 ? slab_release[(size_t)k] : ad.jobs[(size_t)holder[(size_t)k]].end;
+  };
   for (int s = 0; s < steps; ++s) {
     const int rec = s == steps - 1 ? 1 : (s == steps - 2 ? 0 : -1);
     for (int v = 0; v < n; ++v) {
       const int kind = in.kind[v], j = in.block[v], b = v % nb;
       double t = drv;
       if (kind <= 1 && s > 0) {  // the forward of block j waits for its previous Adam
-        double& ready = adam_done[(size_t)(s - 1) * nblocks + j];
-        while (ready < 0 && ad.next()) {
+        const size_t idx = (size_t)(s - 1) * nblocks + j;
+        while (adam_done[idx] < 0 && ad.next())
           for (const SimJob& jb : ad.jobs)
             if (jb.end >= 0) adam_done[(size_t)jb.step * nblocks + jb.block] = jb.end;
-        }
-        if (ready > t) t = ready;
+        if (adam_done[idx] > t) t = adam_done[idx];
       }
+      double pack_end = t, first_chunk = t;
       if (in.p[v] > 0) {
         if (h2d_end[(size_t)b] > t) t = h2d_end[(size_t)b];  // staging b free
         const double pk = in.p[v] / prate;
-        if (rec >= 0) pack_sum[rec] += pk;
-        t += pk;
+        if (rec == 0) pack_sum += pk;
+        first_chunk = t + std::min(in.p[v], in.chunk) / prate;
+        pack_end = t + pk;
       }
-      double hs = t > w_free ? t : w_free;
+      // the copy starts once the first chunk is packed, the weight stream is
+      // free and the buffer was released; it cannot end before the last chunk
+      // is packed and copied
+      double hs = first_chunk > w_free ? first_chunk : w_free;
       if (bf[(size_t)b] > hs) hs = bf[(size_t)b];
-      const double he = hs + in.b[v] / in.bw_h2d;
+      double he = hs + in.b[v] / in.bw_h2d;
+      if (in.p[v] > 0) he = std::max(he, pack_end + std::min(in.b[v], in.chunk) / in.bw_h2d);
       w_free = he;
       h2d_end[(size_t)b] = he;
-      drv = t;
+      drv = pack_end;
       const double cs = c_free > he ? c_free : he;
       // the period runs from step steps-2's first compute to step steps-1's
-      if ((rec == 0 && v > 0) || (rec == 1 && v == 0)) stall_sum[0] += cs - c_free;
+      if ((rec == 0 && v > 0) || (rec == 1 && v == 0)) stall_sum += cs - c_free;
       if (rec >= 0 && v == 0) first_c[rec] = cs;
       if (rec == 1 && stall_v) stall_v[v] = cs - c_free;
       const double ce = cs + in.c[v];
       c_free = ce;
       if (in.d[v] > 0) {
-        // a free slab: released at or before the driver gets here, else the
-        // earliest release of a held one (advancing Adam as needed)
+        // a free slab: one released by the time the driver gets here, else the
+        // earliest release of a held one (a held slab whose Adam is not decided
+        // yet ends after every decided one)
         int k = -1;
         for (;;) {
           double best_t = 1e300;
-          bool unknown = false;
           for (int q = 0; q < K; ++q) {
             const double r = release_of(q);
-            if (r < 0) { unknown = true; continue; }
-            if (r <= drv) { k = q; best_t = drv; break; }
-            if (r < best_t) { best_t = r; k = q; }
+            if (r < 0) continue;
+            if (r <= drv) {
+              k = q;
+              best_t = drv;
+              break;
+            }
+            if (r < best_t) {
+              best_t = r;
+              k = q;
+            }
           }
-          // a held slab whose Adam is not decided yet ends after every
-          // decided one, so the earliest known release is the answer
-          (void)unknown;
           if (k >= 0) {
             if (best_t > drv) {
-              if (rec >= 0) slab_sum[rec] += best_t - drv;
+              if (rec == 0) slab_sum += best_t - drv;
               drv = best_t;
             }
             break;
           }
-          if (!ad.next()) break;  // cannot happen: a held slab belongs to a queued job
+          if (!ad.next()) break;
         }
         if (k < 0) k = 0;
-        const double gs0 = ce > g_free ? ce : g_free;
-        const double gs = gs0 > drv ? gs0 : drv;
+        double gs = ce > g_free ? ce : g_free;
+        if (drv > gs) gs = drv;
         const double ge = gs + in.d[v] / in.bw_d2h;
         g_free = ge;
         bf[(size_t)b] = ge;
@@ -478,52 +469,62 @@ SimOut simulate(const SimIn& in, int32_t K, int32_t n_pack, int32_t steps, doubl
   }
   while (ad.next()) {
   }
-  // Adam work done inside the last period [first_c[0], first_c[1])
-  double abusy = 0;
+  double abusy = 0;  // Adam work inside the period [first_c[0], first_c[1])
   for (const SimJob& jb : ad.jobs) {
     const double a0 = jb.end - jb.elems / ad.rate, a1 = jb.end;
     const double lo = a0 > first_c[0] ? a0 : first_c[0], hi = a1 < first_c[1] ? a1 : first_c[1];
     if (hi > lo) abusy += hi - lo;
   }
   out.period = first_c[1] - first_c[0];
-  out.stall = stall_sum[0];
+  out.stall = stall_sum;
   out.adam_busy = abusy;
-  out.slab_wait = slab_sum[0];
-  out.pack = pack_sum[0];
+  out.slab_wait = slab_sum;
+  out.pack = pack_sum;
+  out.adam_rate = adam_rate;
   return out;
 }
+}  // namespace
 
-Plan plan(const SimIn& in, int32_t k_min, int32_t k_max, int32_t np_min, int32_t np_max) {
+SimOut simulate(const SimIn& in, int32_t K, int32_t steps, double* stall_v) {
+  if (in.n <= 0 || K < 1 || steps < 2 || !(in.bw_h2d > 0) || !(in.bw_d2h > 0)) return SimOut{};
+  double r = in.adam_rate;
+  SimOut o = simulate_at(in, K, steps, nullptr, r);
+  if (in.host_bw > 0 && in.adam_rate > 0) {
+    // host memory is shared: Adam gets what DMA and the pack leave of host_bw
+    double dma = 0, packed = 0;
+    for (int v = 0; v < in.n; ++v) {
+      dma += in.b[v] + in.d[v];
+      packed += 2.0 * in.p[v];
+    }
+    for (int it = 0; it < 20 && o.period > 0; ++it) {
+      const double left = in.host_bw - (dma + packed) / o.period;
+      const double floor_bw = 0.25 * in.host_bw;  // DMA and the pack are never the whole period
+      const double r2 = std::min(in.adam_rate, std::max(left, floor_bw) / in.adam_bytes);
+      if (std::fabs(r2 - r) <= 1e-3 * r) break;
+      r = r2;
+      o = simulate_at(in, K, steps, nullptr, r);
+    }
+  }
+  if (stall_v) o = simulate_at(in, K, steps, stall_v, r);
+  return o;
+}
+
+Plan plan(const SimIn& in, int32_t k_min, int32_t k_max) {
   Plan best;
   if (k_min < 1) k_min = 1;
   if (k_max < k_min) k_max = k_min;
-  bool packs = false;
-  for (int v = 0; v < in.n; ++v) packs = packs || in.p[v] > 0;
-  if (!packs) np_min = np_max = 0;
-  if (packs && np_min < 1) np_min = 1;
-  if (np_max < np_min) np_max = np_min;
-  struct Cand {
-    int K, np;
-    SimOut o;
-  };
-  std::vector<Cand> all;
+  std::vector<SimOut> all;
   double tmin = 1e300;
-  for (int np = np_min; np <= np_max; ++np)
-    for (int K = k_min; K <= k_max; ++K) {
-      const SimOut o = simulate(in, K, np, 4, nullptr);
-      all.push_back({K, np, o});
-      if (o.period < tmin) tmin = o.period;
-    }
-  bool have = false;
-  for (const Cand& c : all) {
-    if (c.o.period > tmin * 1.005) continue;
-    if (!have || c.K < best.K || (c.K == best.K && c.np < best.n_pack)) {
-      best.K = c.K;
-      best.n_pack = c.np;
-      best.out = c.o;
-      have = true;
-    }
+  for (int K = k_min; K <= k_max; ++K) {
+    all.push_back(simulate(in, K, 4, nullptr));
+    tmin = std::min(tmin, all.back().period);
   }
+  for (int K = k_min; K <= k_max; ++K)
+    if (all[(size_t)(K - k_min)].period <= tmin * 1.005) {
+      best.K = K;
+      best.out = all[(size_t)(K - k_min)];
+      break;
+    }
   return best;
 }
 

@@ -72,7 +72,9 @@ class Pool {
   void stop();
   int size() const { return (int)threads_.size(); }
   // fn(i) for i in [0, n); returns false if any call threw (message in *err).
-  bool parallel_for(int64_t n, const std::function<void(int64_t)>& fn, std::string* err);
+  // urgent: the n tasks go ahead of every queued task (in order), so a worker
+  // takes them as soon as it finishes the task it is running.
+  bool parallel_for(int64_t n, const std::function<void(int64_t)>& fn, std::string* err, bool urgent = false);
 
  private:
   // Completion count of one parallel_for, on the caller's stack.  Every
@@ -91,7 +93,7 @@ class Pool {
     int64_t i;
     Latch* latch;
   };
-  bool run_one();
+  bool run_own(const Latch* latch);
   void run(Task& t);
   std::vector<std::thread> threads_;
   std::mutex mu_;
@@ -118,11 +120,12 @@ struct SimIn {
   const double* c = nullptr;       // compute seconds
   const double* a = nullptr;       // Adam elements of the exported block
   int32_t nbuf = 2;                // device buffers (= pinned staging buffers)
-  double bw_h2d = 0, bw_d2h = 0;   // bytes/s
-  double pack_rate1 = 0;           // bytes/s one packing thread copies
-  double adam_rate1 = 0;           // Adam elements/s of one thread and the asymptote of
-  double adam_rate_max = 0;        // r(n) = r_max (1 - exp(-n r1 / r_max)) (host memory bound)
-  int32_t threads = 1;             // host threads shared by packing and Adam
+  double bw_h2d = 0, bw_d2h = 0;   // link bytes/s per direction
+  double pack_rate = 0;            // bytes/s the worker pool packs (0: instant)
+  double adam_rate = 0;            // Adam elements/s of the worker pool on an idle host (0: instant)
+  double adam_bytes = 28;          // host memory bytes Adam moves per element
+  double host_bw = 0;              // bytes/s host memory serves CPU and DMA together (0: unlimited)
+  double chunk = 64.0 * (1 << 20); // bytes per packed chunk (its copy starts once it is packed)
 };
 struct SimOut {
   double period = 0;      // seconds between the starts of two steps' first computes
@@ -130,22 +133,20 @@ struct SimOut {
   double adam_busy = 0;   // seconds host Adam works within it
   double slab_wait = 0;   // seconds the driver waits for a free slab within it
   double pack = 0;        // seconds of packing on the driver's path within it
+  double adam_rate = 0;   // Adam elements/s after the share DMA and packing take
 };
-// Simulates `steps` consecutive steps with K slabs and n_pack packing threads
-// (the rest run Adam) and reports the last step; stall_v (n entries, may be
-// null) receives the compute stream's wait before each visit of that step.
-SimOut simulate(const SimIn& in, int32_t K, int32_t n_pack, int32_t steps, double* stall_v);
-// Adam elements/s of n threads under the saturating model, and the asymptote
-// r_max for which the model gives rn at n threads when one thread gives r1.
-double adam_rate(const SimIn& in, int n);
-double adam_asymptote(double r1, double rn, int n);
-// Chooses K in [k_min, k_max] and the packing threads in [np_min, np_max]
-// (0 without packing): the shortest simulated period, then the fewest slabs
-// and packing threads within 0.5 % of it.
+// Simulates `steps` consecutive steps with K slabs and reports the last one;
+// stall_v (n entries, may be null) receives the compute stream's wait before
+// each visit of that step.  Adam's rate is the smaller of adam_rate and what
+// host_bw leaves after the period's average DMA and pack traffic, found by
+// fixed-point iteration over the period.
+SimOut simulate(const SimIn& in, int32_t K, int32_t steps, double* stall_v);
+// Chooses K in [k_min, k_max]: the shortest simulated period, then the
+// fewest slabs within 0.5 % of it.
 struct Plan {
-  int32_t K = 1, n_pack = 0;
+  int32_t K = 1;
   SimOut out;
 };
-Plan plan(const SimIn& in, int32_t k_min, int32_t k_max, int32_t np_min, int32_t np_max);
+Plan plan(const SimIn& in, int32_t k_min, int32_t k_max);
 
 }  // namespace mth

@@ -212,11 +212,11 @@ struct mt_model {
   cudaEvent_t WR[2] = {}, BD[2] = {}, BF[2] = {}, XR[2] = {}, XS[2] = {}, TOK = nullptr, LOSS = nullptr;
   cudaEvent_t RT = nullptr, ER[2] = {};  // MoE: Route-Ready (counts on the host), Experts-Ready[b]
   std::vector<cudaEvent_t> SR;
-  // host workers: Adam (and initialisation) on `pool`; the just-in-time pack
-  // on `pack_pool`, whose work the driver thread shares, so that a pack never
-  // queues behind Adam's chunks
-  mth::Pool pool, pack_pool;
-  int n_pack = 0, n_pack_active = 0;
+  // host workers: Adam, initialisation and the just-in-time pack share
+  // `pool`; the pack's pieces go ahead of Adam's queued chunks (and the
+  // driver thread copies them too), so a pack waits at most for the chunks
+  // already running
+  mth::Pool pool;
   // static schedule: per-visit inputs of one pass, the plans made at init
   // (compute estimated) and after the first step (compute measured)
   std::vector<int32_t> sk_kind, sk_block;
@@ -225,6 +225,7 @@ struct mt_model {
   mt_sched_plan plan0{}, plan1{};
   bool have_plan1 = false;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> first_ev;  // compute of each visit of the first step
+  std::vector<char> first_rec;                                // ... and whether it was recorded
   std::thread adam_thr;
   std::mutex amu;
   std::condition_variable acv;
@@ -891,7 +892,9 @@ void adam_loop(mt_model* m) {
       // work items: (tensor, chunk) ranges of at most 1 Mi elements; in an MoE
       // block each expert's row is its own range, and an expert no token was
       // routed to takes a zero gradient (its slab range was not exported)
-      constexpr int64_t CH = 1 << 20;
+      // 256 Ki-element chunks: a pack queued ahead of them waits at most for
+      // the chunks already running (about 0.5 ms each)
+      constexpr int64_t CH = 1 << 18;
       struct Item {
         int64_t o, n;
         bool zero;
@@ -1030,26 +1033,38 @@ std::vector<Range> block_ranges(const mt_model* m, int j, bool trunk, bool exper
   return r;
 }
 
-// Host copy of the given ranges of src into dst (the just-in-time pack into
-// pinned staging): 8 MiB pieces split into n_pack_active contiguous shares,
-// copied by the packing threads and the driver thread.
-mt_status pack_ranges(mt_model* m, uint8_t* dst, const uint8_t* src, const std::vector<Range>& rg) {
-  const double t0 = now_ms();
-  constexpr int64_t CH = 8 << 20;
-  std::vector<Range> pieces;
+constexpr int64_t kPackChunk = (int64_t)64 << 20;  // bytes packed before their copy is enqueued
+
+// Host-to-device copy of the given ranges of block j's W region into device
+// buffer b on the weight stream.  With the just-in-time pack (src pageable)
+// each 64 MiB chunk is first copied into pinned staging b -- in 8 MiB pieces
+// on the worker pool, ahead of any queued Adam work, with the driver thread
+// copying too -- and its device copy is enqueued as soon as it is packed, so
+// the pack of a chunk overlaps the transfer of the previous one.
+mt_status copy_ranges(mt_model* m, int b, const uint8_t* src, const std::vector<Range>& rg, bool pack) {
+  constexpr int64_t PIECE = (int64_t)8 << 20;
+  uint8_t* stage = m->staging[b];
   for (const Range& r : rg)
-    for (int64_t o = 0; o < r.bytes; o += CH) pieces.push_back({r.off + o, std::min(CH, r.bytes - o)});
-  const int64_t np = (int64_t)pieces.size();
-  const int64_t nt = std::max<int64_t>(1, std::min<int64_t>(m->n_pack_active, np));
-  std::function<void(int64_t)> fn = [&](int64_t t) {
-    for (int64_t i = t * np / nt; i < (t + 1) * np / nt; ++i) {
-      const Range& q = pieces[(size_t)i];
-      std::memcpy(dst + q.off, src + q.off, (size_t)q.bytes);
+    for (int64_t c0 = 0; c0 < r.bytes;) {
+      const int64_t chunk = pack ? kPackChunk : r.bytes;  // a pinned store copies each range at once
+      const int64_t off = r.off + c0, len = std::min(chunk, r.bytes - c0);
+      c0 += len;
+      const uint8_t* from = src + off;
+      if (pack) {
+        const double t0 = now_ms();
+        const int64_t np = (len + PIECE - 1) / PIECE;
+        std::function<void(int64_t)> fn = [&](int64_t i) {
+          const int64_t o = off + i * PIECE;
+          std::memcpy(stage + o, src + o, (size_t)std::min(PIECE, off + len - o));
+        };
+        std::string werr;
+        if (!m->pool.parallel_for(np, fn, &werr, true)) return set_err(m, MT_ERR_INTERNAL, "pack: " + werr);
+        m->pack_ms += now_ms() - t0;
+        from = stage + off;
+      }
+      CU(m, cudaMemcpyAsync(m->d.buf[b] + off, from, (size_t)len, cudaMemcpyHostToDevice, m->sw));
+      m->h2d += len;
     }
-  };
-  std::string werr;
-  if (!m->pack_pool.parallel_for(nt, fn, &werr)) return set_err(m, MT_ERR_INTERNAL, "pack: " + werr);
-  m->pack_ms += now_ms() - t0;
   return MT_OK;
 }
 
@@ -1067,28 +1082,23 @@ mt_status do_stream_in(mt_model* m, int j, int b) {
   // experts once the router has chosen; recompute and backward visits know
   // the forward's routing and copy both
   const std::vector<Range> rg = m->live ? block_ranges(m, j, true, !fwd) : std::vector<Range>{};
-  if (copies && !m->c.pin_store) {
+  const bool pack = copies && !m->c.pin_store;
+  if (pack) {
     if (m->used[b]) {
       logop(m, "H", "WAIT_STAGE", b, -1);
       if (m->live) OK(wait_event(m, m->WR[b], "staging free"));
       if (m->live && m->moe) OK(wait_event(m, m->ER[b], "staging free (experts)"));
     }
+    // the pack itself runs chunk by chunk inside the copy below (each chunk
+    // packed before its device copy is enqueued)
     logop(m, "H", "PACK", j, b);
-    if (m->live) {
-      OK(pack_ranges(m, m->staging[b], src, rg));
-      src = m->staging[b];
-    }
   }
   logop(m, "W", "WAIT_BF", b, -1);
   if (m->live) CU(m, cudaStreamWaitEvent(m->sw, m->BF[b], 0));
   std::unique_ptr<TraceSpan> trace_in(new TraceSpan(m, m->sw, 'W', TR_H2D, j));
   if (copies) {
     logop(m, "W", "H2D", j, b);
-    if (m->live)
-      for (const Range& r : rg) {
-        CU(m, cudaMemcpyAsync(m->d.buf[b] + r.off, src + r.off, (size_t)r.bytes, cudaMemcpyHostToDevice, m->sw));
-        m->h2d += r.bytes;
-      }
+    if (m->live) OK(copy_ranges(m, b, src, rg, pack));
   }
   if (vd.first && m->c.ckpt_on_host) {
     // The segment's checkpoint X_s (s = j - 1) into slot seg % 2, after the
@@ -1153,20 +1163,11 @@ mt_status moe_forward_visit(mt_model* m, int j, int b) {
   const mth::BlockDesc& bd = m->lay[(size_t)j];
   const std::vector<Range> rg = m->live ? block_ranges(m, j, false, true) : std::vector<Range>{};
   const uint8_t* src = m->live ? m->store + bd.store_off + bd.region[0] : nullptr;
-  if (!m->c.pin_store) {
-    logop(m, "H", "PACK_EXP", j, b);
-    if (m->live) {
-      OK(pack_ranges(m, m->staging[b], src, rg));
-      src = m->staging[b];
-    }
-  }
+  if (!m->c.pin_store) logop(m, "H", "PACK_EXP", j, b);  // packed chunk by chunk in the copy below
   logop(m, "W", "H2D_EXP", j, b);
   if (m->live) {
     TraceSpan trace_exp(m, m->sw, 'W', TR_H2D_EXP, j);
-    for (const Range& r : rg) {
-      CU(m, cudaMemcpyAsync(m->d.buf[b] + r.off, src + r.off, (size_t)r.bytes, cudaMemcpyHostToDevice, m->sw));
-      m->h2d += r.bytes;
-    }
+    OK(copy_ranges(m, b, src, rg, !m->c.pin_store));
   }
   logop(m, "W", "REC_ER", b, -1);
   if (m->live) CU(m, cudaEventRecord(m->ER[b], m->sw));
@@ -1358,7 +1359,10 @@ mt_status run_visit(mt_model* m) {
   if (kind <= V_HEAD) OK(do_forward(m, j, b));
   else if (kind == V_RECOMP) OK(do_recompute(m, j, b));
   else OK(do_backward(m, j, b));
-  if (first) CU(m, cudaEventRecord(m->first_ev[(size_t)v].second, m->sc));
+  if (first) {
+    CU(m, cudaEventRecord(m->first_ev[(size_t)v].second, m->sc));
+    m->first_rec[(size_t)v] = 1;
+  }
   if (ta) {
     cudaEvent_t tb = take_event(m);
     CU(m, cudaEventRecord(tb, m->sc));
@@ -1464,128 +1468,163 @@ void sched_inputs(mt_model* m) {
   in.c = m->sk_c.data();
   in.a = m->sk_a.data();
   in.nbuf = m->nbuf;
+  in.chunk = (double)kPackChunk;
 }
 
 void fill_plan_out(const mth::Plan& pl, const mth::SimIn& in, int measured, mt_sched_plan* o) {
   o->K = pl.K;
-  o->n_pack = pl.n_pack;
   o->measured = measured;
   o->period_ms = pl.out.period * 1e3;
   o->stall_ms = pl.out.stall * 1e3;
   o->adam_busy_ms = pl.out.adam_busy * 1e3;
   o->slab_wait_ms = pl.out.slab_wait * 1e3;
   o->pack_ms = pl.out.pack * 1e3;
+  o->adam_gelem_s = pl.out.adam_rate / 1e9;
   o->bw_h2d_gbs = in.bw_h2d / 1e9;
   o->bw_d2h_gbs = in.bw_d2h / 1e9;
-  o->pack_gbs_thread = in.pack_rate1 / 1e9;
-  o->adam_gelem_s_thread = in.adam_rate1 / 1e9;
-  o->adam_gelem_s_max = in.adam_rate_max / 1e9;
+  o->pack_gbs = in.pack_rate / 1e9;
+  o->adam_gelem_s_idle = in.adam_rate / 1e9;
+  o->host_gbs = in.host_bw / 1e9;
 }
 
 // Init-time measurements for the schedule: pinned copies over the link in
-// each direction (best of three), a one-thread copy from the pageable store
-// into pinned memory (the pack), and host Adam on scratch arrays with one
-// thread and with the whole pool.  A failed probe leaves its rate at 0 (the
-// model then treats that stage as free).
-void run_probes(mt_model* m, int nth) {
+// each direction on the model's streams (best of three), the pool's pack rate
+// (pageable store into pinned memory), host Adam on scratch arrays over the
+// pool on an idle host, and the same Adam while both link directions copy,
+// which gives the bytes host memory serves to CPU and DMA together.  A failed
+// probe leaves its rate at 0 (the model then treats that stage as free).
+void run_probes(mt_model* m) {
   mth::SimIn& in = m->sim;
+  in.adam_bytes = m->c.keep_host_grad ? 30.0 : 28.0;
   const size_t bytes = (size_t)std::min<int64_t>((int64_t)64 << 20, m->wb_max);
   void* hp = nullptr;
-  if (cudaHostAlloc(&hp, bytes, cudaHostAllocDefault) == cudaSuccess) {
-    cudaEvent_t e0 = nullptr, e1 = nullptr;
-    if (cudaEventCreate(&e0) == cudaSuccess && cudaEventCreate(&e1) == cudaSuccess) {
-      for (int dir = 0; dir < 2; ++dir) {
-        cudaStream_t st = dir == 0 ? m->sw : m->sg;
-        float best = 1e30f;
-        for (int r = 0; r < 3; ++r) {
-          cudaEventRecord(e0, st);
-          if (dir == 0) cudaMemcpyAsync(m->d.buf[0], hp, bytes, cudaMemcpyHostToDevice, st);
-          else cudaMemcpyAsync(hp, m->d.buf[0], bytes, cudaMemcpyDeviceToHost, st);
-          cudaEventRecord(e1, st);
-          float ms = 0;
-          if (cudaEventSynchronize(e1) == cudaSuccess && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess && ms > 0)
-            best = std::min(best, ms);
-        }
-        if (best < 1e30f) (dir == 0 ? in.bw_h2d : in.bw_d2h) = (double)bytes / (best * 1e-3);
-      }
-    }
-    if (e0) cudaEventDestroy(e0);
-    if (e1) cudaEventDestroy(e1);
-    const mth::BlockDesc* big = &m->lay[0];
-    for (auto& b : m->lay)
-      if (b.wbytes > big->wbytes) big = &b;
-    const size_t pb = std::min<size_t>(bytes, (size_t)big->wbytes);
-    double best = 1e30;
-    for (int r = 0; r < 2; ++r) {
-      const double t0 = now_ms();
-      std::memcpy(hp, m->store + big->store_off, pb);
-      best = std::min(best, now_ms() - t0);
-    }
-    if (best > 0) in.pack_rate1 = (double)pb / (best * 1e-3);
-    cudaFreeHost(hp);
+  if (cudaHostAlloc(&hp, bytes, cudaHostAllocDefault) != cudaSuccess) {
+    cudaGetLastError();
+    return;
   }
-  // Adam: 2 Mi elements on one thread, 8 Mi elements over the pool
-  const int64_t n1 = (int64_t)2 << 20, nn = (int64_t)8 << 20;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (cudaEventCreate(&e0) == cudaSuccess && cudaEventCreate(&e1) == cudaSuccess) {
+    for (int dir = 0; dir < 2; ++dir) {
+      cudaStream_t st = dir == 0 ? m->sw : m->sg;
+      float best = 1e30f;
+      for (int r = 0; r < 3; ++r) {
+        cudaEventRecord(e0, st);
+        if (dir == 0) cudaMemcpyAsync(m->d.buf[0], hp, bytes, cudaMemcpyHostToDevice, st);
+        else cudaMemcpyAsync(hp, m->d.buf[0], bytes, cudaMemcpyDeviceToHost, st);
+        cudaEventRecord(e1, st);
+        float ms = 0;
+        if (cudaEventSynchronize(e1) == cudaSuccess && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess && ms > 0)
+          best = std::min(best, ms);
+      }
+      if (best < 1e30f) (dir == 0 ? in.bw_h2d : in.bw_d2h) = (double)bytes / (best * 1e-3);
+    }
+  }
+  // the pack: the largest block's first `bytes` of W, in 8 MiB pieces over the pool
+  const mth::BlockDesc* big = &m->lay[0];
+  for (auto& b : m->lay)
+    if (b.wbytes > big->wbytes) big = &b;
+  const int64_t pb = std::min<int64_t>((int64_t)bytes, big->wbytes), PIECE = (int64_t)8 << 20;
+  const uint8_t* src = m->store + big->store_off;
+  std::function<void(int64_t)> cp = [&](int64_t i) {
+    const int64_t o = i * PIECE;
+    std::memcpy((uint8_t*)hp + o, src + o, (size_t)std::min(PIECE, pb - o));
+  };
+  double best = 1e30;
+  std::string err;
+  for (int r = 0; r < 3; ++r) {
+    const double t0 = now_ms();
+    if (m->pool.parallel_for((pb + PIECE - 1) / PIECE, cp, &err, true)) best = std::min(best, now_ms() - t0);
+  }
+  if (best > 0 && best < 1e30) in.pack_rate = (double)pb / (best * 1e-3);
+  // Adam over the pool: 16 Mi elements, on an idle host and under DMA in both directions
+  const int64_t nn = (int64_t)16 << 20;
   std::vector<float> th((size_t)nn, 0.01f), mm((size_t)nn, 0.0f), vv((size_t)nn, 0.0f);
   std::vector<uint16_t> g((size_t)nn, 0x3c00), w((size_t)nn, 0), gc(m->c.keep_host_grad ? (size_t)nn : 0, 0);
   uint16_t* gcp = m->c.keep_host_grad ? gc.data() : nullptr;
-  double best1 = 1e30, bestn = 1e30;
-  for (int r = 0; r < 2; ++r) {
-    double t0 = now_ms();
-    mth::adam(n1, g.data(), gcp, th.data(), mm.data(), vv.data(), w.data(), r + 1, 1e-3f, 0.9f, 0.999f, 1e-8f, 0.f);
-    best1 = std::min(best1, now_ms() - t0);
-    constexpr int64_t CH = 1 << 18;
-    std::function<void(int64_t)> fn = [&](int64_t i) {
-      const int64_t o = i * CH, len = std::min(CH, nn - o);
-      mth::adam(len, g.data() + o, gcp ? gcp + o : nullptr, th.data() + o, mm.data() + o, vv.data() + o,
-                w.data() + o, r + 1, 1e-3f, 0.9f, 0.999f, 1e-8f, 0.f);
-    };
-    std::string err;
-    t0 = now_ms();
-    if (m->pool.parallel_for((nn + CH - 1) / CH, fn, &err)) bestn = std::min(bestn, now_ms() - t0);
+  constexpr int64_t CH = 1 << 18;
+  int rep = 0;
+  std::function<void(int64_t)> fn = [&](int64_t i) {
+    const int64_t o = i * CH, len = std::min(CH, nn - o);
+    mth::adam(len, g.data() + o, gcp ? gcp + o : nullptr, th.data() + o, mm.data() + o, vv.data() + o,
+              w.data() + o, rep + 1, 1e-3f, 0.9f, 0.999f, 1e-8f, 0.f);
+  };
+  double idle = 1e30;
+  for (rep = 0; rep < 3; ++rep) {
+    const double t0 = now_ms();
+    if (m->pool.parallel_for((nn + CH - 1) / CH, fn, &err)) idle = std::min(idle, now_ms() - t0);
   }
-  if (best1 > 0 && best1 < 1e30) in.adam_rate1 = (double)n1 / (best1 * 1e-3);
-  const double rn = bestn > 0 && bestn < 1e30 ? (double)nn / (bestn * 1e-3) : 0.0;
-  in.adam_rate_max = mth::adam_asymptote(in.adam_rate1, rn, nth);
-  in.threads = nth;
+  if (idle > 0 && idle < 1e30) in.adam_rate = (double)nn / (idle * 1e-3);
+  // shared host memory: copies in both link directions (about half as long as
+  // the Adam run, starting with it) while Adam makes four passes; Adam's bytes
+  // inside the copies' window are its total minus the idle-rate part after
+  // the copies ended
+  cudaEvent_t f0 = nullptr, f1 = nullptr;
+  if (e0 && e1 && in.adam_rate > 0 && in.bw_h2d > 0 && in.bw_d2h > 0 && cudaEventCreate(&f0) == cudaSuccess &&
+      cudaEventCreate(&f1) == cudaSuccess) {
+    const int passes = 4;
+    const double t_idle = passes * (double)nn / in.adam_rate;
+    const size_t half = bytes / 2;  // H2D from the first half of the buffer, D2H into the second
+    const int nc = std::max(2, (int)std::ceil(0.5 * t_idle * std::min(in.bw_h2d, in.bw_d2h) / (double)half));
+    cudaEventRecord(e0, m->sw);
+    cudaEventRecord(f0, m->sg);
+    for (int i = 0; i < nc; ++i) {
+      cudaMemcpyAsync(m->d.buf[0], hp, half, cudaMemcpyHostToDevice, m->sw);
+      cudaMemcpyAsync((uint8_t*)hp + half, m->d.buf[0] + half, half, cudaMemcpyDeviceToHost, m->sg);
+    }
+    cudaEventRecord(e1, m->sw);
+    cudaEventRecord(f1, m->sg);
+    const double t0 = now_ms();
+    bool ok = true;
+    for (rep = 3; rep < 3 + passes && ok; ++rep) ok = m->pool.parallel_for((nn + CH - 1) / CH, fn, &err);
+    const double ta = (now_ms() - t0) * 1e-3;
+    float mw = 0, mg = 0;
+    if (ok && cudaEventSynchronize(e1) == cudaSuccess && cudaEventSynchronize(f1) == cudaSuccess &&
+        cudaEventElapsedTime(&mw, e0, e1) == cudaSuccess && cudaEventElapsedTime(&mg, f0, f1) == cudaSuccess) {
+      const double td = std::max(mw, mg) * 1e-3;
+      if (td > 0 && td < ta) {
+        const double adam_in = in.adam_bytes * ((double)passes * nn - in.adam_rate * (ta - td));
+        if (adam_in > 0) in.host_bw = (2.0 * nc * (double)half + adam_in) / td;
+      }
+    }
+  }
+  if (f0) cudaEventDestroy(f0);
+  if (f1) cudaEventDestroy(f1);
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  cudaFreeHost(hp);
+  cudaGetLastError();  // a failed probe call must not surface at a later launch
 }
 
-// The plan with the knobs the config leaves open (K when n_grad_slabs = 0,
-// packing threads when n_pack_threads = 0 and the store is not pinned).
-mth::Plan make_plan(const mt_model* m, int k_max_budget, int np_fixed) {
-  const mt_config& c = m->c;
-  const int kmin = c.n_grad_slabs > 0 ? c.n_grad_slabs : 1;
-  const int kmax = c.n_grad_slabs > 0 ? c.n_grad_slabs : k_max_budget;
-  int npmin = 1, npmax = std::max(1, m->sim.threads / 3);
-  if (np_fixed > 0) npmin = npmax = np_fixed;
-  return mth::plan(m->sim, kmin, kmax, npmin, npmax);
+// The plan with the slab count the config leaves open (n_grad_slabs = 0).
+mth::Plan make_plan(const mt_model* m, int k_max_budget) {
+  const int k = m->c.n_grad_slabs;
+  return mth::plan(m->sim, k > 0 ? k : 1, k > 0 ? k : k_max_budget);
 }
 
 // Once the first step's per-visit compute events have completed: the second
-// plan, on measured compute times, which sets how many packing threads work.
+// plan, on measured compute times (K itself is allocated already).
 void replan_measured(mt_model* m) {
   if (m->have_plan1 || m->first_ev.empty() || m->npass != 1) return;
+  for (size_t v = 0; v < m->first_ev.size(); ++v)
+    if (!m->first_rec[v]) return;  // the first step did not run through mt_train_step
   std::vector<double> c(m->first_ev.size());
   for (size_t v = 0; v < m->first_ev.size(); ++v) {
-    if (cudaEventQuery(m->first_ev[v].second) != cudaSuccess) return;
+    if (cudaEventQuery(m->first_ev[v].second) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
     float ms = 0;
-    if (cudaEventElapsedTime(&ms, m->first_ev[v].first, m->first_ev[v].second) != cudaSuccess) return;
+    if (cudaEventElapsedTime(&ms, m->first_ev[v].first, m->first_ev[v].second) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
     c[v] = ms * 1e-3;
   }
   m->sk_c = c;
   m->sim.c = m->sk_c.data();
-  // K is allocated already; the packing threads can only shrink
-  mth::SimIn in = m->sim;
   mth::Plan pl;
-  const int kfix = m->K;
-  if (m->c.pin_store || m->c.n_pack_threads > 0) {
-    pl.K = kfix;
-    pl.n_pack = m->n_pack;
-    pl.out = mth::simulate(in, kfix, m->n_pack, 4, nullptr);
-  } else {
-    pl = mth::plan(in, kfix, kfix, 1, std::max(1, m->n_pack));
-    m->n_pack_active = pl.n_pack;
-  }
+  pl.K = m->K;
+  pl.out = mth::simulate(m->sim, m->K, 4, nullptr);
   fill_plan_out(pl, m->sim, 1, &m->plan1);
   m->have_plan1 = true;
 }
@@ -1600,7 +1639,6 @@ mt_model::~mt_model() {
   acv.notify_all();
   if (adam_thr.joinable()) adam_thr.join();
   pool.stop();
-  pack_pool.stop();
   if (live) {
     if (sc) cudaStreamSynchronize(sc);
     if (sw) cudaStreamSynchronize(sw);
@@ -1733,24 +1771,18 @@ mt_status mt_init_model(const mt_config* c, mt_dev_region dev, mt_streams s, mt_
   // FLOPs; it sizes the slab pool (n_grad_slabs = 0) within a tenth of the
   // host's memory and splits the host threads between packing and Adam.
   sched_inputs(m.get());
-  run_probes(m.get(), nth);
+  run_probes(m.get());
   {
     const long pages = sysconf(_SC_PHYS_PAGES), psz = sysconf(_SC_PAGESIZE);
     const double phys = pages > 0 && psz > 0 ? (double)pages * (double)psz : 64e9;
     const int kbud = (int)std::max(2.0, std::min(32.0, std::floor(0.1 * phys / (double)m->wb_max)));
-    const mth::Plan pl = make_plan(m.get(), kbud, c->n_pack_threads);
+    const mth::Plan pl = make_plan(m.get(), kbud);
     m->K = c->n_grad_slabs > 0 ? c->n_grad_slabs : pl.K;
-    m->n_pack = c->pin_store ? 0 : (c->n_pack_threads > 0 ? c->n_pack_threads : std::max(1, pl.n_pack));
-    m->n_pack_active = m->n_pack;
     fill_plan_out(pl, m->sim, 0, &m->plan0);
-    if (m->n_pack > 0) {  // the packing threads (the driver is one of them) leave the Adam pool
-      m->pool.stop();
-      m->pool.start(std::max(1, nth - m->n_pack));
-      m->pack_pool.start(m->n_pack - 1);
-    }
   }
   if (m->npass == 1) {
     m->first_ev.assign((size_t)nvisits(m.get()), {nullptr, nullptr});
+    m->first_rec.assign((size_t)nvisits(m.get()), 0);
     for (auto& e : m->first_ev) {
       CU(mm, cudaEventCreate(&e.first));
       CU(mm, cudaEventCreate(&e.second));
@@ -2215,7 +2247,7 @@ int32_t mt_schedule(int32_t n, const double* b, const double* d, const double* c
 
 static bool sim_in(const mt_sched_in* s, mth::SimIn* o) {
   if (!s || s->n_visits < 1 || !s->kind || !s->block || !s->b || !s->p || !s->d || !s->c || !s->a) return false;
-  if (!(s->bw_h2d > 0) || !(s->bw_d2h > 0) || s->n_buffers < 1 || s->threads < 1) return false;
+  if (!(s->bw_h2d > 0) || !(s->bw_d2h > 0) || s->n_buffers < 1) return false;
   for (int v = 0; v < s->n_visits; ++v)
     if (s->block[v] < 0 || s->kind[v] < 0 || s->kind[v] > 3) return false;
   o->n = s->n_visits;
@@ -2229,21 +2261,20 @@ static bool sim_in(const mt_sched_in* s, mth::SimIn* o) {
   o->nbuf = s->n_buffers;
   o->bw_h2d = s->bw_h2d;
   o->bw_d2h = s->bw_d2h;
-  o->pack_rate1 = s->pack_rate1;
-  o->adam_rate1 = s->adam_rate1;
-  o->adam_rate_max = s->adam_rate_max;
-  o->threads = s->threads;
+  o->pack_rate = s->pack_rate;
+  o->adam_rate = s->adam_rate;
+  o->adam_bytes = s->adam_bytes > 0 ? s->adam_bytes : 28.0;
+  o->host_bw = s->host_bw;
+  o->chunk = (double)kPackChunk;
   return true;
 }
 
-mt_status mt_schedule_simulate(const mt_sched_in* in, int32_t K, int32_t n_pack, mt_sched_plan* out,
-                               double* stall_v) {
+mt_status mt_schedule_simulate(const mt_sched_in* in, int32_t K, mt_sched_plan* out, double* stall_v) {
   mth::SimIn si;
-  if (!out || K < 1 || n_pack < 0 || !sim_in(in, &si)) return MT_ERR_ARG;
+  if (!out || K < 1 || !sim_in(in, &si)) return MT_ERR_ARG;
   mth::Plan pl;
   pl.K = K;
-  pl.n_pack = n_pack;
-  pl.out = mth::simulate(si, K, n_pack, 4, stall_v);
+  pl.out = mth::simulate(si, K, 4, stall_v);
   std::memset(out, 0, sizeof *out);
   fill_plan_out(pl, si, 0, out);
   return MT_OK;
@@ -2252,7 +2283,7 @@ mt_status mt_schedule_simulate(const mt_sched_in* in, int32_t K, int32_t n_pack,
 mt_status mt_schedule_plan(const mt_sched_in* in, int32_t k_max, mt_sched_plan* out) {
   mth::SimIn si;
   if (!out || k_max < 1 || !sim_in(in, &si)) return MT_ERR_ARG;
-  const mth::Plan pl = mth::plan(si, 1, k_max, 1, std::max(1, si.threads / 3));
+  const mth::Plan pl = mth::plan(si, 1, k_max);
   std::memset(out, 0, sizeof *out);
   fill_plan_out(pl, si, 0, out);
   return MT_OK;

@@ -8,6 +8,7 @@ python -m host_memory_centric_gb300.kbench attn_bwd --S 2048 --nseq 4 --nh 16 --
 python -m host_memory_centric_gb300.kbench rmsnorm_bwd --T 8192 --H 2048
 python -m host_memory_centric_gb300.kbench cross_entropy --T 8192 --V 32000
 python -m host_memory_centric_gb300.kbench moe_ffn --T 16384 --H 2880 --E 32 --k 4 --Fe 2880
+python -m host_memory_centric_gb300.kbench layer_gemms --config 7.6b
 """
 from __future__ import annotations
 
@@ -52,6 +53,7 @@ def main():
     ap.add_argument("--E", type=int, default=32)
     ap.add_argument("--k", type=int, default=4)
     ap.add_argument("--Fe", type=int, default=2880)
+    ap.add_argument("--config", default="7.6b")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     a = ap.parse_args()
@@ -145,6 +147,63 @@ def main():
         ms = timeit(run, a.iters, a.warmup)
         fl = 2.0 * T * k * 3 * H * Fe * 3 + 2.0 * T * E * H * 3  # experts fwd + dgrad + wgrad, router x3
         res.update(shape=dict(T=T, H=H, E=E, k=k, Fe=Fe), ms=ms, tflops=fl / ms / 1e9)
+    elif a.op == "layer_gemms":
+        # the GEMM launches of one decoder layer's forward and backward visits
+        # and of the LM head, in the forms and order the runtime issues them:
+        # forward qkv, o (+residual), gate/up, down (+residual); the backward's
+        # recompute of qkv, o, gate/up; then one launch per projection pairing
+        # its weight and input gradients (down, gate/up, o, qkv); the head's
+        # logits and its pair.  Each form is timed; launches per step = L per
+        # layer form, 1 per head form.
+        from . import configs
+        c = configs.get(a.config)
+        T = c["micro"] * c["batch"] * c["seq"]
+        H, F, V = c["hidden"], c["ffn"], c["vocab"]
+        nqkv, nhd = (c["n_heads"] + 2 * c["n_kv_heads"]) * c["head_dim"], c["n_heads"] * c["head_dim"]
+        r = lambda *sh: (torch.randn(*sh) * 0.05).to(bf).to(dev)
+        X = r(T, max(H, nhd, F))
+        Wq, Wo, Wgu, Wd = r(nqkv, H), r(H, nhd), r(2 * F, H), r(H, F)
+        Yq, Yo, Ygu, Yd = (torch.empty(T, n, dtype=bf, device=dev) for n in (nqkv, H, 2 * F, H))
+        dWq, dWo, dWgu, dWd = (torch.empty_like(w) for w in (Wq, Wo, Wgu, Wd))
+        dXa = torch.empty(T, max(H, F), dtype=bf, device=dev)
+
+        def fprop(Xin, W, N, K, Y, R=None):
+            return lambda: ops.gemm(Xin, W, T, N, K, lda=X.shape[1], D=Y, R=R)
+
+        def pair(dY, Xin, W, N, K, dW):  # dW = dY^T X, dX = dY W
+            sw = dict(A=dY, B=Xin, M=N, N=K, K=T, a_mn=1, b_mn=1, lda=N, ldb=Xin.shape[1], D=dW)
+            sd = dict(A=dY, B=W, M=T, N=K, K=N, b_mn=1, ldb=K, D=dXa, ldd=dXa.shape[1])
+            return lambda: ops.gemm2([sw, sd])
+
+        forms = [("fwd_qkv", fprop(X, Wq, nqkv, H, Yq), 2 * T * nqkv * H, 2),
+                 ("fwd_o", fprop(X, Wo, H, nhd, Yo, Yo), 2 * T * H * nhd, 2),
+                 ("fwd_gu", fprop(X, Wgu, 2 * F, H, Ygu), 2 * T * 2 * F * H, 2),
+                 ("fwd_down", fprop(X, Wd, H, F, Yd, Yd), 2 * T * H * F, 1),
+                 ("bwd_down", pair(Yd, X, Wd, H, F, dWd), 4 * T * H * F, 1),
+                 ("bwd_gu", pair(Ygu, X, Wgu, 2 * F, H, dWgu), 4 * T * 2 * F * H, 1),
+                 ("bwd_o", pair(Yo, X, Wo, H, nhd, dWo), 4 * T * H * nhd, 1),
+                 ("bwd_qkv", pair(Yq, X, Wq, nqkv, H, dWq), 4 * T * nqkv * H, 1)]
+        del_after = []
+        if a.iters >= 0:
+            Wh = r(V, H)
+            Lg = torch.empty(T, V, dtype=bf, device=dev)
+            dWh = torch.empty_like(Wh)
+            forms += [("head_fwd", lambda: ops.gemm(X, Wh, T, V, H, lda=X.shape[1], D=Lg), 2 * T * V * H, 0),
+                      ("head_pair", pair(Lg, X, Wh, V, H, dWh), 4 * T * V * H, 0)]
+        out = {}
+        per_layer = c["n_layers"]
+        tot_fl = tot_ms = 0.0
+        launches = 0
+        for name, fn, fl, nl in forms:
+            ms = timeit(fn, a.iters, a.warmup)
+            cnt = per_layer * nl if nl else 1
+            out[name] = {"ms": ms, "tflops": fl / ms / 1e9, "launches_per_step": cnt}
+            tot_fl += fl * cnt
+            tot_ms += ms * cnt
+            launches += cnt
+        res.update(config=a.config, T=T, forms=out, step_gemm_ms=tot_ms, step_gemm_tflops=tot_fl / tot_ms / 1e9,
+                   launches_per_step=launches)
+        del del_after
     else:
         raise SystemExit("unknown op " + a.op)
     print(json.dumps(res))

@@ -115,10 +115,6 @@ typedef struct {
                               piece and every pinned host region, checked by
                               mt_sync: an overwrite latches MT_ERR_INTERNAL
                               naming the region (overflow / race detector) */
-  int32_t n_pack_threads;  /* pin_store = 0: host threads that pack weights
-                              into pinned staging (the driver thread is one
-                              of them); the others run Adam.  0 (the
-                              default): chosen by the static schedule */
 } mt_config;
 
 typedef struct { void* base; size_t bytes; } mt_dev_region;          /* caller-owned device memory  */
@@ -300,54 +296,54 @@ int32_t mt_visit_plan(const mt_config* cfg, int32_t* kind, int32_t* block, int32
 int32_t mt_schedule(int32_t n_visits, const double* b, const double* d, const double* c,
                     const double* a, double bw_h2d, double bw_d2h, double* stall);
 /* The static schedule as a steady-state model of the whole pipeline: the
- * pack of each visit's weights into pinned staging (n_pack threads), the
- * host-to-device copy, the compute, the gradient export into one of K slabs
- * and host Adam (the remaining threads, lowest block first among landed
+ * pack of each visit's weights into pinned staging (on the host worker pool,
+ * ahead of Adam's queued work, chunk by chunk with each chunk's copy starting
+ * once it is packed), the host-to-device copy, the compute, the gradient
+ * export into one of K slabs and host Adam (lowest block first among landed
  * slabs), with every dependency of the event protocol (Buffer-Free,
  * Weights-Ready, Backward-Done, a free slab, and the next step's forward of a
- * block after its Adam).  Per visit v of a step (mt_visit_plan order):
- * kind[v], block[v], b[v] host-to-device bytes, p[v] bytes packed first (0
- * with a pinned store), d[v] exported gradient bytes, c[v] compute seconds,
- * a[v] Adam elements of the exported block.  Rates: link bytes/s per
- * direction, pack bytes/s of one thread, Adam elements/s of one thread (r1)
- * and the asymptote r_max of n threads, r(n) = r_max (1 - exp(-n r1 /
- * r_max)) (host memory saturates).  Sources: [Peter]
- * 記憶體預取策略 (prefetch from layer bytes, link bandwidth and compute time);
- * [Hotdry] slab pool and event protocol; [Review] 3-2 (4), (6). */
+ * block after its Adam).  Host memory is shared: Adam runs at the smaller of
+ * its idle-host rate and what host_bw leaves after the period's DMA and pack
+ * traffic.  Per visit v of a step (mt_visit_plan order): kind[v], block[v],
+ * b[v] host-to-device bytes, p[v] bytes packed first (0 with a pinned store),
+ * d[v] exported gradient bytes, c[v] compute seconds, a[v] Adam elements of
+ * the exported block.  Sources: [Peter] 記憶體預取策略 (prefetch from layer
+ * bytes, link bandwidth and compute time); [Hotdry] slab pool and event
+ * protocol; [Review] 3-2 (4), (6). */
 typedef struct {
   int32_t n_visits;
   const int32_t *kind, *block;
   const double *b, *p, *d, *c, *a;
   int32_t n_buffers;
-  double bw_h2d, bw_d2h, pack_rate1, adam_rate1, adam_rate_max;
-  int32_t threads;   /* host threads shared by packing and Adam */
+  double bw_h2d, bw_d2h; /* link bytes/s per direction */
+  double pack_rate;      /* bytes/s the worker pool packs (0: instant) */
+  double adam_rate;      /* Adam elements/s of the worker pool on an idle host (0: instant) */
+  double adam_bytes;     /* host memory bytes Adam moves per element (28; 30 with the G copy) */
+  double host_bw;        /* bytes/s host memory serves CPU and DMA together (0: unlimited) */
 } mt_sched_in;
 typedef struct {
-  int32_t K, n_pack; /* slabs, packing threads */
+  int32_t K;         /* slabs */
   int32_t measured;  /* mt_get_schedule: 1 if c[] was measured in the first step */
   double period_ms;  /* predicted steady-state step time */
   double stall_ms;   /* predicted compute-stream idle time per step */
   double adam_busy_ms, slab_wait_ms, pack_ms;
+  double adam_gelem_s;  /* Adam's rate after DMA and the pack took their share */
   /* mt_get_schedule: the init-time measurements the plan used */
-  double bw_h2d_gbs, bw_d2h_gbs, pack_gbs_thread, adam_gelem_s_thread, adam_gelem_s_max;
+  double bw_h2d_gbs, bw_d2h_gbs, pack_gbs, adam_gelem_s_idle, host_gbs;
 } mt_sched_plan;
-/* Simulates the pipeline with K slabs and n_pack packing threads (stall_v:
- * n_visits entries, may be null: the predicted wait before each visit
- * computes).  MT_ERR_ARG for missing arrays, n_visits < 1, K < 1 or a
- * non-positive link bandwidth. */
-mt_status mt_schedule_simulate(const mt_sched_in* in, int32_t K, int32_t n_pack, mt_sched_plan* out,
-                               double* stall_v);
-/* Chooses K in [1, k_max] and n_pack (0 when nothing is packed, else in
- * [1, threads / 3]): the shortest predicted step, then the fewest slabs and
- * packing threads within 0.5 % of it. */
+/* Simulates the pipeline with K slabs (stall_v: n_visits entries, may be
+ * null: the predicted wait before each visit computes).  MT_ERR_ARG for
+ * missing arrays, n_visits < 1, K < 1 or a non-positive link bandwidth. */
+mt_status mt_schedule_simulate(const mt_sched_in* in, int32_t K, mt_sched_plan* out, double* stall_v);
+/* Chooses K in [1, k_max]: the shortest predicted step, then the fewest slabs
+ * within 0.5 % of it. */
 mt_status mt_schedule_plan(const mt_sched_in* in, int32_t k_max, mt_sched_plan* out);
 /* The plan a model runs with: which = 0, made in mt_init_model from the
- * blocks' bytes, the link, pack and Adam rates measured there and compute
- * times estimated from each visit's tensor FLOPs at 1.2 PFLOP/s (it set K
- * when n_grad_slabs was 0, and the packing threads when n_pack_threads was
- * 0); which = 1, made again once the first step's per-visit compute times
- * (CUDA events) are known, which then sets how many of the packing threads
- * work (MT_ERR_STATE until then). */
+ * blocks' bytes, the link, pack, Adam and shared host-memory rates measured
+ * there and compute times estimated from each visit's tensor FLOPs at 1.2
+ * PFLOP/s (it set K when n_grad_slabs was 0); which = 1, made again once the
+ * first step's per-visit compute times (CUDA events) are known (MT_ERR_STATE
+ * until then). */
 mt_status mt_get_schedule(const mt_model* model, int32_t which, mt_sched_plan* out);
 /* Host memory bandwidth on this machine: a parallel copy of `bytes` (GB/s,
  * read + write bytes) and the library's Adam (G elements/s) on n_threads
