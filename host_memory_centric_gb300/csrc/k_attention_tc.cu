@@ -3,9 +3,11 @@
 // TMA tiles, 320 threads per CTA (a TMA warp, an MMA warp, 8 row warps, two
 // per TMEM lane quarter).
 //
-// Forward: one CTA per (128 queries, query head, sequence):
-//   warp 0      TMA producer: the Q tile once, then K and V tiles of 128 keys
-//               into a 2-stage ring (128-byte swizzle);
+// Forward: a persistent CTA per SM loops over work items (128 queries, query
+// head, sequence), longest rows first; the next item's Q / K loads and first
+// S = Q K^T run while the softmax warps finish the previous item's epilogue:
+//   warp 0      TMA producer: each item's Q tile, then K and V tiles of 128
+//               keys into their rings (128-byte swizzle);
 //   warp 1      allocates TMEM (S0 | S1 | O_0 | O_1) and, from one thread,
 //               issues S_j = Q K_j^T (M=128, N=128) into S[j % 2] and, once the
 //               softmax has written P_{j-1} over S_{j-1} (BF16, in TMEM),
@@ -206,7 +208,7 @@ __device__ int g_attn_error = 0;
 
 template <int HD>
 __global__ void __launch_bounds__(ATTN_THREADS, 1)
-    attn_fwd_tc_k(const __grid_constant__ CUtensorMap tm, int S, int nh, int nkv, bf16* __restrict__ o,
+    attn_fwd_tc_k(const __grid_constant__ CUtensorMap tm, int S, int nh, int nkv, int n_seq, bf16* __restrict__ o,
                   float* __restrict__ lse, float scale_log2) {
   constexpr int NC = HD / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -223,26 +225,32 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   uint64_t* v_full = k_empty + NFK;     // [NFV]
   uint64_t* v_empty = v_full + NFV;     // [NFV]
   uint64_t* s_full = v_empty + NFV;     // [2]
-  // [2]: P_j over S buffer j % 2.  One barrier per buffer: tile j + 2's P
-  // needs S_{j+2}, issued only after O += P_j V, so neither barrier can
+  // [2]: P_g over S buffer g % 2.  One barrier per buffer: tile g + 2's P
+  // needs S_{g+2}, issued only after O += P_g V, so neither barrier can
   // complete a second phase before the MMA thread has seen the first
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 2;
   uint64_t* fin_ready = o_done + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin_ready + 1);
+  uint64_t* q_empty = fin_ready + 1;  // the item's last S = Q K^T has read Q
+  uint64_t* o_free = q_empty + 1;     // the epilogue has read O (the next item may overwrite it)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  // Work items, longest rows first: item i is query tile nqb - 1 - i / (nh
+  // n_seq) of head (i mod nh n_seq) mod nh and sequence (i mod nh n_seq) / nh.
+  // Round r gives the CTA item r G + blockIdx.x for even r and r G + G - 1 -
+  // blockIdx.x for odd r (G = gridDim.x): going back and forth evens out the
+  // lengths, which shrink along the list.  Key tiles, P V products and items
+  // are counted across items, so every barrier phase carries on.
+  const int nqb = (S + 127) / 128, per_qb = nh * n_seq, n_items = nqb * per_qb;
+  const int G = (int)gridDim.x;
+  auto item_of = [&](int rnd) { return rnd * G + ((rnd & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x); };
+  const int64_t T = (int64_t)n_seq * S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first
-  const int h = blockIdx.y, n = blockIdx.z;
-  const int kh = h / (nh / nkv);
-  const int q0 = qb * 128;
-  const int ntiles = qb + 1;
-  const int row0 = n * S;  // first token row of this sequence
-  const int64_t T = (int64_t)gridDim.z * S;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int i = 0; i < NFK; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
@@ -257,6 +265,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     }
     mbar_init(o_done, 1);
     mbar_init(fin_ready, 256);
+    mbar_init(o_free, 256);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm) : "memory");
@@ -270,38 +279,52 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO[2] = {tmem + 256, tmem + 256 + HD};  // O of key halves 0 and 1
+  // TMEM columns: S buffer b at tmem + 128 b, O of key half h at tmem + 256 + HD h
+  auto tS = [tmem](int b) { return tmem + (uint32_t)(128 * b); };
+  auto tO = [tmem](int h) { return tmem + 256u + (uint32_t)(HD * h); };
   uint32_t x_inflight = 0, x_par = 0;  // producer drain bookkeeping (lane 0: K stages, lane 1: V stages)
   bool q_inflight = false;
+  uint32_t q_par = 0;
 
   if (warp == 0) {
-    // lane 0 streams Q and the K ring, lane 1 the V ring, each on its own
-    // barriers, so a V stage still held by O += P V never delays K
+    // lane 0 streams each item's Q and the K ring, lane 1 the V ring, each on
+    // its own barriers, so a V stage still held by O += P V never delays K
     if (lane < 2) {
       const bool is_k = lane == 0;
       const int ns = is_k ? NFK : NFV;
       uint64_t* full = is_k ? k_full : v_full;
       uint64_t* empty = is_k ? k_empty : v_empty;
       uint8_t* base = is_k ? sK : sV;
-      const int col = (is_k ? nh + kh : nh + nkv + kh) * HD;
       bool ok = true;
-      if (is_k) {
-        mbar_expect_tx(q_full, NC * CH);
-        for (int c = 0; c < NC; ++c) tma_load(&tm, q_full, sQ + c * CH, h * HD + 64 * c, row0 + q0);
-        q_inflight = true;
-      }
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int s = j % ns;
-        const uint32_t u = (uint32_t)(j / ns);
-        if (!mbar_wait(&empty[s], (u & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
+      int g = 0;  // key tiles loaded so far
+      int it = 0;
+      for (int i = item_of(0); i < n_items && ok; i = item_of(++it)) {
+        const int qb = nqb - 1 - i / per_qb, r = i % per_qb, h = r % nh, n = r / nh;
+        const int kh = h / (nh / nkv), row0 = n * S;
+        const int col = (is_k ? nh + kh : nh + nkv + kh) * HD;
+        if (is_k) {
+          if (it > 0 && !mbar_wait(q_empty, (uint32_t)((it - 1) & 1), abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(q_full, NC * CH);
+          for (int c = 0; c < NC; ++c) tma_load(&tm, q_full, sQ + c * CH, h * HD + 64 * c, row0 + qb * 128);
+          q_inflight = true;
+          q_par = (uint32_t)(it & 1);
         }
-        mbar_expect_tx(&full[s], NC * CH);
-        for (int c = 0; c < NC; ++c) tma_load(&tm, &full[s], base + (s * NC + c) * CH, col + 64 * c, row0 + 128 * j);
-        x_inflight |= 1u << s;
-        x_par = (x_par & ~(1u << s)) | ((u & 1) << s);
+        for (int j = 0; j <= qb; ++j, ++g) {
+          const int s = g % ns;
+          const uint32_t u = (uint32_t)(g / ns);
+          if (!mbar_wait(&empty[s], (u & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&full[s], NC * CH);
+          for (int c = 0; c < NC; ++c)
+            tma_load(&tm, &full[s], base + (s * NC + c) * CH, col + 64 * c, row0 + 128 * j);
+          x_inflight |= 1u << s;
+          x_par = (x_par & ~(1u << s)) | ((u & 1) << s);
+        }
       }
       if (!ok) {
         *abort_flag = 1;
@@ -310,168 +333,188 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      bool ok = mbar_wait(q_full, 0, abort_flag);
       constexpr uint32_t IS = idesc(128, 128, false, false);
       constexpr uint32_t IO = idesc(128, HD, false, true);  // A = P from TMEM, B = V MN-major
       const uint64_t dV = sdesc(su32(sV), CH, 1024);
       const uint64_t dQ = sdesc(su32(sQ), 16, 1024), dK = sdesc(su32(sK), 16, 1024);
-      // O_0 += P[:, 0:64] V[0:64, :] and O_1 += P[:, 64:128] V[64:128, :]; P_i
-      // sits over S_i: the 64 keys of half h packed in columns 64 h .. 64 h + 31
-      auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(&p_full[i & 1], (uint32_t)((i >> 1) & 1), abort_flag) ||
-            !mbar_wait(&v_full[i % NFV], (uint32_t)((i / NFV) & 1), abort_flag))
+      int it = 0;
+      // O_0 += P[:, 0:64] V[0:64, :] and O_1 += P[:, 64:128] V[64:128, :] for
+      // key tile g (the first of its item when `first`: O starts from zero,
+      // once the previous item's epilogue has read it); P_g sits over S_g:
+      // the 64 keys of half h packed in columns 64 h .. 64 h + 31
+      auto issue_pv = [&](int g, bool first) -> bool {
+        if (!mbar_wait(&p_full[g & 1], (uint32_t)((g >> 1) & 1), abort_flag) ||
+            !mbar_wait(&v_full[g % NFV], (uint32_t)((g / NFV) & 1), abort_flag))
           return false;
+        if (first && it > 0 && !mbar_wait(o_free, (uint32_t)((it - 1) & 1), abort_flag)) return false;
         tc_fence_after();
-        const uint64_t v = dadv(dV, (i % NFV) * NC * CH);
-        const uint32_t tp = tS[i & 1];
-        const uint32_t acc0 = i > 0 ? 1u : 0u;
+        const uint64_t v = dadv(dV, (g % NFV) * NC * CH);
+        const uint32_t tp = tS(g & 1);
+        const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint32_t acc = kk > 0 ? 1u : acc0;
-          tc_mma_ts(tO[0], tp + (uint32_t)(kk * 8), dadv(v, kk * 16 * 128), IO, acc);
-          tc_mma_ts(tO[1], tp + (uint32_t)(64 + kk * 8), dadv(v, (4 + kk) * 16 * 128), IO, acc);
+          tc_mma_ts(tO(0), tp + (uint32_t)(kk * 8), dadv(v, kk * 16 * 128), IO, acc);
+          tc_mma_ts(tO(1), tp + (uint32_t)(64 + kk * 8), dadv(v, (4 + kk) * 16 * 128), IO, acc);
         }
         tc_commit(o_done);
-        tc_commit(&v_empty[i % NFV]);
+        tc_commit(&v_empty[g % NFV]);
         return true;
       };
-      // S_j goes into the columns of S_{j-2} / P_{j-2}, whose O += P V was
-      // issued before it (one thread's MMAs run in order)
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int s = j % NFK, b = j & 1;
-        if (!mbar_wait(&k_full[s], (uint32_t)((j / NFK) & 1), abort_flag)) {
+      bool ok = true;
+      int g = 0;  // key tiles computed so far
+      for (int i = item_of(0); i < n_items && ok; i = item_of(++it)) {
+        const int qb = nqb - 1 - i / per_qb;
+        if (!mbar_wait(q_full, (uint32_t)(it & 1), abort_flag)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint64_t kd = dadv(dK, s * NC * CH);
-        const uint32_t ts = tS[b];
+        // S_g goes into the columns of S_{g-2} / P_{g-2}, whose O += P V was
+        // issued before it (one thread's MMAs run in order)
+        for (int j = 0; j <= qb; ++j, ++g) {
+          const int s = g % NFK, b = g & 1;
+          if (!mbar_wait(&k_full[s], (uint32_t)((g / NFK) & 1), abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t kd = dadv(dK, s * NC * CH);
+          const uint32_t ts = tS(b);
 #pragma unroll
-        for (int c = 0; c < NC; ++c)
+          for (int c = 0; c < NC; ++c)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tc_mma(ts, dadv(dQ, c * CH + k * 32), dadv(kd, c * CH + k * 32), IS, (c | k) != 0);
-        tc_commit(&s_full[b]);
-        tc_commit(&k_empty[s]);  // K_j is read by S_j only
-        if (j >= 1 && !issue_pv(j - 1)) {
-          ok = false;
-          break;
+            for (int k = 0; k < 4; ++k)
+              tc_mma(ts, dadv(dQ, c * CH + k * 32), dadv(kd, c * CH + k * 32), IS, (c | k) != 0);
+          tc_commit(&s_full[b]);
+          tc_commit(&k_empty[s]);  // K_g is read by S_g only
+          if (j == qb) tc_commit(q_empty);  // the item's last S: Q may be replaced once it is done
+          if (j >= 1 && !issue_pv(g - 1, j == 1)) {
+            ok = false;
+            break;
+          }
         }
+        if (ok) ok = issue_pv(g - 1, qb == 0);
       }
-      if (ok) ok = issue_pv(ntiles - 1);
       if (!ok) {
         *abort_flag = 1;
         atomicCAS(&g_attn_error, 0, 12);
       }
     }
   } else {
-    // Softmax warps 2..9: this thread owns query row r (TMEM lane quarter
-    // warp % 4) for keys 64 half .. 64 half + 63 of every key tile, with its
-    // own running max m, sum l and accumulator O_half; the two halves of a
-    // row merge once at the end.
+    // Softmax warps 2..9: for each item this thread owns query row r (TMEM lane
+    // quarter warp % 4) for keys 64 half .. 64 half + 63 of every key tile,
+    // with its own running max m, sum l and accumulator O_half; the two
+    // halves of a row merge once at the item's end.
     const int qw = warp & 3, half = (warp - 2) >> 2;
     const int r = qw * 32 + lane;
-    const int qpos = q0 + r;  // position inside the sequence
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-    float m_used = -INFINITY, l = 0.f;  // exponent base of this half and the sum relative to it
     bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int b = j & 1;
-      const uint32_t u = (uint32_t)(j >> 1);
-      // warp-uniform outcome: the TMEM loads below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], u & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld32_nw(tS[b] + lane_off + half * 64, sr[0]);
-      tmem_ld32_nw(tS[b] + lane_off + half * 64 + 32, sr[1]);
-      tmem_wait_ld2(sr[0], sr[1]);
-      // raw scores (masked ones -inf); the exp2-domain scale enters once, in
-      // the max and in one FMA per score before ex2 (scale_log2 > 0)
-      float sv[64];
-      const int kbase = 128 * j + 64 * half;
-      // only the diagonal tile and a tile crossing the sequence end need masking
-      const bool need_mask = (kbase + 63 > q0) || (kbase + 64 > S);
-      if (need_mask) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const int key = kbase + i;
-          sv[i] = (key > qpos || key >= S) ? -INFINITY : __uint_as_float(sr[i >> 5][i & 31]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) sv[i] = __uint_as_float(sr[i >> 5][i & 31]);
-      }
-      // eight independent chains instead of one 64-long dependency chain
-      float mx8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = sv[k];
-#pragma unroll
-      for (int i = 8; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * scale_log2;
-      // lazy base: move it only when this tile's max exceeds it by more than
-      // 2^8 (always on the first tile with a key); P = 2^(s - base) <= 2^8
-      const bool move = mx > m_used + 8.f;
-      const float alpha = move ? ex2(m_used - mx) : 1.f;  // 0 when m_used = -inf
-      if (move) {
-        m_used = mx;
-        l *= alpha;
-      }
-      // O_half of rows whose base moved is rescaled once the previous P V has
-      // landed in it (warp-collective TMEM traffic: the whole warp joins)
-      if (j > 0 && __any_sync(0xffffffffu, move)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)((j - 1) & 1), abort_flag))) {
+    int g = 0;  // key tiles seen so far
+    int it = 0;
+    for (int i = item_of(0); i < n_items && ok; i = item_of(++it)) {
+      const int qb = nqb - 1 - i / per_qb, ri = i % per_qb, h = ri % nh, n = ri / nh;
+      const int q0 = qb * 128, row0 = n * S;
+      const int qpos = q0 + r;  // position inside the sequence
+      float m_used = -INFINITY, l = 0.f;  // exponent base of this half and the sum relative to it
+      for (int j = 0; j <= qb; ++j, ++g) {
+        const int b = g & 1;
+        const uint32_t u = (uint32_t)(g >> 1);
+        // warp-uniform outcome: the TMEM loads below are warp-collective
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], u & 1, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
+        uint32_t sr[2][32];
+        tmem_ld32_nw(tS(b) + lane_off + half * 64, sr[0]);
+        tmem_ld32_nw(tS(b) + lane_off + half * 64 + 32, sr[1]);
+        tmem_wait_ld2(sr[0], sr[1]);
+        // raw scores (masked ones -inf); the exp2-domain scale enters once, in
+        // the max and in one FMA per score before ex2 (scale_log2 > 0)
+        float sv[64];
+        const int kbase = 128 * j + 64 * half;
+        // only the diagonal tile and a tile crossing the sequence end need masking
+        const bool need_mask = (kbase + 63 > q0) || (kbase + 64 > S);
+        if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          float t[32];
-          tmem_ld32(tO[half] + lane_off + c * 32, t);
+          for (int k = 0; k < 64; ++k) {
+            const int key = kbase + k;
+            sv[k] = (key > qpos || key >= S) ? -INFINITY : __uint_as_float(sr[k >> 5][k & 31]);
+          }
+        } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) t[i] *= alpha;
-          tmem_st32(tO[half] + lane_off + c * 32, t);
+          for (int k = 0; k < 64; ++k) sv[k] = __uint_as_float(sr[k >> 5][k & 31]);
         }
-      }
-      const float base = m_used == -INFINITY ? 0.f : m_used;
-      // paired FP32 arithmetic (two lanes per instruction, each rounded as
-      // the scalar form) for the exponent arguments and the sums
-      const float2 sc2 = make_float2(scale_log2, scale_log2), nb2 = make_float2(-base, -base);
-      float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      uint32_t pw[32];
+        // eight independent chains instead of one 64-long dependency chain
+        float mx8[8];
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
-        const float2 e = __ffma2_rn(make_float2(sv[i], sv[i + 1]), sc2, nb2);
-        const float2 p = make_float2(ex2(e.x), ex2(e.y));
-        sum2[(i >> 1) & 3] = __fadd2_rn(sum2[(i >> 1) & 3], p);
-        pw[i >> 1] = pack2(p.x, p.y);
+        for (int k = 0; k < 8; ++k) mx8[k] = sv[k];
+#pragma unroll
+        for (int k = 8; k < 64; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], sv[k]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * scale_log2;
+        // lazy base: move it only when this tile's max exceeds it by more than
+        // 2^8 (always on the first tile with a key); P = 2^(s - base) <= 2^8
+        const bool move = mx > m_used + 8.f;
+        const float alpha = move ? ex2(m_used - mx) : 1.f;  // 0 when m_used = -inf
+        if (move) {
+          m_used = mx;
+          l *= alpha;
+        }
+        // O_half of rows whose base moved is rescaled once the previous P V has
+        // landed in it (warp-collective TMEM traffic: the whole warp joins)
+        if (j > 0 && __any_sync(0xffffffffu, move)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)((g - 1) & 1), abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            float t[32];
+            tmem_ld32(tO(half) + lane_off + c * 32, t);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) t[k] *= alpha;
+            tmem_st32(tO(half) + lane_off + c * 32, t);
+          }
+        }
+        const float base = m_used == -INFINITY ? 0.f : m_used;
+        // paired FP32 arithmetic (two lanes per instruction, each rounded as
+        // the scalar form) for the exponent arguments and the sums
+        const float2 sc2 = make_float2(scale_log2, scale_log2), nb2 = make_float2(-base, -base);
+        float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
+        uint32_t pw[32];
+#pragma unroll
+        for (int k = 0; k < 64; k += 2) {
+          const float2 e = __ffma2_rn(make_float2(sv[k], sv[k + 1]), sc2, nb2);
+          const float2 p = make_float2(ex2(e.x), ex2(e.y));
+          sum2[(k >> 1) & 3] = __fadd2_rn(sum2[(k >> 1) & 3], p);
+          pw[k >> 1] = pack2(p.x, p.y);
+        }
+        const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
+        const float2 st = __fadd2_rn(s01, s23);
+        l += st.x + st.y;
+        // P_g (BF16 pairs) over this half's first 32 columns of S_g, which this
+        // thread has already read: the A operand of the next O += P V
+        tmem_st32u(tS(b) + lane_off + half * 64, pw);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[b]);
       }
-      const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
-      const float2 st = __fadd2_rn(s01, s23);
-      l += st.x + st.y;
-      // P_j (BF16 pairs) over this half's first 32 columns of S_j, which this
-      // thread has already read: the A operand of the next O += P V
-      tmem_st32u(tS[b] + lane_off + half * 64, pw);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&p_full[b]);
-    }
-    const float m_old = m_used;
-    // merge the two halves of the row: m = max(m_0, m_1), c_h = 2^(m_h - m),
-    // l = l_0 c_0 + l_1 c_1, O = (O_0 c_0 + O_1 c_1) / l; each half writes
-    // half of the hd columns, once the last O += P V has landed
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)((ntiles - 1) & 1), abort_flag));
-    if (ok) {
-      fin[(half * 2) * 128 + r] = m_old;
-      fin[(half * 2 + 1) * 128 + r] = l;
-      mbar_arrive(fin_ready);
-      ok = __all_sync(0xffffffffu, mbar_wait(fin_ready, 0, abort_flag));
-    }
-    if (ok) {
+      if (!ok) break;
+      const float m_old = m_used;
+      // merge the two halves of the row: m = max(m_0, m_1), c_h = 2^(m_h - m),
+      // l = l_0 c_0 + l_1 c_1, O = (O_0 c_0 + O_1 c_1) / l; each half writes
+      // half of the hd columns, once the item's last O += P V has landed
+      ok = __all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)((g - 1) & 1), abort_flag));
+      if (ok) {
+        fin[(half * 2) * 128 + r] = m_old;
+        fin[(half * 2 + 1) * 128 + r] = l;
+        mbar_arrive(fin_ready);
+        ok = __all_sync(0xffffffffu, mbar_wait(fin_ready, (uint32_t)(it & 1), abort_flag));
+      }
+      if (!ok) break;
       tc_fence_after();
       const float m0 = fin[r], l0 = fin[128 + r], m1 = fin[256 + r], l1 = fin[384 + r];
       float m = fmaxf(m0, m1);
@@ -485,21 +528,25 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
 #pragma unroll
       for (int c = 0; c < HD / 64; ++c) {
         float a0[32], a1[32];
-        tmem_ld32(tO[0] + lane_off + half * (HD / 2) + c * 32, a0);
-        tmem_ld32(tO[1] + lane_off + half * (HD / 2) + c * 32, a1);
+        tmem_ld32(tO(0) + lane_off + half * (HD / 2) + c * 32, a0);
+        tmem_ld32(tO(1) + lane_off + half * (HD / 2) + c * 32, a1);
         if (valid) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int k = 0; k < 4; ++k) {
             float v[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = a0[8 * i + e] * f0 + a1[8 * i + e] * f1;
-            reinterpret_cast<uint4*>(orow + c * 32)[i] =
+            for (int e = 0; e < 8; ++e) v[e] = a0[8 * k + e] * f0 + a1[8 * k + e] * f1;
+            reinterpret_cast<uint4*>(orow + c * 32)[k] =
                 make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
           }
         }
       }
+      // O has been read: the next item's first O += P V may overwrite it
+      tc_fence_before();
+      mbar_arrive(o_free);
       if (valid && half == 0) lse[(int64_t)h * T + row0 + qpos] = (m + log2f(lt)) * 0.6931471805599453f;
-    } else if (lane == 0) {
+    }
+    if (!ok && lane == 0) {
       *abort_flag = 1;
       atomicCAS(&g_attn_error, 0, 13);
     }
@@ -507,8 +554,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
 
   if (warp == 0 && lane < 2 && *abort_flag) {
     const long long t0 = clock64();
-    if (q_inflight)
-      while (!mbar_test(q_full, 0) && clock64() - t0 < kWaitCycles) {
+    if (lane == 0 && q_inflight)
+      while (!mbar_test(q_full, q_par) && clock64() - t0 < kWaitCycles) {
       }
     uint64_t* full = lane == 0 ? k_full : v_full;
     for (int s2 = 0; s2 < (lane == 0 ? NFK : NFV); ++s2)
@@ -546,8 +593,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
 //   MMA   dV += P^T dO and dK += dS^T Q (dO, Q as MN-major operands).
 // TMEM: S^T | dP^T | dV | dK.
 //
-// attn_bwd_q_k: one CTA per (128 queries, query head, sequence), longest work
-// first, looping over 128-key tiles up to the diagonal.  Q and dO are written
+// attn_bwd_q_k: a persistent CTA per SM loops over work items (128 queries,
+// query head, sequence), longest work first, each looping over 128-key tiles
+// up to the diagonal; the next item's Q and dO go into TMEM as soon as the
+// current item's last S and dP have been read, so its first products run
+// during the current item's dQ epilogue.  Q and dO are written
 // into TMEM once by the row warps and are the A operands of S = Q K^T and
 // dP = dO V^T; the rows form P as soon as S lands (S's columns then take the
 // next tile's S), then dS = P (dP - delta) written over dP; dQ += dS K reads
@@ -905,26 +955,29 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   uint8_t* sK = sm;                  // NKT stages of [128 keys][HD]
   uint8_t* sV = sK + NKT * NC * CH;  // NKT stages of [128 keys][HD]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NKT * NC * CH);
-  uint64_t* q_ready = bars;         // Q, dO written to TMEM by the rows
+  uint64_t* q_ready = bars;         // an item's Q, dO written to TMEM by the rows
   uint64_t* kvf = bars + 1;         // [NKT]
   uint64_t* kve = kvf + NKT;        // [NKT]
   uint64_t* s1_full = kve + NKT;    // S in TMEM
   uint64_t* s2_full = s1_full + 1;  // dP in TMEM
   uint64_t* ps_free = s2_full + 1;  // the rows have read S
   uint64_t* p_full = ps_free + 1;   // dS written back over dP
-  uint64_t* acc_full = p_full + 1;
+  uint64_t* acc_full = p_full + 1;  // an item's dQ complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Work items, longest first: item i is query tile nqb - 1 - i / (nh n_seq)
+  // of head (i mod nh n_seq) / n_seq and sequence i mod n_seq.  A persistent
+  // CTA takes item r G + blockIdx.x in even rounds r and r G + G - 1 -
+  // blockIdx.x in odd ones (G = gridDim.x), which evens out the shrinking
+  // lengths; key tiles and items are counted across items, so every barrier
+  // phase carries on.
   const int nqb = (S + 127) / 128;
   const int per_qb = nh * n_seq;
-  const int qb = nqb - 1 - (int)(blockIdx.x / per_qb);  // the last query tile has the most keys
-  const int h = (int)(blockIdx.x % per_qb) / n_seq, n = (int)(blockIdx.x % n_seq);
-  const int kh = h / (nh / nkv);
-  const int q0 = qb * 128;
-  const int nkt = qb + 1;  // key tiles 0 .. qb (the last one holds the diagonal)
-  const int row0 = n * S;
+  const int n_items = nqb * per_qb;
+  const int G = (int)gridDim.x;
+  auto item_of = [&](int rnd) { return rnd * G + ((rnd & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x); };
   const int64_t T = (int64_t)n_seq * S;
   const int64_t ld = (int64_t)(nh + 2 * nkv) * HD;
 
@@ -958,23 +1011,28 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      for (int j = 0; j < nkt && ok; ++j) {
-        const int st = j % NKT;
-        const uint32_t u = (uint32_t)(j / NKT);
-        if (!mbar_wait(&kve[st], (u & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        mbar_expect_tx(&kvf[st], 2 * NC * CH);
-        for (int c = 0; c < NC; ++c)
-          for (int hf = 0; hf < 2; ++hf) {
-            tma_load(&tq, &kvf[st], sK + (st * NC + c) * CH + hf * CH64, (nh + kh) * HD + 64 * c,
-                     row0 + 128 * j + 64 * hf);
-            tma_load(&tq, &kvf[st], sV + (st * NC + c) * CH + hf * CH64, (nh + nkv + kh) * HD + 64 * c,
-                     row0 + 128 * j + 64 * hf);
+      int g = 0;  // key tiles loaded so far
+      for (int it = 0, i = item_of(0); i < n_items && ok; i = item_of(++it)) {
+        const int qb = nqb - 1 - i / per_qb, h = (i % per_qb) / n_seq, n = i % n_seq;
+        const int kh = h / (nh / nkv), row0 = n * S;
+        for (int j = 0; j <= qb; ++j, ++g) {
+          const int st = g % NKT;
+          const uint32_t u = (uint32_t)(g / NKT);
+          if (!mbar_wait(&kve[st], (u & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
           }
-        kv_inflight |= 1u << st;
-        kv_par = (kv_par & ~(1u << st)) | ((u & 1) << st);
+          mbar_expect_tx(&kvf[st], 2 * NC * CH);
+          for (int c = 0; c < NC; ++c)
+            for (int hf = 0; hf < 2; ++hf) {
+              tma_load(&tq, &kvf[st], sK + (st * NC + c) * CH + hf * CH64, (nh + kh) * HD + 64 * c,
+                       row0 + 128 * j + 64 * hf);
+              tma_load(&tq, &kvf[st], sV + (st * NC + c) * CH + hf * CH64, (nh + nkv + kh) * HD + 64 * c,
+                       row0 + 128 * j + 64 * hf);
+            }
+          kv_inflight |= 1u << st;
+          kv_par = (kv_par & ~(1u << st)) | ((u & 1) << st);
+        }
       }
       if (!ok) {
         *abort_flag = 1;
@@ -983,17 +1041,16 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      bool ok = mbar_wait(q_ready, 0, abort_flag);
       constexpr uint32_t I_S = idesc(128, 128, false, false);  // S, dP: A (Q, dO) in TMEM, B K-major over hd
       constexpr uint32_t I_G = idesc(128, HD, false, true);    // dQ: A (dS) in TMEM, B = K as MN-major
       const uint64_t dK = sdesc(su32(sK), 16, 1024), dV = sdesc(su32(sV), 16, 1024);
       const uint64_t dKm = sdesc(su32(sK), CH, 1024);
-      // Per tile j: S(j+1) as soon as the rows have read S(j); then dQ(j),
-      // which reads dS(j) from the dP columns, then dP(j+1) over them.
-      auto issue_s = [&](int j) -> bool {  // S = Q K^T
-        const int st = j % NKT;
-        if (!mbar_wait(&kvf[st], (uint32_t)((j / NKT) & 1), abort_flag)) return false;
-        if (j > 0 && !mbar_wait(ps_free, (uint32_t)((j - 1) & 1), abort_flag)) return false;
+      // Per key tile g: S(g+1) as soon as the rows have read S(g); then dQ(g),
+      // which reads dS(g) from the dP columns, then dP(g+1) over them.
+      auto issue_s = [&](int g) -> bool {  // S = Q K^T
+        const int st = g % NKT;
+        if (!mbar_wait(&kvf[st], (uint32_t)((g / NKT) & 1), abort_flag)) return false;
+        if (g > 0 && !mbar_wait(ps_free, (uint32_t)((g - 1) & 1), abort_flag)) return false;
         tc_fence_after();
         const uint64_t kd = dadv(dK, st * NC * CH);
 #pragma unroll
@@ -1002,36 +1059,46 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         tc_commit(s1_full);
         return true;
       };
-      auto issue_dp = [&](int j) {  // dP = dO V^T (its K / V stage was waited for by issue_s)
-        const uint64_t vd = dadv(dV, (j % NKT) * NC * CH);
+      auto issue_dp = [&](int g) {  // dP = dO V^T (its K / V stage was waited for by issue_s)
+        const uint64_t vd = dadv(dV, (g % NKT) * NC * CH);
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks)
           tc_mma_ts(tP, tdO + 8 * ks, dadv(vd, (ks >> 2) * CH + (ks & 3) * 32), I_S, ks != 0);
         tc_commit(s2_full);
       };
-      auto issue_g = [&](int j) -> bool {  // dQ += dS K; the K / V stage is then free
-        const int st = j % NKT;
-        if (!mbar_wait(p_full, (uint32_t)(j & 1), abort_flag)) return false;
+      auto issue_g = [&](int g, bool first) -> bool {  // dQ (+)= dS K; the K / V stage is then free
+        const int st = g % NKT;
+        if (!mbar_wait(p_full, (uint32_t)(g & 1), abort_flag)) return false;
         tc_fence_after();
         const uint64_t km = dadv(dKm, st * NC * CH);
-        const uint32_t acc0 = j > 0 ? 1u : 0u;
+        const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           tc_mma_ts(tdQ, tP + pcol(kk), dadv(km, kk * 2048), I_G, kk > 0 ? 1u : acc0);
         tc_commit(&kve[st]);
         return true;
       };
-      if (ok) ok = issue_s(0);
-      if (ok) issue_dp(0);
-      for (int j = 0; j < nkt && ok; ++j) {
-        const bool more = j + 1 < nkt;
-        if ((more && !issue_s(j + 1)) || !issue_g(j)) {
+      bool ok = true;
+      int g = 0;  // key tiles computed so far
+      for (int it = 0, i = item_of(0); i < n_items && ok; i = item_of(++it)) {
+        const int nkt = nqb - i / per_qb;  // key tiles 0 .. qb (the last one holds the diagonal)
+        // the rows have written this item's Q and dO (after reading the
+        // previous item's last S and dP, so those columns are free)
+        if (!mbar_wait(q_ready, (uint32_t)(it & 1), abort_flag) || !issue_s(g)) {
           ok = false;
           break;
         }
-        if (more) issue_dp(j + 1);
+        issue_dp(g);
+        for (int j = 0; j < nkt; ++j, ++g) {
+          const bool more = j + 1 < nkt;
+          if ((more && !issue_s(g + 1)) || !issue_g(g, j == 0)) {
+            ok = false;
+            break;
+          }
+          if (more) issue_dp(g + 1);
+        }
+        if (ok) tc_commit(acc_full);
       }
-      if (ok) tc_commit(acc_full);
       if (!ok) {
         *abort_flag = 1;
         atomicCAS(&g_attn_error, 0, 25);
@@ -1042,26 +1109,25 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     // 0..63 of a tile (and the first half of Q, dO, dQ's hd columns), warps
     // 6..9 keys 64..127 (and the second half).
     const int qw = warp & 3, half = (warp - 2) >> 2;
-    const int r = qw * 32 + lane;  // query row
+    const int r = qw * 32 + lane;  // query row of the tile
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-    const int q = q0 + r;
-    const bool valid = q < S;
-    const int64_t li = (int64_t)h * T + row0 + (valid ? q : 0);
-    const float lse2 = valid ? lse[li] * 1.4426950408889634f : 0.f;
-    const float dl = valid ? delta[li] : 0.f;
-    // this row's half of Q and of dO into TMEM (the A operands of S and dP)
-    {
+    // this row's half of Q and of dO of item i into TMEM (the A operands of S
+    // and dP), then the q_ready arrival
+    auto load_q = [&](int i) {
+      const int qb = nqb - 1 - i / per_qb, h = (i % per_qb) / n_seq, n = i % n_seq;
+      const int q = qb * 128 + r, row0 = n * S;
+      const bool valid = q < S;
       const uint4* qs = reinterpret_cast<const uint4*>(qkv + ((int64_t)row0 + (valid ? q : 0)) * ld +
-                                                         (int64_t)h * HD + half * (HD / 2));
+                                                       (int64_t)h * HD + half * (HD / 2));
       const uint4* os = reinterpret_cast<const uint4*>(dout + ((int64_t)row0 + (valid ? q : 0)) * ((int64_t)nh * HD) +
-                                                         (int64_t)h * HD + half * (HD / 2));
+                                                       (int64_t)h * HD + half * (HD / 2));
       uint32_t qv[QC / 2], ov[QC / 2];
 #pragma unroll
-      for (int i = 0; i < QC / 8; ++i) {
-        const uint4 a = valid ? qs[i] : make_uint4(0, 0, 0, 0);
-        const uint4 c = valid ? os[i] : make_uint4(0, 0, 0, 0);
-        qv[4 * i] = a.x; qv[4 * i + 1] = a.y; qv[4 * i + 2] = a.z; qv[4 * i + 3] = a.w;
-        ov[4 * i] = c.x; ov[4 * i + 1] = c.y; ov[4 * i + 2] = c.z; ov[4 * i + 3] = c.w;
+      for (int k = 0; k < QC / 8; ++k) {
+        const uint4 a = valid ? qs[k] : make_uint4(0, 0, 0, 0);
+        const uint4 c = valid ? os[k] : make_uint4(0, 0, 0, 0);
+        qv[4 * k] = a.x; qv[4 * k + 1] = a.y; qv[4 * k + 2] = a.z; qv[4 * k + 3] = a.w;
+        ov[4 * k] = c.x; ov[4 * k + 1] = c.y; ov[4 * k + 2] = c.z; ov[4 * k + 3] = c.w;
       }
       if constexpr (QC / 2 == 32) {
         tmem_st32u(tQ + lane_off + half * (QC / 2), qv);
@@ -1073,70 +1139,87 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(q_ready);
-    }
+    };
     bool ok = true;
-    for (int j = 0; j < nkt; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(s1_full, (uint32_t)(j & 1), abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int k0 = 128 * j + 64 * half;  // first key of this thread's 64 columns
-      const bool need_mask = (k0 + 63 > q0) || (k0 + 64 > S);
-      // phase 1: P from S; then S's columns are free for the next tile
-      float p[64];
-      {
-        uint32_t sv[2][32];
-        tmem_ld32_nw(tS + lane_off + half * 64, sv[0]);
-        tmem_ld32_nw(tS + lane_off + half * 64 + 32, sv[1]);
-        tmem_wait_ld2(sv[0], sv[1]);
-        const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(-lse2, -lse2);
+    int g = 0;  // key tiles seen so far
+    if (item_of(0) < n_items) load_q(item_of(0));
+    for (int it = 0, i = item_of(0); i < n_items; i = item_of(++it)) {
+      const int qb = nqb - 1 - i / per_qb, h = (i % per_qb) / n_seq, n = i % n_seq;
+      const int q0 = qb * 128, nkt = qb + 1, row0 = n * S;
+      const int q = q0 + r;
+      const bool valid = q < S;
+      const int64_t li = (int64_t)h * T + row0 + (valid ? q : 0);
+      const float lse2 = valid ? lse[li] * 1.4426950408889634f : 0.f;
+      const float dl = valid ? delta[li] : 0.f;
+      for (int j = 0; j < nkt; ++j, ++g) {
+        if (!__all_sync(0xffffffffu, mbar_wait(s1_full, (uint32_t)(g & 1), abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int k0 = 128 * j + 64 * half;  // first key of this thread's 64 columns
+        const bool need_mask = (k0 + 63 > q0) || (k0 + 64 > S);
+        // phase 1: P from S; then S's columns are free for the next tile
+        float p[64];
+        {
+          uint32_t sv[2][32];
+          tmem_ld32_nw(tS + lane_off + half * 64, sv[0]);
+          tmem_ld32_nw(tS + lane_off + half * 64 + 32, sv[1]);
+          tmem_wait_ld2(sv[0], sv[1]);
+          const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(-lse2, -lse2);
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[e >> 5][e & 31]),
-                                                    __uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31])),
-                                        sc2, nl2);
-          float pa = ex2(arg.x), pb = ex2(arg.y);
-          if (need_mask) {
-            const int key = k0 + e;
-            if (key > q || key >= S) pa = 0.f;
-            if (key + 1 > q || key + 1 >= S) pb = 0.f;
+          for (int e = 0; e < 64; e += 2) {
+            const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[e >> 5][e & 31]),
+                                                      __uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31])),
+                                          sc2, nl2);
+            float pa = ex2(arg.x), pb = ex2(arg.y);
+            if (need_mask) {
+              const int key = k0 + e;
+              if (key > q || key >= S) pa = 0.f;
+              if (key + 1 > q || key + 1 >= S) pb = 0.f;
+            }
+            p[e] = pa;
+            p[e + 1] = pb;
           }
-          p[e] = pa;
-          p[e + 1] = pb;
+          tc_fence_before();
+          mbar_arrive(ps_free);
         }
-        tc_fence_before();
-        mbar_arrive(ps_free);
+        // phase 2: dS = P (dP - delta), back over the first 32 dP columns this thread read
+        if (!__all_sync(0xffffffffu, mbar_wait(s2_full, (uint32_t)(g & 1), abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        {
+          uint32_t dp[2][32];
+          tmem_ld32_nw(tP + lane_off + half * 64, dp[0]);
+          tmem_ld32_nw(tP + lane_off + half * 64 + 32, dp[1]);
+          tmem_wait_ld2(dp[0], dp[1]);
+          uint32_t dw[32];
+          const float2 nd2 = make_float2(-dl, -dl);
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            const float2 dd = __fadd2_rn(make_float2(__uint_as_float(dp[e >> 5][e & 31]),
+                                                     __uint_as_float(dp[(e + 1) >> 5][(e + 1) & 31])),
+                                         nd2);
+            const float2 v = __fmul2_rn(make_float2(p[e], p[e + 1]), dd);
+            dw[e / 2] = pack2(v.x, v.y);
+          }
+          tmem_st32u(tP + lane_off + half * 64, dw);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(p_full);
+        }
       }
-      // phase 2: dS = P (dP - delta), back over the first 32 dP columns this thread read
-      if (!__all_sync(0xffffffffu, mbar_wait(s2_full, (uint32_t)(j & 1), abort_flag))) {
+      if (!ok) break;
+      // the item's last S and dP have been read, so the next item's Q and dO
+      // may go into their columns now: its first products overlap this epilogue
+      const int nxt = item_of(it + 1);
+      if (nxt < n_items) load_q(nxt);
+      if (!__all_sync(0xffffffffu, mbar_wait(acc_full, (uint32_t)(it & 1), abort_flag))) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      {
-        uint32_t dp[2][32];
-        tmem_ld32_nw(tP + lane_off + half * 64, dp[0]);
-        tmem_ld32_nw(tP + lane_off + half * 64 + 32, dp[1]);
-        tmem_wait_ld2(dp[0], dp[1]);
-        uint32_t dw[32];
-        const float2 nd2 = make_float2(-dl, -dl);
-#pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          const float2 dd = __fadd2_rn(make_float2(__uint_as_float(dp[e >> 5][e & 31]),
-                                                   __uint_as_float(dp[(e + 1) >> 5][(e + 1) & 31])),
-                                       nd2);
-          const float2 v = __fmul2_rn(make_float2(p[e], p[e + 1]), dd);
-          dw[e / 2] = pack2(v.x, v.y);
-        }
-        tmem_st32u(tP + lane_off + half * 64, dw);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(p_full);
-      }
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
-    if (ok) {
       tc_fence_after();
       bf16* row = dqkv + ((int64_t)row0 + (valid ? q : 0)) * ld + (int64_t)h * HD + half * (HD / 2);
 #pragma unroll
@@ -1151,7 +1234,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
                 pack2(v[8 * i4 + 4] * scale, v[8 * i4 + 5] * scale), pack2(v[8 * i4 + 6] * scale, v[8 * i4 + 7] * scale));
         }
       }
-    } else if (lane == 0) {
+    }
+    if (!ok && lane == 0) {
       *abort_flag = 1;
       atomicCAS(&g_attn_error, 0, 26);
     }
@@ -1187,6 +1271,19 @@ void init_once() {
   g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 }
 
+// CTAs of a launch over n_items (query tile, head, sequence) items of at
+// most nqb key tiles each.  Up to 64 key tiles (S <= 8192) each CTA is
+// persistent, one per SM, so an item's set-up overlaps the previous item's
+// epilogue (S = 4096: 952 against about 870 TFLOP/s forward); longer items
+// amortise their set-up anyway, and one CTA per item lets the hardware
+// scheduler balance them dynamically (S = 32768: 1,192 against 1,138 with
+// persistent CTAs).  A CTA given one item runs exactly that item.
+int attn_grid(int64_t n_items, int nqb) {
+  if (nqb > 64) return (int)n_items;
+  const int sms = gemm_num_sms();
+  return (int)std::min<int64_t>(n_items, sms > 0 ? sms : 148);
+}
+
 template <int HD>
 constexpr int smem_bytes() {
   return (HD / 64) * 16384 * (1 + NFK + NFV) + 2048 + 1024 + 256;
@@ -1209,8 +1306,10 @@ cudaError_t launch(const bf16* qkv, int n_seq, int S, int nh, int nkv, bf16* o, 
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_k<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SM);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
-  dim3 grid((S + 127) / 128, nh, n_seq);
-  attn_fwd_tc_k<HD><<<grid, ATTN_THREADS, SM, s>>>(m, S, nh, nkv, o, lse, scale_log2);
+  const int64_t n_items = (int64_t)((S + 127) / 128) * nh * n_seq;
+  if (n_items > 0x7fffffff) return cudaErrorInvalidValue;
+  const int grid = attn_grid(n_items, (S + 127) / 128);
+  attn_fwd_tc_k<HD><<<grid, ATTN_THREADS, SM, s>>>(m, S, nh, nkv, n_seq, o, lse, scale_log2);
   return cudaGetLastError();
 }
 
@@ -1244,8 +1343,9 @@ cudaError_t launch_bwd(const bf16* qkv, const bf16* dout, const float* lse, cons
                                                          scale * 1.4426950408889634f, dqkv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_bwd_q_k<HD><<<(unsigned)gq, ATTN_THREADS, SQ, s>>>(mq, qkv, dout, S, n_seq, nh, nkv, lse, delta, scale,
-                                                          scale * 1.4426950408889634f, dqkv);
+  const unsigned gqp = (unsigned)attn_grid(gq, (int)nqb);
+  attn_bwd_q_k<HD><<<gqp, ATTN_THREADS, SQ, s>>>(mq, qkv, dout, S, n_seq, nh, nkv, lse, delta, scale,
+                                                 scale * 1.4426950408889634f, dqkv);
   return cudaGetLastError();
 }
 

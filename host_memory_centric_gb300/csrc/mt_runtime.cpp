@@ -1037,12 +1037,12 @@ constexpr int64_t kPackChunk = (int64_t)64 << 20;  // bytes packed before their 
 
 // Host-to-device copy of the given ranges of block j's W region into device
 // buffer b on the weight stream.  With the just-in-time pack (src pageable)
-// each 64 MiB chunk is first copied into pinned staging b -- in 8 MiB pieces
-// on the worker pool, ahead of any queued Adam work, with the driver thread
-// copying too -- and its device copy is enqueued as soon as it is packed, so
-// the pack of a chunk overlaps the transfer of the previous one.
+// each 64 MiB chunk is first copied into pinned staging b -- in 4 MiB pieces,
+// enough for every worker, queued ahead of any Adam work, with the driver
+// thread copying too -- and its device copy is enqueued as soon as it is
+// packed, so the pack of a chunk overlaps the transfer of the previous one.
 mt_status copy_ranges(mt_model* m, int b, const uint8_t* src, const std::vector<Range>& rg, bool pack) {
-  constexpr int64_t PIECE = (int64_t)8 << 20;
+  constexpr int64_t PIECE = (int64_t)4 << 20;
   uint8_t* stage = m->staging[b];
   for (const Range& r : rg)
     for (int64_t c0 = 0; c0 < r.bytes;) {
@@ -1519,11 +1519,11 @@ void run_probes(mt_model* m) {
       if (best < 1e30f) (dir == 0 ? in.bw_h2d : in.bw_d2h) = (double)bytes / (best * 1e-3);
     }
   }
-  // the pack: the largest block's first `bytes` of W, in 8 MiB pieces over the pool
+  // the pack: the largest block's first `bytes` of W, in 4 MiB pieces over the pool
   const mth::BlockDesc* big = &m->lay[0];
   for (auto& b : m->lay)
     if (b.wbytes > big->wbytes) big = &b;
-  const int64_t pb = std::min<int64_t>((int64_t)bytes, big->wbytes), PIECE = (int64_t)8 << 20;
+  const int64_t pb = std::min<int64_t>((int64_t)bytes, big->wbytes), PIECE = (int64_t)4 << 20;
   const uint8_t* src = m->store + big->store_off;
   std::function<void(int64_t)> cp = [&](int64_t i) {
     const int64_t o = i * PIECE;

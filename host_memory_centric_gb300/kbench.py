@@ -54,6 +54,7 @@ def main():
     ap.add_argument("--k", type=int, default=4)
     ap.add_argument("--Fe", type=int, default=2880)
     ap.add_argument("--config", default="7.6b")
+    ap.add_argument("--no-head", action="store_true", help="layer_gemms: leave out the LM-head forms")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     a = ap.parse_args()
@@ -183,8 +184,7 @@ def main():
                  ("bwd_gu", pair(Ygu, X, Wgu, 2 * F, H, dWgu), 4 * T * 2 * F * H, 1),
                  ("bwd_o", pair(Yo, X, Wo, H, nhd, dWo), 4 * T * H * nhd, 1),
                  ("bwd_qkv", pair(Yq, X, Wq, nqkv, H, dWq), 4 * T * nqkv * H, 1)]
-        del_after = []
-        if a.iters >= 0:
+        if not a.no_head:
             Wh = r(V, H)
             Lg = torch.empty(T, V, dtype=bf, device=dev)
             dWh = torch.empty_like(Wh)
@@ -203,7 +203,6 @@ def main():
             launches += cnt
         res.update(config=a.config, T=T, forms=out, step_gemm_ms=tot_ms, step_gemm_tflops=tot_fl / tot_ms / 1e9,
                    launches_per_step=launches)
-        del del_after
     else:
         raise SystemExit("unknown op " + a.op)
     print(json.dumps(res))

@@ -185,6 +185,10 @@ def test_swiglu(orc):
     (128, 2, 2, 33, 2),    # shorter than one sub-tile
     (64, 2, 1, 129, 1),    # one row past a tile
     (128, 4, 4, 512, 1),   # several full tiles on and off the diagonal
+    # more work items than SMs: a persistent CTA runs several (query tile,
+    # head, sequence) items one after another
+    (64, 16, 4, 384, 4),   # 192 items of 1 to 3 key tiles
+    (128, 40, 8, 100, 4),  # 160 single-tile items, groups of 5 (the 14.7B grouping)
 ])
 def test_attention_fwd_bwd(orc, hd, nh, nkv, S, n_seq):
     T = n_seq * S
