@@ -458,12 +458,13 @@ def _overrides(args):
 
 
 # DRAM bytes (read + write) per GEMM launch, from one ncu capture of the
-# GEMM shapes of one decoder layer of the default workload (the 7.6B-shaped
-# decoder at 16384 tokens per visit; metrics dram__bytes_read.sum and
-# dram__bytes_write.sum, each shape weighted by its launches per step).
-# Valid only for the kernel source it was taken from: any change to the GEMM
-# kernel reports null.
-GEMM_TRAFFIC = {"source_sha256_16": None, "config": "7.6b", "bytes_per_launch": None}
+# GEMM forms of one decoder layer of the default workload (the 7.6B-shaped
+# decoder at 16384 tokens per visit, launched by `kbench layer_gemms`;
+# metrics dram__bytes_read.sum and dram__bytes_write.sum, each form weighted
+# by its launches per step: 308 of the step's 310 GEMM launches, the LM
+# head's two not captured).  Valid only for the kernel source it was taken
+# from: any change to the GEMM kernel reports null.
+GEMM_TRAFFIC = {"source_sha256_16": "d673657982fa8dcb", "config": "7.6b", "bytes_per_launch": 2.8118e9}
 
 
 def gemm_traffic_per_launch(name, c, args):
