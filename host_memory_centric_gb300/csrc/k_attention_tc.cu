@@ -206,10 +206,28 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 
 __device__ int g_attn_error = 0;
 
-template <int HD>
+// Work item i of a launch over (128-query tile, head, sequence) items.
+// Longest first (head_major = 0): every head's last query tile, then every
+// head's second-to-last, ... (balances persistent CTAs).  Head-major
+// (head_major = 1): all query tiles of one head and sequence, longest first,
+// then the next head -- the CTAs running together share one KV head's keys
+// and values in L2 (long sequences, one CTA per item).
+struct AttnItem {
+  int qb, h, n;
+};
+__device__ __forceinline__ AttnItem attn_item(int i, int nqb, int nh, int n_seq, int head_major) {
+  if (head_major) {
+    const int rest = i / nqb;
+    return {nqb - 1 - i % nqb, rest % nh, rest / nh};
+  }
+  const int per_qb = nh * n_seq, r = i % per_qb;
+  return {nqb - 1 - i / per_qb, r % nh, r / nh};
+}
+
+template <int HD, bool PERSIST>
 __global__ void __launch_bounds__(ATTN_THREADS, 1)
     attn_fwd_tc_k(const __grid_constant__ CUtensorMap tm, int S, int nh, int nkv, int n_seq, bf16* __restrict__ o,
-                  float* __restrict__ lse, float scale_log2) {
+                  float* __restrict__ lse, float scale_log2, int head_major) {
   constexpr int NC = HD / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -244,7 +262,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   // are counted across items, so every barrier phase carries on.
   const int nqb = (S + 127) / 128, per_qb = nh * n_seq, n_items = nqb * per_qb;
   const int G = (int)gridDim.x;
-  auto item_of = [&](int rnd) { return rnd * G + ((rnd & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x); };
+  // PERSIST = false: one item per CTA (item blockIdx.x), compiled as
+  // straight-line code without the cross-item waits
+  auto item_of = [&](int rnd) {
+    if constexpr (!PERSIST) return rnd == 0 ? (int)blockIdx.x : n_items;
+    return rnd * G + ((rnd & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+  };
   const int64_t T = (int64_t)n_seq * S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -299,11 +322,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       int g = 0;  // key tiles loaded so far
       int it = 0;
       for (int i = item_of(0); i < n_items && ok; i = item_of(++it)) {
-        const int qb = nqb - 1 - i / per_qb, r = i % per_qb, h = r % nh, n = r / nh;
+        const AttnItem w = attn_item(i, nqb, nh, n_seq, head_major);
+        const int qb = w.qb, h = w.h, n = w.n;
         const int kh = h / (nh / nkv), row0 = n * S;
         const int col = (is_k ? nh + kh : nh + nkv + kh) * HD;
         if (is_k) {
-          if (it > 0 && !mbar_wait(q_empty, (uint32_t)((it - 1) & 1), abort_flag)) {
+          if (PERSIST && it > 0 && !mbar_wait(q_empty, (uint32_t)((it - 1) & 1), abort_flag)) {
             ok = false;
             break;
           }
@@ -346,7 +370,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         if (!mbar_wait(&p_full[g & 1], (uint32_t)((g >> 1) & 1), abort_flag) ||
             !mbar_wait(&v_full[g % NFV], (uint32_t)((g / NFV) & 1), abort_flag))
           return false;
-        if (first && it > 0 && !mbar_wait(o_free, (uint32_t)((it - 1) & 1), abort_flag)) return false;
+        if (PERSIST && first && it > 0 && !mbar_wait(o_free, (uint32_t)((it - 1) & 1), abort_flag)) return false;
         tc_fence_after();
         const uint64_t v = dadv(dV, (g % NFV) * NC * CH);
         const uint32_t tp = tS(g & 1);
@@ -364,7 +388,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       bool ok = true;
       int g = 0;  // key tiles computed so far
       for (int i = item_of(0); i < n_items && ok; i = item_of(++it)) {
-        const int qb = nqb - 1 - i / per_qb;
+        const int qb = attn_item(i, nqb, nh, n_seq, head_major).qb;
         if (!mbar_wait(q_full, (uint32_t)(it & 1), abort_flag)) {
           ok = false;
           break;
@@ -387,7 +411,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
               tc_mma(ts, dadv(dQ, c * CH + k * 32), dadv(kd, c * CH + k * 32), IS, (c | k) != 0);
           tc_commit(&s_full[b]);
           tc_commit(&k_empty[s]);  // K_g is read by S_g only
-          if (j == qb) tc_commit(q_empty);  // the item's last S: Q may be replaced once it is done
+          if (PERSIST && j == qb) tc_commit(q_empty);  // the item's last S: Q may be replaced once it is done
           if (j >= 1 && !issue_pv(g - 1, j == 1)) {
             ok = false;
             break;
@@ -412,8 +436,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     int g = 0;  // key tiles seen so far
     int it = 0;
     for (int i = item_of(0); i < n_items && ok; i = item_of(++it)) {
-      const int qb = nqb - 1 - i / per_qb, ri = i % per_qb, h = ri % nh, n = ri / nh;
-      const int q0 = qb * 128, row0 = n * S;
+      // only the query tile is live through the key-tile loop; the head and
+      // sequence are derived again for the epilogue (register pressure: a
+      // 320-thread CTA gets at most 168 registers per thread)
+      const int qb = attn_item(i, nqb, nh, n_seq, head_major).qb;
+      const int q0 = qb * 128;
       const int qpos = q0 + r;  // position inside the sequence
       float m_used = -INFINITY, l = 0.f;  // exponent base of this half and the sum relative to it
       for (int j = 0; j <= qb; ++j, ++g) {
@@ -524,6 +551,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       const float inv = 1.f / lt;
       const float f0 = c0 * inv, f1 = c1 * inv;
       const bool valid = qpos < S;
+      const AttnItem w = attn_item(i, nqb, nh, n_seq, head_major);
+      const int h = w.h, row0 = w.n * S;
       bf16* orow = o + ((int64_t)row0 + qpos) * ((int64_t)nh * HD) + (int64_t)h * HD + half * (HD / 2);
 #pragma unroll
       for (int c = 0; c < HD / 64; ++c) {
@@ -542,8 +571,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         }
       }
       // O has been read: the next item's first O += P V may overwrite it
-      tc_fence_before();
-      mbar_arrive(o_free);
+      if (PERSIST) {
+        tc_fence_before();
+        mbar_arrive(o_free);
+      }
       if (valid && half == 0) lse[(int64_t)h * T + row0 + qpos] = (m + log2f(lt)) * 0.6931471805599453f;
     }
     if (!ok && lane == 0) {
@@ -593,11 +624,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
 //   MMA   dV += P^T dO and dK += dS^T Q (dO, Q as MN-major operands).
 // TMEM: S^T | dP^T | dV | dK.
 //
-// attn_bwd_q_k: a persistent CTA per SM loops over work items (128 queries,
-// query head, sequence), longest work first, each looping over 128-key tiles
-// up to the diagonal; the next item's Q and dO go into TMEM as soon as the
-// current item's last S and dP have been read, so its first products run
-// during the current item's dQ epilogue.  Q and dO are written
+// attn_bwd_q_k: one CTA per (128 queries, query head, sequence), longest work
+// first, looping over 128-key tiles up to the diagonal.  Q and dO are written
 // into TMEM once by the row warps and are the A operands of S = Q K^T and
 // dP = dO V^T; the rows form P as soon as S lands (S's columns then take the
 // next tile's S), then dS = P (dP - delta) written over dP; dQ += dS K reads
@@ -955,29 +983,26 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   uint8_t* sK = sm;                  // NKT stages of [128 keys][HD]
   uint8_t* sV = sK + NKT * NC * CH;  // NKT stages of [128 keys][HD]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NKT * NC * CH);
-  uint64_t* q_ready = bars;         // an item's Q, dO written to TMEM by the rows
+  uint64_t* q_ready = bars;         // Q, dO written to TMEM by the rows
   uint64_t* kvf = bars + 1;         // [NKT]
   uint64_t* kve = kvf + NKT;        // [NKT]
   uint64_t* s1_full = kve + NKT;    // S in TMEM
   uint64_t* s2_full = s1_full + 1;  // dP in TMEM
   uint64_t* ps_free = s2_full + 1;  // the rows have read S
   uint64_t* p_full = ps_free + 1;   // dS written back over dP
-  uint64_t* acc_full = p_full + 1;  // an item's dQ complete
+  uint64_t* acc_full = p_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Work items, longest first: item i is query tile nqb - 1 - i / (nh n_seq)
-  // of head (i mod nh n_seq) / n_seq and sequence i mod n_seq.  A persistent
-  // CTA takes item r G + blockIdx.x in even rounds r and r G + G - 1 -
-  // blockIdx.x in odd ones (G = gridDim.x), which evens out the shrinking
-  // lengths; key tiles and items are counted across items, so every barrier
-  // phase carries on.
   const int nqb = (S + 127) / 128;
   const int per_qb = nh * n_seq;
-  const int n_items = nqb * per_qb;
-  const int G = (int)gridDim.x;
-  auto item_of = [&](int rnd) { return rnd * G + ((rnd & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x); };
+  const int qb = nqb - 1 - (int)(blockIdx.x / per_qb);  // the last query tile has the most keys
+  const int h = (int)(blockIdx.x % per_qb) / n_seq, n = (int)(blockIdx.x % n_seq);
+  const int kh = h / (nh / nkv);
+  const int q0 = qb * 128;
+  const int nkt = qb + 1;  // key tiles 0 .. qb (the last one holds the diagonal)
+  const int row0 = n * S;
   const int64_t T = (int64_t)n_seq * S;
   const int64_t ld = (int64_t)(nh + 2 * nkv) * HD;
 
@@ -1011,28 +1036,23 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      int g = 0;  // key tiles loaded so far
-      for (int it = 0, i = item_of(0); i < n_items && ok; i = item_of(++it)) {
-        const int qb = nqb - 1 - i / per_qb, h = (i % per_qb) / n_seq, n = i % n_seq;
-        const int kh = h / (nh / nkv), row0 = n * S;
-        for (int j = 0; j <= qb; ++j, ++g) {
-          const int st = g % NKT;
-          const uint32_t u = (uint32_t)(g / NKT);
-          if (!mbar_wait(&kve[st], (u & 1) ^ 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(&kvf[st], 2 * NC * CH);
-          for (int c = 0; c < NC; ++c)
-            for (int hf = 0; hf < 2; ++hf) {
-              tma_load(&tq, &kvf[st], sK + (st * NC + c) * CH + hf * CH64, (nh + kh) * HD + 64 * c,
-                       row0 + 128 * j + 64 * hf);
-              tma_load(&tq, &kvf[st], sV + (st * NC + c) * CH + hf * CH64, (nh + nkv + kh) * HD + 64 * c,
-                       row0 + 128 * j + 64 * hf);
-            }
-          kv_inflight |= 1u << st;
-          kv_par = (kv_par & ~(1u << st)) | ((u & 1) << st);
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int st = j % NKT;
+        const uint32_t u = (uint32_t)(j / NKT);
+        if (!mbar_wait(&kve[st], (u & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
         }
+        mbar_expect_tx(&kvf[st], 2 * NC * CH);
+        for (int c = 0; c < NC; ++c)
+          for (int hf = 0; hf < 2; ++hf) {
+            tma_load(&tq, &kvf[st], sK + (st * NC + c) * CH + hf * CH64, (nh + kh) * HD + 64 * c,
+                     row0 + 128 * j + 64 * hf);
+            tma_load(&tq, &kvf[st], sV + (st * NC + c) * CH + hf * CH64, (nh + nkv + kh) * HD + 64 * c,
+                     row0 + 128 * j + 64 * hf);
+          }
+        kv_inflight |= 1u << st;
+        kv_par = (kv_par & ~(1u << st)) | ((u & 1) << st);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -1041,16 +1061,17 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      bool ok = mbar_wait(q_ready, 0, abort_flag);
       constexpr uint32_t I_S = idesc(128, 128, false, false);  // S, dP: A (Q, dO) in TMEM, B K-major over hd
       constexpr uint32_t I_G = idesc(128, HD, false, true);    // dQ: A (dS) in TMEM, B = K as MN-major
       const uint64_t dK = sdesc(su32(sK), 16, 1024), dV = sdesc(su32(sV), 16, 1024);
       const uint64_t dKm = sdesc(su32(sK), CH, 1024);
-      // Per key tile g: S(g+1) as soon as the rows have read S(g); then dQ(g),
-      // which reads dS(g) from the dP columns, then dP(g+1) over them.
-      auto issue_s = [&](int g) -> bool {  // S = Q K^T
-        const int st = g % NKT;
-        if (!mbar_wait(&kvf[st], (uint32_t)((g / NKT) & 1), abort_flag)) return false;
-        if (g > 0 && !mbar_wait(ps_free, (uint32_t)((g - 1) & 1), abort_flag)) return false;
+      // Per tile j: S(j+1) as soon as the rows have read S(j); then dQ(j),
+      // which reads dS(j) from the dP columns, then dP(j+1) over them.
+      auto issue_s = [&](int j) -> bool {  // S = Q K^T
+        const int st = j % NKT;
+        if (!mbar_wait(&kvf[st], (uint32_t)((j / NKT) & 1), abort_flag)) return false;
+        if (j > 0 && !mbar_wait(ps_free, (uint32_t)((j - 1) & 1), abort_flag)) return false;
         tc_fence_after();
         const uint64_t kd = dadv(dK, st * NC * CH);
 #pragma unroll
@@ -1059,46 +1080,36 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         tc_commit(s1_full);
         return true;
       };
-      auto issue_dp = [&](int g) {  // dP = dO V^T (its K / V stage was waited for by issue_s)
-        const uint64_t vd = dadv(dV, (g % NKT) * NC * CH);
+      auto issue_dp = [&](int j) {  // dP = dO V^T (its K / V stage was waited for by issue_s)
+        const uint64_t vd = dadv(dV, (j % NKT) * NC * CH);
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks)
           tc_mma_ts(tP, tdO + 8 * ks, dadv(vd, (ks >> 2) * CH + (ks & 3) * 32), I_S, ks != 0);
         tc_commit(s2_full);
       };
-      auto issue_g = [&](int g, bool first) -> bool {  // dQ (+)= dS K; the K / V stage is then free
-        const int st = g % NKT;
-        if (!mbar_wait(p_full, (uint32_t)(g & 1), abort_flag)) return false;
+      auto issue_g = [&](int j) -> bool {  // dQ += dS K; the K / V stage is then free
+        const int st = j % NKT;
+        if (!mbar_wait(p_full, (uint32_t)(j & 1), abort_flag)) return false;
         tc_fence_after();
         const uint64_t km = dadv(dKm, st * NC * CH);
-        const uint32_t acc0 = first ? 0u : 1u;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           tc_mma_ts(tdQ, tP + pcol(kk), dadv(km, kk * 2048), I_G, kk > 0 ? 1u : acc0);
         tc_commit(&kve[st]);
         return true;
       };
-      bool ok = true;
-      int g = 0;  // key tiles computed so far
-      for (int it = 0, i = item_of(0); i < n_items && ok; i = item_of(++it)) {
-        const int nkt = nqb - i / per_qb;  // key tiles 0 .. qb (the last one holds the diagonal)
-        // the rows have written this item's Q and dO (after reading the
-        // previous item's last S and dP, so those columns are free)
-        if (!mbar_wait(q_ready, (uint32_t)(it & 1), abort_flag) || !issue_s(g)) {
+      if (ok) ok = issue_s(0);
+      if (ok) issue_dp(0);
+      for (int j = 0; j < nkt && ok; ++j) {
+        const bool more = j + 1 < nkt;
+        if ((more && !issue_s(j + 1)) || !issue_g(j)) {
           ok = false;
           break;
         }
-        issue_dp(g);
-        for (int j = 0; j < nkt; ++j, ++g) {
-          const bool more = j + 1 < nkt;
-          if ((more && !issue_s(g + 1)) || !issue_g(g, j == 0)) {
-            ok = false;
-            break;
-          }
-          if (more) issue_dp(g + 1);
-        }
-        if (ok) tc_commit(acc_full);
+        if (more) issue_dp(j + 1);
       }
+      if (ok) tc_commit(acc_full);
       if (!ok) {
         *abort_flag = 1;
         atomicCAS(&g_attn_error, 0, 25);
@@ -1109,25 +1120,26 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     // 0..63 of a tile (and the first half of Q, dO, dQ's hd columns), warps
     // 6..9 keys 64..127 (and the second half).
     const int qw = warp & 3, half = (warp - 2) >> 2;
-    const int r = qw * 32 + lane;  // query row of the tile
+    const int r = qw * 32 + lane;  // query row
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-    // this row's half of Q and of dO of item i into TMEM (the A operands of S
-    // and dP), then the q_ready arrival
-    auto load_q = [&](int i) {
-      const int qb = nqb - 1 - i / per_qb, h = (i % per_qb) / n_seq, n = i % n_seq;
-      const int q = qb * 128 + r, row0 = n * S;
-      const bool valid = q < S;
+    const int q = q0 + r;
+    const bool valid = q < S;
+    const int64_t li = (int64_t)h * T + row0 + (valid ? q : 0);
+    const float lse2 = valid ? lse[li] * 1.4426950408889634f : 0.f;
+    const float dl = valid ? delta[li] : 0.f;
+    // this row's half of Q and of dO into TMEM (the A operands of S and dP)
+    {
       const uint4* qs = reinterpret_cast<const uint4*>(qkv + ((int64_t)row0 + (valid ? q : 0)) * ld +
-                                                       (int64_t)h * HD + half * (HD / 2));
+                                                         (int64_t)h * HD + half * (HD / 2));
       const uint4* os = reinterpret_cast<const uint4*>(dout + ((int64_t)row0 + (valid ? q : 0)) * ((int64_t)nh * HD) +
-                                                       (int64_t)h * HD + half * (HD / 2));
+                                                         (int64_t)h * HD + half * (HD / 2));
       uint32_t qv[QC / 2], ov[QC / 2];
 #pragma unroll
-      for (int k = 0; k < QC / 8; ++k) {
-        const uint4 a = valid ? qs[k] : make_uint4(0, 0, 0, 0);
-        const uint4 c = valid ? os[k] : make_uint4(0, 0, 0, 0);
-        qv[4 * k] = a.x; qv[4 * k + 1] = a.y; qv[4 * k + 2] = a.z; qv[4 * k + 3] = a.w;
-        ov[4 * k] = c.x; ov[4 * k + 1] = c.y; ov[4 * k + 2] = c.z; ov[4 * k + 3] = c.w;
+      for (int i = 0; i < QC / 8; ++i) {
+        const uint4 a = valid ? qs[i] : make_uint4(0, 0, 0, 0);
+        const uint4 c = valid ? os[i] : make_uint4(0, 0, 0, 0);
+        qv[4 * i] = a.x; qv[4 * i + 1] = a.y; qv[4 * i + 2] = a.z; qv[4 * i + 3] = a.w;
+        ov[4 * i] = c.x; ov[4 * i + 1] = c.y; ov[4 * i + 2] = c.z; ov[4 * i + 3] = c.w;
       }
       if constexpr (QC / 2 == 32) {
         tmem_st32u(tQ + lane_off + half * (QC / 2), qv);
@@ -1139,87 +1151,70 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(q_ready);
-    };
+    }
     bool ok = true;
-    int g = 0;  // key tiles seen so far
-    if (item_of(0) < n_items) load_q(item_of(0));
-    for (int it = 0, i = item_of(0); i < n_items; i = item_of(++it)) {
-      const int qb = nqb - 1 - i / per_qb, h = (i % per_qb) / n_seq, n = i % n_seq;
-      const int q0 = qb * 128, nkt = qb + 1, row0 = n * S;
-      const int q = q0 + r;
-      const bool valid = q < S;
-      const int64_t li = (int64_t)h * T + row0 + (valid ? q : 0);
-      const float lse2 = valid ? lse[li] * 1.4426950408889634f : 0.f;
-      const float dl = valid ? delta[li] : 0.f;
-      for (int j = 0; j < nkt; ++j, ++g) {
-        if (!__all_sync(0xffffffffu, mbar_wait(s1_full, (uint32_t)(g & 1), abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const int k0 = 128 * j + 64 * half;  // first key of this thread's 64 columns
-        const bool need_mask = (k0 + 63 > q0) || (k0 + 64 > S);
-        // phase 1: P from S; then S's columns are free for the next tile
-        float p[64];
-        {
-          uint32_t sv[2][32];
-          tmem_ld32_nw(tS + lane_off + half * 64, sv[0]);
-          tmem_ld32_nw(tS + lane_off + half * 64 + 32, sv[1]);
-          tmem_wait_ld2(sv[0], sv[1]);
-          const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(-lse2, -lse2);
-#pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[e >> 5][e & 31]),
-                                                      __uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31])),
-                                          sc2, nl2);
-            float pa = ex2(arg.x), pb = ex2(arg.y);
-            if (need_mask) {
-              const int key = k0 + e;
-              if (key > q || key >= S) pa = 0.f;
-              if (key + 1 > q || key + 1 >= S) pb = 0.f;
-            }
-            p[e] = pa;
-            p[e + 1] = pb;
-          }
-          tc_fence_before();
-          mbar_arrive(ps_free);
-        }
-        // phase 2: dS = P (dP - delta), back over the first 32 dP columns this thread read
-        if (!__all_sync(0xffffffffu, mbar_wait(s2_full, (uint32_t)(g & 1), abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        {
-          uint32_t dp[2][32];
-          tmem_ld32_nw(tP + lane_off + half * 64, dp[0]);
-          tmem_ld32_nw(tP + lane_off + half * 64 + 32, dp[1]);
-          tmem_wait_ld2(dp[0], dp[1]);
-          uint32_t dw[32];
-          const float2 nd2 = make_float2(-dl, -dl);
-#pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            const float2 dd = __fadd2_rn(make_float2(__uint_as_float(dp[e >> 5][e & 31]),
-                                                     __uint_as_float(dp[(e + 1) >> 5][(e + 1) & 31])),
-                                         nd2);
-            const float2 v = __fmul2_rn(make_float2(p[e], p[e + 1]), dd);
-            dw[e / 2] = pack2(v.x, v.y);
-          }
-          tmem_st32u(tP + lane_off + half * 64, dw);
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(p_full);
-        }
-      }
-      if (!ok) break;
-      // the item's last S and dP have been read, so the next item's Q and dO
-      // may go into their columns now: its first products overlap this epilogue
-      const int nxt = item_of(it + 1);
-      if (nxt < n_items) load_q(nxt);
-      if (!__all_sync(0xffffffffu, mbar_wait(acc_full, (uint32_t)(it & 1), abort_flag))) {
+    for (int j = 0; j < nkt; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(s1_full, (uint32_t)(j & 1), abort_flag))) {
         ok = false;
         break;
       }
+      tc_fence_after();
+      const int k0 = 128 * j + 64 * half;  // first key of this thread's 64 columns
+      const bool need_mask = (k0 + 63 > q0) || (k0 + 64 > S);
+      // phase 1: P from S; then S's columns are free for the next tile
+      float p[64];
+      {
+        uint32_t sv[2][32];
+        tmem_ld32_nw(tS + lane_off + half * 64, sv[0]);
+        tmem_ld32_nw(tS + lane_off + half * 64 + 32, sv[1]);
+        tmem_wait_ld2(sv[0], sv[1]);
+        const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(-lse2, -lse2);
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[e >> 5][e & 31]),
+                                                    __uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31])),
+                                        sc2, nl2);
+          float pa = ex2(arg.x), pb = ex2(arg.y);
+          if (need_mask) {
+            const int key = k0 + e;
+            if (key > q || key >= S) pa = 0.f;
+            if (key + 1 > q || key + 1 >= S) pb = 0.f;
+          }
+          p[e] = pa;
+          p[e + 1] = pb;
+        }
+        tc_fence_before();
+        mbar_arrive(ps_free);
+      }
+      // phase 2: dS = P (dP - delta), back over the first 32 dP columns this thread read
+      if (!__all_sync(0xffffffffu, mbar_wait(s2_full, (uint32_t)(j & 1), abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        uint32_t dp[2][32];
+        tmem_ld32_nw(tP + lane_off + half * 64, dp[0]);
+        tmem_ld32_nw(tP + lane_off + half * 64 + 32, dp[1]);
+        tmem_wait_ld2(dp[0], dp[1]);
+        uint32_t dw[32];
+        const float2 nd2 = make_float2(-dl, -dl);
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          const float2 dd = __fadd2_rn(make_float2(__uint_as_float(dp[e >> 5][e & 31]),
+                                                   __uint_as_float(dp[(e + 1) >> 5][(e + 1) & 31])),
+                                       nd2);
+          const float2 v = __fmul2_rn(make_float2(p[e], p[e + 1]), dd);
+          dw[e / 2] = pack2(v.x, v.y);
+        }
+        tmem_st32u(tP + lane_off + half * 64, dw);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full);
+      }
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
+    if (ok) {
       tc_fence_after();
       bf16* row = dqkv + ((int64_t)row0 + (valid ? q : 0)) * ld + (int64_t)h * HD + half * (HD / 2);
 #pragma unroll
@@ -1234,8 +1229,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
                 pack2(v[8 * i4 + 4] * scale, v[8 * i4 + 5] * scale), pack2(v[8 * i4 + 6] * scale, v[8 * i4 + 7] * scale));
         }
       }
-    }
-    if (!ok && lane == 0) {
+    } else if (lane == 0) {
       *abort_flag = 1;
       atomicCAS(&g_attn_error, 0, 26);
     }
@@ -1271,18 +1265,14 @@ void init_once() {
   g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 }
 
-// CTAs of a launch over n_items (query tile, head, sequence) items of at
-// most nqb key tiles each.  Up to 64 key tiles (S <= 8192) each CTA is
-// persistent, one per SM, so an item's set-up overlaps the previous item's
-// epilogue (S = 4096: 952 against about 870 TFLOP/s forward); longer items
-// amortise their set-up anyway, and one CTA per item lets the hardware
-// scheduler balance them dynamically (S = 32768: 1,192 against 1,138 with
-// persistent CTAs).  A CTA given one item runs exactly that item.
-int attn_grid(int64_t n_items, int nqb) {
-  if (nqb > 64) return (int)n_items;
-  const int sms = gemm_num_sms();
-  return (int)std::min<int64_t>(n_items, sms > 0 ? sms : 148);
-}
+// Forward launches with items of at most 64 key tiles (S <= 8192) use one
+// persistent CTA per SM taking items longest first, so an item's set-up
+// overlaps the previous item's epilogue (S = 4096: 972 against 887 TFLOP/s
+// with one CTA per item, same box); longer items amortise their set-up, and
+// get one CTA per item (the one-item instantiation has no cross-item waits),
+// launched head-major so the CTAs running together share one KV head's keys
+// and values in L2.
+constexpr int kPersistTiles = 64;
 
 template <int HD>
 constexpr int smem_bytes() {
@@ -1303,13 +1293,21 @@ cudaError_t launch(const bf16* qkv, int n_seq, int S, int nh, int nkv, bf16* o, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   constexpr int SM = smem_bytes<HD>();
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_k<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SM);
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_k<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_fwd_tc_k<HD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SM);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   const int64_t n_items = (int64_t)((S + 127) / 128) * nh * n_seq;
   if (n_items > 0x7fffffff) return cudaErrorInvalidValue;
-  const int grid = attn_grid(n_items, (S + 127) / 128);
-  attn_fwd_tc_k<HD><<<grid, ATTN_THREADS, SM, s>>>(m, S, nh, nkv, n_seq, o, lse, scale_log2);
+  const int nqb = (S + 127) / 128;
+  if (nqb <= kPersistTiles) {
+    const int sms = gemm_num_sms();
+    const int grid = (int)std::min<int64_t>(n_items, sms > 0 ? sms : 148);
+    attn_fwd_tc_k<HD, true><<<grid, ATTN_THREADS, SM, s>>>(m, S, nh, nkv, n_seq, o, lse, scale_log2, 0);
+  } else {
+    attn_fwd_tc_k<HD, false><<<(int)n_items, ATTN_THREADS, SM, s>>>(m, S, nh, nkv, n_seq, o, lse, scale_log2, 1);
+  }
   return cudaGetLastError();
 }
 
@@ -1343,9 +1341,8 @@ cudaError_t launch_bwd(const bf16* qkv, const bf16* dout, const float* lse, cons
                                                          scale * 1.4426950408889634f, dqkv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const unsigned gqp = (unsigned)attn_grid(gq, (int)nqb);
-  attn_bwd_q_k<HD><<<gqp, ATTN_THREADS, SQ, s>>>(mq, qkv, dout, S, n_seq, nh, nkv, lse, delta, scale,
-                                                 scale * 1.4426950408889634f, dqkv);
+  attn_bwd_q_k<HD><<<(unsigned)gq, ATTN_THREADS, SQ, s>>>(mq, qkv, dout, S, n_seq, nh, nkv, lse, delta, scale,
+                                                          scale * 1.4426950408889634f, dqkv);
   return cudaGetLastError();
 }
 
