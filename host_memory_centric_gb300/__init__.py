@@ -139,6 +139,7 @@ def lib():
         "mt_load": (i32, [_v, C.c_char_p]),
         "mt_trace_json": (i64, [_v, C.c_char_p, i64]),
         "mt_gemm": (i32, [_v, i64, i32, _v, i64, i32, i32, i32, i32, _v, i64, _v, i64, _v, i64, i32, _v]),
+        "mt_gemm_mode": (i32, [i32]),
         "mt_gemm2": (i32, [_P(_v), _P(i64), _P(i32), _P(_v), _P(i64), _P(i32), _P(i32), _P(i32), _P(i32),
                             _P(_v), _P(i64), _v]),
         "mt_rmsnorm_fwd": (i32, [_v, _v, i64, i32, f32, _v, _v, _v]),

@@ -19,6 +19,18 @@
 // descriptor), so dgrad and wgrad read activations and weights in place.
 // Every mbarrier wait is bounded; on expiry the kernel records an error code,
 // stops issuing, drains its own copies and frees its TMEM.
+//
+// Dense GEMMs default to the CTA-pair form (gemm_pair_kernel): a cluster of
+// two CTAs on neighbouring SMs owns a 256 x 256 output tile.  Each CTA loads
+// its 128 rows of A and its 128 rows of B (the B half the peer does not hold)
+// into a 6-stage ring, both CTAs' copies completing on the even CTA's full
+// barrier; the even CTA's one thread issues tcgen05.mma.cta_group::2 (M=256,
+// N=256), which reads both CTAs' shared memory and writes each CTA's 128
+// accumulator rows into its own TMEM, and its commits arrive on both CTAs'
+// barriers.  Per SM this halves the B bytes a K block moves (32 KB of operands
+// for 128 x 256 x 64 instead of 48 KB), which is what limited the one-CTA
+// form's tensor-pipe activity.  The K blocks are accumulated in the same
+// order either way, so the two forms agree bit for bit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -509,10 +521,300 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
   }
 }
 
+// ---------------------------------------------------------------- CTA-pair GEMM
+// Two CTAs of a cluster compute one 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): each CTA loads its own
+// 128 rows of A and its own 128 rows of B (the B tile's two halves) into its
+// shared memory, and the pair's even CTA issues the MMAs, which read both
+// CTAs' operands; each CTA's TMEM holds its 128 rows of the accumulator.
+// Per SM a 64-deep K block is 32 KB instead of 48 KB for the same MMA time,
+// so six stages fit where four did.  Barriers: every copy of the pair
+// completes on the even CTA's full[stage]; the MMAs' commits arrive on
+// empty[stage] and on the accumulator-full barrier of both CTAs; both CTAs'
+// epilogue threads arrive on the even CTA's accumulator-empty barrier.
+constexpr int P_STAGES = 6;
+constexpr int PA_BYTES = BM * BK * 2;         // this CTA's 128 rows of A: 16 KB
+constexpr int PB_BYTES = (BN / 2) * BK * 2;   // this CTA's 128 rows of B: 16 KB
+constexpr int P_STAGE_BYTES = PA_BYTES + PB_BYTES;
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 + 256;
+constexpr int P_GROUP_M = 8;  // 256-row tiles per raster band
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the object at the same offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(su32(p)), "r"(rank));
+  return a;
+}
+// TMA tile load into this CTA's shared memory whose completion counts on the
+// pair's barrier at shared::cluster address `bar` (the even CTA's)
+__device__ __forceinline__ void tma_load_pair(const CUtensorMap* map, uint32_t bar, void* dst, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum));
+}
+// completion of this thread's MMAs arrives on the barrier at this offset in both CTAs of the pair
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          su32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__host__ __device__ constexpr uint32_t idesc_pair(bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
+}
+// 256-row tile tm and 256-column tile tn of pair tile `tile` of a group,
+// rastered in bands of P_GROUP_M row tiles
+__device__ __forceinline__ void pair_tile_mn(int tile, const Epi& e, int& tm, int& tn) {
+  const int tiles_m = (e.M + 2 * BM - 1) / (2 * BM);
+  const int per_group = P_GROUP_M * e.tiles_n;
+  const int first = (tile / per_group) * P_GROUP_M;
+  const int gsize = min(tiles_m - first, P_GROUP_M);
+  const int in = tile % per_group;
+  tm = first + in % gsize;
+  tn = in / gsize;
+}
+
+// Producer side of one pair tile: this CTA's halves of A and B, K block by K block.
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ bool produce_pair_tile(const CUtensorMap* tmA, const CUtensorMap* tmB, int arow, int brow,
+                                                  int nk, uint8_t* sA, uint8_t* sB, uint64_t* full, uint64_t* empty,
+                                                  bool leader, int& stage, uint32_t& phase, volatile int* abort_flag,
+                                                  uint32_t& inflight_mask, uint32_t& inflight_parity) {
+  for (int kb = 0; kb < nk; ++kb) {
+    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) return false;
+    // the even CTA's full[stage] expects both CTAs' bytes
+    if (leader) mbar_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
+    const uint32_t bar = cluster_addr(&full[stage], 0);
+    uint8_t* a = sA + stage * PA_BYTES;
+    uint8_t* b = sB + stage * PB_BYTES;
+    const int k0 = kb * BK;
+    if (!A_MN) {
+      tma_load_pair(tmA, bar, a, k0, arow);
+    } else {
+      tma_load_pair(tmA, bar, a, arow, k0);
+      tma_load_pair(tmA, bar, a + CHUNK_BYTES, arow + 64, k0);
+    }
+    if (!B_MN) {
+      tma_load_pair(tmB, bar, b, k0, brow);
+    } else {
+      tma_load_pair(tmB, bar, b, brow, k0);
+      tma_load_pair(tmB, bar, b + CHUNK_BYTES, brow + 64, k0);
+    }
+    inflight_mask |= 1u << stage;
+    inflight_parity = (inflight_parity & ~(1u << stage)) | (phase << stage);
+    if (++stage == P_STAGES) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+  return true;
+}
+
+// MMA side of one pair tile (the even CTA's issuing thread).
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ bool mma_pair_tile(uint32_t d, int nk, uint8_t* sA, uint8_t* sB, uint64_t* full,
+                                              uint64_t* empty, int& stage, uint32_t& phase, volatile int* abort_flag) {
+  constexpr uint32_t ID = idesc_pair(A_MN, B_MN);
+  for (int kb = 0; kb < nk; ++kb) {
+    if (!mbar_wait(&full[stage], phase, abort_flag)) return false;
+    tc_fence_after();
+    const uint32_t a0 = su32(sA + stage * PA_BYTES), b0 = su32(sB + stage * PB_BYTES);
+#pragma unroll
+    for (int k = 0; k < BK / UMMA_K; ++k) {
+      const uint64_t ad = A_MN ? sdesc(a0 + k * UMMA_K * 128, CHUNK_BYTES, 1024) : sdesc(a0 + k * UMMA_K * 2, 16, 1024);
+      const uint64_t bd = B_MN ? sdesc(b0 + k * UMMA_K * 128, CHUNK_BYTES, 1024) : sdesc(b0 + k * UMMA_K * 2, 16, 1024);
+      tc_mma_pair(d, ad, bd, ID, (kb | k) != 0);
+    }
+    tc_commit_pair(&empty[stage]);  // the stage is free in both CTAs once these MMAs are done
+    if (++stage == P_STAGES) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+  return true;
+}
+
+template <int NG, bool A0, bool B0, bool A1, bool B1>
+__global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + P_STAGES * PA_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+  uint64_t* empty = full + P_STAGES;
+  uint64_t* tfull = empty + P_STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int cl = (int)(blockIdx.x >> 1), ncl = (int)(gridDim.x >> 1);
+  const int num_tiles = p.tile_start[NG];
+  const int split = NG > 1 ? p.tile_start[1] : num_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * 128);  // the epilogue threads of both CTAs (the even CTA's counts)
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&p.ta[0]) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&p.tb[0]) : "memory");
+    if (NG > 1) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&p.ta[1]) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&p.tb[1]) : "memory");
+    }
+  }
+  if (warp == 1) {  // one warp of each CTA of the pair allocates, together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any copy or arrival reaches them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  uint32_t inflight_mask = 0, inflight_parity = 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = cl; tile < num_tiles && ok && !p.stall; tile += ncl) {
+        int tm, tn;
+        if (NG == 1 || tile < split) {
+          pair_tile_mn(tile, p.e[0], tm, tn);
+          ok = produce_pair_tile<A0, B0>(&p.ta[0], &p.tb[0], tm * 2 * BM + (int)rank * BM, tn * BN + (int)rank * (BN / 2),
+                                         (p.e[0].K + BK - 1) / BK, sA, sB, full, empty, leader, stage, phase,
+                                         abort_flag, inflight_mask, inflight_parity);
+        } else {
+          pair_tile_mn(tile - split, p.e[1], tm, tn);
+          ok = produce_pair_tile<A1, B1>(&p.ta[1], &p.tb[1], tm * 2 * BM + (int)rank * BM, tn * BN + (int)rank * (BN / 2),
+                                         (p.e[1].K + BK - 1) / BK, sA, sB, full, empty, leader, stage, phase,
+                                         abort_flag, inflight_mask, inflight_parity);
+        }
+      }
+      if (!ok) fail(abort_flag, 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
+        const int acc = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        ++it;
+        if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        if (NG == 1 || tile < split)
+          ok = mma_pair_tile<A0, B0>(d, (p.e[0].K + BK - 1) / BK, sA, sB, full, empty, stage, phase, abort_flag);
+        else
+          ok = mma_pair_tile<A1, B1>(d, (p.e[1].K + BK - 1) / BK, sA, sB, full, empty, stage, phase, abort_flag);
+        if (!ok) break;
+        tc_commit_pair(&tfull[acc]);  // both CTAs' epilogues may read their rows
+      }
+      if (!ok) fail(abort_flag, 2);
+    }
+  } else {
+    const int q = warp & 3;  // this warp may read TMEM lanes 32q .. 32q+31
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t tempty_lead[2] = {cluster_addr(&tempty[0], 0), cluster_addr(&tempty[1], 0)};
+    int it = 0;
+    bool ok = true;
+    for (int tile = cl; tile < num_tiles; tile += ncl) {
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      ++it;
+      // warp-uniform outcome: the TMEM loads below are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const Epi& e = (NG == 1 || tile < split) ? p.e[0] : p.e[1];
+      int tm, tn;
+      pair_tile_mn((NG == 1 || tile < split) ? tile : tile - split, e, tm, tn);
+      const int row = tm * 2 * BM + (int)rank * BM + row_in_tile;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(taddr + (uint32_t)(c * 32), r);
+        const int col = tn * BN + c * 32;
+        if (row < e.M && col < e.N) epi_store(e, row, col, r);
+      }
+      tc_fence_before();
+      mbar_arrive_remote(tempty_lead[acc]);  // the even CTA counts both CTAs' epilogues
+    }
+    if (!ok && lane == 0) fail(abort_flag, 3);
+  }
+
+  // On an abort, let every copy in flight land before the pair exits: the
+  // even CTA waits for its full barriers (which count both CTAs' bytes), the
+  // odd CTA, which cannot observe its own copies, waits a fixed time.
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    const long long t0 = clock64();
+    if (leader) {
+      for (int s = 0; s < P_STAGES; ++s)
+        if (inflight_mask & (1u << s))
+          while (!mbar_test(&full[s], (inflight_parity >> s) & 1) && clock64() - t0 < kWaitCycles) {
+          }
+    }
+    while (clock64() - t0 < 400000) {  // about 0.2 ms
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still reach its shared memory or TMEM
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+  }
+}
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
 int g_num_sms = 0;
+int g_pair_clusters = 0;
 cudaError_t g_init_err = cudaSuccess;
 
 void init_once() {
@@ -539,6 +841,34 @@ void init_once() {
     const cudaError_t a = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (a != cudaSuccess) g_init_err = a;
   }
+  const void* pair_kernels[] = {(const void*)gemm_pair_kernel<1, false, false, false, false>,
+                                (const void*)gemm_pair_kernel<1, false, true, false, false>,
+                                (const void*)gemm_pair_kernel<1, true, false, false, false>,
+                                (const void*)gemm_pair_kernel<1, true, true, false, false>,
+                                (const void*)gemm_pair_kernel<2, true, true, false, true>};
+  for (const void* k : pair_kernels) {
+    const cudaError_t a = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+    if (a != cudaSuccess) g_init_err = a;
+  }
+  // pairs resident at once (an SM pair shares a TPC; the count can be below SMs / 2)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(g_num_sms & ~1));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = P_SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int nc = 0;
+  if (cudaOccupancyMaxActiveClusters(&nc, gemm_pair_kernel<1, false, false, false, false>, &cfg) != cudaSuccess ||
+      nc <= 0) {
+    cudaGetLastError();
+    nc = g_num_sms / 2;
+  }
+  g_pair_clusters = nc < g_num_sms / 2 ? nc : g_num_sms / 2;
 }
 
 // 2-D bf16 tensor map of a row-major [rows][cols] matrix with row stride ld,
@@ -573,6 +903,12 @@ inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) =
 }  // namespace
 
 std::atomic<int> g_stall_next{0};
+std::atomic<int> g_gemm_mode{1};  // dense GEMMs: 0 one CTA per 128 x 256 tile, 1 CTA pairs on 256 x 256 tiles
+int gemm_mode(int mode) {
+  const int prev = g_gemm_mode.load();
+  if (mode == 0 || mode == 1) g_gemm_mode = mode;
+  return prev;
+}
 int gemm_stall_take() {
   int v = g_stall_next.load();
   while (v > 0 && !g_stall_next.compare_exchange_weak(v, v - 1)) {
@@ -587,7 +923,8 @@ int gemm_num_sms() {
 }
 
 namespace {
-cudaError_t fill_group(const GemmArgs& g, CUtensorMap* ma, CUtensorMap* mb, Epi* e) {
+// pair: the B map's K-major box is one CTA's half of a 256-row tile
+cudaError_t fill_group(const GemmArgs& g, CUtensorMap* ma, CUtensorMap* mb, Epi* e, bool pair) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0 || !g.A || !g.B) return cudaErrorInvalidValue;
   if (!g.D && !g.acc_mode) return cudaErrorInvalidValue;
   if ((g.lda | g.ldb) % 8 || (g.D && g.ldd % 8) || (g.R && g.ldr % 8) || (g.acc_mode && g.ldacc % 8))
@@ -597,7 +934,7 @@ cudaError_t fill_group(const GemmArgs& g, CUtensorMap* ma, CUtensorMap* mb, Epi*
   if (g.acc_mode && !g.Dacc) return cudaErrorInvalidValue;
   // A: K-major [M][K] (box 64 x 128) or MN-major [K][M] (box 64 x 64)
   bool ok = g.a_mn ? make_map(ma, g.A, g.K, g.M, g.lda, BK) : make_map(ma, g.A, g.M, g.K, g.lda, BM);
-  ok = ok && (g.b_mn ? make_map(mb, g.B, g.K, g.N, g.ldb, BK) : make_map(mb, g.B, g.N, g.K, g.ldb, BN));
+  ok = ok && (g.b_mn ? make_map(mb, g.B, g.K, g.N, g.ldb, BK) : make_map(mb, g.B, g.N, g.K, g.ldb, pair ? BN / 2 : BN));
   if (!ok) return cudaErrorInvalidValue;
   e->D = g.D; e->ldd = g.ldd; e->R = g.R; e->ldr = g.ldr; e->Dacc = g.Dacc; e->ldacc = g.ldacc;
   e->acc_mode = g.acc_mode;
@@ -610,20 +947,53 @@ cudaError_t fill_group(const GemmArgs& g, CUtensorMap* ma, CUtensorMap* mb, Epi*
   return cudaSuccess;
 }
 
+template <int NG, bool A0, bool B0, bool A1, bool B1>
+cudaError_t launch_pair_kernel(const Params& p, int tiles, cudaStream_t s) {
+  const int clusters = tiles < g_pair_clusters ? tiles : g_pair_clusters;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(2 * (clusters > 0 ? clusters : 1)));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = P_SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<NG, A0, B0, A1, B1>, p);
+}
+
 cudaError_t launch(const GemmArgs* gs, int n, cudaStream_t s) {
   std::call_once(g_once, init_once);
   if (g_init_err != cudaSuccess) return g_init_err;
+  const bool pair = g_gemm_mode.load() == 1 && g_pair_clusters >= 1;
   Params p;
   std::memset(&p, 0, sizeof p);
   p.ngroups = n;
   p.tile_start[0] = 0;
   for (int i = 0; i < n; ++i) {
-    cudaError_t e = fill_group(gs[i], &p.ta[i], &p.tb[i], &p.e[i]);
+    cudaError_t e = fill_group(gs[i], &p.ta[i], &p.tb[i], &p.e[i], pair);
     if (e != cudaSuccess) return e;
-    p.tile_start[i + 1] = p.tile_start[i] + p.e[i].tiles_m * p.e[i].tiles_n;
+    const int tm = pair ? (p.e[i].M + 2 * BM - 1) / (2 * BM) : p.e[i].tiles_m;
+    p.tile_start[i + 1] = p.tile_start[i] + tm * p.e[i].tiles_n;
   }
   p.stall = gemm_stall_take();
   const int tiles = p.tile_start[n];
+  if (pair) {
+    const Epi& e = p.e[0];
+    cudaError_t r;
+    if (n == 1) {
+      if (!e.a_mn && !e.b_mn) r = launch_pair_kernel<1, false, false, false, false>(p, tiles, s);
+      else if (!e.a_mn && e.b_mn) r = launch_pair_kernel<1, false, true, false, false>(p, tiles, s);
+      else if (e.a_mn && !e.b_mn) r = launch_pair_kernel<1, true, false, false, false>(p, tiles, s);
+      else r = launch_pair_kernel<1, true, true, false, false>(p, tiles, s);
+    } else {
+      r = launch_pair_kernel<2, true, true, false, true>(p, tiles, s);
+    }
+    return r != cudaSuccess ? r : cudaGetLastError();
+  }
   const int grid = tiles < g_num_sms ? tiles : g_num_sms;
   const Epi& e = p.e[0];
   if (n == 1) {

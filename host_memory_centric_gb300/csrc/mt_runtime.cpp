@@ -2467,6 +2467,8 @@ mt_status mt_gemm(const void* A, int64_t lda, int32_t a_mn, const void* B, int64
   return cu_status(mt::gemm(g, (cudaStream_t)stream));
 }
 
+int32_t mt_gemm_mode(int32_t mode) { return mt::gemm_mode(mode); }
+
 mt_status mt_gemm2(const void* const* A, const int64_t* lda, const int32_t* a_mn, const void* const* B,
                    const int64_t* ldb, const int32_t* b_mn, const int32_t* M, const int32_t* N, const int32_t* K,
                    void* const* D, const int64_t* ldd, void* stream) {

@@ -2,7 +2,7 @@
 CUDA events on the launching stream after warm-up (inputs larger than L2
 unless the shape is small).
 
-python -m host_memory_centric_gb300.kbench gemm --M 8192 --N 11264 --K 2048 [--a-mn] [--b-mn]
+python -m host_memory_centric_gb300.kbench gemm --M 8192 --N 11264 --K 2048 [--a-mn] [--b-mn] [--gemm-mode 1]
 python -m host_memory_centric_gb300.kbench attn_fwd --S 2048 --nseq 4 --nh 16 --nkv 4 --hd 128
 python -m host_memory_centric_gb300.kbench attn_bwd --S 2048 --nseq 4 --nh 16 --nkv 4 --hd 128
 python -m host_memory_centric_gb300.kbench rmsnorm_bwd --T 8192 --H 2048
@@ -55,13 +55,17 @@ def main():
     ap.add_argument("--Fe", type=int, default=2880)
     ap.add_argument("--config", default="7.6b")
     ap.add_argument("--no-head", action="store_true", help="layer_gemms: leave out the LM-head forms")
+    ap.add_argument("--gemm-mode", type=int, default=-1,
+                    help="dense GEMM tiling: 0 one CTA per 128 x 256 tile, 1 CTA pairs per 256 x 256 tile")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     a = ap.parse_args()
     torch.manual_seed(0)
     bf = torch.bfloat16
     dev = "cuda"
-    res = {"op": a.op}
+    if a.gemm_mode >= 0:
+        ops.gemm_mode(a.gemm_mode)
+    res = {"op": a.op, "gemm_mode": ops.gemm_mode(-1)}
     if a.op == "gemm":
         A = (torch.randn(a.K, a.M) if a.a_mn else torch.randn(a.M, a.K)).to(bf).to(dev)
         B = (torch.randn(a.K, a.N) if a.b_mn else torch.randn(a.N, a.K)).to(bf).to(dev)

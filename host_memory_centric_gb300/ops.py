@@ -42,6 +42,12 @@ def gemm(A, B, M, N, K, *, a_mn=False, b_mn=False, lda=None, ldb=None, D=None, l
                       _p(Dacc), ldacc, acc_mode, _stream()))
 
 
+def gemm_mode(mode=-1) -> int:
+    """Dense GEMM tiling: 0 one CTA per 128 x 256 tile, 1 CTA pairs per
+    256 x 256 tile; -1 only reads.  Returns the previous mode."""
+    return int(_L().mt_gemm_mode(int(mode)))
+
+
 def gemm2(specs):
     """Two GEMMs in one launch; specs = two dicts with A, B, M, N, K, D and
     optional a_mn, b_mn, lda, ldb, ldd (defaults as in gemm)."""

@@ -372,6 +372,15 @@ mt_status mt_gemm(const void* A, int64_t lda, int32_t a_mn, const void* B, int64
                   int32_t b_mn, int32_t M, int32_t N, int32_t K, void* D, int64_t ldd,
                   const void* R, int64_t ldr, float* Dacc, int64_t ldacc, int32_t acc_mode,
                   void* stream);
+/* Tiling of the dense GEMMs (mt_gemm, mt_gemm2 and those of the training
+ * step) for the whole process: 0 = one CTA per 128 x 256 output tile, 1 (the
+ * default) = a pair of CTAs (one cluster, cta_group::2 MMAs) per 256 x 256
+ * tile, the operands split between the two SMs' shared memory.  The MoE
+ * grouped GEMMs always use one CTA per tile.  Both give bitwise the
+ * same results (same K order, FP32 accumulation).  Any other value changes
+ * nothing; returns the mode in force before the call.  Takes effect at the
+ * next launch; not synchronised with launches in flight on other threads. */
+int32_t mt_gemm_mode(int32_t mode);
 /* Two independent GEMMs (each as mt_gemm, arguments given as arrays of two)
  * in one persistent launch: their output tiles share one schedule. */
 mt_status mt_gemm2(const void* const* A, const int64_t* lda, const int32_t* a_mn, const void* const* B,

@@ -1,0 +1,171 @@
+"""The CTA-pair GEMM (mt_gemm_mode 1): two SMs of one cluster compute one
+256 x 256 output tile with cta_group::2 MMAs, each holding half of A's rows
+and half of B's rows in its shared memory and its 128 rows of the
+accumulator in its tensor memory.
+
+It is checked against the oracle in every operand layout on shapes that end
+in ragged tails (rows, columns and K), in the epilogue forms the training
+step uses, in the two-GEMM launch, and against the one-CTA tiling, which
+accumulates the same K blocks in the same order and must agree bit for bit.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from host_memory_centric_gb300 import configs, inputs, ops  # noqa: E402
+import host_memory_centric_gb300 as mt  # noqa: E402
+from tests.test_gpu_ops import bf, close, f64, rnd  # noqa: E402
+
+
+@pytest.fixture(autouse=True)
+def _no_kernel_errors():
+    ops.kernel_error(clear=True)
+    yield
+    torch.cuda.synchronize()
+    assert ops.kernel_error(clear=True) == 0
+
+
+@pytest.fixture
+def pair_mode():
+    prev = ops.gemm_mode(1)
+    yield
+    ops.gemm_mode(prev)
+
+
+def both_modes(fn):
+    """fn() under the one-CTA tiling and under CTA pairs."""
+    prev = ops.gemm_mode(0)
+    try:
+        a = fn()
+        ops.gemm_mode(1)
+        b = fn()
+    finally:
+        ops.gemm_mode(prev)
+    return a, b
+
+
+def test_mode_switch_reads_and_sets():
+    prev = ops.gemm_mode(-1)
+    assert prev in (0, 1)
+    assert ops.gemm_mode(1) == prev
+    assert ops.gemm_mode(7) == 1  # ignored
+    assert ops.gemm_mode(prev) == 1
+    assert ops.gemm_mode(-1) == prev
+
+
+def test_single_pair_tile(orc, pair_mode):
+    """One 256 x 256 tile, one K block: the smallest case of the pair."""
+    M = N = 256
+    K = 64
+    A = rnd((M, K), 1); B = rnd((N, K), 2)
+    D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    ops.gemm(bf(A), bf(B), M, N, K, D=D)
+    close(f64(D), orc.linear_fwd(f64(bf(A)), f64(bf(B))), rel=5e-3)
+
+
+def _majors_case(a_mn, b_mn, M, N, K, seed):
+    A = rnd((M, K), seed); B = rnd((N, K), seed + 1)
+    pad = lambda n: (n + 7) // 8 * 8
+    if a_mn:
+        At = np.zeros((K, pad(M)), np.float32); At[:, :M] = A.T
+        Ag, lda = bf(At), pad(M)
+    else:
+        Ag, lda = bf(A), K
+    if b_mn:
+        Bt = np.zeros((K, pad(N)), np.float32); Bt[:, :N] = B.T
+        Bg, ldb = bf(Bt), pad(N)
+    else:
+        Bg, ldb = bf(B), K
+
+    def run():
+        D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        ops.gemm(Ag, Bg, M, N, K, a_mn=a_mn, b_mn=b_mn, lda=lda, ldb=ldb, D=D)
+        torch.cuda.synchronize()
+        return D
+
+    return A, B, run
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (300, 520, 200), (128, 136, 64), (1000, 264, 1032),
+                                   (520, 1800, 328)])
+def test_pair_majors_against_oracle_and_one_cta(orc, a_mn, b_mn, M, N, K):
+    """M = 128 and 300 leave the odd CTA of a pair with no rows or a few;
+    N = 136 and 264 leave it no columns of B or a few."""
+    A, B, run = _majors_case(a_mn, b_mn, M, N, K, 3 * M + N)
+    one, two = both_modes(run)
+    close(f64(two), orc.linear_fwd(f64(bf(A)), f64(bf(B))), rel=5e-3)
+    assert torch.equal(one, two)
+
+
+def test_pair_many_tiles_long_k(orc):
+    """More pair tiles than resident pairs and 64 K blocks (the persistent
+    loop wraps the stage ring many times); sampled rows against the oracle."""
+    M, N, K = 4352, 2816, 4096  # 17 x 11 pair tiles
+    A = rnd((M, K), 5, 0.5); B = rnd((N, K), 6, 0.5)
+    Ag, Bg = bf(A), bf(B)
+
+    def run():
+        D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        ops.gemm(Ag, Bg, M, N, K, D=D)
+        torch.cuda.synchronize()
+        return D
+
+    one, two = both_modes(run)
+    assert torch.equal(one, two)
+    rows = np.random.default_rng(7).choice(M, 24, replace=False)
+    close(f64(two)[rows], orc.linear_fwd(f64(Ag)[rows], f64(Bg)), rel=5e-3)
+
+
+def test_pair_residual_and_fp32_accumulate(orc, pair_mode):
+    M, N, K = 300, 296, 136
+    A1, A2, B, R = rnd((M, K), 6), rnd((M, K), 7), rnd((N, K), 8), rnd((M, N), 9)
+    D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    acc = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    ops.gemm(bf(A1), bf(B), M, N, K, Dacc=acc, acc_mode=1)
+    ops.gemm(bf(A2), bf(B), M, N, K, D=D, R=bf(R), Dacc=acc, acc_mode=2)
+    ref = orc.linear_fwd(f64(bf(A1)), f64(bf(B))) + orc.linear_fwd(f64(bf(A2)), f64(bf(B)))
+    close(acc.double().cpu().numpy(), ref, rel=1e-5, elem_rtol=1e-5, atol=1e-4)
+    close(f64(D), ref + f64(bf(R)), rel=5e-3)
+
+
+def test_pair_wgrad_dgrad_in_one_launch(orc):
+    T, N, K = 320, 264, 200
+    dY = rnd((T, N), 30); X = rnd((T, K), 31); W = rnd((N, K), 32)
+    dYg, Xg, Wg = bf(dY), bf(X), bf(W)
+
+    def run():
+        dW = torch.empty(N, K, dtype=torch.bfloat16, device="cuda")
+        dX = torch.empty(T, K, dtype=torch.bfloat16, device="cuda")
+        ops.gemm2([dict(A=dYg, B=Xg, M=N, N=K, K=T, a_mn=1, b_mn=1, lda=N, ldb=K, D=dW),
+                   dict(A=dYg, B=Wg, M=T, N=K, K=N, b_mn=1, ldb=K, D=dX)])
+        torch.cuda.synchronize()
+        return dW, dX
+
+    (dW1, dX1), (dW2, dX2) = both_modes(run)
+    close(f64(dW2), orc.linear_wgrad(f64(dYg), f64(Xg)), rel=5e-3)
+    close(f64(dX2), orc.linear_dgrad(f64(dYg), f64(Wg)), rel=5e-3)
+    assert torch.equal(dW1, dW2) and torch.equal(dX1, dX2)
+
+
+def test_training_step_identical_under_pairs():
+    """A whole training step (dense GEMMs of every visit) gives the same loss
+    and the same updated parameters bit for bit under either tiling."""
+    c = configs.get("tiny", n_layers=2)
+    tok = inputs.tokens_for(c, 0)
+
+    def run():
+        m = mt.Model(c, seed=11)
+        m.set_tokens(tok)
+        loss = m.train_step(0)
+        m.sync()
+        w = [m.read(j, mt.REGION_MASTER) for j in range(len(m.layout))]
+        m.close()
+        return loss, w
+
+    (l1, w1), (l2, w2) = both_modes(run)
+    assert l1 == l2
+    for a, b in zip(w1, w2):
+        assert np.array_equal(a, b)
