@@ -31,6 +31,16 @@
 // for 128 x 256 x 64 instead of 48 KB), which is what limited the one-CTA
 // form's tensor-pipe activity.  The K blocks are accumulated in the same
 // order either way, so the two forms agree bit for bit.
+//
+// Tile order of the pairs: output tiles are rastered in bands of `group_m`
+// 256-row tiles (chosen per launch from K, so that the operand slices of the
+// tiles in flight fit in about half the L2), and each pair, after its first
+// tile, draws the next from a per-launch counter.  The tiles in flight thus
+// stay a window of consecutive tiles however unevenly the SMs progress, and
+// tiles that share an operand slice read it from L2 rather than DRAM.  The
+// even CTA's producer thread draws the tile (one tile ahead) and passes it
+// through a 4-entry ring in shared memory to its MMA thread, to the odd
+// CTA's producer and to both CTAs' epilogue warps.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -85,6 +95,7 @@ struct Params {
   int tile_start[3];  // tiles of group g are [tile_start[g], tile_start[g+1])
   int stall;          // test hook: the producer issues nothing, so the consumers' bounded waits run out
   const int* tile_expert;
+  int* tile_ctr;      // CTA pairs: the launch's tile-ticket counter (zero on entry, reset by the last draw)
   int64_t d_estride;
   int ngrp;
   int grp_e[MAX_EXPERT_GROUPS], grp_k0[MAX_EXPERT_GROUPS], grp_nk[MAX_EXPERT_GROUPS];
@@ -537,7 +548,6 @@ constexpr int PA_BYTES = BM * BK * 2;         // this CTA's 128 rows of A: 16 KB
 constexpr int PB_BYTES = (BN / 2) * BK * 2;   // this CTA's 128 rows of B: 16 KB
 constexpr int P_STAGE_BYTES = PA_BYTES + PB_BYTES;
 constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 + 256;
-constexpr int P_GROUP_M = 8;  // 256-row tiles per raster band
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -586,12 +596,12 @@ __host__ __device__ constexpr uint32_t idesc_pair(bool a_mn, bool b_mn) {
          ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
 }
 // 256-row tile tm and 256-column tile tn of pair tile `tile` of a group,
-// rastered in bands of P_GROUP_M row tiles
+// rastered in bands of e.group_m row tiles
 __device__ __forceinline__ void pair_tile_mn(int tile, const Epi& e, int& tm, int& tn) {
   const int tiles_m = (e.M + 2 * BM - 1) / (2 * BM);
-  const int per_group = P_GROUP_M * e.tiles_n;
-  const int first = (tile / per_group) * P_GROUP_M;
-  const int gsize = min(tiles_m - first, P_GROUP_M);
+  const int per_group = e.group_m * e.tiles_n;
+  const int first = (tile / per_group) * e.group_m;
+  const int gsize = min(tiles_m - first, e.group_m);
   const int in = tile % per_group;
   tm = first + in % gsize;
   tn = in / gsize;
@@ -657,6 +667,36 @@ __device__ __forceinline__ bool mma_pair_tile(uint32_t d, int nk, uint8_t* sA, u
   return true;
 }
 
+constexpr int P_TRING = 4;  // tile ids in flight between the pair's producer and its consumers
+// consumers that release a tile-id slot on the even CTA: its MMA thread, the odd CTA's
+// producer and lane 0 of the four epilogue warps of each CTA
+constexpr int P_TID_CONSUMERS = 1 + 1 + 2 * 4;
+
+__device__ __forceinline__ bool mbar_test_cl(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded wait whose acquire covers writes the peer CTA released to this barrier
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_test_cl(b, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_test_cl(b, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+}
+__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 template <int NG, bool A0, bool B0, bool A1, bool B1>
 __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -667,8 +707,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
   uint64_t* empty = full + P_STAGES;
   uint64_t* tfull = empty + P_STAGES;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tid_full = tempty + 2;
+  uint64_t* tid_empty = tid_full + P_TRING;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tid_empty + P_TRING);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* tid_ring = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -685,6 +728,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 2 * 128);  // the epilogue threads of both CTAs (the even CTA's counts)
+    }
+    for (int r = 0; r < P_TRING; ++r) {
+      mbar_init(&tid_full[r], 1);
+      mbar_init(&tid_empty[r], P_TID_CONSUMERS);  // the even CTA's counts
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -708,12 +755,56 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
 
   uint32_t inflight_mask = 0, inflight_parity = 0;
 
+  // Tile order: the pair's first tile is its cluster index; every later one is
+  // a ticket drawn from the launch's counter (tile ncl + ticket), so the tiles
+  // in flight are always a window of consecutive tiles of the raster order,
+  // whatever the speed of each SM.  Every cluster draws until it gets a ticket
+  // past the last tile; exactly ncl such tickets exist, and the cluster that
+  // draws the very last one resets the counter for the launch that next uses it.
   if (warp == 0) {
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = cl; tile < num_tiles && ok && !p.stall; tile += ncl) {
+      const int tickets = (num_tiles > ncl ? num_tiles - ncl : 0) + ncl;
+      int ahead = -1;  // the ticket drawn one tile ahead (its latency hides behind the current tile's loads)
+      for (int i = 0; ok && !p.stall; ++i) {
+        const int slot = i % P_TRING;
+        const uint32_t ph = (uint32_t)(i / P_TRING) & 1;
+        int tile;
+        if (leader) {
+          if (!mbar_wait(&tid_empty[slot], ph ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (!p.tile_ctr) {  // static order: every ncl-th tile
+            tile = cl + i * ncl < num_tiles ? cl + i * ncl : -1;
+          } else if (i == 0 && cl < num_tiles) {
+            tile = cl;
+          } else {
+            const int raw = ahead >= 0 ? ahead : atomicAdd(p.tile_ctr, 1);
+            ahead = -1;
+            if (raw >= tickets) {  // a counter left behind by an aborted launch
+              ok = false;
+              break;
+            }
+            if (raw == tickets - 1) atomicExch(p.tile_ctr, 0);
+            tile = ncl + raw < num_tiles ? ncl + raw : -1;
+          }
+          if (tile >= 0 && p.tile_ctr) ahead = atomicAdd(p.tile_ctr, 1);
+          tid_ring[slot] = tile;
+          st_cluster_s32(cluster_addr((const void*)&tid_ring[slot], 1), tile);
+          mbar_arrive(&tid_full[slot]);
+          mbar_arrive_remote(cluster_addr(&tid_full[slot], 1));
+        } else {
+          if (!mbar_wait_cl(&tid_full[slot], ph, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tile = tid_ring[slot];
+          mbar_arrive_remote(cluster_addr(&tid_empty[slot], 0));
+        }
+        if (tile < 0) break;
         int tm, tn;
         if (NG == 1 || tile < split) {
           pair_tile_mn(tile, p.e[0], tm, tn);
@@ -733,12 +824,18 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
     if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
-      int it = 0;
       bool ok = true;
-      for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
+      for (int it = 0;; ++it) {
+        const int slot = it % P_TRING;
+        if (!mbar_wait(&tid_full[slot], (uint32_t)(it / P_TRING) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int tile = tid_ring[slot];
+        mbar_arrive(&tid_empty[slot]);
+        if (tile < 0) break;
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
-        ++it;
         if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag)) {
           ok = false;
           break;
@@ -758,13 +855,20 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
     const int q = warp & 3;  // this warp may read TMEM lanes 32q .. 32q+31
     const int row_in_tile = q * 32 + lane;
     const uint32_t tempty_lead[2] = {cluster_addr(&tempty[0], 0), cluster_addr(&tempty[1], 0)};
-    int it = 0;
     bool ok = true;
-    for (int tile = cl; tile < num_tiles; tile += ncl) {
+    for (int it = 0;; ++it) {
+      const int slot = it % P_TRING;
+      // warp-uniform outcomes: the TMEM loads below are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait_cl(&tid_full[slot], (uint32_t)(it / P_TRING) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      const int tile = tid_ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(cluster_addr(&tid_empty[slot], 0));
+      if (tile < 0) break;
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      ++it;
-      // warp-uniform outcome: the TMEM loads below are warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, abort_flag))) {
         ok = false;
         break;
@@ -815,6 +919,9 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
 int g_num_sms = 0;
 int g_pair_clusters = 0;
+constexpr int kTileCounters = 1024;  // tile-ticket counters, one per pair launch in a ring
+int* g_tile_ctrs = nullptr;
+std::atomic<unsigned> g_tile_ctr_next{0};
 cudaError_t g_init_err = cudaSuccess;
 
 void init_once() {
@@ -869,6 +976,11 @@ void init_once() {
     nc = g_num_sms / 2;
   }
   g_pair_clusters = nc < g_num_sms / 2 ? nc : g_num_sms / 2;
+  if (cudaMalloc(&g_tile_ctrs, kTileCounters * sizeof(int)) != cudaSuccess ||
+      cudaMemset(g_tile_ctrs, 0, kTileCounters * sizeof(int)) != cudaSuccess) {
+    g_init_err = cudaErrorMemoryAllocation;
+    g_tile_ctrs = nullptr;
+  }
 }
 
 // 2-D bf16 tensor map of a row-major [rows][cols] matrix with row stride ld,
@@ -903,10 +1015,12 @@ inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) =
 }  // namespace
 
 std::atomic<int> g_stall_next{0};
-std::atomic<int> g_gemm_mode{1};  // dense GEMMs: 0 one CTA per 128 x 256 tile, 1 CTA pairs on 256 x 256 tiles
+// dense GEMMs: 0 one CTA per 128 x 256 tile; CTA pairs on 256 x 256 tiles,
+// 1 drawing tiles from a counter, 2 taking every ncl-th tile in raster order
+std::atomic<int> g_gemm_mode{1};
 int gemm_mode(int mode) {
   const int prev = g_gemm_mode.load();
-  if (mode == 0 || mode == 1) g_gemm_mode = mode;
+  if (mode >= 0 && mode <= 2) g_gemm_mode = mode;
   return prev;
 }
 int gemm_stall_take() {
@@ -947,6 +1061,25 @@ cudaError_t fill_group(const GemmArgs& g, CUtensorMap* ma, CUtensorMap* mb, Epi*
   return cudaSuccess;
 }
 
+// Raster band of the CTA-pair tiles, in 256-row tiles.  The tiles in flight
+// are a window of about `pairs` consecutive tiles: `band` row tiles by
+// pairs / band column tiles, whose operand slices (256 rows by the whole K,
+// BF16) should stay in L2 while the window passes, so that the column
+// operand is read from DRAM once per band.  The tallest band whose window
+// fits about half the L2 is taken (fewer bands, fewer re-reads of the column
+// operand); when no band fits (long K), a square window (8 rows) keeps the
+// slices the window's tiles share to a minimum.
+int pair_band(int K, int pairs) {
+  const double slice = 2.0 * BM * 2.0 * K;  // bytes of one 256-row operand slice
+  const double budget = 64e6;
+  int best = 8;
+  for (int band = 16; band <= 64; band *= 2) {
+    const int cols = (pairs + band - 1) / band;
+    if ((band + cols + 1) * slice <= budget) best = band;
+  }
+  return best;
+}
+
 template <int NG, bool A0, bool B0, bool A1, bool B1>
 cudaError_t launch_pair_kernel(const Params& p, int tiles, cudaStream_t s) {
   const int clusters = tiles < g_pair_clusters ? tiles : g_pair_clusters;
@@ -968,7 +1101,8 @@ cudaError_t launch_pair_kernel(const Params& p, int tiles, cudaStream_t s) {
 cudaError_t launch(const GemmArgs* gs, int n, cudaStream_t s) {
   std::call_once(g_once, init_once);
   if (g_init_err != cudaSuccess) return g_init_err;
-  const bool pair = g_gemm_mode.load() == 1 && g_pair_clusters >= 1;
+  const int mode = g_gemm_mode.load();
+  const bool pair = mode != 0 && g_pair_clusters >= 1;
   Params p;
   std::memset(&p, 0, sizeof p);
   p.ngroups = n;
@@ -976,12 +1110,14 @@ cudaError_t launch(const GemmArgs* gs, int n, cudaStream_t s) {
   for (int i = 0; i < n; ++i) {
     cudaError_t e = fill_group(gs[i], &p.ta[i], &p.tb[i], &p.e[i], pair);
     if (e != cudaSuccess) return e;
+    if (pair) p.e[i].group_m = pair_band(p.e[i].K, g_pair_clusters);
     const int tm = pair ? (p.e[i].M + 2 * BM - 1) / (2 * BM) : p.e[i].tiles_m;
     p.tile_start[i + 1] = p.tile_start[i] + tm * p.e[i].tiles_n;
   }
   p.stall = gemm_stall_take();
   const int tiles = p.tile_start[n];
   if (pair) {
+    if (mode == 1) p.tile_ctr = g_tile_ctrs + (g_tile_ctr_next.fetch_add(1) % kTileCounters);
     const Epi& e = p.e[0];
     cudaError_t r;
     if (n == 1) {
@@ -1099,6 +1235,13 @@ cudaError_t kernel_error_read(int* code, int clear) {
     const int z = 0;
     e = cudaMemcpyToSymbol(g_kernel_error, &z, sizeof(int));
     if (e != cudaSuccess) return e;
+    // a GEMM that gave up may have left its tile-ticket counter mid-count
+    if (*code != 0 && g_tile_ctrs) {
+      e = cudaDeviceSynchronize();
+      if (e == cudaSuccess) e = cudaMemset(g_tile_ctrs, 0, kTileCounters * sizeof(int));
+      if (e == cudaSuccess) e = cudaDeviceSynchronize();
+      if (e != cudaSuccess) return e;
+    }
   }
   int a = 0;
   e = attention_error_read(&a, clear);

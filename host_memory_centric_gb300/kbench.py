@@ -56,7 +56,8 @@ def main():
     ap.add_argument("--config", default="7.6b")
     ap.add_argument("--no-head", action="store_true", help="layer_gemms: leave out the LM-head forms")
     ap.add_argument("--gemm-mode", type=int, default=-1,
-                    help="dense GEMM tiling: 0 one CTA per 128 x 256 tile, 1 CTA pairs per 256 x 256 tile")
+                    help="dense GEMM tiling: 0 one CTA per 128 x 256 tile; CTA pairs per 256 x 256 tile, "
+                         "1 drawing tiles from a counter, 2 every n-th tile")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     a = ap.parse_args()

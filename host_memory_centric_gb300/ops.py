@@ -43,8 +43,9 @@ def gemm(A, B, M, N, K, *, a_mn=False, b_mn=False, lda=None, ldb=None, D=None, l
 
 
 def gemm_mode(mode=-1) -> int:
-    """Dense GEMM tiling: 0 one CTA per 128 x 256 tile, 1 CTA pairs per
-    256 x 256 tile; -1 only reads.  Returns the previous mode."""
+    """Dense GEMM tiling: 0 one CTA per 128 x 256 tile; 1 CTA pairs per
+    256 x 256 tile drawing tiles from a counter, 2 CTA pairs taking every
+    n-th tile; -1 only reads.  Returns the previous mode."""
     return int(_L().mt_gemm_mode(int(mode)))
 
 

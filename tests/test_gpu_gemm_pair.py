@@ -6,7 +6,10 @@ accumulator in its tensor memory.
 It is checked against the oracle in every operand layout on shapes that end
 in ragged tails (rows, columns and K), in the epilogue forms the training
 step uses, in the two-GEMM launch, and against the one-CTA tiling, which
-accumulates the same K blocks in the same order and must agree bit for bit.
+accumulates the same K blocks in the same order and must agree bit for bit;
+both tile orders of the pair (tiles drawn from a per-launch counter, and
+every n-th tile) are run.  Many successive launches reuse the counters, which
+the last draw of each launch resets.
 """
 import numpy as np
 import pytest
@@ -34,24 +37,27 @@ def pair_mode():
     ops.gemm_mode(prev)
 
 
-def both_modes(fn):
-    """fn() under the one-CTA tiling and under CTA pairs."""
-    prev = ops.gemm_mode(0)
+def all_modes(fn):
+    """fn() under the one-CTA tiling (mode 0), CTA pairs drawing tiles from a
+    counter (1) and CTA pairs in static order (2)."""
+    prev = ops.gemm_mode(-1)
+    out = []
     try:
-        a = fn()
-        ops.gemm_mode(1)
-        b = fn()
+        for mode in (0, 1, 2):
+            ops.gemm_mode(mode)
+            out.append(fn())
     finally:
         ops.gemm_mode(prev)
-    return a, b
+    return out
 
 
 def test_mode_switch_reads_and_sets():
     prev = ops.gemm_mode(-1)
     assert prev in (0, 1)
     assert ops.gemm_mode(1) == prev
-    assert ops.gemm_mode(7) == 1  # ignored
-    assert ops.gemm_mode(prev) == 1
+    assert ops.gemm_mode(2) == 1
+    assert ops.gemm_mode(7) == 2  # ignored
+    assert ops.gemm_mode(prev) == 2
     assert ops.gemm_mode(-1) == prev
 
 
@@ -95,9 +101,30 @@ def test_pair_majors_against_oracle_and_one_cta(orc, a_mn, b_mn, M, N, K):
     """M = 128 and 300 leave the odd CTA of a pair with no rows or a few;
     N = 136 and 264 leave it no columns of B or a few."""
     A, B, run = _majors_case(a_mn, b_mn, M, N, K, 3 * M + N)
-    one, two = both_modes(run)
+    one, two, static = all_modes(run)
     close(f64(two), orc.linear_fwd(f64(bf(A)), f64(bf(B))), rel=5e-3)
-    assert torch.equal(one, two)
+    assert torch.equal(one, two) and torch.equal(one, static)
+
+
+def test_counter_reuse_over_many_launches(orc, pair_mode):
+    """More launches than there are tile counters (1024): every launch finds
+    its counter at zero, so every output tile is computed each time."""
+    M, N, K = 520, 776, 64  # 3 x 4 pair tiles
+    A = rnd((M, K), 11); B = rnd((N, K), 12)
+    Ag, Bg = bf(A), bf(B)
+    ref = orc.linear_fwd(f64(Ag), f64(Bg))
+    D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    first = None
+    for i in range(1100):
+        D.fill_(float("nan"))
+        ops.gemm(Ag, Bg, M, N, K, D=D)
+        if i in (0, 1023, 1024, 1099):
+            torch.cuda.synchronize()
+            assert not torch.isnan(D).any(), i
+            if first is None:
+                first = D.clone()
+                close(f64(D), ref, rel=5e-3)
+            assert torch.equal(D, first), i
 
 
 def test_pair_many_tiles_long_k(orc):
@@ -113,8 +140,8 @@ def test_pair_many_tiles_long_k(orc):
         torch.cuda.synchronize()
         return D
 
-    one, two = both_modes(run)
-    assert torch.equal(one, two)
+    one, two, static = all_modes(run)
+    assert torch.equal(one, two) and torch.equal(one, static)
     rows = np.random.default_rng(7).choice(M, 24, replace=False)
     close(f64(two)[rows], orc.linear_fwd(f64(Ag)[rows], f64(Bg)), rel=5e-3)
 
@@ -144,10 +171,11 @@ def test_pair_wgrad_dgrad_in_one_launch(orc):
         torch.cuda.synchronize()
         return dW, dX
 
-    (dW1, dX1), (dW2, dX2) = both_modes(run)
+    (dW1, dX1), (dW2, dX2), (dW3, dX3) = all_modes(run)
     close(f64(dW2), orc.linear_wgrad(f64(dYg), f64(Xg)), rel=5e-3)
     close(f64(dX2), orc.linear_dgrad(f64(dYg), f64(Wg)), rel=5e-3)
     assert torch.equal(dW1, dW2) and torch.equal(dX1, dX2)
+    assert torch.equal(dW1, dW3) and torch.equal(dX1, dX3)
 
 
 def test_training_step_identical_under_pairs():
@@ -165,7 +193,7 @@ def test_training_step_identical_under_pairs():
         m.close()
         return loss, w
 
-    (l1, w1), (l2, w2) = both_modes(run)
-    assert l1 == l2
-    for a, b in zip(w1, w2):
-        assert np.array_equal(a, b)
+    (l1, w1), (l2, w2), (l3, w3) = all_modes(run)
+    assert l1 == l2 == l3
+    for a, b, c3 in zip(w1, w2, w3):
+        assert np.array_equal(a, b) and np.array_equal(a, c3)
