@@ -36,6 +36,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "mt_kernels.h"
 
@@ -456,78 +457,84 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         tmem_ld32_nw(tS(b) + lane_off + half * 64, sr[0]);
         tmem_ld32_nw(tS(b) + lane_off + half * 64 + 32, sr[1]);
         tmem_wait_ld2(sr[0], sr[1]);
-        // raw scores (masked ones -inf); the exp2-domain scale enters once, in
-        // the max and in one FMA per score before ex2 (scale_log2 > 0)
-        float sv[64];
         const int kbase = 128 * j + 64 * half;
-        // only the diagonal tile and a tile crossing the sequence end need masking
+        // only the diagonal tile and a tile crossing the sequence end need
+        // masking; the rest of the tile's row work is instantiated twice, so
+        // that the common unmasked tiles carry no per-element mask code
+        auto row_tile = [&](auto masked) -> bool {
+          // raw scores (masked ones -inf); the exp2-domain scale enters once, in
+          // the max and in one FMA per score before ex2 (scale_log2 > 0)
+          float sv[64];
+          if constexpr (decltype(masked)::value) {
+#pragma unroll
+            for (int k = 0; k < 64; ++k) {
+              const int key = kbase + k;
+              sv[k] = (key > qpos || key >= S) ? -INFINITY : __uint_as_float(sr[k >> 5][k & 31]);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 64; ++k) sv[k] = __uint_as_float(sr[k >> 5][k & 31]);
+          }
+          // eight independent chains instead of one 64-long dependency chain
+          float mx8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx8[k] = sv[k];
+#pragma unroll
+          for (int k = 8; k < 64; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], sv[k]);
+          const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * scale_log2;
+          // lazy base: move it only when this tile's max exceeds it by more than
+          // 2^8 (always on the first tile with a key); P = 2^(s - base) <= 2^8
+          const bool move = mx > m_used + 8.f;
+          const float alpha = move ? ex2(m_used - mx) : 1.f;  // 0 when m_used = -inf
+          if (move) {
+            m_used = mx;
+            l *= alpha;
+          }
+          // O_half of rows whose base moved is rescaled once the previous P V has
+          // landed in it (warp-collective TMEM traffic: the whole warp joins)
+          if (j > 0 && __any_sync(0xffffffffu, move)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)((g - 1) & 1), abort_flag))) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+              float t[32];
+              tmem_ld32(tO(half) + lane_off + c * 32, t);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) t[k] *= alpha;
+              tmem_st32(tO(half) + lane_off + c * 32, t);
+            }
+          }
+          const float base = m_used == -INFINITY ? 0.f : m_used;
+          // paired FP32 arithmetic (two lanes per instruction, each rounded as
+          // the scalar form) for the exponent arguments and the sums
+          const float2 sc2 = make_float2(scale_log2, scale_log2), nb2 = make_float2(-base, -base);
+          float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
+          uint32_t pw[32];
+#pragma unroll
+          for (int k = 0; k < 64; k += 2) {
+            const float2 e = __ffma2_rn(make_float2(sv[k], sv[k + 1]), sc2, nb2);
+            const float2 p = make_float2(ex2(e.x), ex2(e.y));
+            sum2[(k >> 1) & 3] = __fadd2_rn(sum2[(k >> 1) & 3], p);
+            pw[k >> 1] = pack2(p.x, p.y);
+          }
+          const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
+          const float2 st = __fadd2_rn(s01, s23);
+          l += st.x + st.y;
+          // P_g (BF16 pairs) over this half's first 32 columns of S_g, which this
+          // thread has already read: the A operand of the next O += P V
+          tmem_st32u(tS(b) + lane_off + half * 64, pw);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&p_full[b]);
+          return true;
+        };
         const bool need_mask = (kbase + 63 > q0) || (kbase + 64 > S);
-        if (need_mask) {
-#pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const int key = kbase + k;
-            sv[k] = (key > qpos || key >= S) ? -INFINITY : __uint_as_float(sr[k >> 5][k & 31]);
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 64; ++k) sv[k] = __uint_as_float(sr[k >> 5][k & 31]);
+        if (!(need_mask ? row_tile(std::true_type{}) : row_tile(std::false_type{}))) {
+          ok = false;
+          break;
         }
-        // eight independent chains instead of one 64-long dependency chain
-        float mx8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = sv[k];
-#pragma unroll
-        for (int k = 8; k < 64; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], sv[k]);
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * scale_log2;
-        // lazy base: move it only when this tile's max exceeds it by more than
-        // 2^8 (always on the first tile with a key); P = 2^(s - base) <= 2^8
-        const bool move = mx > m_used + 8.f;
-        const float alpha = move ? ex2(m_used - mx) : 1.f;  // 0 when m_used = -inf
-        if (move) {
-          m_used = mx;
-          l *= alpha;
-        }
-        // O_half of rows whose base moved is rescaled once the previous P V has
-        // landed in it (warp-collective TMEM traffic: the whole warp joins)
-        if (j > 0 && __any_sync(0xffffffffu, move)) {
-          if (!__all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)((g - 1) & 1), abort_flag))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            float t[32];
-            tmem_ld32(tO(half) + lane_off + c * 32, t);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) t[k] *= alpha;
-            tmem_st32(tO(half) + lane_off + c * 32, t);
-          }
-        }
-        const float base = m_used == -INFINITY ? 0.f : m_used;
-        // paired FP32 arithmetic (two lanes per instruction, each rounded as
-        // the scalar form) for the exponent arguments and the sums
-        const float2 sc2 = make_float2(scale_log2, scale_log2), nb2 = make_float2(-base, -base);
-        float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                          make_float2(0.f, 0.f)};
-        uint32_t pw[32];
-#pragma unroll
-        for (int k = 0; k < 64; k += 2) {
-          const float2 e = __ffma2_rn(make_float2(sv[k], sv[k + 1]), sc2, nb2);
-          const float2 p = make_float2(ex2(e.x), ex2(e.y));
-          sum2[(k >> 1) & 3] = __fadd2_rn(sum2[(k >> 1) & 3], p);
-          pw[k >> 1] = pack2(p.x, p.y);
-        }
-        const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
-        const float2 st = __fadd2_rn(s01, s23);
-        l += st.x + st.y;
-        // P_g (BF16 pairs) over this half's first 32 columns of S_g, which this
-        // thread has already read: the A operand of the next O += P V
-        tmem_st32u(tS(b) + lane_off + half * 64, pw);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&p_full[b]);
       }
       if (!ok) break;
       const float m_old = m_used;
@@ -662,8 +669,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   uint8_t* sV = sK + NC * CH;
   uint8_t* sQ = sV + NC * CH;        // NQT stages of [128 q][HD]
   uint8_t* sO = sQ + NQT * NC * CH;  // dO, the same
-  float* ls = reinterpret_cast<float*>(sO + NQT * NC * CH);  // [2][128] lse log2e of the tile
-  float* dls = ls + 256;                                      // [2][128] delta of the tile
+  float* ls = reinterpret_cast<float*>(sO + NQT * NC * CH);  // [2][128] -lse log2e of the tile
+  float* dls = ls + 256;                                      // [2][128] -delta of the tile
   uint64_t* bars = reinterpret_cast<uint64_t*>(dls + 256);
   uint64_t* kv_full = bars;
   uint64_t* qf = bars + 1;           // [NQT] Q / dO tile loaded
@@ -836,7 +843,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       const int h = g * grp + i / per_head, q = (kb + i % per_head) * 128 + (t & 127);
       if (q >= S) return 0.f;
       const int64_t idx = (int64_t)h * T + row0 + q;
-      return t < 128 ? lse[idx] * 1.4426950408889634f : delta[idx];
+      return t < 128 ? -(lse[idx] * 1.4426950408889634f) : -delta[idx];  // staged negated
     };
     bool ok = true;
     float nxt = fetch(0);  // one tile ahead, so the global load latency hides behind a tile
@@ -868,27 +875,35 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         tmem_wait_ld2(sv[0], sv[1]);
         uint32_t pw[32];
         const float2 sc2 = make_float2(scale_log2, scale_log2);
+        // two instantiations, so that tiles without masked entries (all but
+        // the diagonal and the sequence end) carry no per-element mask code
+        auto exps = [&](auto masked) {
 #pragma unroll
-        for (int e4 = 0; e4 < 16; ++e4) {
-          const float4 l4 = lrow[e4];
+          for (int e4 = 0; e4 < 16; ++e4) {
+            const float4 l4 = lrow[e4];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {  // two paired FMAs: exponent arguments of 4 columns
-            const int e = e4 * 4 + 2 * hh;
-            const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[e >> 5][e & 31]),
-                                                      __uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31])),
-                                          sc2, hh ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y));
-            float pa = ex2(arg.x), pb = ex2(arg.y);
-            if (need_mask) {
-              const int q = q0 + half * 64 + e;
-              if (q < key || q >= S) pa = 0.f;
-              if (q + 1 < key || q + 1 >= S) pb = 0.f;
+            for (int hh = 0; hh < 2; ++hh) {  // two paired FMAs: exponent arguments of 4 columns
+              const int e = e4 * 4 + 2 * hh;
+              const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[e >> 5][e & 31]),
+                                                        __uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31])),
+                                            sc2, hh ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
+              float pa = ex2(arg.x), pb = ex2(arg.y);
+              if constexpr (decltype(masked)::value) {
+                const int q = q0 + half * 64 + e;
+                if (q < key || q >= S) pa = 0.f;
+                if (q + 1 < key || q + 1 >= S) pb = 0.f;
+              }
+              p[e] = pa;
+              p[e + 1] = pb;
             }
-            p[e] = pa;
-            p[e + 1] = pb;
+            pw[2 * e4] = pack2(p[4 * e4], p[4 * e4 + 1]);
+            pw[2 * e4 + 1] = pack2(p[4 * e4 + 2], p[4 * e4 + 3]);
           }
-          pw[2 * e4] = pack2(p[4 * e4], p[4 * e4 + 1]);
-          pw[2 * e4 + 1] = pack2(p[4 * e4 + 2], p[4 * e4 + 3]);
-        }
+        };
+        if (need_mask)
+          exps(std::true_type{});
+        else
+          exps(std::false_type{});
         tmem_st32u(tSt + lane_off + half * 64, pw);
         tmem_wait_st();
         tc_fence_before();
@@ -914,7 +929,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
             const int e = e4 * 4 + 2 * hh;
             const float2 dd = __fadd2_rn(make_float2(__uint_as_float(dp[e >> 5][e & 31]),
                                                      __uint_as_float(dp[(e + 1) >> 5][(e + 1) & 31])),
-                                         hh ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y));
+                                         hh ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y));
             const float2 v = __fmul2_rn(make_float2(p[e], p[e + 1]), dd);
             dw[2 * e4 + hh] = pack2(v.x, v.y);
           }
@@ -1169,20 +1184,27 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         tmem_ld32_nw(tS + lane_off + half * 64 + 32, sv[1]);
         tmem_wait_ld2(sv[0], sv[1]);
         const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(-lse2, -lse2);
+        // two instantiations: tiles without masked entries carry no mask code
+        auto exps = [&](auto masked) {
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[e >> 5][e & 31]),
-                                                    __uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31])),
-                                        sc2, nl2);
-          float pa = ex2(arg.x), pb = ex2(arg.y);
-          if (need_mask) {
-            const int key = k0 + e;
-            if (key > q || key >= S) pa = 0.f;
-            if (key + 1 > q || key + 1 >= S) pb = 0.f;
+          for (int e = 0; e < 64; e += 2) {
+            const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[e >> 5][e & 31]),
+                                                      __uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31])),
+                                          sc2, nl2);
+            float pa = ex2(arg.x), pb = ex2(arg.y);
+            if constexpr (decltype(masked)::value) {
+              const int key = k0 + e;
+              if (key > q || key >= S) pa = 0.f;
+              if (key + 1 > q || key + 1 >= S) pb = 0.f;
+            }
+            p[e] = pa;
+            p[e + 1] = pb;
           }
-          p[e] = pa;
-          p[e + 1] = pb;
-        }
+        };
+        if (need_mask)
+          exps(std::true_type{});
+        else
+          exps(std::false_type{});
         tc_fence_before();
         mbar_arrive(ps_free);
       }
