@@ -1554,17 +1554,16 @@ void run_probes(mt_model* m) {
     if (m->pool.parallel_for((nn + CH - 1) / CH, fn, &err)) idle = std::min(idle, now_ms() - t0);
   }
   if (idle > 0 && idle < 1e30) in.adam_rate = (double)nn / (idle * 1e-3);
-  // shared host memory: copies in both link directions (about half as long as
-  // the Adam run, starting with it) while Adam makes four passes; Adam's bytes
-  // inside the copies' window are its total minus the idle-rate part after
-  // the copies ended
+  // shared host memory: copies in both link directions, sized to last about
+  // eight idle Adam passes, while Adam makes passes until both copy streams
+  // are done; the host's total rate is the copies' bytes over their window
+  // plus Adam's bytes at the rate it kept meanwhile
   cudaEvent_t f0 = nullptr, f1 = nullptr;
   if (e0 && e1 && in.adam_rate > 0 && in.bw_h2d > 0 && in.bw_d2h > 0 && cudaEventCreate(&f0) == cudaSuccess &&
       cudaEventCreate(&f1) == cudaSuccess) {
-    const int passes = 4;
-    const double t_idle = passes * (double)nn / in.adam_rate;
+    const double t_pass = (double)nn / in.adam_rate;
     const size_t half = bytes / 2;  // H2D from the first half of the buffer, D2H into the second
-    const int nc = std::max(2, (int)std::ceil(0.5 * t_idle * std::min(in.bw_h2d, in.bw_d2h) / (double)half));
+    const int nc = std::max(2, (int)std::ceil(8.0 * t_pass * std::min(in.bw_h2d, in.bw_d2h) / (double)half));
     cudaEventRecord(e0, m->sw);
     cudaEventRecord(f0, m->sg);
     for (int i = 0; i < nc; ++i) {
@@ -1575,16 +1574,20 @@ void run_probes(mt_model* m) {
     cudaEventRecord(f1, m->sg);
     const double t0 = now_ms();
     bool ok = true;
-    for (rep = 3; rep < 3 + passes && ok; ++rep) ok = m->pool.parallel_for((nn + CH - 1) / CH, fn, &err);
+    int passes = 0;
+    for (rep = 3; ok && passes < 64; ++rep) {
+      ok = m->pool.parallel_for((nn + CH - 1) / CH, fn, &err);
+      ++passes;
+      if (cudaEventQuery(e1) == cudaSuccess && cudaEventQuery(f1) == cudaSuccess) break;
+    }
     const double ta = (now_ms() - t0) * 1e-3;
     float mw = 0, mg = 0;
     if (ok && cudaEventSynchronize(e1) == cudaSuccess && cudaEventSynchronize(f1) == cudaSuccess &&
         cudaEventElapsedTime(&mw, e0, e1) == cudaSuccess && cudaEventElapsedTime(&mg, f0, f1) == cudaSuccess) {
       const double td = std::max(mw, mg) * 1e-3;
-      if (td > 0 && td < ta) {
-        const double adam_in = in.adam_bytes * ((double)passes * nn - in.adam_rate * (ta - td));
-        if (adam_in > 0) in.host_bw = (2.0 * nc * (double)half + adam_in) / td;
-      }
+      // Adam ran through the copies' window (it stops within one pass of its end)
+      if (td > 0 && ta > 0 && passes >= 2 && ta >= 0.8 * td)
+        in.host_bw = 2.0 * nc * (double)half / td + in.adam_bytes * ((double)passes * nn / ta);
     }
   }
   if (f0) cudaEventDestroy(f0);
