@@ -248,8 +248,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   // needs S_{g+2}, issued only after O += P_g V, so neither barrier can
   // complete a second phase before the MMA thread has seen the first
   uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;
-  uint64_t* fin_ready = o_done + 1;
+  // (the next slot is unused: O += P_g V is tracked by v_empty of P_g's V stage)
+  uint64_t* fin_ready = p_full + 3;
   uint64_t* q_empty = fin_ready + 1;  // the item's last S = Q K^T has read Q
   uint64_t* o_free = q_empty + 1;     // the epilogue has read O (the next item may overwrite it)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_free + 1);
@@ -287,7 +287,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 256);
     }
-    mbar_init(o_done, 1);
     mbar_init(fin_ready, 256);
     mbar_init(o_free, 256);
     *abort_flag = 0;
@@ -382,7 +381,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           tc_mma_ts(tO(0), tp + (uint32_t)(kk * 8), dadv(v, kk * 16 * 128), IO, acc);
           tc_mma_ts(tO(1), tp + (uint32_t)(64 + kk * 8), dadv(v, (4 + kk) * 16 * 128), IO, acc);
         }
-        tc_commit(o_done);
+        // one commit serves both: the V stage is free and O_0 / O_1 hold P_g V
         tc_commit(&v_empty[g % NFV]);
         return true;
       };
@@ -494,7 +493,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           // O_half of rows whose base moved is rescaled once the previous P V has
           // landed in it (warp-collective TMEM traffic: the whole warp joins)
           if (j > 0 && __any_sync(0xffffffffu, move)) {
-            if (!__all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)((g - 1) & 1), abort_flag))) return false;
+            if (!__all_sync(0xffffffffu, mbar_wait(&v_empty[(g - 1) % NFV], (uint32_t)(((g - 1) / NFV) & 1),
+                                                   abort_flag)))
+              return false;
             tc_fence_after();
 #pragma unroll
             for (int c = 0; c < HD / 32; ++c) {
@@ -541,7 +542,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       // merge the two halves of the row: m = max(m_0, m_1), c_h = 2^(m_h - m),
       // l = l_0 c_0 + l_1 c_1, O = (O_0 c_0 + O_1 c_1) / l; each half writes
       // half of the hd columns, once the item's last O += P V has landed
-      ok = __all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)((g - 1) & 1), abort_flag));
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&v_empty[(g - 1) % NFV], (uint32_t)(((g - 1) / NFV) & 1), abort_flag));
       if (ok) {
         fin[(half * 2) * 128 + r] = m_old;
         fin[(half * 2 + 1) * 128 + r] = l;
