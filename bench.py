@@ -464,7 +464,7 @@ def _overrides(args):
 # by its launches per step: 308 of the step's 310 GEMM launches, the LM
 # head's two not captured).  Valid only for the kernel source it was taken
 # from: any change to the GEMM kernel reports null.
-GEMM_TRAFFIC = {"source_sha256_16": "32b42dee992ff6ed", "config": "7.6b", "bytes_per_launch": 2.5716e9}
+GEMM_TRAFFIC = {"source_sha256_16": "a80f201da4b6d1a5", "config": "7.6b", "bytes_per_launch": 2.2463e9}
 
 
 def gemm_traffic_per_launch(name, c, args):

@@ -41,6 +41,13 @@
 // even CTA's producer thread draws the tile (one tile ahead) and passes it
 // through a 4-entry ring in shared memory to its MMA thread, to the odd
 // CTA's producer and to both CTAs' epilogue warps.
+//
+// Launches whose every GEMM has K >= 8192, N >= 512 and no residual use
+// 256 x 512 pair tiles: per K step two M = 256, N = 256 MMAs into one 512-column
+// accumulator, each CTA loading two 128-row blocks of B per stage (4 stages
+// of 48 KB).  The epilogue of a tile then cannot overlap the next tile's
+// MMAs, which at these K costs a few per cent, while each tile reads its rows
+// of A once for 512 output columns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -548,6 +555,14 @@ constexpr int PA_BYTES = BM * BK * 2;         // this CTA's 128 rows of A: 16 KB
 constexpr int PB_BYTES = (BN / 2) * BK * 2;   // this CTA's 128 rows of B: 16 KB
 constexpr int P_STAGE_BYTES = PA_BYTES + PB_BYTES;
 constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 + 256;
+// Wide tiles (NW = 2, for long-K launches): 256 x 512 per pair, one 512-column
+// accumulator, each CTA holding two 128-row blocks of B per stage (48 KB), so
+// 4 stages in the same shared memory.
+template <int NW>
+__host__ __device__ constexpr int p_stages() {
+  return NW == 1 ? P_STAGES : 4;
+}
+static_assert(4 * (PA_BYTES + 2 * PB_BYTES) == P_STAGES * P_STAGE_BYTES, "wide and narrow rings share one layout");
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -607,8 +622,9 @@ __device__ __forceinline__ void pair_tile_mn(int tile, const Epi& e, int& tm, in
   tn = in / gsize;
 }
 
-// Producer side of one pair tile: this CTA's halves of A and B, K block by K block.
-template <bool A_MN, bool B_MN>
+// Producer side of one pair tile: this CTA's halves of A and B, K block by K
+// block (B: one 128-row block per 256 columns of the tile, 256 apart).
+template <bool A_MN, bool B_MN, int NW>
 __device__ __forceinline__ bool produce_pair_tile(const CUtensorMap* tmA, const CUtensorMap* tmB, int arow, int brow,
                                                   int nk, uint8_t* sA, uint8_t* sB, uint64_t* full, uint64_t* empty,
                                                   bool leader, int& stage, uint32_t& phase, volatile int* abort_flag,
@@ -616,10 +632,10 @@ __device__ __forceinline__ bool produce_pair_tile(const CUtensorMap* tmA, const 
   for (int kb = 0; kb < nk; ++kb) {
     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) return false;
     // the even CTA's full[stage] expects both CTAs' bytes
-    if (leader) mbar_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
+    if (leader) mbar_expect_tx(&full[stage], 2 * (PA_BYTES + NW * PB_BYTES));
     const uint32_t bar = cluster_addr(&full[stage], 0);
     uint8_t* a = sA + stage * PA_BYTES;
-    uint8_t* b = sB + stage * PB_BYTES;
+    uint8_t* b = sB + stage * (NW * PB_BYTES);
     const int k0 = kb * BK;
     if (!A_MN) {
       tma_load_pair(tmA, bar, a, k0, arow);
@@ -627,15 +643,18 @@ __device__ __forceinline__ bool produce_pair_tile(const CUtensorMap* tmA, const 
       tma_load_pair(tmA, bar, a, arow, k0);
       tma_load_pair(tmA, bar, a + CHUNK_BYTES, arow + 64, k0);
     }
-    if (!B_MN) {
-      tma_load_pair(tmB, bar, b, k0, brow);
-    } else {
-      tma_load_pair(tmB, bar, b, brow, k0);
-      tma_load_pair(tmB, bar, b + CHUNK_BYTES, brow + 64, k0);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      if (!B_MN) {
+        tma_load_pair(tmB, bar, b + w * PB_BYTES, k0, brow + w * BN);
+      } else {
+        tma_load_pair(tmB, bar, b + w * PB_BYTES, brow + w * BN, k0);
+        tma_load_pair(tmB, bar, b + w * PB_BYTES + CHUNK_BYTES, brow + w * BN + 64, k0);
+      }
     }
     inflight_mask |= 1u << stage;
     inflight_parity = (inflight_parity & ~(1u << stage)) | (phase << stage);
-    if (++stage == P_STAGES) {
+    if (++stage == p_stages<NW>()) {
       stage = 0;
       phase ^= 1;
     }
@@ -643,23 +662,29 @@ __device__ __forceinline__ bool produce_pair_tile(const CUtensorMap* tmA, const 
   return true;
 }
 
-// MMA side of one pair tile (the even CTA's issuing thread).
-template <bool A_MN, bool B_MN>
+// MMA side of one pair tile (the even CTA's issuing thread): per K step one
+// M = 256, N = 256 MMA per 256 columns of the tile, into accumulator columns
+// 256 w .. 256 w + 255.
+template <bool A_MN, bool B_MN, int NW>
 __device__ __forceinline__ bool mma_pair_tile(uint32_t d, int nk, uint8_t* sA, uint8_t* sB, uint64_t* full,
                                               uint64_t* empty, int& stage, uint32_t& phase, volatile int* abort_flag) {
   constexpr uint32_t ID = idesc_pair(A_MN, B_MN);
   for (int kb = 0; kb < nk; ++kb) {
     if (!mbar_wait(&full[stage], phase, abort_flag)) return false;
     tc_fence_after();
-    const uint32_t a0 = su32(sA + stage * PA_BYTES), b0 = su32(sB + stage * PB_BYTES);
+    const uint32_t a0 = su32(sA + stage * PA_BYTES), b0 = su32(sB + stage * (NW * PB_BYTES));
 #pragma unroll
     for (int k = 0; k < BK / UMMA_K; ++k) {
       const uint64_t ad = A_MN ? sdesc(a0 + k * UMMA_K * 128, CHUNK_BYTES, 1024) : sdesc(a0 + k * UMMA_K * 2, 16, 1024);
-      const uint64_t bd = B_MN ? sdesc(b0 + k * UMMA_K * 128, CHUNK_BYTES, 1024) : sdesc(b0 + k * UMMA_K * 2, 16, 1024);
-      tc_mma_pair(d, ad, bd, ID, (kb | k) != 0);
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const uint32_t bw = b0 + w * PB_BYTES;
+        const uint64_t bd = B_MN ? sdesc(bw + k * UMMA_K * 128, CHUNK_BYTES, 1024) : sdesc(bw + k * UMMA_K * 2, 16, 1024);
+        tc_mma_pair(d + (uint32_t)(w * BN), ad, bd, ID, (kb | k) != 0);
+      }
     }
     tc_commit_pair(&empty[stage]);  // the stage is free in both CTAs once these MMAs are done
-    if (++stage == P_STAGES) {
+    if (++stage == p_stages<NW>()) {
       stage = 0;
       phase ^= 1;
     }
@@ -697,12 +722,12 @@ __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-template <int NG, bool A0, bool B0, bool A1, bool B1>
+template <int NG, bool A0, bool B0, bool A1, bool B1, int NW = 1>
 __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + P_STAGES * PA_BYTES;
+  uint8_t* sB = smem + p_stages<NW>() * PA_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
   uint64_t* empty = full + P_STAGES;
   uint64_t* tfull = empty + P_STAGES;
@@ -808,12 +833,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
         int tm, tn;
         if (NG == 1 || tile < split) {
           pair_tile_mn(tile, p.e[0], tm, tn);
-          ok = produce_pair_tile<A0, B0>(&p.ta[0], &p.tb[0], tm * 2 * BM + (int)rank * BM, tn * BN + (int)rank * (BN / 2),
+          ok = produce_pair_tile<A0, B0, NW>(&p.ta[0], &p.tb[0], tm * 2 * BM + (int)rank * BM,
+                                             tn * BN * NW + (int)rank * (BN / 2),
                                          (p.e[0].K + BK - 1) / BK, sA, sB, full, empty, leader, stage, phase,
                                          abort_flag, inflight_mask, inflight_parity);
         } else {
           pair_tile_mn(tile - split, p.e[1], tm, tn);
-          ok = produce_pair_tile<A1, B1>(&p.ta[1], &p.tb[1], tm * 2 * BM + (int)rank * BM, tn * BN + (int)rank * (BN / 2),
+          ok = produce_pair_tile<A1, B1, NW>(&p.ta[1], &p.tb[1], tm * 2 * BM + (int)rank * BM,
+                                             tn * BN * NW + (int)rank * (BN / 2),
                                          (p.e[1].K + BK - 1) / BK, sA, sB, full, empty, leader, stage, phase,
                                          abort_flag, inflight_mask, inflight_parity);
         }
@@ -834,8 +861,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
         const int tile = tid_ring[slot];
         mbar_arrive(&tid_empty[slot]);
         if (tile < 0) break;
-        const int acc = it & 1;
-        const uint32_t aph = (it >> 1) & 1;
+        // two 256-column accumulators, or one of 512 columns for wide tiles
+        const int acc = NW == 1 ? (it & 1) : 0;
+        const uint32_t aph = NW == 1 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
         if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag)) {
           ok = false;
           break;
@@ -843,9 +871,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
         if (NG == 1 || tile < split)
-          ok = mma_pair_tile<A0, B0>(d, (p.e[0].K + BK - 1) / BK, sA, sB, full, empty, stage, phase, abort_flag);
+          ok = mma_pair_tile<A0, B0, NW>(d, (p.e[0].K + BK - 1) / BK, sA, sB, full, empty, stage, phase, abort_flag);
         else
-          ok = mma_pair_tile<A1, B1>(d, (p.e[1].K + BK - 1) / BK, sA, sB, full, empty, stage, phase, abort_flag);
+          ok = mma_pair_tile<A1, B1, NW>(d, (p.e[1].K + BK - 1) / BK, sA, sB, full, empty, stage, phase, abort_flag);
         if (!ok) break;
         tc_commit_pair(&tfull[acc]);  // both CTAs' epilogues may read their rows
       }
@@ -867,8 +895,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(cluster_addr(&tid_empty[slot], 0));
       if (tile < 0) break;
-      const int acc = it & 1;
-      const uint32_t aph = (it >> 1) & 1;
+      const int acc = NW == 1 ? (it & 1) : 0;
+      const uint32_t aph = NW == 1 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, abort_flag))) {
         ok = false;
         break;
@@ -879,10 +907,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       pair_tile_mn((NG == 1 || tile < split) ? tile : tile - split, e, tm, tn);
       const int row = tm * 2 * BM + (int)rank * BM + row_in_tile;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < BN * NW / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(taddr + (uint32_t)(c * 32), r);
-        const int col = tn * BN + c * 32;
+        const int col = tn * BN * NW + c * 32;
         if (row < e.M && col < e.N) epi_store(e, row, col, r);
       }
       tc_fence_before();
@@ -919,6 +947,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
 int g_num_sms = 0;
 int g_pair_clusters = 0;
+constexpr int kWideK = 8192;  // K from which dense pair launches use 256 x 512 tiles
 constexpr int kTileCounters = 1024;  // tile-ticket counters, one per pair launch in a ring
 int* g_tile_ctrs = nullptr;
 std::atomic<unsigned> g_tile_ctr_next{0};
@@ -952,7 +981,12 @@ void init_once() {
                                 (const void*)gemm_pair_kernel<1, false, true, false, false>,
                                 (const void*)gemm_pair_kernel<1, true, false, false, false>,
                                 (const void*)gemm_pair_kernel<1, true, true, false, false>,
-                                (const void*)gemm_pair_kernel<2, true, true, false, true>};
+                                (const void*)gemm_pair_kernel<2, true, true, false, true>,
+                                (const void*)gemm_pair_kernel<1, false, false, false, false, 2>,
+                                (const void*)gemm_pair_kernel<1, false, true, false, false, 2>,
+                                (const void*)gemm_pair_kernel<1, true, false, false, false, 2>,
+                                (const void*)gemm_pair_kernel<1, true, true, false, false, 2>,
+                                (const void*)gemm_pair_kernel<2, true, true, false, true, 2>};
   for (const void* k : pair_kernels) {
     const cudaError_t a = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
     if (a != cudaSuccess) g_init_err = a;
@@ -1015,12 +1049,13 @@ inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) =
 }  // namespace
 
 std::atomic<int> g_stall_next{0};
-// dense GEMMs: 0 one CTA per 128 x 256 tile; CTA pairs on 256 x 256 tiles,
-// 1 drawing tiles from a counter, 2 taking every ncl-th tile in raster order
+// dense GEMMs: 0 one CTA per 128 x 256 tile; CTA pairs on 256 x 256 tiles
+// (256 x 512 for long-K launches), 1 drawing tiles from a counter, 2 taking
+// every ncl-th tile in raster order; 3 as 1 without the 512-wide tiles
 std::atomic<int> g_gemm_mode{1};
 int gemm_mode(int mode) {
   const int prev = g_gemm_mode.load();
-  if (mode >= 0 && mode <= 2) g_gemm_mode = mode;
+  if (mode >= 0 && mode <= 3) g_gemm_mode = mode;
   return prev;
 }
 int gemm_stall_take() {
@@ -1080,7 +1115,7 @@ int pair_band(int K, int pairs) {
   return best;
 }
 
-template <int NG, bool A0, bool B0, bool A1, bool B1>
+template <int NG, bool A0, bool B0, bool A1, bool B1, int NW = 1>
 cudaError_t launch_pair_kernel(const Params& p, int tiles, cudaStream_t s) {
   const int clusters = tiles < g_pair_clusters ? tiles : g_pair_clusters;
   cudaLaunchConfig_t cfg{};
@@ -1095,7 +1130,7 @@ cudaError_t launch_pair_kernel(const Params& p, int tiles, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<NG, A0, B0, A1, B1>, p);
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<NG, A0, B0, A1, B1, NW>, p);
 }
 
 cudaError_t launch(const GemmArgs* gs, int n, cudaStream_t s) {
@@ -1103,6 +1138,13 @@ cudaError_t launch(const GemmArgs* gs, int n, cudaStream_t s) {
   if (g_init_err != cudaSuccess) return g_init_err;
   const int mode = g_gemm_mode.load();
   const bool pair = mode != 0 && g_pair_clusters >= 1;
+  // wide pair tiles (256 x 512) when every group has a long K, at least 512
+  // columns and no residual: the serial epilogue of a single accumulator is
+  // then a few per cent of a tile, and each tile reads the row operand once
+  // for twice the columns (with a residual to read, the longer epilogue cost
+  // more than the traffic saved: 6 % on the 7.6B down projection)
+  bool wide = pair && mode != 3;
+  for (int i = 0; i < n; ++i) wide = wide && gs[i].K >= kWideK && gs[i].N >= 2 * BN && !gs[i].R;
   Params p;
   std::memset(&p, 0, sizeof p);
   p.ngroups = n;
@@ -1111,15 +1153,27 @@ cudaError_t launch(const GemmArgs* gs, int n, cudaStream_t s) {
     cudaError_t e = fill_group(gs[i], &p.ta[i], &p.tb[i], &p.e[i], pair);
     if (e != cudaSuccess) return e;
     if (pair) p.e[i].group_m = pair_band(p.e[i].K, g_pair_clusters);
+    if (wide) p.e[i].tiles_n = (p.e[i].N + 2 * BN - 1) / (2 * BN);
     const int tm = pair ? (p.e[i].M + 2 * BM - 1) / (2 * BM) : p.e[i].tiles_m;
     p.tile_start[i + 1] = p.tile_start[i] + tm * p.e[i].tiles_n;
   }
   p.stall = gemm_stall_take();
   const int tiles = p.tile_start[n];
   if (pair) {
-    if (mode == 1) p.tile_ctr = g_tile_ctrs + (g_tile_ctr_next.fetch_add(1) % kTileCounters);
+    if (mode != 2) p.tile_ctr = g_tile_ctrs + (g_tile_ctr_next.fetch_add(1) % kTileCounters);
     const Epi& e = p.e[0];
     cudaError_t r;
+    if (wide) {
+      if (n == 1) {
+        if (!e.a_mn && !e.b_mn) r = launch_pair_kernel<1, false, false, false, false, 2>(p, tiles, s);
+        else if (!e.a_mn && e.b_mn) r = launch_pair_kernel<1, false, true, false, false, 2>(p, tiles, s);
+        else if (e.a_mn && !e.b_mn) r = launch_pair_kernel<1, true, false, false, false, 2>(p, tiles, s);
+        else r = launch_pair_kernel<1, true, true, false, false, 2>(p, tiles, s);
+      } else {
+        r = launch_pair_kernel<2, true, true, false, true, 2>(p, tiles, s);
+      }
+      return r != cudaSuccess ? r : cudaGetLastError();
+    }
     if (n == 1) {
       if (!e.a_mn && !e.b_mn) r = launch_pair_kernel<1, false, false, false, false>(p, tiles, s);
       else if (!e.a_mn && e.b_mn) r = launch_pair_kernel<1, false, true, false, false>(p, tiles, s);

@@ -64,9 +64,10 @@ cudaError_t gemm_expert_kgroups(const GemmKGroupArgs& g, cudaStream_t s);
 // waits expire and they report through the kernel error word.
 void gemm_inject_stall(int launches);
 // Dense GEMM tiling (gemm and gemm_pair): 0 = one CTA per 128 x 256 output
-// tile; CTA pairs (cta_group::2) per 256 x 256 tile, 1 = tiles drawn from a
-// per-launch counter, 2 = every n-th tile; other values only read.  Returns
-// the previous mode.
+// tile; CTA pairs (cta_group::2) per 256 x 256 tile (256 x 512 for launches
+// whose every GEMM has K >= 8192 and N >= 512), 1 = tiles drawn from a
+// per-launch counter, 2 = every n-th tile, 3 = as 1 without the wide tiles;
+// other values only read.  Returns the previous mode.
 int gemm_mode(int mode);
 int gemm_stall_take();
 

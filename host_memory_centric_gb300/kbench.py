@@ -56,8 +56,9 @@ def main():
     ap.add_argument("--config", default="7.6b")
     ap.add_argument("--no-head", action="store_true", help="layer_gemms: leave out the LM-head forms")
     ap.add_argument("--gemm-mode", type=int, default=-1,
-                    help="dense GEMM tiling: 0 one CTA per 128 x 256 tile; CTA pairs per 256 x 256 tile, "
-                         "1 drawing tiles from a counter, 2 every n-th tile")
+                    help="dense GEMM tiling: 0 one CTA per 128 x 256 tile; CTA pairs per 256 x 256 tile "
+                         "(256 x 512 at long K), 1 drawing tiles from a counter, 2 every n-th tile, "
+                         "3 as 1 without the 512-wide tiles")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     a = ap.parse_args()

@@ -44,8 +44,10 @@ def gemm(A, B, M, N, K, *, a_mn=False, b_mn=False, lda=None, ldb=None, D=None, l
 
 def gemm_mode(mode=-1) -> int:
     """Dense GEMM tiling: 0 one CTA per 128 x 256 tile; 1 CTA pairs per
-    256 x 256 tile drawing tiles from a counter, 2 CTA pairs taking every
-    n-th tile; -1 only reads.  Returns the previous mode."""
+    256 x 256 tile (256 x 512 when every GEMM of the launch has K >= 8192 and
+    N >= 512) drawing tiles from a counter, 2 the same taking every n-th
+    tile, 3 as 1 without the 512-wide tiles; -1 only reads.  Returns the
+    previous mode."""
     return int(_L().mt_gemm_mode(int(mode)))
 
 

@@ -374,16 +374,17 @@ mt_status mt_gemm(const void* A, int64_t lda, int32_t a_mn, const void* B, int64
                   void* stream);
 /* Tiling of the dense GEMMs (mt_gemm, mt_gemm2 and those of the training
  * step) for the whole process: 0 = one CTA per 128 x 256 output tile; 1 (the
- * default) and 2 = a pair of CTAs (one cluster, cta_group::2 MMAs) per
- * 256 x 256 tile, the operands split between the two SMs' shared memory,
- * where under 1 each pair draws its next tile from a per-launch counter (the
- * tiles in flight stay a window of consecutive tiles of the raster order, so
- * tiles that share an operand run together) and under 2 takes every n-th tile
- * of that order (n = pairs resident).  The MoE grouped GEMMs always use one
- * CTA per tile.  All modes give bitwise the same results (same K order, FP32
- * accumulation).  Any other value changes nothing; returns the mode in force
- * before the call.  Takes effect at the next launch; not synchronised with
- * launches in flight on other threads. */
+ * default), 2 and 3 = a pair of CTAs (one cluster, cta_group::2 MMAs) per
+ * 256 x 256 tile, the operands split between the two SMs' shared memory.
+ * Under 1 and 2 a launch whose every GEMM has K >= 8192, N >= 512 and no
+ * residual uses 256 x 512 pair tiles instead.  Under 1 and 3 each pair draws its next tile
+ * from a per-launch counter (the tiles in flight stay a window of consecutive
+ * tiles of the raster order, so tiles that share an operand run together);
+ * under 2 it takes every n-th tile of that order (n = pairs resident).  The
+ * MoE grouped GEMMs always use one CTA per tile.  All modes give bitwise the
+ * same results (same K order, FP32 accumulation).  Any other value changes
+ * nothing; returns the mode in force before the call.  Takes effect at the
+ * next launch; not synchronised with launches in flight on other threads. */
 int32_t mt_gemm_mode(int32_t mode);
 /* Two independent GEMMs (each as mt_gemm, arguments given as arrays of two)
  * in one persistent launch: their output tiles share one schedule. */

@@ -37,13 +37,14 @@ def pair_mode():
     ops.gemm_mode(prev)
 
 
-def all_modes(fn):
+def all_modes(fn, modes=(0, 1, 2)):
     """fn() under the one-CTA tiling (mode 0), CTA pairs drawing tiles from a
-    counter (1) and CTA pairs in static order (2)."""
+    counter (1), CTA pairs in static order (2) and, where asked, counter order
+    without the 512-wide tiles of long-K launches (3)."""
     prev = ops.gemm_mode(-1)
     out = []
     try:
-        for mode in (0, 1, 2):
+        for mode in modes:
             ops.gemm_mode(mode)
             out.append(fn())
     finally:
@@ -56,8 +57,9 @@ def test_mode_switch_reads_and_sets():
     assert prev in (0, 1)
     assert ops.gemm_mode(1) == prev
     assert ops.gemm_mode(2) == 1
-    assert ops.gemm_mode(7) == 2  # ignored
-    assert ops.gemm_mode(prev) == 2
+    assert ops.gemm_mode(3) == 2
+    assert ops.gemm_mode(7) == 3  # ignored
+    assert ops.gemm_mode(prev) == 3
     assert ops.gemm_mode(-1) == prev
 
 
@@ -104,6 +106,44 @@ def test_pair_majors_against_oracle_and_one_cta(orc, a_mn, b_mn, M, N, K):
     one, two, static = all_modes(run)
     close(f64(two), orc.linear_fwd(f64(bf(A)), f64(bf(B))), rel=5e-3)
     assert torch.equal(one, two) and torch.equal(one, static)
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_wide_tiles_at_long_k(orc, a_mn, b_mn):
+    """K >= 8192 and N >= 512: the pair launches use 256 x 512 tiles with one
+    512-column accumulator (modes 1 and 2; mode 3 keeps 256 x 256).  N = 1320
+    leaves the last wide tile with its first half inside and 40 columns of
+    its second; M = 300 and K = 8200 are ragged too."""
+    M, N, K = 300, 1320, 8200
+    A, B, run = _majors_case(a_mn, b_mn, M, N, K, 77 + 2 * a_mn + b_mn)
+    one, two, static, narrow = all_modes(run, (0, 1, 2, 3))
+    assert torch.equal(one, two) and torch.equal(one, static) and torch.equal(one, narrow)
+    rows = np.random.default_rng(9).choice(M, 32, replace=False)
+    close(f64(two)[rows], orc.linear_fwd(f64(bf(A))[rows], f64(bf(B))), rel=5e-3)
+
+
+def test_wide_wgrad_dgrad_in_one_launch(orc):
+    """Both GEMMs of the launch have K >= 8192 (T and N), so it runs wide."""
+    T, N, K = 8200, 8256, 600
+    dY = rnd((T, N), 40, 0.5); X = rnd((T, K), 41, 0.5); W = rnd((N, K), 42, 0.5)
+    dYg, Xg, Wg = bf(dY), bf(X), bf(W)
+
+    def run():
+        dW = torch.empty(N, K, dtype=torch.bfloat16, device="cuda")
+        dX = torch.empty(T, K, dtype=torch.bfloat16, device="cuda")
+        ops.gemm2([dict(A=dYg, B=Xg, M=N, N=K, K=T, a_mn=1, b_mn=1, lda=N, ldb=K, D=dW),
+                   dict(A=dYg, B=Wg, M=T, N=K, K=N, b_mn=1, ldb=K, D=dX)])
+        torch.cuda.synchronize()
+        return dW, dX
+
+    (dW1, dX1), (dW2, dX2), (dW3, dX3) = all_modes(run, (0, 1, 3))
+    assert torch.equal(dW1, dW2) and torch.equal(dX1, dX2)
+    assert torch.equal(dW1, dW3) and torch.equal(dX1, dX3)
+    rng = np.random.default_rng(10)
+    rw, rx = rng.choice(N, 16, replace=False), rng.choice(T, 16, replace=False)
+    dY64, X64, W64 = f64(dYg), f64(Xg), f64(Wg)
+    close(f64(dW2)[rw], orc.linear_fwd(np.ascontiguousarray(dY64[:, rw].T), np.ascontiguousarray(X64.T)), rel=5e-3)
+    close(f64(dX2)[rx], orc.linear_fwd(dY64[rx], np.ascontiguousarray(W64.T)), rel=5e-3)
 
 
 def test_counter_reuse_over_many_launches(orc, pair_mode):
