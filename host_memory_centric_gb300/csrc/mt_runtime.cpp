@@ -2020,6 +2020,13 @@ mt_status mt_sync(mt_model* m) {
   if (m->timing) collect_timing(m);
   replan_measured(m);
   if (m->c.debug_guards) OK(check_guards(m));
+  // a GEMM or attention kernel whose bounded wait expired has recorded a
+  // code; its outputs, and the step built on them, are not valid
+  int kcode = 0;
+  if (mt::kernel_error_read(&kcode, 0) != cudaSuccess) cudaGetLastError();
+  if (kcode != 0)
+    return set_err(m, MT_ERR_TIMEOUT,
+                   "a kernel's bounded wait expired (device error code " + std::to_string(kcode) + ")");
   return MT_OK;
 }
 

@@ -213,7 +213,11 @@ mt_status mt_adam_host(mt_model* model, int32_t block, int32_t slab, int32_t ada
  * 記憶體預取策略 (prefetch timed from each layer's bytes, the link bandwidth
  * and the layer's compute time). */
 mt_status mt_train_step(mt_model* model, int32_t step, float* loss);
-/* Waits (bounded) for every queued copy, kernel and Adam job. */
+/* Waits (bounded) for every queued copy, kernel and Adam job.  A kernel
+ * whose bounded barrier wait expired (its code in the process's device error
+ * word, mt_kernel_error) makes the call fail with MT_ERR_TIMEOUT and latches
+ * the model: the outputs of that kernel, and the step built on them, are not
+ * valid. */
 mt_status mt_sync(mt_model* model);
 /* Copies `bytes` of a block's region (MT_REGION_*) out of / into the host
  * store (after mt_sync).  bytes must not exceed the region (MT_ERR_ARG).

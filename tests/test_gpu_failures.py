@@ -145,6 +145,38 @@ def test_moe_route_wait_times_out_and_latches():
     m2.close()
 
 
+def test_expired_kernel_wait_latches_at_sync():
+    """A GEMM made to stall (its bounded waits run out after about 2 s and it
+    records a code, the context intact) inside a training step: mt_sync
+    reports MT_ERR_TIMEOUT and the model latches; once the code is cleared a
+    fresh model trains normally."""
+    c = configs.get("tiny")
+    m = mt.Model(c)
+    m.set_tokens(inputs.tokens_for(c, 0))
+    m.train_step(0)  # first step: lazy loading out of the way
+    m.sync()
+    ops.kernel_error(clear=True)
+    m.set_tokens(inputs.tokens_for(c, 1))
+    assert mt.lib().mt_fault_inject(4, 1) == 0  # the next GEMM issues no loads
+    m.train_step(1, want_loss=False)
+    with pytest.raises(mt.MtError) as ei:
+        m.sync()
+    assert ei.value.status == -5
+    assert "bounded wait" in m.last_error()
+    with pytest.raises(mt.MtError) as ei:
+        m.train_step(2)
+    assert ei.value.status == -2  # latched
+    m.close()
+    torch.cuda.synchronize()
+    assert ops.kernel_error(clear=True) != 0
+    m2 = mt.Model(c)
+    m2.set_tokens(inputs.tokens_for(c, 0))
+    assert np.isfinite(m2.train_step(0))
+    m2.sync()
+    assert ops.kernel_error(clear=True) == 0
+    m2.close()
+
+
 @pytest.mark.parametrize("name,rt", [("tiny", dict(ckpt_interval=2, pin_store=0)), ("tiny_moe", {})])
 def test_debug_guards_hold_over_steps(name, rt):
     """With debug_guards every carved device piece and every pinned region has
