@@ -341,3 +341,23 @@ def test_bad_moe_configs_rejected():
     ok = mt.make_config(configs.get("tiny_moe"))
     assert L.mt_query_device_bytes(C.byref(ok), C.byref(n)) == 0
     assert L.mt_moe_scratch_bytes(256, 256, 8, 2, 256) > 0
+
+
+def test_gemm_mode_switch_is_host_state():
+    """mt_gemm_mode only reads and sets the process's dense-GEMM tiling (no
+    device call): it returns the mode in force before the call, takes 0-3 and
+    ignores anything else."""
+    L = mt.lib()
+    L.mt_gemm_mode.restype = C.c_int32
+    L.mt_gemm_mode.argtypes = [C.c_int32]
+    prev = L.mt_gemm_mode(-1)
+    assert prev in (0, 1, 2, 3)
+    try:
+        for m in (0, 1, 2, 3):
+            L.mt_gemm_mode(m)
+            assert L.mt_gemm_mode(-1) == m
+        assert L.mt_gemm_mode(4) == 3  # out of range: nothing changes
+        assert L.mt_gemm_mode(-7) == 3
+        assert L.mt_gemm_mode(1) == 3
+    finally:
+        L.mt_gemm_mode(prev)
